@@ -1,0 +1,234 @@
+/*
+ * oasis.h - C ABI of the GB300 (sm_103a) lookahead sparse decode hot path.
+ *
+ * The method (OasisKV: Scaling In-Decode KV Cache Beyond HBM with Lookahead
+ * Sparse Prefetching) keeps only the most relevant KV blocks of each KV head in
+ * HBM during decode, predicts them with the queries of lookahead (speculative
+ * draft) tokens, and prefetches the missing ones from a host-memory tier under
+ * a per-step cap.  One layer-step of the hot path is five calls, in order:
+ *
+ *   oasis_score_blocks       score every KV block against the lookahead queries
+ *   oasis_topk_select        keep the Kb best blocks (the token budget)
+ *   oasis_fetch_diff_capped  pick the best selected-but-missing blocks, <= cap
+ *   oasis_gather_h2d         copy them host -> HBM slots, update the tables
+ *   oasis_sparse_decode_attn attention of the true queries over the resident
+ *                            selected blocks
+ *
+ * Conventions for every call
+ *   - Buffers are caller-owned.  "device" pointers are CUDA device memory (or
+ *     any pointer the GPU may dereference); "host" pointers are plain CPU memory.
+ *     The library allocates nothing and frees nothing.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL means the
+ *     legacy default stream) and returns after enqueueing its kernels.
+ *   - Shapes and pointers are validated synchronously: a bad argument returns
+ *     OASIS_ERR_INVALID (or OASIS_ERR_UNSUPPORTED for a shape outside the
+ *     supported range) and launches nothing.  A failed launch returns
+ *     OASIS_ERR_CUDA.  oasis_last_error() describes the last failure of the
+ *     calling thread.
+ *   - Device-side problems that only the kernels can see (an index out of
+ *     range in a table) are OR-ed into a caller-provided uint32 error word
+ *     (OASIS_EW_* bits); the offending entry is skipped, nothing faults.
+ *   - bf16 tensors hold IEEE bfloat16 bit patterns; all inputs must be finite.
+ *   - Layer slicing is done by the caller through pointer offsets; every
+ *     per-layer tensor below is described for one layer.
+ *
+ * Shape (oasis_shape):
+ *   B      requests in the batch               (1 .. 65535)
+ *   Hq     query heads                          Hq = G * Hkv, G in {1,2,4,8}
+ *   Hkv    KV heads
+ *   d      head dimension                       must be 128
+ *   bs     tokens per KV block                  must be 16
+ *   nb_max blocks per (request, KV head) in the key cache, the host tier and
+ *          blk2slot                             (1 .. 8192)
+ *   n_la   lookahead queries per request        n_la * G <= 32
+ *   Kb     token budget in blocks               (1 .. 256)
+ *   P      HBM slots per (request, KV head)     Kb <= P <= 1024
+ *
+ * Context lengths: ctx_len[b] (device int32 [B]) is the number of valid tokens
+ * of request b; request b has nb_b = ceil(ctx_len[b] / bs) blocks (clamped to
+ * nb_max).  Tokens t >= ctx_len[b] are never scored or attended.
+ */
+#ifndef OASIS_H_
+#define OASIS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define OASIS_API __attribute__((visibility("default")))
+#else
+#define OASIS_API
+#endif
+
+struct CUstream_st;
+/* Same type as cudaStream_t; NULL selects the legacy default stream. */
+typedef struct CUstream_st* oasis_stream_t;
+
+typedef enum oasis_status {
+  OASIS_OK = 0,
+  OASIS_ERR_INVALID = 1,      /* bad pointer, size or shape; nothing launched   */
+  OASIS_ERR_CUDA = 2,         /* a CUDA runtime call or launch failed            */
+  OASIS_ERR_TIMEOUT = 3,      /* a bounded wait gave up                          */
+  OASIS_ERR_UNSUPPORTED = 4   /* valid but outside the supported shape range     */
+} oasis_status;
+
+/* Bits OR-ed into the device error word by the kernels. */
+#define OASIS_EW_BAD_BLOCK 0x1u  /* a block index outside [0, nb_max)            */
+#define OASIS_EW_BAD_SLOT 0x2u   /* a slot index outside [0, P)                  */
+#define OASIS_EW_NO_SLOT 0x4u    /* more blocks to fetch than candidate slots    */
+#define OASIS_EW_BAD_COUNT 0x8u  /* nsel / nfetch outside its range              */
+#define OASIS_EW_TIMEOUT 0x10u   /* a bounded wait on a host flag gave up        */
+
+typedef struct oasis_shape {
+  int32_t B, Hq, Hkv, d, bs, nb_max, n_la, Kb, P;
+} oasis_shape;
+
+/* Library version string, e.g. "oasis-gb300 0.1 sm_103a". */
+OASIS_API const char* oasis_version(void);
+
+/* Description of the last non-OK status returned on the calling thread. */
+OASIS_API const char* oasis_last_error(void);
+
+/*
+ * a1. Block scoring.
+ * Defines: the lookahead prediction of the next step's important KV blocks
+ * (OasisKV pages: abstract; metalmedia.ai page, explanatory figure step 2 and
+ * Figure 7 caption, where the draft queries are matched against the keys to
+ * choose next step's top-K blocks).  The block score is the exact form of that
+ * match:
+ *   score[b][h][x] = max over j < n_la, g < G, t in block x with t < ctx_len[b]
+ *                    of  q_la[b][j][h*G + g] . k[b][h][t] / sqrt(d).
+ * Arguments:
+ *   k_hbm     device bf16 [B][Hkv][nb_max*bs][d]  keys of one layer (row-major)
+ *   ctx_len   device int32 [B]
+ *   q_la      device bf16 [B][n_la][Hq][d]        lookahead queries of the layer
+ *   scores    device float [B][Hkv][nb_max][2]    out: for every block x < nb_b,
+ *             scores[..][x][0] = an approximation s~ of score(x) computed on the
+ *             tensor cores, scores[..][x][1] = a bound e with |s~ - score| <= e.
+ *             Entries x >= nb_b are not written.
+ * The bound is e = 2^-12 * max_n |q_n|_2 * max_t |k_t|_2 / sqrt(d) (plus the
+ * rounding of the 1/sqrt(d) product); it is an upper bound on the error of
+ * fp32-accumulated bf16 products with a wide margin.  Selection never trusts
+ * s~ inside this interval: it re-scores those blocks exactly.
+ */
+OASIS_API oasis_status oasis_score_blocks(const oasis_shape* shape, const void* k_hbm,
+                                const int32_t* ctx_len, const void* q_la,
+                                float* scores, oasis_stream_t stream);
+
+/*
+ * a2. Top-K under the token budget.
+ * Defines: keep, per KV head, the Kb highest-scoring blocks (OasisKV pages:
+ * abstract, 2,048-token KV budget; Figure 7 caption, top-K blocks).
+ *   S = the min(Kb, nb_b) blocks ranked first by (exact score descending,
+ *       block index ascending).
+ * Blocks whose score interval from oasis_score_blocks straddles the selection
+ * boundary are re-scored exactly (integer arithmetic on the bf16 products), so
+ * S is exactly the set the definition gives.
+ * Arguments:
+ *   scores    device float [B][Hkv][nb_max][2]  from oasis_score_blocks
+ *   k_hbm, q_la, ctx_len                         the same tensors as for scoring
+ *   sel       device int32 [B][Hkv][Kb]          out: S in ascending block order,
+ *                                                entries >= nsel are set to -1
+ *   nsel      device int32 [B][Hkv]              out: |S| = min(Kb, nb_b)
+ */
+OASIS_API oasis_status oasis_topk_select(const oasis_shape* shape, const float* scores,
+                               const void* k_hbm, const void* q_la,
+                               const int32_t* ctx_len, int32_t* sel, int32_t* nsel,
+                               oasis_stream_t stream);
+
+/*
+ * a3. Capped diff against the HBM-resident set.
+ * Defines: compare the predicted set with the blocks already in HBM, fetch only
+ * the missing ones, at most a per-step cap (metalmedia.ai page, explanatory
+ * figure step 3; Table 2 caption, where a fetch ratio limits how many blocks
+ * one step may fetch).
+ *   M = { x in S : blk2slot[x] == -1 },
+ *   F = the min(fetch_cap, |M|) blocks of M ranked first by (exact score
+ *       descending, block index ascending), emitted in ascending block order.
+ * Arguments:
+ *   scores, k_hbm, q_la, ctx_len   as for oasis_topk_select (exact re-scoring)
+ *   sel, nsel                      from oasis_topk_select
+ *   blk2slot  device int32 [B][Hkv][nb_max]  slot of each resident block, -1 if
+ *                                             not resident (read only)
+ *   fetch_cap blocks per (request, KV head), 0 <= fetch_cap <= Kb
+ *   fetch     device int32 [B][Hkv][Kb]       out: F, entries >= nfetch are -1
+ *   nfetch    device int32 [B][Hkv]           out: |F|
+ */
+OASIS_API oasis_status oasis_fetch_diff_capped(const oasis_shape* shape, const float* scores,
+                                     const void* k_hbm, const void* q_la,
+                                     const int32_t* ctx_len, const int32_t* sel,
+                                     const int32_t* nsel, const int32_t* blk2slot,
+                                     int32_t fetch_cap, int32_t* fetch, int32_t* nfetch,
+                                     oasis_stream_t stream);
+
+/*
+ * a4. Host-tier gather into HBM slots, with the head-wise block table update.
+ * Defines: prefetch the selected blocks from the host tier into the bounded GPU
+ * working set (OasisKV abstract; metalmedia.ai page, explanatory figure step 4),
+ * the head-wise table from GPU blocks to host-tier blocks (Figure 9 caption) and
+ * LRU eviction (Table 2 caption).
+ *   Candidate slots, per (request, KV head): the free slots (slot2blk == -1) in
+ *   ascending order, then the LRU victims, i.e. the slots whose block is not in
+ *   S, ordered by (last_used, block).  F[i] (ascending) takes the i-th
+ *   candidate: its K and V are copied from the host tier into that slot, the
+ *   evicted block gets blk2slot = -1, and blk2slot/slot2blk are updated.
+ *   Finally last_used[slot] = step for every block of S that is resident.
+ * Arguments:
+ *   host_kv   bf16 [B][Hkv][nb_max][2][bs][d] in page-locked host memory the GPU
+ *             can address (cudaHostAlloc / cudaHostRegister, mapped); element
+ *             [..][x][0] holds the keys of block x, [..][x][1] its values.  The
+ *             kernel reads it with zero-copy loads over the host link.
+ *   sel, nsel, fetch, nfetch          from the two calls above
+ *   blk2slot  device int32 [B][Hkv][nb_max]   in/out
+ *   slot2blk  device int32 [B][Hkv][P]        in/out, -1 = free slot
+ *   last_used device int32 [B][Hkv][P]        in/out
+ *   step      the decode step number written into last_used
+ *   k_pool    device bf16 [B][Hkv][P][bs][d]  in/out (slots written for F)
+ *   v_pool    device bf16 [B][Hkv][P][bs][d]  in/out
+ *   err_word  device uint32 [1]               OR-ed with OASIS_EW_* bits
+ * Requires P >= Kb, so a candidate slot always exists for every block of F.
+ */
+OASIS_API oasis_status oasis_gather_h2d(const oasis_shape* shape, const void* host_kv,
+                              const int32_t* sel, const int32_t* nsel,
+                              const int32_t* fetch, const int32_t* nfetch,
+                              int32_t* blk2slot, int32_t* slot2blk, int32_t* last_used,
+                              int32_t step, void* k_pool, void* v_pool,
+                              uint32_t* err_word, oasis_stream_t stream);
+
+/*
+ * a5. Block-sparse paged decode attention.
+ * Defines: decode attention of the next-token queries over only the resident
+ * selected KV blocks (OasisKV abstract; Figure 7 caption, right).
+ *   A = { x in S : blk2slot[x] != -1 }, and for every query head hq = h*G + g
+ *   out[b][hq] = sum over valid tokens t of A of softmax_t(scale * q.k_t) v_t,
+ *   or zero when A has no valid token.
+ * Arguments:
+ *   q         device bf16 [B][Hq][d]            true (next-token) queries
+ *   k_pool, v_pool  device bf16 [B][Hkv][P][bs][d]
+ *   sel, nsel, blk2slot, ctx_len               as above
+ *   scale     softmax scale, normally 1/sqrt(d)
+ *   workspace device scratch of ws_bytes >= oasis_attn_workspace_bytes(shape);
+ *             contents on entry are ignored; not touched by other calls
+ *   out       device float [B][Hq][d]           out
+ * Split-K: the blocks of each head are cut into chunks attended by separate
+ * thread blocks; a second kernel merges the partial softmax states.
+ */
+OASIS_API oasis_status oasis_sparse_decode_attn(const oasis_shape* shape, const void* q,
+                                      const void* k_pool, const void* v_pool,
+                                      const int32_t* sel, const int32_t* nsel,
+                                      const int32_t* blk2slot, const int32_t* ctx_len,
+                                      float scale, void* workspace, size_t ws_bytes,
+                                      float* out, oasis_stream_t stream);
+
+/* Bytes of device workspace oasis_sparse_decode_attn needs for `shape` (0 on a bad shape). */
+OASIS_API size_t oasis_attn_workspace_bytes(const oasis_shape* shape);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OASIS_H_ */

@@ -1,0 +1,151 @@
+"""Thin ctypes binding of ``liboasis.so`` with the C ABI's names.
+
+Argument marshalling only: every function takes torch tensors (or raw integer
+pointers), passes their addresses, sizes and the current CUDA stream to the
+library, and raises :class:`OasisError` when the library returns a non-OK
+status.  No computation of the method happens here.  If the library is missing
+the import of a function raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liboasis.so")
+
+OASIS_OK = 0
+STATUS_NAMES = {0: "OK", 1: "ERR_INVALID", 2: "ERR_CUDA", 3: "ERR_TIMEOUT", 4: "ERR_UNSUPPORTED"}
+
+EW_BAD_BLOCK = 0x1
+EW_BAD_SLOT = 0x2
+EW_NO_SLOT = 0x4
+EW_BAD_COUNT = 0x8
+EW_TIMEOUT = 0x10
+
+
+class OasisError(RuntimeError):
+    def __init__(self, fn: str, status: int, message: str):
+        super().__init__(f"{fn} -> {STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("B", "Hq", "Hkv", "d", "bs", "nb_max", "n_la", "Kb", "P")]
+
+    @classmethod
+    def of(cls, B, Hq, Hkv, nb_max, n_la, Kb, P, d=128, bs=16) -> "Shape":
+        return cls(B, Hq, Hkv, d, bs, nb_max, n_la, Kb, P)
+
+    @classmethod
+    def from_workload(cls, w) -> "Shape":
+        return cls(w.B, w.Hq, w.Hkv, w.d, w.bs, w.nb_max, w.n_la, w.Kb, w.P)
+
+    def astuple(self):
+        return tuple(getattr(self, n) for n, _ in self._fields_)
+
+
+_VP = ctypes.c_void_p
+_SIGS = {
+    "oasis_version": ([], ctypes.c_char_p),
+    "oasis_last_error": ([], ctypes.c_char_p),
+    "oasis_score_blocks": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
+    "oasis_topk_select": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
+    "oasis_fetch_diff_capped": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                 ctypes.c_int32, _VP, _VP, _VP], ctypes.c_int),
+    "oasis_gather_h2d": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                          ctypes.c_int32, _VP, _VP, _VP, _VP], ctypes.c_int),
+    "oasis_sparse_decode_attn": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                  ctypes.c_float, _VP, ctypes.c_size_t, _VP, _VP], ctypes.c_int),
+    "oasis_attn_workspace_bytes": ([ctypes.POINTER(Shape)], ctypes.c_size_t),
+}
+
+_lib = None
+
+
+def load(path: Optional[str] = None):
+    """Load liboasis.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it with sparse_decode_attention_oasis_gb300.build.build()")
+    lib = ctypes.CDLL(p)
+    for name, (args, res) in _SIGS.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, st: int):
+    if st != OASIS_OK:
+        raise OasisError(fn, st, load().oasis_last_error().decode())
+
+
+def oasis_version() -> str:
+    return load().oasis_version().decode()
+
+
+def oasis_last_error() -> str:
+    return load().oasis_last_error().decode()
+
+
+def oasis_attn_workspace_bytes(shape: Shape) -> int:
+    return int(load().oasis_attn_workspace_bytes(ctypes.byref(shape)))
+
+
+def oasis_score_blocks(shape: Shape, k_hbm, ctx_len, q_la, scores, stream=None):
+    _check("oasis_score_blocks", load().oasis_score_blocks(
+        ctypes.byref(shape), _ptr(k_hbm), _ptr(ctx_len), _ptr(q_la), _ptr(scores), _stream(stream)))
+
+
+def oasis_topk_select(shape: Shape, scores, k_hbm, q_la, ctx_len, sel, nsel, stream=None):
+    _check("oasis_topk_select", load().oasis_topk_select(
+        ctypes.byref(shape), _ptr(scores), _ptr(k_hbm), _ptr(q_la), _ptr(ctx_len), _ptr(sel),
+        _ptr(nsel), _stream(stream)))
+
+
+def oasis_fetch_diff_capped(shape: Shape, scores, k_hbm, q_la, ctx_len, sel, nsel, blk2slot,
+                            fetch_cap: int, fetch, nfetch, stream=None):
+    _check("oasis_fetch_diff_capped", load().oasis_fetch_diff_capped(
+        ctypes.byref(shape), _ptr(scores), _ptr(k_hbm), _ptr(q_la), _ptr(ctx_len), _ptr(sel),
+        _ptr(nsel), _ptr(blk2slot), int(fetch_cap), _ptr(fetch), _ptr(nfetch), _stream(stream)))
+
+
+def oasis_gather_h2d(shape: Shape, host_kv, sel, nsel, fetch, nfetch, blk2slot, slot2blk,
+                     last_used, step: int, k_pool, v_pool, err_word, stream=None):
+    _check("oasis_gather_h2d", load().oasis_gather_h2d(
+        ctypes.byref(shape), _ptr(host_kv), _ptr(sel), _ptr(nsel), _ptr(fetch), _ptr(nfetch),
+        _ptr(blk2slot), _ptr(slot2blk), _ptr(last_used), int(step), _ptr(k_pool), _ptr(v_pool),
+        _ptr(err_word), _stream(stream)))
+
+
+def oasis_sparse_decode_attn(shape: Shape, q, k_pool, v_pool, sel, nsel, blk2slot, ctx_len,
+                             scale: float, workspace, ws_bytes: int, out, stream=None):
+    _check("oasis_sparse_decode_attn", load().oasis_sparse_decode_attn(
+        ctypes.byref(shape), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(sel), _ptr(nsel),
+        _ptr(blk2slot), _ptr(ctx_len), float(scale), _ptr(workspace), int(ws_bytes), _ptr(out),
+        _stream(stream)))

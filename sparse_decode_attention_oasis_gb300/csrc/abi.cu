@@ -1,0 +1,190 @@
+// C ABI entry points: argument validation, then the kernel launches.
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "common.cuh"
+
+namespace oasis {
+cudaError_t launch_score_blocks(const Shape&, const uint16_t*, const int*, const uint16_t*, float2*, cudaStream_t);
+cudaError_t launch_topk_select(const Shape&, const float2*, const uint16_t*, const uint16_t*, const int*, int*,
+                               int*, cudaStream_t);
+cudaError_t launch_fetch_diff(const Shape&, const float2*, const uint16_t*, const uint16_t*, const int*,
+                              const int*, const int*, const int*, int, int*, int*, cudaStream_t);
+cudaError_t launch_gather_h2d(const Shape&, const uint16_t*, const int*, const int*, const int*, const int*,
+                              int*, int*, int*, int, uint16_t*, uint16_t*, unsigned*, cudaStream_t);
+cudaError_t launch_sparse_decode_attn(const Shape&, const uint16_t*, const uint16_t*, const uint16_t*,
+                                      const int*, const int*, const int*, const int*, float, void*, float*,
+                                      cudaStream_t);
+size_t attn_workspace_bytes(const Shape&);
+size_t topk_smem_bytes(const Shape&);
+}  // namespace oasis
+
+namespace {
+
+thread_local std::string g_last_error = "no error";
+
+oasis_status fail(oasis_status st, const char* fn, const std::string& msg) {
+  g_last_error = std::string(fn) + ": " + msg;
+  return st;
+}
+
+oasis_status cuda_fail(const char* fn, cudaError_t e) {
+  g_last_error = std::string(fn) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+  return OASIS_ERR_CUDA;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shape checks shared by every call.  Returns OK or the status to return.
+oasis_status check_shape(const oasis_shape* sh, const char* fn, oasis::Shape* out) {
+  if (!sh) return fail(OASIS_ERR_INVALID, fn, "shape is NULL");
+  const oasis_shape& s = *sh;
+  if (s.B < 1 || s.Hq < 1 || s.Hkv < 1 || s.nb_max < 1 || s.n_la < 1 || s.Kb < 1 || s.P < 1)
+    return fail(OASIS_ERR_INVALID, fn, "every shape field must be >= 1");
+  if (s.Hq % s.Hkv) return fail(OASIS_ERR_INVALID, fn, "Hq must be a multiple of Hkv");
+  const int G = s.Hq / s.Hkv;
+  if (s.d != 128) return fail(OASIS_ERR_UNSUPPORTED, fn, "head dim must be 128");
+  if (s.bs != 16) return fail(OASIS_ERR_UNSUPPORTED, fn, "block size must be 16 tokens");
+  if (G != 1 && G != 2 && G != 4 && G != 8) return fail(OASIS_ERR_UNSUPPORTED, fn, "GQA group must be 1, 2, 4 or 8");
+  if (s.n_la * G > 32) return fail(OASIS_ERR_UNSUPPORTED, fn, "n_la * G must be <= 32");
+  if (s.nb_max > 8192) return fail(OASIS_ERR_UNSUPPORTED, fn, "nb_max must be <= 8192");
+  if (s.Kb > 256) return fail(OASIS_ERR_UNSUPPORTED, fn, "Kb must be <= 256");
+  if (s.P < s.Kb || s.P > 1024) return fail(OASIS_ERR_UNSUPPORTED, fn, "P must be in [Kb, 1024]");
+  if ((long long)s.B * s.Hkv > 65535) return fail(OASIS_ERR_UNSUPPORTED, fn, "B * Hkv must be <= 65535");
+  *out = oasis::Shape{s.B, s.Hq, s.Hkv, s.d, s.bs, s.nb_max, s.n_la, s.Kb, s.P};
+  return OASIS_OK;
+}
+
+#define REQUIRE(cond, msg) \
+  do { if (!(cond)) return fail(OASIS_ERR_INVALID, fn, msg); } while (0)
+
+}  // namespace
+
+extern "C" {
+
+const char* oasis_version(void) { return "oasis-gb300 0.1 sm_103a"; }
+
+const char* oasis_last_error(void) { return g_last_error.c_str(); }
+
+oasis_status oasis_score_blocks(const oasis_shape* shape, const void* k_hbm, const int32_t* ctx_len,
+                                const void* q_la, float* scores, oasis_stream_t stream) {
+  static const char* fn = "oasis_score_blocks";
+  oasis::Shape s;
+  oasis_status st = check_shape(shape, fn, &s);
+  if (st != OASIS_OK) return st;
+  REQUIRE(k_hbm && aligned(k_hbm, 16), "k_hbm must be a 16-byte aligned device pointer");
+  REQUIRE(q_la && aligned(q_la, 16), "q_la must be a 16-byte aligned device pointer");
+  REQUIRE(ctx_len && aligned(ctx_len, 4), "ctx_len must be a 4-byte aligned device pointer");
+  REQUIRE(scores && aligned(scores, 8), "scores must be an 8-byte aligned device pointer");
+  cudaError_t e = oasis::launch_score_blocks(s, static_cast<const uint16_t*>(k_hbm), ctx_len,
+                                             static_cast<const uint16_t*>(q_la),
+                                             reinterpret_cast<float2*>(scores), (cudaStream_t)stream);
+  return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
+}
+
+oasis_status oasis_topk_select(const oasis_shape* shape, const float* scores, const void* k_hbm,
+                               const void* q_la, const int32_t* ctx_len, int32_t* sel, int32_t* nsel,
+                               oasis_stream_t stream) {
+  static const char* fn = "oasis_topk_select";
+  oasis::Shape s;
+  oasis_status st = check_shape(shape, fn, &s);
+  if (st != OASIS_OK) return st;
+  REQUIRE(scores && aligned(scores, 8), "scores must be an 8-byte aligned device pointer");
+  REQUIRE(k_hbm && aligned(k_hbm, 16), "k_hbm must be a 16-byte aligned device pointer");
+  REQUIRE(q_la && aligned(q_la, 16), "q_la must be a 16-byte aligned device pointer");
+  REQUIRE(ctx_len && aligned(ctx_len, 4), "ctx_len must be a 4-byte aligned device pointer");
+  REQUIRE(sel && aligned(sel, 4) && nsel && aligned(nsel, 4), "sel/nsel must be 4-byte aligned device pointers");
+  cudaError_t e = oasis::launch_topk_select(s, reinterpret_cast<const float2*>(scores),
+                                            static_cast<const uint16_t*>(k_hbm),
+                                            static_cast<const uint16_t*>(q_la), ctx_len, sel, nsel,
+                                            (cudaStream_t)stream);
+  return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
+}
+
+oasis_status oasis_fetch_diff_capped(const oasis_shape* shape, const float* scores, const void* k_hbm,
+                                     const void* q_la, const int32_t* ctx_len, const int32_t* sel,
+                                     const int32_t* nsel, const int32_t* blk2slot, int32_t fetch_cap,
+                                     int32_t* fetch, int32_t* nfetch, oasis_stream_t stream) {
+  static const char* fn = "oasis_fetch_diff_capped";
+  oasis::Shape s;
+  oasis_status st = check_shape(shape, fn, &s);
+  if (st != OASIS_OK) return st;
+  REQUIRE(scores && aligned(scores, 8), "scores must be an 8-byte aligned device pointer");
+  REQUIRE(k_hbm && aligned(k_hbm, 16), "k_hbm must be a 16-byte aligned device pointer");
+  REQUIRE(q_la && aligned(q_la, 16), "q_la must be a 16-byte aligned device pointer");
+  REQUIRE(ctx_len && aligned(ctx_len, 4), "ctx_len must be a 4-byte aligned device pointer");
+  REQUIRE(sel && nsel && blk2slot && fetch && nfetch, "sel/nsel/blk2slot/fetch/nfetch must be device pointers");
+  REQUIRE(aligned(sel, 4) && aligned(nsel, 4) && aligned(blk2slot, 4) && aligned(fetch, 4) && aligned(nfetch, 4),
+          "int32 arrays must be 4-byte aligned");
+  REQUIRE(fetch_cap >= 0 && fetch_cap <= s.Kb, "fetch_cap must be in [0, Kb]");
+  cudaError_t e = oasis::launch_fetch_diff(s, reinterpret_cast<const float2*>(scores),
+                                           static_cast<const uint16_t*>(k_hbm),
+                                           static_cast<const uint16_t*>(q_la), ctx_len, sel, nsel, blk2slot,
+                                           fetch_cap, fetch, nfetch, (cudaStream_t)stream);
+  return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
+}
+
+oasis_status oasis_gather_h2d(const oasis_shape* shape, const void* host_kv, const int32_t* sel,
+                              const int32_t* nsel, const int32_t* fetch, const int32_t* nfetch,
+                              int32_t* blk2slot, int32_t* slot2blk, int32_t* last_used, int32_t step,
+                              void* k_pool, void* v_pool, uint32_t* err_word, oasis_stream_t stream) {
+  static const char* fn = "oasis_gather_h2d";
+  oasis::Shape s;
+  oasis_status st = check_shape(shape, fn, &s);
+  if (st != OASIS_OK) return st;
+  REQUIRE(host_kv && aligned(host_kv, 16), "host_kv must be a 16-byte aligned pointer");
+  REQUIRE(k_pool && v_pool && aligned(k_pool, 16) && aligned(v_pool, 16),
+          "k_pool/v_pool must be 16-byte aligned device pointers");
+  REQUIRE(sel && nsel && fetch && nfetch && blk2slot && slot2blk && last_used && err_word,
+          "table pointers must be non-NULL");
+  REQUIRE(aligned(sel, 4) && aligned(nsel, 4) && aligned(fetch, 4) && aligned(nfetch, 4) &&
+              aligned(blk2slot, 4) && aligned(slot2blk, 4) && aligned(last_used, 4) && aligned(err_word, 4),
+          "int32 arrays must be 4-byte aligned");
+  // The host tier must be page-locked host memory mapped into the device address space.
+  cudaPointerAttributes attr;
+  cudaError_t e = cudaPointerGetAttributes(&attr, host_kv);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(OASIS_ERR_INVALID, fn, "host_kv is not a CUDA-registered pointer");
+  }
+  if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr)
+    return fail(OASIS_ERR_INVALID, fn, "host_kv must be page-locked, device-mapped host memory");
+  e = oasis::launch_gather_h2d(s, static_cast<const uint16_t*>(attr.devicePointer), sel, nsel, fetch, nfetch,
+                               blk2slot, slot2blk, last_used, step, static_cast<uint16_t*>(k_pool),
+                               static_cast<uint16_t*>(v_pool), err_word, (cudaStream_t)stream);
+  return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
+}
+
+size_t oasis_attn_workspace_bytes(const oasis_shape* shape) {
+  oasis::Shape s;
+  if (check_shape(shape, "oasis_attn_workspace_bytes", &s) != OASIS_OK) return 0;
+  return oasis::attn_workspace_bytes(s);
+}
+
+oasis_status oasis_sparse_decode_attn(const oasis_shape* shape, const void* q, const void* k_pool,
+                                      const void* v_pool, const int32_t* sel, const int32_t* nsel,
+                                      const int32_t* blk2slot, const int32_t* ctx_len, float scale,
+                                      void* workspace, size_t ws_bytes, float* out, oasis_stream_t stream) {
+  static const char* fn = "oasis_sparse_decode_attn";
+  oasis::Shape s;
+  oasis_status st = check_shape(shape, fn, &s);
+  if (st != OASIS_OK) return st;
+  REQUIRE(q && aligned(q, 16), "q must be a 16-byte aligned device pointer");
+  REQUIRE(k_pool && v_pool && aligned(k_pool, 16) && aligned(v_pool, 16),
+          "k_pool/v_pool must be 16-byte aligned device pointers");
+  REQUIRE(sel && nsel && blk2slot && ctx_len, "table pointers must be non-NULL");
+  REQUIRE(aligned(sel, 4) && aligned(nsel, 4) && aligned(blk2slot, 4) && aligned(ctx_len, 4),
+          "int32 arrays must be 4-byte aligned");
+  REQUIRE(out && aligned(out, 16), "out must be a 16-byte aligned device pointer");
+  REQUIRE(workspace && aligned(workspace, 16), "workspace must be a 16-byte aligned device pointer");
+  REQUIRE(ws_bytes >= oasis::attn_workspace_bytes(s), "workspace is smaller than oasis_attn_workspace_bytes()");
+  REQUIRE(scale == scale && scale > 0.f, "scale must be a positive number");
+  cudaError_t e = oasis::launch_sparse_decode_attn(s, static_cast<const uint16_t*>(q),
+                                                   static_cast<const uint16_t*>(k_pool),
+                                                   static_cast<const uint16_t*>(v_pool), sel, nsel, blk2slot,
+                                                   ctx_len, scale, workspace, out, (cudaStream_t)stream);
+  return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
+}
+
+}  // extern "C"

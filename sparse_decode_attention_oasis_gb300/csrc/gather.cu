@@ -1,0 +1,217 @@
+// a4: slot assignment, zero-copy host-tier gather into HBM slots, table update.
+//
+// OasisKV abstract (prefetch from a higher-capacity tier into HBM before the next
+// decode step uses the blocks); metalmedia.ai page, Figure 9 caption (a head-wise
+// table maps each GPU block of the bounded working set to a CPU block) and
+// Table 2 caption (LRU eviction).
+//
+// One thread block per (request, KV head):
+//   1. candidate slots = free slots ascending, then victims (resident blocks not
+//      in S) by (last_used, block) - each slot computes its own rank by counting;
+//   2. F[i] takes candidate i: evicted block -> blk2slot = -1, then the new
+//      mapping is written (evicted blocks are outside S, fetched ones inside, so
+//      the two sets of writes never touch the same entry);
+//   3. last_used = step for every resident block of S;
+//   4. the 8 KiB (K 4 KiB + V 4 KiB) of every fetched block is read from mapped
+//      page-locked host memory with 16-byte loads (several in flight per thread)
+//      and written to its slot.  The copy is bound by the host link.
+// Out-of-range indices set bits of the error word and are skipped.
+#include "common.cuh"
+
+namespace oasis {
+
+constexpr int kGatherThreads = 256;
+constexpr int kGatherUnroll = 4;
+
+__device__ __forceinline__ uint4 ld_host16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__global__ void __launch_bounds__(kGatherThreads)
+gather_h2d_kernel(Shape s, const uint16_t* __restrict__ host_kv, const int* __restrict__ sel,
+                  const int* __restrict__ nsel, const int* __restrict__ fetch,
+                  const int* __restrict__ nfetch, int* __restrict__ blk2slot,
+                  int* __restrict__ slot2blk, int* __restrict__ last_used, int step,
+                  uint16_t* __restrict__ k_pool, uint16_t* __restrict__ v_pool,
+                  unsigned* __restrict__ err) {
+  extern __shared__ __align__(16) int gsm[];
+  const int Kb = s.Kb, P = s.P;
+  int* S = gsm;              // [Kb]
+  int* F = S + Kb;           // [Kb]
+  int* s2b = F + Kb;         // [P]
+  int* lu = s2b + P;         // [P]
+  int* cand = lu + P;        // [P]
+  int* src = cand + P;       // [Kb] fetched block per copy
+  int* dst = src + Kb;       // [Kb] slot per copy
+  int* scal = dst + Kb;      // [4]
+  const int head = blockIdx.x;
+  const long long tb = (long long)head * s.nb_max;
+  const long long ts = (long long)head * P;
+  unsigned ew = 0;
+
+  int ns = nsel[head], nf = nfetch[head];
+  if (ns < 0 || ns > Kb) { ew |= OASIS_EW_BAD_COUNT; ns = ns < 0 ? 0 : Kb; }
+  if (nf < 0 || nf > Kb) { ew |= OASIS_EW_BAD_COUNT; nf = nf < 0 ? 0 : Kb; }
+  for (int i = threadIdx.x; i < ns; i += blockDim.x) {
+    int x = sel[(long long)head * Kb + i];
+    if (x < 0 || x >= s.nb_max) { ew |= OASIS_EW_BAD_BLOCK; x = -1; }
+    S[i] = x;
+  }
+  for (int i = threadIdx.x; i < nf; i += blockDim.x) {
+    int x = fetch[(long long)head * Kb + i];
+    if (x < 0 || x >= s.nb_max) { ew |= OASIS_EW_BAD_BLOCK; x = -1; }
+    F[i] = x;
+  }
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    int o = slot2blk[ts + p];
+    if (o >= s.nb_max || o < -1) { ew |= OASIS_EW_BAD_BLOCK; o = -1; }
+    s2b[p] = o;
+    lu[p] = last_used[ts + p];
+  }
+  if (threadIdx.x == 0) { scal[0] = 0; scal[1] = 0; }
+  __syncthreads();
+
+  // 1. candidate ranks
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    const int o = s2b[p];
+    bool in_s = false;
+    if (o >= 0) {  // binary search in S (ascending)
+      int lo = 0, hi = ns - 1;
+      while (lo <= hi) {
+        const int mid = (lo + hi) >> 1;
+        const int v = S[mid];
+        if (v == o) { in_s = true; break; }
+        if (v < o) lo = mid + 1; else hi = mid - 1;
+      }
+    }
+    const bool is_free = o < 0;
+    if (is_free) atomicAdd(&scal[0], 1);
+    else if (!in_s) atomicAdd(&scal[1], 1);
+    cand[p] = is_free ? 0 : (in_s ? -1 : 1);  // provisional class, ranks below
+  }
+  __syncthreads();
+  const int nfree = scal[0], nvict = scal[1];
+  int myrank[(1024 + kGatherThreads - 1) / kGatherThreads];
+  int k = 0;
+  for (int p = threadIdx.x; p < P; p += blockDim.x, ++k) {
+    const int cl = cand[p];
+    int r = -1;
+    if (cl == 0) {
+      r = 0;
+      for (int q = 0; q < p; ++q) r += (cand[q] == 0);
+    } else if (cl == 1) {
+      r = nfree;
+      const int lp = lu[p], op = s2b[p];
+      for (int q = 0; q < P; ++q) {
+        if (cand[q] != 1 || q == p) continue;
+        const int lq = lu[q], oq = s2b[q];
+        r += (lq < lp) || (lq == lp && oq < op);
+      }
+    }
+    myrank[k] = r;
+  }
+  __syncthreads();
+  k = 0;
+  for (int p = threadIdx.x; p < P; p += blockDim.x, ++k) cand[p] = -1;
+  __syncthreads();
+  k = 0;
+  for (int p = threadIdx.x; p < P; p += blockDim.x, ++k)
+    if (myrank[k] >= 0) cand[myrank[k]] = p;
+  __syncthreads();
+
+  // 2. assignment: evictions, then new mappings
+  const int ncand = nfree + nvict;
+  int ncopy = nf < ncand ? nf : ncand;
+  if (nf > ncand && threadIdx.x == 0) ew |= OASIS_EW_NO_SLOT;
+  for (int i = threadIdx.x; i < ncopy; i += blockDim.x) {
+    const int p = cand[i];
+    if (p < 0 || p >= P) continue;
+    const int old = s2b[p];
+    if (old >= 0) blk2slot[tb + old] = -1;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < ncopy; i += blockDim.x) {
+    const int p = cand[i];
+    int x = F[i];
+    if (p < 0 || p >= P) { ew |= OASIS_EW_BAD_SLOT; src[i] = -1; dst[i] = 0; continue; }
+    src[i] = x;
+    dst[i] = p;
+    if (x >= 0) {
+      blk2slot[tb + x] = p;
+      s2b[p] = x;
+    } else {
+      s2b[p] = s2b[p] >= 0 ? -1 : s2b[p];  // a bad entry frees nothing it did not evict
+    }
+  }
+  __syncthreads();
+
+  // 3. LRU clock of the attended blocks
+  for (int i = threadIdx.x; i < ns; i += blockDim.x) {
+    const int x = S[i];
+    if (x < 0) continue;
+    const int p = blk2slot[tb + x];
+    if (p >= P) { ew |= OASIS_EW_BAD_SLOT; continue; }
+    if (p >= 0) lu[p] = step;
+  }
+  __syncthreads();
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    slot2blk[ts + p] = s2b[p];
+    last_used[ts + p] = lu[p];
+  }
+
+  // 4. copy host tier -> slots (16-byte units: 256 per K block, 256 per V block)
+  constexpr int kUnits = 2 * kBS * kD * 2 / 16;  // 512 per block (K then V)
+  const int total = ncopy * kUnits;
+  for (int base = threadIdx.x; base < total; base += blockDim.x * kGatherUnroll) {
+    uint4 v[kGatherUnroll];
+    int tgt[kGatherUnroll];
+#pragma unroll
+    for (int u = 0; u < kGatherUnroll; ++u) {
+      const int id = base + u * blockDim.x;
+      tgt[u] = -1;
+      if (id < total) {
+        const int i = id / kUnits, w = id - i * kUnits;
+        const int x = src[i];
+        if (x >= 0) {
+          const uint16_t* from = host_kv + ((tb + x) * 2 * kBS * kD) + (long long)w * 8;
+          v[u] = ld_host16(from);
+          tgt[u] = id;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kGatherUnroll; ++u) {
+      if (tgt[u] < 0) continue;
+      const int id = tgt[u];
+      const int i = id / kUnits, w = id - i * kUnits;
+      const int p = dst[i];
+      const int half = w >> 8;  // 0: K, 1: V
+      uint16_t* to = (half ? v_pool : k_pool) + ((ts + p) * kBS * kD) + (long long)(w & 255) * 8;
+      *reinterpret_cast<uint4*>(to) = v[u];
+    }
+  }
+  if (ew) atomicOr(err, ew);
+}
+
+size_t gather_smem_bytes(const Shape& s) { return sizeof(int) * (4 * (size_t)s.Kb + 3 * (size_t)s.P + 4); }
+
+cudaError_t launch_gather_h2d(const Shape& s, const uint16_t* host_kv, const int* sel, const int* nsel,
+                              const int* fetch, const int* nfetch, int* blk2slot, int* slot2blk,
+                              int* last_used, int step, uint16_t* k_pool, uint16_t* v_pool,
+                              unsigned* err, cudaStream_t stream) {
+  const size_t smem = gather_smem_bytes(s);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(gather_h2d_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  gather_h2d_kernel<<<s.B * s.Hkv, kGatherThreads, smem, stream>>>(s, host_kv, sel, nsel, fetch, nfetch,
+                                                                   blk2slot, slot2blk, last_used, step,
+                                                                   k_pool, v_pool, err);
+  return cudaGetLastError();
+}
+
+}  // namespace oasis

@@ -1,0 +1,215 @@
+// a1: block scoring against the lookahead queries, on the tensor cores.
+//
+// score(x) = max over lookahead queries j, GQA query heads g and valid tokens t
+// of block x of q_la[j, hG+g] . k_t / sqrt(d)  (OasisKV, metalmedia.ai page,
+// Figure 7 caption: the draft query scans the keys to predict the next step's
+// top-K blocks).
+//
+// Mapping.  One warp scores one 16-token block at a time as a 16 x N tile
+// D = K_blk (16 tok x 128 d) * Q^T (128 d x N queries) with mma.m16n8k16 (bf16
+// in, fp32 accumulate).  Because a dot product may sum its d terms in any order,
+// the d axis is permuted identically for K and Q: thread (g = lane/4,
+// t = lane%4) loads 16-byte chunks t, t+4, t+8, t+12 of token rows g and g+8
+// straight from HBM (every 32-byte sector is used by one instruction), and
+// those registers are already A fragments.  Q fragments of the head stay in
+// registers for the whole chunk of blocks.  No shared memory is needed.
+//
+// Certified bound.  Each block also gets e >= |s~ - score|: the tensor-core
+// fp32 accumulation of 8 steps of 16 exact products is modelled as at most
+// 17 truncations of 2^-23 of the running magnitude per step, i.e.
+// 136 * 2^-23 ~ 2^-15.9 of sum|q_i k_i| <= |q|_2 |k|_2.  We use 2^-12 (a 15x
+// margin), the max query norm of the head and the max key norm of the block
+// (computed here in fp32 from the same registers), plus the rounding of the
+// 1/sqrt(d) product and an absolute 2^-60 for underflowed products.
+#include "common.cuh"
+
+namespace oasis {
+
+constexpr int kScoreWarps = 4;
+constexpr int kScoreChunk = 128;  // blocks per (CTA, head) work item
+
+template <int NT>
+struct QFrag {
+  uint32_t w[NT][4][4];  // [n-tile][d chunk i][word]
+};
+
+template <int NT>
+__global__ void __launch_bounds__(kScoreWarps * 32, (NT <= 2 ? 3 : 2))
+score_blocks_kernel(Shape s, const uint16_t* __restrict__ k_hbm, const int* __restrict__ ctx_len,
+                    const uint16_t* __restrict__ q_la, float2* __restrict__ scores,
+                    int chunks_per_head, int total_chunks, float inv_sqrt_d) {
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int G = s.Hq / s.Hkv;
+  const int N = s.n_la * G;
+  const long long T_max = (long long)s.nb_max * kBS;
+
+  for (int chunk = blockIdx.x; chunk < total_chunks; chunk += gridDim.x) {
+    const int head = chunk / chunks_per_head;  // b * Hkv + h
+    const int c = chunk - head * chunks_per_head;
+    const int b = head / s.Hkv, h = head - b * s.Hkv;
+    const int ctx = ctx_len[b];
+    const int nb = clamp_nb(ctx, s.nb_max);
+    const int blk0 = c * kScoreChunk;
+    if (blk0 >= nb) continue;
+    const int blk1 = min(nb, blk0 + kScoreChunk);
+
+    // Q fragments: query n = nt*8 + g is lookahead j = n / G, head hG + n % G.
+    QFrag<NT> qf;
+    float qn2 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int n = nt * 8 + g;
+      float ss = 0.f;
+      if (n < N) {
+        const int j = n / G, gg = n - j * G;
+        const uint16_t* qrow = q_la + (((long long)b * s.n_la + j) * s.Hq + h * G + gg) * kD;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint4 v = ldg_nc(qrow + (t + 4 * i) * 8);
+          qf.w[nt][i][0] = v.x; qf.w[nt][i][1] = v.y; qf.w[nt][i][2] = v.z; qf.w[nt][i][3] = v.w;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            float a = bf_lo(qf.w[nt][i][m]), bb = bf_hi(qf.w[nt][i][m]);
+            ss = fmaf(a, a, ss);
+            ss = fmaf(bb, bb, ss);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int m = 0; m < 4; ++m) qf.w[nt][i][m] = 0u;
+      }
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+      qn2 = fmaxf(qn2, ss);
+    }
+    qn2 = warp_max(qn2);
+    const float qnorm = sqrtf(qn2);
+
+    const uint16_t* kbase = k_hbm + ((long long)head * T_max) * kD;
+    int blk = blk0 + warp;
+    uint4 ra[4], rb[4];
+    if (blk < blk1) {
+      const uint16_t* p = kbase + ((long long)blk * kBS) * kD;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        ra[i] = ldg_stream(p + g * kD + (t + 4 * i) * 8);
+        rb[i] = ldg_stream(p + (g + 8) * kD + (t + 4 * i) * 8);
+      }
+    }
+    for (; blk < blk1; blk += kScoreWarps) {
+      uint4 ca[4], cb[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { ca[i] = ra[i]; cb[i] = rb[i]; }
+      const int nxt = blk + kScoreWarps;
+      if (nxt < blk1) {  // prefetch the next block of this warp
+        const uint16_t* p = kbase + ((long long)nxt * kBS) * kD;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          ra[i] = ldg_stream(p + g * kD + (t + 4 * i) * 8);
+          rb[i] = ldg_stream(p + (g + 8) * kD + (t + 4 * i) * 8);
+        }
+      }
+      float acc[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t A[4] = {ca[i].x, ca[i].y, ca[i].z, ca[i].w};
+        const uint32_t Bw[4] = {cb[i].x, cb[i].y, cb[i].z, cb[i].w};
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            mma_bf16_16816(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3], A[2 * hh], Bw[2 * hh],
+                           A[2 * hh + 1], Bw[2 * hh + 1], qf.w[nt][i][2 * hh],
+                           qf.w[nt][i][2 * hh + 1]);
+        }
+      }
+      const int tok = blk * kBS + g;
+      const bool v0 = tok < ctx, v1 = tok + 8 < ctx;
+      float m = neg_inf();
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int n0 = nt * 8 + 2 * t;
+        if (n0 < N) {
+          if (v0) m = fmaxf(m, acc[nt][0]);
+          if (v1) m = fmaxf(m, acc[nt][2]);
+        }
+        if (n0 + 1 < N) {
+          if (v0) m = fmaxf(m, acc[nt][1]);
+          if (v1) m = fmaxf(m, acc[nt][3]);
+        }
+      }
+      m = warp_max(m);
+      // max key norm of the valid tokens of the block
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t A[4] = {ca[i].x, ca[i].y, ca[i].z, ca[i].w};
+        const uint32_t Bw[4] = {cb[i].x, cb[i].y, cb[i].z, cb[i].w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          float a0 = bf_lo(A[w]), a1 = bf_hi(A[w]);
+          float b0 = bf_lo(Bw[w]), b1 = bf_hi(Bw[w]);
+          s0 = fmaf(a0, a0, s0); s0 = fmaf(a1, a1, s0);
+          s1 = fmaf(b0, b0, s1); s1 = fmaf(b1, b1, s1);
+        }
+      }
+      s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+      s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+      float kn2 = fmaxf(v0 ? s0 : 0.f, v1 ? s1 : 0.f);
+      kn2 = warp_max(kn2);
+      if (lane == 0) {
+        const float sc = m * inv_sqrt_d;
+        const float e = kAccRel * 1.0009765625f * qnorm * sqrtf(kn2) * inv_sqrt_d +
+                        fabsf(sc) * 2.384185791015625e-07f /* 2^-22 */ + 8.673617379884035e-19f /* 2^-60 */;
+        scores[(long long)head * s.nb_max + blk] = make_float2(sc, e);
+      }
+    }
+  }
+}
+
+int score_grid_limit(int nt);
+
+cudaError_t launch_score_blocks(const Shape& s, const uint16_t* k, const int* ctx, const uint16_t* q_la,
+                                float2* scores, cudaStream_t stream) {
+  const int N = s.n_la * (s.Hq / s.Hkv);
+  const int NT = (N + 7) / 8;
+  const int chunks_per_head = (s.nb_max + kScoreChunk - 1) / kScoreChunk;
+  const int total = s.B * s.Hkv * chunks_per_head;
+  const float inv = 1.0f / sqrtf((float)s.d);
+  int grid = min(total, score_grid_limit(NT));
+  if (grid < 1) grid = 1;
+  dim3 block(kScoreWarps * 32);
+  switch (NT) {
+    case 1: score_blocks_kernel<1><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, chunks_per_head, total, inv); break;
+    case 2: score_blocks_kernel<2><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, chunks_per_head, total, inv); break;
+    case 3: score_blocks_kernel<3><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, chunks_per_head, total, inv); break;
+    case 4: score_blocks_kernel<4><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, chunks_per_head, total, inv); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+int score_grid_limit(int nt) {
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int threads = kScoreWarps * 32;
+  switch (nt) {
+    case 1: cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_blocks_kernel<1>, threads, 0); break;
+    case 2: cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_blocks_kernel<2>, threads, 0); break;
+    case 3: cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_blocks_kernel<3>, threads, 0); break;
+    default: cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_blocks_kernel<4>, threads, 0); break;
+  }
+  if (per_sm < 1) per_sm = 1;
+  return sms * per_sm;
+}
+
+}  // namespace oasis

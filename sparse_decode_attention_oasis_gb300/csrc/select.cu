@@ -1,0 +1,544 @@
+// a2 top-K under the token budget and a3 capped diff against the resident set.
+//
+// Both steps pick "the r best candidates by (exact score descending, block index
+// ascending)" out of a candidate list: all blocks of a head for the top-K (OasisKV
+// abstract: 2,048-token KV budget; Figure 7 caption: top-K blocks), the
+// selected-but-missing blocks for the capped fetch list (metalmedia.ai page,
+// explanatory figure step 3; Table 2 caption: the per-step fetch cap).
+//
+// Exact selection from certified intervals.  The scores come with a bound e,
+// |s~ - s| <= e.  With t = the r-th largest s~ (radix select on order-preserving
+// keys) and E = max e over the candidates:
+//   s~_i - e_i > t + E  => i is certainly among the r best,
+//   s~_i + e_i < t - E  => i certainly is not,
+// (every candidate that could rank at or above a "certain" one has s~ > t, and
+// at most r-1 do; conversely the r candidates with s~ >= t all rank above a
+// "certainly not").  The remaining candidates U are re-scored exactly:
+//   1. fp32 re-computation of the 16 x N dot products of the block on the CUDA
+//      cores, with the a-priori bound |err| <= 2^-16 |q| |k| + 2^-120
+//      (sequential fma over 128 terms: gamma_128 < 2^-16.9);
+//   2. the dots whose interval reaches the block's best lower bound are
+//      evaluated exactly: each bf16 is m * 2^(E-134), each product is an integer
+//      times 2^-266, and a 544-bit two's complement fixed-point accumulator
+//      (17 limbs of 32 bits, carries deferred in 64-bit shared-memory words)
+//      holds the sum with no rounding at all;
+//   3. U is merged into a running top-r set by exact comparison (a rank count
+//      over the union), 16 blocks at a time.
+// The result equals the definition for every finite input.
+#include "common.cuh"
+
+namespace oasis {
+
+constexpr int kSelThreads = 512;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kLimbs = 17;
+constexpr int kMaxN = 32;      // lookahead queries x GQA group
+constexpr int kMaxR = 256;     // largest budget in blocks
+constexpr int kQStride = 129;  // fp32 query rows padded against bank conflicts
+
+struct SelCtx {
+  const uint16_t* k;   // keys of this head [T_max][128]
+  const uint16_t* q_la;
+  int b, h, ctx, N, G, n_la, Hq;
+  // shared memory
+  float* qf;                   // [kMaxN][kQStride]
+  uint16_t* qb;                // [kMaxN][128]
+  float* qn;                   // [kMaxN]
+  unsigned long long* lacc;    // [kSelWarps][kLimbs]
+  uint32_t* tmp;               // [kSelWarps][kLimbs]
+  uint32_t* bval;              // [kSelWarps][kLimbs]
+  int* bidx;                   // [kSelWarps]
+  uint32_t* tval;              // [kMaxR][kLimbs]
+  int* tidx;                   // [kMaxR]
+  uint32_t* hist;              // [256]
+  int* scal;                   // [8] scalars
+  float* fscal;                // [kSelWarps]
+};
+
+// ---------------------------------------------------------------- exact arithmetic
+__device__ __forceinline__ int exact_cmp(const uint32_t* a, const uint32_t* b) {
+  const int ta = (int)a[kLimbs - 1], tb = (int)b[kLimbs - 1];
+  if (ta != tb) return ta < tb ? -1 : 1;
+  for (int i = kLimbs - 2; i >= 0; --i)
+    if (a[i] != b[i]) return a[i] < b[i] ? -1 : 1;
+  return 0;
+}
+
+// Exact q.k (times 2^266) of a 128-long bf16 row pair, by one warp.
+__device__ void warp_exact_dot(const uint16_t* __restrict__ krow, const uint16_t* qrow,
+                               unsigned long long* acc, uint32_t* out, int lane) {
+  if (lane < kLimbs) acc[lane] = 0ull;
+  __syncwarp();
+  for (int e = lane; e < kD; e += 32) {
+    const uint32_t kb = __ldg(krow + e), qb = qrow[e];
+    const uint32_t kE = (kb >> 7) & 0xffu, qE = (qb >> 7) & 0xffu;
+    const uint32_t km = (kb & 0x7fu) | (kE ? 0x80u : 0u);
+    const uint32_t qm = (qb & 0x7fu) | (qE ? 0x80u : 0u);
+    const uint32_t mm = km * qm;
+    if (mm) {
+      const int ee = (int)(kE ? kE : 1u) + (int)(qE ? qE : 1u) - 2;  // 0 .. 508
+      const unsigned long long v = (unsigned long long)mm << (ee & 31);
+      unsigned long long lo = v & 0xffffffffull, hi = v >> 32;
+      if ((kb ^ qb) & 0x8000u) {
+        lo = (unsigned long long)(-(long long)lo);
+        hi = (unsigned long long)(-(long long)hi);
+      }
+      atomicAdd(acc + (ee >> 5), lo);
+      if (hi) atomicAdd(acc + (ee >> 5) + 1, hi);
+    }
+  }
+  __syncwarp();
+  if (lane == 0) {
+    long long carry = 0;
+    for (int i = 0; i < kLimbs; ++i) {
+      const long long v = (long long)acc[i] + carry;
+      out[i] = (uint32_t)(unsigned long long)v;
+      carry = v >> 32;
+    }
+  }
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------- block-wide helpers
+__device__ __forceinline__ int block_excl_scan(int v, int* red, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) red[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < kSelWarps ? red[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kSelWarps) red[lane] = w;
+    if (lane == kSelWarps - 1) *total = w;
+  }
+  __syncthreads();
+  const int base = warp ? red[warp - 1] : 0;
+  const int res = base + x - v;
+  __syncthreads();
+  return res;
+}
+
+__device__ __forceinline__ float block_max(float v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_max(v);
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float r = red[0];
+  for (int i = 1; i < kSelWarps; ++i) r = fmaxf(r, red[i]);
+  __syncthreads();
+  return r;
+}
+
+// key of the k-th largest (k >= 1) s~ among se[0..n)
+__device__ uint32_t kth_largest_key(const float2* se, int n, int k, uint32_t* hist, int* scal) {
+  uint32_t prefix = 0, mask = 0;
+  int kk = k;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const uint32_t key = float_key(se[i].x);
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      uint32_t c[8], sum = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) { c[q] = hist[255 - (lane * 8 + q)]; sum += c[q]; }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t excl = incl - sum;
+      if (excl < (uint32_t)kk && (uint32_t)kk <= incl) {
+        uint32_t run = excl;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (run + c[q] >= (uint32_t)kk) {
+            scal[0] = 255 - (lane * 8 + q);
+            scal[1] = (int)run;
+            break;
+          }
+          run += c[q];
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= (uint32_t)scal[0] << shift;
+    mask |= 255u << shift;
+    kk -= scal[1];
+    __syncthreads();
+  }
+  return prefix;
+}
+
+// Stage the head's lookahead queries (fp32, bf16 bits, norms) in shared memory.
+__device__ void stage_queries(SelCtx& c) {
+  for (int idx = threadIdx.x; idx < c.N * kD; idx += blockDim.x) {
+    const int n = idx / kD, i = idx - n * kD;
+    const int j = n / c.G, gg = n - j * c.G;
+    const uint16_t v = c.q_la[(((long long)c.b * c.n_la + j) * c.Hq + c.h * c.G + gg) * kD + i];
+    c.qb[n * kD + i] = v;
+    c.qf[n * kQStride + i] = __uint_as_float((uint32_t)v << 16);
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int n = warp; n < c.N; n += kSelWarps) {
+    float ss = 0.f;
+    for (int i = lane; i < kD; i += 32) ss = fmaf(c.qf[n * kQStride + i], c.qf[n * kQStride + i], ss);
+    ss = warp_sum(ss);
+    if (lane == 0) c.qn[n] = sqrtf(ss);
+  }
+  __syncthreads();
+}
+
+// Exact score (x 2^266, as kLimbs words) of block `blk`, by one warp, into out.
+__device__ void warp_exact_block_score(const SelCtx& c, int blk, uint32_t* out, int warp, int lane) {
+  constexpr int kMaxPerLane = (kBS * kMaxN) / 32;
+  const int ndots = kBS * c.N;
+  const uint16_t* kblk = c.k + (long long)blk * kBS * kD;
+  // token norms (lanes 0..15)
+  float kn = 0.f;
+  if (lane < kBS) {
+    const uint32_t* row = reinterpret_cast<const uint32_t*>(kblk + lane * kD);
+    for (int i = 0; i < kD / 2; ++i) {
+      const uint32_t w = __ldg(row + i);
+      kn = fmaf(bf_lo(w), bf_lo(w), kn);
+      kn = fmaf(bf_hi(w), bf_hi(w), kn);
+    }
+    kn = sqrtf(kn);
+  }
+  float vlo[kMaxPerLane], vhi[kMaxPerLane];
+  float best_lo = neg_inf();
+#pragma unroll
+  for (int m = 0; m < kMaxPerLane; ++m) {
+    const int dd = lane + 32 * m;
+    const int tau = dd / c.N, n = dd - tau * c.N;
+    const float kt = __shfl_sync(0xffffffffu, kn, tau & 15);
+    vlo[m] = neg_inf();
+    vhi[m] = neg_inf();
+    if (dd < ndots && blk * kBS + tau < c.ctx) {
+      const uint32_t* row = reinterpret_cast<const uint32_t*>(kblk + tau * kD);
+      const float* qr = c.qf + n * kQStride;
+      float v = 0.f;
+      for (int i = 0; i < kD / 2; ++i) {
+        const uint32_t w = __ldg(row + i);
+        v = fmaf(bf_lo(w), qr[2 * i], v);
+        v = fmaf(bf_hi(w), qr[2 * i + 1], v);
+      }
+      const float eps = __fmaf_ru(1.52587890625e-05f /* 2^-16 */, __fmul_ru(kt, c.qn[n]),
+                                  7.52316384526264e-37f /* 2^-120 */);
+      vlo[m] = __fsub_rd(v, eps);
+      vhi[m] = __fadd_ru(v, eps);
+      if (!(fabsf(v) <= 3.0e38f)) { vlo[m] = neg_inf(); vhi[m] = __int_as_float(0x7f800000); }
+      best_lo = fmaxf(best_lo, vlo[m]);
+    }
+  }
+  best_lo = warp_max(best_lo);
+  bool have = false;
+  uint32_t* tmp = c.tmp + warp * kLimbs;
+  unsigned long long* acc = c.lacc + warp * kLimbs;
+#pragma unroll
+  for (int m = 0; m < kMaxPerLane; ++m) {
+    const bool cand = (lane + 32 * m) < ndots && vhi[m] >= best_lo && vhi[m] != neg_inf();
+    unsigned mask = __ballot_sync(0xffffffffu, cand);
+    while (mask) {
+      const int src = __ffs(mask) - 1;
+      mask &= mask - 1;
+      const int dd = src + 32 * m;
+      const int tau = dd / c.N, n = dd - tau * c.N;
+      warp_exact_dot(kblk + tau * kD, c.qb + n * kD, acc, tmp, lane);
+      if (lane == 0) {
+        if (!have || exact_cmp(tmp, out) > 0)
+          for (int i = 0; i < kLimbs; ++i) out[i] = tmp[i];
+      }
+      have = true;
+      __syncwarp();
+    }
+  }
+  if (!have && lane == 0) {
+    for (int i = 0; i < kLimbs - 1; ++i) out[i] = 0u;
+    out[kLimbs - 1] = 0x80000000u;
+  }
+  __syncwarp();
+}
+
+// Mark (cls = 1) the r best of the uncertain candidates U[0..nU) by exact order;
+// cand_blk maps a candidate index to its block (nullptr = identity).
+__device__ void refine_top_r(SelCtx& c, const int* U, int nU, int r, const int* cand_blk,
+                             uint8_t* cls) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  stage_queries(c);
+  int tcount = 0;
+  for (int base = 0; base < nU; base += kSelWarps) {
+    const int nbat = min(kSelWarps, nU - base);
+    if (warp < nbat) {
+      const int ci = U[base + warp];
+      const int blk = cand_blk ? cand_blk[ci] : ci;
+      warp_exact_block_score(c, blk, c.bval + warp * kLimbs, warp, lane);
+      if (lane == 0) c.bidx[warp] = ci;
+    }
+    __syncthreads();
+    const int tot = tcount + nbat;
+    uint32_t mine[kLimbs];
+    int myidx = -1, rank = 0;
+    if ((int)threadIdx.x < tot) {
+      const uint32_t* src = threadIdx.x < (unsigned)tcount ? c.tval + threadIdx.x * kLimbs
+                                                            : c.bval + (threadIdx.x - tcount) * kLimbs;
+      myidx = threadIdx.x < (unsigned)tcount ? c.tidx[threadIdx.x] : c.bidx[threadIdx.x - tcount];
+#pragma unroll
+      for (int i = 0; i < kLimbs; ++i) mine[i] = src[i];
+      const int myblk = cand_blk ? cand_blk[myidx] : myidx;
+      for (int o = 0; o < tot; ++o) {
+        if (o == (int)threadIdx.x) continue;
+        const uint32_t* ov = o < tcount ? c.tval + o * kLimbs : c.bval + (o - tcount) * kLimbs;
+        const int oidx = o < tcount ? c.tidx[o] : c.bidx[o - tcount];
+        const int oblk = cand_blk ? cand_blk[oidx] : oidx;
+        const int cmpv = exact_cmp(ov, mine);
+        if (cmpv > 0 || (cmpv == 0 && oblk < myblk)) ++rank;
+      }
+    }
+    __syncthreads();
+    if (myidx >= 0 && rank < r) {
+#pragma unroll
+      for (int i = 0; i < kLimbs; ++i) c.tval[rank * kLimbs + i] = mine[i];
+      c.tidx[rank] = myidx;
+    }
+    tcount = min(r, tot);
+    __syncthreads();
+  }
+  for (int i = threadIdx.x; i < nU; i += blockDim.x) cls[U[i]] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < tcount; i += blockDim.x) cls[c.tidx[i]] = 1;
+  __syncthreads();
+}
+
+// cls[i] = 1 for the k best of the n candidates (exact order), 0 otherwise.
+__device__ void select_best(SelCtx& c, const float2* se, int n, int k, const int* cand_blk,
+                            uint8_t* cls, int* U) {
+  if (k >= n || k <= 0) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) cls[i] = k > 0 ? 1 : 0;
+    __syncthreads();
+    return;
+  }
+  const uint32_t tkey = kth_largest_key(se, n, k, c.hist, c.scal);
+  const float tval = key_float(tkey);
+  float em = 0.f;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) em = fmaxf(em, se[i].y);
+  em = block_max(em, c.fscal);
+  const float hi_t = __fadd_ru(tval, em), lo_t = __fsub_rd(tval, em);
+  if (threadIdx.x == 0) { c.scal[2] = 0; c.scal[3] = 0; }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const float2 v = se[i];
+    const float lo = __fsub_rd(v.x, v.y), hi = __fadd_ru(v.x, v.y);
+    uint8_t cl;
+    if (lo > hi_t) {
+      cl = 1;
+      atomicAdd(&c.scal[3], 1);
+    } else if (hi < lo_t) {
+      cl = 0;
+    } else {
+      cl = 2;
+      U[atomicAdd(&c.scal[2], 1)] = i;
+    }
+    cls[i] = cl;
+  }
+  __syncthreads();
+  const int nU = c.scal[2], nin = c.scal[3];
+  __syncthreads();
+  const int r = k - nin;
+  if (r <= 0 || r >= nU) {
+    for (int i = threadIdx.x; i < nU; i += blockDim.x) cls[U[i]] = r > 0 ? 1 : 0;
+    __syncthreads();
+    return;
+  }
+  refine_top_r(c, U, nU, r, cand_blk, cls);
+}
+
+// ---------------------------------------------------------------- shared memory layout
+struct SelLayout {
+  size_t se, cls, U, cblk, qf, qb, qn, lacc, tmp, bval, bidx, tval, tidx, hist, scal, fscal, red, total;
+};
+
+__host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+__host__ __device__ inline SelLayout sel_layout(int ncap) {
+  SelLayout L;
+  size_t o = 0;
+  L.se = o; o = align16(o + sizeof(float2) * ncap);
+  L.cls = o; o = align16(o + ncap);
+  L.U = o; o = align16(o + sizeof(int) * ncap);
+  L.cblk = o; o = align16(o + sizeof(int) * ncap);
+  L.qf = o; o = align16(o + sizeof(float) * kMaxN * kQStride);
+  L.qb = o; o = align16(o + sizeof(uint16_t) * kMaxN * kD);
+  L.qn = o; o = align16(o + sizeof(float) * kMaxN);
+  L.lacc = o; o = align16(o + sizeof(unsigned long long) * kSelWarps * kLimbs);
+  L.tmp = o; o = align16(o + sizeof(uint32_t) * kSelWarps * kLimbs);
+  L.bval = o; o = align16(o + sizeof(uint32_t) * kSelWarps * kLimbs);
+  L.bidx = o; o = align16(o + sizeof(int) * kSelWarps);
+  L.tval = o; o = align16(o + sizeof(uint32_t) * kMaxR * kLimbs);
+  L.tidx = o; o = align16(o + sizeof(int) * kMaxR);
+  L.hist = o; o = align16(o + sizeof(uint32_t) * 256);
+  L.scal = o; o = align16(o + sizeof(int) * 8);
+  L.fscal = o; o = align16(o + sizeof(float) * kSelWarps);
+  L.red = o; o = align16(o + sizeof(int) * 32);
+  L.total = o;
+  return L;
+}
+
+__device__ SelCtx make_ctx(char* sm, const SelLayout& L, const Shape& s, const uint16_t* k_hbm,
+                           const uint16_t* q_la, int head, int ctx) {
+  SelCtx c;
+  c.b = head / s.Hkv;
+  c.h = head - c.b * s.Hkv;
+  c.k = k_hbm + (long long)head * s.nb_max * kBS * kD;
+  c.q_la = q_la;
+  c.ctx = ctx;
+  c.G = s.Hq / s.Hkv;
+  c.N = s.n_la * c.G;
+  c.n_la = s.n_la;
+  c.Hq = s.Hq;
+  c.qf = reinterpret_cast<float*>(sm + L.qf);
+  c.qb = reinterpret_cast<uint16_t*>(sm + L.qb);
+  c.qn = reinterpret_cast<float*>(sm + L.qn);
+  c.lacc = reinterpret_cast<unsigned long long*>(sm + L.lacc);
+  c.tmp = reinterpret_cast<uint32_t*>(sm + L.tmp);
+  c.bval = reinterpret_cast<uint32_t*>(sm + L.bval);
+  c.bidx = reinterpret_cast<int*>(sm + L.bidx);
+  c.tval = reinterpret_cast<uint32_t*>(sm + L.tval);
+  c.tidx = reinterpret_cast<int*>(sm + L.tidx);
+  c.hist = reinterpret_cast<uint32_t*>(sm + L.hist);
+  c.scal = reinterpret_cast<int*>(sm + L.scal);
+  c.fscal = reinterpret_cast<float*>(sm + L.fscal);
+  return c;
+}
+
+// ---------------------------------------------------------------- a2 kernel
+__global__ void __launch_bounds__(kSelThreads, 1)
+topk_select_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __restrict__ k_hbm,
+                   const uint16_t* __restrict__ q_la, const int* __restrict__ ctx_len,
+                   int* __restrict__ sel, int* __restrict__ nsel) {
+  extern __shared__ __align__(16) char sm[];
+  const SelLayout L = sel_layout(s.nb_max);
+  const int head = blockIdx.x;
+  const int b = head / s.Hkv;
+  const int ctx = ctx_len[b];
+  const int nb = clamp_nb(ctx, s.nb_max);
+  int* out = sel + (long long)head * s.Kb;
+  if (nb <= s.Kb) {
+    for (int i = threadIdx.x; i < s.Kb; i += blockDim.x) out[i] = i < nb ? i : -1;
+    if (threadIdx.x == 0) nsel[head] = nb;
+    return;
+  }
+  SelCtx c = make_ctx(sm, L, s, k_hbm, q_la, head, ctx);
+  float2* se = reinterpret_cast<float2*>(sm + L.se);
+  uint8_t* cls = reinterpret_cast<uint8_t*>(sm + L.cls);
+  int* U = reinterpret_cast<int*>(sm + L.U);
+  int* red = reinterpret_cast<int*>(sm + L.red);
+  const float2* src = scores + (long long)head * s.nb_max;
+  for (int i = threadIdx.x; i < nb; i += blockDim.x) se[i] = src[i];
+  __syncthreads();
+  select_best(c, se, nb, s.Kb, nullptr, cls, U);
+  // compaction in ascending block order
+  const int per = (nb + kSelThreads - 1) / kSelThreads;
+  const int i0 = threadIdx.x * per, i1 = min(nb, i0 + per);
+  int cnt = 0;
+  for (int i = i0; i < i1; ++i) cnt += cls[i] == 1;
+  int total = 0;
+  int pos = block_excl_scan(cnt, red, red + 31);
+  total = red[31];
+  for (int i = i0; i < i1; ++i)
+    if (cls[i] == 1) {
+      if (pos < s.Kb) out[pos] = i;
+      ++pos;
+    }
+  for (int i = total + threadIdx.x; i < s.Kb; i += blockDim.x) out[i] = -1;
+  if (threadIdx.x == 0) nsel[head] = total < s.Kb ? total : s.Kb;
+}
+
+// ---------------------------------------------------------------- a3 kernel
+__global__ void __launch_bounds__(kSelThreads, 1)
+fetch_diff_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __restrict__ k_hbm,
+                  const uint16_t* __restrict__ q_la, const int* __restrict__ ctx_len,
+                  const int* __restrict__ sel, const int* __restrict__ nsel,
+                  const int* __restrict__ blk2slot, int cap, int* __restrict__ fetch,
+                  int* __restrict__ nfetch) {
+  extern __shared__ __align__(16) char sm[];
+  const SelLayout L = sel_layout(s.Kb);
+  const int head = blockIdx.x;
+  const int b = head / s.Hkv;
+  const int ctx = ctx_len[b];
+  SelCtx c = make_ctx(sm, L, s, k_hbm, q_la, head, ctx);
+  float2* se = reinterpret_cast<float2*>(sm + L.se);
+  uint8_t* cls = reinterpret_cast<uint8_t*>(sm + L.cls);
+  int* U = reinterpret_cast<int*>(sm + L.U);
+  int* cblk = reinterpret_cast<int*>(sm + L.cblk);
+  int* red = reinterpret_cast<int*>(sm + L.red);
+  int ns = nsel[head];
+  ns = ns < 0 ? 0 : (ns > s.Kb ? s.Kb : ns);
+  const int* S = sel + (long long)head * s.Kb;
+  const int* b2s = blk2slot + (long long)head * s.nb_max;
+  // missing blocks of S, in S order (ascending); one entry per thread (ns <= Kb <= 512)
+  int x = -1, miss = 0;
+  if ((int)threadIdx.x < ns) {
+    x = S[threadIdx.x];
+    miss = (x >= 0 && x < s.nb_max && b2s[x] < 0) ? 1 : 0;
+  }
+  const int pos = block_excl_scan(miss, red, red + 31);
+  const int nM = red[31];
+  if (miss) {
+    cblk[pos] = x;
+    se[pos] = scores[(long long)head * s.nb_max + x];
+  }
+  __syncthreads();
+  const int C = cap < nM ? cap : nM;
+  select_best(c, se, nM, C, cblk, cls, U);
+  int* out = fetch + (long long)head * s.Kb;
+  const int take = ((int)threadIdx.x < nM && cls[threadIdx.x] == 1) ? 1 : 0;
+  const int opos = block_excl_scan(take, red, red + 31);
+  const int total = red[31];
+  if (take && opos < s.Kb) out[opos] = cblk[threadIdx.x];
+  for (int i = total + threadIdx.x; i < s.Kb; i += blockDim.x) out[i] = -1;
+  if (threadIdx.x == 0) nfetch[head] = total < s.Kb ? total : s.Kb;
+}
+
+// ---------------------------------------------------------------- launchers
+size_t topk_smem_bytes(const Shape& s) { return sel_layout(s.nb_max).total; }
+size_t diff_smem_bytes(const Shape& s) { return sel_layout(s.Kb).total; }
+
+cudaError_t launch_topk_select(const Shape& s, const float2* scores, const uint16_t* k,
+                               const uint16_t* q_la, const int* ctx, int* sel, int* nsel,
+                               cudaStream_t stream) {
+  const size_t smem = topk_smem_bytes(s);
+  cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  topk_select_kernel<<<s.B * s.Hkv, kSelThreads, smem, stream>>>(s, scores, k, q_la, ctx, sel, nsel);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fetch_diff(const Shape& s, const float2* scores, const uint16_t* k,
+                              const uint16_t* q_la, const int* ctx, const int* sel,
+                              const int* nsel, const int* blk2slot, int cap, int* fetch,
+                              int* nfetch, cudaStream_t stream) {
+  const size_t smem = diff_smem_bytes(s);
+  cudaError_t e = cudaFuncSetAttribute(fetch_diff_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  fetch_diff_kernel<<<s.B * s.Hkv, kSelThreads, smem, stream>>>(s, scores, k, q_la, ctx, sel, nsel,
+                                                               blk2slot, cap, fetch, nfetch);
+  return cudaGetLastError();
+}
+
+}  // namespace oasis

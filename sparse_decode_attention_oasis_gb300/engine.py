@@ -1,0 +1,145 @@
+"""Device state of a decode workload and the per-layer call sequence.
+
+PyTorch is used only to own memory (HBM tensors, page-locked host tier) and
+streams; every step of the path runs in liboasis.so through :mod:`binding`.
+
+Layout in HBM (one physical layer buffer per entry of the first axis):
+  K        bf16 [L][B][Hkv][nb_max*16][128]   keys kept in HBM for scoring
+  k_pool   bf16 [L][B][Hkv][P][16][128]       HBM slots (bounded working set)
+  v_pool   bf16 [L][B][Hkv][P][16][128]
+  blk2slot int32 [L][B][Hkv][nb_max]          slot of a resident block or -1
+  slot2blk int32 [L][B][Hkv][P]               block held by a slot or -1
+  last_used int32 [L][B][Hkv][P]              LRU clock
+Host tier (page-locked, device-mapped): bf16 [L][B][Hkv][nb_max][2][16][128].
+Per-layer scratch is shared by all layers of a step (scores, sel, fetch, ...).
+When the physical layer count is smaller than the logical one, layer l uses
+buffer l mod L_phys.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import binding as B
+from . import synthetic as syn
+
+
+def _bf16_from_bits(bits: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+class LayerScratch:
+    """Buffers one layer-step writes: scores, selection, fetch list, output."""
+
+    def __init__(self, shape: B.Shape, device):
+        s = shape
+        self.shape = s
+        dev = device
+        self.scores = torch.empty((s.B, s.Hkv, s.nb_max, 2), dtype=torch.float32, device=dev)
+        self.sel = torch.empty((s.B, s.Hkv, s.Kb), dtype=torch.int32, device=dev)
+        self.nsel = torch.empty((s.B, s.Hkv), dtype=torch.int32, device=dev)
+        self.fetch = torch.empty((s.B, s.Hkv, s.Kb), dtype=torch.int32, device=dev)
+        self.nfetch = torch.empty((s.B, s.Hkv), dtype=torch.int32, device=dev)
+        self.ws_bytes = B.oasis_attn_workspace_bytes(s)
+        self.ws = torch.empty(max(16, self.ws_bytes), dtype=torch.uint8, device=dev)
+        self.out = torch.empty((s.B, s.Hq, 128), dtype=torch.float32, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+
+class DecodeState:
+    def __init__(self, w: syn.Workload, device="cuda", l_phys: Optional[int] = None,
+                 l_host: Optional[int] = None, pin_host: bool = True):
+        self.w = w
+        self.device = torch.device(device)
+        self.L_phys = l_phys or w.L
+        self.L_host = l_host or self.L_phys
+        self.shape = B.Shape.from_workload(w)
+        s = self.shape
+        dev = self.device
+        Lp = self.L_phys
+        self.K = torch.zeros((Lp, s.B, s.Hkv, s.nb_max * 16, 128), dtype=torch.bfloat16, device=dev)
+        self.k_pool = torch.zeros((Lp, s.B, s.Hkv, s.P, 16, 128), dtype=torch.bfloat16, device=dev)
+        self.v_pool = torch.zeros_like(self.k_pool)
+        self.blk2slot = torch.full((Lp, s.B, s.Hkv, s.nb_max), -1, dtype=torch.int32, device=dev)
+        self.slot2blk = torch.full((Lp, s.B, s.Hkv, s.P), -1, dtype=torch.int32, device=dev)
+        self.last_used = torch.full((Lp, s.B, s.Hkv, s.P), -1, dtype=torch.int32, device=dev)
+        self.host = torch.zeros((self.L_host, s.B, s.Hkv, s.nb_max, 2, 16, 128), dtype=torch.bfloat16,
+                                pin_memory=pin_host)
+        self.ctx = torch.tensor(w.ctx, dtype=torch.int32, device=dev)
+        self.scratch = LayerScratch(s, dev)
+        self.scale = 1.0 / math.sqrt(w.d)
+
+    # ---------------------------------------------------------------- filling
+    def fill_layer_numpy(self, layer: int, K_bits: np.ndarray, V_bits: np.ndarray,
+                         blk2slot: np.ndarray, slot2blk: np.ndarray, last_used: np.ndarray):
+        """Load one layer from host arrays (bf16 bits [B][Hkv][T_max][d] and int32 tables)."""
+        lp, lh = layer % self.L_phys, layer % self.L_host
+        w = self.w
+        self.K[lp].copy_(_bf16_from_bits(K_bits, self.device))
+        host = syn.host_tier_from_kv(w, K_bits, V_bits)
+        self.host[lh].copy_(torch.from_numpy(host.view(np.int16)).view(torch.bfloat16))
+        self.blk2slot[lp].copy_(torch.from_numpy(blk2slot))
+        self.slot2blk[lp].copy_(torch.from_numpy(slot2blk))
+        self.last_used[lp].copy_(torch.from_numpy(last_used))
+        kp, vp = syn.pools_from_tables(w, host, slot2blk)
+        self.k_pool[lp].copy_(_bf16_from_bits(kp, self.device))
+        self.v_pool[lp].copy_(_bf16_from_bits(vp, self.device))
+
+    def fill_layer_synthetic(self, layer: int):
+        """Generate one layer on the device with the counter-based generator."""
+        lp, lh = layer % self.L_phys, layer % self.L_host
+        w = self.w
+        for b in range(w.B):
+            for h in range(w.Hkv):
+                Kh, Vh = syn.head_kv_torch(w, layer, b, h, self.device)
+                self.K[lp, b, h].copy_(Kh)
+                kv = torch.stack([Kh.view(w.nb_max, 16, 128), Vh.view(w.nb_max, 16, 128)], dim=1)
+                self.host[lh, b, h].copy_(kv, non_blocking=False)
+        b2s, s2b, lu = syn.initial_tables(w, layer)
+        self.blk2slot[lp].copy_(torch.from_numpy(b2s))
+        self.slot2blk[lp].copy_(torch.from_numpy(s2b))
+        self.last_used[lp].copy_(torch.from_numpy(lu))
+        # pools hold the initial residents
+        s2b_t = torch.from_numpy(s2b).to(self.device).long()
+        Kv = self.K[lp].view(w.B, w.Hkv, w.nb_max, 16, 128)
+        idx = s2b_t.clamp(min=0)
+        gathered = torch.gather(Kv, 2, idx[..., None, None].expand(-1, -1, -1, 16, 128))
+        self.k_pool[lp].copy_(gathered * (s2b_t >= 0)[..., None, None])
+        hostv = self.host[lh][:, :, :, 1].to(self.device)
+        gv = torch.gather(hostv, 2, idx[..., None, None].expand(-1, -1, -1, 16, 128))
+        self.v_pool[lp].copy_(gv * (s2b_t >= 0)[..., None, None])
+
+    # ---------------------------------------------------------------- one layer-step
+    def layer_step(self, layer: int, q_la: torch.Tensor, q: torch.Tensor, step: int,
+                   stream=None, gather_stream=None, scratch: Optional[LayerScratch] = None,
+                   ev_pool=None):
+        """Run a1..a5 for one layer: score, top-K, capped diff, gather, attention.
+
+        q_la: bf16 [B][n_la][Hq][d], q: bf16 [B][Hq][d] (device).  Returns the
+        scratch holding the outputs.  With ``gather_stream`` the gather runs on
+        that stream and the attention waits for it.
+        """
+        s = self.shape
+        sc = scratch or self.scratch
+        lp, lh = layer % self.L_phys, layer % self.L_host
+        st = stream or torch.cuda.current_stream(self.device)
+        K = self.K[lp]
+        B.oasis_score_blocks(s, K, self.ctx, q_la, sc.scores, st)
+        B.oasis_topk_select(s, sc.scores, K, q_la, self.ctx, sc.sel, sc.nsel, st)
+        B.oasis_fetch_diff_capped(s, sc.scores, K, q_la, self.ctx, sc.sel, sc.nsel,
+                                  self.blk2slot[lp], self.w.C, sc.fetch, sc.nfetch, st)
+        gs = gather_stream or st
+        if gs is not st:
+            gs.wait_stream(st)
+        B.oasis_gather_h2d(s, self.host[lh], sc.sel, sc.nsel, sc.fetch, sc.nfetch, self.blk2slot[lp],
+                           self.slot2blk[lp], self.last_used[lp], step, self.k_pool[lp],
+                           self.v_pool[lp], sc.err, gs)
+        if gs is not st:
+            st.wait_stream(gs)
+        B.oasis_sparse_decode_attn(s, q, self.k_pool[lp], self.v_pool[lp], sc.sel, sc.nsel,
+                                   self.blk2slot[lp], self.ctx, self.scale, sc.ws, sc.ws_bytes,
+                                   sc.out, st)
+        return sc

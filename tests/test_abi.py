@@ -1,0 +1,75 @@
+"""The C-ABI library builds, loads without a GPU and exports every declared call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_decode_attention_oasis_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "oasis.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"OASIS_API\s+[\w\s\*]+?\b(oasis_\w+)\s*\(", text)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def test_header_declares_the_five_calls():
+    names = declared_functions()
+    for n in ("oasis_score_blocks", "oasis_topk_select", "oasis_fetch_diff_capped",
+              "oasis_gather_h2d", "oasis_sparse_decode_attn"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(binding.LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(raw, n), n
+    assert binding.oasis_version().startswith("oasis-gb300")
+
+
+def test_binding_exposes_the_same_names():
+    for n in declared_functions():
+        assert hasattr(binding, n), n
+
+
+def _shape(**kw):
+    base = dict(B=2, Hq=32, Hkv=8, nb_max=256, n_la=4, Kb=32, P=32)
+    base.update(kw)
+    return binding.Shape.of(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Hq=30), 1), (dict(d=64), 4), (dict(bs=32), 4), (dict(Kb=300, P=300), 4),
+    (dict(P=16), 4), (dict(nb_max=9000), 4), (dict(n_la=9), 4), (dict(Hq=24, Hkv=8), 4),
+])
+def test_shape_validation_rejects_before_launch(lib, kw, status):
+    s = _shape(**kw)
+    st = lib.oasis_score_blocks(ctypes.byref(s), 16, 16, 16, 16, None)
+    assert st == status
+    assert lib.oasis_last_error()
+
+
+def test_null_and_misaligned_pointers_are_invalid(lib):
+    s = _shape()
+    assert lib.oasis_score_blocks(ctypes.byref(s), None, 16, 16, 16, None) == 1
+    assert lib.oasis_score_blocks(ctypes.byref(s), 18, 16, 16, 16, None) == 1
+    assert lib.oasis_fetch_diff_capped(ctypes.byref(s), 16, 16, 16, 16, 16, 16, 16, 33, 16, 16, None) == 1
+    assert lib.oasis_sparse_decode_attn(ctypes.byref(s), 16, 16, 16, 16, 16, 16, 16, 0.1, 16, 0, 16, None) == 1
+    with pytest.raises(binding.OasisError):
+        binding.oasis_score_blocks(s, None, 16, 16, 16, stream=0)
+
+
+def test_workspace_size_formula(lib):
+    s = _shape()
+    # 2 requests * 8 KV heads * 2 splits * 4 query heads * (128 + 2) floats
+    assert binding.oasis_attn_workspace_bytes(s) == 2 * 8 * 2 * 4 * 130 * 4
+    assert binding.oasis_attn_workspace_bytes(_shape(d=64)) == 0

@@ -1,0 +1,197 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Bar: selected blocks, fetch lists, block tables and pool contents bit-exact;
+block scores inside their certified interval; attention outputs within
+abs 2e-3 or rel 1e-2 per element (bf16 inputs, fp32 accumulation).
+"""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import oasis_ref as ref
+from sparse_decode_attention_oasis_gb300 import synthetic as syn
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 2e-3, 1e-2
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_decode_attention_oasis_gb300 import build
+
+    build.build()
+
+
+def _dev_bits(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def _check_out(got, want, what=""):
+    err = np.abs(got - want)
+    ok = (err <= ATOL) | (err <= RTOL * np.abs(want))
+    assert ok.all(), f"{what}: {int((~ok).sum())} elements out of tolerance, max abs {err.max():.3e}"
+    return float(err.max())
+
+
+class Case:
+    """One layer of a workload held both on the GPU and in oracle arrays."""
+
+    def __init__(self, w, K=None, V=None, tables=None):
+        from sparse_decode_attention_oasis_gb300.engine import DecodeState
+
+        self.w = w
+        if K is None:
+            K, V = syn.layer_kv(w, 0)
+        self.K, self.V = K, V
+        self.host = syn.host_tier_from_kv(w, K, V)
+        if tables is None:
+            tables = syn.initial_tables(w, 0)
+        self.b2s, self.s2b, self.lu = [np.array(t) for t in tables]
+        self.kp, self.vp = syn.pools_from_tables(w, self.host, self.s2b)
+        self.st = DecodeState(w, l_phys=1)
+        self.st.fill_layer_numpy(0, K, V, self.b2s, self.s2b, self.lu)
+
+    def step(self, step, q=None, qla=None, C=None):
+        w = self.w
+        if q is None:
+            q, qla = syn.layer_queries(w, 0, step)
+        if C is not None:
+            w.C = C
+        r = ref.layer_step(self.K, qla, q, w.ctx, self.host, self.kp, self.vp, self.b2s, self.s2b,
+                           self.lu, w.Kb, w.C, step, bs=w.bs)
+        sc = self.st.layer_step(0, _dev_bits(qla), _dev_bits(q), step)
+        torch.cuda.synchronize()
+        self.compare(r, sc)
+        return r, sc
+
+    def compare(self, r, sc):
+        w = self.w
+        scores = sc.scores.cpu().numpy()
+        sel = sc.sel.cpu().numpy()
+        nsel = sc.nsel.cpu().numpy()
+        fetch = sc.fetch.cpu().numpy()
+        nfetch = sc.nfetch.cpu().numpy()
+        assert int(sc.err.cpu()[0]) == 0
+        for (b, h), S in r["S"].items():
+            nb = w.nb(b)
+            s_exact, _ = r["score"][(b, h)]
+            if nb > w.Kb:  # scores are only needed (and written) when there is a choice
+                approx = scores[b, h, :nb, 0].astype(np.float64)
+                bound = scores[b, h, :nb, 1].astype(np.float64)
+                assert (np.abs(approx - s_exact) <= bound).all(), f"score outside bound at {(b, h)}"
+                assert (bound < 1e-2 * (1 + np.abs(s_exact))).all()
+            assert nsel[b, h] == len(S)
+            assert sel[b, h, :len(S)].tolist() == S, f"sel mismatch at {(b, h)}"
+            assert (sel[b, h, len(S):] == -1).all()
+            F = r["F"][(b, h)]
+            assert nfetch[b, h] == len(F)
+            assert fetch[b, h, :len(F)].tolist() == F, f"fetch mismatch at {(b, h)}"
+        lp = 0
+        np.testing.assert_array_equal(self.st.blk2slot[lp].cpu().numpy(), self.b2s)
+        np.testing.assert_array_equal(self.st.slot2blk[lp].cpu().numpy(), self.s2b)
+        np.testing.assert_array_equal(self.st.last_used[lp].cpu().numpy(), self.lu)
+        kpool = self.st.k_pool[lp].cpu().view(torch.int16).numpy().view(np.uint16)
+        vpool = self.st.v_pool[lp].cpu().view(torch.int16).numpy().view(np.uint16)
+        occupied = self.s2b >= 0
+        np.testing.assert_array_equal(kpool[occupied], self.kp[occupied])
+        np.testing.assert_array_equal(vpool[occupied], self.vp[occupied])
+        _check_out(sc.out.cpu().numpy().astype(np.float64), r["out"], "attention")
+
+
+def test_tiny_workload_three_steps():
+    w = syn.tiny()
+    c = Case(w)
+    for step in range(3):
+        c.step(step)
+
+
+def test_ragged_contexts_partial_blocks():
+    w = syn.Workload("ragged", L=1, B=3, Hq=32, Hkv=8, ctx=[4096, 1000, 17], Kb=32, C=4, n_hot=16)
+    c = Case(w)
+    for step in range(2):
+        c.step(step)
+
+
+@pytest.mark.parametrize("Hq,n_la", [(64, 4), (8, 4), (16, 3)])
+def test_gqa_groups(Hq, n_la):
+    w = syn.Workload("gqa", L=1, B=2, Hq=Hq, Hkv=8, ctx=[2048, 1531], Kb=32, C=6, n_hot=16, n_la=n_la)
+    c = Case(w)
+    c.step(0)
+    c.step(1)
+
+
+def test_budget_covers_context_and_fetch_all_is_dense():
+    w = syn.Workload("dense", L=1, B=2, Hq=32, Hkv=8, ctx=[500, 77], Kb=32, C=32, n_hot=4)
+    blank = tuple(np.full_like(t, -1) for t in syn.initial_tables(w, 0))
+    c = Case(w, tables=blank)
+    r, sc = c.step(0)
+    out = sc.out.cpu().numpy().astype(np.float64)
+    q, _ = syn.layer_queries(w, 0, 0)
+    for b in range(w.B):
+        for hq in range(w.Hq):
+            h = hq // w.G
+            k = ref.bf16_to_f64(c.K[b, h, :w.ctx[b]])
+            v = ref.bf16_to_f64(c.V[b, h, :w.ctx[b]])
+            lg = k @ ref.bf16_to_f64(q[b, hq]) / math.sqrt(w.d)
+            p = np.exp(lg - lg.max())
+            _check_out(out[b, hq], p @ v / p.sum(), "dense")
+
+
+def test_cap_zero_empty_resident_set():
+    w = syn.Workload("cap0", L=1, B=1, Hq=32, Hkv=8, ctx=[3000], Kb=32, C=0, n_hot=8)
+    blank = tuple(np.full_like(t, -1) for t in syn.initial_tables(w, 0))
+    c = Case(w, tables=blank)
+    r, sc = c.step(0)
+    assert (c.st.blk2slot[0].cpu().numpy() == -1).all()
+    assert (sc.out.cpu().numpy() == 0).all()
+
+
+def test_duplicate_blocks_force_exact_ties():
+    """48 identical top blocks straddle the rank-32 boundary: ties go to the lower index."""
+    w = syn.Workload("ties", L=1, B=1, Hq=32, Hkv=8, ctx=[2048], Kb=32, C=8, n_hot=0)
+    K, V = syn.layer_kv(w, 0)
+    Kf = syn.bf16_bits_to_f32(K) * np.float32(1.0 / 64)     # power-of-two scaling is exact
+    for h in range(w.Hkv):
+        u = syn.unit_dir(w, 0, 0, h)
+        Kf[0, h, 40 * 16:88 * 16] = 3.0 * u[None, :]
+    K = syn.f32_to_bf16_bits(Kf)
+    c = Case(w, K=K, V=V)
+    r, _ = c.step(0)
+    for h in range(w.Hkv):
+        assert r["S"][(0, h)] == list(range(40, 72))
+    c.step(1)
+
+
+def test_all_zero_keys():
+    w = syn.Workload("zeros", L=1, B=1, Hq=32, Hkv=8, ctx=[1024], Kb=32, C=4, n_hot=0)
+    K, V = syn.layer_kv(w, 0)
+    K[:] = 0
+    c = Case(w, K=K, V=V)
+    r, _ = c.step(0)
+    assert r["S"][(0, 0)] == list(range(32))
+
+
+def test_difference_below_fp32_resolution_is_resolved_exactly():
+    """Two blocks whose dots differ by 2^-24 of their value: fp32 ties them, exact does not."""
+    w = syn.Workload("ulp", L=1, B=1, Hq=8, Hkv=8, ctx=[64 * 16], Kb=1, C=1, n_hot=0, n_la=1)
+    K = np.zeros((1, 8, w.T_max, w.d), np.uint16)
+    V = syn.f32_to_bf16_bits(np.random.default_rng(0).standard_normal((1, 8, w.T_max, w.d)).astype(np.float32))
+    one = syn.f32_to_bf16_bits(np.float32(1.0))
+    for h in range(8):
+        K[0, h, 3 * 16, 0] = one                 # block 3: q.k = 1
+        K[0, h, 9 * 16 + 4, 0] = one             # block 9: q.k = 1 + 2^-24
+        K[0, h, 9 * 16 + 4, 1] = one
+    qla = np.zeros((1, 1, 8, w.d), np.float32)
+    qla[..., 0] = 1.0
+    qla[..., 1] = 2.0 ** -24
+    q = np.ones((1, 8, w.d), np.float32)
+    c = Case(w, K=K, V=V)
+    r, sc = c.step(0, q=syn.f32_to_bf16_bits(q), qla=syn.f32_to_bf16_bits(qla))
+    for h in range(8):
+        assert r["S"][(0, h)] == [9]
