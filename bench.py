@@ -1,0 +1,445 @@
+#!/usr/bin/env python
+"""Benchmark of the lookahead sparse decode hot path on one GB300 (or N replicas).
+
+Workload: Qwen3-8B decode shape - 36 layers, batch 32, 32 query / 8 KV heads,
+head dim 128, bf16, context 32768 (2048 blocks of 16), budget 2048 tokens (128
+blocks), 4 lookahead queries, fetch cap 0.02 x budget = 2 blocks per KV head per
+step, 64 planted hot blocks per head, AR(1) query drift (rho 0.9).  Inputs are
+synthetic (seeded counter-based generator), resident in HBM / page-locked host
+memory before the timed region; the per-layer key cache (2 GiB) is far larger
+than L2, so no flush is needed between steps.
+
+One step = one decode step = all 36 layers x (score, top-K, capped diff, host
+gather, sparse attention) over the whole batch.  Metric: layer-steps/s (plus the
+achieved HBM GB/s of the path and of the dominant kernel, block scoring).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun every rank runs its own replica on its own GPU (independent
+requests, no data-path collective): weak scaling, value = all ranks' layer-steps
+over the max time.  ``--impl reference`` times the CPU oracle on the host cores
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse decode layer-steps/sec and achieved HBM GB/s (% of GB300 peak)"
+UNIT = "layer-steps/s"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "score_blocks_traffic.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=8)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="oasis", choices=["oasis", "reference"])
+    ap.add_argument("--layers", type=int, default=36, help="model layers (36 = Qwen3-8B)")
+    ap.add_argument("--batch", type=int, default=32)
+    ap.add_argument("--ctx", type=int, default=32768)
+    ap.add_argument("--host-layers", type=int, default=0,
+                    help="physical host-tier layers (0 = all layers if host memory allows)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-worker", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-heads", type=int, default=3)
+    return ap.parse_args()
+
+
+def workload(args):
+    from sparse_decode_attention_oasis_gb300 import synthetic as syn
+
+    return syn.qwen3_8b_decode(B=args.batch, L=args.layers, ctx=args.ctx)
+
+
+def workload_desc(w) -> str:
+    return (f"{w.name}: {w.L} layers, batch {w.B}, {w.Hq}/{w.Hkv} heads, d {w.d}, bf16, ctx {w.ctx[0]}, "
+            f"block {w.bs}, budget {w.Kb * w.bs} tokens ({w.Kb} blocks), {w.n_la} lookahead queries, "
+            f"fetch cap {w.C} blocks/head/step, {w.n_hot} planted hot blocks/head")
+
+
+# --------------------------------------------------------------------------- CPU oracle timing
+def cpu_sample(args, nheads: int, step: int = 0):
+    """Time the oracle's layer-step on `nheads` sampled (request, KV head) pairs of layer 0.
+
+    Returns seconds per head (the oracle as it stands, numpy float64/exact).
+    """
+    import numpy as np
+
+    from oracle import oasis_ref as ref
+    from sparse_decode_attention_oasis_gb300 import synthetic as syn
+
+    w = workload(args)
+    rng = np.random.default_rng(1234 + step)
+    picks = [(int(rng.integers(w.B)), int(rng.integers(w.Hkv))) for _ in range(nheads)]
+    G = w.G
+    total = 0.0
+    for (b, h) in picks:
+        Kh, Vh = syn.head_kv(w, 0, b, h)
+        qh, qlah = syn.head_queries(w, 0, b, h, step)
+        sub = syn.Workload("sub", L=1, B=1, Hq=G, Hkv=1, ctx=[w.ctx[b]], Kb=w.Kb, C=w.C, n_la=w.n_la,
+                           nb_max=w.nb_max)
+        K = Kh[None, None]
+        V = Vh[None, None]
+        host = syn.host_tier_from_kv(sub, K, V)
+        res = syn.initial_resident(w, 0, b, h)
+        b2s = np.full((1, 1, w.nb_max), -1, np.int32)
+        s2b = np.full((1, 1, w.P), -1, np.int32)
+        lu = np.full((1, 1, w.P), -1, np.int32)
+        for p, x in enumerate(res):
+            s2b[0, 0, p] = x
+            b2s[0, 0, x] = p
+        kp, vp = syn.pools_from_tables(sub, host, s2b)
+        q = qh[None]
+        qla = qlah[None]
+        t0 = time.perf_counter()
+        ref.layer_step(K, qla, q, [w.ctx[b]], host, kp, vp, b2s, s2b, lu, w.Kb, w.C, step)
+        total += time.perf_counter() - t0
+    return total / nheads
+
+
+def cpu_baseline(args, heads: int):
+    """Run the oracle sample in a fresh process (all host cores for its BLAS)."""
+    cores = os.cpu_count() or 1
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = str(cores)
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-worker", str(heads), "--layers", str(args.layers),
+           "--batch", str(args.batch), "--ctx", str(args.ctx)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError("cpu baseline worker failed:\n" + r.stderr[-2000:])
+    per_head = json.loads(r.stdout.strip().splitlines()[-1])["sec_per_head"]
+    w = workload(args)
+    layer_step_s = per_head * w.B * w.Hkv
+    return {"value": 1.0 / layer_step_s, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{heads} (request, KV head) pairs of layer 0 of the {w.name} workload, one full "
+                      f"layer-step each (exact scoring, top-K, capped diff, LRU slots, fp64 attention); "
+                      f"layer-step time = time per head x {w.B * w.Hkv} heads"}
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append(parts)
+        if not rows:
+            return None
+        idxs = sorted(set(r[0] for r in rows))
+        mine = [r for r in rows if r[0] == str(self.index)] if len(idxs) > 1 else rows
+        sm = [float(r[1]) for r in mine if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in mine if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in mine:
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(mine)}
+
+
+# --------------------------------------------------------------------------- helpers
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(world: int, layers: int, steps: int, max_ms: float) -> float:
+    """Whole-job layer-steps/s: every rank runs its own replica of the workload."""
+    return world * layers * steps / (max_ms / 1000.0)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    src = os.path.join(ROOT, "sparse_decode_attention_oasis_gb300", "csrc", "score.cu")
+    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+
+
+def score_traffic_per_launch():
+    """ncu dram bytes of one score launch (full workload), if captured for this kernel source."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    d = json.load(open(PROFILE_TRAFFIC))
+    if d.get("score_cu_sha256_16") != kernel_source_hash():
+        return None
+    return d.get("bytes_per_launch_full")
+
+
+def algorithmic_bytes(w):
+    """Algorithmic HBM bytes of one layer-step, split by kernel."""
+    H = w.B * w.Hkv
+    ctx_blocks = sum(w.nb(b) for b in range(w.B)) * w.Hkv
+    score = ctx_blocks * w.bs * w.d * 2 + w.B * w.n_la * w.Hq * w.d * 2 + ctx_blocks * 8
+    topk = ctx_blocks * 8 + H * (w.Kb + 1) * 4
+    attn = H * w.Kb * w.bs * w.d * 2 * 2 + w.B * w.Hq * w.d * (2 + 4)
+    gather_hbm = H * w.C * w.bs * w.d * 2 * 2
+    return {"score": score, "topk": topk, "attn": attn, "gather_hbm": gather_hbm,
+            "total": score + topk + attn + gather_hbm}
+
+
+# --------------------------------------------------------------------------- reference arm
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    w = workload(args)
+    per_step = []
+    for s in range(args.warmup + args.steps):
+        t = cpu_sample(args, 1, step=s)
+        if s >= args.warmup:
+            per_step.append(t)
+    sec_per_head = sum(per_step) / len(per_step)
+    value = 1.0 / (sec_per_head * w.B * w.Hkv)
+    cores = os.cpu_count() or 1
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * w.L / value, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_desc(w)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "one (request, KV head) pair of layer 0 per step, scaled to a "
+                                       f"full layer-step ({w.B * w.Hkv} heads)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+def host_layers_for(w, requested: int) -> int:
+    if requested:
+        return min(requested, w.L)
+    per_layer = w.B * w.Hkv * w.nb_max * 2 * w.bs * w.d * 2
+    avail = None
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                avail = int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    if avail is None:
+        return w.L
+    fit = int(0.6 * avail // per_layer)
+    return max(2, min(w.L, fit))
+
+
+def run_gpu(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    from sparse_decode_attention_oasis_gb300 import build as _build
+    from sparse_decode_attention_oasis_gb300 import synthetic as syn
+    from sparse_decode_attention_oasis_gb300.engine import DecodeState
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the path has no CPU fallback)")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if local_rank == 0:
+        _build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    w = workload(args)
+    L = w.L
+    l_host = host_layers_for(w, args.host_layers)
+    st = DecodeState(w, device=dev, l_phys=L, l_host=l_host)
+    t0 = time.time()
+    for layer in range(L):
+        lp, lh = layer, layer % l_host
+        for b in range(w.B):
+            Kr, Vr = syn.kv_request_torch(w, layer, b, dev)
+            st.K[lp, b].copy_(Kr)
+            if layer < l_host:
+                kv = torch.stack([Kr.view(w.Hkv, w.nb_max, 16, 128), Vr.view(w.Hkv, w.nb_max, 16, 128)], dim=2)
+                st.host[lh, b].copy_(kv.cpu())
+            vb = Vr.view(w.Hkv, w.nb_max, 16, 128)
+            b2s, s2b, lu = syn.initial_tables(w, layer) if b == 0 else (b2s, s2b, lu)
+            idx = torch.from_numpy(s2b[b]).to(dev).long()
+            st.k_pool[lp, b].copy_(Kr.view(w.Hkv, w.nb_max, 16, 128)[torch.arange(w.Hkv, device=dev)[:, None], idx])
+            st.v_pool[lp, b].copy_(vb[torch.arange(w.Hkv, device=dev)[:, None], idx])
+        st.blk2slot[lp].copy_(torch.from_numpy(b2s))
+        st.slot2blk[lp].copy_(torch.from_numpy(s2b))
+        st.last_used[lp].copy_(torch.from_numpy(lu))
+    torch.cuda.synchronize()
+    gen_s = time.time() - t0
+
+    nsteps = args.warmup + args.steps
+    qs = [syn.QueryStream(w, l) for l in range(L)]
+    q_host = torch.empty((nsteps, L, w.B, w.Hq, w.d), dtype=torch.bfloat16, pin_memory=True)
+    qla_host = torch.empty((nsteps, L, w.B, w.n_la, w.Hq, w.d), dtype=torch.bfloat16, pin_memory=True)
+    for s in range(nsteps):
+        for l in range(L):
+            qb, qlab = qs[l].next()
+            q_host[s, l].copy_(torch.from_numpy(qb.view(np.int16)).view(torch.bfloat16))
+            qla_host[s, l].copy_(torch.from_numpy(qlab.view(np.int16)).view(torch.bfloat16))
+    q_dev = q_host.to(dev)
+    qla_dev = qla_host.to(dev)
+
+    main = torch.cuda.current_stream(dev)
+    side = torch.cuda.Stream(dev)
+    out_dev = torch.empty((L, w.B, w.Hq, w.d), dtype=torch.float32, device=dev)
+
+    def step(s, timers=None, qla=None, q=None):
+        st.decode_step(s, qla if qla is not None else qla_dev[s], q if q is not None else q_dev[s],
+                       out_layers=out_dev, main=main, side=side, score_timers=timers)
+
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize()
+    errw = int(st.scratch.err.item()) | int(st.scratch2.err.item())
+
+    timers = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(L)]
+              for _ in range(args.steps)]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    ev0.record(main)
+    for k in range(args.steps):
+        step(args.warmup + k, timers[k])
+    ev1.record(main)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = reduce_max(ev0.elapsed_time(ev1), world, dev)
+    score_ms = [t[0].elapsed_time(t[1]) for per in timers for t in per]
+
+    # end to end: H2D of the step's queries, the C-ABI calls, D2H of the outputs
+    e2e = None
+    if not args.no_e2e:
+        out_host = torch.empty((L, w.B, w.Hq, w.d), dtype=torch.float32, pin_memory=True)
+        q_in = torch.empty_like(q_dev[0])
+        qla_in = torch.empty_like(qla_dev[0])
+        nrep = args.steps
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        t0 = time.perf_counter()
+        for k in range(nrep):
+            s = args.warmup + (k % args.steps)
+            q_in.copy_(q_host[s], non_blocking=True)
+            qla_in.copy_(qla_host[s], non_blocking=True)
+            step(s, qla=qla_in, q=q_in)
+            out_host.copy_(out_dev, non_blocking=True)
+            torch.cuda.current_stream(dev).synchronize()
+        e2e_s = reduce_max(time.perf_counter() - t0, world, dev)
+        bi = q_in.numel() * 2 + qla_in.numel() * 2
+        bo = out_host.numel() * 4
+        e2e = {"value": aggregate_value(world, L, nrep, 1000.0 * e2e_s), "unit": UNIT, "h2d_bytes_per_step": bi,
+               "d2h_bytes_per_step": bo}
+
+    if rank != 0:
+        return
+    ab = algorithmic_bytes(w)
+    peak, peak_kind = measured_peaks()
+    score_avg_ms = sum(score_ms) / len(score_ms)
+    achieved = ab["score"] / (score_avg_ms / 1000.0) / 1e9
+    value = aggregate_value(world, L, args.steps, ms)
+    path_gbs = ab["total"] * L * args.steps / (ms / 1000.0) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(w), "l2": "inputs larger than L2 (2 GiB of keys per layer)",
+                   "host_tier_layers": l_host, "host_tier_aliased": l_host < L,
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "path_hbm_gbs": path_gbs, "path_hbm_frac": path_gbs / peak,
+        "roofline": {"kernel": "score_blocks", "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": score_traffic_per_launch(), "bytes_per_launch": ab["score"],
+                     "avg_launch_ms": score_avg_ms},
+        "gpu_launches": 6 * L * args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+        "device_error_word": errw,
+        "setup_s": round(gen_s, 1),
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(args, args.cpu_heads)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.cpu_worker:
+        print(json.dumps({"sec_per_head": cpu_sample(args, args.cpu_worker)}), flush=True)
+        return
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_gpu(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

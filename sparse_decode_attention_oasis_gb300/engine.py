@@ -70,6 +70,7 @@ class DecodeState:
                                 pin_memory=pin_host)
         self.ctx = torch.tensor(w.ctx, dtype=torch.int32, device=dev)
         self.scratch = LayerScratch(s, dev)
+        self.scratch2 = None
         self.scale = 1.0 / math.sqrt(w.d)
 
     # ---------------------------------------------------------------- filling
@@ -143,3 +144,69 @@ class DecodeState:
                                    self.blk2slot[lp], self.ctx, self.scale, sc.ws, sc.ws_bytes,
                                    sc.out, st)
         return sc
+
+    # ---------------------------------------------------------------- one decode step
+    def _select(self, layer, q_la, step, sc, st, timers=None):
+        s = self.shape
+        lp = layer % self.L_phys
+        K = self.K[lp]
+        if timers is not None:
+            timers[0].record(st)
+        B.oasis_score_blocks(s, K, self.ctx, q_la, sc.scores, st)
+        if timers is not None:
+            timers[1].record(st)
+        B.oasis_topk_select(s, sc.scores, K, q_la, self.ctx, sc.sel, sc.nsel, st)
+        B.oasis_fetch_diff_capped(s, sc.scores, K, q_la, self.ctx, sc.sel, sc.nsel,
+                                  self.blk2slot[lp], self.w.C, sc.fetch, sc.nfetch, st)
+
+    def _gather(self, layer, step, sc, gs):
+        s = self.shape
+        lp, lh = layer % self.L_phys, layer % self.L_host
+        B.oasis_gather_h2d(s, self.host[lh], sc.sel, sc.nsel, sc.fetch, sc.nfetch, self.blk2slot[lp],
+                           self.slot2blk[lp], self.last_used[lp], step, self.k_pool[lp],
+                           self.v_pool[lp], sc.err, gs)
+
+    def _attend(self, layer, q, sc, st, out=None):
+        s = self.shape
+        lp = layer % self.L_phys
+        B.oasis_sparse_decode_attn(s, q, self.k_pool[lp], self.v_pool[lp], sc.sel, sc.nsel,
+                                   self.blk2slot[lp], self.ctx, self.scale, sc.ws, sc.ws_bytes,
+                                   sc.out if out is None else out, st)
+
+    def decode_step(self, step: int, q_la_layers, q_layers, out_layers=None, main=None, side=None,
+                    score_timers=None):
+        """All layers of one decode step, pipelined across layers.
+
+        Main stream: select(0); select(1); attn(0); select(2); attn(1); ...
+        Side stream: gather(l) as soon as select(l) is done, so the host-link copy
+        of layer l overlaps the HBM-bound scoring of layer l+1; attn(l) waits for
+        gather(l).  Two scratch sets alternate between consecutive layers.
+        q_la_layers[l], q_layers[l]: device tensors of layer l; out_layers[l]
+        (optional) receives the fp32 attention output of layer l.
+        """
+        L = self.w.L
+        main = main or torch.cuda.current_stream(self.device)
+        side = side or main
+        if self.scratch2 is None:
+            self.scratch2 = LayerScratch(self.shape, self.device)
+        scr = (self.scratch, self.scratch2)
+        events = [torch.cuda.Event() for _ in range(2)]
+
+        def launch_select_gather(l):
+            sc = scr[l % 2]
+            self._select(l, q_la_layers[l], step, sc, main,
+                         None if score_timers is None else score_timers[l])
+            if side is not main:
+                side.wait_stream(main)
+            self._gather(l, step, sc, side)
+            if side is not main:
+                events[l % 2].record(side)
+
+        launch_select_gather(0)
+        for l in range(L):
+            if l + 1 < L:
+                launch_select_gather(l + 1)
+            if side is not main:
+                main.wait_event(events[l % 2])
+            self._attend(l, q_layers[l], scr[l % 2], main,
+                         None if out_layers is None else out_layers[l])

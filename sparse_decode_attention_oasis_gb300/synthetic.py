@@ -415,3 +415,91 @@ def head_kv_torch(w: Workload, layer: int, b: int, h: int, device):
     K[: w.ctx[b]] = Kf.to(torch.bfloat16)
     V[: w.ctx[b]] = Vf.to(torch.bfloat16)
     return K, V
+
+
+# --------------------------------------------------------------------------
+# vectorised draws (same bits as the per-head functions above)
+# --------------------------------------------------------------------------
+def _chunk_keys_multi(seed: int, stream: int, layer: int, bs_, hs_):
+    k1 = np.array([chunk_key(seed, stream, layer, int(b), int(h))[0] for b, h in zip(bs_, hs_)], np.uint64)
+    k2 = np.array([mix32_int(int(k) ^ _K2_SALT) for k in k1], np.uint64)
+    return k1, k2
+
+
+def hash_normals_multi(seed: int, stream: int, layer: int, bs_, hs_, start: int, count: int) -> np.ndarray:
+    """[len(bs_)][count] float32 draws; row r equals hash_normals(..., bs_[r], hs_[r], start, count)."""
+    k1, k2 = _chunk_keys_multi(seed, stream, layer, bs_, hs_)
+    idx = np.arange(start, start + count, dtype=np.uint64)[None, :]
+    v = mix32_np(mix32_np(idx ^ k1[:, None]) ^ k2[:, None])
+    return NORMAL_TABLE[(v >> np.uint64(16)).astype(np.int64)]
+
+
+class QueryStream:
+    """Queries of one layer for decode steps 0, 1, 2, ... (AR(1) noise carried over).
+
+    ``next()`` returns (q bits [B][Hq][d], q_la bits [B][n_la][Hq][d]) and is
+    bit-identical to :func:`layer_queries` for the same step.
+    """
+
+    def __init__(self, w: Workload, layer: int):
+        self.w = w
+        self.layer = layer
+        self.step = 0
+        B, Hq, d, G = w.B, w.Hq, w.d, w.G
+        self.bb = np.repeat(np.arange(B), Hq)
+        self.hq = np.tile(np.arange(Hq), B)
+        u = np.stack([unit_dir(w, layer, b, h) for b in range(B) for h in range(w.Hkv)])
+        self.u = u.reshape(B, w.Hkv, 1, d).repeat(G, axis=2).reshape(B * Hq, d).astype(np.float64)
+        self.e = None
+
+    def next(self):
+        w = self.w
+        d = w.d
+        if self.e is None:
+            self.e = hash_normals_multi(w.seed, STREAM_QNOISE, self.layer, self.bb, self.hq, 0, d).astype(np.float64)
+        else:
+            a = math.sqrt(1.0 - w.rho * w.rho)
+            xi = hash_normals_multi(w.seed, STREAM_QNOISE, self.layer, self.bb, self.hq,
+                                    self.step * d, d).astype(np.float64)
+            self.e = w.rho * self.e + a * xi
+        qf = (2.0 * self.u + self.e).astype(np.float32)
+        la = hash_normals_multi(w.seed, STREAM_LANOISE, self.layer, self.bb, self.hq,
+                                self.step * w.n_la * d, w.n_la * d).astype(np.float64)
+        la = la.reshape(-1, w.n_la, d)
+        qla = (qf.astype(np.float64)[:, None, :] + w.la_sigma * la).astype(np.float32)
+        self.step += 1
+        q_bits = f32_to_bf16_bits(qf).reshape(w.B, w.Hq, d)
+        qla_bits = f32_to_bf16_bits(qla).reshape(w.B, w.Hq, w.n_la, d).transpose(0, 2, 1, 3)
+        return q_bits, np.ascontiguousarray(qla_bits)
+
+
+def kv_request_torch(w: Workload, layer: int, b: int, device):
+    """bf16 K, V [Hkv][T_max][d] of one request of one layer on ``device`` (same bits as head_kv)."""
+    import torch
+
+    H, n = w.Hkv, w.ctx[b] * w.d
+    keys = [chunk_key(w.seed, STREAM_K, layer, b, h) for h in range(H)]
+    vkeys = [chunk_key(w.seed, STREAM_V, layer, b, h) for h in range(H)]
+    idx = torch.arange(0, n, dtype=torch.int64, device=device)[None, :]
+    table = normal_table_torch(device)
+
+    def draw(ks):
+        k1 = torch.tensor([k[0] for k in ks], dtype=torch.int64, device=device)[:, None]
+        k2 = torch.tensor([k[1] for k in ks], dtype=torch.int64, device=device)[:, None]
+        v = _mix32_torch(_mix32_torch(idx ^ k1) ^ k2)
+        return table[v >> 16].view(H, w.ctx[b], w.d)
+
+    Kf = draw(keys)
+    Vf = draw(vkeys)
+    for h in range(H):
+        hot = hot_blocks(w, layer, b, h)
+        if len(hot):
+            shift = torch.from_numpy((np.float32(3.0) * unit_dir(w, layer, b, h)).astype(np.float32)).to(device)
+            tok = (hot[:, None] * w.bs + np.arange(w.bs)[None, :]).reshape(-1)
+            tok = torch.from_numpy(tok[tok < w.ctx[b]]).to(device)
+            Kf[h, tok] = Kf[h, tok] + shift[None, :]
+    K = torch.zeros((H, w.T_max, w.d), dtype=torch.bfloat16, device=device)
+    V = torch.zeros_like(K)
+    K[:, : w.ctx[b]] = Kf.to(torch.bfloat16)
+    V[:, : w.ctx[b]] = Vf.to(torch.bfloat16)
+    return K, V

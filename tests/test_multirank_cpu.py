@@ -1,0 +1,53 @@
+"""The N > 1 bench path on CPU: world-size-2 gloo ranks, max-over-ranks timing."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    import bench
+
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        local_ms = 100.0 + 50.0 * rank          # rank 1 is the slow one
+        dist.barrier()
+        m = bench.reduce_max(local_ms, world)
+        v = bench.aggregate_value(world, 36, 8, m)
+        q.put((rank, m, v))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_max_time():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, m, v in res:
+        assert m == 150.0
+        assert v == pytest.approx(2 * 36 * 8 / 0.150)
+
+
+def test_single_rank_is_identity():
+    import bench
+
+    assert bench.reduce_max(3.5, 1) == 3.5
+    assert bench.aggregate_value(1, 36, 10, 1000.0) == pytest.approx(360.0)
