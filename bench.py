@@ -295,8 +295,17 @@ def run_gpu(args, rank, world, local_rank):
     w = workload(args)
     L = w.L
     l_host = host_layers_for(w, args.host_layers)
-    st = DecodeState(w, device=dev, l_phys=L, l_host=l_host)
     t0 = time.time()
+    while True:
+        try:
+            st = DecodeState(w, device=dev, l_phys=L, l_host=l_host)
+            break
+        except RuntimeError:
+            if l_host <= 2:
+                raise
+            l_host = max(2, l_host // 2)
+            torch.cuda.empty_cache()
+    alloc_s = time.time() - t0
     for layer in range(L):
         lp, lh = layer, layer % l_host
         for b in range(w.B):
@@ -304,7 +313,7 @@ def run_gpu(args, rank, world, local_rank):
             st.K[lp, b].copy_(Kr)
             if layer < l_host:
                 kv = torch.stack([Kr.view(w.Hkv, w.nb_max, 16, 128), Vr.view(w.Hkv, w.nb_max, 16, 128)], dim=2)
-                st.host[lh, b].copy_(kv.cpu())
+                st.host[lh, b].copy_(kv)
             vb = Vr.view(w.Hkv, w.nb_max, 16, 128)
             b2s, s2b, lu = syn.initial_tables(w, layer) if b == 0 else (b2s, s2b, lu)
             idx = torch.from_numpy(s2b[b]).to(dev).long()
@@ -409,7 +418,8 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clk,
         "e2e": e2e,
         "device_error_word": errw,
-        "setup_s": round(gen_s, 1),
+        "setup_s": round(gen_s, 1), "alloc_s": round(alloc_s, 1),
+        "score_kernel": os.environ.get("OASIS_SCORE_KERNEL", "mma"),
     }
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args, args.cpu_heads)

@@ -110,6 +110,9 @@ OASIS_API const char* oasis_last_error(void);
  *             scores[..][x][0] = an approximation s~ of score(x) computed on the
  *             tensor cores, scores[..][x][1] = a bound e with |s~ - score| <= e.
  *             Entries x >= nb_b are not written.
+ *   err_word  device uint32 [1] or NULL; OR-ed with OASIS_EW_TIMEOUT if a
+ *             bounded wait inside the kernel gave up (the scores are then
+ *             incomplete).
  * The bound is e = 2^-12 * max_n |q_n|_2 * max_t |k_t|_2 / sqrt(d) (plus the
  * rounding of the 1/sqrt(d) product); it is an upper bound on the error of
  * fp32-accumulated bf16 products with a wide margin.  Selection never trusts
@@ -117,7 +120,7 @@ OASIS_API const char* oasis_last_error(void);
  */
 OASIS_API oasis_status oasis_score_blocks(const oasis_shape* shape, const void* k_hbm,
                                 const int32_t* ctx_len, const void* q_la,
-                                float* scores, oasis_stream_t stream);
+                                float* scores, uint32_t* err_word, oasis_stream_t stream);
 
 /*
  * a2. Top-K under the token budget.

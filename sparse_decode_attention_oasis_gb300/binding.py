@@ -50,7 +50,7 @@ _VP = ctypes.c_void_p
 _SIGS = {
     "oasis_version": ([], ctypes.c_char_p),
     "oasis_last_error": ([], ctypes.c_char_p),
-    "oasis_score_blocks": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
+    "oasis_score_blocks": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
     "oasis_topk_select": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
     "oasis_fetch_diff_capped": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                  ctypes.c_int32, _VP, _VP, _VP], ctypes.c_int),
@@ -117,9 +117,10 @@ def oasis_attn_workspace_bytes(shape: Shape) -> int:
     return int(load().oasis_attn_workspace_bytes(ctypes.byref(shape)))
 
 
-def oasis_score_blocks(shape: Shape, k_hbm, ctx_len, q_la, scores, stream=None):
+def oasis_score_blocks(shape: Shape, k_hbm, ctx_len, q_la, scores, err_word=None, stream=None):
     _check("oasis_score_blocks", load().oasis_score_blocks(
-        ctypes.byref(shape), _ptr(k_hbm), _ptr(ctx_len), _ptr(q_la), _ptr(scores), _stream(stream)))
+        ctypes.byref(shape), _ptr(k_hbm), _ptr(ctx_len), _ptr(q_la), _ptr(scores), _ptr(err_word),
+        _stream(stream)))
 
 
 def oasis_topk_select(shape: Shape, scores, k_hbm, q_la, ctx_len, sel, nsel, stream=None):

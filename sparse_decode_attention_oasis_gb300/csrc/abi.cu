@@ -1,5 +1,6 @@
 // C ABI entry points: argument validation, then the kernel launches.
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 
@@ -7,6 +8,8 @@
 
 namespace oasis {
 cudaError_t launch_score_blocks(const Shape&, const uint16_t*, const int*, const uint16_t*, float2*, cudaStream_t);
+cudaError_t launch_score_blocks_tc(const Shape&, const uint16_t*, const int*, const uint16_t*, float2*, unsigned*,
+                                   cudaStream_t);
 cudaError_t launch_topk_select(const Shape&, const float2*, const uint16_t*, const uint16_t*, const int*, int*,
                                int*, cudaStream_t);
 cudaError_t launch_fetch_diff(const Shape&, const float2*, const uint16_t*, const uint16_t*, const int*,
@@ -67,8 +70,15 @@ const char* oasis_version(void) { return "oasis-gb300 0.1 sm_103a"; }
 
 const char* oasis_last_error(void) { return g_last_error.c_str(); }
 
+// Scoring kernel: "mma" (mma.sync, registers only, default) or "tc" (TMA + tcgen05),
+// chosen by OASIS_SCORE_KERNEL; both implement the same definition and bound.
+static bool use_tc_scoring() {
+  const char* v = getenv("OASIS_SCORE_KERNEL");
+  return v && strcmp(v, "tc") == 0;
+}
+
 oasis_status oasis_score_blocks(const oasis_shape* shape, const void* k_hbm, const int32_t* ctx_len,
-                                const void* q_la, float* scores, oasis_stream_t stream) {
+                                const void* q_la, float* scores, uint32_t* err_word, oasis_stream_t stream) {
   static const char* fn = "oasis_score_blocks";
   oasis::Shape s;
   oasis_status st = check_shape(shape, fn, &s);
@@ -77,9 +87,15 @@ oasis_status oasis_score_blocks(const oasis_shape* shape, const void* k_hbm, con
   REQUIRE(q_la && aligned(q_la, 16), "q_la must be a 16-byte aligned device pointer");
   REQUIRE(ctx_len && aligned(ctx_len, 4), "ctx_len must be a 4-byte aligned device pointer");
   REQUIRE(scores && aligned(scores, 8), "scores must be an 8-byte aligned device pointer");
-  cudaError_t e = oasis::launch_score_blocks(s, static_cast<const uint16_t*>(k_hbm), ctx_len,
-                                             static_cast<const uint16_t*>(q_la),
-                                             reinterpret_cast<float2*>(scores), (cudaStream_t)stream);
+  REQUIRE(!err_word || aligned(err_word, 4), "err_word must be NULL or a 4-byte aligned device pointer");
+  cudaError_t e = use_tc_scoring()
+                      ? oasis::launch_score_blocks_tc(s, static_cast<const uint16_t*>(k_hbm), ctx_len,
+                                                      static_cast<const uint16_t*>(q_la),
+                                                      reinterpret_cast<float2*>(scores), err_word,
+                                                      (cudaStream_t)stream)
+                      : oasis::launch_score_blocks(s, static_cast<const uint16_t*>(k_hbm), ctx_len,
+                                                   static_cast<const uint16_t*>(q_la),
+                                                   reinterpret_cast<float2*>(scores), (cudaStream_t)stream);
   return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
 }
 

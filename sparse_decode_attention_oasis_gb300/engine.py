@@ -128,7 +128,7 @@ class DecodeState:
         lp, lh = layer % self.L_phys, layer % self.L_host
         st = stream or torch.cuda.current_stream(self.device)
         K = self.K[lp]
-        B.oasis_score_blocks(s, K, self.ctx, q_la, sc.scores, st)
+        B.oasis_score_blocks(s, K, self.ctx, q_la, sc.scores, sc.err, st)
         B.oasis_topk_select(s, sc.scores, K, q_la, self.ctx, sc.sel, sc.nsel, st)
         B.oasis_fetch_diff_capped(s, sc.scores, K, q_la, self.ctx, sc.sel, sc.nsel,
                                   self.blk2slot[lp], self.w.C, sc.fetch, sc.nfetch, st)
@@ -152,7 +152,7 @@ class DecodeState:
         K = self.K[lp]
         if timers is not None:
             timers[0].record(st)
-        B.oasis_score_blocks(s, K, self.ctx, q_la, sc.scores, st)
+        B.oasis_score_blocks(s, K, self.ctx, q_la, sc.scores, sc.err, st)
         if timers is not None:
             timers[1].record(st)
         B.oasis_topk_select(s, sc.scores, K, q_la, self.ctx, sc.sel, sc.nsel, st)

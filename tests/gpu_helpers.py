@@ -1,0 +1,91 @@
+"""Shared pieces of the GPU parity tests: one layer held on the GPU and in oracle arrays."""
+import numpy as np
+
+from oracle import oasis_ref as ref
+from sparse_decode_attention_oasis_gb300 import synthetic as syn
+
+ATOL, RTOL = 2e-3, 1e-2
+
+
+def _dev_bits(bits):
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def _check_out(got, want, what=""):
+    err = np.abs(got - want)
+    ok = (err <= ATOL) | (err <= RTOL * np.abs(want))
+    assert ok.all(), f"{what}: {int((~ok).sum())} elements out of tolerance, max abs {err.max():.3e}"
+    return float(err.max())
+
+
+class Case:
+    """One layer of a workload held both on the GPU and in oracle arrays."""
+
+    def __init__(self, w, K=None, V=None, tables=None):
+        from sparse_decode_attention_oasis_gb300.engine import DecodeState
+
+        self.w = w
+        if K is None:
+            K, V = syn.layer_kv(w, 0)
+        self.K, self.V = K, V
+        self.host = syn.host_tier_from_kv(w, K, V)
+        if tables is None:
+            tables = syn.initial_tables(w, 0)
+        self.b2s, self.s2b, self.lu = [np.array(t) for t in tables]
+        self.kp, self.vp = syn.pools_from_tables(w, self.host, self.s2b)
+        self.st = DecodeState(w, l_phys=1)
+        self.st.fill_layer_numpy(0, K, V, self.b2s, self.s2b, self.lu)
+
+    def step(self, step, q=None, qla=None, C=None):
+        import torch
+
+        w = self.w
+        if q is None:
+            q, qla = syn.layer_queries(w, 0, step)
+        if C is not None:
+            w.C = C
+        r = ref.layer_step(self.K, qla, q, w.ctx, self.host, self.kp, self.vp, self.b2s, self.s2b,
+                           self.lu, w.Kb, w.C, step, bs=w.bs)
+        sc = self.st.layer_step(0, _dev_bits(qla), _dev_bits(q), step)
+        torch.cuda.synchronize()
+        self.compare(r, sc)
+        return r, sc
+
+    def compare(self, r, sc):
+        import torch
+
+        w = self.w
+        scores = sc.scores.cpu().numpy()
+        sel = sc.sel.cpu().numpy()
+        nsel = sc.nsel.cpu().numpy()
+        fetch = sc.fetch.cpu().numpy()
+        nfetch = sc.nfetch.cpu().numpy()
+        assert int(sc.err.cpu()[0]) == 0
+        for (b, h), S in r["S"].items():
+            nb = w.nb(b)
+            s_exact, _ = r["score"][(b, h)]
+            if nb > w.Kb:  # scores are only needed (and written) when there is a choice
+                approx = scores[b, h, :nb, 0].astype(np.float64)
+                bound = scores[b, h, :nb, 1].astype(np.float64)
+                assert (np.abs(approx - s_exact) <= bound).all(), f"score outside bound at {(b, h)}"
+                assert (bound < 1e-2 * (1 + np.abs(s_exact))).all()
+            assert nsel[b, h] == len(S)
+            assert sel[b, h, :len(S)].tolist() == S, f"sel mismatch at {(b, h)}"
+            assert (sel[b, h, len(S):] == -1).all()
+            F = r["F"][(b, h)]
+            assert nfetch[b, h] == len(F)
+            assert fetch[b, h, :len(F)].tolist() == F, f"fetch mismatch at {(b, h)}"
+        lp = 0
+        np.testing.assert_array_equal(self.st.blk2slot[lp].cpu().numpy(), self.b2s)
+        np.testing.assert_array_equal(self.st.slot2blk[lp].cpu().numpy(), self.s2b)
+        np.testing.assert_array_equal(self.st.last_used[lp].cpu().numpy(), self.lu)
+        kpool = self.st.k_pool[lp].cpu().view(torch.int16).numpy().view(np.uint16)
+        vpool = self.st.v_pool[lp].cpu().view(torch.int16).numpy().view(np.uint16)
+        occupied = self.s2b >= 0
+        np.testing.assert_array_equal(kpool[occupied], self.kp[occupied])
+        np.testing.assert_array_equal(vpool[occupied], self.vp[occupied])
+        _check_out(sc.out.cpu().numpy().astype(np.float64), r["out"], "attention")
+
+

@@ -53,19 +53,20 @@ def _shape(**kw):
 ])
 def test_shape_validation_rejects_before_launch(lib, kw, status):
     s = _shape(**kw)
-    st = lib.oasis_score_blocks(ctypes.byref(s), 16, 16, 16, 16, None)
+    st = lib.oasis_score_blocks(ctypes.byref(s), 16, 16, 16, 16, None, None)
     assert st == status
     assert lib.oasis_last_error()
 
 
 def test_null_and_misaligned_pointers_are_invalid(lib):
     s = _shape()
-    assert lib.oasis_score_blocks(ctypes.byref(s), None, 16, 16, 16, None) == 1
-    assert lib.oasis_score_blocks(ctypes.byref(s), 18, 16, 16, 16, None) == 1
+    assert lib.oasis_score_blocks(ctypes.byref(s), None, 16, 16, 16, None, None) == 1
+    assert lib.oasis_score_blocks(ctypes.byref(s), 18, 16, 16, 16, None, None) == 1
+    assert lib.oasis_score_blocks(ctypes.byref(s), 16, 16, 16, 16, 18, None) == 1
     assert lib.oasis_fetch_diff_capped(ctypes.byref(s), 16, 16, 16, 16, 16, 16, 16, 33, 16, 16, None) == 1
     assert lib.oasis_sparse_decode_attn(ctypes.byref(s), 16, 16, 16, 16, 16, 16, 16, 0.1, 16, 0, 16, None) == 1
     with pytest.raises(binding.OasisError):
-        binding.oasis_score_blocks(s, None, 16, 16, 16, stream=0)
+        binding.oasis_score_blocks(s, None, 16, 16, 16, None, stream=0)
 
 
 def test_workspace_size_formula(lib):

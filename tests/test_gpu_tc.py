@@ -1,0 +1,51 @@
+"""The TMA + tcgen05 scoring kernel, checked like the default one (bound, selection, full step)."""
+import numpy as np
+import pytest
+
+from sparse_decode_attention_oasis_gb300 import synthetic as syn
+
+from gpu_helpers import Case
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(autouse=True)
+def _tc_kernel(monkeypatch):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_decode_attention_oasis_gb300 import build
+
+    build.build()
+    monkeypatch.setenv("OASIS_SCORE_KERNEL", "tc")
+
+
+def test_tc_tiny_workload_two_steps():
+    c = Case(syn.tiny())
+    c.step(0)
+    c.step(1)
+
+
+@pytest.mark.parametrize("Hq,n_la,ctx", [(32, 4, [4096, 1000, 17]), (64, 4, [2048, 1531]),
+                                        (16, 3, [1024, 700]), (8, 4, [3000, 129])])
+def test_tc_shapes(Hq, n_la, ctx):
+    w = syn.Workload("tc", L=1, B=len(ctx), Hq=Hq, Hkv=8, ctx=ctx, Kb=32, C=5, n_hot=16, n_la=n_la)
+    c = Case(w)
+    c.step(0)
+
+
+def test_tc_matches_the_default_kernel_within_bounds(monkeypatch):
+    w = syn.Workload("cmp", L=1, B=2, Hq=32, Hkv=8, ctx=[4096, 2500], Kb=32, C=4, n_hot=16)
+    c = Case(w)
+    r, sc = c.step(0)
+    tc_scores = sc.scores.cpu().numpy().copy()
+    monkeypatch.setenv("OASIS_SCORE_KERNEL", "mma")
+    c2 = Case(w)
+    r2, sc2 = c2.step(0)
+    mma_scores = sc2.scores.cpu().numpy()
+    for b in range(w.B):
+        nb = w.nb(b)
+        a, e = tc_scores[b, :, :nb, 0], tc_scores[b, :, :nb, 1]
+        m, e2 = mma_scores[b, :, :nb, 0], mma_scores[b, :, :nb, 1]
+        assert (np.abs(a - m) <= e + e2).all()
+        np.testing.assert_allclose(e, e2, rtol=1e-5)
