@@ -44,6 +44,7 @@ struct SelCtx {
   float* qf;                   // [kMaxN][kQStride]
   uint16_t* qb;                // [kMaxN][128]
   float* qn;                   // [kMaxN]
+  uint16_t* kst;               // [kSelWarps][16][128] staged key blocks
   unsigned long long* lacc;    // [kSelWarps][kLimbs]
   uint32_t* tmp;               // [kSelWarps][kLimbs]
   uint32_t* bval;              // [kSelWarps][kLimbs]
@@ -65,12 +66,12 @@ __device__ __forceinline__ int exact_cmp(const uint32_t* a, const uint32_t* b) {
 }
 
 // Exact q.k (times 2^266) of a 128-long bf16 row pair, by one warp.
-__device__ void warp_exact_dot(const uint16_t* __restrict__ krow, const uint16_t* qrow,
+__device__ void warp_exact_dot(const uint16_t* krow, const uint16_t* qrow,
                                unsigned long long* acc, uint32_t* out, int lane) {
   if (lane < kLimbs) acc[lane] = 0ull;
   __syncwarp();
   for (int e = lane; e < kD; e += 32) {
-    const uint32_t kb = __ldg(krow + e), qb = qrow[e];
+    const uint32_t kb = krow[e], qb = qrow[e];
     const uint32_t kE = (kb >> 7) & 0xffu, qE = (qb >> 7) & 0xffu;
     const uint32_t km = (kb & 0x7fu) | (kE ? 0x80u : 0u);
     const uint32_t qm = (qb & 0x7fu) | (qE ? 0x80u : 0u);
@@ -205,16 +206,30 @@ __device__ void stage_queries(SelCtx& c) {
 }
 
 // Exact score (x 2^266, as kLimbs words) of block `blk`, by one warp, into out.
+// The block's 16 key rows (4 KiB) are first staged in this warp's shared-memory
+// slot with one round of coalesced 16-byte loads; everything after that reads
+// shared memory only.
 __device__ void warp_exact_block_score(const SelCtx& c, int blk, uint32_t* out, int warp, int lane) {
   constexpr int kMaxPerLane = (kBS * kMaxN) / 32;
   const int ndots = kBS * c.N;
-  const uint16_t* kblk = c.k + (long long)blk * kBS * kD;
+  uint16_t* kst = c.kst + warp * (kBS * kD);
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(c.k + (long long)blk * kBS * kD);
+    uint4* dst = reinterpret_cast<uint4*>(kst);
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = ldg_nc(src + lane + 32 * i);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dst[lane + 32 * i] = v[i];
+  }
+  __syncwarp();
   // token norms (lanes 0..15)
   float kn = 0.f;
   if (lane < kBS) {
-    const uint32_t* row = reinterpret_cast<const uint32_t*>(kblk + lane * kD);
+    const uint32_t* row = reinterpret_cast<const uint32_t*>(kst + lane * kD);
+#pragma unroll 8
     for (int i = 0; i < kD / 2; ++i) {
-      const uint32_t w = __ldg(row + i);
+      const uint32_t w = row[(i + lane) & (kD / 2 - 1)];
       kn = fmaf(bf_lo(w), bf_lo(w), kn);
       kn = fmaf(bf_hi(w), bf_hi(w), kn);
     }
@@ -230,11 +245,12 @@ __device__ void warp_exact_block_score(const SelCtx& c, int blk, uint32_t* out, 
     vlo[m] = neg_inf();
     vhi[m] = neg_inf();
     if (dd < ndots && blk * kBS + tau < c.ctx) {
-      const uint32_t* row = reinterpret_cast<const uint32_t*>(kblk + tau * kD);
+      const uint32_t* row = reinterpret_cast<const uint32_t*>(kst + tau * kD);
       const float* qr = c.qf + n * kQStride;
       float v = 0.f;
+#pragma unroll 8
       for (int i = 0; i < kD / 2; ++i) {
-        const uint32_t w = __ldg(row + i);
+        const uint32_t w = row[i];
         v = fmaf(bf_lo(w), qr[2 * i], v);
         v = fmaf(bf_hi(w), qr[2 * i + 1], v);
       }
@@ -259,7 +275,7 @@ __device__ void warp_exact_block_score(const SelCtx& c, int blk, uint32_t* out, 
       mask &= mask - 1;
       const int dd = src + 32 * m;
       const int tau = dd / c.N, n = dd - tau * c.N;
-      warp_exact_dot(kblk + tau * kD, c.qb + n * kD, acc, tmp, lane);
+      warp_exact_dot(kst + tau * kD, c.qb + n * kD, acc, tmp, lane);
       if (lane == 0) {
         if (!have || exact_cmp(tmp, out) > 0)
           for (int i = 0; i < kLimbs; ++i) out[i] = tmp[i];
@@ -370,18 +386,19 @@ __device__ void select_best(SelCtx& c, const float2* se, int n, int k, const int
 
 // ---------------------------------------------------------------- shared memory layout
 struct SelLayout {
-  size_t se, cls, U, cblk, qf, qb, qn, lacc, tmp, bval, bidx, tval, tidx, hist, scal, fscal, red, total;
+  size_t se, cls, U, cblk, kst, qf, qb, qn, lacc, tmp, bval, bidx, tval, tidx, hist, scal, fscal, red, total;
 };
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
-__host__ __device__ inline SelLayout sel_layout(int ncap) {
+__host__ __device__ inline SelLayout sel_layout(int ncap, bool with_cblk) {
   SelLayout L;
   size_t o = 0;
   L.se = o; o = align16(o + sizeof(float2) * ncap);
   L.cls = o; o = align16(o + ncap);
   L.U = o; o = align16(o + sizeof(int) * ncap);
-  L.cblk = o; o = align16(o + sizeof(int) * ncap);
+  L.cblk = o; o = align16(o + (with_cblk ? sizeof(int) * ncap : 0));
+  L.kst = o; o = align16(o + sizeof(uint16_t) * kSelWarps * kBS * kD);
   L.qf = o; o = align16(o + sizeof(float) * kMaxN * kQStride);
   L.qb = o; o = align16(o + sizeof(uint16_t) * kMaxN * kD);
   L.qn = o; o = align16(o + sizeof(float) * kMaxN);
@@ -414,6 +431,7 @@ __device__ SelCtx make_ctx(char* sm, const SelLayout& L, const Shape& s, const u
   c.qf = reinterpret_cast<float*>(sm + L.qf);
   c.qb = reinterpret_cast<uint16_t*>(sm + L.qb);
   c.qn = reinterpret_cast<float*>(sm + L.qn);
+  c.kst = reinterpret_cast<uint16_t*>(sm + L.kst);
   c.lacc = reinterpret_cast<unsigned long long*>(sm + L.lacc);
   c.tmp = reinterpret_cast<uint32_t*>(sm + L.tmp);
   c.bval = reinterpret_cast<uint32_t*>(sm + L.bval);
@@ -432,7 +450,7 @@ topk_select_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* _
                    const uint16_t* __restrict__ q_la, const int* __restrict__ ctx_len,
                    int* __restrict__ sel, int* __restrict__ nsel) {
   extern __shared__ __align__(16) char sm[];
-  const SelLayout L = sel_layout(s.nb_max);
+  const SelLayout L = sel_layout(s.nb_max, false);
   const int head = blockIdx.x;
   const int b = head / s.Hkv;
   const int ctx = ctx_len[b];
@@ -477,7 +495,7 @@ fetch_diff_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __
                   const int* __restrict__ blk2slot, int cap, int* __restrict__ fetch,
                   int* __restrict__ nfetch) {
   extern __shared__ __align__(16) char sm[];
-  const SelLayout L = sel_layout(s.Kb);
+  const SelLayout L = sel_layout(s.Kb, true);
   const int head = blockIdx.x;
   const int b = head / s.Hkv;
   const int ctx = ctx_len[b];
@@ -516,8 +534,8 @@ fetch_diff_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __
 }
 
 // ---------------------------------------------------------------- launchers
-size_t topk_smem_bytes(const Shape& s) { return sel_layout(s.nb_max).total; }
-size_t diff_smem_bytes(const Shape& s) { return sel_layout(s.Kb).total; }
+size_t topk_smem_bytes(const Shape& s) { return sel_layout(s.nb_max, false).total; }
+size_t diff_smem_bytes(const Shape& s) { return sel_layout(s.Kb, true).total; }
 
 cudaError_t launch_topk_select(const Shape& s, const float2* scores, const uint16_t* k,
                                const uint16_t* q_la, const int* ctx, int* sel, int* nsel,
