@@ -182,6 +182,32 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- helpers
+class KernelMarks:
+    """CUDA events recorded before/after each kernel of the decode step, per stream."""
+
+    def __init__(self, n):
+        import torch
+
+        self.pool = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        self.used = []
+
+    def __call__(self, name, stream):
+        ev = self.pool[len(self.used)]
+        ev.record(stream)
+        self.used.append((name, stream, ev))
+
+    def durations(self):
+        """Per kernel name, the list of launch durations in ms (consecutive marks on one stream)."""
+        out = {"score": [], "topk": [], "diff": [], "gather": [], "attn": []}
+        last = {}
+        for name, stream, ev in self.used:
+            key = id(stream)
+            if key in last and last[key][0] in out:
+                out[last[key][0]].append(last[key][1].elapsed_time(ev))
+            last[key] = (name, ev)
+        return out
+
+
 def reduce_max(x: float, world: int, device=None) -> float:
     """Max of a per-rank float over all ranks (identity for one rank)."""
     if world <= 1:
@@ -207,8 +233,14 @@ def measured_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the scoring kernel's code with comments and blank lines removed."""
     src = os.path.join(ROOT, "sparse_decode_attention_oasis_gb300", "csrc", "score.cu")
-    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    code = []
+    for line in open(src, encoding="utf-8"):
+        line = line.split("//", 1)[0].strip()
+        if line:
+            code.append(line)
+    return hashlib.sha256("\n".join(code).encode()).hexdigest()[:16]
 
 
 def score_traffic_per_launch():
@@ -306,22 +338,7 @@ def run_gpu(args, rank, world, local_rank):
             l_host = max(2, l_host // 2)
             torch.cuda.empty_cache()
     alloc_s = time.time() - t0
-    for layer in range(L):
-        lp, lh = layer, layer % l_host
-        for b in range(w.B):
-            Kr, Vr = syn.kv_request_torch(w, layer, b, dev)
-            st.K[lp, b].copy_(Kr)
-            if layer < l_host:
-                kv = torch.stack([Kr.view(w.Hkv, w.nb_max, 16, 128), Vr.view(w.Hkv, w.nb_max, 16, 128)], dim=2)
-                st.host[lh, b].copy_(kv)
-            vb = Vr.view(w.Hkv, w.nb_max, 16, 128)
-            b2s, s2b, lu = syn.initial_tables(w, layer) if b == 0 else (b2s, s2b, lu)
-            idx = torch.from_numpy(s2b[b]).to(dev).long()
-            st.k_pool[lp, b].copy_(Kr.view(w.Hkv, w.nb_max, 16, 128)[torch.arange(w.Hkv, device=dev)[:, None], idx])
-            st.v_pool[lp, b].copy_(vb[torch.arange(w.Hkv, device=dev)[:, None], idx])
-        st.blk2slot[lp].copy_(torch.from_numpy(b2s))
-        st.slot2blk[lp].copy_(torch.from_numpy(s2b))
-        st.last_used[lp].copy_(torch.from_numpy(lu))
+    st.fill_synthetic()
     torch.cuda.synchronize()
     gen_s = time.time() - t0
 
@@ -341,17 +358,16 @@ def run_gpu(args, rank, world, local_rank):
     side = torch.cuda.Stream(dev)
     out_dev = torch.empty((L, w.B, w.Hq, w.d), dtype=torch.float32, device=dev)
 
-    def step(s, timers=None, qla=None, q=None):
+    def step(s, mark=None, qla=None, q=None):
         st.decode_step(s, qla if qla is not None else qla_dev[s], q if q is not None else q_dev[s],
-                       out_layers=out_dev, main=main, side=side, score_timers=timers)
+                       out_layers=out_dev, main=main, side=side, mark=mark)
 
     for s in range(args.warmup):
         step(s)
     torch.cuda.synchronize()
     errw = int(st.scratch.err.item()) | int(st.scratch2.err.item())
 
-    timers = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(L)]
-              for _ in range(args.steps)]
+    marks = KernelMarks(L * args.steps * 8 + 16)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local_rank)
     if world > 1:
@@ -361,14 +377,15 @@ def run_gpu(args, rank, world, local_rank):
     time.sleep(0.3)
     ev0.record(main)
     for k in range(args.steps):
-        step(args.warmup + k, timers[k])
+        step(args.warmup + k, marks)
     ev1.record(main)
     torch.cuda.synchronize()
     clk = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
     ms = reduce_max(ev0.elapsed_time(ev1), world, dev)
-    score_ms = [t[0].elapsed_time(t[1]) for per in timers for t in per]
+    kernel_ms = marks.durations()
+    score_ms = kernel_ms["score"]
 
     # end to end: H2D of the step's queries, the C-ABI calls, D2H of the outputs
     e2e = None
@@ -414,6 +431,7 @@ def run_gpu(args, rank, world, local_rank):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": score_traffic_per_launch(), "bytes_per_launch": ab["score"],
                      "avg_launch_ms": score_avg_ms},
+        "kernel_avg_us": {k: round(1000.0 * sum(v) / len(v), 2) for k, v in kernel_ms.items() if v},
         "gpu_launches": 6 * L * args.steps,
         "clocks": clk,
         "e2e": e2e,

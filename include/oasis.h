@@ -170,8 +170,8 @@ OASIS_API oasis_status oasis_fetch_diff_capped(const oasis_shape* shape, const f
 
 /*
  * a4. Host-tier gather into HBM slots, with the head-wise block table update.
- * Defines: prefetch the selected blocks from the host tier into the bounded GPU
- * working set (OasisKV abstract; metalmedia.ai page, explanatory figure step 4),
+ * Defines: prefetch the selected blocks from the host tier into the limited set
+ * of HBM slots (OasisKV abstract; metalmedia.ai page, explanatory figure step 4),
  * the head-wise table from GPU blocks to host-tier blocks (Figure 9 caption) and
  * LRU eviction (Table 2 caption).
  *   Candidate slots, per (request, KV head): the free slots (slot2blk == -1) in
@@ -226,6 +226,32 @@ OASIS_API oasis_status oasis_sparse_decode_attn(const oasis_shape* shape, const 
                                       const int32_t* blk2slot, const int32_t* ctx_len,
                                       float scale, void* workspace, size_t ws_bytes,
                                       float* out, oasis_stream_t stream);
+
+/*
+ * Token append (long-output decode).
+ * Defines: decode grows each request's KV cache by one token per step (OasisKV
+ * abstract; metalmedia.ai page, Table 1 "long output" rows and Figure 11
+ * caption).  For every request b with t = ctx_len[b] < nb_max*bs, and every KV
+ * head h, the new key/value row is written to
+ *   k_hbm[b][h][t], host_kv[b][h][t/bs][0][t%bs] (key), host_kv[..][1][t%bs]
+ *   (value), and, when blk2slot[b][h][t/bs] = p >= 0, to k_pool/v_pool[b][h][p][t%bs];
+ * then, if `advance` is nonzero, ctx_len[b] = t + 1.  A model with several
+ * layers calls this once per layer with the same ctx_len and advance = 1 on the
+ * last call only.  A full cache (t >= nb_max*bs) sets OASIS_EW_BAD_COUNT and
+ * leaves request b unchanged.
+ * Arguments:
+ *   k_new, v_new  device bf16 [B][Hkv][d]      the new token's key and value
+ *   ctx_len       device int32 [B]             in/out
+ *   k_hbm         device bf16 [B][Hkv][nb_max*bs][d]   in/out
+ *   host_kv       page-locked mapped host memory, layout as in oasis_gather_h2d
+ *   blk2slot      device int32 [B][Hkv][nb_max]        read only
+ *   k_pool, v_pool device bf16 [B][Hkv][P][bs][d]      in/out
+ *   err_word      device uint32 [1] or NULL
+ */
+OASIS_API oasis_status oasis_append_kv(const oasis_shape* shape, const void* k_new, const void* v_new,
+                                       int32_t* ctx_len, void* k_hbm, void* host_kv,
+                                       const int32_t* blk2slot, void* k_pool, void* v_pool,
+                                       int32_t advance, uint32_t* err_word, oasis_stream_t stream);
 
 /* Bytes of device workspace oasis_sparse_decode_attn needs for `shape` (0 on a bad shape). */
 OASIS_API size_t oasis_attn_workspace_bytes(const oasis_shape* shape);

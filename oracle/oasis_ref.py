@@ -16,13 +16,14 @@ Lookahead Sparse Prefetching"):
           prediction of next-step KV blocks; comparing the prediction with the
           blocks already on the GPU and fetching only the missing ones, under a
           per-step cap; the predict/select/transfer pipeline.
-  [fig7]  metalmedia.ai page, Figure 7 caption (look-ahead attention): the draft
-          query scans the keys to predict the next step's top-K blocks; the
-          attention kernel runs over the sparse KV working set.
+  [fig7]  metalmedia.ai page, Figure 7 caption (look-ahead attention): the
+          draft queries are compared with the keys to pick the K blocks the next
+          decode step will need; attention itself only reads the sparse set of
+          blocks kept on the GPU.
   [fig9]  metalmedia.ai page, Figure 9 caption: a head-wise table maps each GPU
           block of the bounded working set to a CPU (host-tier) block.
-  [tab2]  metalmedia.ai page, Table 2 caption: the fetch cap bounds the blocks
-          fetched per step by a fetch ratio; LRU eviction.
+  [tab2]  metalmedia.ai page, Table 2 caption: a fetch ratio sets how many
+          blocks a single step may bring in; evictions follow LRU.
 
 Readings where the pages are silent (each is listed in the design notes):
   * score(b) = max over lookahead queries j, query heads g of the GQA group of
@@ -255,6 +256,37 @@ def head_sparse_attention(q_bits: np.ndarray, kpool_bits: np.ndarray, vpool_bits
     K = bf16_to_f64(np.concatenate(rows_k)) if rows_k else np.zeros((0, d))
     V = bf16_to_f64(np.concatenate(rows_v)) if rows_v else np.zeros((0, d))
     return attention_over_tokens(bf16_to_f64(q_bits), K, V, scale)
+
+
+# --------------------------------------------------------------------------
+# token append (long-output decode)  ([abs]: the KV cache grows during decode)
+# --------------------------------------------------------------------------
+def append_token(k_bits, host_kv, k_pool, v_pool, blk2slot, ctx_len, k_new, v_new,
+                 bs: int = BS_DEFAULT, advance: bool = True):
+    """Append one token per request to keys, host tier and (if resident) its slot.
+
+    k_bits [B][Hkv][T_max][d]; host_kv [B][Hkv][nb_max][2][bs][d];
+    k_pool/v_pool [B][Hkv][P][bs][d]; blk2slot [B][Hkv][nb_max]; ctx_len is a
+    mutable list/array of per-request lengths; k_new/v_new [B][Hkv][d].  With
+    ``advance`` the lengths grow by one (a model calls this once per layer and
+    advances on the last).  A full cache leaves the request unchanged.
+    """
+    B, Hkv, T_max, _ = k_bits.shape
+    for b in range(B):
+        t = int(ctx_len[b])
+        if t < 0 or t >= T_max:
+            continue
+        blk, r = divmod(t, bs)
+        for h in range(Hkv):
+            k_bits[b, h, t] = k_new[b, h]
+            host_kv[b, h, blk, 0, r] = k_new[b, h]
+            host_kv[b, h, blk, 1, r] = v_new[b, h]
+            p = int(blk2slot[b, h, blk])
+            if p >= 0:
+                k_pool[b, h, p, r] = k_new[b, h]
+                v_pool[b, h, p, r] = v_new[b, h]
+        if advance:
+            ctx_len[b] = t + 1
 
 
 # --------------------------------------------------------------------------

@@ -59,6 +59,8 @@ _SIGS = {
     "oasis_sparse_decode_attn": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                   ctypes.c_float, _VP, ctypes.c_size_t, _VP, _VP], ctypes.c_int),
     "oasis_attn_workspace_bytes": ([ctypes.POINTER(Shape)], ctypes.c_size_t),
+    "oasis_append_kv": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_int32,
+                         _VP, _VP], ctypes.c_int),
 }
 
 _lib = None
@@ -150,3 +152,10 @@ def oasis_sparse_decode_attn(shape: Shape, q, k_pool, v_pool, sel, nsel, blk2slo
         ctypes.byref(shape), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(sel), _ptr(nsel),
         _ptr(blk2slot), _ptr(ctx_len), float(scale), _ptr(workspace), int(ws_bytes), _ptr(out),
         _stream(stream)))
+
+
+def oasis_append_kv(shape: Shape, k_new, v_new, ctx_len, k_hbm, host_kv, blk2slot, k_pool, v_pool,
+                    advance: bool = True, err_word=None, stream=None):
+    _check("oasis_append_kv", load().oasis_append_kv(
+        ctypes.byref(shape), _ptr(k_new), _ptr(v_new), _ptr(ctx_len), _ptr(k_hbm), _ptr(host_kv),
+        _ptr(blk2slot), _ptr(k_pool), _ptr(v_pool), 1 if advance else 0, _ptr(err_word), _stream(stream)))

@@ -20,6 +20,8 @@ cudaError_t launch_sparse_decode_attn(const Shape&, const uint16_t*, const uint1
                                       const int*, const int*, const int*, const int*, float, void*, float*,
                                       cudaStream_t);
 size_t attn_workspace_bytes(const Shape&);
+cudaError_t launch_append_kv(const Shape&, const uint16_t*, const uint16_t*, int*, uint16_t*, uint16_t*, const int*,
+                             uint16_t*, uint16_t*, int, unsigned*, cudaStream_t);
 size_t topk_smem_bytes(const Shape&);
 }  // namespace oasis
 
@@ -169,6 +171,39 @@ oasis_status oasis_gather_h2d(const oasis_shape* shape, const void* host_kv, con
   e = oasis::launch_gather_h2d(s, static_cast<const uint16_t*>(attr.devicePointer), sel, nsel, fetch, nfetch,
                                blk2slot, slot2blk, last_used, step, static_cast<uint16_t*>(k_pool),
                                static_cast<uint16_t*>(v_pool), err_word, (cudaStream_t)stream);
+  return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
+}
+
+// Device address of page-locked mapped host memory (NULL if `p` is not such memory).
+static void* mapped_host_ptr(const void* p) {
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (attr.type != cudaMemoryTypeHost) return nullptr;
+  return attr.devicePointer;
+}
+
+oasis_status oasis_append_kv(const oasis_shape* shape, const void* k_new, const void* v_new, int32_t* ctx_len,
+                             void* k_hbm, void* host_kv, const int32_t* blk2slot, void* k_pool, void* v_pool,
+                             int32_t advance, uint32_t* err_word, oasis_stream_t stream) {
+  static const char* fn = "oasis_append_kv";
+  oasis::Shape s;
+  oasis_status st = check_shape(shape, fn, &s);
+  if (st != OASIS_OK) return st;
+  REQUIRE(k_new && v_new && aligned(k_new, 16) && aligned(v_new, 16), "k_new/v_new must be 16-byte aligned");
+  REQUIRE(k_hbm && aligned(k_hbm, 16), "k_hbm must be a 16-byte aligned device pointer");
+  REQUIRE(k_pool && v_pool && aligned(k_pool, 16) && aligned(v_pool, 16), "pools must be 16-byte aligned");
+  REQUIRE(ctx_len && aligned(ctx_len, 4) && blk2slot && aligned(blk2slot, 4), "ctx_len/blk2slot must be int32 arrays");
+  REQUIRE(!err_word || aligned(err_word, 4), "err_word must be NULL or 4-byte aligned");
+  REQUIRE(host_kv && aligned(host_kv, 16), "host_kv must be a 16-byte aligned pointer");
+  void* host_dev = mapped_host_ptr(host_kv);
+  if (!host_dev) return fail(OASIS_ERR_INVALID, fn, "host_kv must be page-locked, device-mapped host memory");
+  cudaError_t e = oasis::launch_append_kv(s, static_cast<const uint16_t*>(k_new), static_cast<const uint16_t*>(v_new),
+                                          ctx_len, static_cast<uint16_t*>(k_hbm), static_cast<uint16_t*>(host_dev),
+                                          blk2slot, static_cast<uint16_t*>(k_pool), static_cast<uint16_t*>(v_pool),
+                                          advance, err_word, (cudaStream_t)stream);
   return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
 }
 

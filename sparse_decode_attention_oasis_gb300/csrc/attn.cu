@@ -1,8 +1,8 @@
 // a5: block-sparse paged decode attention over the resident selected blocks.
 //
 // OasisKV abstract (attention over only the most relevant tokens kept in HBM) and
-// metalmedia.ai page, Figure 7 caption, right (the attention kernel runs over the
-// sparse KV working set).  A = { x in S : blk2slot[x] != -1 }; for each query head
+// metalmedia.ai page, Figure 7 caption, right (decode attention reads only the
+// blocks selected and held on the GPU).  A = { x in S : blk2slot[x] != -1 }; for each query head
 // of the GQA group, softmax(scale * q.k) v over the valid tokens of A.
 //
 // Split-K flash decode.  Grid (split, request*KV head); a split covers

@@ -2,8 +2,8 @@
 //
 // score(x) = max over lookahead queries j, GQA query heads g and valid tokens t
 // of block x of q_la[j, hG+g] . k_t / sqrt(d)  (OasisKV, metalmedia.ai page,
-// Figure 7 caption: the draft query scans the keys to predict the next step's
-// top-K blocks).
+// Figure 7 caption: the draft queries are compared with the keys to choose the
+// blocks the next step needs).
 //
 // Mapping.  One warp scores one 16-token block at a time as a 16 x N tile
 // D = K_blk (16 tok x 128 d) * Q^T (128 d x N queries) with mma.m16n8k16 (bf16

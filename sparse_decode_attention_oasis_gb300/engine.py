@@ -89,6 +89,35 @@ class DecodeState:
         self.k_pool[lp].copy_(_bf16_from_bits(kp, self.device))
         self.v_pool[lp].copy_(_bf16_from_bits(vp, self.device))
 
+    def fill_synthetic(self):
+        """Generate every layer on the device (keys, host tier, pools, tables).
+
+        Uses the counter-based generator (bit-identical to the host one).  With
+        a host tier of fewer layers than the model, only layers < L_host write
+        the host tier; layer l's gathers read host buffer l mod L_host.
+        """
+        w = self.w
+        dev = self.device
+        ar = torch.arange(w.Hkv, device=dev)[:, None]
+        for layer in range(w.L):
+            lp, lh = layer % self.L_phys, layer % self.L_host
+            b2s, s2b, lu = syn.initial_tables(w, layer)
+            for b in range(w.B):
+                Kr, Vr = syn.kv_request_torch(w, layer, b, dev)
+                self.K[lp, b].copy_(Kr)
+                kb = Kr.view(w.Hkv, w.nb_max, 16, 128)
+                vb = Vr.view(w.Hkv, w.nb_max, 16, 128)
+                if layer < self.L_host:
+                    self.host[lh, b].copy_(torch.stack([kb, vb], dim=2))
+                idx = torch.from_numpy(s2b[b]).to(dev).long()
+                occ = (idx >= 0)[..., None, None]
+                self.k_pool[lp, b].copy_(kb[ar, idx.clamp(min=0)] * occ)
+                self.v_pool[lp, b].copy_(vb[ar, idx.clamp(min=0)] * occ)
+            self.blk2slot[lp].copy_(torch.from_numpy(b2s))
+            self.slot2blk[lp].copy_(torch.from_numpy(s2b))
+            self.last_used[lp].copy_(torch.from_numpy(lu))
+        torch.cuda.synchronize(dev)
+
     def fill_layer_synthetic(self, layer: int):
         """Generate one layer on the device with the counter-based generator."""
         lp, lh = layer % self.L_phys, layer % self.L_host
@@ -146,18 +175,22 @@ class DecodeState:
         return sc
 
     # ---------------------------------------------------------------- one decode step
-    def _select(self, layer, q_la, step, sc, st, timers=None):
+    def _select(self, layer, q_la, step, sc, st, mark=None):
         s = self.shape
         lp = layer % self.L_phys
         K = self.K[lp]
-        if timers is not None:
-            timers[0].record(st)
+        if mark:
+            mark("score", st)
         B.oasis_score_blocks(s, K, self.ctx, q_la, sc.scores, sc.err, st)
-        if timers is not None:
-            timers[1].record(st)
+        if mark:
+            mark("topk", st)
         B.oasis_topk_select(s, sc.scores, K, q_la, self.ctx, sc.sel, sc.nsel, st)
+        if mark:
+            mark("diff", st)
         B.oasis_fetch_diff_capped(s, sc.scores, K, q_la, self.ctx, sc.sel, sc.nsel,
                                   self.blk2slot[lp], self.w.C, sc.fetch, sc.nfetch, st)
+        if mark:
+            mark("end", st)
 
     def _gather(self, layer, step, sc, gs):
         s = self.shape
@@ -174,7 +207,7 @@ class DecodeState:
                                    sc.out if out is None else out, st)
 
     def decode_step(self, step: int, q_la_layers, q_layers, out_layers=None, main=None, side=None,
-                    score_timers=None):
+                    mark=None):
         """All layers of one decode step, pipelined across layers.
 
         Main stream: select(0); select(1); attn(0); select(2); attn(1); ...
@@ -182,7 +215,10 @@ class DecodeState:
         of layer l overlaps the HBM-bound scoring of layer l+1; attn(l) waits for
         gather(l).  Two scratch sets alternate between consecutive layers.
         q_la_layers[l], q_layers[l]: device tensors of layer l; out_layers[l]
-        (optional) receives the fp32 attention output of layer l.
+        (optional) receives the fp32 attention output of layer l.  ``mark(name,
+        stream)``, if given, is called before each kernel ("score", "topk",
+        "diff", "gather", "attn") and after the last one of a group ("end",
+        "gather_end", "attn_end") so the caller can record CUDA events.
         """
         L = self.w.L
         main = main or torch.cuda.current_stream(self.device)
@@ -194,11 +230,14 @@ class DecodeState:
 
         def launch_select_gather(l):
             sc = scr[l % 2]
-            self._select(l, q_la_layers[l], step, sc, main,
-                         None if score_timers is None else score_timers[l])
+            self._select(l, q_la_layers[l], step, sc, main, mark)
             if side is not main:
                 side.wait_stream(main)
+            if mark:
+                mark("gather", side)
             self._gather(l, step, sc, side)
+            if mark:
+                mark("gather_end", side)
             if side is not main:
                 events[l % 2].record(side)
 
@@ -208,5 +247,19 @@ class DecodeState:
                 launch_select_gather(l + 1)
             if side is not main:
                 main.wait_event(events[l % 2])
+            if mark:
+                mark("attn", main)
             self._attend(l, q_layers[l], scr[l % 2], main,
                          None if out_layers is None else out_layers[l])
+            if mark:
+                mark("attn_end", main)
+
+    # ---------------------------------------------------------------- appends
+    def append_tokens(self, layer: int, k_new: torch.Tensor, v_new: torch.Tensor, advance: bool,
+                      stream=None, err=None):
+        """Append one token per request (bf16 [B][Hkv][d]) to layer `layer`'s caches."""
+        lp, lh = layer % self.L_phys, layer % self.L_host
+        st = stream or torch.cuda.current_stream(self.device)
+        B.oasis_append_kv(self.shape, k_new, v_new, self.ctx, self.K[lp], self.host[lh], self.blk2slot[lp],
+                          self.k_pool[lp], self.v_pool[lp], advance,
+                          self.scratch.err if err is None else err, st)

@@ -503,3 +503,12 @@ def kv_request_torch(w: Workload, layer: int, b: int, device):
     K[:, : w.ctx[b]] = Kf.to(torch.bfloat16)
     V[:, : w.ctx[b]] = Vf.to(torch.bfloat16)
     return K, V
+
+
+def append_tokens(w: Workload, layer: int, step: int):
+    """Key/value rows (bf16 bits [B][Hkv][d]) appended at decode step `step`: N(0,1) draws."""
+    k = np.stack([np.stack([hash_normals(w.seed, STREAM_APPEND_K, layer, b, h, step * w.d, w.d)
+                            for h in range(w.Hkv)]) for b in range(w.B)])
+    v = np.stack([np.stack([hash_normals(w.seed, STREAM_APPEND_V, layer, b, h, step * w.d, w.d)
+                            for h in range(w.Hkv)]) for b in range(w.B)])
+    return f32_to_bf16_bits(k), f32_to_bf16_bits(v)

@@ -38,10 +38,16 @@ class Case:
         self.st = DecodeState(w, l_phys=1)
         self.st.fill_layer_numpy(0, K, V, self.b2s, self.s2b, self.lu)
 
-    def step(self, step, q=None, qla=None, C=None):
+    def step(self, step, q=None, qla=None, C=None, append=False):
         import torch
 
         w = self.w
+        if append:
+            kn, vn = syn.append_tokens(w, 0, step)
+            ref.append_token(self.K, self.host, self.kp, self.vp, self.b2s, w.ctx, kn, vn, bs=w.bs)
+            for b in range(w.B):
+                self.V[b, :, w.ctx[b] - 1] = vn[b]
+            self.st.append_tokens(0, _dev_bits(kn), _dev_bits(vn), advance=True)
         if q is None:
             q, qla = syn.layer_queries(w, 0, step)
         if C is not None:
@@ -89,3 +95,13 @@ class Case:
         _check_out(sc.out.cpu().numpy().astype(np.float64), r["out"], "attention")
 
 
+
+    def compare_caches(self):
+        """Keys in HBM and the whole host tier, bit for bit."""
+        import torch
+
+        kh = self.st.K[0].cpu().view(torch.int16).numpy().view(np.uint16)
+        np.testing.assert_array_equal(kh, self.K)
+        host = self.st.host[0].view(torch.int16).numpy().view(np.uint16)
+        np.testing.assert_array_equal(host, self.host)
+        np.testing.assert_array_equal(self.st.ctx.cpu().numpy(), np.array(self.w.ctx))

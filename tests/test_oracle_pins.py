@@ -354,3 +354,54 @@ def test_multistep_table_invariants():
             assert (b2s[b, h] >= 0).sum() == len(R1)
             for x in r["A"][(b, h)]:
                 assert lu[b, h, b2s[b, h, x]] == step
+
+
+# ---------------------------------------------------------------- token append
+def test_append_then_full_budget_attention_is_dense_over_the_new_context():
+    w = _small_workload(ctx=[333, 96], Kb=64, C=64, P=64, nb_max=24)
+    K, V, host, b2s, s2b, lu, kp, vp = _tiny_state(w)
+    ctx = list(w.ctx)
+    kn, vn = syn.append_tokens(w, 0, 0)
+    ref.append_token(K, host, kp, vp, b2s, ctx, kn, vn, bs=w.bs)
+    assert ctx == [334, 97]
+    for b in range(w.B):
+        t = ctx[b] - 1
+        assert (K[b, :, t] == kn[b]).all() and (V[b, :, t] == 0).all()   # V lives in the host tier
+        assert (host[b, :, t // 16, 0, t % 16] == kn[b]).all()
+        assert (host[b, :, t // 16, 1, t % 16] == vn[b]).all()
+        for h in range(w.Hkv):
+            p = b2s[b, h, t // 16]
+            if p >= 0:
+                assert (kp[b, h, p, t % 16] == kn[b, h]).all() and (vp[b, h, p, t % 16] == vn[b, h]).all()
+    V2 = V.copy()
+    for b in range(w.B):
+        V2[b, :, ctx[b] - 1] = vn[b]
+    q, qla = syn.layer_queries(w, 0, 0)
+    r = ref.layer_step(K, qla, q, ctx, host, kp, vp, b2s, s2b, lu, w.Kb, w.C, 1, bs=w.bs)
+    for b in range(w.B):
+        for hq in range(w.Hq):
+            h = hq // w.G
+            k = ref.bf16_to_f64(K[b, h, :ctx[b]])
+            v = ref.bf16_to_f64(V2[b, h, :ctx[b]])
+            dense = softmax(k @ ref.bf16_to_f64(q[b, hq]) / math.sqrt(w.d)) @ v
+            np.testing.assert_allclose(r["out"][b, hq], dense, rtol=1e-12, atol=1e-12)
+
+
+def test_append_to_a_full_cache_changes_nothing():
+    w = _small_workload(ctx=[64, 10], nb_max=4)
+    K, V, host, b2s, s2b, lu, kp, vp = _tiny_state(w)
+    ctx = list(w.ctx)
+    K0, host0 = K.copy(), host.copy()
+    kn, vn = syn.append_tokens(w, 0, 0)
+    ref.append_token(K, host, kp, vp, b2s, ctx, kn, vn, bs=w.bs)
+    assert ctx == [64, 11]
+    assert (K[0] == K0[0]).all() and (host[0] == host0[0]).all()
+
+
+def test_append_without_advance_keeps_the_length():
+    w = _small_workload(ctx=[40, 10])
+    K, V, host, b2s, s2b, lu, kp, vp = _tiny_state(w)
+    ctx = list(w.ctx)
+    kn, vn = syn.append_tokens(w, 0, 3)
+    ref.append_token(K, host, kp, vp, b2s, ctx, kn, vn, bs=w.bs, advance=False)
+    assert ctx == [40, 10] and (K[0, :, 40] == kn[0]).all()
