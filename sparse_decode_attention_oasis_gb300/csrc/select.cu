@@ -23,13 +23,13 @@
 //      (17 limbs of 32 bits, carries deferred in 64-bit shared-memory words)
 //      holds the sum with no rounding at all;
 //   3. U is merged into a running top-r set by exact comparison (a rank count
-//      over the union), 16 blocks at a time.
+//      over the union), kSelWarps blocks at a time.
 // The result equals the definition for every finite input.
 #include "common.cuh"
 
 namespace oasis {
 
-constexpr int kSelThreads = 512;
+constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kLimbs = 17;
 constexpr int kMaxN = 32;      // lookahead queries x GQA group
@@ -49,8 +49,11 @@ struct SelCtx {
   uint32_t* tmp;               // [kSelWarps][kLimbs]
   uint32_t* bval;              // [kSelWarps][kLimbs]
   int* bidx;                   // [kSelWarps]
-  uint32_t* tval;              // [kMaxR][kLimbs]
-  int* tidx;                   // [kMaxR]
+  uint32_t* tval;              // [Kb][kLimbs] running top-r set (exact values)
+  int* tidx;                   // [Kb]
+  uint32_t* tval2;             // [Kb][kLimbs] next top-r set
+  int* tidx2;                  // [Kb]
+  int* rank;                   // [Kb + kSelWarps]
   uint32_t* hist;              // [256]
   int* scal;                   // [8] scalars
   float* fscal;                // [kSelWarps]
@@ -292,12 +295,19 @@ __device__ void warp_exact_block_score(const SelCtx& c, int blk, uint32_t* out, 
 }
 
 // Mark (cls = 1) the r best of the uncertain candidates U[0..nU) by exact order;
-// cand_blk maps a candidate index to its block (nullptr = identity).
+// cand_blk maps a candidate index to its block (nullptr = identity).  The running
+// top-r set T (exact values, in rank order) is merged with each batch of
+// kSelWarps freshly scored blocks by counting, for every member of the union, how
+// many members rank before it; the r first go to the other buffer.
 __device__ void refine_top_r(SelCtx& c, const int* U, int nU, int r, const int* cand_blk,
                              uint8_t* cls) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   stage_queries(c);
   int tcount = 0;
+  uint32_t* tv = c.tval;
+  int* ti = c.tidx;
+  uint32_t* tv2 = c.tval2;
+  int* ti2 = c.tidx2;
   for (int base = 0; base < nU; base += kSelWarps) {
     const int nbat = min(kSelWarps, nU - base);
     if (warp < nbat) {
@@ -308,36 +318,38 @@ __device__ void refine_top_r(SelCtx& c, const int* U, int nU, int r, const int* 
     }
     __syncthreads();
     const int tot = tcount + nbat;
-    uint32_t mine[kLimbs];
-    int myidx = -1, rank = 0;
-    if ((int)threadIdx.x < tot) {
-      const uint32_t* src = threadIdx.x < (unsigned)tcount ? c.tval + threadIdx.x * kLimbs
-                                                            : c.bval + (threadIdx.x - tcount) * kLimbs;
-      myidx = threadIdx.x < (unsigned)tcount ? c.tidx[threadIdx.x] : c.bidx[threadIdx.x - tcount];
-#pragma unroll
-      for (int i = 0; i < kLimbs; ++i) mine[i] = src[i];
-      const int myblk = cand_blk ? cand_blk[myidx] : myidx;
+    for (int m = threadIdx.x; m < tot; m += blockDim.x) {
+      const uint32_t* mv = m < tcount ? tv + m * kLimbs : c.bval + (m - tcount) * kLimbs;
+      const int midx = m < tcount ? ti[m] : c.bidx[m - tcount];
+      const int mblk = cand_blk ? cand_blk[midx] : midx;
+      int rk = 0;
       for (int o = 0; o < tot; ++o) {
-        if (o == (int)threadIdx.x) continue;
-        const uint32_t* ov = o < tcount ? c.tval + o * kLimbs : c.bval + (o - tcount) * kLimbs;
-        const int oidx = o < tcount ? c.tidx[o] : c.bidx[o - tcount];
+        if (o == m) continue;
+        const uint32_t* ov = o < tcount ? tv + o * kLimbs : c.bval + (o - tcount) * kLimbs;
+        const int oidx = o < tcount ? ti[o] : c.bidx[o - tcount];
         const int oblk = cand_blk ? cand_blk[oidx] : oidx;
-        const int cmpv = exact_cmp(ov, mine);
-        if (cmpv > 0 || (cmpv == 0 && oblk < myblk)) ++rank;
+        const int cmpv = exact_cmp(ov, mv);
+        if (cmpv > 0 || (cmpv == 0 && oblk < mblk)) ++rk;
       }
+      c.rank[m] = rk;
     }
     __syncthreads();
-    if (myidx >= 0 && rank < r) {
+    for (int m = threadIdx.x; m < tot; m += blockDim.x) {
+      const int rk = c.rank[m];
+      if (rk >= r) continue;
+      const uint32_t* mv = m < tcount ? tv + m * kLimbs : c.bval + (m - tcount) * kLimbs;
 #pragma unroll
-      for (int i = 0; i < kLimbs; ++i) c.tval[rank * kLimbs + i] = mine[i];
-      c.tidx[rank] = myidx;
+      for (int i = 0; i < kLimbs; ++i) tv2[rk * kLimbs + i] = mv[i];
+      ti2[rk] = m < tcount ? ti[m] : c.bidx[m - tcount];
     }
     tcount = min(r, tot);
     __syncthreads();
+    uint32_t* sv = tv; tv = tv2; tv2 = sv;
+    int* si = ti; ti = ti2; ti2 = si;
   }
   for (int i = threadIdx.x; i < nU; i += blockDim.x) cls[U[i]] = 0;
   __syncthreads();
-  for (int i = threadIdx.x; i < tcount; i += blockDim.x) cls[c.tidx[i]] = 1;
+  for (int i = threadIdx.x; i < tcount; i += blockDim.x) cls[ti[i]] = 1;
   __syncthreads();
 }
 
@@ -386,12 +398,13 @@ __device__ void select_best(SelCtx& c, const float2* se, int n, int k, const int
 
 // ---------------------------------------------------------------- shared memory layout
 struct SelLayout {
-  size_t se, cls, U, cblk, kst, qf, qb, qn, lacc, tmp, bval, bidx, tval, tidx, hist, scal, fscal, red, total;
+  size_t se, cls, U, cblk, kst, qf, qb, qn, lacc, tmp, bval, bidx, tval, tidx, tval2, tidx2, rank, hist, scal,
+      fscal, red, total;
 };
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
-__host__ __device__ inline SelLayout sel_layout(int ncap, bool with_cblk) {
+__host__ __device__ inline SelLayout sel_layout(int ncap, bool with_cblk, int kb) {
   SelLayout L;
   size_t o = 0;
   L.se = o; o = align16(o + sizeof(float2) * ncap);
@@ -406,8 +419,11 @@ __host__ __device__ inline SelLayout sel_layout(int ncap, bool with_cblk) {
   L.tmp = o; o = align16(o + sizeof(uint32_t) * kSelWarps * kLimbs);
   L.bval = o; o = align16(o + sizeof(uint32_t) * kSelWarps * kLimbs);
   L.bidx = o; o = align16(o + sizeof(int) * kSelWarps);
-  L.tval = o; o = align16(o + sizeof(uint32_t) * kMaxR * kLimbs);
-  L.tidx = o; o = align16(o + sizeof(int) * kMaxR);
+  L.tval = o; o = align16(o + sizeof(uint32_t) * kb * kLimbs);
+  L.tidx = o; o = align16(o + sizeof(int) * kb);
+  L.tval2 = o; o = align16(o + sizeof(uint32_t) * kb * kLimbs);
+  L.tidx2 = o; o = align16(o + sizeof(int) * kb);
+  L.rank = o; o = align16(o + sizeof(int) * (kb + kSelWarps));
   L.hist = o; o = align16(o + sizeof(uint32_t) * 256);
   L.scal = o; o = align16(o + sizeof(int) * 8);
   L.fscal = o; o = align16(o + sizeof(float) * kSelWarps);
@@ -438,6 +454,9 @@ __device__ SelCtx make_ctx(char* sm, const SelLayout& L, const Shape& s, const u
   c.bidx = reinterpret_cast<int*>(sm + L.bidx);
   c.tval = reinterpret_cast<uint32_t*>(sm + L.tval);
   c.tidx = reinterpret_cast<int*>(sm + L.tidx);
+  c.tval2 = reinterpret_cast<uint32_t*>(sm + L.tval2);
+  c.tidx2 = reinterpret_cast<int*>(sm + L.tidx2);
+  c.rank = reinterpret_cast<int*>(sm + L.rank);
   c.hist = reinterpret_cast<uint32_t*>(sm + L.hist);
   c.scal = reinterpret_cast<int*>(sm + L.scal);
   c.fscal = reinterpret_cast<float*>(sm + L.fscal);
@@ -445,12 +464,12 @@ __device__ SelCtx make_ctx(char* sm, const SelLayout& L, const Shape& s, const u
 }
 
 // ---------------------------------------------------------------- a2 kernel
-__global__ void __launch_bounds__(kSelThreads, 1)
+__global__ void __launch_bounds__(kSelThreads, 2)
 topk_select_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __restrict__ k_hbm,
                    const uint16_t* __restrict__ q_la, const int* __restrict__ ctx_len,
                    int* __restrict__ sel, int* __restrict__ nsel) {
   extern __shared__ __align__(16) char sm[];
-  const SelLayout L = sel_layout(s.nb_max, false);
+  const SelLayout L = sel_layout(s.nb_max, false, s.Kb);
   const int head = blockIdx.x;
   const int b = head / s.Hkv;
   const int ctx = ctx_len[b];
@@ -488,14 +507,14 @@ topk_select_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* _
 }
 
 // ---------------------------------------------------------------- a3 kernel
-__global__ void __launch_bounds__(kSelThreads, 1)
+__global__ void __launch_bounds__(kSelThreads, 2)
 fetch_diff_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __restrict__ k_hbm,
                   const uint16_t* __restrict__ q_la, const int* __restrict__ ctx_len,
                   const int* __restrict__ sel, const int* __restrict__ nsel,
                   const int* __restrict__ blk2slot, int cap, int* __restrict__ fetch,
                   int* __restrict__ nfetch) {
   extern __shared__ __align__(16) char sm[];
-  const SelLayout L = sel_layout(s.Kb, true);
+  const SelLayout L = sel_layout(s.Kb, true, s.Kb);
   const int head = blockIdx.x;
   const int b = head / s.Hkv;
   const int ctx = ctx_len[b];
@@ -509,7 +528,7 @@ fetch_diff_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __
   ns = ns < 0 ? 0 : (ns > s.Kb ? s.Kb : ns);
   const int* S = sel + (long long)head * s.Kb;
   const int* b2s = blk2slot + (long long)head * s.nb_max;
-  // missing blocks of S, in S order (ascending); one entry per thread (ns <= Kb <= 512)
+  // missing blocks of S, in S order (ascending); one entry per thread (ns <= Kb <= 256)
   int x = -1, miss = 0;
   if ((int)threadIdx.x < ns) {
     x = S[threadIdx.x];
@@ -534,8 +553,8 @@ fetch_diff_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __
 }
 
 // ---------------------------------------------------------------- launchers
-size_t topk_smem_bytes(const Shape& s) { return sel_layout(s.nb_max, false).total; }
-size_t diff_smem_bytes(const Shape& s) { return sel_layout(s.Kb, true).total; }
+size_t topk_smem_bytes(const Shape& s) { return sel_layout(s.nb_max, false, s.Kb).total; }
+size_t diff_smem_bytes(const Shape& s) { return sel_layout(s.Kb, true, s.Kb).total; }
 
 cudaError_t launch_topk_select(const Shape& s, const float2* scores, const uint16_t* k,
                                const uint16_t* q_la, const int* ctx, int* sel, int* nsel,
