@@ -256,6 +256,35 @@ OASIS_API oasis_status oasis_append_kv(const oasis_shape* shape, const void* k_n
 /* Bytes of device workspace oasis_sparse_decode_attn needs for `shape` (0 on a bad shape). */
 OASIS_API size_t oasis_attn_workspace_bytes(const oasis_shape* shape);
 
+/*
+ * Allocation-free attention.  The pages have no counterpart: this is a calling
+ * convenience of this library, not a step of the method.
+ *
+ * Same operation, arguments, output and error behaviour as
+ * oasis_sparse_decode_attn, minus the workspace: the split-K scratch lives in a
+ * device array built into the library (OASIS_ATTN_NOALLOC_MAX_WORKSPACE_BYTES
+ * on every GPU that loads it, held until the process exits).  It is for callers
+ * that cannot allocate device memory when they call - a serving loop whose
+ * device-memory budget is fixed at start-up, or host code that must not call
+ * cudaMalloc on its decode path because that call can block on the device.
+ *   - It allocates nothing: no cudaMalloc/cudaFree or allocating library call.
+ *   - The first call on a device looks up the array's device address once for
+ *     that device (cudaGetSymbolAddress, with the device current); make that
+ *     first call before any stream capture.
+ *   - Shapes whose scratch (oasis_attn_workspace_bytes) exceeds the array are
+ *     rejected with OASIS_ERR_UNSUPPORTED and a message in oasis_last_error().
+ *   - Every call on a device shares the one array, whose contents persist
+ *     between calls; two calls whose kernels overlap on the GPU (different
+ *     streams without ordering) race on it and produce wrong outputs.  Order
+ *     such calls, or use oasis_sparse_decode_attn with separate workspaces.
+ */
+#define OASIS_ATTN_NOALLOC_MAX_WORKSPACE_BYTES (8u << 20)
+OASIS_API oasis_status oasis_sparse_decode_attn_noalloc(const oasis_shape* shape, const void* q,
+                                                        const void* k_pool, const void* v_pool,
+                                                        const int32_t* sel, const int32_t* nsel,
+                                                        const int32_t* blk2slot, const int32_t* ctx_len,
+                                                        float scale, float* out, oasis_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

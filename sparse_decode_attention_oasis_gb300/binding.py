@@ -59,6 +59,8 @@ _SIGS = {
     "oasis_sparse_decode_attn": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                   ctypes.c_float, _VP, ctypes.c_size_t, _VP, _VP], ctypes.c_int),
     "oasis_attn_workspace_bytes": ([ctypes.POINTER(Shape)], ctypes.c_size_t),
+    "oasis_sparse_decode_attn_noalloc": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                          ctypes.c_float, _VP, _VP], ctypes.c_int),
     "oasis_append_kv": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_int32,
                          _VP, _VP], ctypes.c_int),
 }
@@ -159,3 +161,11 @@ def oasis_append_kv(shape: Shape, k_new, v_new, ctx_len, k_hbm, host_kv, blk2slo
     _check("oasis_append_kv", load().oasis_append_kv(
         ctypes.byref(shape), _ptr(k_new), _ptr(v_new), _ptr(ctx_len), _ptr(k_hbm), _ptr(host_kv),
         _ptr(blk2slot), _ptr(k_pool), _ptr(v_pool), 1 if advance else 0, _ptr(err_word), _stream(stream)))
+
+
+def oasis_sparse_decode_attn_noalloc(shape: Shape, q, k_pool, v_pool, sel, nsel, blk2slot, ctx_len,
+                                     scale: float, out, stream=None):
+    """Attention with the library's built-in device scratch instead of a workspace."""
+    _check("oasis_sparse_decode_attn_noalloc", load().oasis_sparse_decode_attn_noalloc(
+        ctypes.byref(shape), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(sel), _ptr(nsel),
+        _ptr(blk2slot), _ptr(ctx_len), float(scale), _ptr(out), _stream(stream)))

@@ -61,6 +61,15 @@ oasis_status check_shape(const oasis_shape* sh, const char* fn, oasis::Shape* ou
   return OASIS_OK;
 }
 
+}  // namespace
+
+namespace oasis {
+// Record the message oasis_last_error() returns on this thread.
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+}  // namespace oasis
+
+namespace {
+
 #define REQUIRE(cond, msg) \
   do { if (!(cond)) return fail(OASIS_ERR_INVALID, fn, msg); } while (0)
 
