@@ -183,15 +183,22 @@ class ClockSampler:
 
 # --------------------------------------------------------------------------- helpers
 class KernelMarks:
-    """CUDA events recorded before/after each kernel of the decode step, per stream."""
+    """CUDA events recorded before/after each kernel of the decode step, per stream.
 
-    def __init__(self, n):
+    ``names`` limits the marks recorded (the timed region records only the two
+    around the scoring kernel, so the measurement barely perturbs the schedule).
+    """
+
+    def __init__(self, n, names=None):
         import torch
 
         self.pool = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
         self.used = []
+        self.names = names
 
     def __call__(self, name, stream):
+        if self.names is not None and name not in self.names:
+            return
         ev = self.pool[len(self.used)]
         ev.record(stream)
         self.used.append((name, stream, ev))
@@ -367,7 +374,7 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     errw = int(st.scratch.err.item()) | int(st.scratch2.err.item())
 
-    marks = KernelMarks(L * args.steps * 8 + 16)
+    marks = KernelMarks(L * args.steps * 2 + 16, names={"score", "topk"})
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local_rank)
     if world > 1:
@@ -376,16 +383,35 @@ def run_gpu(args, rank, world, local_rank):
     clocks.start()
     time.sleep(0.3)
     ev0.record(main)
+    issue_s = 0.0
     for k in range(args.steps):
+        t_issue = time.perf_counter()
         step(args.warmup + k, marks)
+        issue_s += time.perf_counter() - t_issue
     ev1.record(main)
     torch.cuda.synchronize()
     clk = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
     ms = reduce_max(ev0.elapsed_time(ev1), world, dev)
-    kernel_ms = marks.durations()
-    score_ms = kernel_ms["score"]
+    score_ms = marks.durations()["score"]
+
+    # per-kernel device time on a single stream (untimed pass, every kernel bracketed)
+    iso = KernelMarks(L * 3 * 8 + 16)
+    for k in range(3):
+        st.decode_step(args.warmup + k, qla_dev[args.warmup + k], q_dev[args.warmup + k], out_layers=out_dev,
+                       main=main, side=main, mark=iso)
+    torch.cuda.synchronize()
+    kernel_ms = iso.durations()
+    # the same steps with everything on one stream, timed as a whole
+    e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_a.record(main)
+    for k in range(3):
+        st.decode_step(args.warmup + k, qla_dev[args.warmup + k], q_dev[args.warmup + k], out_layers=out_dev,
+                       main=main, side=main)
+    e_b.record(main)
+    torch.cuda.synchronize()
+    single_stream_ms = e_a.elapsed_time(e_b) / 3
 
     # end to end: H2D of the step's queries, the C-ABI calls, D2H of the outputs
     e2e = None
@@ -431,7 +457,9 @@ def run_gpu(args, rank, world, local_rank):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": score_traffic_per_launch(), "bytes_per_launch": ab["score"],
                      "avg_launch_ms": score_avg_ms},
-        "kernel_avg_us": {k: round(1000.0 * sum(v) / len(v), 2) for k, v in kernel_ms.items() if v},
+        "kernel_avg_us_single_stream": {k: round(1000.0 * sum(v) / len(v), 2) for k, v in kernel_ms.items() if v},
+        "ms_per_step_single_stream": single_stream_ms,
+        "host_issue_ms_per_step": 1000.0 * issue_s / args.steps,
         "gpu_launches": 6 * L * args.steps,
         "clocks": clk,
         "e2e": e2e,

@@ -89,4 +89,34 @@ __device__ __forceinline__ float key_float(uint32_t k) {
   return __uint_as_float(u);
 }
 
+// Host-side caches so that a launch costs no more than the launch itself.
+constexpr int kMaxDevicesCached = 64;
+
+inline int current_device() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return dev < 0 || dev >= kMaxDevicesCached ? 0 : dev;
+}
+
+inline int sm_count() {
+  static int cached[kMaxDevicesCached] = {};
+  const int dev = current_device();
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
+}
+
+// Raise a kernel's dynamic shared-memory limit once per device (and when a larger
+// size is needed); `cache` is that kernel's per-device record.
+inline cudaError_t ensure_dyn_smem(const void* fn, size_t bytes, int* cache) {
+  const int dev = current_device();
+  if (cache[dev] >= (int)bytes) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) cache[dev] = (int)bytes;
+  return e;
+}
+
 }  // namespace oasis

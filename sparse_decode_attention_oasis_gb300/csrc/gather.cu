@@ -205,7 +205,8 @@ cudaError_t launch_gather_h2d(const Shape& s, const uint16_t* host_kv, const int
                               unsigned* err, cudaStream_t stream) {
   const size_t smem = gather_smem_bytes(s);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(gather_h2d_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static int attr_cache[kMaxDevicesCached] = {};
+    cudaError_t e = ensure_dyn_smem((const void*)gather_h2d_kernel, smem, attr_cache);
     if (e != cudaSuccess) return e;
   }
   gather_h2d_kernel<<<s.B * s.Hkv, kGatherThreads, smem, stream>>>(s, host_kv, sel, nsel, fetch, nfetch,

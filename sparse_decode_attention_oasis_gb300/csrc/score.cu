@@ -198,18 +198,21 @@ cudaError_t launch_score_blocks(const Shape& s, const uint16_t* k, const int* ct
 }
 
 int score_grid_limit(int nt) {
-  int dev = 0, sms = 0, per_sm = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int threads = kScoreWarps * 32;
-  switch (nt) {
-    case 1: cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_blocks_kernel<1>, threads, 0); break;
-    case 2: cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_blocks_kernel<2>, threads, 0); break;
-    case 3: cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_blocks_kernel<3>, threads, 0); break;
-    default: cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_blocks_kernel<4>, threads, 0); break;
+  static int per_sm_cached[kMaxDevicesCached][5] = {};
+  const int dev = current_device();
+  int& per_sm = per_sm_cached[dev][nt];
+  if (!per_sm) {
+    const int threads = kScoreWarps * 32;
+    int v = 0;
+    switch (nt) {
+      case 1: cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, score_blocks_kernel<1>, threads, 0); break;
+      case 2: cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, score_blocks_kernel<2>, threads, 0); break;
+      case 3: cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, score_blocks_kernel<3>, threads, 0); break;
+      default: cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, score_blocks_kernel<4>, threads, 0); break;
+    }
+    per_sm = v < 1 ? 1 : v;
   }
-  if (per_sm < 1) per_sm = 1;
-  return sms * per_sm;
+  return sm_count() * per_sm;
 }
 
 }  // namespace oasis

@@ -403,12 +403,10 @@ cudaError_t launch_score_blocks_tc(const Shape& s, const uint16_t* k, const int*
   }
   const int tiles_per_head = (s.nb_max + 7) / 8;
   const int total = s.B * s.Hkv * tiles_per_head;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = sm_count();
   const int grid = total < sms ? total : sms;
-  cudaError_t e = cudaFuncSetAttribute(score_blocks_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemBytes);
+  static int attr_cache[kMaxDevicesCached] = {};
+  cudaError_t e = ensure_dyn_smem((const void*)score_blocks_tc_kernel, kSmemBytes, attr_cache);
   if (e != cudaSuccess) return e;
   score_blocks_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mk, mq, s, ctx, scores, err, tiles_per_head,
                                                                  total, npad, 1.0f / sqrtf((float)s.d));

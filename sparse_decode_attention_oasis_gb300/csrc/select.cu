@@ -149,9 +149,15 @@ __device__ uint32_t kth_largest_key(const float2* se, int n, int k, uint32_t* hi
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0u;
     __syncthreads();
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      const uint32_t key = float_key(se[i].x);
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    // warp-aggregated counting: scores share their leading bits, so most lanes of
+    // a warp hit the same bin; one atomic per distinct bin per warp
+    const int n_pad = (n + 31) & ~31;
+    for (int i = threadIdx.x; i < n_pad; i += blockDim.x) {
+      const uint32_t key = i < n ? float_key(se[i].x) : 0u;
+      const bool take = i < n && (key & mask) == prefix;
+      const uint32_t bin = take ? ((key >> shift) & 255u) : 256u;
+      const unsigned peers = __match_any_sync(0xffffffffu, bin);
+      if (take && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
     }
     __syncthreads();
     if (threadIdx.x < 32) {
@@ -559,8 +565,9 @@ size_t diff_smem_bytes(const Shape& s) { return sel_layout(s.Kb, true, s.Kb).tot
 cudaError_t launch_topk_select(const Shape& s, const float2* scores, const uint16_t* k,
                                const uint16_t* q_la, const int* ctx, int* sel, int* nsel,
                                cudaStream_t stream) {
+  static int attr_cache[kMaxDevicesCached] = {};
   const size_t smem = topk_smem_bytes(s);
-  cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_dyn_smem((const void*)topk_select_kernel, smem, attr_cache);
   if (e != cudaSuccess) return e;
   topk_select_kernel<<<s.B * s.Hkv, kSelThreads, smem, stream>>>(s, scores, k, q_la, ctx, sel, nsel);
   return cudaGetLastError();
@@ -570,8 +577,9 @@ cudaError_t launch_fetch_diff(const Shape& s, const float2* scores, const uint16
                               const uint16_t* q_la, const int* ctx, const int* sel,
                               const int* nsel, const int* blk2slot, int cap, int* fetch,
                               int* nfetch, cudaStream_t stream) {
+  static int attr_cache[kMaxDevicesCached] = {};
   const size_t smem = diff_smem_bytes(s);
-  cudaError_t e = cudaFuncSetAttribute(fetch_diff_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_dyn_smem((const void*)fetch_diff_kernel, smem, attr_cache);
   if (e != cudaSuccess) return e;
   fetch_diff_kernel<<<s.B * s.Hkv, kSelThreads, smem, stream>>>(s, scores, k, q_la, ctx, sel, nsel,
                                                                blk2slot, cap, fetch, nfetch);

@@ -72,6 +72,14 @@ class DecodeState:
         self.scratch = LayerScratch(s, dev)
         self.scratch2 = None
         self.scale = 1.0 / math.sqrt(w.d)
+        # per-layer views made once (indexing a tensor costs host time on every call)
+        self.Kl = [self.K[l] for l in range(Lp)]
+        self.kpl = [self.k_pool[l] for l in range(Lp)]
+        self.vpl = [self.v_pool[l] for l in range(Lp)]
+        self.b2sl = [self.blk2slot[l] for l in range(Lp)]
+        self.s2bl = [self.slot2blk[l] for l in range(Lp)]
+        self.lul = [self.last_used[l] for l in range(Lp)]
+        self.hostl = [self.host[l] for l in range(self.L_host)]
 
     # ---------------------------------------------------------------- filling
     def fill_layer_numpy(self, layer: int, K_bits: np.ndarray, V_bits: np.ndarray,
@@ -178,7 +186,7 @@ class DecodeState:
     def _select(self, layer, q_la, step, sc, st, mark=None):
         s = self.shape
         lp = layer % self.L_phys
-        K = self.K[lp]
+        K = self.Kl[lp]
         if mark:
             mark("score", st)
         B.oasis_score_blocks(s, K, self.ctx, q_la, sc.scores, sc.err, st)
@@ -188,22 +196,21 @@ class DecodeState:
         if mark:
             mark("diff", st)
         B.oasis_fetch_diff_capped(s, sc.scores, K, q_la, self.ctx, sc.sel, sc.nsel,
-                                  self.blk2slot[lp], self.w.C, sc.fetch, sc.nfetch, st)
+                                  self.b2sl[lp], self.w.C, sc.fetch, sc.nfetch, st)
         if mark:
             mark("end", st)
 
     def _gather(self, layer, step, sc, gs):
         s = self.shape
         lp, lh = layer % self.L_phys, layer % self.L_host
-        B.oasis_gather_h2d(s, self.host[lh], sc.sel, sc.nsel, sc.fetch, sc.nfetch, self.blk2slot[lp],
-                           self.slot2blk[lp], self.last_used[lp], step, self.k_pool[lp],
-                           self.v_pool[lp], sc.err, gs)
+        B.oasis_gather_h2d(s, self.hostl[lh], sc.sel, sc.nsel, sc.fetch, sc.nfetch, self.b2sl[lp],
+                           self.s2bl[lp], self.lul[lp], step, self.kpl[lp], self.vpl[lp], sc.err, gs)
 
     def _attend(self, layer, q, sc, st, out=None):
         s = self.shape
         lp = layer % self.L_phys
-        B.oasis_sparse_decode_attn(s, q, self.k_pool[lp], self.v_pool[lp], sc.sel, sc.nsel,
-                                   self.blk2slot[lp], self.ctx, self.scale, sc.ws, sc.ws_bytes,
+        B.oasis_sparse_decode_attn(s, q, self.kpl[lp], self.vpl[lp], sc.sel, sc.nsel, self.b2sl[lp],
+                                   self.ctx, self.scale, sc.ws, sc.ws_bytes,
                                    sc.out if out is None else out, st)
 
     def decode_step(self, step: int, q_la_layers, q_layers, out_layers=None, main=None, side=None,
