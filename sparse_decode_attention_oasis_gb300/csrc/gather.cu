@@ -14,7 +14,10 @@
 //   3. last_used = step for every resident block of S;
 //   4. the 8 KiB (K 4 KiB + V 4 KiB) of every fetched block is read from mapped
 //      page-locked host memory with 16-byte loads (several in flight per thread)
-//      and written to its slot.  The copy is bound by the host link.
+//      and written to its slot.  The first round of host reads is issued right
+//      after the fetch list arrives, before the slot bookkeeping, so the link's
+//      latency overlaps it; all table reads happen in one round of loads and the
+//      LRU clock is set from shared memory.  The copy is bound by the host link.
 // Out-of-range indices set bits of the error word and are skipped.
 #include "common.cuh"
 
@@ -44,38 +47,51 @@ gather_h2d_kernel(Shape s, const uint16_t* __restrict__ host_kv, const int* __re
   int* F = S + Kb;           // [Kb]
   int* s2b = F + Kb;         // [P]
   int* lu = s2b + P;         // [P]
-  int* cand = lu + P;        // [P]
-  int* src = cand + P;       // [Kb] fetched block per copy
-  int* dst = src + Kb;       // [Kb] slot per copy
-  int* scal = dst + Kb;      // [4]
+  int* cand = lu + P;        // [P]  slot of the i-th candidate, later class per slot
+  int* ins = cand + P;       // [P]  1 if the slot's block is in S
+  int* scal = ins + P;       // [4]
   const int head = blockIdx.x;
   const long long tb = (long long)head * s.nb_max;
   const long long ts = (long long)head * P;
+  constexpr int kUnits = 2 * kBS * kD * 2 / 16;  // 16-byte pieces per block (K then V): 512
   unsigned ew = 0;
 
+  // one round of independent loads: counts, lists, slot tables
   int ns = nsel[head], nf = nfetch[head];
-  if (ns < 0 || ns > Kb) { ew |= OASIS_EW_BAD_COUNT; ns = ns < 0 ? 0 : Kb; }
-  if (nf < 0 || nf > Kb) { ew |= OASIS_EW_BAD_COUNT; nf = nf < 0 ? 0 : Kb; }
-  for (int i = threadIdx.x; i < ns; i += blockDim.x) {
-    int x = sel[(long long)head * Kb + i];
-    if (x < 0 || x >= s.nb_max) { ew |= OASIS_EW_BAD_BLOCK; x = -1; }
-    S[i] = x;
-  }
-  for (int i = threadIdx.x; i < nf; i += blockDim.x) {
-    int x = fetch[(long long)head * Kb + i];
-    if (x < 0 || x >= s.nb_max) { ew |= OASIS_EW_BAD_BLOCK; x = -1; }
-    F[i] = x;
+  for (int i = threadIdx.x; i < Kb; i += blockDim.x) {
+    S[i] = sel[(long long)head * Kb + i];
+    F[i] = fetch[(long long)head * Kb + i];
   }
   for (int p = threadIdx.x; p < P; p += blockDim.x) {
-    int o = slot2blk[ts + p];
-    if (o >= s.nb_max || o < -1) { ew |= OASIS_EW_BAD_BLOCK; o = -1; }
-    s2b[p] = o;
+    s2b[p] = slot2blk[ts + p];
     lu[p] = last_used[ts + p];
   }
+  if (ns < 0 || ns > Kb) { ew |= OASIS_EW_BAD_COUNT; ns = ns < 0 ? 0 : Kb; }
+  if (nf < 0 || nf > Kb) { ew |= OASIS_EW_BAD_COUNT; nf = nf < 0 ? 0 : Kb; }
   if (threadIdx.x == 0) { scal[0] = 0; scal[1] = 0; }
   __syncthreads();
+  for (int i = threadIdx.x; i < Kb; i += blockDim.x) {
+    if (i < ns && (S[i] < 0 || S[i] >= s.nb_max)) { ew |= OASIS_EW_BAD_BLOCK; S[i] = -1; }
+    if (i < nf && (F[i] < 0 || F[i] >= s.nb_max)) { ew |= OASIS_EW_BAD_BLOCK; F[i] = -1; }
+  }
+  for (int p = threadIdx.x; p < P; p += blockDim.x)
+    if (s2b[p] >= s.nb_max || s2b[p] < -1) { ew |= OASIS_EW_BAD_BLOCK; s2b[p] = -1; }
+  __syncthreads();
 
-  // 1. candidate ranks
+  // start the first round of host reads now, so the link latency overlaps the table work
+  const int total = nf * kUnits;
+  uint4 pre[kGatherUnroll];
+#pragma unroll
+  for (int u = 0; u < kGatherUnroll; ++u) {
+    const int id = threadIdx.x + u * blockDim.x;
+    if (id < total) {
+      const int i = id / kUnits, w = id - i * kUnits;
+      const int x = F[i];
+      if (x >= 0) pre[u] = ld_host16(host_kv + ((tb + x) * 2 * kBS * kD) + (long long)w * 8);
+    }
+  }
+
+  // 1. classes and candidate ranks: free slots ascending, then victims by (last_used, block)
   for (int p = threadIdx.x; p < P; p += blockDim.x) {
     const int o = s2b[p];
     bool in_s = false;
@@ -88,116 +104,109 @@ gather_h2d_kernel(Shape s, const uint16_t* __restrict__ host_kv, const int* __re
         if (v < o) lo = mid + 1; else hi = mid - 1;
       }
     }
-    const bool is_free = o < 0;
-    if (is_free) atomicAdd(&scal[0], 1);
+    ins[p] = in_s ? 1 : 0;
+    cand[p] = -1;
+    if (o < 0) atomicAdd(&scal[0], 1);
     else if (!in_s) atomicAdd(&scal[1], 1);
-    cand[p] = is_free ? 0 : (in_s ? -1 : 1);  // provisional class, ranks below
   }
   __syncthreads();
   const int nfree = scal[0], nvict = scal[1];
   int myrank[(1024 + kGatherThreads - 1) / kGatherThreads];
   int k = 0;
   for (int p = threadIdx.x; p < P; p += blockDim.x, ++k) {
-    const int cl = cand[p];
+    const int o = s2b[p];
     int r = -1;
-    if (cl == 0) {
+    if (o < 0) {
       r = 0;
-      for (int q = 0; q < p; ++q) r += (cand[q] == 0);
-    } else if (cl == 1) {
+      for (int q = 0; q < p; ++q) r += (s2b[q] < 0);
+    } else if (!ins[p]) {
       r = nfree;
-      const int lp = lu[p], op = s2b[p];
+      const int lp = lu[p];
       for (int q = 0; q < P; ++q) {
-        if (cand[q] != 1 || q == p) continue;
-        const int lq = lu[q], oq = s2b[q];
-        r += (lq < lp) || (lq == lp && oq < op);
+        const int oq = s2b[q];
+        if (oq < 0 || ins[q] || q == p) continue;
+        const int lq = lu[q];
+        r += (lq < lp) || (lq == lp && oq < o);
       }
     }
     myrank[k] = r;
   }
   __syncthreads();
   k = 0;
-  for (int p = threadIdx.x; p < P; p += blockDim.x, ++k) cand[p] = -1;
-  __syncthreads();
-  k = 0;
   for (int p = threadIdx.x; p < P; p += blockDim.x, ++k)
-    if (myrank[k] >= 0) cand[myrank[k]] = p;
+    if (myrank[k] >= 0 && myrank[k] < P) cand[myrank[k]] = p;
   __syncthreads();
 
-  // 2. assignment: evictions, then new mappings
+  // 2. assignment: evict, map, LRU clock (all from shared memory)
   const int ncand = nfree + nvict;
-  int ncopy = nf < ncand ? nf : ncand;
-  if (nf > ncand && threadIdx.x == 0) ew |= OASIS_EW_NO_SLOT;
+  const int ncopy = nf < ncand ? nf : ncand;
+  if (nf > ncand) ew |= OASIS_EW_NO_SLOT;
   for (int i = threadIdx.x; i < ncopy; i += blockDim.x) {
     const int p = cand[i];
-    if (p < 0 || p >= P) continue;
+    if (p < 0) { ew |= OASIS_EW_BAD_SLOT; continue; }  // duplicate entries in slot2blk
     const int old = s2b[p];
     if (old >= 0) blk2slot[tb + old] = -1;
   }
   __syncthreads();
   for (int i = threadIdx.x; i < ncopy; i += blockDim.x) {
     const int p = cand[i];
-    int x = F[i];
-    if (p < 0 || p >= P) { ew |= OASIS_EW_BAD_SLOT; src[i] = -1; dst[i] = 0; continue; }
-    src[i] = x;
-    dst[i] = p;
+    const int x = F[i];
+    if (p < 0) continue;
     if (x >= 0) {
       blk2slot[tb + x] = p;
       s2b[p] = x;
+      lu[p] = step;
     } else {
-      s2b[p] = s2b[p] >= 0 ? -1 : s2b[p];  // a bad entry frees nothing it did not evict
+      s2b[p] = -1;
     }
   }
-  __syncthreads();
-
-  // 3. LRU clock of the attended blocks
-  for (int i = threadIdx.x; i < ns; i += blockDim.x) {
-    const int x = S[i];
-    if (x < 0) continue;
-    const int p = blk2slot[tb + x];
-    if (p >= P) { ew |= OASIS_EW_BAD_SLOT; continue; }
-    if (p >= 0) lu[p] = step;
-  }
+  for (int p = threadIdx.x; p < P; p += blockDim.x)
+    if (ins[p]) lu[p] = step;
   __syncthreads();
   for (int p = threadIdx.x; p < P; p += blockDim.x) {
     slot2blk[ts + p] = s2b[p];
     last_used[ts + p] = lu[p];
   }
 
-  // 4. copy host tier -> slots (16-byte units: 256 per K block, 256 per V block)
-  constexpr int kUnits = 2 * kBS * kD * 2 / 16;  // 512 per block (K then V)
-  const int total = ncopy * kUnits;
-  for (int base = threadIdx.x; base < total; base += blockDim.x * kGatherUnroll) {
+  // 3. copies: first the prefetched round, then the rest in rounds of kGatherUnroll
+#pragma unroll
+  for (int u = 0; u < kGatherUnroll; ++u) {
+    const int id = threadIdx.x + u * blockDim.x;
+    if (id < total) {
+      const int i = id / kUnits, w = id - i * kUnits;
+      if (i < ncopy && F[i] >= 0 && cand[i] >= 0) {
+        uint16_t* to = ((w >> 8) ? v_pool : k_pool) + ((ts + cand[i]) * kBS * kD) + (long long)(w & 255) * 8;
+        *reinterpret_cast<uint4*>(to) = pre[u];
+      }
+    }
+  }
+  for (int base = threadIdx.x + kGatherUnroll * blockDim.x; base < total; base += blockDim.x * kGatherUnroll) {
     uint4 v[kGatherUnroll];
-    int tgt[kGatherUnroll];
 #pragma unroll
     for (int u = 0; u < kGatherUnroll; ++u) {
       const int id = base + u * blockDim.x;
-      tgt[u] = -1;
       if (id < total) {
         const int i = id / kUnits, w = id - i * kUnits;
-        const int x = src[i];
-        if (x >= 0) {
-          const uint16_t* from = host_kv + ((tb + x) * 2 * kBS * kD) + (long long)w * 8;
-          v[u] = ld_host16(from);
-          tgt[u] = id;
-        }
+        const int x = F[i];
+        if (x >= 0) v[u] = ld_host16(host_kv + ((tb + x) * 2 * kBS * kD) + (long long)w * 8);
       }
     }
 #pragma unroll
     for (int u = 0; u < kGatherUnroll; ++u) {
-      if (tgt[u] < 0) continue;
-      const int id = tgt[u];
-      const int i = id / kUnits, w = id - i * kUnits;
-      const int p = dst[i];
-      const int half = w >> 8;  // 0: K, 1: V
-      uint16_t* to = (half ? v_pool : k_pool) + ((ts + p) * kBS * kD) + (long long)(w & 255) * 8;
-      *reinterpret_cast<uint4*>(to) = v[u];
+      const int id = base + u * blockDim.x;
+      if (id < total) {
+        const int i = id / kUnits, w = id - i * kUnits;
+        if (i < ncopy && F[i] >= 0 && cand[i] >= 0) {
+          uint16_t* to = ((w >> 8) ? v_pool : k_pool) + ((ts + cand[i]) * kBS * kD) + (long long)(w & 255) * 8;
+          *reinterpret_cast<uint4*>(to) = v[u];
+        }
+      }
     }
   }
   if (ew) atomicOr(err, ew);
 }
 
-size_t gather_smem_bytes(const Shape& s) { return sizeof(int) * (4 * (size_t)s.Kb + 3 * (size_t)s.P + 4); }
+size_t gather_smem_bytes(const Shape& s) { return sizeof(int) * (2 * (size_t)s.Kb + 4 * (size_t)s.P + 4); }
 
 cudaError_t launch_gather_h2d(const Shape& s, const uint16_t* host_kv, const int* sel, const int* nsel,
                               const int* fetch, const int* nfetch, int* blk2slot, int* slot2blk,
