@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--ctx", type=int, default=32768)
     ap.add_argument("--host-layers", type=int, default=0,
                     help="physical host-tier layers (0 = all layers if host memory allows)")
+    ap.add_argument("--preroll", type=int, default=40,
+                    help="untimed decode steps run first, so the timed steps see a warmed-up resident set")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-worker", type=int, default=0, help=argparse.SUPPRESS)
@@ -260,13 +262,18 @@ def score_traffic_per_launch():
     return d.get("bytes_per_launch_full")
 
 
-def algorithmic_bytes(w):
-    """Algorithmic HBM bytes of one layer-step, split by kernel."""
+def algorithmic_bytes(w, attended_per_head=None):
+    """Algorithmic HBM bytes of one layer-step, split by kernel.
+
+    Attention reads the K and V of the attended blocks: ``attended_per_head``
+    (measured) or, if not given, the full budget Kb.
+    """
     H = w.B * w.Hkv
     ctx_blocks = sum(w.nb(b) for b in range(w.B)) * w.Hkv
     score = ctx_blocks * w.bs * w.d * 2 + w.B * w.n_la * w.Hq * w.d * 2 + ctx_blocks * 8
     topk = ctx_blocks * 8 + H * (w.Kb + 1) * 4
-    attn = H * w.Kb * w.bs * w.d * 2 * 2 + w.B * w.Hq * w.d * (2 + 4)
+    na = w.Kb if attended_per_head is None else attended_per_head
+    attn = int(H * na * w.bs * w.d * 2 * 2) + w.B * w.Hq * w.d * (2 + 4)
     gather_hbm = H * w.C * w.bs * w.d * 2 * 2
     return {"score": score, "topk": topk, "attn": attn, "gather_hbm": gather_hbm,
             "total": score + topk + attn + gather_hbm}
@@ -349,17 +356,20 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     gen_s = time.time() - t0
 
-    nsteps = args.warmup + args.steps
-    qs = [syn.QueryStream(w, l) for l in range(L)]
-    q_host = torch.empty((nsteps, L, w.B, w.Hq, w.d), dtype=torch.bfloat16, pin_memory=True)
-    qla_host = torch.empty((nsteps, L, w.B, w.n_la, w.Hq, w.d), dtype=torch.bfloat16, pin_memory=True)
+    pre = args.preroll
+    nsteps = pre + args.warmup + args.steps
+    qs = [syn.QueryStreamTorch(w, l, dev) for l in range(L)]
+    q_dev = torch.empty((nsteps, L, w.B, w.Hq, w.d), dtype=torch.bfloat16, device=dev)
+    qla_dev = torch.empty((nsteps, L, w.B, w.n_la, w.Hq, w.d), dtype=torch.bfloat16, device=dev)
     for s in range(nsteps):
         for l in range(L):
             qb, qlab = qs[l].next()
-            q_host[s, l].copy_(torch.from_numpy(qb.view(np.int16)).view(torch.bfloat16))
-            qla_host[s, l].copy_(torch.from_numpy(qlab.view(np.int16)).view(torch.bfloat16))
-    q_dev = q_host.to(dev)
-    qla_dev = qla_host.to(dev)
+            q_dev[s, l].copy_(qb)
+            qla_dev[s, l].copy_(qlab)
+    first = pre + args.warmup
+    q_host = q_dev[first:].cpu().pin_memory()      # inputs of the timed steps, for the end-to-end pass
+    qla_host = qla_dev[first:].cpu().pin_memory()
+    torch.cuda.synchronize()
 
     main = torch.cuda.current_stream(dev)
     side = main  # one stream: with the gather on a side stream its CTAs delayed the scoring kernel
@@ -369,7 +379,7 @@ def run_gpu(args, rank, world, local_rank):
         st.decode_step(s, qla if qla is not None else qla_dev[s], q if q is not None else q_dev[s],
                        out_layers=out_dev, main=main, side=side, mark=mark)
 
-    for s in range(args.warmup):
+    for s in range(pre + args.warmup):
         step(s)
     torch.cuda.synchronize()
     errw = int(st.scratch.err.item()) | int(st.scratch2.err.item())
@@ -386,7 +396,7 @@ def run_gpu(args, rank, world, local_rank):
     issue_s = 0.0
     for k in range(args.steps):
         t_issue = time.perf_counter()
-        step(args.warmup + k, marks)
+        step(pre + args.warmup + k, marks)
         issue_s += time.perf_counter() - t_issue
     ev1.record(main)
     torch.cuda.synchronize()
@@ -398,16 +408,19 @@ def run_gpu(args, rank, world, local_rank):
 
     # per-kernel device time on a single stream (untimed pass, every kernel bracketed)
     iso = KernelMarks(L * 3 * 8 + 16)
+    attended = torch.zeros((), dtype=torch.int64, device=dev)
     for k in range(3):
-        s_k = args.warmup + k % args.steps
-        st.decode_step(s_k, qla_dev[s_k], q_dev[s_k], out_layers=out_dev, main=main, side=side, mark=iso)
+        s_k = pre + args.warmup + k % args.steps
+        st.decode_step(s_k, qla_dev[s_k], q_dev[s_k], out_layers=out_dev, main=main, side=side, mark=iso,
+                       count=attended)
     torch.cuda.synchronize()
     kernel_ms = iso.durations()
+    attended_per_head = float(attended.item()) / (3 * L * w.B * w.Hkv)
     # the same steps with everything on one stream, timed as a whole
     e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_a.record(main)
     for k in range(3):
-        s_k = args.warmup + k % args.steps
+        s_k = pre + args.warmup + k % args.steps
         st.decode_step(s_k, qla_dev[s_k], q_dev[s_k], out_layers=out_dev, main=main, side=torch.cuda.Stream(dev))
     e_b.record(main)
     torch.cuda.synchronize()
@@ -425,9 +438,9 @@ def run_gpu(args, rank, world, local_rank):
             torch.distributed.barrier()
         t0 = time.perf_counter()
         for k in range(nrep):
-            s = args.warmup + (k % args.steps)
-            q_in.copy_(q_host[s], non_blocking=True)
-            qla_in.copy_(qla_host[s], non_blocking=True)
+            s = pre + args.warmup + (k % args.steps)
+            q_in.copy_(q_host[s - first], non_blocking=True)
+            qla_in.copy_(qla_host[s - first], non_blocking=True)
             step(s, qla=qla_in, q=q_in)
             out_host.copy_(out_dev, non_blocking=True)
             torch.cuda.current_stream(dev).synchronize()
@@ -439,7 +452,7 @@ def run_gpu(args, rank, world, local_rank):
 
     if rank != 0:
         return
-    ab = algorithmic_bytes(w)
+    ab = algorithmic_bytes(w, attended_per_head)
     peak, peak_kind = measured_peaks()
     score_avg_ms = sum(score_ms) / len(score_ms)
     achieved = ab["score"] / (score_avg_ms / 1000.0) / 1e9
@@ -458,6 +471,8 @@ def run_gpu(args, rank, world, local_rank):
                      "traffic": score_traffic_per_launch(), "bytes_per_launch": ab["score"],
                      "avg_launch_ms": score_avg_ms},
         "kernel_avg_us": {k: round(1000.0 * sum(v) / len(v), 2) for k, v in kernel_ms.items() if v},
+        "attended_blocks_per_head": round(attended_per_head, 2),
+        "timed_steps": [pre + args.warmup, pre + args.warmup + args.steps - 1],
         "ms_per_step_gather_on_side_stream": two_stream_ms,
         "host_issue_ms_per_step": 1000.0 * issue_s / args.steps,
         "gpu_launches": 6 * L * args.steps,

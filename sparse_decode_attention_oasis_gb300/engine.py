@@ -213,8 +213,16 @@ class DecodeState:
                                    self.ctx, self.scale, sc.ws, sc.ws_bytes,
                                    sc.out if out is None else out, st)
 
+    def attended_blocks(self, layer: int, sc: "LayerScratch") -> torch.Tensor:
+        """Device count of attended blocks (selected and resident) of one layer, all heads."""
+        lp = layer % self.L_phys
+        sel = sc.sel.long()
+        valid = (sel >= 0) & (torch.arange(self.shape.Kb, device=self.device) < sc.nsel[..., None])
+        slot = torch.gather(self.b2sl[lp].long(), 2, sel.clamp(min=0))
+        return ((slot >= 0) & valid).sum()
+
     def decode_step(self, step: int, q_la_layers, q_layers, out_layers=None, main=None, side=None,
-                    mark=None):
+                    mark=None, count=None):
         """All layers of one decode step, pipelined across layers.
 
         Main stream: select(0); select(1); attn(0); select(2); attn(1); ...
@@ -260,6 +268,8 @@ class DecodeState:
                          None if out_layers is None else out_layers[l])
             if mark:
                 mark("attn_end", main)
+            if count is not None:
+                count += self.attended_blocks(l, scr[l % 2])
 
     # ---------------------------------------------------------------- appends
     def append_tokens(self, layer: int, k_new: torch.Tensor, v_new: torch.Tensor, advance: bool,

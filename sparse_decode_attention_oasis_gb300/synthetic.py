@@ -512,3 +512,52 @@ def append_tokens(w: Workload, layer: int, step: int):
     v = np.stack([np.stack([hash_normals(w.seed, STREAM_APPEND_V, layer, b, h, step * w.d, w.d)
                             for h in range(w.Hkv)]) for b in range(w.B)])
     return f32_to_bf16_bits(k), f32_to_bf16_bits(v)
+
+
+def hash_normals_multi_torch(seed: int, stream: int, layer: int, bs_, hs_, start: int, count: int, device):
+    """torch version of :func:`hash_normals_multi` (same bits on any device)."""
+    import torch
+
+    k1, k2 = _chunk_keys_multi(seed, stream, layer, bs_, hs_)
+    k1 = torch.from_numpy(k1.astype(np.int64)).to(device)[:, None]
+    k2 = torch.from_numpy(k2.astype(np.int64)).to(device)[:, None]
+    idx = torch.arange(start, start + count, dtype=torch.int64, device=device)[None, :]
+    v = _mix32_torch(_mix32_torch(idx ^ k1) ^ k2)
+    return normal_table_torch(device)[v >> 16]
+
+
+class QueryStreamTorch:
+    """Device twin of :class:`QueryStream`: the same bits, generated with torch ops."""
+
+    def __init__(self, w: Workload, layer: int, device):
+        import torch
+
+        self.w, self.layer, self.device = w, layer, device
+        self.step = 0
+        self.bb = np.repeat(np.arange(w.B), w.Hq)
+        self.hq = np.tile(np.arange(w.Hq), w.B)
+        u = np.stack([unit_dir(w, layer, b, h) for b in range(w.B) for h in range(w.Hkv)])
+        u = u.reshape(w.B, w.Hkv, 1, w.d).repeat(w.G, axis=2).reshape(w.B * w.Hq, w.d).astype(np.float64)
+        self.u2 = torch.from_numpy(2.0 * u).to(device)
+        self.e = None
+        self.a = math.sqrt(1.0 - w.rho * w.rho)
+
+    def next(self):
+        import torch
+
+        w, d, dev = self.w, self.w.d, self.device
+        if self.e is None:
+            self.e = hash_normals_multi_torch(w.seed, STREAM_QNOISE, self.layer, self.bb, self.hq, 0, d,
+                                              dev).double()
+        else:
+            xi = hash_normals_multi_torch(w.seed, STREAM_QNOISE, self.layer, self.bb, self.hq, self.step * d, d,
+                                          dev).double()
+            self.e = w.rho * self.e + self.a * xi
+        qf = (self.u2 + self.e).float()
+        la = hash_normals_multi_torch(w.seed, STREAM_LANOISE, self.layer, self.bb, self.hq,
+                                      self.step * w.n_la * d, w.n_la * d, dev).double().view(-1, w.n_la, d)
+        qla = (qf.double()[:, None, :] + w.la_sigma * la).float()
+        self.step += 1
+        q = qf.to(torch.bfloat16).view(w.B, w.Hq, d)
+        qla = qla.to(torch.bfloat16).view(w.B, w.Hq, w.n_la, d).transpose(1, 2).contiguous()
+        return q, qla

@@ -119,3 +119,17 @@ def test_difference_below_fp32_resolution_is_resolved_exactly():
     r, sc = c.step(0, q=syn.f32_to_bf16_bits(q), qla=syn.f32_to_bf16_bits(qla))
     for h in range(8):
         assert r["S"][(0, h)] == [9]
+
+
+def test_device_query_generator_matches_host():
+    w = syn.qwen3_8b_decode(B=4, L=1)
+    a = syn.QueryStream(w, 0)
+    t = syn.QueryStreamTorch(w, 0, "cuda")
+    for s in range(3):
+        qa, la = a.next()
+        qt, lt = t.next()
+        assert (qt.cpu().view(torch.int16).numpy().view(np.uint16) == qa).all()
+        assert (lt.cpu().view(torch.int16).numpy().view(np.uint16) == la).all()
+    K, V = syn.kv_request_torch(w, 0, 1, "cuda")
+    Kn, Vn = syn.head_kv(w, 0, 1, 3)
+    assert (K[3].cpu().view(torch.int16).numpy().view(np.uint16) == Kn).all()
