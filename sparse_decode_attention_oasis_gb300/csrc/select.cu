@@ -7,10 +7,10 @@
 // explanatory figure step 3; Table 2 caption: the per-step fetch cap).
 //
 // Exact selection from certified intervals.  The scores come with a bound e,
-// |s~ - s| <= e.  With t = the r-th largest s~ (radix select on order-preserving
-// keys) and E = max e over the candidates:
-//   s~_i - e_i > t + E  => i is certainly among the r best,
-//   s~_i + e_i < t - E  => i certainly is not,
+// |s~ - s| <= e.  With t the r-th largest s~, bracketed as t_lo <= t <= t_hi by a
+// two-level histogram, and E = max e over the candidates:
+//   s~_i - e_i > t_hi + E  => i is certainly among the r best,
+//   s~_i + e_i < t_lo - E  => i certainly is not,
 // (every candidate that could rank at or above a "certain" one has s~ > t, and
 // at most r-1 do; conversely the r candidates with s~ >= t all rank above a
 // "certainly not").  The remaining candidates U are re-scored exactly:
@@ -45,7 +45,6 @@ struct SelCtx {
   uint16_t* qb;                // [kMaxN][128]
   float* qn;                   // [kMaxN]
   uint16_t* kst;               // [kSelWarps][16][128] staged key blocks
-  unsigned long long* lacc;    // [kSelWarps][kLimbs]
   uint32_t* tmp;               // [kSelWarps][kLimbs]
   uint32_t* bval;              // [kSelWarps][kLimbs]
   int* bidx;                   // [kSelWarps]
@@ -68,38 +67,57 @@ __device__ __forceinline__ int exact_cmp(const uint32_t* a, const uint32_t* b) {
   return 0;
 }
 
-// Exact q.k (times 2^266) of a 128-long bf16 row pair, by one warp.
-__device__ void warp_exact_dot(const uint16_t* krow, const uint16_t* qrow,
-                               unsigned long long* acc, uint32_t* out, int lane) {
-  if (lane < kLimbs) acc[lane] = 0ull;
-  __syncwarp();
-  for (int e = lane; e < kD; e += 32) {
+// Exact q.k (times 2^266) of a 128-long bf16 row pair, by one warp.  Each lane
+// forms 4 exact products as (limb, low 32 bits, high bits); the limbs the warp
+// touches are summed one at a time with a 64-bit warp reduction (no atomics),
+// then every lane runs the same carry chain and lane i < 17 stores limb i.
+__device__ void warp_exact_dot(const uint16_t* krow, const uint16_t* qrow, uint32_t* out, int lane) {
+  int limb[4];
+  long long lo[4], hi[4];
+  int lmin = kLimbs, lmax = -1;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = lane + 32 * j;
     const uint32_t kb = krow[e], qb = qrow[e];
     const uint32_t kE = (kb >> 7) & 0xffu, qE = (qb >> 7) & 0xffu;
     const uint32_t km = (kb & 0x7fu) | (kE ? 0x80u : 0u);
     const uint32_t qm = (qb & 0x7fu) | (qE ? 0x80u : 0u);
     const uint32_t mm = km * qm;
+    limb[j] = -2;
+    lo[j] = hi[j] = 0;
     if (mm) {
       const int ee = (int)(kE ? kE : 1u) + (int)(qE ? qE : 1u) - 2;  // 0 .. 508
       const unsigned long long v = (unsigned long long)mm << (ee & 31);
-      unsigned long long lo = v & 0xffffffffull, hi = v >> 32;
-      if ((kb ^ qb) & 0x8000u) {
-        lo = (unsigned long long)(-(long long)lo);
-        hi = (unsigned long long)(-(long long)hi);
-      }
-      atomicAdd(acc + (ee >> 5), lo);
-      if (hi) atomicAdd(acc + (ee >> 5) + 1, hi);
+      lo[j] = (long long)(v & 0xffffffffull);
+      hi[j] = (long long)(v >> 32);
+      if ((kb ^ qb) & 0x8000u) { lo[j] = -lo[j]; hi[j] = -hi[j]; }
+      limb[j] = ee >> 5;
+      lmin = min(lmin, limb[j]);
+      lmax = max(lmax, limb[j] + 1);
     }
   }
-  __syncwarp();
-  if (lane == 0) {
-    long long carry = 0;
-    for (int i = 0; i < kLimbs; ++i) {
-      const long long v = (long long)acc[i] + carry;
-      out[i] = (uint32_t)(unsigned long long)v;
-      carry = v >> 32;
+  lmin = __reduce_min_sync(0xffffffffu, lmin);
+  lmax = __reduce_max_sync(0xffffffffu, lmax);
+  long long mine = 0;
+  for (int L = lmin; L <= lmax; ++L) {
+    long long sum = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (limb[j] == L) sum += lo[j];
+      if (limb[j] + 1 == L) sum += hi[j];
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == L) mine = sum;
   }
+  long long carry = 0;
+  uint32_t word = 0;
+  for (int i = 0; i < kLimbs; ++i) {
+    const long long v = __shfl_sync(0xffffffffu, mine, i) + carry;
+    if (lane == i) word = (uint32_t)(unsigned long long)v;
+    carry = v >> 32;
+  }
+  if (lane < kLimbs) out[lane] = word;
   __syncwarp();
 }
 
@@ -142,56 +160,114 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   return r;
 }
 
-// key of the k-th largest (k >= 1) s~ among se[0..n)
-__device__ uint32_t kth_largest_key(const float2* se, int n, int k, uint32_t* hist, int* scal) {
-  uint32_t prefix = 0, mask = 0;
-  int kk = k;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0u;
-    __syncthreads();
-    // warp-aggregated counting: scores share their leading bits, so most lanes of
-    // a warp hit the same bin; one atomic per distinct bin per warp
-    const int n_pad = (n + 31) & ~31;
-    for (int i = threadIdx.x; i < n_pad; i += blockDim.x) {
-      const uint32_t key = i < n ? float_key(se[i].x) : 0u;
-      const bool take = i < n && (key & mask) == prefix;
-      const uint32_t bin = take ? ((key >> shift) & 255u) : 256u;
-      const unsigned peers = __match_any_sync(0xffffffffu, bin);
-      if (take && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      const int lane = threadIdx.x;
-      uint32_t c[8], sum = 0;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) { c[q] = hist[255 - (lane * 8 + q)]; sum += c[q]; }
-      uint32_t incl = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const uint32_t excl = incl - sum;
-      if (excl < (uint32_t)kk && (uint32_t)kk <= incl) {
-        uint32_t run = excl;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          if (run + c[q] >= (uint32_t)kk) {
-            scal[0] = 255 - (lane * 8 + q);
-            scal[1] = (int)run;
-            break;
-          }
-          run += c[q];
-        }
-      }
-    }
-    __syncthreads();
-    prefix |= (uint32_t)scal[0] << shift;
-    mask |= 255u << shift;
-    kk -= scal[1];
-    __syncthreads();
+// Bracket [t_lo, t_hi] around the k-th largest s~ among se[0..n) (1 <= k <= n), and
+// E = max e.  Two passes of 256 bins: bin1 = floor(256 (x - min)/(max - min)),
+// then 256 sub-bins of bin1's fraction.  Both bin maps are monotone in x (one
+// subtraction and a multiplication by a positive constant, exact sub-bin
+// offsets), so the k-th largest lies in the selected (bin1, bin2) cell; t_lo and
+// t_hi are the smallest and largest s~ in that cell.
+__device__ void kth_bracket(const float2* se, int n, int k, uint32_t* hist, int* scal, float* fs,
+                            float& t_lo, float& t_hi, float& emax) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float mn = __int_as_float(0x7f800000), mx = neg_inf(), em = 0.f;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const float2 v = se[i];
+    mn = fminf(mn, v.x);
+    mx = fmaxf(mx, v.x);
+    em = fmaxf(em, v.y);
   }
-  return prefix;
+  mn = -warp_max(-mn);
+  mx = warp_max(mx);
+  em = warp_max(em);
+  if (lane == 0) { fs[3 * warp] = mn; fs[3 * warp + 1] = mx; fs[3 * warp + 2] = em; }
+  for (int i = threadIdx.x; i < 512; i += blockDim.x) hist[i] = 0u;
+  __syncthreads();
+  mn = fs[0]; mx = fs[1]; em = fs[2];
+  for (int w = 1; w < kSelWarps; ++w) {
+    mn = fminf(mn, fs[3 * w]); mx = fmaxf(mx, fs[3 * w + 1]); em = fmaxf(em, fs[3 * w + 2]);
+  }
+  emax = em;
+  const float span = mx - mn;
+  const float sc1 = span > 1e-30f ? 256.0f / span : 0.f;
+  const int n_pad = (n + 31) & ~31;
+  // pass 1
+  for (int i = threadIdx.x; i < n_pad; i += blockDim.x) {
+    uint32_t bin = 1024u;
+    if (i < n) bin = (uint32_t)min(255, (int)((se[i].x - mn) * sc1));
+    const unsigned peers = __match_any_sync(0xffffffffu, bin);
+    if (i < n && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+  }
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t c[8], sum = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) { c[q] = hist[255 - (lane * 8 + q)]; sum += c[q]; }
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const uint32_t excl = incl - sum;
+    if (excl < (uint32_t)k && (uint32_t)k <= incl) {
+      uint32_t run = excl;
+      for (int q = 0; q < 8; ++q) {
+        if (run + c[q] >= (uint32_t)k) { scal[0] = 255 - (lane * 8 + q); scal[1] = (int)run; break; }
+        run += c[q];
+      }
+    }
+  }
+  __syncthreads();
+  const int b1 = scal[0];
+  const int k1 = k - scal[1];
+  uint32_t* h2 = hist + 256;                    // reuse: counts of sub-bins
+  uint32_t* kmin = reinterpret_cast<uint32_t*>(fs + 64);   // per sub-bin min / max keys
+  uint32_t* kmax = kmin + 256;
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) { h2[i] = 0u; kmin[i] = 0xffffffffu; kmax[i] = 0u; }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n_pad; i += blockDim.x) {
+    uint32_t bin = 1024u;
+    uint32_t key = 0u;
+    if (i < n) {
+      const float x = se[i].x;
+      const float y = (x - mn) * sc1;
+      const int bb1 = min(255, (int)y);
+      if (bb1 == b1) {
+        bin = (uint32_t)max(0, min(255, (int)((y - (float)bb1) * 256.0f)));
+        key = float_key(x);
+      }
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, bin);
+    if (bin < 1024u) {
+      atomicMin(&kmin[bin], key);
+      atomicMax(&kmax[bin], key);
+      if (lane == __ffs(peers) - 1) atomicAdd(&h2[bin], (uint32_t)__popc(peers));
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t c[8], sum = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) { c[q] = h2[255 - (lane * 8 + q)]; sum += c[q]; }
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const uint32_t excl = incl - sum;
+    if (excl < (uint32_t)k1 && (uint32_t)k1 <= incl) {
+      uint32_t run = excl;
+      for (int q = 0; q < 8; ++q) {
+        if (run + c[q] >= (uint32_t)k1) { scal[2] = 255 - (lane * 8 + q); break; }
+        run += c[q];
+      }
+    }
+  }
+  __syncthreads();
+  t_lo = key_float(kmin[scal[2]]);
+  t_hi = key_float(kmax[scal[2]]);
+  __syncthreads();
 }
 
 // Stage the head's lookahead queries (fp32, bf16 bits, norms) in shared memory.
@@ -256,13 +332,22 @@ __device__ void warp_exact_block_score(const SelCtx& c, int blk, uint32_t* out, 
     if (dd < ndots && blk * kBS + tau < c.ctx) {
       const uint32_t* row = reinterpret_cast<const uint32_t*>(kst + tau * kD);
       const float* qr = c.qf + n * kQStride;
-      float v = 0.f;
-#pragma unroll 8
-      for (int i = 0; i < kD / 2; ++i) {
-        const uint32_t w = row[i];
-        v = fmaf(bf_lo(w), qr[2 * i], v);
-        v = fmaf(bf_hi(w), qr[2 * i + 1], v);
+      // four interleaved chains of 32 terms, then a pairwise sum: the error stays
+      // below gamma_34 * sum|q_i k_i| < 2^-16 |q| |k|
+      float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
+#pragma unroll 4
+      for (int i = 0; i < kD / 2; i += 4) {
+        const uint32_t w0 = row[i], w1 = row[i + 1], w2 = row[i + 2], w3 = row[i + 3];
+        v0 = fmaf(bf_lo(w0), qr[2 * i], v0);
+        v1 = fmaf(bf_lo(w1), qr[2 * i + 2], v1);
+        v2 = fmaf(bf_lo(w2), qr[2 * i + 4], v2);
+        v3 = fmaf(bf_lo(w3), qr[2 * i + 6], v3);
+        v0 = fmaf(bf_hi(w0), qr[2 * i + 1], v0);
+        v1 = fmaf(bf_hi(w1), qr[2 * i + 3], v1);
+        v2 = fmaf(bf_hi(w2), qr[2 * i + 5], v2);
+        v3 = fmaf(bf_hi(w3), qr[2 * i + 7], v3);
       }
+      const float v = (v0 + v1) + (v2 + v3);
       const float eps = __fmaf_ru(1.52587890625e-05f /* 2^-16 */, __fmul_ru(kt, c.qn[n]),
                                   7.52316384526264e-37f /* 2^-120 */);
       vlo[m] = __fsub_rd(v, eps);
@@ -274,7 +359,6 @@ __device__ void warp_exact_block_score(const SelCtx& c, int blk, uint32_t* out, 
   best_lo = warp_max(best_lo);
   bool have = false;
   uint32_t* tmp = c.tmp + warp * kLimbs;
-  unsigned long long* acc = c.lacc + warp * kLimbs;
 #pragma unroll
   for (int m = 0; m < kMaxPerLane; ++m) {
     const bool cand = (lane + 32 * m) < ndots && vhi[m] >= best_lo && vhi[m] != neg_inf();
@@ -284,7 +368,7 @@ __device__ void warp_exact_block_score(const SelCtx& c, int blk, uint32_t* out, 
       mask &= mask - 1;
       const int dd = src + 32 * m;
       const int tau = dd / c.N, n = dd - tau * c.N;
-      warp_exact_dot(kst + tau * kD, c.qb + n * kD, acc, tmp, lane);
+      warp_exact_dot(kst + tau * kD, c.qb + n * kD, tmp, lane);
       if (lane == 0) {
         if (!have || exact_cmp(tmp, out) > 0)
           for (int i = 0; i < kLimbs; ++i) out[i] = tmp[i];
@@ -367,12 +451,9 @@ __device__ void select_best(SelCtx& c, const float2* se, int n, int k, const int
     __syncthreads();
     return;
   }
-  const uint32_t tkey = kth_largest_key(se, n, k, c.hist, c.scal);
-  const float tval = key_float(tkey);
-  float em = 0.f;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) em = fmaxf(em, se[i].y);
-  em = block_max(em, c.fscal);
-  const float hi_t = __fadd_ru(tval, em), lo_t = __fsub_rd(tval, em);
+  float t_lo, t_hi, em;
+  kth_bracket(se, n, k, c.hist, c.scal, c.fscal, t_lo, t_hi, em);
+  const float hi_t = __fadd_ru(t_hi, em), lo_t = __fsub_rd(t_lo, em);
   if (threadIdx.x == 0) { c.scal[2] = 0; c.scal[3] = 0; }
   __syncthreads();
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
@@ -404,7 +485,7 @@ __device__ void select_best(SelCtx& c, const float2* se, int n, int k, const int
 
 // ---------------------------------------------------------------- shared memory layout
 struct SelLayout {
-  size_t se, cls, U, cblk, kst, qf, qb, qn, lacc, tmp, bval, bidx, tval, tidx, tval2, tidx2, rank, hist, scal,
+  size_t se, cls, U, cblk, kst, qf, qb, qn, tmp, bval, bidx, tval, tidx, tval2, tidx2, rank, hist, scal,
       fscal, red, total;
 };
 
@@ -421,7 +502,6 @@ __host__ __device__ inline SelLayout sel_layout(int ncap, bool with_cblk, int kb
   L.qf = o; o = align16(o + sizeof(float) * kMaxN * kQStride);
   L.qb = o; o = align16(o + sizeof(uint16_t) * kMaxN * kD);
   L.qn = o; o = align16(o + sizeof(float) * kMaxN);
-  L.lacc = o; o = align16(o + sizeof(unsigned long long) * kSelWarps * kLimbs);
   L.tmp = o; o = align16(o + sizeof(uint32_t) * kSelWarps * kLimbs);
   L.bval = o; o = align16(o + sizeof(uint32_t) * kSelWarps * kLimbs);
   L.bidx = o; o = align16(o + sizeof(int) * kSelWarps);
@@ -430,9 +510,9 @@ __host__ __device__ inline SelLayout sel_layout(int ncap, bool with_cblk, int kb
   L.tval2 = o; o = align16(o + sizeof(uint32_t) * kb * kLimbs);
   L.tidx2 = o; o = align16(o + sizeof(int) * kb);
   L.rank = o; o = align16(o + sizeof(int) * (kb + kSelWarps));
-  L.hist = o; o = align16(o + sizeof(uint32_t) * 256);
+  L.hist = o; o = align16(o + sizeof(uint32_t) * 512);
   L.scal = o; o = align16(o + sizeof(int) * 8);
-  L.fscal = o; o = align16(o + sizeof(float) * kSelWarps);
+  L.fscal = o; o = align16(o + sizeof(float) * (64 + 512));
   L.red = o; o = align16(o + sizeof(int) * 32);
   L.total = o;
   return L;
@@ -454,7 +534,6 @@ __device__ SelCtx make_ctx(char* sm, const SelLayout& L, const Shape& s, const u
   c.qb = reinterpret_cast<uint16_t*>(sm + L.qb);
   c.qn = reinterpret_cast<float*>(sm + L.qn);
   c.kst = reinterpret_cast<uint16_t*>(sm + L.kst);
-  c.lacc = reinterpret_cast<unsigned long long*>(sm + L.lacc);
   c.tmp = reinterpret_cast<uint32_t*>(sm + L.tmp);
   c.bval = reinterpret_cast<uint32_t*>(sm + L.bval);
   c.bidx = reinterpret_cast<int*>(sm + L.bidx);
