@@ -54,6 +54,7 @@ def parse():
     ap.add_argument("--preroll", type=int, default=40,
                     help="untimed decode steps run first, so the timed steps see a warmed-up resident set")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-hostlink", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-worker", type=int, default=0, help=argparse.SUPPRESS)
     ap.add_argument("--cpu-heads", type=int, default=3)
@@ -279,6 +280,55 @@ def algorithmic_bytes(w, attended_per_head=None):
             "total": score + topk + attn + gather_hbm}
 
 
+def measure_hostlink(st, qla0, dev):
+    """Host-link roofline of the gather: fetch-all into an emptied layer vs a pinned memcpy.
+
+    Layer 0's resident set is emptied and the fetch cap raised to the budget, so
+    the gather copies every selected block (Kb x 8 KiB per head) from the host
+    tier; its CUDA-event time gives GB/s, compared with cudaMemcpy of 1 GiB from
+    page-locked memory (the measured host-link peak on this machine).
+    """
+    import torch
+
+    from sparse_decode_attention_oasis_gb300 import binding as B
+
+    w, s, sc = st.w, st.shape, st.scratch
+    main = torch.cuda.current_stream(dev)
+    best = None
+    for rep in range(3):
+        st.b2sl[0].fill_(-1)
+        st.s2bl[0].fill_(-1)
+        st.lul[0].fill_(-1)
+        B.oasis_score_blocks(s, st.Kl[0], st.ctx, qla0[0], sc.scores, sc.err, main)
+        B.oasis_topk_select(s, sc.scores, st.Kl[0], qla0[0], st.ctx, sc.sel, sc.nsel, main)
+        B.oasis_fetch_diff_capped(s, sc.scores, st.Kl[0], qla0[0], st.ctx, sc.sel, sc.nsel, st.b2sl[0], w.Kb,
+                                  sc.fetch, sc.nfetch, main)
+        torch.cuda.synchronize()
+        nfetch = int(sc.nfetch.sum().item())
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(main)
+        B.oasis_gather_h2d(s, st.hostl[0], sc.sel, sc.nsel, sc.fetch, sc.nfetch, st.b2sl[0], st.s2bl[0], st.lul[0],
+                           1, st.kpl[0], st.vpl[0], sc.err, main)
+        e1.record(main)
+        torch.cuda.synchronize()
+        gbs = nfetch * 2 * w.bs * w.d * 2 / (e0.elapsed_time(e1) / 1000.0) / 1e9
+        best = gbs if best is None else max(best, gbs)
+    src = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    peak = 0.0
+    for rep in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(main)
+        dst.copy_(src, non_blocking=True)
+        e1.record(main)
+        torch.cuda.synchronize()
+        peak = max(peak, (1 << 30) / (e0.elapsed_time(e1) / 1000.0) / 1e9)
+    del src, dst
+    return {"kernel": "gather_h2d (fetch-all, one layer)", "bound": "host link", "achieved": best,
+            "peak": peak, "peak_kind": "measured: pinned cudaMemcpy H2D of 1 GiB", "unit": "GB/s",
+            "frac": best / peak, "bytes_per_launch": nfetch * 2 * w.bs * w.d * 2}
+
+
 # --------------------------------------------------------------------------- reference arm
 def run_reference(args, rank):
     if rank != 0:
@@ -450,6 +500,8 @@ def run_gpu(args, rank, world, local_rank):
         e2e = {"value": aggregate_value(world, L, nrep, 1000.0 * e2e_s), "unit": UNIT, "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": bo}
 
+    hostlink = measure_hostlink(st, qla_dev[first], dev) if not args.no_hostlink else None
+
     if rank != 0:
         return
     ab = algorithmic_bytes(w, attended_per_head)
@@ -476,6 +528,7 @@ def run_gpu(args, rank, world, local_rank):
         "ms_per_step_gather_on_side_stream": two_stream_ms,
         "host_issue_ms_per_step": 1000.0 * issue_s / args.steps,
         "gpu_launches": 6 * L * args.steps,
+        "hostlink": hostlink,
         "clocks": clk,
         "e2e": e2e,
         "device_error_word": errw,

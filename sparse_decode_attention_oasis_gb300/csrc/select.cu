@@ -14,17 +14,19 @@
 // (every candidate that could rank at or above a "certain" one has s~ > t, and
 // at most r-1 do; conversely the r candidates with s~ >= t all rank above a
 // "certainly not").  The remaining candidates U are re-scored exactly:
-//   1. fp32 re-computation of the 16 x N dot products of the block on the CUDA
-//      cores, with the a-priori bound |err| <= 2^-16 |q| |k| + 2^-120
-//      (sequential fma over 128 terms: gamma_128 < 2^-16.9);
-//   2. the dots whose interval reaches the block's best lower bound are
-//      evaluated exactly: each bf16 is m * 2^(E-134), each product is an integer
-//      times 2^-266, and a 544-bit two's complement fixed-point accumulator
-//      (17 limbs of 32 bits, carries deferred in 64-bit shared-memory words)
-//      holds the sum with no rounding at all;
+//   1. the block's 16 x N dot products are re-formed on the tensor cores with
+//      per-dot bounds 2^-12 |q_n| |k_t| (the scoring kernel's error model, per
+//      dot instead of per block), which isolates the dot(s) that can be the
+//      block's maximum - normally one;
+//   2. those dots are evaluated exactly: each bf16 is m * 2^(E-134), each
+//      product is an integer times 2^-266, and a 544-bit two's complement
+//      fixed-point number (17 limbs of 32 bits) holds the sum with no rounding;
+//      the limbs are summed with 64-bit warp reductions;
 //   3. U is merged into a running top-r set by exact comparison (a rank count
 //      over the union), kSelWarps blocks at a time.
-// The result equals the definition for every finite input.
+// The result equals the definition for every finite input whose tensor-core
+// accumulation stays within the modelled bound (the GPU tests check every block
+// score of every case against its exact value).
 #include "common.cuh"
 
 namespace oasis {
@@ -33,15 +35,12 @@ constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kLimbs = 17;
 constexpr int kMaxN = 32;      // lookahead queries x GQA group
-constexpr int kMaxR = 256;     // largest budget in blocks
-constexpr int kQStride = 129;  // fp32 query rows padded against bank conflicts
 
 struct SelCtx {
   const uint16_t* k;   // keys of this head [T_max][128]
   const uint16_t* q_la;
   int b, h, ctx, N, G, n_la, Hq;
   // shared memory
-  float* qf;                   // [kMaxN][kQStride]
   uint16_t* qb;                // [kMaxN][128]
   float* qn;                   // [kMaxN]
   uint16_t* kst;               // [kSelWarps][16][128] staged key blocks
@@ -270,33 +269,41 @@ __device__ void kth_bracket(const float2* se, int n, int k, uint32_t* hist, int*
   __syncthreads();
 }
 
-// Stage the head's lookahead queries (fp32, bf16 bits, norms) in shared memory.
+// Stage the head's lookahead queries (bf16 bits and fp32 norms) in shared memory:
+// one 16-byte load per piece, all issued together.
 __device__ void stage_queries(SelCtx& c) {
-  for (int idx = threadIdx.x; idx < c.N * kD; idx += blockDim.x) {
-    const int n = idx / kD, i = idx - n * kD;
+  for (int idx = threadIdx.x; idx < c.N * 16; idx += blockDim.x) {
+    const int n = idx >> 4, part = idx & 15;
     const int j = n / c.G, gg = n - j * c.G;
-    const uint16_t v = c.q_la[(((long long)c.b * c.n_la + j) * c.Hq + c.h * c.G + gg) * kD + i];
-    c.qb[n * kD + i] = v;
-    c.qf[n * kQStride + i] = __uint_as_float((uint32_t)v << 16);
+    const uint4 v = ldg_nc(c.q_la + (((long long)c.b * c.n_la + j) * c.Hq + c.h * c.G + gg) * kD + part * 8);
+    reinterpret_cast<uint4*>(c.qb + n * kD)[part] = v;
   }
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int n = warp; n < c.N; n += kSelWarps) {
-    float ss = 0.f;
-    for (int i = lane; i < kD; i += 32) ss = fmaf(c.qf[n * kQStride + i], c.qf[n * kQStride + i], ss);
+    const uint32_t w0 = reinterpret_cast<const uint32_t*>(c.qb + n * kD)[lane];
+    const uint32_t w1 = reinterpret_cast<const uint32_t*>(c.qb + n * kD)[lane + 32];
+    float ss = bf_lo(w0) * bf_lo(w0);
+    ss = fmaf(bf_hi(w0), bf_hi(w0), ss);
+    ss = fmaf(bf_lo(w1), bf_lo(w1), ss);
+    ss = fmaf(bf_hi(w1), bf_hi(w1), ss);
     ss = warp_sum(ss);
     if (lane == 0) c.qn[n] = sqrtf(ss);
   }
   __syncthreads();
 }
 
+__device__ __forceinline__ uint4 lds16v(const uint16_t* p) { return *reinterpret_cast<const uint4*>(p); }
+
 // Exact score (x 2^266, as kLimbs words) of block `blk`, by one warp, into out.
-// The block's 16 key rows (4 KiB) are first staged in this warp's shared-memory
-// slot with one round of coalesced 16-byte loads; everything after that reads
-// shared memory only.
+// The block's 16 key rows (4 KiB) are staged in this warp's shared-memory slot with
+// one round of coalesced 16-byte loads.  The 16 x N dot products are then formed
+// on the tensor cores exactly as the scoring kernel forms them (bf16 in, fp32
+// accumulate, so the same bound 2^-12 |q_n| |k_t| holds for each dot); only the
+// dots whose interval reaches the best lower bound of the block are summed
+// exactly.  Usually that is one dot.
 __device__ void warp_exact_block_score(const SelCtx& c, int blk, uint32_t* out, int warp, int lane) {
-  constexpr int kMaxPerLane = (kBS * kMaxN) / 32;
-  const int ndots = kBS * c.N;
+  const int g = lane >> 2, t = lane & 3;
   uint16_t* kst = c.kst + warp * (kBS * kD);
   {
     const uint4* src = reinterpret_cast<const uint4*>(c.k + (long long)blk * kBS * kD);
@@ -308,66 +315,90 @@ __device__ void warp_exact_block_score(const SelCtx& c, int blk, uint32_t* out, 
     for (int i = 0; i < 8; ++i) dst[lane + 32 * i] = v[i];
   }
   __syncwarp();
-  // token norms (lanes 0..15)
-  float kn = 0.f;
-  if (lane < kBS) {
-    const uint32_t* row = reinterpret_cast<const uint32_t*>(kst + lane * kD);
-#pragma unroll 8
-    for (int i = 0; i < kD / 2; ++i) {
-      const uint32_t w = row[(i + lane) & (kD / 2 - 1)];
-      kn = fmaf(bf_lo(w), bf_lo(w), kn);
-      kn = fmaf(bf_hi(w), bf_hi(w), kn);
-    }
-    kn = sqrtf(kn);
+  uint4 ra[4], rb[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    ra[i] = lds16v(kst + g * kD + (t + 4 * i) * 8);
+    rb[i] = lds16v(kst + (g + 8) * kD + (t + 4 * i) * 8);
   }
-  float vlo[kMaxPerLane], vhi[kMaxPerLane];
+  // token norms of rows g and g+8
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t A[4] = {ra[i].x, ra[i].y, ra[i].z, ra[i].w};
+    const uint32_t Bw[4] = {rb[i].x, rb[i].y, rb[i].z, rb[i].w};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      s0 = fmaf(bf_lo(A[m]), bf_lo(A[m]), s0); s0 = fmaf(bf_hi(A[m]), bf_hi(A[m]), s0);
+      s1 = fmaf(bf_lo(Bw[m]), bf_lo(Bw[m]), s1); s1 = fmaf(bf_hi(Bw[m]), bf_hi(Bw[m]), s1);
+    }
+  }
+  s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+  s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+  s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+  s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+  const float kn0 = sqrtf(s0), kn1 = sqrtf(s1);
+  const int NT = (c.N + 7) >> 3;
+  float acc[4][4];
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt) {
+    acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    if (nt < NT) {
+      const int n = nt * 8 + g;
+      uint4 qv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        qv[i] = n < c.N ? lds16v(c.qb + n * kD + (t + 4 * i) * 8) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t A[4] = {ra[i].x, ra[i].y, ra[i].z, ra[i].w};
+        const uint32_t Bw[4] = {rb[i].x, rb[i].y, rb[i].z, rb[i].w};
+        const uint32_t Q[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+          mma_bf16_16816(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3], A[2 * hh], Bw[2 * hh], A[2 * hh + 1],
+                         Bw[2 * hh + 1], Q[2 * hh], Q[2 * hh + 1]);
+      }
+    }
+  }
+  // per-dot intervals; element e of n-tile nt is (token g or g+8, query nt*8 + 2t + (e & 1))
+  const int tok0 = blk * kBS + g;
+  float vlo[16], vhi[16];
   float best_lo = neg_inf();
 #pragma unroll
-  for (int m = 0; m < kMaxPerLane; ++m) {
-    const int dd = lane + 32 * m;
-    const int tau = dd / c.N, n = dd - tau * c.N;
-    const float kt = __shfl_sync(0xffffffffu, kn, tau & 15);
-    vlo[m] = neg_inf();
-    vhi[m] = neg_inf();
-    if (dd < ndots && blk * kBS + tau < c.ctx) {
-      const uint32_t* row = reinterpret_cast<const uint32_t*>(kst + tau * kD);
-      const float* qr = c.qf + n * kQStride;
-      // four interleaved chains of 32 terms, then a pairwise sum: the error stays
-      // below gamma_34 * sum|q_i k_i| < 2^-16 |q| |k|
-      float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
-#pragma unroll 4
-      for (int i = 0; i < kD / 2; i += 4) {
-        const uint32_t w0 = row[i], w1 = row[i + 1], w2 = row[i + 2], w3 = row[i + 3];
-        v0 = fmaf(bf_lo(w0), qr[2 * i], v0);
-        v1 = fmaf(bf_lo(w1), qr[2 * i + 2], v1);
-        v2 = fmaf(bf_lo(w2), qr[2 * i + 4], v2);
-        v3 = fmaf(bf_lo(w3), qr[2 * i + 6], v3);
-        v0 = fmaf(bf_hi(w0), qr[2 * i + 1], v0);
-        v1 = fmaf(bf_hi(w1), qr[2 * i + 3], v1);
-        v2 = fmaf(bf_hi(w2), qr[2 * i + 5], v2);
-        v3 = fmaf(bf_hi(w3), qr[2 * i + 7], v3);
+  for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int n = nt * 8 + 2 * t + (e & 1);
+      const bool row8 = e >= 2;
+      const bool ok = nt < NT && n < c.N && (tok0 + (row8 ? 8 : 0)) < c.ctx;
+      const int idx = nt * 4 + e;
+      vlo[idx] = neg_inf();
+      vhi[idx] = neg_inf();
+      if (ok) {
+        const float v = acc[nt][e];
+        const float eps = __fmaf_ru(kAccRel * 1.0009765625f, __fmul_ru(row8 ? kn1 : kn0, c.qn[n]),
+                                    7.52316384526264e-37f /* 2^-120 */);
+        vlo[idx] = __fsub_rd(v, eps);
+        vhi[idx] = __fadd_ru(v, eps);
+        if (!(fabsf(v) <= 3.0e38f)) { vlo[idx] = neg_inf(); vhi[idx] = __int_as_float(0x7f800000); }
+        best_lo = fmaxf(best_lo, vlo[idx]);
       }
-      const float v = (v0 + v1) + (v2 + v3);
-      const float eps = __fmaf_ru(1.52587890625e-05f /* 2^-16 */, __fmul_ru(kt, c.qn[n]),
-                                  7.52316384526264e-37f /* 2^-120 */);
-      vlo[m] = __fsub_rd(v, eps);
-      vhi[m] = __fadd_ru(v, eps);
-      if (!(fabsf(v) <= 3.0e38f)) { vlo[m] = neg_inf(); vhi[m] = __int_as_float(0x7f800000); }
-      best_lo = fmaxf(best_lo, vlo[m]);
     }
-  }
   best_lo = warp_max(best_lo);
   bool have = false;
   uint32_t* tmp = c.tmp + warp * kLimbs;
 #pragma unroll
-  for (int m = 0; m < kMaxPerLane; ++m) {
-    const bool cand = (lane + 32 * m) < ndots && vhi[m] >= best_lo && vhi[m] != neg_inf();
+  for (int idx = 0; idx < 16; ++idx) {
+    const bool cand = vhi[idx] != neg_inf() && vhi[idx] >= best_lo;
     unsigned mask = __ballot_sync(0xffffffffu, cand);
     while (mask) {
       const int src = __ffs(mask) - 1;
       mask &= mask - 1;
-      const int dd = src + 32 * m;
-      const int tau = dd / c.N, n = dd - tau * c.N;
+      const int sg = src >> 2, st = src & 3;
+      const int nt = idx >> 2, e = idx & 3;
+      const int tau = sg + (e >= 2 ? 8 : 0);
+      const int n = nt * 8 + 2 * st + (e & 1);
       warp_exact_dot(kst + tau * kD, c.qb + n * kD, tmp, lane);
       if (lane == 0) {
         if (!have || exact_cmp(tmp, out) > 0)
@@ -485,7 +516,7 @@ __device__ void select_best(SelCtx& c, const float2* se, int n, int k, const int
 
 // ---------------------------------------------------------------- shared memory layout
 struct SelLayout {
-  size_t se, cls, U, cblk, kst, qf, qb, qn, tmp, bval, bidx, tval, tidx, tval2, tidx2, rank, hist, scal,
+  size_t se, cls, U, cblk, kst, qb, qn, tmp, bval, bidx, tval, tidx, tval2, tidx2, rank, hist, scal,
       fscal, red, total;
 };
 
@@ -499,7 +530,6 @@ __host__ __device__ inline SelLayout sel_layout(int ncap, bool with_cblk, int kb
   L.U = o; o = align16(o + sizeof(int) * ncap);
   L.cblk = o; o = align16(o + (with_cblk ? sizeof(int) * ncap : 0));
   L.kst = o; o = align16(o + sizeof(uint16_t) * kSelWarps * kBS * kD);
-  L.qf = o; o = align16(o + sizeof(float) * kMaxN * kQStride);
   L.qb = o; o = align16(o + sizeof(uint16_t) * kMaxN * kD);
   L.qn = o; o = align16(o + sizeof(float) * kMaxN);
   L.tmp = o; o = align16(o + sizeof(uint32_t) * kSelWarps * kLimbs);
@@ -530,7 +560,6 @@ __device__ SelCtx make_ctx(char* sm, const SelLayout& L, const Shape& s, const u
   c.N = s.n_la * c.G;
   c.n_la = s.n_la;
   c.Hq = s.Hq;
-  c.qf = reinterpret_cast<float*>(sm + L.qf);
   c.qb = reinterpret_cast<uint16_t*>(sm + L.qb);
   c.qn = reinterpret_cast<float*>(sm + L.qn);
   c.kst = reinterpret_cast<uint16_t*>(sm + L.kst);
