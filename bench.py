@@ -308,7 +308,7 @@ def measure_hostlink(st, qla0, dev):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(main)
         B.oasis_gather_h2d(s, st.hostl[0], sc.sel, sc.nsel, sc.fetch, sc.nfetch, st.b2sl[0], st.s2bl[0], st.lul[0],
-                           1, st.kpl[0], st.vpl[0], sc.err, main)
+                           st.step_dev, st.kpl[0], st.vpl[0], sc.err, main)
         e1.record(main)
         torch.cuda.synchronize()
         gbs = nfetch * 2 * w.bs * w.d * 2 / (e0.elapsed_time(e1) / 1000.0) / 1e9
@@ -434,7 +434,16 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     errw = int(st.scratch.err.item()) | int(st.scratch2.err.item())
 
+    # the timed steps, captured once as a CUDA graph (inputs already in HBM, the LRU
+    # clock advanced by the graph); events around every scoring launch are graph nodes
+    from sparse_decode_attention_oasis_gb300.engine import StepGraph
+
     marks = KernelMarks(L * args.steps * 2 + 16, names={"score", "topk"})
+    out_steps = [torch.empty((L, w.B, w.Hq, w.d), dtype=torch.float32, device=dev) for _ in range(2)]
+    ts = range(first, first + args.steps)
+    graph = StepGraph(st, first, [qla_dev[s] for s in ts], [q_dev[s] for s in ts],
+                      [out_steps[k % 2] for k in range(args.steps)], mark=marks)
+    gstream = graph.stream
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local_rank)
     if world > 1:
@@ -442,58 +451,63 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
-    ev0.record(main)
-    issue_s = 0.0
-    for k in range(args.steps):
-        t_issue = time.perf_counter()
-        step(pre + args.warmup + k, marks)
-        issue_s += time.perf_counter() - t_issue
-    ev1.record(main)
+    with torch.cuda.stream(gstream):
+        ev0.record(gstream)
+        graph.replay()
+        ev1.record(gstream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
     ms = reduce_max(ev0.elapsed_time(ev1), world, dev)
     score_ms = marks.durations()["score"]
+    errw |= int(st.scratch.err.item()) | int(st.scratch2.err.item())
 
-    # per-kernel device time on a single stream (untimed pass, every kernel bracketed)
+    # the same kind of steps issued eagerly from Python (one stream), timed as a whole
+    e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nxt = first + args.steps
+    e_a.record(main)
+    for k in range(3):
+        s_k = first + k % args.steps
+        st.decode_step(nxt + k, qla_dev[s_k], q_dev[s_k], out_layers=out_dev, main=main, side=main)
+    e_b.record(main)
+    torch.cuda.synchronize()
+    eager_ms = e_a.elapsed_time(e_b) / 3
+    nxt += 3
+
+    # per-kernel device time (eager, every kernel bracketed by events) and attended blocks
     iso = KernelMarks(L * 3 * 8 + 16)
     attended = torch.zeros((), dtype=torch.int64, device=dev)
     for k in range(3):
-        s_k = pre + args.warmup + k % args.steps
-        st.decode_step(s_k, qla_dev[s_k], q_dev[s_k], out_layers=out_dev, main=main, side=side, mark=iso,
+        s_k = first + k % args.steps
+        st.decode_step(nxt + k, qla_dev[s_k], q_dev[s_k], out_layers=out_dev, main=main, side=main, mark=iso,
                        count=attended)
     torch.cuda.synchronize()
+    nxt += 3
     kernel_ms = iso.durations()
     attended_per_head = float(attended.item()) / (3 * L * w.B * w.Hkv)
-    # the same steps with everything on one stream, timed as a whole
-    e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e_a.record(main)
-    for k in range(3):
-        s_k = pre + args.warmup + k % args.steps
-        st.decode_step(s_k, qla_dev[s_k], q_dev[s_k], out_layers=out_dev, main=main, side=torch.cuda.Stream(dev))
-    e_b.record(main)
-    torch.cuda.synchronize()
-    two_stream_ms = e_a.elapsed_time(e_b) / 3
 
-    # end to end: H2D of the step's queries, the C-ABI calls, D2H of the outputs
+    # end to end: every step copies its queries from pinned host memory into the
+    # graph's input buffers, replays the one-step graph and copies the outputs back
     e2e = None
     if not args.no_e2e:
-        out_host = torch.empty((L, w.B, w.Hq, w.d), dtype=torch.float32, pin_memory=True)
         q_in = torch.empty_like(q_dev[0])
         qla_in = torch.empty_like(qla_dev[0])
+        out_e2e = torch.empty((L, w.B, w.Hq, w.d), dtype=torch.float32, device=dev)
+        out_host = torch.empty((L, w.B, w.Hq, w.d), dtype=torch.float32, pin_memory=True)
+        g1 = StepGraph(st, nxt, [qla_in], [q_in], [out_e2e])
         nrep = args.steps
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
         t0 = time.perf_counter()
-        for k in range(nrep):
-            s = pre + args.warmup + (k % args.steps)
-            q_in.copy_(q_host[s - first], non_blocking=True)
-            qla_in.copy_(qla_host[s - first], non_blocking=True)
-            step(s, qla=qla_in, q=q_in)
-            out_host.copy_(out_dev, non_blocking=True)
-            torch.cuda.current_stream(dev).synchronize()
+        with torch.cuda.stream(g1.stream):
+            for k in range(nrep):
+                q_in.copy_(q_host[k % args.steps], non_blocking=True)
+                qla_in.copy_(qla_host[k % args.steps], non_blocking=True)
+                g1.replay()
+                out_host.copy_(out_e2e, non_blocking=True)
+                g1.stream.synchronize()
         e2e_s = reduce_max(time.perf_counter() - t0, world, dev)
         bi = q_in.numel() * 2 + qla_in.numel() * 2
         bo = out_host.numel() * 4
@@ -525,8 +539,7 @@ def run_gpu(args, rank, world, local_rank):
         "kernel_avg_us": {k: round(1000.0 * sum(v) / len(v), 2) for k, v in kernel_ms.items() if v},
         "attended_blocks_per_head": round(attended_per_head, 2),
         "timed_steps": [pre + args.warmup, pre + args.warmup + args.steps - 1],
-        "ms_per_step_gather_on_side_stream": two_stream_ms,
-        "host_issue_ms_per_step": 1000.0 * issue_s / args.steps,
+        "ms_per_step_eager_python": eager_ms,
         "gpu_launches": 6 * L * args.steps,
         "hostlink": hostlink,
         "clocks": clk,

@@ -189,7 +189,9 @@ OASIS_API oasis_status oasis_fetch_diff_capped(const oasis_shape* shape, const f
  *   blk2slot  device int32 [B][Hkv][nb_max]   in/out
  *   slot2blk  device int32 [B][Hkv][P]        in/out, -1 = free slot
  *   last_used device int32 [B][Hkv][P]        in/out
- *   step      the decode step number written into last_used
+ *   step      device int32 [1]: the decode step number written into last_used
+ *             (read on the device, so a captured sequence of calls can advance
+ *             it without host involvement)
  *   k_pool    device bf16 [B][Hkv][P][bs][d]  in/out (slots written for F)
  *   v_pool    device bf16 [B][Hkv][P][bs][d]  in/out
  *   err_word  device uint32 [1]               OR-ed with OASIS_EW_* bits
@@ -199,7 +201,7 @@ OASIS_API oasis_status oasis_gather_h2d(const oasis_shape* shape, const void* ho
                               const int32_t* sel, const int32_t* nsel,
                               const int32_t* fetch, const int32_t* nfetch,
                               int32_t* blk2slot, int32_t* slot2blk, int32_t* last_used,
-                              int32_t step, void* k_pool, void* v_pool,
+                              const int32_t* step, void* k_pool, void* v_pool,
                               uint32_t* err_word, oasis_stream_t stream);
 
 /*

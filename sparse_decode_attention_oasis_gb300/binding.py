@@ -55,7 +55,7 @@ _SIGS = {
     "oasis_fetch_diff_capped": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                  ctypes.c_int32, _VP, _VP, _VP], ctypes.c_int),
     "oasis_gather_h2d": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
-                          ctypes.c_int32, _VP, _VP, _VP, _VP], ctypes.c_int),
+                          _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
     "oasis_sparse_decode_attn": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                   ctypes.c_float, _VP, ctypes.c_size_t, _VP, _VP], ctypes.c_int),
     "oasis_attn_workspace_bytes": ([ctypes.POINTER(Shape)], ctypes.c_size_t),
@@ -141,10 +141,11 @@ def oasis_fetch_diff_capped(shape: Shape, scores, k_hbm, q_la, ctx_len, sel, nse
 
 
 def oasis_gather_h2d(shape: Shape, host_kv, sel, nsel, fetch, nfetch, blk2slot, slot2blk,
-                     last_used, step: int, k_pool, v_pool, err_word, stream=None):
+                     last_used, step, k_pool, v_pool, err_word, stream=None):
+    """``step`` is a device int32 tensor of one element (the LRU clock value)."""
     _check("oasis_gather_h2d", load().oasis_gather_h2d(
         ctypes.byref(shape), _ptr(host_kv), _ptr(sel), _ptr(nsel), _ptr(fetch), _ptr(nfetch),
-        _ptr(blk2slot), _ptr(slot2blk), _ptr(last_used), int(step), _ptr(k_pool), _ptr(v_pool),
+        _ptr(blk2slot), _ptr(slot2blk), _ptr(last_used), _ptr(step), _ptr(k_pool), _ptr(v_pool),
         _ptr(err_word), _stream(stream)))
 
 

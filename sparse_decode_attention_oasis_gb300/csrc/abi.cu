@@ -15,7 +15,7 @@ cudaError_t launch_topk_select(const Shape&, const float2*, const uint16_t*, con
 cudaError_t launch_fetch_diff(const Shape&, const float2*, const uint16_t*, const uint16_t*, const int*,
                               const int*, const int*, const int*, int, int*, int*, cudaStream_t);
 cudaError_t launch_gather_h2d(const Shape&, const uint16_t*, const int*, const int*, const int*, const int*,
-                              int*, int*, int*, int, uint16_t*, uint16_t*, unsigned*, cudaStream_t);
+                              int*, int*, int*, const int*, uint16_t*, uint16_t*, unsigned*, cudaStream_t);
 cudaError_t launch_sparse_decode_attn(const Shape&, const uint16_t*, const uint16_t*, const uint16_t*,
                                       const int*, const int*, const int*, const int*, float, void*, float*,
                                       cudaStream_t);
@@ -154,7 +154,7 @@ oasis_status oasis_fetch_diff_capped(const oasis_shape* shape, const float* scor
 
 oasis_status oasis_gather_h2d(const oasis_shape* shape, const void* host_kv, const int32_t* sel,
                               const int32_t* nsel, const int32_t* fetch, const int32_t* nfetch,
-                              int32_t* blk2slot, int32_t* slot2blk, int32_t* last_used, int32_t step,
+                              int32_t* blk2slot, int32_t* slot2blk, int32_t* last_used, const int32_t* step,
                               void* k_pool, void* v_pool, uint32_t* err_word, oasis_stream_t stream) {
   static const char* fn = "oasis_gather_h2d";
   oasis::Shape s;
@@ -163,8 +163,9 @@ oasis_status oasis_gather_h2d(const oasis_shape* shape, const void* host_kv, con
   REQUIRE(host_kv && aligned(host_kv, 16), "host_kv must be a 16-byte aligned pointer");
   REQUIRE(k_pool && v_pool && aligned(k_pool, 16) && aligned(v_pool, 16),
           "k_pool/v_pool must be 16-byte aligned device pointers");
-  REQUIRE(sel && nsel && fetch && nfetch && blk2slot && slot2blk && last_used && err_word,
+  REQUIRE(sel && nsel && fetch && nfetch && blk2slot && slot2blk && last_used && err_word && step,
           "table pointers must be non-NULL");
+  REQUIRE(aligned(step, 4), "step must be a 4-byte aligned device pointer");
   REQUIRE(aligned(sel, 4) && aligned(nsel, 4) && aligned(fetch, 4) && aligned(nfetch, 4) &&
               aligned(blk2slot, 4) && aligned(slot2blk, 4) && aligned(last_used, 4) && aligned(err_word, 4),
           "int32 arrays must be 4-byte aligned");

@@ -38,7 +38,7 @@ __global__ void __launch_bounds__(kGatherThreads)
 gather_h2d_kernel(Shape s, const uint16_t* __restrict__ host_kv, const int* __restrict__ sel,
                   const int* __restrict__ nsel, const int* __restrict__ fetch,
                   const int* __restrict__ nfetch, int* __restrict__ blk2slot,
-                  int* __restrict__ slot2blk, int* __restrict__ last_used, int step,
+                  int* __restrict__ slot2blk, int* __restrict__ last_used, const int* __restrict__ step_ptr,
                   uint16_t* __restrict__ k_pool, uint16_t* __restrict__ v_pool,
                   unsigned* __restrict__ err) {
   extern __shared__ __align__(16) int gsm[];
@@ -58,6 +58,7 @@ gather_h2d_kernel(Shape s, const uint16_t* __restrict__ host_kv, const int* __re
 
   // one round of independent loads: counts, lists, slot tables
   int ns = nsel[head], nf = nfetch[head];
+  const int step = *step_ptr;
   for (int i = threadIdx.x; i < Kb; i += blockDim.x) {
     S[i] = sel[(long long)head * Kb + i];
     F[i] = fetch[(long long)head * Kb + i];
@@ -210,7 +211,7 @@ size_t gather_smem_bytes(const Shape& s) { return sizeof(int) * (2 * (size_t)s.K
 
 cudaError_t launch_gather_h2d(const Shape& s, const uint16_t* host_kv, const int* sel, const int* nsel,
                               const int* fetch, const int* nfetch, int* blk2slot, int* slot2blk,
-                              int* last_used, int step, uint16_t* k_pool, uint16_t* v_pool,
+                              int* last_used, const int* step, uint16_t* k_pool, uint16_t* v_pool,
                               unsigned* err, cudaStream_t stream) {
   const size_t smem = gather_smem_bytes(s);
   if (smem > 48 * 1024) {

@@ -71,6 +71,7 @@ class DecodeState:
         self.ctx = torch.tensor(w.ctx, dtype=torch.int32, device=dev)
         self.scratch = LayerScratch(s, dev)
         self.scratch2 = None
+        self.step_dev = torch.zeros(1, dtype=torch.int32, device=dev)  # LRU clock read by the gather
         self.scale = 1.0 / math.sqrt(w.d)
         # per-layer views made once (indexing a tensor costs host time on every call)
         self.Kl = [self.K[l] for l in range(Lp)]
@@ -164,6 +165,7 @@ class DecodeState:
         sc = scratch or self.scratch
         lp, lh = layer % self.L_phys, layer % self.L_host
         st = stream or torch.cuda.current_stream(self.device)
+        step = self._step_tensor(step, st)
         K = self.K[lp]
         B.oasis_score_blocks(s, K, self.ctx, q_la, sc.scores, sc.err, st)
         B.oasis_topk_select(s, sc.scores, K, q_la, self.ctx, sc.sel, sc.nsel, st)
@@ -183,6 +185,14 @@ class DecodeState:
         return sc
 
     # ---------------------------------------------------------------- one decode step
+    def _step_tensor(self, step, stream):
+        """The LRU clock as a device int32 scalar (an int is written into step_dev on `stream`)."""
+        if isinstance(step, torch.Tensor):
+            return step
+        with torch.cuda.stream(stream):
+            self.step_dev.fill_(int(step))
+        return self.step_dev
+
     def _select(self, layer, q_la, step, sc, st, mark=None):
         s = self.shape
         lp = layer % self.L_phys
@@ -221,7 +231,7 @@ class DecodeState:
         slot = torch.gather(self.b2sl[lp].long(), 2, sel.clamp(min=0))
         return ((slot >= 0) & valid).sum()
 
-    def decode_step(self, step: int, q_la_layers, q_layers, out_layers=None, main=None, side=None,
+    def decode_step(self, step, q_la_layers, q_layers, out_layers=None, main=None, side=None,
                     mark=None, count=None):
         """All layers of one decode step, pipelined across layers.
 
@@ -238,6 +248,7 @@ class DecodeState:
         L = self.w.L
         main = main or torch.cuda.current_stream(self.device)
         side = side or main
+        step = self._step_tensor(step, main)
         if self.scratch2 is None:
             self.scratch2 = LayerScratch(self.shape, self.device)
         scr = (self.scratch, self.scratch2)
@@ -280,3 +291,35 @@ class DecodeState:
         B.oasis_append_kv(self.shape, k_new, v_new, self.ctx, self.K[lp], self.host[lh], self.blk2slot[lp],
                           self.k_pool[lp], self.v_pool[lp], advance,
                           self.scratch.err if err is None else err, st)
+
+
+class StepGraph:
+    """Decode steps captured as one CUDA graph and replayed.
+
+    ``q_la_steps[k]`` / ``q_steps[k]`` are the device inputs of captured step k
+    (per-layer tensors or [L]-leading tensors) and ``out_steps[k]`` its [L]-leading
+    fp32 output.  The LRU clock ``step`` (device int32 [1]) starts at
+    ``first_step`` and the graph itself advances it after every step, so each
+    replay continues the decode.  ``mark`` (as for decode_step) is called during
+    capture; CUDA events recorded by it become nodes of the graph.
+    """
+
+    def __init__(self, st: DecodeState, first_step: int, q_la_steps, q_steps, out_steps, mark=None):
+        self.st = st
+        dev = st.device
+        if st.scratch2 is None:
+            st.scratch2 = LayerScratch(st.shape, dev)
+        self.step = torch.full((1,), int(first_step), dtype=torch.int32, device=dev)
+        self.graph = torch.cuda.CUDAGraph()
+        self.stream = torch.cuda.Stream(dev)
+        self.stream.wait_stream(torch.cuda.current_stream(dev))
+        torch.cuda.synchronize(dev)
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            for k in range(len(q_steps)):
+                st.decode_step(self.step, q_la_steps[k], q_steps[k], out_layers=out_steps[k],
+                               main=self.stream, side=self.stream, mark=mark)
+                self.step.add_(1)
+        torch.cuda.synchronize(dev)
+
+    def replay(self):
+        self.graph.replay()
