@@ -185,6 +185,65 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- helpers
+class GraphEvents:
+    """Timing events recorded as nodes of a captured CUDA graph.
+
+    cudaEventRecordWithFlags(..., cudaEventRecordExternal) during stream capture
+    adds an event-record node; after a replay, cudaEventElapsedTime between two
+    such events gives the device time between the nodes.
+    """
+
+    def __init__(self, n):
+        import ctypes
+
+        self.ct = ctypes
+        lib = None
+        for name in ("libcudart.so.13", "libcudart.so"):
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if lib is None:
+            raise RuntimeError("libcudart not found")
+        self.lib = lib
+        lib.cudaEventCreate.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
+        lib.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+        lib.cudaEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p, ctypes.c_void_p]
+        lib.cudaEventDestroy.argtypes = [ctypes.c_void_p]
+        self.pool = []
+        for _ in range(n):
+            h = ctypes.c_void_p()
+            if lib.cudaEventCreate(ctypes.byref(h)) != 0:
+                raise RuntimeError("cudaEventCreate failed")
+            self.pool.append(h)
+        self.used = []
+        self.names = {"score", "topk"}
+
+    def __call__(self, name, stream):
+        if name not in self.names:
+            return
+        h = self.pool[len(self.used)]
+        if self.lib.cudaEventRecordWithFlags(h, self.ct.c_void_p(stream.cuda_stream), 1) != 0:
+            raise RuntimeError("cudaEventRecordWithFlags failed")
+        self.used.append((name, h))
+
+    def durations(self):
+        out = {"score": [], "topk": [], "diff": [], "gather": [], "attn": []}
+        prev = None
+        for name, h in self.used:
+            if prev is not None and prev[0] in out:
+                ms = self.ct.c_float()
+                if self.lib.cudaEventElapsedTime(self.ct.byref(ms), prev[1], h) == 0:
+                    out[prev[0]].append(ms.value)
+            prev = (name, h)
+        return out
+
+    def close(self):
+        for h in self.pool:
+            self.lib.cudaEventDestroy(h)
+
+
 class KernelMarks:
     """CUDA events recorded before/after each kernel of the decode step, per stream.
 
@@ -438,7 +497,7 @@ def run_gpu(args, rank, world, local_rank):
     # clock advanced by the graph); events around every scoring launch are graph nodes
     from sparse_decode_attention_oasis_gb300.engine import StepGraph
 
-    marks = KernelMarks(L * args.steps * 2 + 16, names={"score", "topk"})
+    marks = GraphEvents(L * args.steps * 2 + 16)
     out_steps = [torch.empty((L, w.B, w.Hq, w.d), dtype=torch.float32, device=dev) for _ in range(2)]
     ts = range(first, first + args.steps)
     graph = StepGraph(st, first, [qla_dev[s] for s in ts], [q_dev[s] for s in ts],
@@ -462,6 +521,9 @@ def run_gpu(args, rank, world, local_rank):
     ms = reduce_max(ev0.elapsed_time(ev1), world, dev)
     score_ms = marks.durations()["score"]
     errw |= int(st.scratch.err.item()) | int(st.scratch2.err.item())
+    del graph
+    torch.cuda.synchronize()
+    marks.close()
 
     # the same kind of steps issued eagerly from Python (one stream), timed as a whole
     e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

@@ -27,6 +27,59 @@ from . import binding as B
 from . import synthetic as syn
 
 
+class HugePinnedBuffer:
+    """Page-locked, device-mapped host memory backed by transparent huge pages.
+
+    The host tier is read by zero-copy loads at random block positions; on a
+    64 KiB-page host every block touches a different page, and translation misses
+    dominated the gather.  An anonymous mapping advised MADV_HUGEPAGE (512 MiB
+    pages) and then registered with cudaHostRegister(Mapped) keeps the number of
+    translations per layer small.  The memory starts zeroed.
+    """
+
+    _ALIGN = 1 << 29
+
+    def __init__(self, nbytes: int):
+        import ctypes
+
+        libc = ctypes.CDLL("libc.so.6", use_errno=True)
+        libc.mmap.restype = ctypes.c_void_p
+        libc.mmap.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                              ctypes.c_long]
+        libc.madvise.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int]
+        libc.munmap.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
+        self.libc = libc
+        self.map_bytes = nbytes + self._ALIGN
+        raw = libc.mmap(None, self.map_bytes, 0x1 | 0x2, 0x02 | 0x20, -1, 0)  # RW, private anonymous
+        if raw in (None, ctypes.c_void_p(-1).value):
+            raise RuntimeError("mmap of the host tier failed")
+        self.raw = raw
+        self.base = (raw + self._ALIGN - 1) // self._ALIGN * self._ALIGN
+        libc.madvise(ctypes.c_void_p(self.base), nbytes, 14)  # MADV_HUGEPAGE (advice only)
+        rc = torch.cuda.cudart().cudaHostRegister(self.base, nbytes, 0x1 | 0x2)  # portable | mapped
+        rc = int(rc[0] if isinstance(rc, tuple) else rc)
+        if rc != 0:
+            libc.munmap(ctypes.c_void_p(self.raw), self.map_bytes)
+            raise RuntimeError(f"cudaHostRegister of the host tier failed ({rc})")
+        self.nbytes = nbytes
+        buf = (ctypes.c_uint8 * nbytes).from_address(self.base)
+        self.tensor = torch.from_numpy(np.frombuffer(buf, dtype=np.uint8))
+
+    def close(self):
+        if getattr(self, "raw", None):
+            import ctypes
+
+            torch.cuda.cudart().cudaHostUnregister(self.base)
+            self.libc.munmap(ctypes.c_void_p(self.raw), self.map_bytes)
+            self.raw = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 def _bf16_from_bits(bits: np.ndarray, device) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
 
@@ -66,8 +119,14 @@ class DecodeState:
         self.blk2slot = torch.full((Lp, s.B, s.Hkv, s.nb_max), -1, dtype=torch.int32, device=dev)
         self.slot2blk = torch.full((Lp, s.B, s.Hkv, s.P), -1, dtype=torch.int32, device=dev)
         self.last_used = torch.full((Lp, s.B, s.Hkv, s.P), -1, dtype=torch.int32, device=dev)
-        self.host = torch.zeros((self.L_host, s.B, s.Hkv, s.nb_max, 2, 16, 128), dtype=torch.bfloat16,
-                                pin_memory=pin_host)
+        host_shape = (self.L_host, s.B, s.Hkv, s.nb_max, 2, 16, 128)
+        self._host_buf = None
+        if pin_host:
+            nbytes = int(np.prod(host_shape)) * 2
+            self._host_buf = HugePinnedBuffer(nbytes)
+            self.host = self._host_buf.tensor.view(torch.bfloat16).view(host_shape)
+        else:
+            self.host = torch.zeros(host_shape, dtype=torch.bfloat16)
         self.ctx = torch.tensor(w.ctx, dtype=torch.int32, device=dev)
         self.scratch = LayerScratch(s, dev)
         self.scratch2 = None
