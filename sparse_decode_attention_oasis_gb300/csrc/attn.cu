@@ -5,33 +5,54 @@
 // blocks selected and held on the GPU).  A = { x in S : blk2slot[x] != -1 }; for each query head
 // of the GQA group, softmax(scale * q.k) v over the valid tokens of A.
 //
-// Split-K flash decode.  Grid (split, request*KV head); a split covers
-// kAttnSplit consecutive entries of S, 4 warps take kAttnPerWarp each.  Per
-// 16-token block a warp computes S = Q K^T with the G query heads as the rows of
-// one m16n8k16 tile (rows >= G are zero), runs the online softmax in fp32 (exp2
-// with scale*log2(e) folded in), and accumulates O += P V where P is split into
-// a bf16 high part and a bf16 residual (two MMAs), so the weights carry ~16
-// significant bits.  K rows are loaded as B fragments straight from HBM with the
-// same d permutation as the Q fragments; V rows are loaded as 32-byte row
-// segments and re-paired into B fragments with byte permutes, the output column
-// of n-tile j / column n being d = 16 n + j.  The 4 warps merge in shared memory;
-// a second kernel merges the splits of each query head.
+// Split-K flash decode.  Grid (split, request*KV head); a split covers a range
+// of entries of S and its 4 warps take every 4th entry.  A warp first looks up
+// 32 entries at once (sel, then blk2slot: two rounds of loads), keeps the
+// resident ones, and streams their K and V (8 KiB per block) through a 2-stage
+// shared-memory ring with cp.async, so the next block is in flight while the
+// current one is computed.  Rows are stored with their 16-byte chunks XOR-ed by
+// (row mod 8) to spread the fragment reads over the banks.  Per block the warp
+// computes S = Q K^T with the G query heads as the rows of one m16n8k16 tile
+// (rows >= G are zero; the d axis is permuted identically for Q and K), runs the
+// online softmax in fp32 (exp2 with scale*log2(e) folded in), and accumulates
+// O += P V with P split into a bf16 high part and a bf16 residual (two MMAs, ~16
+// significant bits); V rows are re-paired into B fragments with byte permutes,
+// the output column of n-tile j / column n being d = 16 n + j.  The 4 warps merge
+// in shared memory; with one split the CTA writes the output, otherwise a second
+// kernel merges the splits of each query head.  The split count is chosen so
+// the grid covers the GPU about four times.
 #include "common.cuh"
 
 namespace oasis {
 
 constexpr int kAttnWarps = 4;
-constexpr int kAttnPerWarp = 4;
-constexpr int kAttnSplit = kAttnWarps * kAttnPerWarp;  // 16 blocks = 256 tokens per CTA
+constexpr int kStageBytes = 2 * kBS * kD * 2;                    // K + V of one block
+constexpr int kAttnSmem = kAttnWarps * 2 * kStageBytes;          // 64 KiB
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+// byte offset of 16-byte chunk c of row r in a staged 16 x 128 bf16 tile
+__device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 256 + ((c ^ (r & 7)) << 4)); }
 
 template <int G>
-__global__ void __launch_bounds__(kAttnWarps * 32, 3)
+__global__ void __launch_bounds__(kAttnWarps * 32, 2)
 attn_partial_kernel(Shape s, const uint16_t* __restrict__ q, const uint16_t* __restrict__ k_pool,
                     const uint16_t* __restrict__ v_pool, const int* __restrict__ sel,
                     const int* __restrict__ nsel, const int* __restrict__ blk2slot,
                     const int* __restrict__ ctx_len, float scale_log2, float* __restrict__ part_o,
-                    float* __restrict__ part_ml, int nsplit) {
-  __shared__ float sm_o[kAttnWarps][G][kD];
+                    float* __restrict__ part_ml, float* __restrict__ out, int nsplit, int per_split) {
+  extern __shared__ __align__(128) uint8_t asmem[];
   __shared__ float sm_m[kAttnWarps][G];
   __shared__ float sm_l[kAttnWarps][G];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -41,8 +62,9 @@ attn_partial_kernel(Shape s, const uint16_t* __restrict__ q, const uint16_t* __r
   int n = nsel[head];
   n = n < 0 ? 0 : (n > s.Kb ? s.Kb : n);
   const int ctx = ctx_len[b];
-  const int p0 = split * kAttnSplit + warp * kAttnPerWarp;
-  const int p1 = min(n, p0 + kAttnPerWarp);
+  const int p_begin = split * per_split;
+  const int p_end = min(n, p_begin + per_split);
+  const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(asmem)) + warp * 2 * kStageBytes;
 
   // Q fragments (rows g < G); chunk t+4i of the row gives words for k-steps 2i, 2i+1
   uint32_t qa[4][4];
@@ -62,98 +84,133 @@ attn_partial_kernel(Shape s, const uint16_t* __restrict__ q, const uint16_t* __r
 #pragma unroll
   for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   float m_run = neg_inf(), l_run = 0.f;
-
   const long long slot_base = (long long)head * s.P;
-  for (int p = p0; p < p1; ++p) {
-    const int x = sel[(long long)head * s.Kb + p];
-    if (x < 0 || x >= s.nb_max) continue;
-    const int slot = blk2slot[(long long)head * s.nb_max + x];
-    if (slot < 0 || slot >= s.P) continue;
-    const int ntok = min(kBS, ctx - x * kBS);
-    if (ntok <= 0) continue;
-    const uint16_t* kb = k_pool + (slot_base + slot) * kBS * kD;
-    const uint16_t* vb = v_pool + (slot_base + slot) * kBS * kD;
-    uint4 kr[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) kr[nt][i] = ldg_stream(kb + (nt * 8 + g) * kD + (t + 4 * i) * 8);
-    uint4 vr[4][2];
-    const int vrow[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) vr[r][hf] = ldg_stream(vb + vrow[r] * kD + 16 * g + 8 * hf);
 
-    float sc[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const uint32_t kw[4] = {kr[nt][i].x, kr[nt][i].y, kr[nt][i].z, kr[nt][i].w};
-          mma_bf16_16816(sc[nt][0], sc[nt][1], sc[nt][2], sc[nt][3], qa[i][2 * hh], 0u,
-                         qa[i][2 * hh + 1], 0u, kw[2 * hh], kw[2 * hh + 1]);
-        }
+  for (int base = p_begin + warp; base < p_end; base += kAttnWarps * 32) {
+    // lane j looks up entry base + 4j
+    const int p = base + kAttnWarps * lane;
+    int slot = -1, ntok = 0;
+    if (p < p_end) {
+      const int x = sel[(long long)head * s.Kb + p];
+      if (x >= 0 && x < s.nb_max) {
+        const int sl = blk2slot[(long long)head * s.nb_max + x];
+        ntok = min(kBS, ctx - x * kBS);
+        if (sl >= 0 && sl < s.P && ntok > 0) slot = sl;
       }
     }
-    // row g: tokens nt*8 + 2t + {0,1}
-    float sv[2][2];
+    unsigned mask = __ballot_sync(0xffffffffu, slot >= 0);
+    if (!mask) continue;
+    int stage = 0;
+    int cur = __ffs(mask) - 1;
+    mask &= mask - 1;
+    auto issue = [&](int st, int src_lane) {
+      const int sl = __shfl_sync(0xffffffffu, slot, src_lane);
+      const uint16_t* kb = k_pool + (slot_base + sl) * kBS * kD;
+      const uint16_t* vb = v_pool + (slot_base + sl) * kBS * kD;
+      const uint32_t dk = ring + st * kStageBytes, dv = dk + kStageBytes / 2;
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int tok = nt * 8 + 2 * t + e;
-        sv[nt][e] = tok < ntok ? sc[nt][e] * scale_log2 : neg_inf();
+      for (int j = 0; j < 8; ++j) {
+        const int c = lane + 32 * j;  // chunk of the 4 KiB tile
+        const int r = c >> 4, cc = c & 15;
+        cp_async16(dk + swz(r, cc), kb + r * kD + cc * 8);
+        cp_async16(dv + swz(r, cc), vb + r * kD + cc * 8);
       }
-    float bm = fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1]));
-    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
-    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
-    const float m_new = fmaxf(m_run, bm);  // finite: token 0 of the block is valid
-    const float alpha = exp2f(m_run - m_new);
-    float pv[2][2];
-    float rs = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        pv[nt][e] = exp2f(sv[nt][e] - m_new);
-        rs += pv[nt][e];
+      cp_async_commit();
+    };
+    issue(0, cur);
+    while (true) {
+      const int nxt = mask ? __ffs(mask) - 1 : -1;
+      if (nxt >= 0) {
+        mask &= mask - 1;
+        issue(stage ^ 1, nxt);
+        cp_async_wait<1>();
+      } else {
+        cp_async_wait<0>();
       }
-    rs += __shfl_xor_sync(0xffffffffu, rs, 1);
-    rs += __shfl_xor_sync(0xffffffffu, rs, 2);
-    l_run = l_run * alpha + rs;
-    m_run = m_new;
+      __syncwarp();
+      const int nt_cur = __shfl_sync(0xffffffffu, ntok, cur);
+      const uint32_t dk = ring + stage * kStageBytes, dv = dk + kStageBytes / 2;
+      float sc[2][4];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) { o[j][0] *= alpha; o[j][1] *= alpha; }
-    const uint32_t ph0 = pack_bf16x2(pv[0][0], pv[0][1]);
-    const uint32_t ph1 = pack_bf16x2(pv[1][0], pv[1][1]);
-    const uint32_t pl0 = pack_bf16x2(pv[0][0] - bf_lo(ph0), pv[0][1] - bf_hi(ph0));
-    const uint32_t pl1 = pack_bf16x2(pv[1][0] - bf_lo(ph1), pv[1][1] - bf_hi(ph1));
+      for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const uint32_t sel_half = (j & 1) ? 0x7632u : 0x5410u;
-      const int wi = j >> 1;
-      const uint32_t w0[4] = {vr[0][wi >> 2].x, vr[0][wi >> 2].y, vr[0][wi >> 2].z, vr[0][wi >> 2].w};
-      const uint32_t w1[4] = {vr[1][wi >> 2].x, vr[1][wi >> 2].y, vr[1][wi >> 2].z, vr[1][wi >> 2].w};
-      const uint32_t w2[4] = {vr[2][wi >> 2].x, vr[2][wi >> 2].y, vr[2][wi >> 2].z, vr[2][wi >> 2].w};
-      const uint32_t w3[4] = {vr[3][wi >> 2].x, vr[3][wi >> 2].y, vr[3][wi >> 2].z, vr[3][wi >> 2].w};
-      const uint32_t b0 = __byte_perm(w0[wi & 3], w1[wi & 3], sel_half);
-      const uint32_t b1 = __byte_perm(w2[wi & 3], w3[wi & 3], sel_half);
-      mma_bf16_16816(o[j][0], o[j][1], o[j][2], o[j][3], ph0, 0u, ph1, 0u, b0, b1);
-      mma_bf16_16816(o[j][0], o[j][1], o[j][2], o[j][3], pl0, 0u, pl1, 0u, b0, b1);
+      for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const uint4 kv = lds_v4(dk + swz(nt * 8 + g, t + 4 * i));
+          const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+            mma_bf16_16816(sc[nt][0], sc[nt][1], sc[nt][2], sc[nt][3], qa[i][2 * hh], 0u, qa[i][2 * hh + 1], 0u,
+                           kw[2 * hh], kw[2 * hh + 1]);
+        }
+      }
+      float sv[2][2];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int tok = nt * 8 + 2 * t + e;
+          sv[nt][e] = tok < nt_cur ? sc[nt][e] * scale_log2 : neg_inf();
+        }
+      float bm = fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1]));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+      const float m_new = fmaxf(m_run, bm);  // finite: token 0 of the block is valid
+      const float alpha = exp2f(m_run - m_new);
+      float pv[2][2];
+      float rs = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          pv[nt][e] = exp2f(sv[nt][e] - m_new);
+          rs += pv[nt][e];
+        }
+      rs += __shfl_xor_sync(0xffffffffu, rs, 1);
+      rs += __shfl_xor_sync(0xffffffffu, rs, 2);
+      l_run = l_run * alpha + rs;
+      m_run = m_new;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) { o[j][0] *= alpha; o[j][1] *= alpha; }
+      const uint32_t ph0 = pack_bf16x2(pv[0][0], pv[0][1]);
+      const uint32_t ph1 = pack_bf16x2(pv[1][0], pv[1][1]);
+      const uint32_t pl0 = pack_bf16x2(pv[0][0] - bf_lo(ph0), pv[0][1] - bf_hi(ph0));
+      const uint32_t pl1 = pack_bf16x2(pv[1][0] - bf_lo(ph1), pv[1][1] - bf_hi(ph1));
+      uint4 vr[4][2];
+      const int vrow[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) vr[r][hf] = lds_v4(dv + swz(vrow[r], 2 * g + hf));
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t sel_half = (j & 1) ? 0x7632u : 0x5410u;
+        const int wi = j >> 1;
+        const uint32_t w0[4] = {vr[0][wi >> 2].x, vr[0][wi >> 2].y, vr[0][wi >> 2].z, vr[0][wi >> 2].w};
+        const uint32_t w1[4] = {vr[1][wi >> 2].x, vr[1][wi >> 2].y, vr[1][wi >> 2].z, vr[1][wi >> 2].w};
+        const uint32_t w2[4] = {vr[2][wi >> 2].x, vr[2][wi >> 2].y, vr[2][wi >> 2].z, vr[2][wi >> 2].w};
+        const uint32_t w3[4] = {vr[3][wi >> 2].x, vr[3][wi >> 2].y, vr[3][wi >> 2].z, vr[3][wi >> 2].w};
+        const uint32_t b0 = __byte_perm(w0[wi & 3], w1[wi & 3], sel_half);
+        const uint32_t b1 = __byte_perm(w2[wi & 3], w3[wi & 3], sel_half);
+        mma_bf16_16816(o[j][0], o[j][1], o[j][2], o[j][3], ph0, 0u, ph1, 0u, b0, b1);
+        mma_bf16_16816(o[j][0], o[j][1], o[j][2], o[j][3], pl0, 0u, pl1, 0u, b0, b1);
+      }
+      __syncwarp();  // the stage is refilled by the next issue
+      if (nxt < 0) break;
+      cur = nxt;
+      stage ^= 1;
     }
   }
 
-  // merge the warps of this split
+  // merge the warps of this split (the staging ring is reused for the partial outputs)
+  __syncthreads();
+  float* sm_o = reinterpret_cast<float*>(asmem);  // [kAttnWarps][G][kD]
   if (g < G) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      sm_o[warp][g][32 * t + j] = o[j][0];
-      sm_o[warp][g][32 * t + 16 + j] = o[j][1];
+      sm_o[(warp * G + g) * kD + 32 * t + j] = o[j][0];
+      sm_o[(warp * G + g) * kD + 32 * t + 16 + j] = o[j][1];
     }
     if (t == 0) { sm_m[warp][g] = m_run; sm_l[warp][g] = l_run; }
   }
@@ -169,14 +226,18 @@ attn_partial_kernel(Shape s, const uint16_t* __restrict__ q, const uint16_t* __r
 #pragma unroll
       for (int w = 0; w < kAttnWarps; ++w) {
         const float f = exp2f(sm_m[w][gg] - M);
-        acc += f * sm_o[w][gg][dd];
+        acc += f * sm_o[(w * G + gg) * kD + dd];
         L += f * sm_l[w][gg];
       }
     }
-    part_o[(pbase + gg) * kD + dd] = acc;
-    if (dd == 0) {
-      part_ml[(pbase + gg) * 2] = M;
-      part_ml[(pbase + gg) * 2 + 1] = L;
+    if (nsplit == 1) {
+      out[((long long)b * s.Hq + h * G + gg) * kD + dd] = L > 0.f ? acc / L : 0.f;
+    } else {
+      part_o[(pbase + gg) * kD + dd] = acc;
+      if (dd == 0) {
+        part_ml[(pbase + gg) * 2] = M;
+        part_ml[(pbase + gg) * 2 + 1] = L;
+      }
     }
   }
 }
@@ -210,7 +271,16 @@ attn_combine_kernel(Shape s, const float* __restrict__ part_o, const float* __re
       make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
-int attn_nsplit(const Shape& s) { return (s.Kb + kAttnSplit - 1) / kAttnSplit; }
+// Splits per head: enough thread blocks to cover the GPU about four times, each
+// split holding at least 4 entries of S.
+int attn_nsplit(const Shape& s) {
+  const int heads = s.B * s.Hkv;
+  const int target = 4 * sm_count();
+  int ns = (target + heads - 1) / heads;
+  const int max_ns = (s.Kb + 3) / 4;
+  if (ns > max_ns) ns = max_ns;
+  return ns < 1 ? 1 : ns;
+}
 
 size_t attn_workspace_bytes(const Shape& s) {
   const size_t rows = (size_t)s.B * s.Hkv * attn_nsplit(s) * (s.Hq / s.Hkv);
@@ -222,6 +292,7 @@ cudaError_t launch_sparse_decode_attn(const Shape& s, const uint16_t* q, const u
                                       const int* blk2slot, const int* ctx, float scale, void* ws,
                                       float* out, cudaStream_t stream) {
   const int nsplit = attn_nsplit(s);
+  const int per_split = (s.Kb + nsplit - 1) / nsplit;
   const int G = s.Hq / s.Hkv;
   const size_t rows = (size_t)s.B * s.Hkv * nsplit * G;
   float* part_o = static_cast<float*>(ws);
@@ -229,15 +300,24 @@ cudaError_t launch_sparse_decode_attn(const Shape& s, const uint16_t* q, const u
   const float scale_log2 = scale * 1.4426950408889634f;
   dim3 grid(nsplit, s.B * s.Hkv);
   dim3 block(kAttnWarps * 32);
+  static int attr_cache[4][kMaxDevicesCached] = {};
+  cudaError_t e = cudaSuccess;
+#define OASIS_ATTN_LAUNCH(GG, IDX)                                                                              \
+  e = ensure_dyn_smem((const void*)attn_partial_kernel<GG>, kAttnSmem, attr_cache[IDX]);                      \
+  if (e != cudaSuccess) return e;                                                                              \
+  attn_partial_kernel<GG><<<grid, block, kAttnSmem, stream>>>(s, q, k_pool, v_pool, sel, nsel, blk2slot, ctx,  \
+                                                              scale_log2, part_o, part_ml, out, nsplit,       \
+                                                              per_split);
   switch (G) {
-    case 1: attn_partial_kernel<1><<<grid, block, 0, stream>>>(s, q, k_pool, v_pool, sel, nsel, blk2slot, ctx, scale_log2, part_o, part_ml, nsplit); break;
-    case 2: attn_partial_kernel<2><<<grid, block, 0, stream>>>(s, q, k_pool, v_pool, sel, nsel, blk2slot, ctx, scale_log2, part_o, part_ml, nsplit); break;
-    case 4: attn_partial_kernel<4><<<grid, block, 0, stream>>>(s, q, k_pool, v_pool, sel, nsel, blk2slot, ctx, scale_log2, part_o, part_ml, nsplit); break;
-    case 8: attn_partial_kernel<8><<<grid, block, 0, stream>>>(s, q, k_pool, v_pool, sel, nsel, blk2slot, ctx, scale_log2, part_o, part_ml, nsplit); break;
+    case 1: OASIS_ATTN_LAUNCH(1, 0) break;
+    case 2: OASIS_ATTN_LAUNCH(2, 1) break;
+    case 4: OASIS_ATTN_LAUNCH(4, 2) break;
+    case 8: OASIS_ATTN_LAUNCH(8, 3) break;
     default: return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+#undef OASIS_ATTN_LAUNCH
+  e = cudaGetLastError();
+  if (e != cudaSuccess || nsplit == 1) return e;
   const int rowsq = s.B * s.Hq;
   attn_combine_kernel<<<(rowsq + 3) / 4, 128, 0, stream>>>(s, part_o, part_ml, nsplit, out);
   return cudaGetLastError();

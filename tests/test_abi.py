@@ -71,6 +71,9 @@ def test_null_and_misaligned_pointers_are_invalid(lib):
 
 def test_workspace_size_formula(lib):
     s = _shape()
-    # 2 requests * 8 KV heads * 2 splits * 4 query heads * (128 + 2) floats
-    assert binding.oasis_attn_workspace_bytes(s) == 2 * 8 * 2 * 4 * 130 * 4
+    # splits x (2 requests * 8 KV heads * 4 query heads) rows of (128 + 2) floats;
+    # the split count (1 .. Kb/4) follows the device's SM count
+    row = 2 * 8 * 4 * 130 * 4
+    ws = binding.oasis_attn_workspace_bytes(s)
+    assert ws % row == 0 and 1 <= ws // row <= 32 // 4
     assert binding.oasis_attn_workspace_bytes(_shape(d=64)) == 0
