@@ -537,17 +537,31 @@ def run_gpu(args, rank, world, local_rank):
     eager_ms = e_a.elapsed_time(e_b) / 3
     nxt += 3
 
-    # per-kernel device time (eager, every kernel bracketed by events) and attended blocks
-    iso = KernelMarks(L * 3 * 8 + 16)
-    attended = torch.zeros((), dtype=torch.int64, device=dev)
+    # per-kernel device time: one decode step captured with an event node around
+    # every kernel (no host in the loop), replayed 3 times
+    iso = GraphEvents(L * 10 + 16)
+    iso.names = {"score", "topk", "diff", "end", "gather", "gather_end", "attn", "attn_end"}
+    g_iso = StepGraph(st, nxt, [qla_dev[first]], [q_dev[first]], [out_dev], mark=iso)
+    kernel_ms = {k: [] for k in ("score", "topk", "diff", "gather", "attn")}
     for k in range(3):
+        with torch.cuda.stream(g_iso.stream):
+            g_iso.replay()
+        torch.cuda.synchronize()
+        for name, v in iso.durations().items():
+            kernel_ms[name] += v
+    nxt += 3
+    del g_iso
+    torch.cuda.synchronize()
+    iso.close()
+    # attended blocks (selected and resident) per head, counted on eager steps
+    attended = torch.zeros((), dtype=torch.int64, device=dev)
+    for k in range(2):
         s_k = first + k % args.steps
-        st.decode_step(nxt + k, qla_dev[s_k], q_dev[s_k], out_layers=out_dev, main=main, side=main, mark=iso,
+        st.decode_step(nxt + k, qla_dev[s_k], q_dev[s_k], out_layers=out_dev, main=main, side=main,
                        count=attended)
     torch.cuda.synchronize()
-    nxt += 3
-    kernel_ms = iso.durations()
-    attended_per_head = float(attended.item()) / (3 * L * w.B * w.Hkv)
+    nxt += 2
+    attended_per_head = float(attended.item()) / (2 * L * w.B * w.Hkv)
 
     # end to end: every step copies its queries from pinned host memory into the
     # graph's input buffers, replays the one-step graph and copies the outputs back
