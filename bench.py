@@ -53,6 +53,9 @@ def parse():
                     help="physical host-tier layers (0 = all layers if host memory allows)")
     ap.add_argument("--preroll", type=int, default=40,
                     help="untimed decode steps run first, so the timed steps see a warmed-up resident set")
+    ap.add_argument("--copy", default="carry", choices=["carry", "gather"],
+                    help="carry: the host copy of layer l rides in layer l+1's scoring launch; "
+                         "gather: one gather launch per layer after its selection")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-hostlink", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -229,7 +232,7 @@ class GraphEvents:
         self.used.append((name, h))
 
     def durations(self):
-        out = {"score": [], "topk": [], "diff": [], "gather": [], "attn": []}
+        out = {"score": [], "topk": [], "diff": [], "assign": [], "copy": [], "gather": [], "attn": []}
         prev = None
         for name, h in self.used:
             if prev is not None and prev[0] in out:
@@ -267,7 +270,7 @@ class KernelMarks:
 
     def durations(self):
         """Per kernel name, the list of launch durations in ms (consecutive marks on one stream)."""
-        out = {"score": [], "topk": [], "diff": [], "gather": [], "attn": []}
+        out = {"score": [], "topk": [], "diff": [], "assign": [], "copy": [], "gather": [], "attn": []}
         last = {}
         for name, stream, ev in self.used:
             key = id(stream)
@@ -353,8 +356,9 @@ def measure_hostlink(st, qla0, dev):
 
     w, s, sc = st.w, st.shape, st.scratch
     main = torch.cuda.current_stream(dev)
-    best = None
-    for rep in range(3):
+    best = {"gather": None, "copy": None}
+    for rep in range(6):
+        which = "gather" if rep % 2 == 0 else "copy"
         st.b2sl[0].fill_(-1)
         st.s2bl[0].fill_(-1)
         st.lul[0].fill_(-1)
@@ -362,16 +366,23 @@ def measure_hostlink(st, qla0, dev):
         B.oasis_topk_select(s, sc.scores, st.Kl[0], qla0[0], st.ctx, sc.sel, sc.nsel, main)
         B.oasis_fetch_diff_capped(s, sc.scores, st.Kl[0], qla0[0], st.ctx, sc.sel, sc.nsel, st.b2sl[0], w.Kb,
                                   sc.fetch, sc.nfetch, main)
+        if which == "copy":  # the table half first, untimed: the copy kernel alone is timed
+            B.oasis_assign_slots(s, sc.sel, sc.nsel, sc.fetch, sc.nfetch, st.b2sl[0], st.s2bl[0], st.lul[0],
+                                 st.step_dev, sc.err, main)
         torch.cuda.synchronize()
         nfetch = int(sc.nfetch.sum().item())
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(main)
-        B.oasis_gather_h2d(s, st.hostl[0], sc.sel, sc.nsel, sc.fetch, sc.nfetch, st.b2sl[0], st.s2bl[0], st.lul[0],
-                           st.step_dev, st.kpl[0], st.vpl[0], sc.err, main)
+        if which == "gather":
+            B.oasis_gather_h2d(s, st.hostl[0], sc.sel, sc.nsel, sc.fetch, sc.nfetch, st.b2sl[0], st.s2bl[0],
+                               st.lul[0], st.step_dev, st.kpl[0], st.vpl[0], sc.err, main)
+        else:
+            B.oasis_copy_fetched(s, st.hostl[0], sc.fetch, sc.nfetch, st.b2sl[0], st.kpl[0], st.vpl[0], sc.err,
+                                 main)
         e1.record(main)
         torch.cuda.synchronize()
         gbs = nfetch * 2 * w.bs * w.d * 2 / (e0.elapsed_time(e1) / 1000.0) / 1e9
-        best = gbs if best is None else max(best, gbs)
+        best[which] = gbs if best[which] is None else max(best[which], gbs)
     src = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
     dst = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
     peak = 0.0
@@ -383,9 +394,10 @@ def measure_hostlink(st, qla0, dev):
         torch.cuda.synchronize()
         peak = max(peak, (1 << 30) / (e0.elapsed_time(e1) / 1000.0) / 1e9)
     del src, dst
-    return {"kernel": "gather_h2d (fetch-all, one layer)", "bound": "host link", "achieved": best,
+    return {"kernel": "gather_h2d (fetch-all, one layer)", "bound": "host link", "achieved": best["gather"],
             "peak": peak, "peak_kind": "measured: pinned cudaMemcpy H2D of 1 GiB", "unit": "GB/s",
-            "frac": best / peak, "bytes_per_launch": nfetch * 2 * w.bs * w.d * 2}
+            "frac": best["gather"] / peak, "bytes_per_launch": nfetch * 2 * w.bs * w.d * 2,
+            "copy_fetched_achieved": best["copy"], "copy_fetched_frac": best["copy"] / peak}
 
 
 # --------------------------------------------------------------------------- reference arm
@@ -429,6 +441,17 @@ def host_layers_for(w, requested: int) -> int:
         return w.L
     fit = int(0.6 * avail // per_layer)
     return max(2, min(w.L, fit))
+
+
+def launches_per_step(st, copy):
+    """Kernels of this library one decode step launches (the graph's own LRU-clock
+    increment is a PyTorch kernel and is not counted)."""
+    s = st.shape
+    G = s.Hq // s.Hkv
+    nsplit = st.scratch.ws_bytes // (s.B * s.Hkv * G * (s.d + 2) * 4)
+    attn = 1 if nsplit <= 1 else 2  # split-K partials, then the combine kernel
+    per_layer = 4 + attn  # score (carrying the previous layer's copy), topk, diff, assign or gather
+    return st.w.L * per_layer + (1 if copy == "carry" else 0)
 
 
 def run_gpu(args, rank, world, local_rank):
@@ -486,7 +509,7 @@ def run_gpu(args, rank, world, local_rank):
 
     def step(s, mark=None, qla=None, q=None):
         st.decode_step(s, qla if qla is not None else qla_dev[s], q if q is not None else q_dev[s],
-                       out_layers=out_dev, main=main, side=side, mark=mark)
+                       out_layers=out_dev, main=main, side=side, mark=mark, copy=args.copy)
 
     for s in range(pre + args.warmup):
         step(s)
@@ -501,7 +524,7 @@ def run_gpu(args, rank, world, local_rank):
     out_steps = [torch.empty((L, w.B, w.Hq, w.d), dtype=torch.float32, device=dev) for _ in range(2)]
     ts = range(first, first + args.steps)
     graph = StepGraph(st, first, [qla_dev[s] for s in ts], [q_dev[s] for s in ts],
-                      [out_steps[k % 2] for k in range(args.steps)], mark=marks)
+                      [out_steps[k % 2] for k in range(args.steps)], mark=marks, copy=args.copy)
     gstream = graph.stream
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local_rank)
@@ -531,7 +554,8 @@ def run_gpu(args, rank, world, local_rank):
     e_a.record(main)
     for k in range(3):
         s_k = first + k % args.steps
-        st.decode_step(nxt + k, qla_dev[s_k], q_dev[s_k], out_layers=out_dev, main=main, side=main)
+        st.decode_step(nxt + k, qla_dev[s_k], q_dev[s_k], out_layers=out_dev, main=main, side=main,
+                       copy=args.copy)
     e_b.record(main)
     torch.cuda.synchronize()
     eager_ms = e_a.elapsed_time(e_b) / 3
@@ -540,9 +564,9 @@ def run_gpu(args, rank, world, local_rank):
     # per-kernel device time: one decode step captured with an event node around
     # every kernel (no host in the loop), replayed 3 times
     iso = GraphEvents(L * 10 + 16)
-    iso.names = {"score", "topk", "diff", "end", "gather", "gather_end", "attn", "attn_end"}
-    g_iso = StepGraph(st, nxt, [qla_dev[first]], [q_dev[first]], [out_dev], mark=iso)
-    kernel_ms = {k: [] for k in ("score", "topk", "diff", "gather", "attn")}
+    iso.names = {"score", "topk", "diff", "end", "assign", "copy", "gather", "gather_end", "attn", "attn_end"}
+    g_iso = StepGraph(st, nxt, [qla_dev[first]], [q_dev[first]], [out_dev], mark=iso, copy=args.copy)
+    kernel_ms = {k: [] for k in ("score", "topk", "diff", "assign", "copy", "gather", "attn")}
     for k in range(3):
         with torch.cuda.stream(g_iso.stream):
             g_iso.replay()
@@ -558,7 +582,7 @@ def run_gpu(args, rank, world, local_rank):
     for k in range(2):
         s_k = first + k % args.steps
         st.decode_step(nxt + k, qla_dev[s_k], q_dev[s_k], out_layers=out_dev, main=main, side=main,
-                       count=attended)
+                       count=attended, copy=args.copy)
     torch.cuda.synchronize()
     nxt += 2
     attended_per_head = float(attended.item()) / (2 * L * w.B * w.Hkv)
@@ -571,7 +595,7 @@ def run_gpu(args, rank, world, local_rank):
         qla_in = torch.empty_like(qla_dev[0])
         out_e2e = torch.empty((L, w.B, w.Hq, w.d), dtype=torch.float32, device=dev)
         out_host = torch.empty((L, w.B, w.Hq, w.d), dtype=torch.float32, pin_memory=True)
-        g1 = StepGraph(st, nxt, [qla_in], [q_in], [out_e2e])
+        g1 = StepGraph(st, nxt, [qla_in], [q_in], [out_e2e], copy=args.copy)
         nrep = args.steps
         torch.cuda.synchronize()
         if world > 1:
@@ -616,7 +640,8 @@ def run_gpu(args, rank, world, local_rank):
         "attended_blocks_per_head": round(attended_per_head, 2),
         "timed_steps": [pre + args.warmup, pre + args.warmup + args.steps - 1],
         "ms_per_step_eager_python": eager_ms,
-        "gpu_launches": 6 * L * args.steps,
+        "gpu_launches": launches_per_step(st, args.copy) * args.steps,
+        "copy_mode": args.copy,
         "hostlink": hostlink,
         "clocks": clk,
         "e2e": e2e,

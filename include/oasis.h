@@ -117,6 +117,10 @@ OASIS_API const char* oasis_last_error(void);
  * rounding of the 1/sqrt(d) product); it is an upper bound on the error of
  * fp32-accumulated bf16 products with a wide margin.  Selection never trusts
  * s~ inside this interval: it re-scores those blocks exactly.
+ * Two kernels implement it: by default warp-level mma.sync tiles fed by direct
+ * 16-byte loads; with the environment variable OASIS_SCORE_KERNEL=tc (read at
+ * every call) a tcgen05/TMA/TMEM kernel.  Their s~ may differ inside the bound;
+ * everything selection derives from them is identical.
  */
 OASIS_API oasis_status oasis_score_blocks(const oasis_shape* shape, const void* k_hbm,
                                 const int32_t* ctx_len, const void* q_la,
@@ -203,6 +207,61 @@ OASIS_API oasis_status oasis_gather_h2d(const oasis_shape* shape, const void* ho
                               int32_t* blk2slot, int32_t* slot2blk, int32_t* last_used,
                               const int32_t* step, void* k_pool, void* v_pool,
                               uint32_t* err_word, oasis_stream_t stream);
+
+/*
+ * a4, split in two halves so that the host-link copy can leave the critical path
+ * (prefetching ahead of use is the point of the method: OasisKV abstract,
+ * metalmedia.ai page, Figure 7 caption).  The three calls below together give
+ * exactly the tables and pools of oasis_gather_h2d.
+ *
+ * oasis_assign_slots: the table half of oasis_gather_h2d - candidate slots,
+ *   evictions, the new blk2slot/slot2blk entries and the LRU clock - with the
+ *   same arguments minus host_kv, k_pool and v_pool.  The pools are not touched:
+ *   until the data half has run, the slots assigned to F hold stale data.
+ */
+OASIS_API oasis_status oasis_assign_slots(const oasis_shape* shape, const int32_t* sel,
+                                          const int32_t* nsel, const int32_t* fetch,
+                                          const int32_t* nfetch, int32_t* blk2slot,
+                                          int32_t* slot2blk, int32_t* last_used,
+                                          const int32_t* step, uint32_t* err_word,
+                                          oasis_stream_t stream);
+
+/*
+ * oasis_copy_fetched: the data half.  For every entry x = fetch[b][h][i],
+ *   i < nfetch[b][h], copies K and V of block x from host_kv into slot
+ *   blk2slot[b][h][x] of k_pool/v_pool.  It must run after the
+ *   oasis_assign_slots call of the same fetch list and before anything reads
+ *   those slots.  An entry whose block has no slot (-1) is skipped; a block or
+ *   slot index out of range sets OASIS_EW_BAD_BLOCK / OASIS_EW_BAD_SLOT.
+ * Arguments:
+ *   host_kv        as for oasis_gather_h2d (mapped page-locked host memory)
+ *   fetch, nfetch  from oasis_fetch_diff_capped (read only)
+ *   blk2slot       device int32 [B][Hkv][nb_max] after oasis_assign_slots (read only)
+ *   k_pool, v_pool device bf16 [B][Hkv][P][bs][d]   slots of F written
+ *   err_word       device uint32 [1], required
+ */
+OASIS_API oasis_status oasis_copy_fetched(const oasis_shape* shape, const void* host_kv,
+                                          const int32_t* fetch, const int32_t* nfetch,
+                                          const int32_t* blk2slot, void* k_pool, void* v_pool,
+                                          uint32_t* err_word, oasis_stream_t stream);
+
+/*
+ * oasis_score_blocks_copy: oasis_score_blocks of one layer and
+ *   oasis_copy_fetched of another (the copy arguments may belong to any layer
+ *   of the same shape; they must not alias k_hbm, q_la or scores) in one launch.
+ *   Each warp stages its first fetched block from the host before it scores and
+ *   writes it to the slot after, so the host-link latency overlaps the HBM-bound
+ *   scoring.  Results are those of the two calls made one after the other.
+ *   err_word is required (it receives both calls' bits).  With
+ *   OASIS_SCORE_KERNEL=tc the two are launched one after the other instead.
+ */
+OASIS_API oasis_status oasis_score_blocks_copy(const oasis_shape* shape, const void* k_hbm,
+                                               const int32_t* ctx_len, const void* q_la,
+                                               float* scores, const void* host_kv,
+                                               const int32_t* fetch, const int32_t* nfetch,
+                                               const int32_t* blk2slot, void* k_pool,
+                                               void* v_pool, uint32_t* err_word,
+                                               oasis_stream_t stream);
 
 /*
  * a5. Block-sparse paged decode attention.

@@ -56,6 +56,11 @@ _SIGS = {
                                  ctypes.c_int32, _VP, _VP, _VP], ctypes.c_int),
     "oasis_gather_h2d": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                           _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
+    "oasis_assign_slots": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP],
+                           ctypes.c_int),
+    "oasis_copy_fetched": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
+    "oasis_score_blocks_copy": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                 _VP, _VP, _VP], ctypes.c_int),
     "oasis_sparse_decode_attn": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                   ctypes.c_float, _VP, ctypes.c_size_t, _VP, _VP], ctypes.c_int),
     "oasis_attn_workspace_bytes": ([ctypes.POINTER(Shape)], ctypes.c_size_t),
@@ -147,6 +152,31 @@ def oasis_gather_h2d(shape: Shape, host_kv, sel, nsel, fetch, nfetch, blk2slot, 
         ctypes.byref(shape), _ptr(host_kv), _ptr(sel), _ptr(nsel), _ptr(fetch), _ptr(nfetch),
         _ptr(blk2slot), _ptr(slot2blk), _ptr(last_used), _ptr(step), _ptr(k_pool), _ptr(v_pool),
         _ptr(err_word), _stream(stream)))
+
+
+def oasis_assign_slots(shape: Shape, sel, nsel, fetch, nfetch, blk2slot, slot2blk, last_used, step,
+                       err_word, stream=None):
+    """Table half of the gather (slots, evictions, LRU clock); the pools are not touched."""
+    _check("oasis_assign_slots", load().oasis_assign_slots(
+        ctypes.byref(shape), _ptr(sel), _ptr(nsel), _ptr(fetch), _ptr(nfetch), _ptr(blk2slot),
+        _ptr(slot2blk), _ptr(last_used), _ptr(step), _ptr(err_word), _stream(stream)))
+
+
+def oasis_copy_fetched(shape: Shape, host_kv, fetch, nfetch, blk2slot, k_pool, v_pool, err_word,
+                       stream=None):
+    """Data half of the gather: host tier -> the slots oasis_assign_slots gave the fetch list."""
+    _check("oasis_copy_fetched", load().oasis_copy_fetched(
+        ctypes.byref(shape), _ptr(host_kv), _ptr(fetch), _ptr(nfetch), _ptr(blk2slot), _ptr(k_pool),
+        _ptr(v_pool), _ptr(err_word), _stream(stream)))
+
+
+def oasis_score_blocks_copy(shape: Shape, k_hbm, ctx_len, q_la, scores, host_kv, fetch, nfetch,
+                            blk2slot, k_pool, v_pool, err_word, stream=None):
+    """Block scoring of one layer carrying the data half of another layer's gather."""
+    _check("oasis_score_blocks_copy", load().oasis_score_blocks_copy(
+        ctypes.byref(shape), _ptr(k_hbm), _ptr(ctx_len), _ptr(q_la), _ptr(scores), _ptr(host_kv),
+        _ptr(fetch), _ptr(nfetch), _ptr(blk2slot), _ptr(k_pool), _ptr(v_pool), _ptr(err_word),
+        _stream(stream)))
 
 
 def oasis_sparse_decode_attn(shape: Shape, q, k_pool, v_pool, sel, nsel, blk2slot, ctx_len,

@@ -4,7 +4,7 @@
 #include <cstring>
 #include <string>
 
-#include "common.cuh"
+#include "fetch_copy.cuh"
 
 namespace oasis {
 cudaError_t launch_score_blocks(const Shape&, const uint16_t*, const int*, const uint16_t*, float2*, cudaStream_t);
@@ -20,6 +20,11 @@ cudaError_t launch_sparse_decode_attn(const Shape&, const uint16_t*, const uint1
                                       const int*, const int*, const int*, const int*, float, void*, float*,
                                       cudaStream_t);
 size_t attn_workspace_bytes(const Shape&);
+cudaError_t launch_assign_slots(const Shape&, const int*, const int*, const int*, const int*, int*, int*, int*,
+                                const int*, unsigned*, cudaStream_t);
+cudaError_t launch_copy_fetched(const Shape&, const CopyJob&, cudaStream_t);
+cudaError_t launch_score_blocks_copy(const Shape&, const uint16_t*, const int*, const uint16_t*, float2*,
+                                     const CopyJob&, cudaStream_t);
 cudaError_t launch_append_kv(const Shape&, const uint16_t*, const uint16_t*, int*, uint16_t*, uint16_t*, const int*,
                              uint16_t*, uint16_t*, int, unsigned*, cudaStream_t);
 size_t topk_smem_bytes(const Shape&);
@@ -152,6 +157,17 @@ oasis_status oasis_fetch_diff_capped(const oasis_shape* shape, const float* scor
   return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
 }
 
+// Device address of page-locked mapped host memory (NULL if `p` is not such memory).
+static void* mapped_host_ptr(const void* p) {
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (attr.type != cudaMemoryTypeHost) return nullptr;
+  return attr.devicePointer;
+}
+
 oasis_status oasis_gather_h2d(const oasis_shape* shape, const void* host_kv, const int32_t* sel,
                               const int32_t* nsel, const int32_t* fetch, const int32_t* nfetch,
                               int32_t* blk2slot, int32_t* slot2blk, int32_t* last_used, const int32_t* step,
@@ -184,15 +200,83 @@ oasis_status oasis_gather_h2d(const oasis_shape* shape, const void* host_kv, con
   return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
 }
 
-// Device address of page-locked mapped host memory (NULL if `p` is not such memory).
-static void* mapped_host_ptr(const void* p) {
-  cudaPointerAttributes attr;
-  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
-    cudaGetLastError();
-    return nullptr;
+
+oasis_status oasis_assign_slots(const oasis_shape* shape, const int32_t* sel, const int32_t* nsel,
+                                const int32_t* fetch, const int32_t* nfetch, int32_t* blk2slot,
+                                int32_t* slot2blk, int32_t* last_used, const int32_t* step, uint32_t* err_word,
+                                oasis_stream_t stream) {
+  static const char* fn = "oasis_assign_slots";
+  oasis::Shape s;
+  oasis_status st = check_shape(shape, fn, &s);
+  if (st != OASIS_OK) return st;
+  REQUIRE(sel && nsel && fetch && nfetch && blk2slot && slot2blk && last_used && err_word && step,
+          "table pointers must be non-NULL");
+  REQUIRE(aligned(sel, 4) && aligned(nsel, 4) && aligned(fetch, 4) && aligned(nfetch, 4) &&
+              aligned(blk2slot, 4) && aligned(slot2blk, 4) && aligned(last_used, 4) && aligned(err_word, 4) &&
+              aligned(step, 4),
+          "int32 arrays must be 4-byte aligned");
+  cudaError_t e = oasis::launch_assign_slots(s, sel, nsel, fetch, nfetch, blk2slot, slot2blk, last_used, step,
+                                             err_word, (cudaStream_t)stream);
+  return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
+}
+
+// Validate the copy arguments and build the job (device address of the host tier).
+static oasis_status make_copy_job(const char* fn, const void* host_kv, const int32_t* fetch,
+                                  const int32_t* nfetch, const int32_t* blk2slot, void* k_pool, void* v_pool,
+                                  uint32_t* err_word, oasis::CopyJob* job) {
+  REQUIRE(host_kv && aligned(host_kv, 16), "host_kv must be a 16-byte aligned pointer");
+  REQUIRE(k_pool && v_pool && aligned(k_pool, 16) && aligned(v_pool, 16),
+          "k_pool/v_pool must be 16-byte aligned device pointers");
+  REQUIRE(fetch && nfetch && blk2slot && err_word, "fetch, nfetch, blk2slot and err_word must be non-NULL");
+  REQUIRE(aligned(fetch, 4) && aligned(nfetch, 4) && aligned(blk2slot, 4) && aligned(err_word, 4),
+          "int32 arrays must be 4-byte aligned");
+  void* dev_host = mapped_host_ptr(host_kv);
+  REQUIRE(dev_host, "host_kv must be page-locked, device-mapped host memory");
+  *job = oasis::CopyJob{static_cast<const uint16_t*>(dev_host), fetch, nfetch, blk2slot,
+                        static_cast<uint16_t*>(k_pool), static_cast<uint16_t*>(v_pool), err_word};
+  return OASIS_OK;
+}
+
+oasis_status oasis_copy_fetched(const oasis_shape* shape, const void* host_kv, const int32_t* fetch,
+                                const int32_t* nfetch, const int32_t* blk2slot, void* k_pool, void* v_pool,
+                                uint32_t* err_word, oasis_stream_t stream) {
+  static const char* fn = "oasis_copy_fetched";
+  oasis::Shape s;
+  oasis_status st = check_shape(shape, fn, &s);
+  if (st != OASIS_OK) return st;
+  oasis::CopyJob job;
+  st = make_copy_job(fn, host_kv, fetch, nfetch, blk2slot, k_pool, v_pool, err_word, &job);
+  if (st != OASIS_OK) return st;
+  cudaError_t e = oasis::launch_copy_fetched(s, job, (cudaStream_t)stream);
+  return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
+}
+
+oasis_status oasis_score_blocks_copy(const oasis_shape* shape, const void* k_hbm, const int32_t* ctx_len,
+                                     const void* q_la, float* scores, const void* host_kv, const int32_t* fetch,
+                                     const int32_t* nfetch, const int32_t* blk2slot, void* k_pool, void* v_pool,
+                                     uint32_t* err_word, oasis_stream_t stream) {
+  static const char* fn = "oasis_score_blocks_copy";
+  oasis::Shape s;
+  oasis_status st = check_shape(shape, fn, &s);
+  if (st != OASIS_OK) return st;
+  REQUIRE(k_hbm && aligned(k_hbm, 16), "k_hbm must be a 16-byte aligned device pointer");
+  REQUIRE(q_la && aligned(q_la, 16), "q_la must be a 16-byte aligned device pointer");
+  REQUIRE(ctx_len && aligned(ctx_len, 4), "ctx_len must be a 4-byte aligned device pointer");
+  REQUIRE(scores && aligned(scores, 8), "scores must be an 8-byte aligned device pointer");
+  oasis::CopyJob job;
+  st = make_copy_job(fn, host_kv, fetch, nfetch, blk2slot, k_pool, v_pool, err_word, &job);
+  if (st != OASIS_OK) return st;
+  const auto* k = static_cast<const uint16_t*>(k_hbm);
+  const auto* q = static_cast<const uint16_t*>(q_la);
+  auto* sc = reinterpret_cast<float2*>(scores);
+  cudaError_t e;
+  if (use_tc_scoring()) {
+    e = oasis::launch_score_blocks_tc(s, k, ctx_len, q, sc, err_word, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = oasis::launch_copy_fetched(s, job, (cudaStream_t)stream);
+  } else {
+    e = oasis::launch_score_blocks_copy(s, k, ctx_len, q, sc, job, (cudaStream_t)stream);
   }
-  if (attr.type != cudaMemoryTypeHost) return nullptr;
-  return attr.devicePointer;
+  return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
 }
 
 oasis_status oasis_append_kv(const oasis_shape* shape, const void* k_new, const void* v_new, int32_t* ctx_len,

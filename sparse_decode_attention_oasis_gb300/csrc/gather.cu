@@ -19,7 +19,11 @@
 //      latency overlaps it; all table reads happen in one round of loads and the
 //      LRU clock is set from shared memory.  The copy is bound by the host link.
 // Out-of-range indices set bits of the error word and are skipped.
-#include "common.cuh"
+//
+// The same kernel without step 4 is the table half alone (oasis_assign_slots);
+// the data half then runs later as a warp-level copy (fetch_copy.cuh), either
+// carried by the next layer's block scorer or as its own small kernel here.
+#include "fetch_copy.cuh"
 
 namespace oasis {
 
@@ -34,6 +38,7 @@ __device__ __forceinline__ uint4 ld_host16(const void* p) {
   return r;
 }
 
+template <bool kCopy>
 __global__ void __launch_bounds__(kGatherThreads)
 gather_h2d_kernel(Shape s, const uint16_t* __restrict__ host_kv, const int* __restrict__ sel,
                   const int* __restrict__ nsel, const int* __restrict__ fetch,
@@ -82,13 +87,15 @@ gather_h2d_kernel(Shape s, const uint16_t* __restrict__ host_kv, const int* __re
   // start the first round of host reads now, so the link latency overlaps the table work
   const int total = nf * kUnits;
   uint4 pre[kGatherUnroll];
+  if constexpr (kCopy) {
 #pragma unroll
-  for (int u = 0; u < kGatherUnroll; ++u) {
-    const int id = threadIdx.x + u * blockDim.x;
-    if (id < total) {
-      const int i = id / kUnits, w = id - i * kUnits;
-      const int x = F[i];
-      if (x >= 0) pre[u] = ld_host16(host_kv + ((tb + x) * 2 * kBS * kD) + (long long)w * 8);
+    for (int u = 0; u < kGatherUnroll; ++u) {
+      const int id = threadIdx.x + u * blockDim.x;
+      if (id < total) {
+        const int i = id / kUnits, w = id - i * kUnits;
+        const int x = F[i];
+        if (x >= 0) pre[u] = ld_host16(host_kv + ((tb + x) * 2 * kBS * kD) + (long long)w * 8);
+      }
     }
   }
 
@@ -169,6 +176,10 @@ gather_h2d_kernel(Shape s, const uint16_t* __restrict__ host_kv, const int* __re
     last_used[ts + p] = lu[p];
   }
 
+  if constexpr (!kCopy) {
+    if (ew) atomicOr(err, ew);
+    return;
+  }
   // 3. copies: first the prefetched round, then the rest in rounds of kGatherUnroll
 #pragma unroll
   for (int u = 0; u < kGatherUnroll; ++u) {
@@ -209,19 +220,58 @@ gather_h2d_kernel(Shape s, const uint16_t* __restrict__ host_kv, const int* __re
 
 size_t gather_smem_bytes(const Shape& s) { return sizeof(int) * (2 * (size_t)s.Kb + 4 * (size_t)s.P + 4); }
 
+template <bool kCopy>
+static cudaError_t launch_gather(const Shape& s, const uint16_t* host_kv, const int* sel, const int* nsel,
+                                 const int* fetch, const int* nfetch, int* blk2slot, int* slot2blk,
+                                 int* last_used, const int* step, uint16_t* k_pool, uint16_t* v_pool,
+                                 unsigned* err, cudaStream_t stream) {
+  const size_t smem = gather_smem_bytes(s);
+  if (smem > 48 * 1024) {
+    static int attr_cache[kMaxDevicesCached] = {};
+    cudaError_t e = ensure_dyn_smem((const void*)gather_h2d_kernel<kCopy>, smem, attr_cache);
+    if (e != cudaSuccess) return e;
+  }
+  gather_h2d_kernel<kCopy><<<s.B * s.Hkv, kGatherThreads, smem, stream>>>(
+      s, host_kv, sel, nsel, fetch, nfetch, blk2slot, slot2blk, last_used, step, k_pool, v_pool, err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gather_h2d(const Shape& s, const uint16_t* host_kv, const int* sel, const int* nsel,
                               const int* fetch, const int* nfetch, int* blk2slot, int* slot2blk,
                               int* last_used, const int* step, uint16_t* k_pool, uint16_t* v_pool,
                               unsigned* err, cudaStream_t stream) {
-  const size_t smem = gather_smem_bytes(s);
-  if (smem > 48 * 1024) {
-    static int attr_cache[kMaxDevicesCached] = {};
-    cudaError_t e = ensure_dyn_smem((const void*)gather_h2d_kernel, smem, attr_cache);
-    if (e != cudaSuccess) return e;
-  }
-  gather_h2d_kernel<<<s.B * s.Hkv, kGatherThreads, smem, stream>>>(s, host_kv, sel, nsel, fetch, nfetch,
-                                                                   blk2slot, slot2blk, last_used, step,
-                                                                   k_pool, v_pool, err);
+  return launch_gather<true>(s, host_kv, sel, nsel, fetch, nfetch, blk2slot, slot2blk, last_used, step, k_pool,
+                             v_pool, err, stream);
+}
+
+cudaError_t launch_assign_slots(const Shape& s, const int* sel, const int* nsel, const int* fetch,
+                                const int* nfetch, int* blk2slot, int* slot2blk, int* last_used, const int* step,
+                                unsigned* err, cudaStream_t stream) {
+  return launch_gather<false>(s, nullptr, sel, nsel, fetch, nfetch, blk2slot, slot2blk, last_used, step, nullptr,
+                              nullptr, err, stream);
+}
+
+// The data half on its own: warps of 4-warp CTAs, 8 KiB of staging per warp.
+constexpr int kCopyWarps = 4;
+
+__global__ void __launch_bounds__(kCopyWarps * 32) copy_fetched_kernel(Shape s, CopyJob job) {
+  extern __shared__ uint4 copy_buf[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint4* buf = copy_buf + warp * (kCopyUnitBytes / 16);
+  const long long gwarp = (long long)blockIdx.x * kCopyWarps + warp;
+  const long long nwarps = (long long)gridDim.x * kCopyWarps;
+  copy_begin(job, s, gwarp, nwarps, buf, lane);
+  copy_finish(job, s, gwarp, nwarps, buf, lane);
+}
+
+cudaError_t launch_copy_fetched(const Shape& s, const CopyJob& job, cudaStream_t stream) {
+  // one warp per live entry up to four CTAs per SM; a warp streams any further entries
+  const long long items = (long long)s.B * s.Hkv * s.Kb;
+  long long ctas = (items + kCopyWarps - 1) / kCopyWarps;
+  const long long cap = 4LL * sm_count();
+  if (ctas > cap) ctas = cap;
+  if (ctas < 1) ctas = 1;
+  copy_fetched_kernel<<<(int)ctas, kCopyWarps * 32, kCopyWarps * kCopyUnitBytes, stream>>>(s, job);
   return cudaGetLastError();
 }
 

@@ -21,7 +21,12 @@
 // margin), the max query norm of the head and the max key norm of the block
 // (computed here in fp32 from the same registers), plus the rounding of the
 // 1/sqrt(d) product and an absolute 2^-60 for underflowed products.
-#include "common.cuh"
+//
+// With a copy job the kernel also carries the data half of another layer's
+// gather (fetch_copy.cuh): every warp stages its first fetched block through
+// 8 KiB of shared memory before it starts scoring and writes it to its HBM slot
+// afterwards, so the host-link latency overlaps the scoring.
+#include "fetch_copy.cuh"
 
 namespace oasis {
 
@@ -33,13 +38,17 @@ struct QFrag {
   uint32_t w[NT][4][4];  // [n-tile][d chunk i][word]
 };
 
-template <int NT>
+template <int NT, bool kCopy>
 __global__ void __launch_bounds__(kScoreWarps * 32, (NT <= 2 ? 3 : 2))
 score_blocks_kernel(Shape s, const uint16_t* __restrict__ k_hbm, const int* __restrict__ ctx_len,
                     const uint16_t* __restrict__ q_la, float2* __restrict__ scores,
-                    int chunks_per_head, int total_chunks, float inv_sqrt_d) {
+                    int chunks_per_head, int total_chunks, float inv_sqrt_d, CopyJob job) {
+  extern __shared__ uint4 copy_buf[];  // [kScoreWarps][512] when kCopy
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
+  const long long gwarp = (long long)blockIdx.x * kScoreWarps + warp;
+  const long long nwarps = (long long)gridDim.x * kScoreWarps;
+  if constexpr (kCopy) copy_begin(job, s, gwarp, nwarps, copy_buf + warp * (kCopyUnitBytes / 16), lane);
   const int g = lane >> 2, t = lane & 3;
   const int G = s.Hq / s.Hkv;
   const int N = s.n_la * G;
@@ -173,28 +182,44 @@ score_blocks_kernel(Shape s, const uint16_t* __restrict__ k_hbm, const int* __re
       }
     }
   }
+  if constexpr (kCopy) copy_finish(job, s, gwarp, nwarps, copy_buf + warp * (kCopyUnitBytes / 16), lane);
 }
 
 int score_grid_limit(int nt);
 
-cudaError_t launch_score_blocks(const Shape& s, const uint16_t* k, const int* ctx, const uint16_t* q_la,
-                                float2* scores, cudaStream_t stream) {
+constexpr int kScoreCopySmem = kScoreWarps * kCopyUnitBytes;  // 32 KiB
+
+template <bool kCopy>
+static cudaError_t launch_score(const Shape& s, const uint16_t* k, const int* ctx, const uint16_t* q_la,
+                                float2* scores, const CopyJob& job, cudaStream_t stream) {
   const int N = s.n_la * (s.Hq / s.Hkv);
   const int NT = (N + 7) / 8;
   const int chunks_per_head = (s.nb_max + kScoreChunk - 1) / kScoreChunk;
   const int total = s.B * s.Hkv * chunks_per_head;
   const float inv = 1.0f / sqrtf((float)s.d);
-  int grid = min(total, score_grid_limit(NT));
+  // the copy wants a warp for each live fetch entry, so its grid is never cut to the work
+  int grid = kCopy ? score_grid_limit(NT) : min(total, score_grid_limit(NT));
   if (grid < 1) grid = 1;
-  dim3 block(kScoreWarps * 32);
+  const dim3 block(kScoreWarps * 32);
+  const size_t smem = kCopy ? kScoreCopySmem : 0;
   switch (NT) {
-    case 1: score_blocks_kernel<1><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, chunks_per_head, total, inv); break;
-    case 2: score_blocks_kernel<2><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, chunks_per_head, total, inv); break;
-    case 3: score_blocks_kernel<3><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, chunks_per_head, total, inv); break;
-    case 4: score_blocks_kernel<4><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, chunks_per_head, total, inv); break;
+    case 1: score_blocks_kernel<1, kCopy><<<grid, block, smem, stream>>>(s, k, ctx, q_la, scores, chunks_per_head, total, inv, job); break;
+    case 2: score_blocks_kernel<2, kCopy><<<grid, block, smem, stream>>>(s, k, ctx, q_la, scores, chunks_per_head, total, inv, job); break;
+    case 3: score_blocks_kernel<3, kCopy><<<grid, block, smem, stream>>>(s, k, ctx, q_la, scores, chunks_per_head, total, inv, job); break;
+    case 4: score_blocks_kernel<4, kCopy><<<grid, block, smem, stream>>>(s, k, ctx, q_la, scores, chunks_per_head, total, inv, job); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_score_blocks(const Shape& s, const uint16_t* k, const int* ctx, const uint16_t* q_la,
+                                float2* scores, cudaStream_t stream) {
+  return launch_score<false>(s, k, ctx, q_la, scores, CopyJob{}, stream);
+}
+
+cudaError_t launch_score_blocks_copy(const Shape& s, const uint16_t* k, const int* ctx, const uint16_t* q_la,
+                                     float2* scores, const CopyJob& job, cudaStream_t stream) {
+  return launch_score<true>(s, k, ctx, q_la, scores, job, stream);
 }
 
 int score_grid_limit(int nt) {
@@ -205,10 +230,10 @@ int score_grid_limit(int nt) {
     const int threads = kScoreWarps * 32;
     int v = 0;
     switch (nt) {
-      case 1: cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, score_blocks_kernel<1>, threads, 0); break;
-      case 2: cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, score_blocks_kernel<2>, threads, 0); break;
-      case 3: cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, score_blocks_kernel<3>, threads, 0); break;
-      default: cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, score_blocks_kernel<4>, threads, 0); break;
+      case 1: cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, score_blocks_kernel<1, false>, threads, 0); break;
+      case 2: cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, score_blocks_kernel<2, false>, threads, 0); break;
+      case 3: cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, score_blocks_kernel<3, false>, threads, 0); break;
+      default: cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, score_blocks_kernel<4, false>, threads, 0); break;
     }
     per_sm = v < 1 ? 1 : v;
   }

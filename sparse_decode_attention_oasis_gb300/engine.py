@@ -213,12 +213,15 @@ class DecodeState:
     # ---------------------------------------------------------------- one layer-step
     def layer_step(self, layer: int, q_la: torch.Tensor, q: torch.Tensor, step: int,
                    stream=None, gather_stream=None, scratch: Optional[LayerScratch] = None,
-                   ev_pool=None):
+                   ev_pool=None, gather: str = "fused"):
         """Run a1..a5 for one layer: score, top-K, capped diff, gather, attention.
 
         q_la: bf16 [B][n_la][Hq][d], q: bf16 [B][Hq][d] (device).  Returns the
         scratch holding the outputs.  With ``gather_stream`` the gather runs on
-        that stream and the attention waits for it.
+        that stream and the attention waits for it.  ``gather`` picks how a4 is
+        issued: "fused" (oasis_gather_h2d), "split" (oasis_assign_slots then
+        oasis_copy_fetched) or "carry" (oasis_assign_slots, then the copy carried
+        by a second scoring launch of the same layer, oasis_score_blocks_copy).
         """
         s = self.shape
         sc = scratch or self.scratch
@@ -233,9 +236,22 @@ class DecodeState:
         gs = gather_stream or st
         if gs is not st:
             gs.wait_stream(st)
-        B.oasis_gather_h2d(s, self.host[lh], sc.sel, sc.nsel, sc.fetch, sc.nfetch, self.blk2slot[lp],
-                           self.slot2blk[lp], self.last_used[lp], step, self.k_pool[lp],
-                           self.v_pool[lp], sc.err, gs)
+        if gather == "fused":
+            B.oasis_gather_h2d(s, self.host[lh], sc.sel, sc.nsel, sc.fetch, sc.nfetch, self.blk2slot[lp],
+                               self.slot2blk[lp], self.last_used[lp], step, self.k_pool[lp],
+                               self.v_pool[lp], sc.err, gs)
+        elif gather in ("split", "carry"):
+            B.oasis_assign_slots(s, sc.sel, sc.nsel, sc.fetch, sc.nfetch, self.blk2slot[lp],
+                                 self.slot2blk[lp], self.last_used[lp], step, sc.err, gs)
+            if gather == "split":
+                B.oasis_copy_fetched(s, self.host[lh], sc.fetch, sc.nfetch, self.blk2slot[lp],
+                                     self.k_pool[lp], self.v_pool[lp], sc.err, gs)
+            else:
+                B.oasis_score_blocks_copy(s, K, self.ctx, q_la, sc.scores, self.host[lh], sc.fetch,
+                                          sc.nfetch, self.blk2slot[lp], self.k_pool[lp], self.v_pool[lp],
+                                          sc.err, gs)
+        else:
+            raise ValueError(f"unknown gather mode {gather!r}")
         if gs is not st:
             st.wait_stream(gs)
         B.oasis_sparse_decode_attn(s, q, self.k_pool[lp], self.v_pool[lp], sc.sel, sc.nsel,
@@ -252,13 +268,21 @@ class DecodeState:
             self.step_dev.fill_(int(step))
         return self.step_dev
 
-    def _select(self, layer, q_la, step, sc, st, mark=None):
+    def _select(self, layer, q_la, step, sc, st, mark=None, carry=None):
+        """a1..a3 of one layer; ``carry=(layer', scratch')`` makes the scoring launch
+        also copy the fetched blocks of layer' (whose slots are already assigned)."""
         s = self.shape
         lp = layer % self.L_phys
         K = self.Kl[lp]
         if mark:
             mark("score", st)
-        B.oasis_score_blocks(s, K, self.ctx, q_la, sc.scores, sc.err, st)
+        if carry is None:
+            B.oasis_score_blocks(s, K, self.ctx, q_la, sc.scores, sc.err, st)
+        else:
+            cl, csc = carry
+            clp, clh = cl % self.L_phys, cl % self.L_host
+            B.oasis_score_blocks_copy(s, K, self.ctx, q_la, sc.scores, self.hostl[clh], csc.fetch, csc.nfetch,
+                                      self.b2sl[clp], self.kpl[clp], self.vpl[clp], sc.err, st)
         if mark:
             mark("topk", st)
         B.oasis_topk_select(s, sc.scores, K, q_la, self.ctx, sc.sel, sc.nsel, st)
@@ -274,6 +298,18 @@ class DecodeState:
         lp, lh = layer % self.L_phys, layer % self.L_host
         B.oasis_gather_h2d(s, self.hostl[lh], sc.sel, sc.nsel, sc.fetch, sc.nfetch, self.b2sl[lp],
                            self.s2bl[lp], self.lul[lp], step, self.kpl[lp], self.vpl[lp], sc.err, gs)
+
+    def _assign(self, layer, step, sc, st):
+        s = self.shape
+        lp = layer % self.L_phys
+        B.oasis_assign_slots(s, sc.sel, sc.nsel, sc.fetch, sc.nfetch, self.b2sl[lp], self.s2bl[lp],
+                             self.lul[lp], step, sc.err, st)
+
+    def _copy(self, layer, sc, st):
+        s = self.shape
+        lp, lh = layer % self.L_phys, layer % self.L_host
+        B.oasis_copy_fetched(s, self.hostl[lh], sc.fetch, sc.nfetch, self.b2sl[lp], self.kpl[lp],
+                             self.vpl[lp], sc.err, st)
 
     def _attend(self, layer, q, sc, st, out=None):
         s = self.shape
@@ -291,26 +327,60 @@ class DecodeState:
         return ((slot >= 0) & valid).sum()
 
     def decode_step(self, step, q_la_layers, q_layers, out_layers=None, main=None, side=None,
-                    mark=None, count=None):
+                    mark=None, count=None, copy: str = "carry"):
         """All layers of one decode step, pipelined across layers.
 
-        Main stream: select(0); select(1); attn(0); select(2); attn(1); ...
-        Side stream: gather(l) as soon as select(l) is done, so the host-link copy
-        of layer l overlaps the HBM-bound scoring of layer l+1; attn(l) waits for
-        gather(l).  Two scratch sets alternate between consecutive layers.
-        q_la_layers[l], q_layers[l]: device tensors of layer l; out_layers[l]
-        (optional) receives the fp32 attention output of layer l.  ``mark(name,
-        stream)``, if given, is called before each kernel ("score", "topk",
-        "diff", "gather", "attn") and after the last one of a group ("end",
-        "gather_end", "attn_end") so the caller can record CUDA events.
+        copy="carry" (default), all on the main stream:
+            score(0) topk(0) diff(0) assign(0)
+            score(1)+copy(0) topk(1) diff(1) assign(1) attn(0)
+            score(2)+copy(1) ...                         attn(1)
+            ...  copy(L-1) attn(L-1)
+          The table half of layer l's gather runs right after its selection; the
+          host-link copy of layer l rides in layer l+1's scoring launch, whose
+          HBM-bound work hides the link latency; attn(l) follows that launch.
+        copy="gather": select(0); select(1); attn(0); select(2); attn(1); ... with
+          the whole gather (oasis_gather_h2d) of layer l right after select(l), on
+          ``side`` if given (attn(l) then waits for it).
+        Two scratch sets alternate between consecutive layers.  q_la_layers[l],
+        q_layers[l]: device tensors of layer l; out_layers[l] (optional) receives
+        the fp32 attention output of layer l.  ``mark(name, stream)``, if given, is
+        called before each kernel ("score", "topk", "diff", "assign", "copy",
+        "gather", "attn") and after the last one of a group ("end", "gather_end",
+        "attn_end") so the caller can record CUDA events.
         """
         L = self.w.L
         main = main or torch.cuda.current_stream(self.device)
-        side = side or main
         step = self._step_tensor(step, main)
         if self.scratch2 is None:
             self.scratch2 = LayerScratch(self.shape, self.device)
         scr = (self.scratch, self.scratch2)
+
+        def attend(l):
+            if mark:
+                mark("attn", main)
+            self._attend(l, q_layers[l], scr[l % 2], main, None if out_layers is None else out_layers[l])
+            if mark:
+                mark("attn_end", main)
+            if count is not None:
+                count += self.attended_blocks(l, scr[l % 2])
+
+        if copy == "carry":
+            for l in range(L):
+                self._select(l, q_la_layers[l], step, scr[l % 2], main, mark,
+                             carry=None if l == 0 else (l - 1, scr[(l - 1) % 2]))
+                if mark:
+                    mark("assign", main)
+                self._assign(l, step, scr[l % 2], main)
+                if l > 0:
+                    attend(l - 1)
+            if mark:
+                mark("copy", main)
+            self._copy(L - 1, scr[(L - 1) % 2], main)
+            attend(L - 1)
+            return
+        if copy != "gather":
+            raise ValueError(f"unknown copy mode {copy!r}")
+        side = side or main
         events = [torch.cuda.Event() for _ in range(2)]
 
         def launch_select_gather(l):
@@ -332,14 +402,7 @@ class DecodeState:
                 launch_select_gather(l + 1)
             if side is not main:
                 main.wait_event(events[l % 2])
-            if mark:
-                mark("attn", main)
-            self._attend(l, q_layers[l], scr[l % 2], main,
-                         None if out_layers is None else out_layers[l])
-            if mark:
-                mark("attn_end", main)
-            if count is not None:
-                count += self.attended_blocks(l, scr[l % 2])
+            attend(l)
 
     # ---------------------------------------------------------------- appends
     def append_tokens(self, layer: int, k_new: torch.Tensor, v_new: torch.Tensor, advance: bool,
@@ -363,7 +426,8 @@ class StepGraph:
     capture; CUDA events recorded by it become nodes of the graph.
     """
 
-    def __init__(self, st: DecodeState, first_step: int, q_la_steps, q_steps, out_steps, mark=None):
+    def __init__(self, st: DecodeState, first_step: int, q_la_steps, q_steps, out_steps, mark=None,
+                 copy: str = "carry"):
         self.st = st
         dev = st.device
         if st.scratch2 is None:
@@ -376,7 +440,7 @@ class StepGraph:
         with torch.cuda.graph(self.graph, stream=self.stream):
             for k in range(len(q_steps)):
                 st.decode_step(self.step, q_la_steps[k], q_steps[k], out_layers=out_steps[k],
-                               main=self.stream, side=self.stream, mark=mark)
+                               main=self.stream, side=self.stream, mark=mark, copy=copy)
                 self.step.add_(1)
         torch.cuda.synchronize(dev)
 

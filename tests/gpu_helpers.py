@@ -38,7 +38,7 @@ class Case:
         self.st = DecodeState(w, l_phys=1)
         self.st.fill_layer_numpy(0, K, V, self.b2s, self.s2b, self.lu)
 
-    def step(self, step, q=None, qla=None, C=None, append=False):
+    def step(self, step, q=None, qla=None, C=None, append=False, gather="fused"):
         import torch
 
         w = self.w
@@ -54,7 +54,7 @@ class Case:
             w.C = C
         r = ref.layer_step(self.K, qla, q, w.ctx, self.host, self.kp, self.vp, self.b2s, self.s2b,
                            self.lu, w.Kb, w.C, step, bs=w.bs)
-        sc = self.st.layer_step(0, _dev_bits(qla), _dev_bits(q), step)
+        sc = self.st.layer_step(0, _dev_bits(qla), _dev_bits(q), step, gather=gather)
         torch.cuda.synchronize()
         self.compare(r, sc)
         return r, sc

@@ -1,0 +1,110 @@
+"""The gather in two halves (oasis_assign_slots + oasis_copy_fetched) and the copy
+carried by a scoring launch (oasis_score_blocks_copy), against the oracle.
+
+Tables and pools must come out bit-identical to the one-call gather's, which the
+oracle fixes; the multi-layer decode step is checked layer by layer in both of
+its launch orders (copy carried by the next layer's scoring, or the whole gather
+after each selection)."""
+import numpy as np
+import pytest
+
+from oracle import oasis_ref as ref
+from sparse_decode_attention_oasis_gb300 import synthetic as syn
+
+from gpu_helpers import Case, _check_out, _dev_bits
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_decode_attention_oasis_gb300 import build
+
+    build.build()
+
+
+@pytest.mark.parametrize("gather", ["split", "carry"])
+def test_tiny_workload_split_gather(gather):
+    w = syn.tiny()
+    c = Case(w)
+    for step in range(3):
+        c.step(step, gather=gather)
+
+
+@pytest.mark.parametrize("gather", ["split", "carry"])
+def test_ragged_and_fetch_all_split_gather(gather):
+    w = syn.Workload("ragged", L=1, B=3, Hq=32, Hkv=8, ctx=[4096, 1000, 17], Kb=32, C=32, n_hot=16)
+    c = Case(w)
+    for step in range(2):
+        c.step(step, gather=gather)
+
+
+def test_cap_zero_copy_is_a_no_op():
+    w = syn.Workload("cap0", L=1, B=2, Hq=32, Hkv=8, ctx=[2048, 999], Kb=32, C=0, n_hot=16)
+    c = Case(w)
+    c.step(0, gather="carry")
+
+
+def _multi_layer(copy, L=3, steps=3):
+    from sparse_decode_attention_oasis_gb300.engine import DecodeState
+
+    w = syn.Workload("layers", L=L, B=2, Hq=32, Hkv=8, ctx=[3000, 1777], Kb=32, C=3, n_hot=16)
+    st = DecodeState(w, l_phys=L, l_host=L)
+    layers = []
+    for l in range(L):
+        K, V = syn.layer_kv(w, l)
+        host = syn.host_tier_from_kv(w, K, V)
+        b2s, s2b, lu = [np.array(t) for t in syn.initial_tables(w, l)]
+        kp, vp = syn.pools_from_tables(w, host, s2b)
+        st.fill_layer_numpy(l, K, V, b2s, s2b, lu)
+        layers.append([K, host, b2s, s2b, lu, kp, vp])
+    out = torch.empty((L, w.B, w.Hq, w.d), dtype=torch.float32, device="cuda")
+    for step in range(steps):
+        qs = [syn.layer_queries(w, l, step) for l in range(L)]
+        st.decode_step(step, [_dev_bits(qla) for _, qla in qs], [_dev_bits(q) for q, _ in qs],
+                       out_layers=out, copy=copy)
+        torch.cuda.synchronize()
+        assert int(st.scratch.err.item()) == 0 and int(st.scratch2.err.item()) == 0
+        for l in range(L):
+            K, host, b2s, s2b, lu, kp, vp = layers[l]
+            q, qla = qs[l]
+            r = ref.layer_step(K, qla, q, w.ctx, host, kp, vp, b2s, s2b, lu, w.Kb, w.C, step)
+            np.testing.assert_array_equal(st.blk2slot[l].cpu().numpy(), b2s)
+            np.testing.assert_array_equal(st.slot2blk[l].cpu().numpy(), s2b)
+            np.testing.assert_array_equal(st.last_used[l].cpu().numpy(), lu)
+            kpool = st.k_pool[l].cpu().view(torch.int16).numpy().view(np.uint16)
+            vpool = st.v_pool[l].cpu().view(torch.int16).numpy().view(np.uint16)
+            occ = s2b >= 0
+            np.testing.assert_array_equal(kpool[occ], kp[occ])
+            np.testing.assert_array_equal(vpool[occ], vp[occ])
+            _check_out(out[l].cpu().numpy().astype(np.float64), r["out"], f"layer {l} step {step}")
+
+
+@pytest.mark.parametrize("copy", ["carry", "gather"])
+def test_multi_layer_decode_step_both_orders(copy):
+    _multi_layer(copy)
+
+
+def test_copy_reports_out_of_range_fetch_entry():
+    """A fetch entry naming a block past nb_max is skipped and flagged; nothing else changes."""
+    from sparse_decode_attention_oasis_gb300 import binding as B
+    from sparse_decode_attention_oasis_gb300.engine import DecodeState
+
+    w = syn.Workload("bad", L=1, B=1, Hq=32, Hkv=8, ctx=[1024], Kb=16, C=2, n_hot=4)
+    st = DecodeState(w, l_phys=1)
+    K, V = syn.layer_kv(w, 0)
+    st.fill_layer_numpy(0, K, V, *[np.array(t) for t in syn.initial_tables(w, 0)])
+    s = st.shape
+    fetch = torch.full((w.B, w.Hkv, w.Kb), -1, dtype=torch.int32, device="cuda")
+    nfetch = torch.zeros((w.B, w.Hkv), dtype=torch.int32, device="cuda")
+    fetch[0, 3, 0] = w.nb_max + 5
+    nfetch[0, 3] = 1
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kp0, vp0 = st.k_pool.clone(), st.v_pool.clone()
+    B.oasis_copy_fetched(s, st.host[0], fetch, nfetch, st.blk2slot[0], st.k_pool[0], st.v_pool[0], err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == B.EW_BAD_BLOCK
+    assert torch.equal(st.k_pool, kp0) and torch.equal(st.v_pool, vp0)
