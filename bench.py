@@ -342,6 +342,35 @@ def algorithmic_bytes(w, attended_per_head=None):
             "total": score + topk + attn + gather_hbm}
 
 
+def measure_agreement(st, qla_layers, q_layers, q_prev_layers):
+    """Fraction of the exact top-K blocks of the true query that a predictor selects.
+
+    Per layer, over all heads: the lookahead queries' top-K ("lookahead"), the
+    previous step's true query ("previous_token"), and the exact blocks the
+    attention actually reads (lookahead set and resident, "attended").  At K =
+    Kb (the budget) and K = 20 (the top-20 of Figure 4).
+    """
+    import torch
+
+    from sparse_decode_attention_oasis_gb300.engine import AgreementProbe
+
+    out = {}
+    for K in (st.shape.Kb, 20):
+        probe = AgreementProbe(st, K=K)
+        per_layer = {"lookahead": [], "previous_token": [], "attended": []}
+        for l in range(st.w.L):
+            c = probe.run(l, qla_layers[l], q_layers[l], q_prev_layers[l])
+            la, prev = c["la"].sum(dim=(0, 1)).tolist(), c["prev"].sum(dim=(0, 1)).tolist()
+            per_layer["lookahead"].append(la[0] / la[2])
+            per_layer["attended"].append(la[1] / la[2])
+            per_layer["previous_token"].append(prev[0] / prev[2])
+        torch.cuda.synchronize()
+        out[f"K{K}"] = {k: {"mean": round(sum(v) / len(v), 4), "min": round(min(v), 4)}
+                        for k, v in per_layer.items()}
+        del probe
+    return out
+
+
 def measure_hostlink(st, qla0, dev):
     """Host-link roofline of the gather: fetch-all into an emptied layer vs a pinned memcpy.
 
@@ -614,6 +643,9 @@ def run_gpu(args, rank, world, local_rank):
         e2e = {"value": aggregate_value(world, L, nrep, 1000.0 * e2e_s), "unit": UNIT, "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": bo}
 
+    # prediction agreement per layer (Figure 6 / Figure 4 analogue), one step, untimed
+    agreement = measure_agreement(st, qla_dev[first], q_dev[first], q_dev[first - 1])
+
     hostlink = measure_hostlink(st, qla_dev[first], dev) if not args.no_hostlink else None
 
     if rank != 0:
@@ -643,6 +675,7 @@ def run_gpu(args, rank, world, local_rank):
         "gpu_launches": launches_per_step(st, args.copy) * args.steps,
         "copy_mode": args.copy,
         "hostlink": hostlink,
+        "prediction_agreement": agreement,
         "clocks": clk,
         "e2e": e2e,
         "device_error_word": errw,

@@ -346,6 +346,34 @@ OASIS_API oasis_status oasis_sparse_decode_attn_noalloc(const oasis_shape* shape
                                                         const int32_t* blk2slot, const int32_t* ctx_len,
                                                         float scale, float* out, oasis_stream_t stream);
 
+/*
+ * f3. Agreement of a predicted top-K set with the exact one (measurement only).
+ * Defines: the per-layer agreement between the blocks the draft (lookahead)
+ * queries select and the exact top-K blocks of the true next-token query
+ * (metalmedia.ai page, Figure 6 caption; at K = 20 with the previous token as
+ * the predictor, Figure 4 caption).  Obtain the exact set with
+ * oasis_score_blocks + oasis_topk_select on a shape with n_la = 1 and the true
+ * queries [B][Hq][d] as q_la; the predicted set is oasis_topk_select's output.
+ *   counts[b][h][0] = |pred & exact|
+ *   counts[b][h][1] = |pred & exact & resident| (resident: blk2slot >= 0), or -1
+ *                     when blk2slot is NULL
+ *   counts[b][h][2] = |exact|
+ * Arguments:
+ *   pred, npred    device int32 [B][Hkv][Kb], [B][Hkv]  ascending block lists
+ *   exact, nexact  device int32 [B][Hkv][Kb], [B][Hkv]  ascending block lists
+ *   blk2slot       device int32 [B][Hkv][nb_max] or NULL
+ *   counts         device int32 [B][Hkv][3]             out
+ *   err_word       device uint32 [1] or NULL (OASIS_EW_BAD_COUNT / _BAD_BLOCK)
+ * Only shape.B, Hkv, Kb and nb_max are used; the other fields are checked as
+ * for every call.  Unsorted pred gives wrong counts but never reads out of
+ * bounds.
+ */
+OASIS_API oasis_status oasis_set_agreement(const oasis_shape* shape, const int32_t* pred,
+                                           const int32_t* npred, const int32_t* exact,
+                                           const int32_t* nexact, const int32_t* blk2slot,
+                                           int32_t* counts, uint32_t* err_word,
+                                           oasis_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

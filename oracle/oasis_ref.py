@@ -24,6 +24,11 @@ Lookahead Sparse Prefetching"):
           block of the bounded working set to a CPU (host-tier) block.
   [tab2]  metalmedia.ai page, Table 2 caption: a fetch ratio sets how many
           blocks a single step may bring in; evictions follow LRU.
+  [fig6]  metalmedia.ai page, Figure 6 caption: per layer, how well the top-K
+          set predicted by the draft query agrees with the exact top-K set of
+          the true next-token query.
+  [fig4]  metalmedia.ai page, Figure 4 caption: top-20 block prediction
+          accuracy per layer from the previous token versus a lookahead token.
 
 Readings where the pages are silent (each is listed in the design notes):
   * score(b) = max over lookahead queries j, query heads g of the GQA group of
@@ -287,6 +292,35 @@ def append_token(k_bits, host_kv, k_pool, v_pool, blk2slot, ctx_len, k_new, v_ne
                 v_pool[b, h, p, r] = v_new[b, h]
         if advance:
             ctx_len[b] = t + 1
+
+
+# --------------------------------------------------------------------------
+# f3: agreement of a predicted top-K set with the exact one  ([fig6], [fig4])
+# --------------------------------------------------------------------------
+def exact_topk_true_query(k_bits: np.ndarray, q_bits: np.ndarray, ctx_len: Sequence[int], Kb: int,
+                          bs: int = BS_DEFAULT, heads=None) -> Dict:
+    """Per head, the top-Kb set of the true next-token query.
+
+    The same block score as a1 with the true queries of the GQA group in place of
+    the lookahead ones (one "lookahead" position): the exact set against which
+    Figure 6 measures the draft query's prediction.
+    """
+    q1 = q_bits[:, None]  # [B][1][Hq][d]
+    scores = block_scores(k_bits, q1, ctx_len, bs, heads=heads)
+    return {bh: topk_select(key, Kb) for bh, (_, key) in scores.items()}
+
+
+def set_agreement(pred: Sequence[int], exact: Sequence[int], blk2slot: np.ndarray = None):
+    """(|pred & exact|, |pred & exact & resident|, |exact|) for one head.
+
+    The first count over |exact| is the per-head agreement of Figure 6 (and, at
+    K = 20 with the previous token's query as the predictor, of Figure 4); the
+    second counts the exact blocks that attention actually reads when pred is
+    the selected set (resident = blk2slot >= 0 after the gather).
+    """
+    common = set(int(x) for x in pred) & set(int(x) for x in exact)
+    res = sum(1 for x in common if blk2slot is not None and blk2slot[x] >= 0)
+    return len(common), res, len(set(int(x) for x in exact))
 
 
 # --------------------------------------------------------------------------

@@ -61,6 +61,7 @@ _SIGS = {
     "oasis_copy_fetched": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
     "oasis_score_blocks_copy": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                  _VP, _VP, _VP], ctypes.c_int),
+    "oasis_set_agreement": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
     "oasis_sparse_decode_attn": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                   ctypes.c_float, _VP, ctypes.c_size_t, _VP, _VP], ctypes.c_int),
     "oasis_attn_workspace_bytes": ([ctypes.POINTER(Shape)], ctypes.c_size_t),
@@ -177,6 +178,14 @@ def oasis_score_blocks_copy(shape: Shape, k_hbm, ctx_len, q_la, scores, host_kv,
         ctypes.byref(shape), _ptr(k_hbm), _ptr(ctx_len), _ptr(q_la), _ptr(scores), _ptr(host_kv),
         _ptr(fetch), _ptr(nfetch), _ptr(blk2slot), _ptr(k_pool), _ptr(v_pool), _ptr(err_word),
         _stream(stream)))
+
+
+def oasis_set_agreement(shape: Shape, pred, npred, exact, nexact, blk2slot, counts, err_word=None,
+                        stream=None):
+    """Per head (|pred & exact|, |pred & exact & resident| or -1, |exact|) into counts [B][Hkv][3]."""
+    _check("oasis_set_agreement", load().oasis_set_agreement(
+        ctypes.byref(shape), _ptr(pred), _ptr(npred), _ptr(exact), _ptr(nexact), _ptr(blk2slot),
+        _ptr(counts), _ptr(err_word), _stream(stream)))
 
 
 def oasis_sparse_decode_attn(shape: Shape, q, k_pool, v_pool, sel, nsel, blk2slot, ctx_len,

@@ -25,6 +25,8 @@ cudaError_t launch_assign_slots(const Shape&, const int*, const int*, const int*
 cudaError_t launch_copy_fetched(const Shape&, const CopyJob&, cudaStream_t);
 cudaError_t launch_score_blocks_copy(const Shape&, const uint16_t*, const int*, const uint16_t*, float2*,
                                      const CopyJob&, cudaStream_t);
+cudaError_t launch_set_agreement(const Shape&, const int*, const int*, const int*, const int*, const int*, int*,
+                                 unsigned*, cudaStream_t);
 cudaError_t launch_append_kv(const Shape&, const uint16_t*, const uint16_t*, int*, uint16_t*, uint16_t*, const int*,
                              uint16_t*, uint16_t*, int, unsigned*, cudaStream_t);
 size_t topk_smem_bytes(const Shape&);
@@ -276,6 +278,22 @@ oasis_status oasis_score_blocks_copy(const oasis_shape* shape, const void* k_hbm
   } else {
     e = oasis::launch_score_blocks_copy(s, k, ctx_len, q, sc, job, (cudaStream_t)stream);
   }
+  return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
+}
+
+oasis_status oasis_set_agreement(const oasis_shape* shape, const int32_t* pred, const int32_t* npred,
+                                 const int32_t* exact, const int32_t* nexact, const int32_t* blk2slot,
+                                 int32_t* counts, uint32_t* err_word, oasis_stream_t stream) {
+  static const char* fn = "oasis_set_agreement";
+  oasis::Shape s;
+  oasis_status st = check_shape(shape, fn, &s);
+  if (st != OASIS_OK) return st;
+  REQUIRE(pred && npred && exact && nexact && counts, "pred, npred, exact, nexact and counts must be non-NULL");
+  REQUIRE(aligned(pred, 4) && aligned(npred, 4) && aligned(exact, 4) && aligned(nexact, 4) && aligned(counts, 4) &&
+              (!blk2slot || aligned(blk2slot, 4)) && (!err_word || aligned(err_word, 4)),
+          "int32 arrays must be 4-byte aligned");
+  cudaError_t e = oasis::launch_set_agreement(s, pred, npred, exact, nexact, blk2slot, counts, err_word,
+                                              (cudaStream_t)stream);
   return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
 }
 

@@ -415,6 +415,57 @@ class DecodeState:
                           self.scratch.err if err is None else err, st)
 
 
+class AgreementProbe:
+    """Per-layer agreement of predicted top-K sets with the exact one (f3).
+
+    For one layer and step: the exact set E = top-K of the true queries (the
+    block score with the true query as the only lookahead row), the lookahead
+    prediction S_la = top-K of the lookahead queries, and optionally the
+    previous-token prediction S_prev = top-K of the previous step's true
+    queries; oasis_set_agreement then counts |S & E| (and |S & E & resident|)
+    per head.  Uses its own buffers; the decode state's tables are only read.
+    """
+
+    def __init__(self, st: "DecodeState", K: Optional[int] = None):
+        s = st.shape
+        self.st = st
+        self.K = K or s.Kb
+        self.shape = B.Shape(s.B, s.Hq, s.Hkv, s.d, s.bs, s.nb_max, s.n_la, self.K, max(s.P, self.K))
+        self.shape1 = B.Shape(s.B, s.Hq, s.Hkv, s.d, s.bs, s.nb_max, 1, self.K, max(s.P, self.K))
+        dev = st.device
+        self.scores = torch.empty((s.B, s.Hkv, s.nb_max, 2), dtype=torch.float32, device=dev)
+        self.sel = {k: torch.empty((s.B, s.Hkv, self.K), dtype=torch.int32, device=dev)
+                    for k in ("exact", "la", "prev")}
+        self.nsel = {k: torch.empty((s.B, s.Hkv), dtype=torch.int32, device=dev) for k in self.sel}
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def _topk(self, shape, layer, q_rows, which, stream):
+        st = self.st
+        K = st.Kl[layer % st.L_phys]
+        B.oasis_score_blocks(shape, K, st.ctx, q_rows, self.scores, self.err, stream)
+        B.oasis_topk_select(shape, self.scores, K, q_rows, st.ctx, self.sel[which], self.nsel[which], stream)
+
+    def run(self, layer: int, q_la: torch.Tensor, q: torch.Tensor, q_prev: Optional[torch.Tensor] = None,
+            stream=None):
+        """Counts [B][Hkv][3] for the lookahead prediction (and the previous-token one)."""
+        st = self.st
+        stream = stream or torch.cuda.current_stream(st.device)
+        self._topk(self.shape1, layer, q, "exact", stream)
+        self._topk(self.shape, layer, q_la, "la", stream)
+        b2s = st.b2sl[layer % st.L_phys]
+        out = {}
+        for which, q_pred in (("la", None), ("prev", q_prev)):
+            if which == "prev":
+                if q_pred is None:
+                    continue
+                self._topk(self.shape1, layer, q_pred, "prev", stream)
+            counts = torch.empty((self.shape.B, self.shape.Hkv, 3), dtype=torch.int32, device=st.device)
+            B.oasis_set_agreement(self.shape, self.sel[which], self.nsel[which], self.sel["exact"],
+                                  self.nsel["exact"], b2s, counts, self.err, stream)
+            out[which] = counts
+        return out
+
+
 class StepGraph:
     """Decode steps captured as one CUDA graph and replayed.
 
