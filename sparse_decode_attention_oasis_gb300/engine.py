@@ -362,7 +362,7 @@ class DecodeState:
             if mark:
                 mark("attn_end", main)
             if count is not None:
-                count += self.attended_blocks(l, scr[l % 2])
+                count.add_(self.attended_blocks(l, scr[l % 2]))
 
         if copy == "carry":
             for l in range(L):
