@@ -162,6 +162,92 @@ def block_scores(k_bits: np.ndarray, q_la_bits: np.ndarray, ctx_len: Sequence[in
 
 
 # --------------------------------------------------------------------------
+# f1: block scores from min/max pooled compressed keys  ([fig7] left)
+# --------------------------------------------------------------------------
+def pool_keys(k_bits: np.ndarray, ctx: int, nb_max: int, bs: int = BS_DEFAULT):
+    """Per-block min/max pooling of one head's keys.
+
+    k_bits: bf16 [T_max][d].  Returns (hi, lo) bf16 bit arrays [nb_max][d]:
+    hi[x][i] = max over the valid tokens t of block x (t < ctx) of k[t][i], lo
+    the minimum; blocks without a valid token are all zero.  A maximum of bf16
+    values is one of them, so the pooled keys are exact bf16.
+    """
+    T, d = k_bits.shape
+    hi = np.zeros((nb_max, d), np.uint16)
+    lo = np.zeros((nb_max, d), np.uint16)
+    vals = bf16_to_f64(k_bits)
+    for x in range(min(nb_max, -(-ctx // bs))):
+        rows = list(range(x * bs, min(ctx, (x + 1) * bs)))
+        v = vals[rows]
+        ih = v.argmax(axis=0)
+        il = v.argmin(axis=0)
+        hi[x] = k_bits[[rows[j] for j in ih], range(d)]
+        lo[x] = k_bits[[rows[j] for j in il], range(d)]
+    return hi, lo
+
+
+def head_block_scores_pooled(hi_bits: np.ndarray, lo_bits: np.ndarray, Q: np.ndarray, nb: int):
+    """Exact pooled block scores of one KV head.
+
+    hi_bits, lo_bits: bf16 [nb_max][d] from pool_keys; Q: float64 [N][d] (the head's
+    lookahead query rows).  For block x:
+        pooled(x) = max over n of  sum_i max(Q[n][i] * hi[x][i], Q[n][i] * lo[x][i])
+    (unscaled), i.e. for each query the largest value any key inside the block's
+    per-dimension [lo, hi] box can reach, an upper bound of the block's max-dot
+    score.  Returns (score float64 [nb], exact integer keys = pooled x 2^266).
+    """
+    H = bf16_to_f64(hi_bits[:nb])
+    Lo = bf16_to_f64(lo_bits[:nb])
+    terms = np.maximum(H[:, None, :] * Q[None, :, :], Lo[:, None, :] * Q[None, :, :])  # [nb][N][d]
+    D = terms.sum(axis=2)
+    A = np.abs(terms).sum(axis=2)
+    Lk = np.minimum(_lsb_lower_bound(H).min(axis=1), _lsb_lower_bound(Lo).min(axis=1))
+    Lq = _lsb_lower_bound(Q).min(axis=1)
+    L = Lk[:, None] + Lq[None, :]
+    with np.errstate(over="ignore"):
+        ok = A < np.ldexp(1.0, np.minimum(L + 52, 2000))
+    if ok.all():
+        score = D.max(axis=1)
+        return score, [int(v) for v in np.ldexp(score, 2 * _EXACT_SHIFT)]
+    Hq = [_to_int(r) for r in H]
+    Lq_ = [_to_int(r) for r in Lo]
+    Qq = [_to_int(r) for r in Q]
+    key = []
+    for x in range(nb):
+        best = None
+        for n in range(Q.shape[0]):
+            if ok[x, n]:
+                v = int(np.ldexp(D[x, n], 2 * _EXACT_SHIFT))
+            else:
+                v = sum(max(q * a, q * b) for q, a, b in zip(Qq[n], Hq[x], Lq_[x]))
+            best = v if best is None or v > best else best
+        key.append(best)
+    score = np.array([math.ldexp(float(k), -2 * _EXACT_SHIFT) if abs(k) < 2 ** 1000
+                      else float(k) * 2.0 ** (-2 * _EXACT_SHIFT) for k in key])
+    return score, key
+
+
+def block_scores_pooled(pooled: Dict, q_la_bits: np.ndarray, ctx_len: Sequence[int], d: int,
+                        bs: int = BS_DEFAULT, heads=None):
+    """Pooled scores of every (request, KV head): pooled[(b, h)] = (hi, lo) bits.
+
+    Returns dict (b, h) -> (score scaled by 1/sqrt(d), exact key list), like
+    block_scores.
+    """
+    Hq = q_la_bits.shape[2]
+    Hkv = len({h for (_, h) in pooled})
+    G = Hq // Hkv
+    out = {}
+    for (b, h) in (heads if heads is not None else sorted(pooled)):
+        hi, lo = pooled[(b, h)]
+        Q = head_queries_f64(q_la_bits, b, h, G)
+        nb = -(-int(ctx_len[b]) // bs)
+        score, key = head_block_scores_pooled(hi, lo, Q, nb)
+        out[(b, h)] = (score / math.sqrt(d), key)
+    return out
+
+
+# --------------------------------------------------------------------------
 # a2: top-K under the token budget  ([abs] 2,048-token budget, [fig7] top-K)
 # --------------------------------------------------------------------------
 def rank_order(key: Sequence[int], blocks: Sequence[int]) -> List[int]:
@@ -328,19 +414,28 @@ def set_agreement(pred: Sequence[int], exact: Sequence[int], blk2slot: np.ndarra
 # --------------------------------------------------------------------------
 def layer_step(k_bits, q_la_bits, q_bits, ctx_len, host_kv, k_pool, v_pool,
                blk2slot, slot2blk, last_used, Kb: int, C: int, step: int,
-               scale: float = None, bs: int = BS_DEFAULT, heads=None) -> Dict:
+               scale: float = None, bs: int = BS_DEFAULT, heads=None, scoring: str = "maxdot") -> Dict:
     """Run a1..a5 for one layer.  Tables and pools are updated in place.
 
     host_kv bits [B][Hkv][nb_max][2][bs][d]; k_pool/v_pool bits [B][Hkv][P][bs][d].
+    scoring: "maxdot" (a1, the exact max over tokens) or "pooled" (f1, the score
+    from the per-block min/max pooled keys of the valid tokens).
     Returns dict with per-head S, F, copies, A and out float64 [B][Hq][d].
     """
-    B, Hkv, _, d = k_bits.shape
+    B, Hkv, T_max, d = k_bits.shape
     Hq = q_bits.shape[1]
     G = Hq // Hkv
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     pairs = heads if heads is not None else [(b, h) for b in range(B) for h in range(Hkv)]
-    scores = block_scores(k_bits, q_la_bits, ctx_len, bs, heads=pairs)
+    if scoring == "pooled":
+        nb_max = T_max // bs
+        pooled = {(b, h): pool_keys(k_bits[b, h], int(ctx_len[b]), nb_max, bs) for (b, h) in pairs}
+        scores = block_scores_pooled(pooled, q_la_bits, ctx_len, d, bs, heads=pairs)
+    elif scoring == "maxdot":
+        scores = block_scores(k_bits, q_la_bits, ctx_len, bs, heads=pairs)
+    else:
+        raise ValueError(scoring)
     res = {"S": {}, "F": {}, "copies": {}, "A": {}, "score": {},
            "out": np.zeros((B, Hq, d))}
     for (b, h) in pairs:
