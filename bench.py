@@ -53,9 +53,12 @@ def parse():
                     help="physical host-tier layers (0 = all layers if host memory allows)")
     ap.add_argument("--preroll", type=int, default=40,
                     help="untimed decode steps run first, so the timed steps see a warmed-up resident set")
-    ap.add_argument("--copy", default="carry", choices=["carry", "gather"],
-                    help="carry: the host copy of layer l rides in layer l+1's scoring launch; "
-                         "gather: one gather launch per layer after its selection")
+    ap.add_argument("--copy", default="overlap", choices=["overlap", "gather", "carry"],
+                    help="overlap: gather of layer l on a side stream beside the attention of layer l-1; "
+                         "gather: one gather launch per layer after its selection, one stream; "
+                         "carry: the host copy of layer l rides in layer l+1's scoring launch")
+    ap.add_argument("--scoring", default="maxdot", choices=["maxdot", "pooled"],
+                    help="maxdot: scan of the full keys; pooled: scan of the min/max pooled keys")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-hostlink", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -325,15 +328,18 @@ def score_traffic_per_launch():
     return d.get("bytes_per_launch_full")
 
 
-def algorithmic_bytes(w, attended_per_head=None):
+def algorithmic_bytes(w, attended_per_head=None, scoring="maxdot"):
     """Algorithmic HBM bytes of one layer-step, split by kernel.
 
+    The scorer reads every valid block's keys (4 KiB) or, with pooled scoring,
+    its two pooled rows (512 B), plus the queries, and writes 8 B per block.
     Attention reads the K and V of the attended blocks: ``attended_per_head``
     (measured) or, if not given, the full budget Kb.
     """
     H = w.B * w.Hkv
     ctx_blocks = sum(w.nb(b) for b in range(w.B)) * w.Hkv
-    score = ctx_blocks * w.bs * w.d * 2 + w.B * w.n_la * w.Hq * w.d * 2 + ctx_blocks * 8
+    per_block = 2 * w.d * 2 if scoring == "pooled" else w.bs * w.d * 2
+    score = ctx_blocks * per_block + w.B * w.n_la * w.Hq * w.d * 2 + ctx_blocks * 8
     topk = ctx_blocks * 8 + H * (w.Kb + 1) * 4
     na = w.Kb if attended_per_head is None else attended_per_head
     attn = int(H * na * w.bs * w.d * 2 * 2) + w.B * w.Hq * w.d * (2 + 4)
@@ -505,7 +511,7 @@ def run_gpu(args, rank, world, local_rank):
     t0 = time.time()
     while True:
         try:
-            st = DecodeState(w, device=dev, l_phys=L, l_host=l_host)
+            st = DecodeState(w, device=dev, l_phys=L, l_host=l_host, scoring=args.scoring)
             break
         except RuntimeError:
             if l_host <= 2:
@@ -533,7 +539,7 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
 
     main = torch.cuda.current_stream(dev)
-    side = main  # one stream: with the gather on a side stream its CTAs delayed the scoring kernel
+    side = main  # the overlap mode makes its own side stream; the others run on one stream
     out_dev = torch.empty((L, w.B, w.Hq, w.d), dtype=torch.float32, device=dev)
 
     def step(s, mark=None, qla=None, q=None):
@@ -650,7 +656,7 @@ def run_gpu(args, rank, world, local_rank):
 
     if rank != 0:
         return
-    ab = algorithmic_bytes(w, attended_per_head)
+    ab = algorithmic_bytes(w, attended_per_head, args.scoring)
     peak, peak_kind = measured_peaks()
     score_avg_ms = sum(score_ms) / len(score_ms)
     achieved = ab["score"] / (score_avg_ms / 1000.0) / 1e9
@@ -660,13 +666,17 @@ def run_gpu(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_desc(w), "l2": "inputs larger than L2 (2 GiB of keys per layer)",
+        "config": {"workload": workload_desc(w), "l2": ("inputs larger than L2 (256 MiB of pooled keys per layer)" if args.scoring == "pooled"
+                                else "inputs larger than L2 (2 GiB of keys per layer)"),
+                   "scoring": args.scoring, "copy": args.copy,
                    "host_tier_layers": l_host, "host_tier_aliased": l_host < L,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "path_hbm_gbs": path_gbs, "path_hbm_frac": path_gbs / peak,
-        "roofline": {"kernel": "score_blocks", "bound": "hbm", "achieved": achieved, "peak": peak,
+        "roofline": {"kernel": "score_blocks_pooled" if args.scoring == "pooled" else "score_blocks",
+                     "bound": "hbm", "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": score_traffic_per_launch(), "bytes_per_launch": ab["score"],
+                     "traffic": score_traffic_per_launch() if args.scoring == "maxdot" else None,
+                     "bytes_per_launch": ab["score"],
                      "avg_launch_ms": score_avg_ms},
         "kernel_avg_us": {k: round(1000.0 * sum(v) / len(v), 2) for k, v in kernel_ms.items() if v},
         "attended_blocks_per_head": round(attended_per_head, 2),

@@ -347,6 +347,67 @@ OASIS_API oasis_status oasis_sparse_decode_attn_noalloc(const oasis_shape* shape
                                                         float scale, float* out, oasis_stream_t stream);
 
 /*
+ * f1. Scoring from min/max pooled compressed keys.
+ * Defines: the GPU keeps, besides the sparse working set, compressed keys made by
+ * per-block min/max pooling, and the draft query scans those to predict the next
+ * step's top-K blocks (metalmedia.ai page, Figure 7 caption, left).  The pooled
+ * score of block x is the largest value a key inside the block's per-dimension
+ * [lo, hi] box can give:
+ *   pooled(x) = max over j < n_la, g < G of
+ *               sum_i max(q_la[b][j][h*G+g][i] * hi[x][i], q_la[..][i] * lo[x][i]) / sqrt(d),
+ *   hi[x][i] / lo[x][i] = max / min over the valid tokens t of x of k[t][i].
+ * It bounds the max-dot score of a1 from above and equals it for a block with one
+ * valid token.  Ranking, ties, S and F are as for a2/a3 with this score.
+ *
+ * k_pooled: device bf16 [B][Hkv][nb_max][2][d]: row 0 = hi, row 1 = lo; blocks
+ * without a valid token hold zeros.  512 bytes per block.
+ *
+ * oasis_pool_keys: builds k_pooled for every block from k_hbm (layout as for
+ *   oasis_score_blocks) and ctx_len.
+ * oasis_pool_append: folds k_new (device bf16 [B][Hkv][d]) into the block of
+ *   token position ctx_len[b] (a block's first token sets both rows).  Call it
+ *   with the same ctx_len as the oasis_append_kv of that token, before that
+ *   call advances ctx_len.  A position outside [0, nb_max*bs) sets
+ *   OASIS_EW_BAD_COUNT in err_word (may be NULL) and is skipped.
+ * oasis_score_blocks_pooled: writes scores exactly as oasis_score_blocks does
+ *   (approximation and certified bound; here e = 2^-12 |q| |k'| / sqrt(d) + ...,
+ *   |k'|^2 = |hi|^2 + |lo|^2), reading 512 bytes per block.  If host_kv is not
+ *   NULL the launch also carries oasis_copy_fetched(host_kv, fetch, nfetch,
+ *   blk2slot, k_pool, v_pool, err_word) as oasis_score_blocks_copy does (err_word
+ *   then required); with host_kv NULL those five pointers are ignored.
+ * oasis_topk_select_pooled / oasis_fetch_diff_capped_pooled: as a2 / a3 with the
+ *   pooled score; k_pooled takes the place of k_hbm for the exact re-scoring.
+ */
+OASIS_API oasis_status oasis_pool_keys(const oasis_shape* shape, const void* k_hbm,
+                                       const int32_t* ctx_len, void* k_pooled,
+                                       oasis_stream_t stream);
+
+OASIS_API oasis_status oasis_pool_append(const oasis_shape* shape, const void* k_new,
+                                         const int32_t* ctx_len, void* k_pooled,
+                                         uint32_t* err_word, oasis_stream_t stream);
+
+OASIS_API oasis_status oasis_score_blocks_pooled(const oasis_shape* shape, const void* k_pooled,
+                                                 const int32_t* ctx_len, const void* q_la,
+                                                 float* scores, const void* host_kv,
+                                                 const int32_t* fetch, const int32_t* nfetch,
+                                                 const int32_t* blk2slot, void* k_pool,
+                                                 void* v_pool, uint32_t* err_word,
+                                                 oasis_stream_t stream);
+
+OASIS_API oasis_status oasis_topk_select_pooled(const oasis_shape* shape, const float* scores,
+                                                const void* k_pooled, const void* q_la,
+                                                const int32_t* ctx_len, int32_t* sel,
+                                                int32_t* nsel, oasis_stream_t stream);
+
+OASIS_API oasis_status oasis_fetch_diff_capped_pooled(const oasis_shape* shape,
+                                                      const float* scores, const void* k_pooled,
+                                                      const void* q_la, const int32_t* ctx_len,
+                                                      const int32_t* sel, const int32_t* nsel,
+                                                      const int32_t* blk2slot,
+                                                      int32_t fetch_cap, int32_t* fetch,
+                                                      int32_t* nfetch, oasis_stream_t stream);
+
+/*
  * f3. Agreement of a predicted top-K set with the exact one (measurement only).
  * Defines: the per-layer agreement between the blocks the draft (lookahead)
  * queries select and the exact top-K blocks of the true next-token query

@@ -62,6 +62,13 @@ _SIGS = {
     "oasis_score_blocks_copy": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                  _VP, _VP, _VP], ctypes.c_int),
     "oasis_set_agreement": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
+    "oasis_pool_keys": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP], ctypes.c_int),
+    "oasis_pool_append": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
+    "oasis_score_blocks_pooled": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                   _VP, _VP, _VP], ctypes.c_int),
+    "oasis_topk_select_pooled": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
+    "oasis_fetch_diff_capped_pooled": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                        ctypes.c_int32, _VP, _VP, _VP], ctypes.c_int),
     "oasis_sparse_decode_attn": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                   ctypes.c_float, _VP, ctypes.c_size_t, _VP, _VP], ctypes.c_int),
     "oasis_attn_workspace_bytes": ([ctypes.POINTER(Shape)], ctypes.c_size_t),
@@ -186,6 +193,41 @@ def oasis_set_agreement(shape: Shape, pred, npred, exact, nexact, blk2slot, coun
     _check("oasis_set_agreement", load().oasis_set_agreement(
         ctypes.byref(shape), _ptr(pred), _ptr(npred), _ptr(exact), _ptr(nexact), _ptr(blk2slot),
         _ptr(counts), _ptr(err_word), _stream(stream)))
+
+
+def oasis_pool_keys(shape: Shape, k_hbm, ctx_len, k_pooled, stream=None):
+    """Min/max pooled compressed keys bf16 [B][Hkv][nb_max][2][d] from the full keys."""
+    _check("oasis_pool_keys", load().oasis_pool_keys(
+        ctypes.byref(shape), _ptr(k_hbm), _ptr(ctx_len), _ptr(k_pooled), _stream(stream)))
+
+
+def oasis_pool_append(shape: Shape, k_new, ctx_len, k_pooled, err_word=None, stream=None):
+    """Fold each request's new key at position ctx_len[b] into its block's pooled rows."""
+    _check("oasis_pool_append", load().oasis_pool_append(
+        ctypes.byref(shape), _ptr(k_new), _ptr(ctx_len), _ptr(k_pooled), _ptr(err_word), _stream(stream)))
+
+
+def oasis_score_blocks_pooled(shape: Shape, k_pooled, ctx_len, q_la, scores, host_kv=None, fetch=None,
+                              nfetch=None, blk2slot=None, k_pool=None, v_pool=None, err_word=None,
+                              stream=None):
+    """Pooled block scores; with host_kv the launch also carries a gather's copy half."""
+    _check("oasis_score_blocks_pooled", load().oasis_score_blocks_pooled(
+        ctypes.byref(shape), _ptr(k_pooled), _ptr(ctx_len), _ptr(q_la), _ptr(scores), _ptr(host_kv),
+        _ptr(fetch), _ptr(nfetch), _ptr(blk2slot), _ptr(k_pool), _ptr(v_pool), _ptr(err_word),
+        _stream(stream)))
+
+
+def oasis_topk_select_pooled(shape: Shape, scores, k_pooled, q_la, ctx_len, sel, nsel, stream=None):
+    _check("oasis_topk_select_pooled", load().oasis_topk_select_pooled(
+        ctypes.byref(shape), _ptr(scores), _ptr(k_pooled), _ptr(q_la), _ptr(ctx_len), _ptr(sel), _ptr(nsel),
+        _stream(stream)))
+
+
+def oasis_fetch_diff_capped_pooled(shape: Shape, scores, k_pooled, q_la, ctx_len, sel, nsel, blk2slot,
+                                   fetch_cap: int, fetch, nfetch, stream=None):
+    _check("oasis_fetch_diff_capped_pooled", load().oasis_fetch_diff_capped_pooled(
+        ctypes.byref(shape), _ptr(scores), _ptr(k_pooled), _ptr(q_la), _ptr(ctx_len), _ptr(sel), _ptr(nsel),
+        _ptr(blk2slot), int(fetch_cap), _ptr(fetch), _ptr(nfetch), _stream(stream)))
 
 
 def oasis_sparse_decode_attn(shape: Shape, q, k_pool, v_pool, sel, nsel, blk2slot, ctx_len,

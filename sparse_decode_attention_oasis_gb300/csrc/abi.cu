@@ -27,6 +27,14 @@ cudaError_t launch_score_blocks_copy(const Shape&, const uint16_t*, const int*, 
                                      const CopyJob&, cudaStream_t);
 cudaError_t launch_set_agreement(const Shape&, const int*, const int*, const int*, const int*, const int*, int*,
                                  unsigned*, cudaStream_t);
+cudaError_t launch_pool_keys(const Shape&, const uint16_t*, const int*, uint16_t*, cudaStream_t);
+cudaError_t launch_pool_append(const Shape&, const uint16_t*, const int*, uint16_t*, unsigned*, cudaStream_t);
+cudaError_t launch_score_pooled(const Shape&, const uint16_t*, const int*, const uint16_t*, float2*, const CopyJob*,
+                                cudaStream_t);
+cudaError_t launch_topk_select_pooled(const Shape&, const float2*, const uint16_t*, const uint16_t*, const int*,
+                                      int*, int*, cudaStream_t);
+cudaError_t launch_fetch_diff_pooled(const Shape&, const float2*, const uint16_t*, const uint16_t*, const int*,
+                                     const int*, const int*, const int*, int, int*, int*, cudaStream_t);
 cudaError_t launch_append_kv(const Shape&, const uint16_t*, const uint16_t*, int*, uint16_t*, uint16_t*, const int*,
                              uint16_t*, uint16_t*, int, unsigned*, cudaStream_t);
 size_t topk_smem_bytes(const Shape&);
@@ -278,6 +286,101 @@ oasis_status oasis_score_blocks_copy(const oasis_shape* shape, const void* k_hbm
   } else {
     e = oasis::launch_score_blocks_copy(s, k, ctx_len, q, sc, job, (cudaStream_t)stream);
   }
+  return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
+}
+
+oasis_status oasis_pool_keys(const oasis_shape* shape, const void* k_hbm, const int32_t* ctx_len, void* k_pooled,
+                             oasis_stream_t stream) {
+  static const char* fn = "oasis_pool_keys";
+  oasis::Shape s;
+  oasis_status st = check_shape(shape, fn, &s);
+  if (st != OASIS_OK) return st;
+  REQUIRE(k_hbm && aligned(k_hbm, 16), "k_hbm must be a 16-byte aligned device pointer");
+  REQUIRE(k_pooled && aligned(k_pooled, 16), "k_pooled must be a 16-byte aligned device pointer");
+  REQUIRE(ctx_len && aligned(ctx_len, 4), "ctx_len must be a 4-byte aligned device pointer");
+  cudaError_t e = oasis::launch_pool_keys(s, static_cast<const uint16_t*>(k_hbm), ctx_len,
+                                          static_cast<uint16_t*>(k_pooled), (cudaStream_t)stream);
+  return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
+}
+
+oasis_status oasis_pool_append(const oasis_shape* shape, const void* k_new, const int32_t* ctx_len, void* k_pooled,
+                               uint32_t* err_word, oasis_stream_t stream) {
+  static const char* fn = "oasis_pool_append";
+  oasis::Shape s;
+  oasis_status st = check_shape(shape, fn, &s);
+  if (st != OASIS_OK) return st;
+  REQUIRE(k_new && aligned(k_new, 16), "k_new must be a 16-byte aligned device pointer");
+  REQUIRE(k_pooled && aligned(k_pooled, 16), "k_pooled must be a 16-byte aligned device pointer");
+  REQUIRE(ctx_len && aligned(ctx_len, 4), "ctx_len must be a 4-byte aligned device pointer");
+  REQUIRE(!err_word || aligned(err_word, 4), "err_word must be NULL or 4-byte aligned");
+  cudaError_t e = oasis::launch_pool_append(s, static_cast<const uint16_t*>(k_new), ctx_len,
+                                            static_cast<uint16_t*>(k_pooled), err_word, (cudaStream_t)stream);
+  return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
+}
+
+oasis_status oasis_score_blocks_pooled(const oasis_shape* shape, const void* k_pooled, const int32_t* ctx_len,
+                                       const void* q_la, float* scores, const void* host_kv, const int32_t* fetch,
+                                       const int32_t* nfetch, const int32_t* blk2slot, void* k_pool,
+                                       void* v_pool, uint32_t* err_word, oasis_stream_t stream) {
+  static const char* fn = "oasis_score_blocks_pooled";
+  oasis::Shape s;
+  oasis_status st = check_shape(shape, fn, &s);
+  if (st != OASIS_OK) return st;
+  REQUIRE(k_pooled && aligned(k_pooled, 16), "k_pooled must be a 16-byte aligned device pointer");
+  REQUIRE(q_la && aligned(q_la, 16), "q_la must be a 16-byte aligned device pointer");
+  REQUIRE(ctx_len && aligned(ctx_len, 4), "ctx_len must be a 4-byte aligned device pointer");
+  REQUIRE(scores && aligned(scores, 8), "scores must be an 8-byte aligned device pointer");
+  oasis::CopyJob job;
+  const bool copy = host_kv != nullptr;
+  if (copy) {
+    st = make_copy_job(fn, host_kv, fetch, nfetch, blk2slot, k_pool, v_pool, err_word, &job);
+    if (st != OASIS_OK) return st;
+  }
+  cudaError_t e = oasis::launch_score_pooled(s, static_cast<const uint16_t*>(k_pooled), ctx_len,
+                                             static_cast<const uint16_t*>(q_la), reinterpret_cast<float2*>(scores),
+                                             copy ? &job : nullptr, (cudaStream_t)stream);
+  return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
+}
+
+oasis_status oasis_topk_select_pooled(const oasis_shape* shape, const float* scores, const void* k_pooled,
+                                      const void* q_la, const int32_t* ctx_len, int32_t* sel, int32_t* nsel,
+                                      oasis_stream_t stream) {
+  static const char* fn = "oasis_topk_select_pooled";
+  oasis::Shape s;
+  oasis_status st = check_shape(shape, fn, &s);
+  if (st != OASIS_OK) return st;
+  REQUIRE(scores && aligned(scores, 8), "scores must be an 8-byte aligned device pointer");
+  REQUIRE(k_pooled && aligned(k_pooled, 16), "k_pooled must be a 16-byte aligned device pointer");
+  REQUIRE(q_la && aligned(q_la, 16), "q_la must be a 16-byte aligned device pointer");
+  REQUIRE(ctx_len && aligned(ctx_len, 4), "ctx_len must be a 4-byte aligned device pointer");
+  REQUIRE(sel && aligned(sel, 4) && nsel && aligned(nsel, 4), "sel/nsel must be 4-byte aligned device pointers");
+  cudaError_t e = oasis::launch_topk_select_pooled(s, reinterpret_cast<const float2*>(scores),
+                                                   static_cast<const uint16_t*>(k_pooled),
+                                                   static_cast<const uint16_t*>(q_la), ctx_len, sel, nsel,
+                                                   (cudaStream_t)stream);
+  return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
+}
+
+oasis_status oasis_fetch_diff_capped_pooled(const oasis_shape* shape, const float* scores, const void* k_pooled,
+                                            const void* q_la, const int32_t* ctx_len, const int32_t* sel,
+                                            const int32_t* nsel, const int32_t* blk2slot, int32_t fetch_cap,
+                                            int32_t* fetch, int32_t* nfetch, oasis_stream_t stream) {
+  static const char* fn = "oasis_fetch_diff_capped_pooled";
+  oasis::Shape s;
+  oasis_status st = check_shape(shape, fn, &s);
+  if (st != OASIS_OK) return st;
+  REQUIRE(scores && aligned(scores, 8), "scores must be an 8-byte aligned device pointer");
+  REQUIRE(k_pooled && aligned(k_pooled, 16), "k_pooled must be a 16-byte aligned device pointer");
+  REQUIRE(q_la && aligned(q_la, 16), "q_la must be a 16-byte aligned device pointer");
+  REQUIRE(ctx_len && aligned(ctx_len, 4), "ctx_len must be a 4-byte aligned device pointer");
+  REQUIRE(sel && nsel && blk2slot && fetch && nfetch, "sel/nsel/blk2slot/fetch/nfetch must be device pointers");
+  REQUIRE(aligned(sel, 4) && aligned(nsel, 4) && aligned(blk2slot, 4) && aligned(fetch, 4) && aligned(nfetch, 4),
+          "int32 arrays must be 4-byte aligned");
+  REQUIRE(fetch_cap >= 0 && fetch_cap <= s.Kb, "fetch_cap must be in [0, Kb]");
+  cudaError_t e = oasis::launch_fetch_diff_pooled(s, reinterpret_cast<const float2*>(scores),
+                                                  static_cast<const uint16_t*>(k_pooled),
+                                                  static_cast<const uint16_t*>(q_la), ctx_len, sel, nsel, blk2slot,
+                                                  fetch_cap, fetch, nfetch, (cudaStream_t)stream);
   return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
 }
 

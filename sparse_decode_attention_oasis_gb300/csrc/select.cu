@@ -70,14 +70,20 @@ __device__ __forceinline__ int exact_cmp(const uint32_t* a, const uint32_t* b) {
 // forms 4 exact products as (limb, low 32 bits, high bits); the limbs the warp
 // touches are summed one at a time with a 64-bit warp reduction (no atomics),
 // then every lane runs the same carry chain and lane i < 17 stores limb i.
-__device__ void warp_exact_dot(const uint16_t* krow, const uint16_t* qrow, uint32_t* out, int lane) {
+// With kBox the key element is chosen per dimension by the query's sign: krow
+// (the pooled maxima) where q >= 0, krow_neg (the minima) where q < 0, which makes
+// the sum the pooled score sum_i max(q_i hi_i, q_i lo_i).
+template <bool kBox>
+__device__ void warp_exact_dot(const uint16_t* krow, const uint16_t* qrow, uint32_t* out, int lane,
+                               const uint16_t* krow_neg = nullptr) {
   int limb[4];
   long long lo[4], hi[4];
   int lmin = kLimbs, lmax = -1;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int e = lane + 32 * j;
-    const uint32_t kb = krow[e], qb = qrow[e];
+    const uint32_t qb = qrow[e];
+    const uint32_t kb = (kBox && (qb & 0x8000u)) ? krow_neg[e] : krow[e];
     const uint32_t kE = (kb >> 7) & 0xffu, qE = (qb >> 7) & 0xffu;
     const uint32_t km = (kb & 0x7fu) | (kE ? 0x80u : 0u);
     const uint32_t qm = (qb & 0x7fu) | (qE ? 0x80u : 0u);
@@ -399,7 +405,7 @@ __device__ void warp_exact_block_score(const SelCtx& c, int blk, uint32_t* out, 
       const int nt = idx >> 2, e = idx & 3;
       const int tau = sg + (e >= 2 ? 8 : 0);
       const int n = nt * 8 + 2 * st + (e & 1);
-      warp_exact_dot(kst + tau * kD, c.qb + n * kD, tmp, lane);
+      warp_exact_dot<false>(kst + tau * kD, c.qb + n * kD, tmp, lane);
       if (lane == 0) {
         if (!have || exact_cmp(tmp, out) > 0)
           for (int i = 0; i < kLimbs; ++i) out[i] = tmp[i];
@@ -415,11 +421,69 @@ __device__ void warp_exact_block_score(const SelCtx& c, int blk, uint32_t* out, 
   __syncwarp();
 }
 
+// Exact pooled score (x 2^266) of block `blk` (f1: max over the queries n of
+// sum_i max(q_ni hi_i, q_ni lo_i)), by one warp, into out.  The block's two pooled
+// rows (512 bytes) are staged in the warp's slot; each query's sum is first formed
+// in fp32 from its exact products (4 per lane, then a 5-level tree) with the bound
+// 2^-16 sum|p| + 2^-120 (at most 8 roundings of 2^-24 of that sum, plus
+// underflowed products); only the queries whose interval reaches the best lower
+// bound are summed exactly.
+__device__ void warp_exact_pooled_score(const SelCtx& c, int blk, uint32_t* out, int warp, int lane) {
+  uint16_t* kst = c.kst + warp * (kBS * kD);
+  reinterpret_cast<uint4*>(kst)[lane] = ldg_nc(reinterpret_cast<const uint4*>(c.k + (long long)blk * 2 * kD) + lane);
+  __syncwarp();
+  const uint16_t* hi = kst;
+  const uint16_t* lo = kst + kD;
+  float my_lo = neg_inf(), my_hi = neg_inf();
+  for (int n = 0; n < c.N; ++n) {
+    const uint16_t* q = c.qb + n * kD;
+    float v = 0.f, a = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = lane + 32 * j;
+      const uint32_t qb = q[e];
+      const uint32_t kb = (qb & 0x8000u) ? lo[e] : hi[e];
+      const float p = __uint_as_float(qb << 16) * __uint_as_float(kb << 16);
+      v += p;
+      a += fabsf(p);
+    }
+    v = warp_sum(v);
+    a = warp_sum(a);
+    if (lane == n) {
+      const float eps = __fmaf_ru(1.52587890625e-05f /* 2^-16 */, a, 7.52316384526264e-37f /* 2^-120 */);
+      my_lo = __fsub_rd(v, eps);
+      my_hi = __fadd_ru(v, eps);
+      if (!(fabsf(v) <= 3.0e38f) || !(a <= 3.0e38f)) { my_lo = neg_inf(); my_hi = __int_as_float(0x7f800000); }
+    }
+  }
+  const float best_lo = warp_max(my_lo);
+  unsigned mask = __ballot_sync(0xffffffffu, lane < c.N && my_hi >= best_lo);
+  uint32_t* tmp = c.tmp + warp * kLimbs;
+  bool have = false;
+  while (mask) {
+    const int n = __ffs(mask) - 1;
+    mask &= mask - 1;
+    warp_exact_dot<true>(hi, c.qb + n * kD, tmp, lane, lo);
+    if (lane == 0) {
+      if (!have || exact_cmp(tmp, out) > 0)
+        for (int i = 0; i < kLimbs; ++i) out[i] = tmp[i];
+    }
+    have = true;
+    __syncwarp();
+  }
+  if (!have && lane == 0) {
+    for (int i = 0; i < kLimbs - 1; ++i) out[i] = 0u;
+    out[kLimbs - 1] = 0x80000000u;
+  }
+  __syncwarp();
+}
+
 // Mark (cls = 1) the r best of the uncertain candidates U[0..nU) by exact order;
 // cand_blk maps a candidate index to its block (nullptr = identity).  The running
 // top-r set T (exact values, in rank order) is merged with each batch of
 // kSelWarps freshly scored blocks by counting, for every member of the union, how
 // many members rank before it; the r first go to the other buffer.
+template <bool kPooled>
 __device__ void refine_top_r(SelCtx& c, const int* U, int nU, int r, const int* cand_blk,
                              uint8_t* cls) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -434,7 +498,10 @@ __device__ void refine_top_r(SelCtx& c, const int* U, int nU, int r, const int* 
     if (warp < nbat) {
       const int ci = U[base + warp];
       const int blk = cand_blk ? cand_blk[ci] : ci;
-      warp_exact_block_score(c, blk, c.bval + warp * kLimbs, warp, lane);
+      if constexpr (kPooled)
+        warp_exact_pooled_score(c, blk, c.bval + warp * kLimbs, warp, lane);
+      else
+        warp_exact_block_score(c, blk, c.bval + warp * kLimbs, warp, lane);
       if (lane == 0) c.bidx[warp] = ci;
     }
     __syncthreads();
@@ -475,6 +542,7 @@ __device__ void refine_top_r(SelCtx& c, const int* U, int nU, int r, const int* 
 }
 
 // cls[i] = 1 for the k best of the n candidates (exact order), 0 otherwise.
+template <bool kPooled>
 __device__ void select_best(SelCtx& c, const float2* se, int n, int k, const int* cand_blk,
                             uint8_t* cls, int* U) {
   if (k >= n || k <= 0) {
@@ -511,7 +579,7 @@ __device__ void select_best(SelCtx& c, const float2* se, int n, int k, const int
     __syncthreads();
     return;
   }
-  refine_top_r(c, U, nU, r, cand_blk, cls);
+  refine_top_r<kPooled>(c, U, nU, r, cand_blk, cls);
 }
 
 // ---------------------------------------------------------------- shared memory layout
@@ -548,12 +616,14 @@ __host__ __device__ inline SelLayout sel_layout(int ncap, bool with_cblk, int kb
   return L;
 }
 
-__device__ SelCtx make_ctx(char* sm, const SelLayout& L, const Shape& s, const uint16_t* k_hbm,
-                           const uint16_t* q_la, int head, int ctx) {
+// keys: the full keys [heads][nb_max*16][128], or with `pooled` the pooled keys
+// [heads][nb_max][2][128].
+__device__ SelCtx make_ctx(char* sm, const SelLayout& L, const Shape& s, const uint16_t* keys,
+                           const uint16_t* q_la, int head, int ctx, bool pooled) {
   SelCtx c;
   c.b = head / s.Hkv;
   c.h = head - c.b * s.Hkv;
-  c.k = k_hbm + (long long)head * s.nb_max * kBS * kD;
+  c.k = keys + (long long)head * s.nb_max * (pooled ? 2 * kD : kBS * kD);
   c.q_la = q_la;
   c.ctx = ctx;
   c.G = s.Hq / s.Hkv;
@@ -578,6 +648,7 @@ __device__ SelCtx make_ctx(char* sm, const SelLayout& L, const Shape& s, const u
 }
 
 // ---------------------------------------------------------------- a2 kernel
+template <bool kPooled>
 __global__ void __launch_bounds__(kSelThreads, 2)
 topk_select_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __restrict__ k_hbm,
                    const uint16_t* __restrict__ q_la, const int* __restrict__ ctx_len,
@@ -594,7 +665,7 @@ topk_select_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* _
     if (threadIdx.x == 0) nsel[head] = nb;
     return;
   }
-  SelCtx c = make_ctx(sm, L, s, k_hbm, q_la, head, ctx);
+  SelCtx c = make_ctx(sm, L, s, k_hbm, q_la, head, ctx, kPooled);
   float2* se = reinterpret_cast<float2*>(sm + L.se);
   uint8_t* cls = reinterpret_cast<uint8_t*>(sm + L.cls);
   int* U = reinterpret_cast<int*>(sm + L.U);
@@ -602,7 +673,7 @@ topk_select_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* _
   const float2* src = scores + (long long)head * s.nb_max;
   for (int i = threadIdx.x; i < nb; i += blockDim.x) se[i] = src[i];
   __syncthreads();
-  select_best(c, se, nb, s.Kb, nullptr, cls, U);
+  select_best<kPooled>(c, se, nb, s.Kb, nullptr, cls, U);
   // compaction in ascending block order
   const int per = (nb + kSelThreads - 1) / kSelThreads;
   const int i0 = threadIdx.x * per, i1 = min(nb, i0 + per);
@@ -621,6 +692,7 @@ topk_select_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* _
 }
 
 // ---------------------------------------------------------------- a3 kernel
+template <bool kPooled>
 __global__ void __launch_bounds__(kSelThreads, 2)
 fetch_diff_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __restrict__ k_hbm,
                   const uint16_t* __restrict__ q_la, const int* __restrict__ ctx_len,
@@ -632,7 +704,7 @@ fetch_diff_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __
   const int head = blockIdx.x;
   const int b = head / s.Hkv;
   const int ctx = ctx_len[b];
-  SelCtx c = make_ctx(sm, L, s, k_hbm, q_la, head, ctx);
+  SelCtx c = make_ctx(sm, L, s, k_hbm, q_la, head, ctx, kPooled);
   float2* se = reinterpret_cast<float2*>(sm + L.se);
   uint8_t* cls = reinterpret_cast<uint8_t*>(sm + L.cls);
   int* U = reinterpret_cast<int*>(sm + L.U);
@@ -656,7 +728,7 @@ fetch_diff_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __
   }
   __syncthreads();
   const int C = cap < nM ? cap : nM;
-  select_best(c, se, nM, C, cblk, cls, U);
+  select_best<kPooled>(c, se, nM, C, cblk, cls, U);
   int* out = fetch + (long long)head * s.Kb;
   const int take = ((int)threadIdx.x < nM && cls[threadIdx.x] == 1) ? 1 : 0;
   const int opos = block_excl_scan(take, red, red + 31);
@@ -670,28 +742,54 @@ fetch_diff_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __
 size_t topk_smem_bytes(const Shape& s) { return sel_layout(s.nb_max, false, s.Kb).total; }
 size_t diff_smem_bytes(const Shape& s) { return sel_layout(s.Kb, true, s.Kb).total; }
 
+template <bool kPooled>
+static cudaError_t launch_topk(const Shape& s, const float2* scores, const uint16_t* k, const uint16_t* q_la,
+                               const int* ctx, int* sel, int* nsel, cudaStream_t stream) {
+  static int attr_cache[kMaxDevicesCached] = {};
+  const size_t smem = topk_smem_bytes(s);
+  cudaError_t e = ensure_dyn_smem((const void*)topk_select_kernel<kPooled>, smem, attr_cache);
+  if (e != cudaSuccess) return e;
+  topk_select_kernel<kPooled><<<s.B * s.Hkv, kSelThreads, smem, stream>>>(s, scores, k, q_la, ctx, sel, nsel);
+  return cudaGetLastError();
+}
+
+template <bool kPooled>
+static cudaError_t launch_diff(const Shape& s, const float2* scores, const uint16_t* k, const uint16_t* q_la,
+                               const int* ctx, const int* sel, const int* nsel, const int* blk2slot, int cap,
+                               int* fetch, int* nfetch, cudaStream_t stream) {
+  static int attr_cache[kMaxDevicesCached] = {};
+  const size_t smem = diff_smem_bytes(s);
+  cudaError_t e = ensure_dyn_smem((const void*)fetch_diff_kernel<kPooled>, smem, attr_cache);
+  if (e != cudaSuccess) return e;
+  fetch_diff_kernel<kPooled><<<s.B * s.Hkv, kSelThreads, smem, stream>>>(s, scores, k, q_la, ctx, sel, nsel,
+                                                                        blk2slot, cap, fetch, nfetch);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_topk_select(const Shape& s, const float2* scores, const uint16_t* k,
                                const uint16_t* q_la, const int* ctx, int* sel, int* nsel,
                                cudaStream_t stream) {
-  static int attr_cache[kMaxDevicesCached] = {};
-  const size_t smem = topk_smem_bytes(s);
-  cudaError_t e = ensure_dyn_smem((const void*)topk_select_kernel, smem, attr_cache);
-  if (e != cudaSuccess) return e;
-  topk_select_kernel<<<s.B * s.Hkv, kSelThreads, smem, stream>>>(s, scores, k, q_la, ctx, sel, nsel);
-  return cudaGetLastError();
+  return launch_topk<false>(s, scores, k, q_la, ctx, sel, nsel, stream);
+}
+
+cudaError_t launch_topk_select_pooled(const Shape& s, const float2* scores, const uint16_t* kp,
+                                      const uint16_t* q_la, const int* ctx, int* sel, int* nsel,
+                                      cudaStream_t stream) {
+  return launch_topk<true>(s, scores, kp, q_la, ctx, sel, nsel, stream);
 }
 
 cudaError_t launch_fetch_diff(const Shape& s, const float2* scores, const uint16_t* k,
                               const uint16_t* q_la, const int* ctx, const int* sel,
                               const int* nsel, const int* blk2slot, int cap, int* fetch,
                               int* nfetch, cudaStream_t stream) {
-  static int attr_cache[kMaxDevicesCached] = {};
-  const size_t smem = diff_smem_bytes(s);
-  cudaError_t e = ensure_dyn_smem((const void*)fetch_diff_kernel, smem, attr_cache);
-  if (e != cudaSuccess) return e;
-  fetch_diff_kernel<<<s.B * s.Hkv, kSelThreads, smem, stream>>>(s, scores, k, q_la, ctx, sel, nsel,
-                                                               blk2slot, cap, fetch, nfetch);
-  return cudaGetLastError();
+  return launch_diff<false>(s, scores, k, q_la, ctx, sel, nsel, blk2slot, cap, fetch, nfetch, stream);
+}
+
+cudaError_t launch_fetch_diff_pooled(const Shape& s, const float2* scores, const uint16_t* kp,
+                                     const uint16_t* q_la, const int* ctx, const int* sel,
+                                     const int* nsel, const int* blk2slot, int cap, int* fetch,
+                                     int* nfetch, cudaStream_t stream) {
+  return launch_diff<true>(s, scores, kp, q_la, ctx, sel, nsel, blk2slot, cap, fetch, nfetch, stream);
 }
 
 }  // namespace oasis

@@ -104,7 +104,13 @@ class LayerScratch:
 
 class DecodeState:
     def __init__(self, w: syn.Workload, device="cuda", l_phys: Optional[int] = None,
-                 l_host: Optional[int] = None, pin_host: bool = True):
+                 l_host: Optional[int] = None, pin_host: bool = True, scoring: str = "maxdot"):
+        """scoring: "maxdot" (a1, scan of the full keys) or "pooled" (f1, scan of the
+        min/max pooled keys ``Kp``, bf16 [L][B][Hkv][nb_max][2][128], built from K
+        by ``pool_all`` / the fill methods and kept current by ``append_tokens``)."""
+        if scoring not in ("maxdot", "pooled"):
+            raise ValueError(f"unknown scoring {scoring!r}")
+        self.scoring = scoring
         self.w = w
         self.device = torch.device(device)
         self.L_phys = l_phys or w.L
@@ -114,6 +120,8 @@ class DecodeState:
         dev = self.device
         Lp = self.L_phys
         self.K = torch.zeros((Lp, s.B, s.Hkv, s.nb_max * 16, 128), dtype=torch.bfloat16, device=dev)
+        self.Kp = (torch.zeros((Lp, s.B, s.Hkv, s.nb_max, 2, 128), dtype=torch.bfloat16, device=dev)
+                   if scoring == "pooled" else None)
         self.k_pool = torch.zeros((Lp, s.B, s.Hkv, s.P, 16, 128), dtype=torch.bfloat16, device=dev)
         self.v_pool = torch.zeros_like(self.k_pool)
         self.blk2slot = torch.full((Lp, s.B, s.Hkv, s.nb_max), -1, dtype=torch.int32, device=dev)
@@ -134,6 +142,7 @@ class DecodeState:
         self.scale = 1.0 / math.sqrt(w.d)
         # per-layer views made once (indexing a tensor costs host time on every call)
         self.Kl = [self.K[l] for l in range(Lp)]
+        self.Kpl = [self.Kp[l] for l in range(Lp)] if self.Kp is not None else None
         self.kpl = [self.k_pool[l] for l in range(Lp)]
         self.vpl = [self.v_pool[l] for l in range(Lp)]
         self.b2sl = [self.blk2slot[l] for l in range(Lp)]
@@ -156,6 +165,7 @@ class DecodeState:
         kp, vp = syn.pools_from_tables(w, host, slot2blk)
         self.k_pool[lp].copy_(_bf16_from_bits(kp, self.device))
         self.v_pool[lp].copy_(_bf16_from_bits(vp, self.device))
+        self.pool_layer(lp)
 
     def fill_synthetic(self):
         """Generate every layer on the device (keys, host tier, pools, tables).
@@ -184,7 +194,15 @@ class DecodeState:
             self.blk2slot[lp].copy_(torch.from_numpy(b2s))
             self.slot2blk[lp].copy_(torch.from_numpy(s2b))
             self.last_used[lp].copy_(torch.from_numpy(lu))
+            self.pool_layer(lp)
         torch.cuda.synchronize(dev)
+
+    def pool_layer(self, lp: int, stream=None):
+        """Rebuild layer lp's pooled keys from its full keys (pooled scoring only)."""
+        if self.Kp is None:
+            return
+        B.oasis_pool_keys(self.shape, self.K[lp], self.ctx, self.Kp[lp],
+                          stream or torch.cuda.current_stream(self.device))
 
     def fill_layer_synthetic(self, layer: int):
         """Generate one layer on the device with the counter-based generator."""
@@ -209,6 +227,7 @@ class DecodeState:
         hostv = self.host[lh][:, :, :, 1].to(self.device)
         gv = torch.gather(hostv, 2, idx[..., None, None].expand(-1, -1, -1, 16, 128))
         self.v_pool[lp].copy_(gv * (s2b_t >= 0)[..., None, None])
+        self.pool_layer(lp)
 
     # ---------------------------------------------------------------- one layer-step
     def layer_step(self, layer: int, q_la: torch.Tensor, q: torch.Tensor, step: int,
@@ -229,10 +248,7 @@ class DecodeState:
         st = stream or torch.cuda.current_stream(self.device)
         step = self._step_tensor(step, st)
         K = self.K[lp]
-        B.oasis_score_blocks(s, K, self.ctx, q_la, sc.scores, sc.err, st)
-        B.oasis_topk_select(s, sc.scores, K, q_la, self.ctx, sc.sel, sc.nsel, st)
-        B.oasis_fetch_diff_capped(s, sc.scores, K, q_la, self.ctx, sc.sel, sc.nsel,
-                                  self.blk2slot[lp], self.w.C, sc.fetch, sc.nfetch, st)
+        self._score_topk_diff(lp, q_la, sc, st)
         gs = gather_stream or st
         if gs is not st:
             gs.wait_stream(st)
@@ -246,6 +262,10 @@ class DecodeState:
             if gather == "split":
                 B.oasis_copy_fetched(s, self.host[lh], sc.fetch, sc.nfetch, self.blk2slot[lp],
                                      self.k_pool[lp], self.v_pool[lp], sc.err, gs)
+            elif self.Kp is not None:
+                B.oasis_score_blocks_pooled(s, self.Kp[lp], self.ctx, q_la, sc.scores, self.host[lh], sc.fetch,
+                                            sc.nfetch, self.blk2slot[lp], self.k_pool[lp], self.v_pool[lp],
+                                            sc.err, gs)
             else:
                 B.oasis_score_blocks_copy(s, K, self.ctx, q_la, sc.scores, self.host[lh], sc.fetch,
                                           sc.nfetch, self.blk2slot[lp], self.k_pool[lp], self.v_pool[lp],
@@ -268,28 +288,41 @@ class DecodeState:
             self.step_dev.fill_(int(step))
         return self.step_dev
 
+    def _score_topk_diff(self, lp, q_la, sc, st):
+        self._select_lp(lp, q_la, sc, st)
+
     def _select(self, layer, q_la, step, sc, st, mark=None, carry=None):
         """a1..a3 of one layer; ``carry=(layer', scratch')`` makes the scoring launch
         also copy the fetched blocks of layer' (whose slots are already assigned)."""
+        self._select_lp(layer % self.L_phys, q_la, sc, st, mark, carry)
+
+    def _select_lp(self, lp, q_la, sc, st, mark=None, carry=None):
         s = self.shape
-        lp = layer % self.L_phys
-        K = self.Kl[lp]
+        pooled = self.Kp is not None
+        K = self.Kpl[lp] if pooled else self.Kl[lp]
         if mark:
             mark("score", st)
         if carry is None:
-            B.oasis_score_blocks(s, K, self.ctx, q_la, sc.scores, sc.err, st)
+            if pooled:
+                B.oasis_score_blocks_pooled(s, K, self.ctx, q_la, sc.scores, err_word=sc.err, stream=st)
+            else:
+                B.oasis_score_blocks(s, K, self.ctx, q_la, sc.scores, sc.err, st)
         else:
             cl, csc = carry
             clp, clh = cl % self.L_phys, cl % self.L_host
-            B.oasis_score_blocks_copy(s, K, self.ctx, q_la, sc.scores, self.hostl[clh], csc.fetch, csc.nfetch,
-                                      self.b2sl[clp], self.kpl[clp], self.vpl[clp], sc.err, st)
+            args = (self.hostl[clh], csc.fetch, csc.nfetch, self.b2sl[clp], self.kpl[clp], self.vpl[clp], sc.err, st)
+            if pooled:
+                B.oasis_score_blocks_pooled(s, K, self.ctx, q_la, sc.scores, *args)
+            else:
+                B.oasis_score_blocks_copy(s, K, self.ctx, q_la, sc.scores, *args)
         if mark:
             mark("topk", st)
-        B.oasis_topk_select(s, sc.scores, K, q_la, self.ctx, sc.sel, sc.nsel, st)
+        topk = B.oasis_topk_select_pooled if pooled else B.oasis_topk_select
+        diff = B.oasis_fetch_diff_capped_pooled if pooled else B.oasis_fetch_diff_capped
+        topk(s, sc.scores, K, q_la, self.ctx, sc.sel, sc.nsel, st)
         if mark:
             mark("diff", st)
-        B.oasis_fetch_diff_capped(s, sc.scores, K, q_la, self.ctx, sc.sel, sc.nsel,
-                                  self.b2sl[lp], self.w.C, sc.fetch, sc.nfetch, st)
+        diff(s, sc.scores, K, q_la, self.ctx, sc.sel, sc.nsel, self.b2sl[lp], self.w.C, sc.fetch, sc.nfetch, st)
         if mark:
             mark("end", st)
 
@@ -338,6 +371,8 @@ class DecodeState:
           The table half of layer l's gather runs right after its selection; the
           host-link copy of layer l rides in layer l+1's scoring launch, whose
           HBM-bound work hides the link latency; attn(l) follows that launch.
+        copy="overlap": select(l) on ``main``, then the whole gather of layer l on a
+          side stream while ``main`` runs attn(l-1); select(l+1) waits for gather(l).
         copy="gather": select(0); select(1); attn(0); select(2); attn(1); ... with
           the whole gather (oasis_gather_h2d) of layer l right after select(l), on
           ``side`` if given (attn(l) then waits for it).
@@ -378,6 +413,29 @@ class DecodeState:
             self._copy(L - 1, scr[(L - 1) % 2], main)
             attend(L - 1)
             return
+        if copy == "overlap":
+            # main: S(l) [A(l-1)] wait G(l) S(l+1) ...; side: G(l) once S(l) is done.
+            # G(l) overlaps A(l-1) only: the next scoring launch waits for it, so the
+            # persistent scorer never shares the GPU with the gather.
+            side = side if (side is not None and side is not main) else self._side_stream()
+            ev_sel = [torch.cuda.Event() for _ in range(2)]
+            ev_gat = [torch.cuda.Event() for _ in range(2)]
+            for l in range(L):
+                sc = scr[l % 2]
+                self._select(l, q_la_layers[l], step, sc, main, mark)
+                ev_sel[l % 2].record(main)
+                side.wait_event(ev_sel[l % 2])
+                if mark:
+                    mark("gather", side)
+                self._gather(l, step, sc, side)
+                if mark:
+                    mark("gather_end", side)
+                ev_gat[l % 2].record(side)
+                if l > 0:
+                    attend(l - 1)
+                main.wait_event(ev_gat[l % 2])
+            attend(L - 1)
+            return
         if copy != "gather":
             raise ValueError(f"unknown copy mode {copy!r}")
         side = side or main
@@ -404,12 +462,23 @@ class DecodeState:
                 main.wait_event(events[l % 2])
             attend(l)
 
+    def _side_stream(self):
+        if getattr(self, "_side", None) is None:
+            self._side = torch.cuda.Stream(self.device)
+        return self._side
+
     # ---------------------------------------------------------------- appends
     def append_tokens(self, layer: int, k_new: torch.Tensor, v_new: torch.Tensor, advance: bool,
                       stream=None, err=None):
-        """Append one token per request (bf16 [B][Hkv][d]) to layer `layer`'s caches."""
+        """Append one token per request (bf16 [B][Hkv][d]) to layer `layer`'s caches.
+
+        With pooled scoring the token is folded into its block's pooled keys only
+        when ``advance`` makes it valid; after advancing ctx some other way, call
+        ``pool_layer``."""
         lp, lh = layer % self.L_phys, layer % self.L_host
         st = stream or torch.cuda.current_stream(self.device)
+        if self.Kp is not None and advance:  # before the append advances ctx
+            B.oasis_pool_append(self.shape, k_new, self.ctx, self.Kp[lp], self.scratch.err if err is None else err, st)
         B.oasis_append_kv(self.shape, k_new, v_new, self.ctx, self.K[lp], self.host[lh], self.blk2slot[lp],
                           self.k_pool[lp], self.v_pool[lp], advance,
                           self.scratch.err if err is None else err, st)

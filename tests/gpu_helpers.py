@@ -23,7 +23,7 @@ def _check_out(got, want, what=""):
 class Case:
     """One layer of a workload held both on the GPU and in oracle arrays."""
 
-    def __init__(self, w, K=None, V=None, tables=None):
+    def __init__(self, w, K=None, V=None, tables=None, scoring="maxdot"):
         from sparse_decode_attention_oasis_gb300.engine import DecodeState
 
         self.w = w
@@ -35,7 +35,8 @@ class Case:
             tables = syn.initial_tables(w, 0)
         self.b2s, self.s2b, self.lu = [np.array(t) for t in tables]
         self.kp, self.vp = syn.pools_from_tables(w, self.host, self.s2b)
-        self.st = DecodeState(w, l_phys=1)
+        self.scoring = scoring
+        self.st = DecodeState(w, l_phys=1, scoring=scoring)
         self.st.fill_layer_numpy(0, K, V, self.b2s, self.s2b, self.lu)
 
     def step(self, step, q=None, qla=None, C=None, append=False, gather="fused"):
@@ -53,7 +54,7 @@ class Case:
         if C is not None:
             w.C = C
         r = ref.layer_step(self.K, qla, q, w.ctx, self.host, self.kp, self.vp, self.b2s, self.s2b,
-                           self.lu, w.Kb, w.C, step, bs=w.bs)
+                           self.lu, w.Kb, w.C, step, bs=w.bs, scoring=self.scoring)
         sc = self.st.layer_step(0, _dev_bits(qla), _dev_bits(q), step, gather=gather)
         torch.cuda.synchronize()
         self.compare(r, sc)
@@ -95,6 +96,18 @@ class Case:
         _check_out(sc.out.cpu().numpy().astype(np.float64), r["out"], "attention")
 
 
+
+    def compare_pooled(self):
+        """Pooled keys on the GPU against the oracle's pooling of the current keys (values)."""
+        import torch
+
+        w = self.w
+        got = self.st.Kp[0].float().cpu().numpy()
+        for b in range(w.B):
+            for h in range(w.Hkv):
+                hi, lo = ref.pool_keys(self.K[b, h], w.ctx[b], w.nb_max, w.bs)
+                np.testing.assert_array_equal(got[b, h, :, 0], ref.bf16_to_f64(hi))
+                np.testing.assert_array_equal(got[b, h, :, 1], ref.bf16_to_f64(lo))
 
     def compare_caches(self):
         """Keys in HBM and the whole host tier, bit for bit."""
