@@ -53,7 +53,7 @@ def parse():
                     help="physical host-tier layers (0 = all layers if host memory allows)")
     ap.add_argument("--preroll", type=int, default=40,
                     help="untimed decode steps run first, so the timed steps see a warmed-up resident set")
-    ap.add_argument("--copy", default="overlap", choices=["overlap", "gather", "carry"],
+    ap.add_argument("--copy", default="gather", choices=["gather", "overlap", "carry"],
                     help="overlap: gather of layer l on a side stream beside the attention of layer l-1; "
                          "gather: one gather launch per layer after its selection, one stream; "
                          "carry: the host copy of layer l rides in layer l+1's scoring launch")

@@ -488,10 +488,10 @@ class AgreementProbe:
     """Per-layer agreement of predicted top-K sets with the exact one (f3).
 
     For one layer and step: the exact set E = top-K of the true queries (the
-    block score with the true query as the only lookahead row), the lookahead
-    prediction S_la = top-K of the lookahead queries, and optionally the
-    previous-token prediction S_prev = top-K of the previous step's true
-    queries; oasis_set_agreement then counts |S & E| (and |S & E & resident|)
+    max-dot block score with the true query as the only lookahead row), the
+    lookahead prediction S_la = top-K of the lookahead queries, and optionally
+    the previous-token prediction S_prev = top-K of the previous step's true
+    queries (both predictions with the decode path's scoring, max-dot or pooled); oasis_set_agreement then counts |S & E| (and |S & E & resident|)
     per head.  Uses its own buffers; the decode state's tables are only read.
     """
 
@@ -508,9 +508,16 @@ class AgreementProbe:
         self.nsel = {k: torch.empty((s.B, s.Hkv), dtype=torch.int32, device=dev) for k in self.sel}
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
 
-    def _topk(self, shape, layer, q_rows, which, stream):
+    def _topk(self, shape, layer, q_rows, which, stream, pooled=False):
         st = self.st
-        K = st.Kl[layer % st.L_phys]
+        lp = layer % st.L_phys
+        if pooled:
+            Kp = st.Kpl[lp]
+            B.oasis_score_blocks_pooled(shape, Kp, st.ctx, q_rows, self.scores, err_word=self.err, stream=stream)
+            B.oasis_topk_select_pooled(shape, self.scores, Kp, q_rows, st.ctx, self.sel[which], self.nsel[which],
+                                       stream)
+            return
+        K = st.Kl[lp]
         B.oasis_score_blocks(shape, K, st.ctx, q_rows, self.scores, self.err, stream)
         B.oasis_topk_select(shape, self.scores, K, q_rows, st.ctx, self.sel[which], self.nsel[which], stream)
 
@@ -519,15 +526,16 @@ class AgreementProbe:
         """Counts [B][Hkv][3] for the lookahead prediction (and the previous-token one)."""
         st = self.st
         stream = stream or torch.cuda.current_stream(st.device)
+        pooled = st.Kp is not None  # the predictors score as the decode path does
         self._topk(self.shape1, layer, q, "exact", stream)
-        self._topk(self.shape, layer, q_la, "la", stream)
+        self._topk(self.shape, layer, q_la, "la", stream, pooled)
         b2s = st.b2sl[layer % st.L_phys]
         out = {}
         for which, q_pred in (("la", None), ("prev", q_prev)):
             if which == "prev":
                 if q_pred is None:
                     continue
-                self._topk(self.shape1, layer, q_pred, "prev", stream)
+                self._topk(self.shape1, layer, q_pred, "prev", stream, pooled)
             counts = torch.empty((self.shape.B, self.shape.Hkv, 3), dtype=torch.int32, device=st.device)
             B.oasis_set_agreement(self.shape, self.sel[which], self.nsel[which], self.sel["exact"],
                                   self.nsel["exact"], b2s, counts, self.err, stream)

@@ -28,12 +28,22 @@ def _check(w, c, probe, step, q, qla, q_prev, S):
     assert int(probe.err.item()) == 0
     K = probe.K
     exact = ref.exact_topk_true_query(c.K, q, w.ctx, K)
-    la = {bh: ref.topk_select(key, K) for bh, (_, key) in ref.block_scores(c.K, qla, w.ctx).items()}
+
+    def predicted(rows):  # top-K under the decode path's scoring, rows [B][n][Hq][d]
+        if c.scoring == "pooled":
+            pooled = {(b, h): ref.pool_keys(c.K[b, h], w.ctx[b], w.nb_max) for b in range(w.B)
+                      for h in range(w.Hkv)}
+            sc = ref.block_scores_pooled(pooled, rows, w.ctx, w.d)
+        else:
+            sc = ref.block_scores(c.K, rows, w.ctx)
+        return {bh: ref.topk_select(key, K) for bh, (_, key) in sc.items()}
+
+    la = predicted(qla)
     if K == w.Kb:
         assert la == S  # the probe's lookahead set is the decode step's S
     preds = {"la": la}
     if q_prev is not None:
-        preds["prev"] = ref.exact_topk_true_query(c.K, q_prev, w.ctx, K)
+        preds["prev"] = predicted(q_prev[:, None])
     for which, pred in preds.items():
         counts = got[which].cpu().numpy()
         for (b, h), E in exact.items():
@@ -41,12 +51,12 @@ def _check(w, c, probe, step, q, qla, q_prev, S):
             assert tuple(counts[b, h].tolist()) == want, (which, b, h)
 
 
-@pytest.mark.parametrize("K", [None, 20])
-def test_agreement_counts_match_oracle(K):
+@pytest.mark.parametrize("K,scoring", [(None, "maxdot"), (20, "maxdot"), (None, "pooled")])
+def test_agreement_counts_match_oracle(K, scoring):
     from sparse_decode_attention_oasis_gb300.engine import AgreementProbe
 
     w = syn.Workload("agree", L=1, B=2, Hq=32, Hkv=8, ctx=[4096, 1500], Kb=32, C=4, n_hot=16)
-    c = Case(w)
+    c = Case(w, scoring=scoring)
     probe = AgreementProbe(c.st, K=K)
     q_prev = None
     for step in range(3):
