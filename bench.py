@@ -59,6 +59,7 @@ def parse():
                          "carry: the host copy of layer l rides in layer l+1's scoring launch")
     ap.add_argument("--scoring", default="maxdot", choices=["maxdot", "pooled"],
                     help="maxdot: scan of the full keys; pooled: scan of the min/max pooled keys")
+    ap.add_argument("--no-pooled", action="store_true", help="skip the pooled-scoring variant")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-hostlink", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -648,6 +649,44 @@ def run_gpu(args, rank, world, local_rank):
         bo = out_host.numel() * 4
         e2e = {"value": aggregate_value(world, L, nrep, 1000.0 * e2e_s), "unit": UNIT, "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": bo}
+        nxt += nrep
+
+    # the pooled-key scoring path (f1) on the same state: a short eager pre-roll under
+    # the new scorer, then the same timed steps captured as one graph
+    pooled = None
+    if args.scoring == "maxdot" and not args.no_pooled:
+        st.set_scoring("pooled")
+        for k in range(8):
+            s_k = first + k % args.steps
+            st.decode_step(nxt + k, qla_dev[s_k], q_dev[s_k], out_layers=out_dev, main=main, side=main,
+                           copy=args.copy)
+        nxt += 8
+        pmarks = GraphEvents(L * args.steps * 2 + 16)
+        pgraph = StepGraph(st, nxt, [qla_dev[s] for s in ts], [q_dev[s] for s in ts],
+                           [out_steps[k % 2] for k in range(args.steps)], mark=pmarks, copy=args.copy)
+        nxt += args.steps
+        torch.cuda.synchronize()
+        pa, pb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(pgraph.stream):
+            pa.record(pgraph.stream)
+            pgraph.replay()
+            pb.record(pgraph.stream)
+        torch.cuda.synchronize()
+        pms = reduce_max(pa.elapsed_time(pb), world, dev)
+        pscore = pmarks.durations()["score"]
+        del pgraph
+        torch.cuda.synchronize()
+        pmarks.close()
+        pab = algorithmic_bytes(w, attended_per_head, "pooled")
+        pavg = sum(pscore) / len(pscore)
+        pach = pab["score"] / (pavg / 1000.0) / 1e9
+        pooled = {"value": aggregate_value(world, L, args.steps, pms), "unit": UNIT,
+                  "ms_per_step": pms / args.steps,
+                  "score_kernel": {"kernel": "score_pooled_kernel", "avg_launch_ms": pavg,
+                                   "bytes_per_launch": pab["score"], "achieved_gbs": pach,
+                                   "frac": pach / measured_peaks()[0]}}
+        errw |= int(st.scratch.err.item()) | int(st.scratch2.err.item())
+        st.set_scoring("maxdot")
 
     # prediction agreement per layer (Figure 6 / Figure 4 analogue), one step, untimed
     agreement = measure_agreement(st, qla_dev[first], q_dev[first], q_dev[first - 1])
@@ -686,6 +725,7 @@ def run_gpu(args, rank, world, local_rank):
         "copy_mode": args.copy,
         "hostlink": hostlink,
         "prediction_agreement": agreement,
+        "pooled_scoring": pooled,
         "clocks": clk,
         "e2e": e2e,
         "device_error_word": errw,

@@ -14,8 +14,9 @@
 //
 // As in the full scorer, the 256-long axis is permuted identically for K' and Q'
 // so that each thread's 16-byte loads of rows g and g+8 are its A fragments
-// (chunks t, t+4, ..., t+28 of the row); Q' fragments are built once per chunk of
-// blocks in shared memory (fragment order, conflict-free).  Bound: e = 2^-12 |q'|
+// (chunks t, t+4, ..., t+28 of the row).  Each CTA takes a contiguous range of
+// chunks of 128 blocks; Q' fragments are built in shared memory (fragment order,
+// conflict-free) whenever that range moves to another head.  Bound: e = 2^-12 |q'|
 // |k'| / sqrt(d) + |s~| 2^-22 + 2^-60 with |q'| = |q|; the modelled tensor-core
 // accumulation error of 16 steps of 16 exact products is 272 x 2^-23 ~ 2^-14.9,
 // a 7x margin.  Optionally carries the copy half of a gather (fetch_copy.cuh).
@@ -54,7 +55,13 @@ score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restr
   const int G = s.Hq / s.Hkv;
   const int N = s.n_la * G;
 
-  for (int chunk = blockIdx.x; chunk < total_chunks; chunk += gridDim.x) {
+  // a contiguous range of chunks per CTA: consecutive chunks mostly share a head,
+  // so the Q' fragments are rebuilt only when the head changes
+  const int c_begin = (int)((long long)blockIdx.x * total_chunks / gridDim.x);
+  const int c_end = (int)((long long)(blockIdx.x + 1) * total_chunks / gridDim.x);
+  int cur_head = -1;
+  float qnorm = 0.f;
+  for (int chunk = c_begin; chunk < c_end; ++chunk) {
     const int head = chunk / chunks_per_head;
     const int c = chunk - head * chunks_per_head;
     const int b = head / s.Hkv, h = head - b * s.Hkv;
@@ -62,7 +69,9 @@ score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restr
     const int blk0 = c * kPsChunk;
     if (blk0 >= nb) continue;
     const int blk1 = min(nb, blk0 + kPsChunk);
-    __syncthreads();  // every warp is done with the previous chunk's fragments
+    if (head != cur_head) {
+    cur_head = head;
+    __syncthreads();  // every warp is done with the previous head's fragments
     float qn2 = 0.f;
     for (int nt = warp; nt < NT; nt += kPsWarps) {
       const int n = nt * 8 + g;
@@ -100,7 +109,8 @@ score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restr
     float qmax = qn_w[0];
 #pragma unroll
     for (int w = 1; w < kPsWarps; ++w) qmax = fmaxf(qmax, qn_w[w]);
-    const float qnorm = sqrtf(qmax);
+    qnorm = sqrtf(qmax);
+    }
 
     const uint16_t* base = kp + (long long)head * s.nb_max * kPK;
     for (int tile = blk0 + warp * 16; tile < blk1; tile += kPsWarps * 16) {

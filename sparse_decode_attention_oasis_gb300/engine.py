@@ -197,6 +197,21 @@ class DecodeState:
             self.pool_layer(lp)
         torch.cuda.synchronize(dev)
 
+    def set_scoring(self, scoring: str):
+        """Switch the decode path between max-dot and pooled scoring.  The pooled key
+        cache is made (and built from the current keys) on first use and then kept
+        current by appends in either mode."""
+        if scoring not in ("maxdot", "pooled"):
+            raise ValueError(f"unknown scoring {scoring!r}")
+        if scoring == "pooled" and self.Kp is None:
+            s = self.shape
+            self.Kp = torch.zeros((self.L_phys, s.B, s.Hkv, s.nb_max, 2, 128), dtype=torch.bfloat16,
+                                  device=self.device)
+            self.Kpl = [self.Kp[l] for l in range(self.L_phys)]
+            for lp in range(self.L_phys):
+                self.pool_layer(lp)
+        self.scoring = scoring
+
     def pool_layer(self, lp: int, stream=None):
         """Rebuild layer lp's pooled keys from its full keys (pooled scoring only)."""
         if self.Kp is None:
@@ -262,7 +277,7 @@ class DecodeState:
             if gather == "split":
                 B.oasis_copy_fetched(s, self.host[lh], sc.fetch, sc.nfetch, self.blk2slot[lp],
                                      self.k_pool[lp], self.v_pool[lp], sc.err, gs)
-            elif self.Kp is not None:
+            elif self.scoring == "pooled":
                 B.oasis_score_blocks_pooled(s, self.Kp[lp], self.ctx, q_la, sc.scores, self.host[lh], sc.fetch,
                                             sc.nfetch, self.blk2slot[lp], self.k_pool[lp], self.v_pool[lp],
                                             sc.err, gs)
@@ -298,7 +313,7 @@ class DecodeState:
 
     def _select_lp(self, lp, q_la, sc, st, mark=None, carry=None):
         s = self.shape
-        pooled = self.Kp is not None
+        pooled = self.scoring == "pooled"
         K = self.Kpl[lp] if pooled else self.Kl[lp]
         if mark:
             mark("score", st)
@@ -526,7 +541,7 @@ class AgreementProbe:
         """Counts [B][Hkv][3] for the lookahead prediction (and the previous-token one)."""
         st = self.st
         stream = stream or torch.cuda.current_stream(st.device)
-        pooled = st.Kp is not None  # the predictors score as the decode path does
+        pooled = st.scoring == "pooled"  # the predictors score as the decode path does
         self._topk(self.shape1, layer, q, "exact", stream)
         self._topk(self.shape, layer, q_la, "la", stream, pooled)
         b2s = st.b2sl[layer % st.L_phys]
