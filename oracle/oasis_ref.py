@@ -29,6 +29,9 @@ Lookahead Sparse Prefetching"):
           the true next-token query.
   [fig4]  metalmedia.ai page, Figure 4 caption: top-20 block prediction
           accuracy per layer from the previous token versus a lookahead token.
+  [fig8]  metalmedia.ai page, Figure 8 caption: across two decode steps, the
+          draft query of step t drives a layer's top-K prediction, selection and
+          transfer, which complete before that layer's attention at step t+1.
 
 Readings where the pages are silent (each is listed in the design notes):
   * score(b) = max over lookahead queries j, query heads g of the GQA group of
@@ -414,12 +417,18 @@ def set_agreement(pred: Sequence[int], exact: Sequence[int], blk2slot: np.ndarra
 # --------------------------------------------------------------------------
 def layer_step(k_bits, q_la_bits, q_bits, ctx_len, host_kv, k_pool, v_pool,
                blk2slot, slot2blk, last_used, Kb: int, C: int, step: int,
-               scale: float = None, bs: int = BS_DEFAULT, heads=None, scoring: str = "maxdot") -> Dict:
+               scale: float = None, bs: int = BS_DEFAULT, heads=None, scoring: str = "maxdot",
+               prev_S: Dict = None) -> Dict:
     """Run a1..a5 for one layer.  Tables and pools are updated in place.
 
     host_kv bits [B][Hkv][nb_max][2][bs][d]; k_pool/v_pool bits [B][Hkv][P][bs][d].
     scoring: "maxdot" (a1, the exact max over tokens) or "pooled" (f1, the score
     from the per-block min/max pooled keys of the valid tokens).
+    prev_S: the cross-step pipeline of [fig8] (f4): the lookahead queries of the
+    previous step chose this step's blocks.  Attention then runs first, over
+    A = prev_S[(b, h)] intersected with the blocks resident on entry (the previous
+    step's gather brought them in), with the pools as they are on entry; the
+    selection and gather of this step only prepare the next one.
     Returns dict with per-head S, F, copies, A and out float64 [B][Hq][d].
     """
     B, Hkv, T_max, d = k_bits.shape
@@ -438,6 +447,13 @@ def layer_step(k_bits, q_la_bits, q_bits, ctx_len, host_kv, k_pool, v_pool,
         raise ValueError(scoring)
     res = {"S": {}, "F": {}, "copies": {}, "A": {}, "score": {},
            "out": np.zeros((B, Hq, d))}
+    if prev_S is not None:
+        for (b, h) in pairs:
+            A = attended_blocks(prev_S[(b, h)], blk2slot[b, h])
+            res["out"][b, h * G:(h + 1) * G] = head_sparse_attention(
+                q_bits[b, h * G:(h + 1) * G], k_pool[b, h], v_pool[b, h], A, blk2slot[b, h], int(ctx_len[b]),
+                scale, bs)
+            res["A"][(b, h)] = A
     for (b, h) in pairs:
         sc, key = scores[(b, h)]
         S = topk_select(key, Kb)
@@ -446,13 +462,14 @@ def layer_step(k_bits, q_la_bits, q_bits, ctx_len, host_kv, k_pool, v_pool,
         for (x, p) in copies:
             k_pool[b, h, p] = host_kv[b, h, x, 0]
             v_pool[b, h, p] = host_kv[b, h, x, 1]
-        A = attended_blocks(S, blk2slot[b, h])
-        o = head_sparse_attention(q_bits[b, h * G:(h + 1) * G], k_pool[b, h], v_pool[b, h],
-                                  A, blk2slot[b, h], int(ctx_len[b]), scale, bs)
-        res["out"][b, h * G:(h + 1) * G] = o
+        if prev_S is None:
+            A = attended_blocks(S, blk2slot[b, h])
+            o = head_sparse_attention(q_bits[b, h * G:(h + 1) * G], k_pool[b, h], v_pool[b, h],
+                                      A, blk2slot[b, h], int(ctx_len[b]), scale, bs)
+            res["out"][b, h * G:(h + 1) * G] = o
+            res["A"][(b, h)] = A
         res["S"][(b, h)] = S
         res["F"][(b, h)] = F
         res["copies"][(b, h)] = copies
-        res["A"][(b, h)] = A
         res["score"][(b, h)] = (sc, key)
     return res
