@@ -53,10 +53,11 @@ def parse():
                     help="physical host-tier layers (0 = all layers if host memory allows)")
     ap.add_argument("--preroll", type=int, default=40,
                     help="untimed decode steps run first, so the timed steps see a warmed-up resident set")
-    ap.add_argument("--copy", default="gather", choices=["gather", "overlap", "carry"],
-                    help="overlap: gather of layer l on a side stream beside the attention of layer l-1; "
-                         "gather: one gather launch per layer after its selection, one stream; "
-                         "carry: the host copy of layer l rides in layer l+1's scoring launch")
+    ap.add_argument("--copy", default="gather", choices=["gather", "overlap", "carry", "lag"],
+                    help="gather: one gather launch per layer after its selection, one stream; "
+                         "overlap: gather of layer l on a side stream beside the attention of layer l-1; "
+                         "carry: the host copy of layer l rides in layer l+1's scoring launch; "
+                         "lag: cross-step pipeline, attention over the previous step's selection")
     ap.add_argument("--scoring", default="maxdot", choices=["maxdot", "pooled"],
                     help="maxdot: scan of the full keys; pooled: scan of the min/max pooled keys")
     ap.add_argument("--no-pooled", action="store_true", help="skip the pooled-scoring variant")

@@ -102,6 +102,19 @@ class LayerScratch:
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
 
 
+class _SelView:
+    """A scratch set whose selection (sel, nsel) lives in per-layer buffers that
+    outlast the step (the cross-step pipeline reads them one step later)."""
+
+    def __init__(self, base: LayerScratch, sel: torch.Tensor, nsel: torch.Tensor):
+        self._base = base
+        self.sel = sel
+        self.nsel = nsel
+
+    def __getattr__(self, name):
+        return getattr(self._base, name)
+
+
 class DecodeState:
     def __init__(self, w: syn.Workload, device="cuda", l_phys: Optional[int] = None,
                  l_host: Optional[int] = None, pin_host: bool = True, scoring: str = "maxdot"):
@@ -149,6 +162,9 @@ class DecodeState:
         self.s2bl = [self.slot2blk[l] for l in range(Lp)]
         self.lul = [self.last_used[l] for l in range(Lp)]
         self.hostl = [self.host[l] for l in range(self.L_host)]
+        self._lag_sel = None  # per-layer selections of the cross-step pipeline (copy="lag")
+        self._lag_nsel = None
+        self._lag_ready = False
 
     # ---------------------------------------------------------------- filling
     def fill_layer_numpy(self, layer: int, K_bits: np.ndarray, V_bits: np.ndarray,
@@ -386,6 +402,9 @@ class DecodeState:
           The table half of layer l's gather runs right after its selection; the
           host-link copy of layer l rides in layer l+1's scoring launch, whose
           HBM-bound work hides the link latency; attn(l) follows that launch.
+        copy="lag": the cross-step pipeline (f4): attn(l) over the selection the
+          previous step made for layer l, then select(l) and gather(l) for the next
+          step; one stream.
         copy="overlap": select(l) on ``main``, then the whole gather of layer l on a
           side stream while ``main`` runs attn(l-1); select(l+1) waits for gather(l).
         copy="gather": select(0); select(1); attn(0); select(2); attn(1); ... with
@@ -414,6 +433,45 @@ class DecodeState:
             if count is not None:
                 count.add_(self.attended_blocks(l, scr[l % 2]))
 
+        if copy == "lag":
+            # f4: attn(l) over the blocks the previous step's lookahead selected (held
+            # in per-layer buffers), then this step's selection and gather of layer l,
+            # which only prepare the next step.  The first lagged step has no earlier
+            # selection: it selects and gathers first, then attends, like "gather".
+            if self._lag_sel is None:
+                s_ = self.shape
+                self._lag_sel = torch.full((self.L_phys, s_.B, s_.Hkv, s_.Kb), -1, dtype=torch.int32,
+                                           device=self.device)
+                self._lag_nsel = torch.zeros((self.L_phys, s_.B, s_.Hkv), dtype=torch.int32, device=self.device)
+                self._lag_ready = False
+            first = not self._lag_ready
+            for l in range(L):
+                lp = l % self.L_phys
+                view = _SelView(scr[l % 2], self._lag_sel[lp], self._lag_nsel[lp])
+                if not first:
+                    if mark:
+                        mark("attn", main)
+                    self._attend(l, q_layers[l], view, main, None if out_layers is None else out_layers[l])
+                    if mark:
+                        mark("attn_end", main)
+                    if count is not None:
+                        count.add_(self.attended_blocks(l, view))
+                self._select(l, q_la_layers[l], step, view, main, mark)
+                if mark:
+                    mark("gather", main)
+                self._gather(l, step, view, main)
+                if mark:
+                    mark("gather_end", main)
+                if first:
+                    if mark:
+                        mark("attn", main)
+                    self._attend(l, q_layers[l], view, main, None if out_layers is None else out_layers[l])
+                    if mark:
+                        mark("attn_end", main)
+                    if count is not None:
+                        count.add_(self.attended_blocks(l, view))
+            self._lag_ready = True
+            return
         if copy == "carry":
             for l in range(L):
                 self._select(l, q_la_layers[l], step, scr[l % 2], main, mark,

@@ -108,3 +108,37 @@ def test_copy_reports_out_of_range_fetch_entry():
     torch.cuda.synchronize()
     assert int(err.item()) == B.EW_BAD_BLOCK
     assert torch.equal(st.k_pool, kp0) and torch.equal(st.v_pool, vp0)
+
+
+def test_cross_step_pipeline_matches_oracle():
+    """copy="lag": step 0 selects, gathers and attends; later steps attend the
+    previous step's selection first (oracle prev_S), then select and gather."""
+    from sparse_decode_attention_oasis_gb300.engine import DecodeState
+
+    L = 2
+    w = syn.Workload("lag", L=L, B=2, Hq=32, Hkv=8, ctx=[2500, 1234], Kb=32, C=3, n_hot=16)
+    st = DecodeState(w, l_phys=L, l_host=L)
+    layers = []
+    for l in range(L):
+        K, V = syn.layer_kv(w, l)
+        host = syn.host_tier_from_kv(w, K, V)
+        b2s, s2b, lu = [np.array(t) for t in syn.initial_tables(w, l)]
+        kp, vp = syn.pools_from_tables(w, host, s2b)
+        st.fill_layer_numpy(l, K, V, b2s, s2b, lu)
+        layers.append([K, host, b2s, s2b, lu, kp, vp, None])
+    out = torch.empty((L, w.B, w.Hq, w.d), dtype=torch.float32, device="cuda")
+    for step in range(4):
+        qs = [syn.layer_queries(w, l, step) for l in range(L)]
+        st.decode_step(step, [_dev_bits(qla) for _, qla in qs], [_dev_bits(q) for q, _ in qs],
+                       out_layers=out, copy="lag")
+        torch.cuda.synchronize()
+        assert int(st.scratch.err.item()) == 0 and int(st.scratch2.err.item()) == 0
+        for l in range(L):
+            K, host, b2s, s2b, lu, kp, vp, prev = layers[l]
+            q, qla = qs[l]
+            r = ref.layer_step(K, qla, q, w.ctx, host, kp, vp, b2s, s2b, lu, w.Kb, w.C, step, prev_S=prev)
+            layers[l][7] = r["S"]
+            np.testing.assert_array_equal(st.blk2slot[l].cpu().numpy(), b2s)
+            np.testing.assert_array_equal(st.slot2blk[l].cpu().numpy(), s2b)
+            np.testing.assert_array_equal(st.last_used[l].cpu().numpy(), lu)
+            _check_out(out[l].cpu().numpy().astype(np.float64), r["out"], f"layer {l} step {step}")
