@@ -719,6 +719,8 @@ def run_gpu(args, rank, world, local_rank):
                      "bytes_per_launch": ab["score"],
                      "avg_launch_ms": score_avg_ms},
         "kernel_avg_us": {k: round(1000.0 * sum(v) / len(v), 2) for k, v in kernel_ms.items() if v},
+        "kernel_p50_us": {k: round(1000.0 * statistics.median(v), 2) for k, v in kernel_ms.items() if v},
+        "kernel_max_us": {k: round(1000.0 * max(v), 2) for k, v in kernel_ms.items() if v},
         "attended_blocks_per_head": round(attended_per_head, 2),
         "timed_steps": [pre + args.warmup, pre + args.warmup + args.steps - 1],
         "ms_per_step_eager_python": eager_ms,

@@ -408,6 +408,32 @@ OASIS_API oasis_status oasis_fetch_diff_capped_pooled(const oasis_shape* shape,
                                                       int32_t* nfetch, oasis_stream_t stream);
 
 /*
+ * f2. Fused look-ahead attention.
+ * Defines: the attention kernel processes the normal and the draft queries
+ * together over the sparse KV (metalmedia.ai page, Figure 7 caption, right).
+ * With A as in oasis_sparse_decode_attn, for every query head hq = h*G + g:
+ *   out[b][hq]       = sum over valid tokens t of A of softmax_t(scale * q[b][hq] . k_t) v_t
+ *   out_la[b][j][hq] = the same with q_la[b][j][hq] (j < n_la),
+ * zero where A has no valid token.  Each attended block's K and V are read once
+ * per 16 query rows ((1 + n_la) * G rows per KV head).
+ * Arguments: as oasis_sparse_decode_attn, plus
+ *   q_la      device bf16 [B][n_la][Hq][d]   the lookahead queries
+ *   out_la    device float [B][n_la][Hq][d]  out
+ *   workspace ws_bytes >= oasis_attn_lookahead_workspace_bytes(shape)
+ */
+OASIS_API size_t oasis_attn_lookahead_workspace_bytes(const oasis_shape* shape);
+
+OASIS_API oasis_status oasis_sparse_decode_attn_lookahead(const oasis_shape* shape, const void* q,
+                                                          const void* q_la, const void* k_pool,
+                                                          const void* v_pool, const int32_t* sel,
+                                                          const int32_t* nsel,
+                                                          const int32_t* blk2slot,
+                                                          const int32_t* ctx_len, float scale,
+                                                          void* workspace, size_t ws_bytes,
+                                                          float* out, float* out_la,
+                                                          oasis_stream_t stream);
+
+/*
  * f3. Agreement of a predicted top-K set with the exact one (measurement only).
  * Defines: the per-layer agreement between the blocks the draft (lookahead)
  * queries select and the exact top-K blocks of the true next-token query

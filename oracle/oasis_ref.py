@@ -418,7 +418,7 @@ def set_agreement(pred: Sequence[int], exact: Sequence[int], blk2slot: np.ndarra
 def layer_step(k_bits, q_la_bits, q_bits, ctx_len, host_kv, k_pool, v_pool,
                blk2slot, slot2blk, last_used, Kb: int, C: int, step: int,
                scale: float = None, bs: int = BS_DEFAULT, heads=None, scoring: str = "maxdot",
-               prev_S: Dict = None) -> Dict:
+               prev_S: Dict = None, lookahead_out: bool = False) -> Dict:
     """Run a1..a5 for one layer.  Tables and pools are updated in place.
 
     host_kv bits [B][Hkv][nb_max][2][bs][d]; k_pool/v_pool bits [B][Hkv][P][bs][d].
@@ -429,6 +429,8 @@ def layer_step(k_bits, q_la_bits, q_bits, ctx_len, host_kv, k_pool, v_pool,
     A = prev_S[(b, h)] intersected with the blocks resident on entry (the previous
     step's gather brought them in), with the pools as they are on entry; the
     selection and gather of this step only prepare the next one.
+    lookahead_out: also attend the lookahead queries over the same A (f2, the
+    fused look-ahead attention of [fig7] right): res["out_la"] [B][n_la][Hq][d].
     Returns dict with per-head S, F, copies, A and out float64 [B][Hq][d].
     """
     B, Hkv, T_max, d = k_bits.shape
@@ -445,14 +447,25 @@ def layer_step(k_bits, q_la_bits, q_bits, ctx_len, host_kv, k_pool, v_pool,
         scores = block_scores(k_bits, q_la_bits, ctx_len, bs, heads=pairs)
     else:
         raise ValueError(scoring)
+    n_la = q_la_bits.shape[1]
     res = {"S": {}, "F": {}, "copies": {}, "A": {}, "score": {},
            "out": np.zeros((B, Hq, d))}
+    if lookahead_out:
+        res["out_la"] = np.zeros((B, n_la, Hq, d))
+
+    def attend_la(b, h, A):
+        if lookahead_out:
+            for j in range(n_la):
+                res["out_la"][b, j, h * G:(h + 1) * G] = head_sparse_attention(
+                    q_la_bits[b, j, h * G:(h + 1) * G], k_pool[b, h], v_pool[b, h], A, blk2slot[b, h],
+                    int(ctx_len[b]), scale, bs)
     if prev_S is not None:
         for (b, h) in pairs:
             A = attended_blocks(prev_S[(b, h)], blk2slot[b, h])
             res["out"][b, h * G:(h + 1) * G] = head_sparse_attention(
                 q_bits[b, h * G:(h + 1) * G], k_pool[b, h], v_pool[b, h], A, blk2slot[b, h], int(ctx_len[b]),
                 scale, bs)
+            attend_la(b, h, A)
             res["A"][(b, h)] = A
     for (b, h) in pairs:
         sc, key = scores[(b, h)]
@@ -467,6 +480,7 @@ def layer_step(k_bits, q_la_bits, q_bits, ctx_len, host_kv, k_pool, v_pool,
             o = head_sparse_attention(q_bits[b, h * G:(h + 1) * G], k_pool[b, h], v_pool[b, h],
                                       A, blk2slot[b, h], int(ctx_len[b]), scale, bs)
             res["out"][b, h * G:(h + 1) * G] = o
+            attend_la(b, h, A)
             res["A"][(b, h)] = A
         res["S"][(b, h)] = S
         res["F"][(b, h)] = F

@@ -69,6 +69,9 @@ _SIGS = {
     "oasis_topk_select_pooled": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
     "oasis_fetch_diff_capped_pooled": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                         ctypes.c_int32, _VP, _VP, _VP], ctypes.c_int),
+    "oasis_attn_lookahead_workspace_bytes": ([ctypes.POINTER(Shape)], ctypes.c_size_t),
+    "oasis_sparse_decode_attn_lookahead": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                            ctypes.c_float, _VP, ctypes.c_size_t, _VP, _VP, _VP], ctypes.c_int),
     "oasis_sparse_decode_attn": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                   ctypes.c_float, _VP, ctypes.c_size_t, _VP, _VP], ctypes.c_int),
     "oasis_attn_workspace_bytes": ([ctypes.POINTER(Shape)], ctypes.c_size_t),
@@ -228,6 +231,19 @@ def oasis_fetch_diff_capped_pooled(shape: Shape, scores, k_pooled, q_la, ctx_len
     _check("oasis_fetch_diff_capped_pooled", load().oasis_fetch_diff_capped_pooled(
         ctypes.byref(shape), _ptr(scores), _ptr(k_pooled), _ptr(q_la), _ptr(ctx_len), _ptr(sel), _ptr(nsel),
         _ptr(blk2slot), int(fetch_cap), _ptr(fetch), _ptr(nfetch), _stream(stream)))
+
+
+def oasis_attn_lookahead_workspace_bytes(shape: Shape) -> int:
+    return int(load().oasis_attn_lookahead_workspace_bytes(ctypes.byref(shape)))
+
+
+def oasis_sparse_decode_attn_lookahead(shape: Shape, q, q_la, k_pool, v_pool, sel, nsel, blk2slot, ctx_len,
+                                       scale: float, workspace, ws_bytes: int, out, out_la, stream=None):
+    """True and lookahead queries over the same sparse KV: out [B][Hq][d], out_la [B][n_la][Hq][d]."""
+    _check("oasis_sparse_decode_attn_lookahead", load().oasis_sparse_decode_attn_lookahead(
+        ctypes.byref(shape), _ptr(q), _ptr(q_la), _ptr(k_pool), _ptr(v_pool), _ptr(sel), _ptr(nsel),
+        _ptr(blk2slot), _ptr(ctx_len), float(scale), _ptr(workspace), int(ws_bytes), _ptr(out), _ptr(out_la),
+        _stream(stream)))
 
 
 def oasis_sparse_decode_attn(shape: Shape, q, k_pool, v_pool, sel, nsel, blk2slot, ctx_len,

@@ -35,6 +35,10 @@ cudaError_t launch_topk_select_pooled(const Shape&, const float2*, const uint16_
                                       int*, int*, cudaStream_t);
 cudaError_t launch_fetch_diff_pooled(const Shape&, const float2*, const uint16_t*, const uint16_t*, const int*,
                                      const int*, const int*, const int*, int, int*, int*, cudaStream_t);
+cudaError_t launch_attn_lookahead(const Shape&, const uint16_t*, const uint16_t*, const uint16_t*, const uint16_t*,
+                                  const int*, const int*, const int*, const int*, float, void*, float*, float*,
+                                  cudaStream_t);
+size_t attn_la_workspace_bytes(const Shape&);
 cudaError_t launch_append_kv(const Shape&, const uint16_t*, const uint16_t*, int*, uint16_t*, uint16_t*, const int*,
                              uint16_t*, uint16_t*, int, unsigned*, cudaStream_t);
 size_t topk_smem_bytes(const Shape&);
@@ -381,6 +385,41 @@ oasis_status oasis_fetch_diff_capped_pooled(const oasis_shape* shape, const floa
                                                   static_cast<const uint16_t*>(k_pooled),
                                                   static_cast<const uint16_t*>(q_la), ctx_len, sel, nsel, blk2slot,
                                                   fetch_cap, fetch, nfetch, (cudaStream_t)stream);
+  return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
+}
+
+size_t oasis_attn_lookahead_workspace_bytes(const oasis_shape* shape) {
+  oasis::Shape s;
+  if (check_shape(shape, "oasis_attn_lookahead_workspace_bytes", &s) != OASIS_OK) return 0;
+  return oasis::attn_la_workspace_bytes(s);
+}
+
+oasis_status oasis_sparse_decode_attn_lookahead(const oasis_shape* shape, const void* q, const void* q_la,
+                                                const void* k_pool, const void* v_pool, const int32_t* sel,
+                                                const int32_t* nsel, const int32_t* blk2slot,
+                                                const int32_t* ctx_len, float scale, void* workspace,
+                                                size_t ws_bytes, float* out, float* out_la,
+                                                oasis_stream_t stream) {
+  static const char* fn = "oasis_sparse_decode_attn_lookahead";
+  oasis::Shape s;
+  oasis_status st = check_shape(shape, fn, &s);
+  if (st != OASIS_OK) return st;
+  REQUIRE(q && aligned(q, 16) && q_la && aligned(q_la, 16), "q and q_la must be 16-byte aligned device pointers");
+  REQUIRE(k_pool && v_pool && aligned(k_pool, 16) && aligned(v_pool, 16),
+          "k_pool/v_pool must be 16-byte aligned device pointers");
+  REQUIRE(sel && nsel && blk2slot && ctx_len, "table pointers must be non-NULL");
+  REQUIRE(aligned(sel, 4) && aligned(nsel, 4) && aligned(blk2slot, 4) && aligned(ctx_len, 4),
+          "int32 arrays must be 4-byte aligned");
+  REQUIRE(out && aligned(out, 16) && out_la && aligned(out_la, 16),
+          "out and out_la must be 16-byte aligned device pointers");
+  REQUIRE(workspace && aligned(workspace, 16), "workspace must be a 16-byte aligned device pointer");
+  REQUIRE(ws_bytes >= oasis::attn_la_workspace_bytes(s),
+          "workspace is smaller than oasis_attn_lookahead_workspace_bytes()");
+  REQUIRE(scale == scale && scale > 0.f, "scale must be a positive number");
+  cudaError_t e = oasis::launch_attn_lookahead(s, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(q_la),
+                                               static_cast<const uint16_t*>(k_pool),
+                                               static_cast<const uint16_t*>(v_pool), sel, nsel, blk2slot, ctx_len,
+                                               scale, workspace, out, out_la, (cudaStream_t)stream);
   return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
 }
 

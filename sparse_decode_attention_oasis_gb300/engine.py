@@ -382,6 +382,20 @@ class DecodeState:
                                    self.ctx, self.scale, sc.ws, sc.ws_bytes,
                                    sc.out if out is None else out, st)
 
+    def attend_lookahead(self, layer: int, q: torch.Tensor, q_la: torch.Tensor, sc, out: torch.Tensor,
+                         out_la: torch.Tensor, stream=None):
+        """f2: the true and the lookahead queries of one layer over the resident
+        blocks of sc's selection, in one launch (out [B][Hq][d], out_la
+        [B][n_la][Hq][d], fp32)."""
+        s = self.shape
+        lp = layer % self.L_phys
+        nbytes = B.oasis_attn_lookahead_workspace_bytes(s)
+        if getattr(self, "_la_ws", None) is None or self._la_ws.numel() < nbytes:
+            self._la_ws = torch.empty(max(16, nbytes), dtype=torch.uint8, device=self.device)
+        B.oasis_sparse_decode_attn_lookahead(s, q, q_la, self.kpl[lp], self.vpl[lp], sc.sel, sc.nsel, self.b2sl[lp],
+                                             self.ctx, self.scale, self._la_ws, nbytes, out, out_la,
+                                             stream or torch.cuda.current_stream(self.device))
+
     def attended_blocks(self, layer: int, sc: "LayerScratch") -> torch.Tensor:
         """Device count of attended blocks (selected and resident) of one layer, all heads."""
         lp = layer % self.L_phys

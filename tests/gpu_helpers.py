@@ -39,7 +39,7 @@ class Case:
         self.st = DecodeState(w, l_phys=1, scoring=scoring)
         self.st.fill_layer_numpy(0, K, V, self.b2s, self.s2b, self.lu)
 
-    def step(self, step, q=None, qla=None, C=None, append=False, gather="fused"):
+    def step(self, step, q=None, qla=None, C=None, append=False, gather="fused", lookahead=False):
         import torch
 
         w = self.w
@@ -54,10 +54,17 @@ class Case:
         if C is not None:
             w.C = C
         r = ref.layer_step(self.K, qla, q, w.ctx, self.host, self.kp, self.vp, self.b2s, self.s2b,
-                           self.lu, w.Kb, w.C, step, bs=w.bs, scoring=self.scoring)
+                           self.lu, w.Kb, w.C, step, bs=w.bs, scoring=self.scoring, lookahead_out=lookahead)
         sc = self.st.layer_step(0, _dev_bits(qla), _dev_bits(q), step, gather=gather)
         torch.cuda.synchronize()
         self.compare(r, sc)
+        if lookahead:
+            out = torch.empty((w.B, w.Hq, w.d), dtype=torch.float32, device="cuda")
+            out_la = torch.empty((w.B, w.n_la, w.Hq, w.d), dtype=torch.float32, device="cuda")
+            self.st.attend_lookahead(0, _dev_bits(q), _dev_bits(qla), sc, out, out_la)
+            torch.cuda.synchronize()
+            _check_out(out.cpu().numpy().astype(np.float64), r["out"], "fused true-query rows")
+            _check_out(out_la.cpu().numpy().astype(np.float64), r["out_la"], "fused lookahead rows")
         return r, sc
 
     def compare(self, r, sc):
