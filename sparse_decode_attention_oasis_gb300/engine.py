@@ -117,7 +117,8 @@ class _SelView:
 
 class DecodeState:
     def __init__(self, w: syn.Workload, device="cuda", l_phys: Optional[int] = None,
-                 l_host: Optional[int] = None, pin_host: bool = True, scoring: str = "maxdot"):
+                 l_host: Optional[int] = None, pin_host: bool = True, scoring: str = "maxdot",
+                 host_alloc: str = "thp"):
         """scoring: "maxdot" (a1, scan of the full keys) or "pooled" (f1, scan of the
         min/max pooled keys ``Kp``, bf16 [L][B][Hkv][nb_max][2][128], built from K
         by ``pool_all`` / the fill methods and kept current by ``append_tokens``)."""
@@ -142,10 +143,12 @@ class DecodeState:
         self.last_used = torch.full((Lp, s.B, s.Hkv, s.P), -1, dtype=torch.int32, device=dev)
         host_shape = (self.L_host, s.B, s.Hkv, s.nb_max, 2, 16, 128)
         self._host_buf = None
-        if pin_host:
+        if pin_host and host_alloc == "thp":
             nbytes = int(np.prod(host_shape)) * 2
             self._host_buf = HugePinnedBuffer(nbytes)
             self.host = self._host_buf.tensor.view(torch.bfloat16).view(host_shape)
+        elif pin_host:  # "cuda": page-locked by the CUDA allocator (cudaHostAlloc), base pages
+            self.host = torch.empty(host_shape, dtype=torch.bfloat16, pin_memory=True)
         else:
             self.host = torch.zeros(host_shape, dtype=torch.bfloat16)
         self.ctx = torch.tensor(w.ctx, dtype=torch.int32, device=dev)
@@ -212,6 +215,15 @@ class DecodeState:
             self.last_used[lp].copy_(torch.from_numpy(lu))
             self.pool_layer(lp)
         torch.cuda.synchronize(dev)
+
+    def touch_host_tier(self, chunk_bytes: int = 1 << 30):
+        """Read the whole host tier once through the copy engines (1 GiB at a time)."""
+        flat = self.host.view(-1).view(torch.uint8)
+        buf = torch.empty(min(chunk_bytes, flat.numel()), dtype=torch.uint8, device=self.device)
+        for off in range(0, flat.numel(), buf.numel()):
+            n = min(buf.numel(), flat.numel() - off)
+            buf[:n].copy_(flat[off:off + n], non_blocking=True)
+        torch.cuda.synchronize(self.device)
 
     def set_scoring(self, scoring: str):
         """Switch the decode path between max-dot and pooled scoring.  The pooled key
