@@ -493,7 +493,8 @@ def launches_per_step(st, copy):
     G = s.Hq // s.Hkv
     nsplit = st.scratch.ws_bytes // (s.B * s.Hkv * G * (s.d + 2) * 4)
     attn = 1 if nsplit <= 1 else 2  # split-K partials, then the combine kernel
-    per_layer = 4 + attn  # score (carrying the previous layer's copy), topk, diff, assign or gather
+    select = 1 if st.fused_select else 2  # top-K and diff in one launch, or two
+    per_layer = 1 + select + 1 + attn  # score (maybe carrying a copy), selection, gather or assign, attention
     return st.w.L * per_layer + (1 if copy == "carry" else 0)
 
 

@@ -173,6 +173,27 @@ OASIS_API oasis_status oasis_fetch_diff_capped(const oasis_shape* shape, const f
                                      oasis_stream_t stream);
 
 /*
+ * a2 + a3 in one launch: oasis_topk_select followed by oasis_fetch_diff_capped on
+ * the selection it wrote, run by the same thread block of each (request, KV head).
+ * Arguments are the union of the two calls'; outputs (sel, nsel, fetch, nfetch)
+ * are exactly those of the two calls made one after the other.
+ * oasis_topk_select_diff_pooled: the same with the pooled score (f1 below).
+ */
+OASIS_API oasis_status oasis_topk_select_diff(const oasis_shape* shape, const float* scores,
+                                              const void* k_hbm, const void* q_la,
+                                              const int32_t* ctx_len, const int32_t* blk2slot,
+                                              int32_t fetch_cap, int32_t* sel, int32_t* nsel,
+                                              int32_t* fetch, int32_t* nfetch,
+                                              oasis_stream_t stream);
+
+OASIS_API oasis_status oasis_topk_select_diff_pooled(const oasis_shape* shape,
+                                                     const float* scores, const void* k_pooled,
+                                                     const void* q_la, const int32_t* ctx_len,
+                                                     const int32_t* blk2slot, int32_t fetch_cap,
+                                                     int32_t* sel, int32_t* nsel, int32_t* fetch,
+                                                     int32_t* nfetch, oasis_stream_t stream);
+
+/*
  * a4. Host-tier gather into HBM slots, with the head-wise block table update.
  * Defines: prefetch the selected blocks from the host tier into the limited set
  * of HBM slots (OasisKV abstract; metalmedia.ai page, explanatory figure step 4),

@@ -72,6 +72,10 @@ _SIGS = {
     "oasis_attn_lookahead_workspace_bytes": ([ctypes.POINTER(Shape)], ctypes.c_size_t),
     "oasis_sparse_decode_attn_lookahead": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                             ctypes.c_float, _VP, ctypes.c_size_t, _VP, _VP, _VP], ctypes.c_int),
+    "oasis_topk_select_diff": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, ctypes.c_int32, _VP, _VP, _VP,
+                                _VP, _VP], ctypes.c_int),
+    "oasis_topk_select_diff_pooled": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, ctypes.c_int32, _VP, _VP,
+                                       _VP, _VP, _VP], ctypes.c_int),
     "oasis_sparse_decode_attn": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                   ctypes.c_float, _VP, ctypes.c_size_t, _VP, _VP], ctypes.c_int),
     "oasis_attn_workspace_bytes": ([ctypes.POINTER(Shape)], ctypes.c_size_t),
@@ -244,6 +248,21 @@ def oasis_sparse_decode_attn_lookahead(shape: Shape, q, q_la, k_pool, v_pool, se
         ctypes.byref(shape), _ptr(q), _ptr(q_la), _ptr(k_pool), _ptr(v_pool), _ptr(sel), _ptr(nsel),
         _ptr(blk2slot), _ptr(ctx_len), float(scale), _ptr(workspace), int(ws_bytes), _ptr(out), _ptr(out_la),
         _stream(stream)))
+
+
+def oasis_topk_select_diff(shape: Shape, scores, k_hbm, q_la, ctx_len, blk2slot, fetch_cap: int, sel, nsel,
+                           fetch, nfetch, stream=None):
+    """Top-K and the capped diff in one launch."""
+    _check("oasis_topk_select_diff", load().oasis_topk_select_diff(
+        ctypes.byref(shape), _ptr(scores), _ptr(k_hbm), _ptr(q_la), _ptr(ctx_len), _ptr(blk2slot), int(fetch_cap),
+        _ptr(sel), _ptr(nsel), _ptr(fetch), _ptr(nfetch), _stream(stream)))
+
+
+def oasis_topk_select_diff_pooled(shape: Shape, scores, k_pooled, q_la, ctx_len, blk2slot, fetch_cap: int, sel,
+                                  nsel, fetch, nfetch, stream=None):
+    _check("oasis_topk_select_diff_pooled", load().oasis_topk_select_diff_pooled(
+        ctypes.byref(shape), _ptr(scores), _ptr(k_pooled), _ptr(q_la), _ptr(ctx_len), _ptr(blk2slot),
+        int(fetch_cap), _ptr(sel), _ptr(nsel), _ptr(fetch), _ptr(nfetch), _stream(stream)))
 
 
 def oasis_sparse_decode_attn(shape: Shape, q, k_pool, v_pool, sel, nsel, blk2slot, ctx_len,

@@ -271,12 +271,14 @@ attn_combine_kernel(Shape s, const float* __restrict__ part_o, const float* __re
       make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
-// Splits per head: enough thread blocks to cover the GPU about four times, each
-// split holding at least 4 entries of S.
+// Splits per head: as many as keep the whole grid resident at once (2 CTAs per
+// SM: 208 registers x 128 threads), each split holding at least 4 entries of S.
+// A second wave would double the latency chain; a warp with more blocks keeps
+// its 2-stage ring busy instead.
 int attn_nsplit(const Shape& s) {
   const int heads = s.B * s.Hkv;
-  const int target = 4 * sm_count();
-  int ns = (target + heads - 1) / heads;
+  const int resident = 2 * sm_count();
+  int ns = resident / heads;
   const int max_ns = (s.Kb + 3) / 4;
   if (ns > max_ns) ns = max_ns;
   return ns < 1 ? 1 : ns;

@@ -297,8 +297,7 @@ int attn_la_nsplit(const Shape& s) {
   const int G = s.Hq / s.Hkv;
   const int MT = ((1 + s.n_la) * G + 15) / 16;
   const int units = s.B * s.Hkv * MT;
-  const int target = 4 * sm_count();
-  int ns = (target + units - 1) / units;
+  int ns = 2 * sm_count() / units;  // one resident wave, as for a5
   const int max_ns = (s.Kb + 3) / 4;
   if (ns > max_ns) ns = max_ns;
   return ns < 1 ? 1 : ns;

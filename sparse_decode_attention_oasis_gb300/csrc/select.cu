@@ -647,72 +647,14 @@ __device__ SelCtx make_ctx(char* sm, const SelLayout& L, const Shape& s, const u
   return c;
 }
 
-// ---------------------------------------------------------------- a2 kernel
+// ---------------------------------------------------------------- a3 (shared by both kernels)
+// F = the best min(cap, |M|) of the missing blocks M of S (ascending S of ns <= Kb
+// entries, one per thread), written ascending to fetch[head].  se, cls, U, cblk
+// hold at least Kb entries.
 template <bool kPooled>
-__global__ void __launch_bounds__(kSelThreads, 2)
-topk_select_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __restrict__ k_hbm,
-                   const uint16_t* __restrict__ q_la, const int* __restrict__ ctx_len,
-                   int* __restrict__ sel, int* __restrict__ nsel) {
-  extern __shared__ __align__(16) char sm[];
-  const SelLayout L = sel_layout(s.nb_max, false, s.Kb);
-  const int head = blockIdx.x;
-  const int b = head / s.Hkv;
-  const int ctx = ctx_len[b];
-  const int nb = clamp_nb(ctx, s.nb_max);
-  int* out = sel + (long long)head * s.Kb;
-  if (nb <= s.Kb) {
-    for (int i = threadIdx.x; i < s.Kb; i += blockDim.x) out[i] = i < nb ? i : -1;
-    if (threadIdx.x == 0) nsel[head] = nb;
-    return;
-  }
-  SelCtx c = make_ctx(sm, L, s, k_hbm, q_la, head, ctx, kPooled);
-  float2* se = reinterpret_cast<float2*>(sm + L.se);
-  uint8_t* cls = reinterpret_cast<uint8_t*>(sm + L.cls);
-  int* U = reinterpret_cast<int*>(sm + L.U);
-  int* red = reinterpret_cast<int*>(sm + L.red);
-  const float2* src = scores + (long long)head * s.nb_max;
-  for (int i = threadIdx.x; i < nb; i += blockDim.x) se[i] = src[i];
-  __syncthreads();
-  select_best<kPooled>(c, se, nb, s.Kb, nullptr, cls, U);
-  // compaction in ascending block order
-  const int per = (nb + kSelThreads - 1) / kSelThreads;
-  const int i0 = threadIdx.x * per, i1 = min(nb, i0 + per);
-  int cnt = 0;
-  for (int i = i0; i < i1; ++i) cnt += cls[i] == 1;
-  int total = 0;
-  int pos = block_excl_scan(cnt, red, red + 31);
-  total = red[31];
-  for (int i = i0; i < i1; ++i)
-    if (cls[i] == 1) {
-      if (pos < s.Kb) out[pos] = i;
-      ++pos;
-    }
-  for (int i = total + threadIdx.x; i < s.Kb; i += blockDim.x) out[i] = -1;
-  if (threadIdx.x == 0) nsel[head] = total < s.Kb ? total : s.Kb;
-}
-
-// ---------------------------------------------------------------- a3 kernel
-template <bool kPooled>
-__global__ void __launch_bounds__(kSelThreads, 2)
-fetch_diff_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __restrict__ k_hbm,
-                  const uint16_t* __restrict__ q_la, const int* __restrict__ ctx_len,
-                  const int* __restrict__ sel, const int* __restrict__ nsel,
-                  const int* __restrict__ blk2slot, int cap, int* __restrict__ fetch,
-                  int* __restrict__ nfetch) {
-  extern __shared__ __align__(16) char sm[];
-  const SelLayout L = sel_layout(s.Kb, true, s.Kb);
-  const int head = blockIdx.x;
-  const int b = head / s.Hkv;
-  const int ctx = ctx_len[b];
-  SelCtx c = make_ctx(sm, L, s, k_hbm, q_la, head, ctx, kPooled);
-  float2* se = reinterpret_cast<float2*>(sm + L.se);
-  uint8_t* cls = reinterpret_cast<uint8_t*>(sm + L.cls);
-  int* U = reinterpret_cast<int*>(sm + L.U);
-  int* cblk = reinterpret_cast<int*>(sm + L.cblk);
-  int* red = reinterpret_cast<int*>(sm + L.red);
-  int ns = nsel[head];
-  ns = ns < 0 ? 0 : (ns > s.Kb ? s.Kb : ns);
-  const int* S = sel + (long long)head * s.Kb;
+__device__ void capped_diff(SelCtx& c, const Shape& s, const float2* scores, const int* S, int ns,
+                            const int* blk2slot, int cap, int head, int* fetch, int* nfetch, float2* se,
+                            uint8_t* cls, int* U, int* cblk, int* red) {
   const int* b2s = blk2slot + (long long)head * s.nb_max;
   // missing blocks of S, in S order (ascending); one entry per thread (ns <= Kb <= 256)
   int x = -1, miss = 0;
@@ -738,19 +680,111 @@ fetch_diff_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __
   if (threadIdx.x == 0) nfetch[head] = total < s.Kb ? total : s.Kb;
 }
 
+// ---------------------------------------------------------------- a2 kernel
+// With kDiff the same CTA then runs a3 on the selection it just wrote (one launch
+// for top-K and capped diff).
+template <bool kPooled, bool kDiff>
+__global__ void __launch_bounds__(kSelThreads, 2)
+topk_select_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __restrict__ k_hbm,
+                   const uint16_t* __restrict__ q_la, const int* __restrict__ ctx_len,
+                   int* __restrict__ sel, int* __restrict__ nsel, const int* __restrict__ blk2slot, int cap,
+                   int* __restrict__ fetch, int* __restrict__ nfetch) {
+  extern __shared__ __align__(16) char sm[];
+  const SelLayout L = sel_layout(s.nb_max, kDiff, s.Kb);
+  const int head = blockIdx.x;
+  const int b = head / s.Hkv;
+  const int ctx = ctx_len[b];
+  const int nb = clamp_nb(ctx, s.nb_max);
+  int* out = sel + (long long)head * s.Kb;
+  SelCtx c = make_ctx(sm, L, s, k_hbm, q_la, head, ctx, kPooled);
+  float2* se = reinterpret_cast<float2*>(sm + L.se);
+  uint8_t* cls = reinterpret_cast<uint8_t*>(sm + L.cls);
+  int* U = reinterpret_cast<int*>(sm + L.U);
+  int* red = reinterpret_cast<int*>(sm + L.red);
+  if (nb <= s.Kb) {
+    for (int i = threadIdx.x; i < s.Kb; i += blockDim.x) out[i] = i < nb ? i : -1;
+    if (threadIdx.x == 0) nsel[head] = nb;
+    if constexpr (kDiff) {
+      __syncthreads();  // the selection written above is visible to the whole CTA
+      capped_diff<kPooled>(c, s, scores, out, nb, blk2slot, cap, head, fetch, nfetch, se, cls, U,
+                           reinterpret_cast<int*>(sm + L.cblk), red);
+    }
+    return;
+  }
+  const float2* src = scores + (long long)head * s.nb_max;
+  for (int i = threadIdx.x; i < nb; i += blockDim.x) se[i] = src[i];
+  __syncthreads();
+  select_best<kPooled>(c, se, nb, s.Kb, nullptr, cls, U);
+  // compaction in ascending block order
+  const int per = (nb + kSelThreads - 1) / kSelThreads;
+  const int i0 = threadIdx.x * per, i1 = min(nb, i0 + per);
+  int cnt = 0;
+  for (int i = i0; i < i1; ++i) cnt += cls[i] == 1;
+  int total = 0;
+  int pos = block_excl_scan(cnt, red, red + 31);
+  total = red[31];
+  for (int i = i0; i < i1; ++i)
+    if (cls[i] == 1) {
+      if (pos < s.Kb) out[pos] = i;
+      ++pos;
+    }
+  for (int i = total + threadIdx.x; i < s.Kb; i += blockDim.x) out[i] = -1;
+  if (threadIdx.x == 0) nsel[head] = total < s.Kb ? total : s.Kb;
+  if constexpr (kDiff) {
+    __syncthreads();  // the selection written above is visible to the whole CTA
+    capped_diff<kPooled>(c, s, scores, out, total < s.Kb ? total : s.Kb, blk2slot, cap, head, fetch, nfetch, se,
+                         cls, U, reinterpret_cast<int*>(sm + L.cblk), red);
+  }
+}
+
+// ---------------------------------------------------------------- a3 kernel
+template <bool kPooled>
+__global__ void __launch_bounds__(kSelThreads, 2)
+fetch_diff_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __restrict__ k_hbm,
+                  const uint16_t* __restrict__ q_la, const int* __restrict__ ctx_len,
+                  const int* __restrict__ sel, const int* __restrict__ nsel,
+                  const int* __restrict__ blk2slot, int cap, int* __restrict__ fetch,
+                  int* __restrict__ nfetch) {
+  extern __shared__ __align__(16) char sm[];
+  const SelLayout L = sel_layout(s.Kb, true, s.Kb);
+  const int head = blockIdx.x;
+  const int b = head / s.Hkv;
+  const int ctx = ctx_len[b];
+  SelCtx c = make_ctx(sm, L, s, k_hbm, q_la, head, ctx, kPooled);
+  float2* se = reinterpret_cast<float2*>(sm + L.se);
+  uint8_t* cls = reinterpret_cast<uint8_t*>(sm + L.cls);
+  int* U = reinterpret_cast<int*>(sm + L.U);
+  int* cblk = reinterpret_cast<int*>(sm + L.cblk);
+  int* red = reinterpret_cast<int*>(sm + L.red);
+  int ns = nsel[head];
+  ns = ns < 0 ? 0 : (ns > s.Kb ? s.Kb : ns);
+  capped_diff<kPooled>(c, s, scores, sel + (long long)head * s.Kb, ns, blk2slot, cap, head, fetch, nfetch, se, cls,
+                       U, cblk, red);
+}
+
 // ---------------------------------------------------------------- launchers
 size_t topk_smem_bytes(const Shape& s) { return sel_layout(s.nb_max, false, s.Kb).total; }
 size_t diff_smem_bytes(const Shape& s) { return sel_layout(s.Kb, true, s.Kb).total; }
 
-template <bool kPooled>
+template <bool kPooled, bool kDiff = false>
 static cudaError_t launch_topk(const Shape& s, const float2* scores, const uint16_t* k, const uint16_t* q_la,
-                               const int* ctx, int* sel, int* nsel, cudaStream_t stream) {
+                               const int* ctx, int* sel, int* nsel, cudaStream_t stream,
+                               const int* blk2slot = nullptr, int cap = 0, int* fetch = nullptr,
+                               int* nfetch = nullptr) {
   static int attr_cache[kMaxDevicesCached] = {};
-  const size_t smem = topk_smem_bytes(s);
-  cudaError_t e = ensure_dyn_smem((const void*)topk_select_kernel<kPooled>, smem, attr_cache);
+  const size_t smem = sel_layout(s.nb_max, kDiff, s.Kb).total;
+  cudaError_t e = ensure_dyn_smem((const void*)topk_select_kernel<kPooled, kDiff>, smem, attr_cache);
   if (e != cudaSuccess) return e;
-  topk_select_kernel<kPooled><<<s.B * s.Hkv, kSelThreads, smem, stream>>>(s, scores, k, q_la, ctx, sel, nsel);
+  topk_select_kernel<kPooled, kDiff><<<s.B * s.Hkv, kSelThreads, smem, stream>>>(s, scores, k, q_la, ctx, sel, nsel,
+                                                                                  blk2slot, cap, fetch, nfetch);
   return cudaGetLastError();
+}
+
+cudaError_t launch_topk_select_diff(const Shape& s, const float2* scores, const uint16_t* k, const uint16_t* q_la,
+                                    const int* ctx, const int* blk2slot, int cap, int* sel, int* nsel, int* fetch,
+                                    int* nfetch, bool pooled, cudaStream_t stream) {
+  return pooled ? launch_topk<true, true>(s, scores, k, q_la, ctx, sel, nsel, stream, blk2slot, cap, fetch, nfetch)
+                : launch_topk<false, true>(s, scores, k, q_la, ctx, sel, nsel, stream, blk2slot, cap, fetch, nfetch);
 }
 
 template <bool kPooled>

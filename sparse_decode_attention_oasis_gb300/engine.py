@@ -165,6 +165,7 @@ class DecodeState:
         self.s2bl = [self.slot2blk[l] for l in range(Lp)]
         self.lul = [self.last_used[l] for l in range(Lp)]
         self.hostl = [self.host[l] for l in range(self.L_host)]
+        self.fused_select = True  # a2 + a3 in one launch (oasis_topk_select_diff) on the decode path
         self._lag_sel = None  # per-layer selections of the cross-step pipeline (copy="lag")
         self._lag_nsel = None
         self._lag_ready = False
@@ -360,12 +361,17 @@ class DecodeState:
                 B.oasis_score_blocks_copy(s, K, self.ctx, q_la, sc.scores, *args)
         if mark:
             mark("topk", st)
-        topk = B.oasis_topk_select_pooled if pooled else B.oasis_topk_select
-        diff = B.oasis_fetch_diff_capped_pooled if pooled else B.oasis_fetch_diff_capped
-        topk(s, sc.scores, K, q_la, self.ctx, sc.sel, sc.nsel, st)
-        if mark:
-            mark("diff", st)
-        diff(s, sc.scores, K, q_la, self.ctx, sc.sel, sc.nsel, self.b2sl[lp], self.w.C, sc.fetch, sc.nfetch, st)
+        if self.fused_select:
+            f = B.oasis_topk_select_diff_pooled if pooled else B.oasis_topk_select_diff
+            f(s, sc.scores, K, q_la, self.ctx, self.b2sl[lp], self.w.C, sc.sel, sc.nsel, sc.fetch, sc.nfetch, st)
+        else:
+            topk = B.oasis_topk_select_pooled if pooled else B.oasis_topk_select
+            diff = B.oasis_fetch_diff_capped_pooled if pooled else B.oasis_fetch_diff_capped
+            topk(s, sc.scores, K, q_la, self.ctx, sc.sel, sc.nsel, st)
+            if mark:
+                mark("diff", st)
+            diff(s, sc.scores, K, q_la, self.ctx, sc.sel, sc.nsel, self.b2sl[lp], self.w.C, sc.fetch, sc.nfetch,
+                 st)
         if mark:
             mark("end", st)
 

@@ -133,3 +133,14 @@ def test_device_query_generator_matches_host():
     K, V = syn.kv_request_torch(w, 0, 1, "cuda")
     Kn, Vn = syn.head_kv(w, 0, 1, 3)
     assert (K[3].cpu().view(torch.int16).numpy().view(np.uint16) == Kn).all()
+
+
+@pytest.mark.parametrize("scoring", ["maxdot", "pooled"])
+def test_separate_topk_and_diff_kernels(scoring):
+    """The decode path runs top-K and the diff as one launch; the two separate
+    calls must give the same (oracle) results."""
+    w = syn.Workload("ragged", L=1, B=3, Hq=32, Hkv=8, ctx=[4096, 1000, 17], Kb=32, C=4, n_hot=16)
+    c = Case(w, scoring=scoring)
+    c.st.fused_select = False
+    for step in range(2):
+        c.step(step)
