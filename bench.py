@@ -64,7 +64,8 @@ def parse():
     ap.add_argument("--no-pooled", action="store_true", help="skip the pooled-scoring variant")
     ap.add_argument("--host-alloc", default="thp", choices=["thp", "cuda"],
                     help="host tier on transparent huge pages registered with CUDA, or from cudaHostAlloc")
-    ap.add_argument("--touch-host", action="store_true", help="read the whole host tier once before the pre-roll")
+    ap.add_argument("--no-warm-host", action="store_true",
+                    help="skip the one-time zero-copy read of the host tier before the pre-roll")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-hostlink", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -531,9 +532,12 @@ def run_gpu(args, rank, world, local_rank):
     alloc_s = time.time() - t0
     st.fill_synthetic()
     torch.cuda.synchronize()
-    if args.touch_host:
-        st.touch_host_tier()
     gen_s = time.time() - t0
+    warm_s = None
+    if not args.no_warm_host:
+        t1 = time.time()
+        st.warm_host_tier()
+        warm_s = time.time() - t1
 
     pre = args.preroll
     nsteps = pre + args.warmup + args.steps
@@ -744,6 +748,7 @@ def run_gpu(args, rank, world, local_rank):
         "e2e": e2e,
         "device_error_word": errw,
         "setup_s": round(gen_s, 1), "alloc_s": round(alloc_s, 1),
+        "host_tier_warm_s": None if warm_s is None else round(warm_s, 2),
         "score_kernel": os.environ.get("OASIS_SCORE_KERNEL", "mma"),
     }
     if not args.no_cpu_baseline and world == 1:

@@ -455,6 +455,21 @@ OASIS_API oasis_status oasis_sparse_decode_attn_lookahead(const oasis_shape* sha
                                                           oasis_stream_t stream);
 
 /*
+ * Host-tier warm-up (the pages have no counterpart: a platform utility).
+ * oasis_touch_host: reads every byte of [host_ptr, host_ptr + bytes) once with
+ * the SMs' zero-copy loads and discards the data.  On the GB300 systems this
+ * library was measured on, the first SM reads into some regions of a large
+ * page-locked allocation stall for milliseconds until the region has been read
+ * once (copy-engine transfers do not clear this); calling this after filling the
+ * host tier keeps those stalls out of the gathers.  host_ptr: page-locked,
+ * device-mapped host memory (as host_kv), 16-byte aligned; bytes a multiple of
+ * 16; sink: device uint32 or NULL (written only in a case that does not occur).
+ * Asynchronous on stream; a 100 GiB tier takes about half a second.
+ */
+OASIS_API oasis_status oasis_touch_host(const void* host_ptr, size_t bytes, uint32_t* sink,
+                                        oasis_stream_t stream);
+
+/*
  * f3. Agreement of a predicted top-K set with the exact one (measurement only).
  * Defines: the per-layer agreement between the blocks the draft (lookahead)
  * queries select and the exact top-K blocks of the true next-token query

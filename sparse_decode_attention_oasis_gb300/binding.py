@@ -76,6 +76,7 @@ _SIGS = {
                                 _VP, _VP], ctypes.c_int),
     "oasis_topk_select_diff_pooled": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, ctypes.c_int32, _VP, _VP,
                                        _VP, _VP, _VP], ctypes.c_int),
+    "oasis_touch_host": ([_VP, ctypes.c_size_t, _VP, _VP], ctypes.c_int),
     "oasis_sparse_decode_attn": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                   ctypes.c_float, _VP, ctypes.c_size_t, _VP, _VP], ctypes.c_int),
     "oasis_attn_workspace_bytes": ([ctypes.POINTER(Shape)], ctypes.c_size_t),
@@ -263,6 +264,12 @@ def oasis_topk_select_diff_pooled(shape: Shape, scores, k_pooled, q_la, ctx_len,
     _check("oasis_topk_select_diff_pooled", load().oasis_topk_select_diff_pooled(
         ctypes.byref(shape), _ptr(scores), _ptr(k_pooled), _ptr(q_la), _ptr(ctx_len), _ptr(blk2slot),
         int(fetch_cap), _ptr(sel), _ptr(nsel), _ptr(fetch), _ptr(nfetch), _stream(stream)))
+
+
+def oasis_touch_host(host_tensor, nbytes: Optional[int] = None, sink=None, stream=None):
+    """Read a pinned, mapped host range once through the SMs' load path (host-tier warm-up)."""
+    n = host_tensor.numel() * host_tensor.element_size() if nbytes is None else int(nbytes)
+    _check("oasis_touch_host", load().oasis_touch_host(_ptr(host_tensor), n, _ptr(sink), _stream(stream)))
 
 
 def oasis_sparse_decode_attn(shape: Shape, q, k_pool, v_pool, sel, nsel, blk2slot, ctx_len,

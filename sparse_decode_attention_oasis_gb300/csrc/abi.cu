@@ -41,6 +41,7 @@ cudaError_t launch_attn_lookahead(const Shape&, const uint16_t*, const uint16_t*
 size_t attn_la_workspace_bytes(const Shape&);
 cudaError_t launch_topk_select_diff(const Shape&, const float2*, const uint16_t*, const uint16_t*, const int*,
                                     const int*, int, int*, int*, int*, int*, bool, cudaStream_t);
+cudaError_t launch_touch_host(const void*, size_t, unsigned*, cudaStream_t);
 cudaError_t launch_append_kv(const Shape&, const uint16_t*, const uint16_t*, int*, uint16_t*, uint16_t*, const int*,
                              uint16_t*, uint16_t*, int, unsigned*, cudaStream_t);
 size_t topk_smem_bytes(const Shape&);
@@ -476,6 +477,17 @@ oasis_status oasis_set_agreement(const oasis_shape* shape, const int32_t* pred, 
           "int32 arrays must be 4-byte aligned");
   cudaError_t e = oasis::launch_set_agreement(s, pred, npred, exact, nexact, blk2slot, counts, err_word,
                                               (cudaStream_t)stream);
+  return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
+}
+
+oasis_status oasis_touch_host(const void* host_ptr, size_t bytes, uint32_t* sink, oasis_stream_t stream) {
+  static const char* fn = "oasis_touch_host";
+  REQUIRE(host_ptr && aligned(host_ptr, 16), "host_ptr must be a 16-byte aligned pointer");
+  REQUIRE(bytes % 16 == 0, "bytes must be a multiple of 16");
+  REQUIRE(!sink || aligned(sink, 4), "sink must be NULL or a 4-byte aligned device pointer");
+  void* dev = mapped_host_ptr(host_ptr);
+  REQUIRE(dev, "host_ptr must be page-locked, device-mapped host memory");
+  cudaError_t e = oasis::launch_touch_host(dev, bytes, sink, (cudaStream_t)stream);
   return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
 }
 

@@ -217,13 +217,12 @@ class DecodeState:
             self.pool_layer(lp)
         torch.cuda.synchronize(dev)
 
-    def touch_host_tier(self, chunk_bytes: int = 1 << 30):
-        """Read the whole host tier once through the copy engines (1 GiB at a time)."""
-        flat = self.host.view(-1).view(torch.uint8)
-        buf = torch.empty(min(chunk_bytes, flat.numel()), dtype=torch.uint8, device=self.device)
-        for off in range(0, flat.numel(), buf.numel()):
-            n = min(buf.numel(), flat.numel() - off)
-            buf[:n].copy_(flat[off:off + n], non_blocking=True)
+    def warm_host_tier(self, stream=None):
+        """Read the whole host tier once through the SMs' zero-copy loads
+        (oasis_touch_host), so that later gathers do not meet first-read stalls."""
+        st = stream or torch.cuda.current_stream(self.device)
+        for l in range(self.L_host):
+            B.oasis_touch_host(self.hostl[l], stream=st)
         torch.cuda.synchronize(self.device)
 
     def set_scoring(self, scoring: str):

@@ -77,3 +77,27 @@ def test_workspace_size_formula(lib):
     ws = binding.oasis_attn_workspace_bytes(s)
     assert ws % row == 0 and 1 <= ws // row <= 32 // 4
     assert binding.oasis_attn_workspace_bytes(_shape(d=64)) == 0
+
+
+def test_new_calls_validate_before_launch(lib):
+    s = _shape()
+    # fetch cap beyond Kb, misaligned pointers, NULL outputs: rejected without a launch
+    assert lib.oasis_topk_select_diff(ctypes.byref(s), 16, 16, 16, 16, 16, 33, 16, 16, 16, 16, None) == 1
+    assert lib.oasis_topk_select_diff_pooled(ctypes.byref(s), 16, 18, 16, 16, 16, 2, 16, 16, 16, 16, None) == 1
+    assert lib.oasis_copy_fetched(ctypes.byref(s), 16, 16, 16, 16, 16, 16, None, None) == 1
+    assert lib.oasis_assign_slots(ctypes.byref(s), 16, 16, 16, 16, 16, 16, 16, 18, 16, None) == 1
+    assert lib.oasis_score_blocks_pooled(ctypes.byref(s), 16, 16, 16, 12, None, None, None, None, None, None,
+                                         None, None) == 1
+    assert lib.oasis_sparse_decode_attn_lookahead(ctypes.byref(s), 16, 16, 16, 16, 16, 16, 16, 16, 0.1, 16, 0,
+                                                  16, 16, None) == 1
+    assert lib.oasis_set_agreement(ctypes.byref(s), 16, 16, 16, 16, None, None, None, None) == 1
+    assert lib.oasis_touch_host(None, 16, None, None) == 1
+    assert lib.oasis_touch_host(16, 15, None, None) == 1
+
+
+def test_lookahead_workspace_size_formula(lib):
+    s = _shape()
+    # splits x row tiles of 16 rows of (128 + 2) floats; (1 + n_la) G = 20 rows -> 2 tiles
+    tile = 2 * 8 * 2 * 16 * 130 * 4
+    ws = binding.oasis_attn_lookahead_workspace_bytes(s)
+    assert ws % tile == 0 and 1 <= ws // tile <= 32 // 4

@@ -142,3 +142,16 @@ def test_cross_step_pipeline_matches_oracle():
             np.testing.assert_array_equal(st.slot2blk[l].cpu().numpy(), s2b)
             np.testing.assert_array_equal(st.last_used[l].cpu().numpy(), lu)
             _check_out(out[l].cpu().numpy().astype(np.float64), r["out"], f"layer {l} step {step}")
+
+
+def test_touch_host_reads_a_pinned_range():
+    from sparse_decode_attention_oasis_gb300 import binding as B
+
+    host = torch.arange(1 << 20, dtype=torch.int32).pin_memory()
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.oasis_touch_host(host, sink=sink)
+    B.oasis_touch_host(host, nbytes=4096 + 16)
+    torch.cuda.synchronize()
+    assert int(sink.item()) == 0
+    with pytest.raises(B.OasisError):
+        B.oasis_touch_host(host, nbytes=100)  # not a multiple of 16
