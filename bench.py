@@ -62,8 +62,9 @@ def parse():
     ap.add_argument("--scoring", default="maxdot", choices=["maxdot", "pooled"],
                     help="maxdot: scan of the full keys; pooled: scan of the min/max pooled keys")
     ap.add_argument("--no-pooled", action="store_true", help="skip the pooled-scoring variant")
-    ap.add_argument("--host-alloc", default="thp", choices=["thp", "cuda"],
-                    help="host tier on transparent huge pages registered with CUDA, or from cudaHostAlloc")
+    ap.add_argument("--host-alloc", default="thp", choices=["thp", "cuda", "thp_layers", "cuda_layers"],
+                    help="host tier on transparent huge pages registered with CUDA, or from cudaHostAlloc; "
+                         "*_layers: one allocation per host layer")
     ap.add_argument("--no-warm-host", action="store_true",
                     help="skip the one-time zero-copy read of the host tier before the pre-roll")
     ap.add_argument("--no-e2e", action="store_true")

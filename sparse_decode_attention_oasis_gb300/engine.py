@@ -143,12 +143,21 @@ class DecodeState:
         self.last_used = torch.full((Lp, s.B, s.Hkv, s.P), -1, dtype=torch.int32, device=dev)
         host_shape = (self.L_host, s.B, s.Hkv, s.nb_max, 2, 16, 128)
         self._host_buf = None
+        if host_alloc not in ("thp", "cuda", "thp_layers", "cuda_layers"):
+            raise ValueError(f"unknown host_alloc {host_alloc!r}")
         if pin_host and host_alloc == "thp":
             nbytes = int(np.prod(host_shape)) * 2
             self._host_buf = HugePinnedBuffer(nbytes)
             self.host = self._host_buf.tensor.view(torch.bfloat16).view(host_shape)
-        elif pin_host:  # "cuda": page-locked by the CUDA allocator (cudaHostAlloc), base pages
+        elif pin_host and host_alloc == "cuda":  # page-locked by the CUDA allocator (cudaHostAlloc), base pages
             self.host = torch.empty(host_shape, dtype=torch.bfloat16, pin_memory=True)
+        elif pin_host:  # one allocation (and registration) per layer: "thp_layers" or "cuda_layers"
+            per = host_shape[1:]
+            if host_alloc == "thp_layers":
+                self._host_bufs = [HugePinnedBuffer(int(np.prod(per)) * 2) for _ in range(self.L_host)]
+                self.host = [b_.tensor.view(torch.bfloat16).view(per) for b_ in self._host_bufs]
+            else:
+                self.host = [torch.empty(per, dtype=torch.bfloat16, pin_memory=True) for _ in range(self.L_host)]
         else:
             self.host = torch.zeros(host_shape, dtype=torch.bfloat16)
         self.ctx = torch.tensor(w.ctx, dtype=torch.int32, device=dev)
@@ -206,7 +215,7 @@ class DecodeState:
                 kb = Kr.view(w.Hkv, w.nb_max, 16, 128)
                 vb = Vr.view(w.Hkv, w.nb_max, 16, 128)
                 if layer < self.L_host:
-                    self.host[lh, b].copy_(torch.stack([kb, vb], dim=2))
+                    self.hostl[lh][b].copy_(torch.stack([kb, vb], dim=2))
                 idx = torch.from_numpy(s2b[b]).to(dev).long()
                 occ = (idx >= 0)[..., None, None]
                 self.k_pool[lp, b].copy_(kb[ar, idx.clamp(min=0)] * occ)
@@ -256,7 +265,7 @@ class DecodeState:
                 Kh, Vh = syn.head_kv_torch(w, layer, b, h, self.device)
                 self.K[lp, b, h].copy_(Kh)
                 kv = torch.stack([Kh.view(w.nb_max, 16, 128), Vh.view(w.nb_max, 16, 128)], dim=1)
-                self.host[lh, b, h].copy_(kv, non_blocking=False)
+                self.hostl[lh][b, h].copy_(kv, non_blocking=False)
         b2s, s2b, lu = syn.initial_tables(w, layer)
         self.blk2slot[lp].copy_(torch.from_numpy(b2s))
         self.slot2blk[lp].copy_(torch.from_numpy(s2b))
