@@ -49,9 +49,9 @@ def parse():
     ap.add_argument("--layers", type=int, default=36, help="model layers (36 = Qwen3-8B)")
     ap.add_argument("--batch", type=int, default=32)
     ap.add_argument("--ctx", type=int, default=32768)
-    ap.add_argument("--host-layers", type=int, default=8,
-                    help="distinct host-tier layers (4 GiB each; layer l uses buffer l mod N; 0 = as many as fit). "
-                         "Larger pinned tiers showed rare multi-millisecond stalls of the zero-copy reads")
+    ap.add_argument("--host-layers", type=int, default=0,
+                    help="distinct host-tier layers (layer l uses buffer l mod N; 0 = as many as 60%% of the "
+                         "available host memory holds)")
     ap.add_argument("--preroll", type=int, default=40,
                     help="untimed decode steps run first, so the timed steps see a warmed-up resident set")
     ap.add_argument("--copy", default="gather", choices=["gather", "overlap", "carry", "lag"],
@@ -62,7 +62,7 @@ def parse():
     ap.add_argument("--scoring", default="maxdot", choices=["maxdot", "pooled"],
                     help="maxdot: scan of the full keys; pooled: scan of the min/max pooled keys")
     ap.add_argument("--no-pooled", action="store_true", help="skip the pooled-scoring variant")
-    ap.add_argument("--host-alloc", default="thp", choices=["thp", "cuda", "thp_layers", "cuda_layers"],
+    ap.add_argument("--host-alloc", default="cuda", choices=["cuda", "thp", "thp_layers", "cuda_layers"],
                     help="host tier on transparent huge pages registered with CUDA, or from cudaHostAlloc; "
                          "*_layers: one allocation per host layer")
     ap.add_argument("--no-warm-host", action="store_true",
