@@ -70,15 +70,68 @@ __device__ __forceinline__ int exact_cmp(const uint32_t* a, const uint32_t* b) {
 // forms 4 exact products as (limb, low 32 bits, high bits); the limbs the warp
 // touches are summed one at a time with a 64-bit warp reduction (no atomics),
 // then every lane runs the same carry chain and lane i < 17 stores limb i.
-// With kBox the key element is chosen per dimension by the query's sign: krow
-// (the pooled maxima) where q >= 0, krow_neg (the minima) where q < 0, which makes
-// the sum the pooled score sum_i max(q_i hi_i, q_i lo_i).
+// x * 2^266 of a double x that is a multiple of 2^-266, as kLimbs 32-bit words of a
+// two's complement integer (one thread).
+__device__ void f64_to_limbs(double x, uint32_t* out) {
+  uint32_t w[kLimbs];
+#pragma unroll
+  for (int i = 0; i < kLimbs; ++i) w[i] = 0u;
+  if (x != 0.0) {
+    const unsigned long long bits = (unsigned long long)__double_as_longlong(x);
+    const bool neg = (bits >> 63) != 0;
+    const int bexp = (int)((bits >> 52) & 0x7ffull);
+    unsigned long long m = bits & ((1ull << 52) - 1);
+    int e2;  // |x| = m * 2^e2
+    if (bexp == 0) {
+      e2 = -1074;
+    } else {
+      m |= 1ull << 52;
+      e2 = bexp - 1075;
+    }
+    int sh = e2 + 266;  // |x| * 2^266 = m * 2^sh
+    if (sh < 0) {       // exact: x is a multiple of 2^-266
+      m >>= -sh;
+      sh = 0;
+    }
+    const int li = sh >> 5, bo = sh & 31;
+    const unsigned long long lo64 = m << bo;
+    const unsigned long long hi64 = bo ? (m >> (64 - bo)) : 0ull;
+    if (li < kLimbs) w[li] = (uint32_t)lo64;
+    if (li + 1 < kLimbs) w[li + 1] = (uint32_t)(lo64 >> 32);
+    if (li + 2 < kLimbs) w[li + 2] = (uint32_t)hi64;
+    if (neg) {
+      unsigned long long carry = 1ull;
+#pragma unroll
+      for (int i = 0; i < kLimbs; ++i) {
+        const unsigned long long t = (unsigned long long)(~w[i]) + carry;
+        w[i] = (uint32_t)t;
+        carry = t >> 32;
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kLimbs; ++i) out[i] = w[i];
+}
+
+// Exact q.k (times 2^266) of a 128-long bf16 row pair, by one warp.  Each product
+// is mm * 2^(ee - 266) with mm < 2^16.  Fast path: with Lmin the smallest ee of a
+// nonzero product, every partial sum is a multiple of 2^(Lmin - 266), and if
+// sum |products| < 2^(Lmin - 266 + 52) every partial sum is exactly representable
+// in fp64, so the fp64 tree sum is the exact value (the usual case).  Otherwise
+// each lane forms its products as (limb, low 32 bits, high bits); the limbs the
+// warp touches are summed one at a time with a 64-bit warp reduction (no
+// atomics), then every lane runs the same carry chain and lane i < 17 stores limb
+// i.  With kBox the key element is chosen per dimension by the query's sign:
+// krow (the pooled maxima) where q >= 0, krow_neg (the minima) where q < 0, which
+// makes the sum the pooled score sum_i max(q_i hi_i, q_i lo_i).
 template <bool kBox>
 __device__ void warp_exact_dot(const uint16_t* krow, const uint16_t* qrow, uint32_t* out, int lane,
                                const uint16_t* krow_neg = nullptr) {
   int limb[4];
   long long lo[4], hi[4];
   int lmin = kLimbs, lmax = -1;
+  int emin = 1 << 20;
+  double fv = 0.0, fa = 0.0;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int e = lane + 32 * j;
@@ -95,11 +148,31 @@ __device__ void warp_exact_dot(const uint16_t* krow, const uint16_t* qrow, uint3
       const unsigned long long v = (unsigned long long)mm << (ee & 31);
       lo[j] = (long long)(v & 0xffffffffull);
       hi[j] = (long long)(v >> 32);
-      if ((kb ^ qb) & 0x8000u) { lo[j] = -lo[j]; hi[j] = -hi[j]; }
+      const double p = ldexp((double)mm, ee - 266);  // exact
+      fa += p;
+      if ((kb ^ qb) & 0x8000u) {
+        lo[j] = -lo[j];
+        hi[j] = -hi[j];
+        fv -= p;
+      } else {
+        fv += p;
+      }
+      emin = min(emin, ee);
       limb[j] = ee >> 5;
       lmin = min(lmin, limb[j]);
       lmax = max(lmax, limb[j] + 1);
     }
+  }
+  emin = __reduce_min_sync(0xffffffffu, emin);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    fv += __shfl_xor_sync(0xffffffffu, fv, o);
+    fa += __shfl_xor_sync(0xffffffffu, fa, o);
+  }
+  if (emin == (1 << 20) || fa < ldexp(1.0, emin - 266 + 52)) {
+    if (lane == 0) f64_to_limbs(emin == (1 << 20) ? 0.0 : fv, out);
+    __syncwarp();
+    return;
   }
   lmin = __reduce_min_sync(0xffffffffu, lmin);
   lmax = __reduce_max_sync(0xffffffffu, lmax);

@@ -144,3 +144,40 @@ def test_separate_topk_and_diff_kernels(scoring):
     c.st.fused_select = False
     for step in range(2):
         c.step(step)
+
+
+def _two_block_case(k_rows, q_vals, want):
+    """Keys zero except the given (block, token, dim) -> value entries; one lookahead
+    query per head with the given (dim -> value); Kb = 1: the kept block must be want."""
+    w = syn.Workload("exact", L=1, B=1, Hq=8, Hkv=8, ctx=[64 * 16], Kb=1, C=1, n_hot=0, n_la=1)
+    K = np.zeros((1, 8, w.T_max, w.d), np.float32)
+    for (blk, tok, dim), val in k_rows.items():
+        K[0, :, blk * 16 + tok, dim] = val
+    V = syn.f32_to_bf16_bits(np.random.default_rng(0).standard_normal((1, 8, w.T_max, w.d)).astype(np.float32))
+    qla = np.zeros((1, 1, 8, w.d), np.float32)
+    for dim, val in q_vals.items():
+        qla[..., dim] = val
+    q = np.ones((1, 8, w.d), np.float32)
+    c = Case(w, K=syn.f32_to_bf16_bits(K), V=V)
+    r, sc = c.step(0, q=syn.f32_to_bf16_bits(q), qla=syn.f32_to_bf16_bits(qla))
+    for h in range(8):
+        assert r["S"][(0, h)] == [want]
+
+
+def test_exact_sum_beyond_fp64_resolution_uses_the_limb_path():
+    """Dots 2^60 + 2^-60 (block 9) and 2^60 (block 3): 120 bits apart, so the fp64
+    certificate fails and the 544-bit sum decides; block 9 must win."""
+    _two_block_case({(3, 0, 0): 2.0 ** 30, (9, 5, 0): 2.0 ** 30, (9, 5, 1): 2.0 ** -30},
+                    {0: 2.0 ** 30, 1: 2.0 ** -30}, 9)
+
+
+def test_exact_negative_dots_compare_correctly():
+    """All dots negative: -1 (block 4) beats -1 - 2^-20 (block 11) and -2 (the others);
+    the exact sums are negative, so their limb encoding is two's complement."""
+    rows = {}
+    for blk in range(64):
+        for tok in range(16):  # every token of a block negative, so its max-dot is negative
+            rows[(blk, tok, 0)] = -1.0 if blk in (4, 11) else -2.0
+            if blk == 11:
+                rows[(blk, tok, 1)] = -(2.0 ** -20)
+    _two_block_case(rows, {0: 1.0, 1: 1.0}, 4)
