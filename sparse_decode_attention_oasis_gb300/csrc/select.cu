@@ -70,68 +70,24 @@ __device__ __forceinline__ int exact_cmp(const uint32_t* a, const uint32_t* b) {
 // forms 4 exact products as (limb, low 32 bits, high bits); the limbs the warp
 // touches are summed one at a time with a 64-bit warp reduction (no atomics),
 // then every lane runs the same carry chain and lane i < 17 stores limb i.
-// x * 2^266 of a double x that is a multiple of 2^-266, as kLimbs 32-bit words of a
-// two's complement integer (one thread).
-__device__ void f64_to_limbs(double x, uint32_t* out) {
-  uint32_t w[kLimbs];
-#pragma unroll
-  for (int i = 0; i < kLimbs; ++i) w[i] = 0u;
-  if (x != 0.0) {
-    const unsigned long long bits = (unsigned long long)__double_as_longlong(x);
-    const bool neg = (bits >> 63) != 0;
-    const int bexp = (int)((bits >> 52) & 0x7ffull);
-    unsigned long long m = bits & ((1ull << 52) - 1);
-    int e2;  // |x| = m * 2^e2
-    if (bexp == 0) {
-      e2 = -1074;
-    } else {
-      m |= 1ull << 52;
-      e2 = bexp - 1075;
-    }
-    int sh = e2 + 266;  // |x| * 2^266 = m * 2^sh
-    if (sh < 0) {       // exact: x is a multiple of 2^-266
-      m >>= -sh;
-      sh = 0;
-    }
-    const int li = sh >> 5, bo = sh & 31;
-    const unsigned long long lo64 = m << bo;
-    const unsigned long long hi64 = bo ? (m >> (64 - bo)) : 0ull;
-    if (li < kLimbs) w[li] = (uint32_t)lo64;
-    if (li + 1 < kLimbs) w[li + 1] = (uint32_t)(lo64 >> 32);
-    if (li + 2 < kLimbs) w[li + 2] = (uint32_t)hi64;
-    if (neg) {
-      unsigned long long carry = 1ull;
-#pragma unroll
-      for (int i = 0; i < kLimbs; ++i) {
-        const unsigned long long t = (unsigned long long)(~w[i]) + carry;
-        w[i] = (uint32_t)t;
-        carry = t >> 32;
-      }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < kLimbs; ++i) out[i] = w[i];
-}
-
 // Exact q.k (times 2^266) of a 128-long bf16 row pair, by one warp.  Each product
-// is mm * 2^(ee - 266) with mm < 2^16.  Fast path: with Lmin the smallest ee of a
-// nonzero product, every partial sum is a multiple of 2^(Lmin - 266), and if
-// sum |products| < 2^(Lmin - 266 + 52) every partial sum is exactly representable
-// in fp64, so the fp64 tree sum is the exact value (the usual case).  Otherwise
-// each lane forms its products as (limb, low 32 bits, high bits); the limbs the
-// warp touches are summed one at a time with a 64-bit warp reduction (no
-// atomics), then every lane runs the same carry chain and lane i < 17 stores limb
-// i.  With kBox the key element is chosen per dimension by the query's sign:
-// krow (the pooled maxima) where q >= 0, krow_neg (the minima) where q < 0, which
-// makes the sum the pooled score sum_i max(q_i hi_i, q_i lo_i).
+// is mm * 2^(ee - 266) with mm < 2^16 (signed).  Fast path: when the nonzero
+// products' ee span at most 40, sum_j mm_j 2^(ee_j - emin) over 128 products is
+// below 2^63 and is summed exactly in 64-bit integers (the usual case); lane i
+// then writes limb i of that sum shifted by emin.  Otherwise each lane forms its
+// products as (limb, low 32 bits, high bits); the limbs the warp touches are
+// summed one at a time with a 64-bit warp reduction (no atomics), then every lane
+// runs the same carry chain and lane i < 17 stores limb i.  With kBox the key
+// element is chosen per dimension by the query's sign: krow (the pooled maxima)
+// where q >= 0, krow_neg (the minima) where q < 0, which makes the sum the pooled
+// score sum_i max(q_i hi_i, q_i lo_i).
 template <bool kBox>
 __device__ void warp_exact_dot(const uint16_t* krow, const uint16_t* qrow, uint32_t* out, int lane,
                                const uint16_t* krow_neg = nullptr) {
-  int limb[4];
-  long long lo[4], hi[4];
+  int limb[4], eev[4];
+  long long lo[4], hi[4], mms[4];
   int lmin = kLimbs, lmax = -1;
-  int emin = 1 << 20;
-  double fv = 0.0, fa = 0.0;
+  int emin = 1 << 20, emax = -1;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int e = lane + 32 * j;
@@ -142,35 +98,52 @@ __device__ void warp_exact_dot(const uint16_t* krow, const uint16_t* qrow, uint3
     const uint32_t qm = (qb & 0x7fu) | (qE ? 0x80u : 0u);
     const uint32_t mm = km * qm;
     limb[j] = -2;
+    eev[j] = 0;
+    mms[j] = 0;
     lo[j] = hi[j] = 0;
     if (mm) {
       const int ee = (int)(kE ? kE : 1u) + (int)(qE ? qE : 1u) - 2;  // 0 .. 508
       const unsigned long long v = (unsigned long long)mm << (ee & 31);
       lo[j] = (long long)(v & 0xffffffffull);
       hi[j] = (long long)(v >> 32);
-      const double p = ldexp((double)mm, ee - 266);  // exact
-      fa += p;
+      mms[j] = (long long)mm;
       if ((kb ^ qb) & 0x8000u) {
         lo[j] = -lo[j];
         hi[j] = -hi[j];
-        fv -= p;
-      } else {
-        fv += p;
+        mms[j] = -mms[j];
       }
+      eev[j] = ee;
       emin = min(emin, ee);
+      emax = max(emax, ee);
       limb[j] = ee >> 5;
       lmin = min(lmin, limb[j]);
       lmax = max(lmax, limb[j] + 1);
     }
   }
   emin = __reduce_min_sync(0xffffffffu, emin);
+  emax = __reduce_max_sync(0xffffffffu, emax);
+  if (emax < 0 || emax - emin <= 40) {
+    long long acc = 0;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    fv += __shfl_xor_sync(0xffffffffu, fv, o);
-    fa += __shfl_xor_sync(0xffffffffu, fa, o);
-  }
-  if (emin == (1 << 20) || fa < ldexp(1.0, emin - 266 + 52)) {
-    if (lane == 0) f64_to_limbs(emin == (1 << 20) ? 0.0 : fv, out);
+    for (int j = 0; j < 4; ++j)
+      if (mms[j]) acc += mms[j] * (1LL << (eev[j] - emin));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    // limb i of |acc| * 2^emin, then two's complement if negative: the +1 carries
+    // into limb i exactly when every lower limb of the magnitude is zero
+    const unsigned long long mag = acc < 0 ? (unsigned long long)(-acc) : (unsigned long long)acc;
+    uint32_t w = 0u;
+    if (emax >= 0 && lane < kLimbs) {
+      const int b = 32 * lane - emin;  // bit of mag that lands at bit 0 of limb `lane`
+      if (b >= 0 && b < 64) w = (uint32_t)(mag >> b);
+      else if (b < 0 && b > -32) w = (uint32_t)(mag << (-b));
+    }
+    const unsigned nz = __ballot_sync(0xffffffffu, w != 0u);
+    if (acc < 0) {
+      const uint32_t carry = (nz & ((1u << lane) - 1u)) == 0u ? 1u : 0u;
+      w = ~w + carry;
+    }
+    if (lane < kLimbs) out[lane] = w;
     __syncwarp();
     return;
   }
