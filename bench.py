@@ -649,22 +649,35 @@ def run_gpu(args, rank, world, local_rank):
         out_host = torch.empty((L, w.B, w.Hq, w.d), dtype=torch.float32, pin_memory=True)
         g1 = StepGraph(st, nxt, [qla_in], [q_in], [out_e2e], copy=args.copy)
         nrep = args.steps
+        # one untimed read of every staged input (a serving loop reuses warm pinned buffers)
+        with torch.cuda.stream(g1.stream):
+            for k in range(args.steps):
+                q_in.copy_(q_host[k], non_blocking=True)
+                qla_in.copy_(qla_host[k], non_blocking=True)
+            out_host.copy_(out_e2e, non_blocking=True)
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nrep)]
         t0 = time.perf_counter()
         with torch.cuda.stream(g1.stream):
             for k in range(nrep):
+                ev[k][0].record(g1.stream)
                 q_in.copy_(q_host[k % args.steps], non_blocking=True)
                 qla_in.copy_(qla_host[k % args.steps], non_blocking=True)
+                ev[k][1].record(g1.stream)
                 g1.replay()
+                ev[k][2].record(g1.stream)
                 out_host.copy_(out_e2e, non_blocking=True)
+                ev[k][3].record(g1.stream)
                 g1.stream.synchronize()
         e2e_s = reduce_max(time.perf_counter() - t0, world, dev)
         bi = q_in.numel() * 2 + qla_in.numel() * 2
         bo = out_host.numel() * 4
+        part = [sum(e[i].elapsed_time(e[i + 1]) for e in ev) / nrep for i in range(3)]
         e2e = {"value": aggregate_value(world, L, nrep, 1000.0 * e2e_s), "unit": UNIT, "h2d_bytes_per_step": bi,
-               "d2h_bytes_per_step": bo}
+               "d2h_bytes_per_step": bo, "ms_per_step": 1000.0 * e2e_s / nrep,
+               "device_ms": {"h2d": round(part[0], 3), "step": round(part[1], 3), "d2h": round(part[2], 3)}}
         nxt += nrep
 
     # the pooled-key scoring path (f1) on the same state: a short eager pre-roll under
