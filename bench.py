@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--scoring", default="maxdot", choices=["maxdot", "pooled"],
                     help="maxdot: scan of the full keys; pooled: scan of the min/max pooled keys")
     ap.add_argument("--no-pooled", action="store_true", help="skip the pooled-scoring variant")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the cross-step pipeline and fused look-ahead attention measurements")
     ap.add_argument("--host-alloc", default="cuda", choices=["cuda", "thp", "thp_layers", "cuda_layers"],
                     help="host tier on transparent huge pages registered with CUDA, or from cudaHostAlloc; "
                          "*_layers: one allocation per host layer")
@@ -717,6 +719,54 @@ def run_gpu(args, rank, world, local_rank):
         errw |= int(st.scratch.err.item()) | int(st.scratch2.err.item())
         st.set_scoring("maxdot")
 
+    # the cross-step pipeline (f4): attention over the previous step's selection;
+    # a short eager pre-roll in that order, then the same timed steps as one graph
+    lag = None
+    if not args.no_variants:
+        for k in range(4):
+            s_k = first + k % args.steps
+            st.decode_step(nxt + k, qla_dev[s_k], q_dev[s_k], out_layers=out_dev, main=main, side=main,
+                           copy="lag")
+        nxt += 4
+        lgraph = StepGraph(st, nxt, [qla_dev[s] for s in ts], [q_dev[s] for s in ts],
+                           [out_steps[k % 2] for k in range(args.steps)], copy="lag")
+        nxt += args.steps
+        torch.cuda.synchronize()
+        la_, lb_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(lgraph.stream):
+            la_.record(lgraph.stream)
+            lgraph.replay()
+            lb_.record(lgraph.stream)
+        torch.cuda.synchronize()
+        lms = reduce_max(la_.elapsed_time(lb_), world, dev)
+        del lgraph
+        lag = {"value": aggregate_value(world, L, args.steps, lms), "unit": UNIT, "ms_per_step": lms / args.steps}
+        errw |= int(st.scratch.err.item()) | int(st.scratch2.err.item())
+
+    # fused look-ahead attention (f2): one launch per layer for the true and the n_la
+    # draft queries over the same resident blocks, against the plain attention launch
+    la_attn = None
+    if not args.no_variants:
+        sc = st.scratch
+        out_la = torch.empty((w.B, w.n_la, w.Hq, w.d), dtype=torch.float32, device=dev)
+        times = {"plain": [], "fused": []}
+        for rep in range(4):
+            for kind in ("plain", "fused"):
+                e0_, e1_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0_.record(main)
+                for l in range(L):
+                    if kind == "plain":
+                        st._attend(l, q_dev[first][l], sc, main, out_dev[l])
+                    else:
+                        st.attend_lookahead(l, q_dev[first][l], qla_dev[first][l], sc, out_dev[l], out_la, main)
+                e1_.record(main)
+                torch.cuda.synchronize()
+                if rep:
+                    times[kind].append(e0_.elapsed_time(e1_) * 1000.0 / L)
+        la_attn = {"plain_us_per_layer": round(sum(times["plain"]) / len(times["plain"]), 2),
+                   "fused_us_per_layer": round(sum(times["fused"]) / len(times["fused"]), 2),
+                   "rows_per_kv_head": {"plain": w.G, "fused": (1 + w.n_la) * w.G}}
+
     # prediction agreement per layer (Figure 6 / Figure 4 analogue), one step, untimed
     agreement = measure_agreement(st, qla_dev[first], q_dev[first], q_dev[first - 1])
 
@@ -758,6 +808,8 @@ def run_gpu(args, rank, world, local_rank):
         "hostlink": hostlink,
         "prediction_agreement": agreement,
         "pooled_scoring": pooled,
+        "lag_pipeline": lag,
+        "lookahead_attention": la_attn,
         "clocks": clk,
         "e2e": e2e,
         "device_error_word": errw,
