@@ -8,9 +8,9 @@
 // Split-K flash decode.  Grid (split, request*KV head); a split covers a range
 // of entries of S and its 4 warps take every 4th entry.  A warp first looks up
 // 32 entries at once (sel, then blk2slot: two rounds of loads), keeps the
-// resident ones, and streams their K and V (8 KiB per block) through a 3-stage
-// shared-memory ring with cp.async, so the next two blocks are in flight while
-// the current one is computed.  Rows are stored with their 16-byte chunks XOR-ed by
+// resident ones, and streams their K and V (8 KiB per block) through a 2-stage
+// shared-memory ring with cp.async, so the next block is in flight while the
+// current one is computed.  Rows are stored with their 16-byte chunks XOR-ed by
 // (row mod 8) to spread the fragment reads over the banks.  Per block the warp
 // computes S = Q K^T with the G query heads as the rows of one m16n8k16 tile
 // (rows >= G are zero; the d axis is permuted identically for Q and K), runs the
@@ -27,8 +27,7 @@ namespace oasis {
 
 constexpr int kAttnWarps = 4;
 constexpr int kStageBytes = 2 * kBS * kD * 2;                    // K + V of one block
-constexpr int kAttnStages = 3;                                   // blocks in flight per warp
-constexpr int kAttnSmem = kAttnWarps * kAttnStages * kStageBytes; // 96 KiB: two CTAs per SM
+constexpr int kAttnSmem = kAttnWarps * 2 * kStageBytes;          // 64 KiB
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -65,7 +64,7 @@ attn_partial_kernel(Shape s, const uint16_t* __restrict__ q, const uint16_t* __r
   const int ctx = ctx_len[b];
   const int p_begin = split * per_split;
   const int p_end = min(n, p_begin + per_split);
-  const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(asmem)) + warp * kAttnStages * kStageBytes;
+  const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(asmem)) + warp * 2 * kStageBytes;
 
   // Q fragments (rows g < G); chunk t+4i of the row gives words for k-steps 2i, 2i+1
   uint32_t qa[4][4];
@@ -99,17 +98,16 @@ attn_partial_kernel(Shape s, const uint16_t* __restrict__ q, const uint16_t* __r
         if (sl >= 0 && sl < s.P && ntok > 0) slot = sl;
       }
     }
-    const unsigned found = __ballot_sync(0xffffffffu, slot >= 0);
-    if (!found) continue;
-    const int count = __popc(found);
-    // block k of this round is the k-th set lane of `found`; up to kAttnStages - 1
-    // blocks are in flight ahead of the one being computed
-    auto issue = [&](int k) {
-      const int src_lane = __fns(found, 0, k + 1);
+    unsigned mask = __ballot_sync(0xffffffffu, slot >= 0);
+    if (!mask) continue;
+    int stage = 0;
+    int cur = __ffs(mask) - 1;
+    mask &= mask - 1;
+    auto issue = [&](int st, int src_lane) {
       const int sl = __shfl_sync(0xffffffffu, slot, src_lane);
       const uint16_t* kb = k_pool + (slot_base + sl) * kBS * kD;
       const uint16_t* vb = v_pool + (slot_base + sl) * kBS * kD;
-      const uint32_t dk = ring + (k % kAttnStages) * kStageBytes, dv = dk + kStageBytes / 2;
+      const uint32_t dk = ring + st * kStageBytes, dv = dk + kStageBytes / 2;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int c = lane + 32 * j;  // chunk of the 4 KiB tile
@@ -119,18 +117,19 @@ attn_partial_kernel(Shape s, const uint16_t* __restrict__ q, const uint16_t* __r
       }
       cp_async_commit();
     };
-    int issued = 0;
-    for (; issued < kAttnStages - 1 && issued < count; ++issued) issue(issued);
-    for (int k = 0; k < count; ++k) {
-      if (issued < count) issue(issued++);
-      const int after = issued - k - 1;  // groups committed after block k's
-      if (after >= 2) cp_async_wait<2>();
-      else if (after == 1) cp_async_wait<1>();
-      else cp_async_wait<0>();
+    issue(0, cur);
+    while (true) {
+      const int nxt = mask ? __ffs(mask) - 1 : -1;
+      if (nxt >= 0) {
+        mask &= mask - 1;
+        issue(stage ^ 1, nxt);
+        cp_async_wait<1>();
+      } else {
+        cp_async_wait<0>();
+      }
       __syncwarp();
-      const int cur = __fns(found, 0, k + 1);
       const int nt_cur = __shfl_sync(0xffffffffu, ntok, cur);
-      const uint32_t dk = ring + (k % kAttnStages) * kStageBytes, dv = dk + kStageBytes / 2;
+      const uint32_t dk = ring + stage * kStageBytes, dv = dk + kStageBytes / 2;
       float sc[2][4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
@@ -197,7 +196,10 @@ attn_partial_kernel(Shape s, const uint16_t* __restrict__ q, const uint16_t* __r
         mma_bf16_16816(o[j][0], o[j][1], o[j][2], o[j][3], ph0, 0u, ph1, 0u, b0, b1);
         mma_bf16_16816(o[j][0], o[j][1], o[j][2], o[j][3], pl0, 0u, pl1, 0u, b0, b1);
       }
-      __syncwarp();  // the stage is refilled by a later issue
+      __syncwarp();  // the stage is refilled by the next issue
+      if (nxt < 0) break;
+      cur = nxt;
+      stage ^= 1;
     }
   }
 
@@ -272,7 +274,7 @@ attn_combine_kernel(Shape s, const float* __restrict__ part_o, const float* __re
 // Splits per head: as many as keep the whole grid resident at once (2 CTAs per
 // SM: 208 registers x 128 threads), each split holding at least 4 entries of S.
 // A second wave would double the latency chain; a warp with more blocks keeps
-// its ring busy instead.
+// its 2-stage ring busy instead.
 int attn_nsplit(const Shape& s) {
   const int heads = s.B * s.Hkv;
   const int resident = 2 * sm_count();
