@@ -176,14 +176,17 @@ OASIS_API oasis_status oasis_fetch_diff_capped(const oasis_shape* shape, const f
  * a2 + a3 in one launch: oasis_topk_select followed by oasis_fetch_diff_capped on
  * the selection it wrote, run by the same thread block of each (request, KV head).
  * Arguments are the union of the two calls'; outputs (sel, nsel, fetch, nfetch)
- * are exactly those of the two calls made one after the other.
+ * are exactly those of the two calls made one after the other.  host_kv, if not
+ * NULL (the mapped host tier as for oasis_gather_h2d), makes each fetched block's
+ * 8 KiB be prefetched into L2 as soon as F is known, so a gather right after
+ * finds it there; it changes no output.
  * oasis_topk_select_diff_pooled: the same with the pooled score (f1 below).
  */
 OASIS_API oasis_status oasis_topk_select_diff(const oasis_shape* shape, const float* scores,
                                               const void* k_hbm, const void* q_la,
                                               const int32_t* ctx_len, const int32_t* blk2slot,
                                               int32_t fetch_cap, int32_t* sel, int32_t* nsel,
-                                              int32_t* fetch, int32_t* nfetch,
+                                              int32_t* fetch, int32_t* nfetch, const void* host_kv,
                                               oasis_stream_t stream);
 
 OASIS_API oasis_status oasis_topk_select_diff_pooled(const oasis_shape* shape,
@@ -191,7 +194,8 @@ OASIS_API oasis_status oasis_topk_select_diff_pooled(const oasis_shape* shape,
                                                      const void* q_la, const int32_t* ctx_len,
                                                      const int32_t* blk2slot, int32_t fetch_cap,
                                                      int32_t* sel, int32_t* nsel, int32_t* fetch,
-                                                     int32_t* nfetch, oasis_stream_t stream);
+                                                     int32_t* nfetch, const void* host_kv,
+                                                     oasis_stream_t stream);
 
 /*
  * a4. Host-tier gather into HBM slots, with the head-wise block table update.

@@ -73,9 +73,9 @@ _SIGS = {
     "oasis_sparse_decode_attn_lookahead": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                             ctypes.c_float, _VP, ctypes.c_size_t, _VP, _VP, _VP], ctypes.c_int),
     "oasis_topk_select_diff": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, ctypes.c_int32, _VP, _VP, _VP,
-                                _VP, _VP], ctypes.c_int),
+                                _VP, _VP, _VP], ctypes.c_int),
     "oasis_topk_select_diff_pooled": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, ctypes.c_int32, _VP, _VP,
-                                       _VP, _VP, _VP], ctypes.c_int),
+                                       _VP, _VP, _VP, _VP], ctypes.c_int),
     "oasis_touch_host": ([_VP, ctypes.c_size_t, _VP, _VP], ctypes.c_int),
     "oasis_sparse_decode_attn": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                   ctypes.c_float, _VP, ctypes.c_size_t, _VP, _VP], ctypes.c_int),
@@ -252,18 +252,18 @@ def oasis_sparse_decode_attn_lookahead(shape: Shape, q, q_la, k_pool, v_pool, se
 
 
 def oasis_topk_select_diff(shape: Shape, scores, k_hbm, q_la, ctx_len, blk2slot, fetch_cap: int, sel, nsel,
-                           fetch, nfetch, stream=None):
-    """Top-K and the capped diff in one launch."""
+                           fetch, nfetch, host_kv=None, stream=None):
+    """Top-K and the capped diff in one launch (host_kv: prefetch the fetched blocks into L2)."""
     _check("oasis_topk_select_diff", load().oasis_topk_select_diff(
         ctypes.byref(shape), _ptr(scores), _ptr(k_hbm), _ptr(q_la), _ptr(ctx_len), _ptr(blk2slot), int(fetch_cap),
-        _ptr(sel), _ptr(nsel), _ptr(fetch), _ptr(nfetch), _stream(stream)))
+        _ptr(sel), _ptr(nsel), _ptr(fetch), _ptr(nfetch), _ptr(host_kv), _stream(stream)))
 
 
 def oasis_topk_select_diff_pooled(shape: Shape, scores, k_pooled, q_la, ctx_len, blk2slot, fetch_cap: int, sel,
-                                  nsel, fetch, nfetch, stream=None):
+                                  nsel, fetch, nfetch, host_kv=None, stream=None):
     _check("oasis_topk_select_diff_pooled", load().oasis_topk_select_diff_pooled(
         ctypes.byref(shape), _ptr(scores), _ptr(k_pooled), _ptr(q_la), _ptr(ctx_len), _ptr(blk2slot),
-        int(fetch_cap), _ptr(sel), _ptr(nsel), _ptr(fetch), _ptr(nfetch), _stream(stream)))
+        int(fetch_cap), _ptr(sel), _ptr(nsel), _ptr(fetch), _ptr(nfetch), _ptr(host_kv), _stream(stream)))
 
 
 def oasis_touch_host(host_tensor, nbytes: Optional[int] = None, sink=None, stream=None):

@@ -40,7 +40,7 @@ cudaError_t launch_attn_lookahead(const Shape&, const uint16_t*, const uint16_t*
                                   cudaStream_t);
 size_t attn_la_workspace_bytes(const Shape&);
 cudaError_t launch_topk_select_diff(const Shape&, const float2*, const uint16_t*, const uint16_t*, const int*,
-                                    const int*, int, int*, int*, int*, int*, bool, cudaStream_t);
+                                    const int*, int, int*, int*, int*, int*, bool, const uint16_t*, cudaStream_t);
 cudaError_t launch_touch_host(const void*, size_t, unsigned*, cudaStream_t);
 cudaError_t launch_append_kv(const Shape&, const uint16_t*, const uint16_t*, int*, uint16_t*, uint16_t*, const int*,
                              uint16_t*, uint16_t*, int, unsigned*, cudaStream_t);
@@ -429,7 +429,7 @@ oasis_status oasis_sparse_decode_attn_lookahead(const oasis_shape* shape, const 
 static oasis_status topk_diff_call(const char* fn, const oasis_shape* shape, const float* scores, const void* keys,
                                    const void* q_la, const int32_t* ctx_len, const int32_t* blk2slot,
                                    int32_t fetch_cap, int32_t* sel, int32_t* nsel, int32_t* fetch, int32_t* nfetch,
-                                   bool pooled, oasis_stream_t stream) {
+                                   const void* host_kv, bool pooled, oasis_stream_t stream) {
   oasis::Shape s;
   oasis_status st = check_shape(shape, fn, &s);
   if (st != OASIS_OK) return st;
@@ -441,27 +441,34 @@ static oasis_status topk_diff_call(const char* fn, const oasis_shape* shape, con
   REQUIRE(aligned(sel, 4) && aligned(nsel, 4) && aligned(blk2slot, 4) && aligned(fetch, 4) && aligned(nfetch, 4),
           "int32 arrays must be 4-byte aligned");
   REQUIRE(fetch_cap >= 0 && fetch_cap <= s.Kb, "fetch_cap must be in [0, Kb]");
+  const void* dev_host = nullptr;
+  if (host_kv) {
+    REQUIRE(aligned(host_kv, 16), "host_kv must be 16-byte aligned");
+    dev_host = mapped_host_ptr(host_kv);
+    REQUIRE(dev_host, "host_kv must be page-locked, device-mapped host memory");
+  }
   cudaError_t e = oasis::launch_topk_select_diff(s, reinterpret_cast<const float2*>(scores),
                                                  static_cast<const uint16_t*>(keys),
                                                  static_cast<const uint16_t*>(q_la), ctx_len, blk2slot, fetch_cap,
-                                                 sel, nsel, fetch, nfetch, pooled, (cudaStream_t)stream);
+                                                 sel, nsel, fetch, nfetch, pooled,
+                                                 static_cast<const uint16_t*>(dev_host), (cudaStream_t)stream);
   return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
 }
 
 oasis_status oasis_topk_select_diff(const oasis_shape* shape, const float* scores, const void* k_hbm,
                                     const void* q_la, const int32_t* ctx_len, const int32_t* blk2slot,
                                     int32_t fetch_cap, int32_t* sel, int32_t* nsel, int32_t* fetch,
-                                    int32_t* nfetch, oasis_stream_t stream) {
+                                    int32_t* nfetch, const void* host_kv, oasis_stream_t stream) {
   return topk_diff_call("oasis_topk_select_diff", shape, scores, k_hbm, q_la, ctx_len, blk2slot, fetch_cap, sel,
-                        nsel, fetch, nfetch, false, stream);
+                        nsel, fetch, nfetch, host_kv, false, stream);
 }
 
 oasis_status oasis_topk_select_diff_pooled(const oasis_shape* shape, const float* scores, const void* k_pooled,
                                            const void* q_la, const int32_t* ctx_len, const int32_t* blk2slot,
                                            int32_t fetch_cap, int32_t* sel, int32_t* nsel, int32_t* fetch,
-                                           int32_t* nfetch, oasis_stream_t stream) {
+                                           int32_t* nfetch, const void* host_kv, oasis_stream_t stream) {
   return topk_diff_call("oasis_topk_select_diff_pooled", shape, scores, k_pooled, q_la, ctx_len, blk2slot,
-                        fetch_cap, sel, nsel, fetch, nfetch, true, stream);
+                        fetch_cap, sel, nsel, fetch, nfetch, host_kv, true, stream);
 }
 
 oasis_status oasis_set_agreement(const oasis_shape* shape, const int32_t* pred, const int32_t* npred,

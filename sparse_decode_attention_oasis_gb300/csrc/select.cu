@@ -697,10 +697,12 @@ __device__ SelCtx make_ctx(char* sm, const SelLayout& L, const Shape& s, const u
 // F = the best min(cap, |M|) of the missing blocks M of S (ascending S of ns <= Kb
 // entries, one per thread), written ascending to fetch[head].  se, cls, U, cblk
 // hold at least Kb entries.
+// With host_kv (device address of the mapped host tier) each fetched block's
+// 8 KiB is also prefetched into L2, so the gather that follows reads it there.
 template <bool kPooled>
 __device__ void capped_diff(SelCtx& c, const Shape& s, const float2* scores, const int* S, int ns,
                             const int* blk2slot, int cap, int head, int* fetch, int* nfetch, float2* se,
-                            uint8_t* cls, int* U, int* cblk, int* red) {
+                            uint8_t* cls, int* U, int* cblk, int* red, const uint16_t* host_kv = nullptr) {
   const int* b2s = blk2slot + (long long)head * s.nb_max;
   // missing blocks of S, in S order (ascending); one entry per thread (ns <= Kb <= 256)
   int x = -1, miss = 0;
@@ -722,6 +724,13 @@ __device__ void capped_diff(SelCtx& c, const Shape& s, const float2* scores, con
   const int opos = block_excl_scan(take, red, red + 31);
   const int total = red[31];
   if (take && opos < s.Kb) out[opos] = cblk[threadIdx.x];
+  if (take && host_kv) {
+    const char* unit = reinterpret_cast<const char*>(host_kv + ((long long)head * s.nb_max + cblk[threadIdx.x]) *
+                                                                   (2 * kBS * kD));
+#pragma unroll 4
+    for (int ln = 0; ln < 2 * kBS * kD * 2 / 128; ++ln)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(unit + ln * 128));
+  }
   for (int i = total + threadIdx.x; i < s.Kb; i += blockDim.x) out[i] = -1;
   if (threadIdx.x == 0) nfetch[head] = total < s.Kb ? total : s.Kb;
 }
@@ -734,7 +743,7 @@ __global__ void __launch_bounds__(kSelThreads, 2)
 topk_select_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __restrict__ k_hbm,
                    const uint16_t* __restrict__ q_la, const int* __restrict__ ctx_len,
                    int* __restrict__ sel, int* __restrict__ nsel, const int* __restrict__ blk2slot, int cap,
-                   int* __restrict__ fetch, int* __restrict__ nfetch) {
+                   int* __restrict__ fetch, int* __restrict__ nfetch, const uint16_t* __restrict__ host_kv) {
   extern __shared__ __align__(16) char sm[];
   const SelLayout L = sel_layout(s.nb_max, kDiff, s.Kb);
   const int head = blockIdx.x;
@@ -753,7 +762,7 @@ topk_select_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* _
     if constexpr (kDiff) {
       __syncthreads();  // the selection written above is visible to the whole CTA
       capped_diff<kPooled>(c, s, scores, out, nb, blk2slot, cap, head, fetch, nfetch, se, cls, U,
-                           reinterpret_cast<int*>(sm + L.cblk), red);
+                           reinterpret_cast<int*>(sm + L.cblk), red, host_kv);
     }
     return;
   }
@@ -779,7 +788,7 @@ topk_select_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* _
   if constexpr (kDiff) {
     __syncthreads();  // the selection written above is visible to the whole CTA
     capped_diff<kPooled>(c, s, scores, out, total < s.Kb ? total : s.Kb, blk2slot, cap, head, fetch, nfetch, se,
-                         cls, U, reinterpret_cast<int*>(sm + L.cblk), red);
+                         cls, U, reinterpret_cast<int*>(sm + L.cblk), red, host_kv);
   }
 }
 
@@ -816,21 +825,24 @@ template <bool kPooled, bool kDiff = false>
 static cudaError_t launch_topk(const Shape& s, const float2* scores, const uint16_t* k, const uint16_t* q_la,
                                const int* ctx, int* sel, int* nsel, cudaStream_t stream,
                                const int* blk2slot = nullptr, int cap = 0, int* fetch = nullptr,
-                               int* nfetch = nullptr) {
+                               int* nfetch = nullptr, const uint16_t* host_kv = nullptr) {
   static int attr_cache[kMaxDevicesCached] = {};
   const size_t smem = sel_layout(s.nb_max, kDiff, s.Kb).total;
   cudaError_t e = ensure_dyn_smem((const void*)topk_select_kernel<kPooled, kDiff>, smem, attr_cache);
   if (e != cudaSuccess) return e;
   topk_select_kernel<kPooled, kDiff><<<s.B * s.Hkv, kSelThreads, smem, stream>>>(s, scores, k, q_la, ctx, sel, nsel,
-                                                                                  blk2slot, cap, fetch, nfetch);
+                                                                                  blk2slot, cap, fetch, nfetch,
+                                                                                  host_kv);
   return cudaGetLastError();
 }
 
 cudaError_t launch_topk_select_diff(const Shape& s, const float2* scores, const uint16_t* k, const uint16_t* q_la,
                                     const int* ctx, const int* blk2slot, int cap, int* sel, int* nsel, int* fetch,
-                                    int* nfetch, bool pooled, cudaStream_t stream) {
-  return pooled ? launch_topk<true, true>(s, scores, k, q_la, ctx, sel, nsel, stream, blk2slot, cap, fetch, nfetch)
-                : launch_topk<false, true>(s, scores, k, q_la, ctx, sel, nsel, stream, blk2slot, cap, fetch, nfetch);
+                                    int* nfetch, bool pooled, const uint16_t* host_kv, cudaStream_t stream) {
+  return pooled ? launch_topk<true, true>(s, scores, k, q_la, ctx, sel, nsel, stream, blk2slot, cap, fetch, nfetch,
+                                          host_kv)
+                : launch_topk<false, true>(s, scores, k, q_la, ctx, sel, nsel, stream, blk2slot, cap, fetch, nfetch,
+                                           host_kv);
 }
 
 template <bool kPooled>

@@ -175,6 +175,7 @@ class DecodeState:
         self.lul = [self.last_used[l] for l in range(Lp)]
         self.hostl = [self.host[l] for l in range(self.L_host)]
         self.fused_select = True  # a2 + a3 in one launch (oasis_topk_select_diff) on the decode path
+        self.prefetch_host = True  # ... which also prefetches the fetched blocks' host data into L2
         self._lag_sel = None  # per-layer selections of the cross-step pipeline (copy="lag")
         self._lag_nsel = None
         self._lag_ready = False
@@ -300,7 +301,7 @@ class DecodeState:
         st = stream or torch.cuda.current_stream(self.device)
         step = self._step_tensor(step, st)
         K = self.K[lp]
-        self._score_topk_diff(lp, q_la, sc, st)
+        self._score_topk_diff(lp, q_la, sc, st, layer)
         gs = gather_stream or st
         if gs is not st:
             gs.wait_stream(st)
@@ -340,15 +341,15 @@ class DecodeState:
             self.step_dev.fill_(int(step))
         return self.step_dev
 
-    def _score_topk_diff(self, lp, q_la, sc, st):
-        self._select_lp(lp, q_la, sc, st)
+    def _score_topk_diff(self, lp, q_la, sc, st, layer=None):
+        self._select_lp(lp, q_la, sc, st, host_layer=layer)
 
     def _select(self, layer, q_la, step, sc, st, mark=None, carry=None):
         """a1..a3 of one layer; ``carry=(layer', scratch')`` makes the scoring launch
         also copy the fetched blocks of layer' (whose slots are already assigned)."""
-        self._select_lp(layer % self.L_phys, q_la, sc, st, mark, carry)
+        self._select_lp(layer % self.L_phys, q_la, sc, st, mark, carry, host_layer=layer)
 
-    def _select_lp(self, lp, q_la, sc, st, mark=None, carry=None):
+    def _select_lp(self, lp, q_la, sc, st, mark=None, carry=None, host_layer=None):
         s = self.shape
         pooled = self.scoring == "pooled"
         K = self.Kpl[lp] if pooled else self.Kl[lp]
@@ -371,7 +372,9 @@ class DecodeState:
             mark("topk", st)
         if self.fused_select:
             f = B.oasis_topk_select_diff_pooled if pooled else B.oasis_topk_select_diff
-            f(s, sc.scores, K, q_la, self.ctx, self.b2sl[lp], self.w.C, sc.sel, sc.nsel, sc.fetch, sc.nfetch, st)
+            hl = lp if host_layer is None else host_layer
+            hp = self.hostl[hl % self.L_host] if self.prefetch_host else None
+            f(s, sc.scores, K, q_la, self.ctx, self.b2sl[lp], self.w.C, sc.sel, sc.nsel, sc.fetch, sc.nfetch, hp, st)
         else:
             topk = B.oasis_topk_select_pooled if pooled else B.oasis_topk_select
             diff = B.oasis_fetch_diff_capped_pooled if pooled else B.oasis_fetch_diff_capped

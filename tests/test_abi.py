@@ -82,8 +82,10 @@ def test_workspace_size_formula(lib):
 def test_new_calls_validate_before_launch(lib):
     s = _shape()
     # fetch cap beyond Kb, misaligned pointers, NULL outputs: rejected without a launch
-    assert lib.oasis_topk_select_diff(ctypes.byref(s), 16, 16, 16, 16, 16, 33, 16, 16, 16, 16, None) == 1
-    assert lib.oasis_topk_select_diff_pooled(ctypes.byref(s), 16, 18, 16, 16, 16, 2, 16, 16, 16, 16, None) == 1
+    assert lib.oasis_topk_select_diff(ctypes.byref(s), 16, 16, 16, 16, 16, 33, 16, 16, 16, 16, None, None) == 1
+    assert lib.oasis_topk_select_diff_pooled(ctypes.byref(s), 16, 18, 16, 16, 16, 2, 16, 16, 16, 16, None,
+                                             None) == 1
+    assert lib.oasis_topk_select_diff(ctypes.byref(s), 16, 16, 16, 16, 16, 2, 16, 16, 16, 16, 24, None) == 1
     assert lib.oasis_copy_fetched(ctypes.byref(s), 16, 16, 16, 16, 16, 16, None, None) == 1
     assert lib.oasis_assign_slots(ctypes.byref(s), 16, 16, 16, 16, 16, 16, 16, 18, 16, None) == 1
     assert lib.oasis_score_blocks_pooled(ctypes.byref(s), 16, 16, 16, 12, None, None, None, None, None, None,
