@@ -54,7 +54,7 @@ def parse():
                          "available host memory holds)")
     ap.add_argument("--preroll", type=int, default=40,
                     help="untimed decode steps run first, so the timed steps see a warmed-up resident set")
-    ap.add_argument("--copy", default="gather", choices=["gather", "overlap", "carry", "lag"],
+    ap.add_argument("--copy", default="overlap", choices=["overlap", "gather", "carry", "lag"],
                     help="gather: one gather launch per layer after its selection, one stream; "
                          "overlap: gather of layer l on a side stream beside the attention of layer l-1; "
                          "carry: the host copy of layer l rides in layer l+1's scoring launch; "
