@@ -175,7 +175,9 @@ class DecodeState:
         self.lul = [self.last_used[l] for l in range(Lp)]
         self.hostl = [self.host[l] for l in range(self.L_host)]
         self.fused_select = True  # a2 + a3 in one launch (oasis_topk_select_diff) on the decode path
-        self.prefetch_host = True  # ... which also prefetches the fetched blocks' host data into L2
+        # prefetching the fetched blocks' host data into L2 from that launch moved the
+        # host-link latency into it (top-K + diff +15 us, gather -15 us): off
+        self.prefetch_host = False
         self._lag_sel = None  # per-layer selections of the cross-step pipeline (copy="lag")
         self._lag_nsel = None
         self._lag_ready = False
