@@ -54,11 +54,14 @@ def parse():
                          "available host memory holds)")
     ap.add_argument("--preroll", type=int, default=40,
                     help="untimed decode steps run first, so the timed steps see a warmed-up resident set")
-    ap.add_argument("--copy", default="overlap", choices=["overlap", "gather", "carry", "lag"],
+    ap.add_argument("--copy", default="overlap", choices=["overlap", "pipe", "gather", "carry", "lag"],
                     help="gather: one gather launch per layer after its selection, one stream; "
                          "overlap: gather of layer l on a side stream beside the attention of layer l-1; "
                          "carry: the host copy of layer l rides in layer l+1's scoring launch; "
-                         "lag: cross-step pipeline, attention over the previous step's selection")
+                         "lag: cross-step pipeline, attention over the previous step's selection; "
+                         "pipe: scorers back to back, each layer's selection, gather and attention on a side stream")
+    ap.add_argument("--score-ctas", type=int, default=-1,
+                    help="scorer CTAs per SM (0 = as many as fit; -1 = 2 with --copy pipe, else 0)")
     ap.add_argument("--scoring", default="maxdot", choices=["maxdot", "pooled"],
                     help="maxdot: scan of the full keys; pooled: scan of the min/max pooled keys")
     ap.add_argument("--no-pooled", action="store_true", help="skip the pooled-scoring variant")
@@ -557,6 +560,10 @@ def run_gpu(args, rank, world, local_rank):
     qla_host = qla_dev[first:].cpu().pin_memory()
     torch.cuda.synchronize()
 
+    score_ctas = args.score_ctas if args.score_ctas >= 0 else (2 if args.copy == "pipe" else 0)
+    from sparse_decode_attention_oasis_gb300 import binding as _B
+
+    _B.oasis_set_option(_B.OPT_SCORE_CTAS_PER_SM, score_ctas)
     main = torch.cuda.current_stream(dev)
     side = main  # the overlap mode makes its own side stream; the others run on one stream
     out_dev = torch.empty((L, w.B, w.Hq, w.d), dtype=torch.float32, device=dev)
@@ -568,7 +575,7 @@ def run_gpu(args, rank, world, local_rank):
     for s in range(pre + args.warmup):
         step(s)
     torch.cuda.synchronize()
-    errw = int(st.scratch.err.item()) | int(st.scratch2.err.item())
+    errw = st.error_word()
 
     # the timed steps, captured once as a CUDA graph (inputs already in HBM, the LRU
     # clock advanced by the graph); events around every scoring launch are graph nodes
@@ -597,7 +604,7 @@ def run_gpu(args, rank, world, local_rank):
         torch.distributed.barrier()
     ms = reduce_max(ev0.elapsed_time(ev1), world, dev)
     score_ms = marks.durations()["score"]
-    errw |= int(st.scratch.err.item()) | int(st.scratch2.err.item())
+    errw |= st.error_word()
     del graph
     torch.cuda.synchronize()
     marks.close()
@@ -716,7 +723,7 @@ def run_gpu(args, rank, world, local_rank):
                   "score_kernel": {"kernel": "score_pooled_kernel", "avg_launch_ms": pavg,
                                    "bytes_per_launch": pab["score"], "achieved_gbs": pach,
                                    "frac": pach / measured_peaks()[0]}}
-        errw |= int(st.scratch.err.item()) | int(st.scratch2.err.item())
+        errw |= st.error_word()
         st.set_scoring("maxdot")
 
     # the cross-step pipeline (f4): attention over the previous step's selection;
@@ -741,7 +748,7 @@ def run_gpu(args, rank, world, local_rank):
         lms = reduce_max(la_.elapsed_time(lb_), world, dev)
         del lgraph
         lag = {"value": aggregate_value(world, L, args.steps, lms), "unit": UNIT, "ms_per_step": lms / args.steps}
-        errw |= int(st.scratch.err.item()) | int(st.scratch2.err.item())
+        errw |= st.error_word()
 
     # fused look-ahead attention (f2): one launch per layer for the true and the n_la
     # draft queries over the same resident blocks, against the plain attention launch
@@ -786,7 +793,7 @@ def run_gpu(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(w), "l2": ("inputs larger than L2 (256 MiB of pooled keys per layer)" if args.scoring == "pooled"
                                 else "inputs larger than L2 (2 GiB of keys per layer)"),
-                   "scoring": args.scoring, "copy": args.copy,
+                   "scoring": args.scoring, "copy": args.copy, "score_ctas_per_sm": score_ctas,
                    "host_tier_layers": l_host, "host_tier_aliased": l_host < L,
                    "host_alloc": args.host_alloc,
                    "parallelism": "replicas" if world > 1 else "single GPU"},

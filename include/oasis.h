@@ -474,6 +474,18 @@ OASIS_API oasis_status oasis_touch_host(const void* host_ptr, size_t bytes, uint
                                         oasis_stream_t stream);
 
 /*
+ * Process-wide launch options (the pages have no counterpart: scheduling knobs).
+ * OASIS_OPT_SCORE_CTAS_PER_SM: the mma.sync block scorers (max-dot and pooled,
+ *   with or without a carried copy) size their persistent grid to value CTAs per SM (0 = as many as
+ *   fit, the default).  A caller that runs the selection, gather and attention
+ *   kernels of one layer beside the scorer of the next on another stream leaves
+ *   them room this way.  Read at every launch; results do not depend on it.
+ * Unknown options or values return OASIS_ERR_INVALID.
+ */
+#define OASIS_OPT_SCORE_CTAS_PER_SM 1
+OASIS_API oasis_status oasis_set_option(int32_t option, int32_t value);
+
+/*
  * f3. Agreement of a predicted top-K set with the exact one (measurement only).
  * Defines: the per-layer agreement between the blocks the draft (lookahead)
  * queries select and the exact top-K blocks of the true next-token query

@@ -77,6 +77,7 @@ _SIGS = {
     "oasis_topk_select_diff_pooled": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, ctypes.c_int32, _VP, _VP,
                                        _VP, _VP, _VP, _VP], ctypes.c_int),
     "oasis_touch_host": ([_VP, ctypes.c_size_t, _VP, _VP], ctypes.c_int),
+    "oasis_set_option": ([ctypes.c_int32, ctypes.c_int32], ctypes.c_int),
     "oasis_sparse_decode_attn": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                   ctypes.c_float, _VP, ctypes.c_size_t, _VP, _VP], ctypes.c_int),
     "oasis_attn_workspace_bytes": ([ctypes.POINTER(Shape)], ctypes.c_size_t),
@@ -270,6 +271,14 @@ def oasis_touch_host(host_tensor, nbytes: Optional[int] = None, sink=None, strea
     """Read a pinned, mapped host range once through the SMs' load path (host-tier warm-up)."""
     n = host_tensor.numel() * host_tensor.element_size() if nbytes is None else int(nbytes)
     _check("oasis_touch_host", load().oasis_touch_host(_ptr(host_tensor), n, _ptr(sink), _stream(stream)))
+
+
+OPT_SCORE_CTAS_PER_SM = 1
+
+
+def oasis_set_option(option: int, value: int):
+    """Process-wide launch option (OPT_SCORE_CTAS_PER_SM: scorer CTAs per SM, 0 = as many as fit)."""
+    _check("oasis_set_option", load().oasis_set_option(int(option), int(value)))
 
 
 def oasis_sparse_decode_attn(shape: Shape, q, k_pool, v_pool, sel, nsel, blk2slot, ctx_len,

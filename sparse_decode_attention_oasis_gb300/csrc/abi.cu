@@ -1,4 +1,5 @@
 // C ABI entry points: argument validation, then the kernel launches.
+#include <atomic>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -86,6 +87,8 @@ oasis_status check_shape(const oasis_shape* sh, const char* fn, oasis::Shape* ou
 }  // namespace
 
 namespace oasis {
+static std::atomic<int> g_score_ctas_per_sm{0};
+int score_ctas_per_sm_option() { return g_score_ctas_per_sm.load(std::memory_order_relaxed); }
 // Record the message oasis_last_error() returns on this thread.
 void set_last_error(const std::string& msg) { g_last_error = msg; }
 }  // namespace oasis
@@ -469,6 +472,16 @@ oasis_status oasis_topk_select_diff_pooled(const oasis_shape* shape, const float
                                            int32_t* nfetch, const void* host_kv, oasis_stream_t stream) {
   return topk_diff_call("oasis_topk_select_diff_pooled", shape, scores, k_pooled, q_la, ctx_len, blk2slot,
                         fetch_cap, sel, nsel, fetch, nfetch, host_kv, true, stream);
+}
+
+oasis_status oasis_set_option(int32_t option, int32_t value) {
+  static const char* fn = "oasis_set_option";
+  if (option == OASIS_OPT_SCORE_CTAS_PER_SM) {
+    REQUIRE(value >= 0 && value <= 64, "OASIS_OPT_SCORE_CTAS_PER_SM takes 0 (the kernel's choice) to 64");
+    oasis::g_score_ctas_per_sm.store(value, std::memory_order_relaxed);
+    return OASIS_OK;
+  }
+  return fail(OASIS_ERR_INVALID, fn, "unknown option");
 }
 
 oasis_status oasis_set_agreement(const oasis_shape* shape, const int32_t* pred, const int32_t* npred,

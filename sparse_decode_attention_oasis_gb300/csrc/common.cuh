@@ -89,6 +89,9 @@ __device__ __forceinline__ float key_float(uint32_t k) {
   return __uint_as_float(u);
 }
 
+// Process-wide launch option set by oasis_set_option (0 = the kernel's own choice).
+int score_ctas_per_sm_option();
+
 // Host-side caches so that a launch costs no more than the launch itself.
 constexpr int kMaxDevicesCached = 64;
 

@@ -237,7 +237,9 @@ int score_grid_limit(int nt) {
     }
     per_sm = v < 1 ? 1 : v;
   }
-  return sm_count() * per_sm;
+  // a caller that runs other kernels beside the scorer can ask for fewer CTAs per SM
+  const int cap = score_ctas_per_sm_option();
+  return sm_count() * (cap > 0 && cap < per_sm ? cap : per_sm);
 }
 
 }  // namespace oasis

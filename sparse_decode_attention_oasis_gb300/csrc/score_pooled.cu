@@ -193,7 +193,8 @@ static int pooled_grid_limit() {
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, score_pooled_kernel<NT, false>, kPsWarps * 32, 0);
     per_sm = v < 1 ? 1 : v;
   }
-  return sm_count() * per_sm;
+  const int cap = score_ctas_per_sm_option();
+  return sm_count() * (cap > 0 && cap < per_sm ? cap : per_sm);
 }
 
 template <int NT>

@@ -352,6 +352,10 @@ class DecodeState:
         self._select_lp(layer % self.L_phys, q_la, sc, st, mark, carry, host_layer=layer)
 
     def _select_lp(self, lp, q_la, sc, st, mark=None, carry=None, host_layer=None):
+        self._score_lp(lp, q_la, sc, st, mark, carry)
+        self._topk_diff_lp(lp, q_la, sc, st, mark, host_layer)
+
+    def _score_lp(self, lp, q_la, sc, st, mark=None, carry=None):
         s = self.shape
         pooled = self.scoring == "pooled"
         K = self.Kpl[lp] if pooled else self.Kl[lp]
@@ -370,6 +374,11 @@ class DecodeState:
                 B.oasis_score_blocks_pooled(s, K, self.ctx, q_la, sc.scores, *args)
             else:
                 B.oasis_score_blocks_copy(s, K, self.ctx, q_la, sc.scores, *args)
+
+    def _topk_diff_lp(self, lp, q_la, sc, st, mark=None, host_layer=None):
+        s = self.shape
+        pooled = self.scoring == "pooled"
+        K = self.Kpl[lp] if pooled else self.Kl[lp]
         if mark:
             mark("topk", st)
         if self.fused_select:
@@ -447,6 +456,9 @@ class DecodeState:
           The table half of layer l's gather runs right after its selection; the
           host-link copy of layer l rides in layer l+1's scoring launch, whose
           HBM-bound work hides the link latency; attn(l) follows that launch.
+        copy="pipe": the scorers of all layers back to back on ``main``; layer l's
+          top-K + diff, gather and attention on a side stream once its scores
+          exist, running beside the following scorers (a ring of 4 scratch sets).
         copy="lag": the cross-step pipeline (f4): attn(l) over the selection the
           previous step made for layer l, then select(l) and gather(l) for the next
           step; one stream.
@@ -478,6 +490,40 @@ class DecodeState:
             if count is not None:
                 count.add_(self.attended_blocks(l, scr[l % 2]))
 
+        if copy == "pipe":
+            # scorers back to back on `main`; each layer's selection, gather and
+            # attention on a side stream as soon as its scores exist, beside the
+            # next scorers (which should leave SM room: OPT_SCORE_CTAS_PER_SM).
+            # A ring of scratch sets; scorer l waits until layer l - R is done.
+            side = side if (side is not None and side is not main) else self._side_stream()
+            R = 4
+            ring = self._pipe_ring(R)
+            ev_score = [torch.cuda.Event() for _ in range(L)]
+            ev_done = [torch.cuda.Event() for _ in range(L)]
+            for l in range(L):
+                sc = ring[l % R]
+                lp = l % self.L_phys
+                if l >= R:
+                    main.wait_event(ev_done[l - R])
+                self._score_lp(lp, q_la_layers[l], sc, main, mark)
+                ev_score[l].record(main)
+                side.wait_event(ev_score[l])
+                self._topk_diff_lp(lp, q_la_layers[l], sc, side, mark, host_layer=l)
+                if mark:
+                    mark("gather", side)
+                self._gather(l, step, sc, side)
+                if mark:
+                    mark("gather_end", side)
+                if mark:
+                    mark("attn", side)
+                self._attend(l, q_layers[l], sc, side, None if out_layers is None else out_layers[l])
+                if mark:
+                    mark("attn_end", side)
+                if count is not None:
+                    count.add_(self.attended_blocks(l, sc))
+                ev_done[l].record(side)
+            main.wait_stream(side)
+            return
         if copy == "lag":
             # f4: attn(l) over the blocks the previous step's lookahead selected (held
             # in per-layer buffers), then this step's selection and gather of layer l,
@@ -579,6 +625,20 @@ class DecodeState:
             if side is not main:
                 main.wait_event(events[l % 2])
             attend(l)
+
+    def error_word(self) -> int:
+        """OR of the device error words of every scratch set (synchronizes)."""
+        sets = [self.scratch] + ([self.scratch2] if self.scratch2 is not None else []) + list(
+            getattr(self, "_ring", None) or [])
+        v = 0
+        for sc in sets:
+            v |= int(sc.err.item())
+        return v
+
+    def _pipe_ring(self, R: int):
+        if getattr(self, "_ring", None) is None or len(self._ring) < R:
+            self._ring = [self.scratch, self.scratch2] + [LayerScratch(self.shape, self.device) for _ in range(R - 2)]
+        return self._ring[:R]
 
     def _side_stream(self):
         if getattr(self, "_side", None) is None:

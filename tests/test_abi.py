@@ -103,3 +103,9 @@ def test_lookahead_workspace_size_formula(lib):
     tile = 2 * 8 * 2 * 16 * 130 * 4
     ws = binding.oasis_attn_lookahead_workspace_bytes(s)
     assert ws % tile == 0 and 1 <= ws // tile <= 32 // 4
+
+
+def test_set_option_validates(lib):
+    assert lib.oasis_set_option(1, -1) == 1
+    assert lib.oasis_set_option(99, 0) == 1
+    assert lib.oasis_set_option(1, 0) == 0

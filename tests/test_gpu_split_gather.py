@@ -67,7 +67,7 @@ def _multi_layer(copy, L=3, steps=3):
         st.decode_step(step, [_dev_bits(qla) for _, qla in qs], [_dev_bits(q) for q, _ in qs],
                        out_layers=out, copy=copy)
         torch.cuda.synchronize()
-        assert int(st.scratch.err.item()) == 0 and int(st.scratch2.err.item()) == 0
+        assert st.error_word() == 0
         for l in range(L):
             K, host, b2s, s2b, lu, kp, vp = layers[l]
             q, qla = qs[l]
@@ -83,9 +83,19 @@ def _multi_layer(copy, L=3, steps=3):
             _check_out(out[l].cpu().numpy().astype(np.float64), r["out"], f"layer {l} step {step}")
 
 
-@pytest.mark.parametrize("copy", ["carry", "gather"])
-def test_multi_layer_decode_step_both_orders(copy):
-    _multi_layer(copy)
+@pytest.mark.parametrize("copy", ["carry", "gather", "overlap", "pipe"])
+def test_multi_layer_decode_step_all_orders(copy):
+    _multi_layer(copy, L=6 if copy == "pipe" else 3)
+
+
+def test_pipe_order_with_fewer_scorer_ctas():
+    from sparse_decode_attention_oasis_gb300 import binding as B
+
+    B.oasis_set_option(B.OPT_SCORE_CTAS_PER_SM, 1)
+    try:
+        _multi_layer("pipe", L=5, steps=2)
+    finally:
+        B.oasis_set_option(B.OPT_SCORE_CTAS_PER_SM, 0)
 
 
 def test_copy_reports_out_of_range_fetch_entry():
