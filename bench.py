@@ -13,6 +13,16 @@ One step = one decode step = all 36 layers x (score, top-K, capped diff, host
 gather, sparse attention) over the whole batch.  Metric: layer-steps/s (plus the
 achieved HBM GB/s of the path and of the dominant kernel, block scoring).
 
+Defaults: max-dot scoring; the `overlap` launch order (each layer's gather on a
+side stream beside the previous layer's attention); the host tier in one
+cudaHostAlloc allocation holding as many layers of distinct data as 60% of the
+available host memory allows (layer l reads buffer l mod N), read once through
+the SMs before the pre-roll.  The timed steps are one captured CUDA graph.  The
+JSON line also reports the pooled-key scoring and cross-step pipeline variants,
+the fused look-ahead attention, the host-link roofline of the gather, per-layer
+prediction agreement, an end-to-end run with host copies, clocks and the CPU
+oracle baseline.
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
 Under torchrun every rank runs its own replica on its own GPU (independent
