@@ -121,16 +121,6 @@ score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restr
         ra[i] = r0 < blk1 ? ldg_stream(base + (long long)r0 * kPK + (t + 4 * i) * 8) : make_uint4(0u, 0u, 0u, 0u);
         rb[i] = r1 < blk1 ? ldg_stream(base + (long long)r1 * kPK + (t + 4 * i) * 8) : make_uint4(0u, 0u, 0u, 0u);
       }
-      {  // ask L2 for this warp's next tile (16 rows x 512 B, two 128-byte lines per lane)
-        const int nxt = tile + kPsWarps * 16;
-        if (nxt < blk1) {
-          const char* p = reinterpret_cast<const char*>(base + (long long)nxt * kPK);
-          const long long lim = (long long)(blk1 - nxt) * kPK * 2;  // bytes of the next tile in range
-          const int o0 = lane * 128, o1 = (lane + 32) * 128;
-          if (o0 < lim) asm volatile("prefetch.global.L2 [%0];" ::"l"(p + o0));
-          if (o1 < lim) asm volatile("prefetch.global.L2 [%0];" ::"l"(p + o1));
-        }
-      }
       float acc[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
