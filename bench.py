@@ -659,6 +659,9 @@ def run_gpu(args, rank, world, local_rank):
     nxt += 2
     attended_per_head = float(attended.item()) / (2 * L * w.B * w.Hkv)
 
+    # prediction agreement per layer (Figure 6 / Figure 4 analogue), one step, untimed
+    agreement = measure_agreement(st, qla_dev[first], q_dev[first], q_dev[first - 1])
+
     # end to end: every step copies its queries from pinned host memory into the
     # graph's input buffers, replays the one-step graph and copies the outputs back
     e2e = None
@@ -784,9 +787,6 @@ def run_gpu(args, rank, world, local_rank):
         la_attn = {"plain_us_per_layer": round(sum(times["plain"]) / len(times["plain"]), 2),
                    "fused_us_per_layer": round(sum(times["fused"]) / len(times["fused"]), 2),
                    "rows_per_kv_head": {"plain": w.G, "fused": (1 + w.n_la) * w.G}}
-
-    # prediction agreement per layer (Figure 6 / Figure 4 analogue), one step, untimed
-    agreement = measure_agreement(st, qla_dev[first], q_dev[first], q_dev[first - 1])
 
     hostlink = measure_hostlink(st, qla_dev[first], dev) if not args.no_hostlink else None
 
