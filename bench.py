@@ -75,6 +75,13 @@ def parse():
                     help="scorer CTAs per SM (0 = as many as fit; -1 = 2 with --copy pipe, else 0)")
     ap.add_argument("--scoring", default="maxdot", choices=["maxdot", "pooled"],
                     help="maxdot: scan of the full keys; pooled: scan of the min/max pooled keys")
+    ap.add_argument("--workload", default="qwen3_8b_decode",
+                    choices=["qwen3_8b_decode", "tiny", "llama31_8b_long", "qwen3_32b", "long_output"],
+                    help="the timed configuration (--layers/--batch/--ctx apply to qwen3_8b_decode)")
+    ap.add_argument("--ratio", default="0.01", help="fetch ratio of qwen3_32b: a number or 'all'")
+    ap.add_argument("--phys-layers", type=int, default=0,
+                    help="layers of distinct keys and pools in HBM (layer l uses l mod N; 0 = all, or 12 for "
+                         "long_output, whose 36 layers of keys do not fit)")
     ap.add_argument("--no-pooled", action="store_true", help="skip the pooled-scoring variant")
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the cross-step pipeline and fused look-ahead attention measurements")
@@ -94,11 +101,28 @@ def parse():
 def workload(args):
     from sparse_decode_attention_oasis_gb300 import synthetic as syn
 
+    if args.workload == "tiny":
+        return syn.tiny()
+    if args.workload == "llama31_8b_long":
+        return syn.llama31_8b_long()
+    if args.workload == "qwen3_32b":
+        return syn.qwen3_32b(ratio=None if args.ratio == "all" else float(args.ratio))
+    if args.workload == "long_output":
+        return syn.long_output()
     return syn.qwen3_8b_decode(B=args.batch, L=args.layers, ctx=args.ctx)
 
 
+def l2_note(w, scoring) -> str:
+    per_block = 2 * w.d * 2 if scoring == "pooled" else w.bs * w.d * 2
+    nbytes = sum(w.nb(b) for b in range(w.B)) * w.Hkv * per_block
+    what = "pooled keys" if scoring == "pooled" else "keys"
+    rel = "larger than" if nbytes > 129 * 2 ** 20 else "smaller than (the workload is launch-bound)"
+    return f"inputs {rel} L2 ({nbytes / 2 ** 30:.2f} GiB of {what} per layer)"
+
+
 def workload_desc(w) -> str:
-    return (f"{w.name}: {w.L} layers, batch {w.B}, {w.Hq}/{w.Hkv} heads, d {w.d}, bf16, ctx {w.ctx[0]}, "
+    ctx = f"{w.ctx[0]}" if min(w.ctx) == max(w.ctx) else f"{min(w.ctx)}-{max(w.ctx)} (+1 token per step)"
+    return (f"{w.name}: {w.L} layers, batch {w.B}, {w.Hq}/{w.Hkv} heads, d {w.d}, bf16, ctx {ctx}, "
             f"block {w.bs}, budget {w.Kb * w.bs} tokens ({w.Kb} blocks), {w.n_la} lookahead queries, "
             f"fetch cap {w.C} blocks/head/step, {w.n_hot} planted hot blocks/head")
 
@@ -488,8 +512,6 @@ def run_reference(args, rank):
 def host_layers_for(w, requested: int) -> int:
     """Layers of distinct host-tier data (layer l reads buffer l mod this).  A
     request of 0 takes as many as 60% of the available host memory holds."""
-    if requested:
-        return min(requested, w.L)
     per_layer = w.B * w.Hkv * w.nb_max * 2 * w.bs * w.d * 2
     avail = None
     try:
@@ -498,10 +520,8 @@ def host_layers_for(w, requested: int) -> int:
                 avail = int(line.split()[1]) * 1024
     except OSError:
         pass
-    if avail is None:
-        return w.L
-    fit = int(0.6 * avail // per_layer)
-    return max(2, min(w.L, fit))
+    fit = w.L if avail is None else max(1, int(0.6 * avail // per_layer))
+    return max(1, min(w.L, fit, requested or w.L))
 
 
 def launches_per_step(st, copy):
@@ -534,11 +554,12 @@ def run_gpu(args, rank, world, local_rank):
         torch.distributed.barrier()
     w = workload(args)
     L = w.L
-    l_host = host_layers_for(w, args.host_layers)
+    l_phys = args.phys_layers or (min(12, L) if args.workload == "long_output" else L)
+    l_host = min(host_layers_for(w, args.host_layers), l_phys)
     t0 = time.time()
     while True:
         try:
-            st = DecodeState(w, device=dev, l_phys=L, l_host=l_host, scoring=args.scoring,
+            st = DecodeState(w, device=dev, l_phys=l_phys, l_host=l_host, scoring=args.scoring,
                              host_alloc=args.host_alloc)
             break
         except RuntimeError:
@@ -567,6 +588,27 @@ def run_gpu(args, rank, world, local_rank):
             q_dev[s, l].copy_(qb)
             qla_dev[s, l].copy_(qlab)
     first = pre + args.warmup
+    # the growing context of long-output decode: one new token per request and layer per step
+    appends = None
+    if args.workload == "long_output":
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(7)
+        n_app = 16
+        k_app = torch.randn((n_app, L, w.B, w.Hkv, w.d), generator=gen, device=dev).to(torch.bfloat16)
+        v_app = torch.randn((n_app, L, w.B, w.Hkv, w.d), generator=gen, device=dev).to(torch.bfloat16)
+        appends = [(k_app[i], v_app[i]) for i in range(n_app)]
+
+    def app(s_):
+        return None if appends is None else appends[s_ % len(appends)]
+
+    def app_list(steps_):
+        return None if appends is None else [app(s_) for s_ in steps_]
+
+    def eager_step(s_, qla, q, **kw):
+        if appends is not None:
+            st.append_step(*app(s_), stream=main)
+        st.decode_step(s_, qla, q, **kw)
+
     q_host = q_dev[first:].cpu().pin_memory()      # inputs of the timed steps, for the end-to-end pass
     qla_host = qla_dev[first:].cpu().pin_memory()
     torch.cuda.synchronize()
@@ -580,7 +622,7 @@ def run_gpu(args, rank, world, local_rank):
     out_dev = torch.empty((L, w.B, w.Hq, w.d), dtype=torch.float32, device=dev)
 
     def step(s, mark=None, qla=None, q=None):
-        st.decode_step(s, qla if qla is not None else qla_dev[s], q if q is not None else q_dev[s],
+        eager_step(s, qla if qla is not None else qla_dev[s], q if q is not None else q_dev[s],
                        out_layers=out_dev, main=main, side=side, mark=mark, copy=args.copy)
 
     for s in range(pre + args.warmup):
@@ -596,7 +638,8 @@ def run_gpu(args, rank, world, local_rank):
     out_steps = [torch.empty((L, w.B, w.Hq, w.d), dtype=torch.float32, device=dev) for _ in range(2)]
     ts = range(first, first + args.steps)
     graph = StepGraph(st, first, [qla_dev[s] for s in ts], [q_dev[s] for s in ts],
-                      [out_steps[k % 2] for k in range(args.steps)], mark=marks, copy=args.copy)
+                      [out_steps[k % 2] for k in range(args.steps)], mark=marks, copy=args.copy,
+                      appends=app_list(ts))
     gstream = graph.stream
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local_rank)
@@ -626,7 +669,7 @@ def run_gpu(args, rank, world, local_rank):
     e_a.record(main)
     for k in range(3):
         s_k = first + k % args.steps
-        st.decode_step(nxt + k, qla_dev[s_k], q_dev[s_k], out_layers=out_dev, main=main, side=main,
+        eager_step(nxt + k, qla_dev[s_k], q_dev[s_k], out_layers=out_dev, main=main, side=main,
                        copy=args.copy)
     e_b.record(main)
     torch.cuda.synchronize()
@@ -637,7 +680,8 @@ def run_gpu(args, rank, world, local_rank):
     # every kernel (no host in the loop), replayed 3 times
     iso = GraphEvents(L * 10 + 16)
     iso.names = {"score", "topk", "diff", "end", "assign", "copy", "gather", "gather_end", "attn", "attn_end"}
-    g_iso = StepGraph(st, nxt, [qla_dev[first]], [q_dev[first]], [out_dev], mark=iso, copy=args.copy)
+    g_iso = StepGraph(st, nxt, [qla_dev[first]], [q_dev[first]], [out_dev], mark=iso, copy=args.copy,
+                      appends=app_list([nxt]))
     kernel_ms = {k: [] for k in ("score", "topk", "diff", "assign", "copy", "gather", "attn")}
     for k in range(3):
         with torch.cuda.stream(g_iso.stream):
@@ -651,13 +695,15 @@ def run_gpu(args, rank, world, local_rank):
     iso.close()
     # attended blocks (selected and resident) per head, counted on eager steps
     attended = torch.zeros((), dtype=torch.int64, device=dev)
+    fetched = torch.zeros((), dtype=torch.int64, device=dev)
     for k in range(2):
         s_k = first + k % args.steps
-        st.decode_step(nxt + k, qla_dev[s_k], q_dev[s_k], out_layers=out_dev, main=main, side=main,
-                       count=attended, copy=args.copy)
+        eager_step(nxt + k, qla_dev[s_k], q_dev[s_k], out_layers=out_dev, main=main, side=main,
+                   count=attended, fetched=fetched, copy=args.copy)
     torch.cuda.synchronize()
     nxt += 2
     attended_per_head = float(attended.item()) / (2 * L * w.B * w.Hkv)
+    fetched_bytes_per_step = float(fetched.item()) / 2 * 2 * w.bs * w.d * 2
 
     # prediction agreement per layer (Figure 6 / Figure 4 analogue), one step, untimed
     agreement = measure_agreement(st, qla_dev[first], q_dev[first], q_dev[first - 1])
@@ -670,7 +716,7 @@ def run_gpu(args, rank, world, local_rank):
         qla_in = torch.empty_like(qla_dev[0])
         out_e2e = torch.empty((L, w.B, w.Hq, w.d), dtype=torch.float32, device=dev)
         out_host = torch.empty((L, w.B, w.Hq, w.d), dtype=torch.float32, pin_memory=True)
-        g1 = StepGraph(st, nxt, [qla_in], [q_in], [out_e2e], copy=args.copy)
+        g1 = StepGraph(st, nxt, [qla_in], [q_in], [out_e2e], copy=args.copy, appends=app_list([nxt]))
         nrep = args.steps
         # one untimed read of every staged input (a serving loop reuses warm pinned buffers)
         with torch.cuda.stream(g1.stream):
@@ -710,12 +756,13 @@ def run_gpu(args, rank, world, local_rank):
         st.set_scoring("pooled")
         for k in range(8):
             s_k = first + k % args.steps
-            st.decode_step(nxt + k, qla_dev[s_k], q_dev[s_k], out_layers=out_dev, main=main, side=main,
+            eager_step(nxt + k, qla_dev[s_k], q_dev[s_k], out_layers=out_dev, main=main, side=main,
                            copy=args.copy)
         nxt += 8
         pmarks = GraphEvents(L * args.steps * 2 + 16)
         pgraph = StepGraph(st, nxt, [qla_dev[s] for s in ts], [q_dev[s] for s in ts],
-                           [out_steps[k % 2] for k in range(args.steps)], mark=pmarks, copy=args.copy)
+                           [out_steps[k % 2] for k in range(args.steps)], mark=pmarks, copy=args.copy,
+                           appends=app_list(ts))
         nxt += args.steps
         torch.cuda.synchronize()
         pa, pb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -746,11 +793,11 @@ def run_gpu(args, rank, world, local_rank):
     if not args.no_variants:
         for k in range(4):
             s_k = first + k % args.steps
-            st.decode_step(nxt + k, qla_dev[s_k], q_dev[s_k], out_layers=out_dev, main=main, side=main,
+            eager_step(nxt + k, qla_dev[s_k], q_dev[s_k], out_layers=out_dev, main=main, side=main,
                            copy="lag")
         nxt += 4
         lgraph = StepGraph(st, nxt, [qla_dev[s] for s in ts], [q_dev[s] for s in ts],
-                           [out_steps[k % 2] for k in range(args.steps)], copy="lag")
+                           [out_steps[k % 2] for k in range(args.steps)], copy="lag", appends=app_list(ts))
         nxt += args.steps
         torch.cuda.synchronize()
         la_, lb_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -802,10 +849,10 @@ def run_gpu(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_desc(w), "l2": ("inputs larger than L2 (256 MiB of pooled keys per layer)" if args.scoring == "pooled"
-                                else "inputs larger than L2 (2 GiB of keys per layer)"),
+        "config": {"workload": workload_desc(w), "l2": l2_note(w, args.scoring),
                    "scoring": args.scoring, "copy": args.copy, "score_ctas_per_sm": score_ctas,
                    "host_tier_layers": l_host, "host_tier_aliased": l_host < L,
+                   "hbm_layers": l_phys, "hbm_layers_aliased": l_phys < L,
                    "host_alloc": args.host_alloc,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "path_hbm_gbs": path_gbs, "path_hbm_frac": path_gbs / peak,
@@ -819,6 +866,7 @@ def run_gpu(args, rank, world, local_rank):
         "kernel_p50_us": {k: round(1000.0 * statistics.median(v), 2) for k, v in kernel_ms.items() if v},
         "kernel_max_us": {k: round(1000.0 * max(v), 2) for k, v in kernel_ms.items() if v},
         "attended_blocks_per_head": round(attended_per_head, 2),
+        "fetched_bytes_per_step": int(fetched_bytes_per_step),
         "timed_steps": [pre + args.warmup, pre + args.warmup + args.steps - 1],
         "ms_per_step_eager_python": eager_ms,
         "gpu_launches": launches_per_step(st, args.copy) * args.steps,

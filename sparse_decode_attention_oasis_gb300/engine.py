@@ -436,6 +436,12 @@ class DecodeState:
                                              self.ctx, self.scale, self._la_ws, nbytes, out, out_la,
                                              stream or torch.cuda.current_stream(self.device))
 
+    def _tally(self, layer, sc, count, fetched):
+        if count is not None:
+            count.add_(self.attended_blocks(layer, sc))
+        if fetched is not None:
+            fetched.add_(sc.nfetch.sum())
+
     def attended_blocks(self, layer: int, sc: "LayerScratch") -> torch.Tensor:
         """Device count of attended blocks (selected and resident) of one layer, all heads."""
         lp = layer % self.L_phys
@@ -445,7 +451,7 @@ class DecodeState:
         return ((slot >= 0) & valid).sum()
 
     def decode_step(self, step, q_la_layers, q_layers, out_layers=None, main=None, side=None,
-                    mark=None, count=None, copy: str = "carry"):
+                    mark=None, count=None, copy: str = "carry", fetched=None):
         """All layers of one decode step, pipelined across layers.
 
         copy="carry" (default), all on the main stream:
@@ -487,8 +493,8 @@ class DecodeState:
             self._attend(l, q_layers[l], scr[l % 2], main, None if out_layers is None else out_layers[l])
             if mark:
                 mark("attn_end", main)
-            if count is not None:
-                count.add_(self.attended_blocks(l, scr[l % 2]))
+            if count is not None or fetched is not None:
+                self._tally(l, scr[l % 2], count, fetched)
 
         if copy == "pipe":
             # scorers back to back on `main`; each layer's selection, gather and
@@ -519,8 +525,8 @@ class DecodeState:
                 self._attend(l, q_layers[l], sc, side, None if out_layers is None else out_layers[l])
                 if mark:
                     mark("attn_end", side)
-                if count is not None:
-                    count.add_(self.attended_blocks(l, sc))
+                if count is not None or fetched is not None:
+                    self._tally(l, sc, count, fetched)
                 ev_done[l].record(side)
             main.wait_stream(side)
             return
@@ -545,8 +551,8 @@ class DecodeState:
                     self._attend(l, q_layers[l], view, main, None if out_layers is None else out_layers[l])
                     if mark:
                         mark("attn_end", main)
-                    if count is not None:
-                        count.add_(self.attended_blocks(l, view))
+                    if count is not None or fetched is not None:
+                        self._tally(l, view, count, fetched)
                 self._select(l, q_la_layers[l], step, view, main, mark)
                 if mark:
                     mark("gather", main)
@@ -559,8 +565,8 @@ class DecodeState:
                     self._attend(l, q_layers[l], view, main, None if out_layers is None else out_layers[l])
                     if mark:
                         mark("attn_end", main)
-                    if count is not None:
-                        count.add_(self.attended_blocks(l, view))
+                    if count is not None or fetched is not None:
+                        self._tally(l, view, count, fetched)
             self._lag_ready = True
             return
         if copy == "carry":
@@ -646,6 +652,19 @@ class DecodeState:
         return self._side
 
     # ---------------------------------------------------------------- appends
+    def append_step(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
+        """One decode step's new token of every request in every layer (bf16
+        [L][B][Hkv][d] each); ctx advances once, with the last layer."""
+        L = self.w.L
+        st = stream or torch.cuda.current_stream(self.device)
+        if self.Kp is not None:  # every layer's token becomes valid when ctx advances below
+            for l in range(L):
+                B.oasis_pool_append(self.shape, k_new[l], self.ctx, self.Kp[l % self.L_phys], self.scratch.err, st)
+        for l in range(L):
+            lp, lh = l % self.L_phys, l % self.L_host
+            B.oasis_append_kv(self.shape, k_new[l], v_new[l], self.ctx, self.K[lp], self.host[lh], self.blk2slot[lp],
+                              self.k_pool[lp], self.v_pool[lp], l == L - 1, self.scratch.err, st)
+
     def append_tokens(self, layer: int, k_new: torch.Tensor, v_new: torch.Tensor, advance: bool,
                       stream=None, err=None):
         """Append one token per request (bf16 [B][Hkv][d]) to layer `layer`'s caches.
@@ -733,7 +752,7 @@ class StepGraph:
     """
 
     def __init__(self, st: DecodeState, first_step: int, q_la_steps, q_steps, out_steps, mark=None,
-                 copy: str = "carry"):
+                 copy: str = "carry", appends=None):
         self.st = st
         dev = st.device
         if st.scratch2 is None:
@@ -745,6 +764,8 @@ class StepGraph:
         torch.cuda.synchronize(dev)
         with torch.cuda.graph(self.graph, stream=self.stream):
             for k in range(len(q_steps)):
+                if appends is not None:  # (k_new, v_new) of captured step k: the growing context
+                    st.append_step(appends[k][0], appends[k][1], stream=self.stream)
                 st.decode_step(self.step, q_la_steps[k], q_steps[k], out_layers=out_steps[k],
                                main=self.stream, side=self.stream, mark=mark, copy=copy)
                 self.step.add_(1)
