@@ -165,3 +165,46 @@ def test_touch_host_reads_a_pinned_range():
     assert int(sink.item()) == 0
     with pytest.raises(B.OasisError):
         B.oasis_touch_host(host, nbytes=100)  # not a multiple of 16
+
+
+@pytest.mark.parametrize("scoring", ["maxdot", "pooled"])
+def test_decode_steps_with_appends_in_every_layer(scoring):
+    """append_step (every layer gets the step's token, ctx advances once) then a
+    decode step, against the oracle's per-layer appends and layer steps."""
+    from sparse_decode_attention_oasis_gb300.engine import DecodeState
+
+    L = 3
+    ctx0 = [1000, 1531, 2047]
+    w = syn.Workload("grow", L=L, B=3, Hq=32, Hkv=8, ctx=list(ctx0), Kb=32, C=2, n_hot=16,
+                     nb_max=-(-(max(ctx0) + 20) // 16))
+    st = DecodeState(w, l_phys=L, l_host=L, scoring=scoring)
+    layers = []
+    for l in range(L):
+        K, V = syn.layer_kv(w, l)
+        host = syn.host_tier_from_kv(w, K, V)
+        b2s, s2b, lu = [np.array(t) for t in syn.initial_tables(w, l)]
+        kp, vp = syn.pools_from_tables(w, host, s2b)
+        st.fill_layer_numpy(l, K, V, b2s, s2b, lu)
+        layers.append([K, host, b2s, s2b, lu, kp, vp])
+    out = torch.empty((L, w.B, w.Hq, w.d), dtype=torch.float32, device="cuda")
+    ctx_ref = list(ctx0)
+    for step in range(4):
+        news = [syn.append_tokens(w, l, step) for l in range(L)]
+        st.append_step(torch.stack([_dev_bits(k) for k, _ in news]), torch.stack([_dev_bits(v) for _, v in news]))
+        for l in range(L):
+            K, host, b2s, s2b, lu, kp, vp = layers[l]
+            ref.append_token(K, host, kp, vp, b2s, ctx_ref, news[l][0], news[l][1], advance=(l == L - 1))
+        w.ctx = list(ctx_ref)
+        qs = [syn.layer_queries(w, l, step) for l in range(L)]
+        st.decode_step(step, [_dev_bits(qla) for _, qla in qs], [_dev_bits(q) for q, _ in qs], out_layers=out,
+                       copy="overlap")
+        torch.cuda.synchronize()
+        assert st.error_word() == 0
+        np.testing.assert_array_equal(st.ctx.cpu().numpy(), np.array(ctx_ref))
+        for l in range(L):
+            K, host, b2s, s2b, lu, kp, vp = layers[l]
+            q, qla = qs[l]
+            r = ref.layer_step(K, qla, q, ctx_ref, host, kp, vp, b2s, s2b, lu, w.Kb, w.C, step, scoring=scoring)
+            np.testing.assert_array_equal(st.blk2slot[l].cpu().numpy(), b2s)
+            np.testing.assert_array_equal(st.slot2blk[l].cpu().numpy(), s2b)
+            _check_out(out[l].cpu().numpy().astype(np.float64), r["out"], f"layer {l} step {step}")
