@@ -39,7 +39,7 @@ struct QFrag {
 };
 
 template <int NT, bool kCopy>
-__global__ void __launch_bounds__(kScoreWarps * 32, (NT <= 2 ? 4 : 2))
+__global__ void __launch_bounds__(kScoreWarps * 32, (NT <= 2 ? 4 : 3))
 score_blocks_kernel(Shape s, const uint16_t* __restrict__ k_hbm, const int* __restrict__ ctx_len,
                     const uint16_t* __restrict__ q_la, float2* __restrict__ scores,
                     int chunks_per_head, int total_chunks, float inv_sqrt_d, CopyJob job) {
