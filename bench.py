@@ -65,7 +65,7 @@ def parse():
                          "available host memory holds); 8 layers (32 GiB) gave ~15%% more layer-steps/s than 29 on the same box")
     ap.add_argument("--preroll", type=int, default=40,
                     help="untimed decode steps run first, so the timed steps see a warmed-up resident set")
-    ap.add_argument("--copy", default="overlap", choices=["overlap", "pipe", "gather", "carry", "lag"],
+    ap.add_argument("--copy", default="overlap", choices=["overlap", "fork", "pipe", "gather", "carry", "lag"],
                     help="gather: one gather launch per layer after its selection, one stream; "
                          "overlap: gather of layer l on a side stream beside the attention of layer l-1; "
                          "carry: the host copy of layer l rides in layer l+1's scoring launch; "

@@ -487,6 +487,15 @@ class DecodeState:
             self.scratch2 = LayerScratch(self.shape, self.device)
         scr = (self.scratch, self.scratch2)
 
+        def attend_on(l, stream_):
+            if mark:
+                mark("attn", stream_)
+            self._attend(l, q_layers[l], scr[l % 2], stream_, None if out_layers is None else out_layers[l])
+            if mark:
+                mark("attn_end", stream_)
+            if count is not None or fetched is not None:
+                self._tally(l, scr[l % 2], count, fetched)
+
         def attend(l):
             if mark:
                 mark("attn", main)
@@ -583,6 +592,39 @@ class DecodeState:
             self._copy(L - 1, scr[(L - 1) % 2], main)
             attend(L - 1)
             return
+        if copy == "fork":
+            # main: score(l) topk(l); side A: attn(l-1) once score(l) is done (beside
+            # topk(l)); side B: gather(l) once topk(l) is done.  score(l+1) waits for
+            # gather(l) and attn(l-1).
+            sa = self._side_stream()
+            sb = self._side_stream2()
+            ev_sc = [torch.cuda.Event() for _ in range(2)]
+            ev_sel = [torch.cuda.Event() for _ in range(2)]
+            ev_gat = [torch.cuda.Event() for _ in range(2)]
+            ev_att = [torch.cuda.Event() for _ in range(2)]
+            for l in range(L):
+                sc = scr[l % 2]
+                lp = l % self.L_phys
+                self._score_lp(lp, q_la_layers[l], sc, main, mark)
+                if l > 0:
+                    ev_sc[l % 2].record(main)
+                    sa.wait_event(ev_sc[l % 2])
+                    attend_on(l - 1, sa)
+                    ev_att[l % 2].record(sa)
+                self._topk_diff_lp(lp, q_la_layers[l], sc, main, mark, host_layer=l)
+                ev_sel[l % 2].record(main)
+                sb.wait_event(ev_sel[l % 2])
+                if mark:
+                    mark("gather", sb)
+                self._gather(l, step, sc, sb)
+                if mark:
+                    mark("gather_end", sb)
+                ev_gat[l % 2].record(sb)
+                main.wait_event(ev_gat[l % 2])
+                if l > 0:
+                    main.wait_event(ev_att[l % 2])
+            attend(L - 1)
+            return
         if copy == "overlap":
             # main: S(l) [A(l-1)] wait G(l) S(l+1) ...; side: G(l) once S(l) is done.
             # G(l) overlaps A(l-1) only: the next scoring launch waits for it, so the
@@ -645,6 +687,11 @@ class DecodeState:
         if getattr(self, "_ring", None) is None or len(self._ring) < R:
             self._ring = [self.scratch, self.scratch2] + [LayerScratch(self.shape, self.device) for _ in range(R - 2)]
         return self._ring[:R]
+
+    def _side_stream2(self):
+        if getattr(self, "_side2", None) is None:
+            self._side2 = torch.cuda.Stream(self.device)
+        return self._side2
 
     def _side_stream(self):
         if getattr(self, "_side", None) is None:

@@ -83,7 +83,7 @@ def _multi_layer(copy, L=3, steps=3):
             _check_out(out[l].cpu().numpy().astype(np.float64), r["out"], f"layer {l} step {step}")
 
 
-@pytest.mark.parametrize("copy", ["carry", "gather", "overlap", "pipe"])
+@pytest.mark.parametrize("copy", ["carry", "gather", "overlap", "fork", "pipe"])
 def test_multi_layer_decode_step_all_orders(copy):
     _multi_layer(copy, L=6 if copy == "pipe" else 3)
 
