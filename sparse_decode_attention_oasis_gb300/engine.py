@@ -10,10 +10,15 @@ Layout in HBM (one physical layer buffer per entry of the first axis):
   blk2slot int32 [L][B][Hkv][nb_max]          slot of a resident block or -1
   slot2blk int32 [L][B][Hkv][P]               block held by a slot or -1
   last_used int32 [L][B][Hkv][P]              LRU clock
-Host tier (page-locked, device-mapped): bf16 [L][B][Hkv][nb_max][2][16][128].
-Per-layer scratch is shared by all layers of a step (scores, sel, fetch, ...).
-When the physical layer count is smaller than the logical one, layer l uses
-buffer l mod L_phys.
+  Kp       bf16 [L][B][Hkv][nb_max][2][128]   min/max pooled keys (pooled scoring only)
+Host tier (page-locked, device-mapped): bf16 [L_host][B][Hkv][nb_max][2][16][128],
+from cudaHostAlloc (default) or a huge-page mapping registered with CUDA.
+Scratch sets (scores, sel, fetch, workspace, ...) alternate between consecutive
+layers of a step.  When the physical layer count is smaller than the logical
+one, layer l uses buffer l mod L_phys (host tier: l mod L_host).
+
+decode_step issues a whole decode step in one of several launch orders (see its
+docstring); StepGraph captures decode steps as one CUDA graph.
 """
 from __future__ import annotations
 
@@ -31,10 +36,12 @@ class HugePinnedBuffer:
     """Page-locked, device-mapped host memory backed by transparent huge pages.
 
     The host tier is read by zero-copy loads at random block positions; on a
-    64 KiB-page host every block touches a different page, and translation misses
-    dominated the gather.  An anonymous mapping advised MADV_HUGEPAGE (512 MiB
-    pages) and then registered with cudaHostRegister(Mapped) keeps the number of
-    translations per layer small.  The memory starts zeroed.
+    64 KiB-page host every block touches a different page.  An anonymous mapping
+    advised MADV_HUGEPAGE (512 MiB pages) and then registered with
+    cudaHostRegister(Mapped) keeps the number of translations per layer small
+    (a lower gather median), but on some systems large registrations of this
+    kind stalled zero-copy reads for milliseconds; DecodeState takes its host
+    tier from cudaHostAlloc unless asked for this.  The memory starts zeroed.
     """
 
     _ALIGN = 1 << 29
@@ -287,7 +294,7 @@ class DecodeState:
     # ---------------------------------------------------------------- one layer-step
     def layer_step(self, layer: int, q_la: torch.Tensor, q: torch.Tensor, step: int,
                    stream=None, gather_stream=None, scratch: Optional[LayerScratch] = None,
-                   ev_pool=None, gather: str = "fused"):
+                   gather: str = "fused"):
         """Run a1..a5 for one layer: score, top-K, capped diff, gather, attention.
 
         q_la: bf16 [B][n_la][Hq][d], q: bf16 [B][Hq][d] (device).  Returns the
