@@ -125,7 +125,7 @@ class _SelView:
 class DecodeState:
     def __init__(self, w: syn.Workload, device="cuda", l_phys: Optional[int] = None,
                  l_host: Optional[int] = None, pin_host: bool = True, scoring: str = "maxdot",
-                 host_alloc: str = "thp"):
+                 host_alloc: str = "cuda"):
         """scoring: "maxdot" (a1, scan of the full keys) or "pooled" (f1, scan of the
         min/max pooled keys ``Kp``, bf16 [L][B][Hkv][nb_max][2][128], built from K
         by ``pool_all`` / the fill methods and kept current by ``append_tokens``)."""

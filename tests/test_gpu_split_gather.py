@@ -48,11 +48,11 @@ def test_cap_zero_copy_is_a_no_op():
     c.step(0, gather="carry")
 
 
-def _multi_layer(copy, L=3, steps=3):
+def _multi_layer(copy, L=3, steps=3, host_alloc="cuda"):
     from sparse_decode_attention_oasis_gb300.engine import DecodeState
 
     w = syn.Workload("layers", L=L, B=2, Hq=32, Hkv=8, ctx=[3000, 1777], Kb=32, C=3, n_hot=16)
-    st = DecodeState(w, l_phys=L, l_host=L)
+    st = DecodeState(w, l_phys=L, l_host=L, host_alloc=host_alloc)
     layers = []
     for l in range(L):
         K, V = syn.layer_kv(w, l)
@@ -86,6 +86,11 @@ def _multi_layer(copy, L=3, steps=3):
 @pytest.mark.parametrize("copy", ["carry", "gather", "overlap", "fork", "pipe"])
 def test_multi_layer_decode_step_all_orders(copy):
     _multi_layer(copy, L=6 if copy == "pipe" else 3)
+
+
+@pytest.mark.parametrize("host_alloc", ["thp", "thp_layers", "cuda_layers"])
+def test_host_tier_allocations(host_alloc):
+    _multi_layer("overlap", L=2, steps=2, host_alloc=host_alloc)
 
 
 def test_pipe_order_with_fewer_scorer_ctas():
