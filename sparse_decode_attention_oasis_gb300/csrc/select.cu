@@ -55,97 +55,77 @@ struct SelCtx {
   uint32_t* hist;              // [256]
   int* scal;                   // [8] scalars
   float* fscal;                // [kSelWarps]
+  int qstate;                  // queries: 0 not staged, 1 copies in flight, 2 staged with norms
+  int kcap;                    // entries of tval (Kb)
 };
 
-// ---------------------------------------------------------------- exact arithmetic
-__device__ __forceinline__ int exact_cmp(const uint32_t* a, const uint32_t* b) {
-  const int ta = (int)a[kLimbs - 1], tb = (int)b[kLimbs - 1];
-  if (ta != tb) return ta < tb ? -1 : 1;
-  for (int i = kLimbs - 2; i >= 0; --i)
-    if (a[i] != b[i]) return a[i] < b[i] ? -1 : 1;
-  return 0;
+__device__ __forceinline__ void sel_cp_async16(void* dst, const void* src) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void sel_cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
-// Exact q.k (times 2^266) of a 128-long bf16 row pair, by one warp.  Each lane
-// forms 4 exact products as (limb, low 32 bits, high bits); the limbs the warp
-// touches are summed one at a time with a 64-bit warp reduction (no atomics),
-// then every lane runs the same carry chain and lane i < 17 stores limb i.
-// Exact q.k (times 2^266) of a 128-long bf16 row pair, by one warp.  Each product
-// is mm * 2^(ee - 266) with mm < 2^16 (signed).  Fast path: when the nonzero
-// products' ee span at most 40, sum_j mm_j 2^(ee_j - emin) over 128 products is
-// below 2^63 and is summed exactly in 64-bit integers (the usual case); lane i
-// then writes limb i of that sum shifted by emin.  Otherwise each lane forms its
-// products as (limb, low 32 bits, high bits); the limbs the warp touches are
-// summed one at a time with a 64-bit warp reduction (no atomics), then every lane
-// runs the same carry chain and lane i < 17 stores limb i.  With kBox the key
-// element is chosen per dimension by the query's sign: krow (the pooled maxima)
-// where q >= 0, krow_neg (the minima) where q < 0, which makes the sum the pooled
-// score sum_i max(q_i hi_i, q_i lo_i).
+// ---------------------------------------------------------------- exact arithmetic
+// Sign of a - b for two 544-bit two's complement numbers (kLimbs words, least
+// significant first).  Every limb is loaded and compared at once; a higher
+// differing limb overrides a lower one, the top limb compares signed.
+__device__ __forceinline__ int exact_cmp(const uint32_t* a, const uint32_t* b) {
+  int r = 0;
+#pragma unroll
+  for (int i = 0; i < kLimbs - 1; ++i) {
+    const uint32_t x = a[i], y = b[i];
+    r = x != y ? (x < y ? -1 : 1) : r;
+  }
+  const int ta = (int)a[kLimbs - 1], tb = (int)b[kLimbs - 1];
+  return ta != tb ? (ta < tb ? -1 : 1) : r;
+}
+
+// Exact product of one bf16 pair as mms * 2^(ee - 266): mms the signed product of
+// the two 8-bit significands (|mms| < 2^16), ee in 0 .. 508 (mms = 0: no term).
+__device__ __forceinline__ void exact_prod(uint32_t qb, uint32_t kb, long long& mms, int& ee) {
+  const uint32_t kE = (kb >> 7) & 0xffu, qE = (qb >> 7) & 0xffu;
+  const uint32_t km = (kb & 0x7fu) | (kE ? 0x80u : 0u);
+  const uint32_t qm = (qb & 0x7fu) | (qE ? 0x80u : 0u);
+  const uint32_t mm = km * qm;
+  ee = (int)(kE ? kE : 1u) + (int)(qE ? qE : 1u) - 2;
+  mms = ((kb ^ qb) & 0x8000u) ? -(long long)mm : (long long)mm;
+}
+
+// The general case of warp_exact_dot (products spread over more than 40 binades;
+// rare, so kept out of line): each lane forms its products as (limb, low 32
+// bits, high bits); the limbs the warp touches are summed one at a time with a
+// 64-bit warp reduction (no atomics), then every lane runs the same carry chain
+// and lane i < 17 stores limb i.
 template <bool kBox>
-__device__ void warp_exact_dot(const uint16_t* krow, const uint16_t* qrow, uint32_t* out, int lane,
-                               const uint16_t* krow_neg = nullptr) {
-  int limb[4], eev[4];
-  long long lo[4], hi[4], mms[4];
+__device__ __noinline__ void warp_exact_dot_limbs(const uint16_t* krow, const uint16_t* qrow, uint32_t* out, int lane,
+                                                  const uint16_t* krow_neg) {
+  int limb[4];
+  long long lo[4], hi[4];
   int lmin = kLimbs, lmax = -1;
-  int emin = 1 << 20, emax = -1;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int e = lane + 32 * j;
     const uint32_t qb = qrow[e];
     const uint32_t kb = (kBox && (qb & 0x8000u)) ? krow_neg[e] : krow[e];
-    const uint32_t kE = (kb >> 7) & 0xffu, qE = (qb >> 7) & 0xffu;
-    const uint32_t km = (kb & 0x7fu) | (kE ? 0x80u : 0u);
-    const uint32_t qm = (qb & 0x7fu) | (qE ? 0x80u : 0u);
-    const uint32_t mm = km * qm;
+    long long mms;
+    int ee;
+    exact_prod(qb, kb, mms, ee);
     limb[j] = -2;
-    eev[j] = 0;
-    mms[j] = 0;
     lo[j] = hi[j] = 0;
-    if (mm) {
-      const int ee = (int)(kE ? kE : 1u) + (int)(qE ? qE : 1u) - 2;  // 0 .. 508
-      const unsigned long long v = (unsigned long long)mm << (ee & 31);
+    if (mms) {
+      const unsigned long long v = (unsigned long long)(mms < 0 ? -mms : mms) << (ee & 31);
       lo[j] = (long long)(v & 0xffffffffull);
       hi[j] = (long long)(v >> 32);
-      mms[j] = (long long)mm;
-      if ((kb ^ qb) & 0x8000u) {
+      if (mms < 0) {
         lo[j] = -lo[j];
         hi[j] = -hi[j];
-        mms[j] = -mms[j];
       }
-      eev[j] = ee;
-      emin = min(emin, ee);
-      emax = max(emax, ee);
       limb[j] = ee >> 5;
       lmin = min(lmin, limb[j]);
       lmax = max(lmax, limb[j] + 1);
     }
-  }
-  emin = __reduce_min_sync(0xffffffffu, emin);
-  emax = __reduce_max_sync(0xffffffffu, emax);
-  if (emax < 0 || emax - emin <= 40) {
-    long long acc = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (mms[j]) acc += mms[j] * (1LL << (eev[j] - emin));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    // limb i of |acc| * 2^emin, then two's complement if negative: the +1 carries
-    // into limb i exactly when every lower limb of the magnitude is zero
-    const unsigned long long mag = acc < 0 ? (unsigned long long)(-acc) : (unsigned long long)acc;
-    uint32_t w = 0u;
-    if (emax >= 0 && lane < kLimbs) {
-      const int b = 32 * lane - emin;  // bit of mag that lands at bit 0 of limb `lane`
-      if (b >= 0 && b < 64) w = (uint32_t)(mag >> b);
-      else if (b < 0 && b > -32) w = (uint32_t)(mag << (-b));
-    }
-    const unsigned nz = __ballot_sync(0xffffffffu, w != 0u);
-    if (acc < 0) {
-      const uint32_t carry = (nz & ((1u << lane) - 1u)) == 0u ? 1u : 0u;
-      w = ~w + carry;
-    }
-    if (lane < kLimbs) out[lane] = w;
-    __syncwarp();
-    return;
   }
   lmin = __reduce_min_sync(0xffffffffu, lmin);
   lmax = __reduce_max_sync(0xffffffffu, lmax);
@@ -169,6 +149,61 @@ __device__ void warp_exact_dot(const uint16_t* krow, const uint16_t* qrow, uint3
     carry = v >> 32;
   }
   if (lane < kLimbs) out[lane] = word;
+  __syncwarp();
+}
+
+// Exact q.k (times 2^266) of a 128-long bf16 row pair, by one warp, as kLimbs
+// words.  Each product is mm * 2^(ee - 266) with |mm| < 2^16.  When the nonzero
+// products' ee span at most 40 (the usual case), sum_j mm_j 2^(ee_j - emin) over
+// 128 products is below 2^63 and is summed exactly in 64-bit integers; lane i
+// then writes limb i of that sum shifted by emin.  Otherwise warp_exact_dot_limbs
+// sums it limb by limb.  With kBox the key element is chosen per dimension by the
+// query's sign: krow (the pooled maxima) where q >= 0, krow_neg (the minima) where
+// q < 0, which makes the sum the pooled score sum_i max(q_i hi_i, q_i lo_i).
+template <bool kBox>
+__device__ __forceinline__ void warp_exact_dot(const uint16_t* krow, const uint16_t* qrow, uint32_t* out, int lane,
+                                               const uint16_t* krow_neg = nullptr) {
+  long long mms[4];
+  int eev[4];
+  int emin = 1 << 20, emax = -1;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = lane + 32 * j;
+    const uint32_t qb = qrow[e];
+    const uint32_t kb = (kBox && (qb & 0x8000u)) ? krow_neg[e] : krow[e];
+    exact_prod(qb, kb, mms[j], eev[j]);
+    if (mms[j]) {
+      emin = min(emin, eev[j]);
+      emax = max(emax, eev[j]);
+    }
+  }
+  emin = __reduce_min_sync(0xffffffffu, emin);
+  emax = __reduce_max_sync(0xffffffffu, emax);
+  if (emax >= 0 && emax - emin > 40) {
+    warp_exact_dot_limbs<kBox>(krow, qrow, out, lane, krow_neg);
+    return;
+  }
+  long long acc = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (mms[j]) acc += mms[j] * (1LL << (eev[j] - emin));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  // limb i of |acc| * 2^emin, then two's complement if negative: the +1 carries
+  // into limb i exactly when every lower limb of the magnitude is zero
+  const unsigned long long mag = acc < 0 ? (unsigned long long)(-acc) : (unsigned long long)acc;
+  uint32_t w = 0u;
+  if (emax >= 0 && lane < kLimbs) {
+    const int b = 32 * lane - emin;  // bit of mag that lands at bit 0 of limb `lane`
+    if (b >= 0 && b < 64) w = (uint32_t)(mag >> b);
+    else if (b < 0 && b > -32) w = (uint32_t)(mag << (-b));
+  }
+  const unsigned nz = __ballot_sync(0xffffffffu, w != 0u);
+  if (acc < 0) {
+    const uint32_t carry = (nz & ((1u << lane) - 1u)) == 0u ? 1u : 0u;
+    w = ~w + carry;
+  }
+  if (lane < kLimbs) out[lane] = w;
   __syncwarp();
 }
 
@@ -211,15 +246,42 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   return r;
 }
 
+// Lists up to this long get their k-th largest by rank counting.
+constexpr int kRankMax = kSelThreads;
+
+// The k-th largest (1 <= k <= m) of v[0], v[kStride], ..., v[(m-1) kStride]: the
+// value with fewer than k larger values and at least k values at least as large
+// (thread i takes values i, i + blockDim.x, ...; every thread that finds it writes
+// the same value to *out).  Ends with *out visible to the CTA.
+template <int kStride>
+__device__ void kth_by_rank(const float* v, int m, int k, float* out) {
+  for (int i = threadIdx.x; i < m; i += blockDim.x) {
+    const float x = v[i * kStride];
+    int gt = 0, ge = 0;
+#pragma unroll 8
+    for (int j = 0; j < m; ++j) {
+      const float y = v[j * kStride];
+      gt += y > x ? 1 : 0;
+      ge += y >= x ? 1 : 0;
+    }
+    if (gt < k && k <= ge) *out = x;
+  }
+  __syncthreads();
+}
+
 // Bracket [t_lo, t_hi] around the k-th largest s~ among se[0..n) (1 <= k <= n), and
-// E = max e.  Two passes of 256 bins: bin1 = floor(256 (x - min)/(max - min)),
-// then 256 sub-bins of bin1's fraction.  Both bin maps are monotone in x (one
+// E = max e.  Up to kRankMax entries: t itself, by rank counting.  Longer lists:
+// a pass of 256 bins, bin1 = floor(256 (x - min)/(max - min)), finds the bin that
+// holds the k-th largest; if that bin holds at most kRankMax entries they are
+// listed (in `scratch`, n floats) and t is found among them by rank counting,
+// otherwise a second pass of 256 sub-bins of bin1's fraction narrows it to the
+// cell's smallest and largest s~.  Both bin maps are monotone in x (one
 // subtraction and a multiplication by a positive constant, exact sub-bin
-// offsets), so the k-th largest lies in the selected (bin1, bin2) cell; t_lo and
-// t_hi are the smallest and largest s~ in that cell.
-__device__ void kth_bracket(const float2* se, int n, int k, uint32_t* hist, int* scal, float* fs,
+// offsets), so the k-th largest lies in the selected bin and cell.
+__device__ void kth_bracket(const float2* se, int n, int k, uint32_t* hist, int* scal, float* fs, float* scratch,
                             float& t_lo, float& t_hi, float& emax) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float* tslot = fs + 60;   // fs[0 .. 3 kSelWarps) hold the partial reductions, fs + 64 the cell keys
   float mn = __int_as_float(0x7f800000), mx = neg_inf(), em = 0.f;
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const float2 v = se[i];
@@ -231,13 +293,22 @@ __device__ void kth_bracket(const float2* se, int n, int k, uint32_t* hist, int*
   mx = warp_max(mx);
   em = warp_max(em);
   if (lane == 0) { fs[3 * warp] = mn; fs[3 * warp + 1] = mx; fs[3 * warp + 2] = em; }
-  for (int i = threadIdx.x; i < 512; i += blockDim.x) hist[i] = 0u;
+  const bool small = n <= kRankMax;
+  if (!small)
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0u;
+  if (threadIdx.x == 0) { *tslot = neg_inf(); scal[5] = 0; }
   __syncthreads();
   mn = fs[0]; mx = fs[1]; em = fs[2];
   for (int w = 1; w < kSelWarps; ++w) {
     mn = fminf(mn, fs[3 * w]); mx = fmaxf(mx, fs[3 * w + 1]); em = fmaxf(em, fs[3 * w + 2]);
   }
   emax = em;
+  if (small) {
+    kth_by_rank<2>(reinterpret_cast<const float*>(se), n, k, tslot);
+    t_lo = t_hi = *tslot;
+    __syncthreads();
+    return;
+  }
   const float span = mx - mn;
   const float sc1 = span > 1e-30f ? 256.0f / span : 0.f;
   const int n_pad = (n + 31) & ~31;
@@ -271,6 +342,28 @@ __device__ void kth_bracket(const float2* se, int n, int k, uint32_t* hist, int*
   __syncthreads();
   const int b1 = scal[0];
   const int k1 = k - scal[1];
+  const int m1 = (int)hist[b1];
+  if (m1 <= kRankMax) {
+    // list bin b1's entries (warp-aggregated slots), then rank them
+    for (int i = threadIdx.x; i < n_pad; i += blockDim.x) {
+      float x = 0.f;
+      bool in = false;
+      if (i < n) {
+        x = se[i].x;
+        in = (int)min(255, (int)((x - mn) * sc1)) == b1;
+      }
+      const unsigned ball = __ballot_sync(0xffffffffu, in);
+      int base = 0;
+      if (lane == 0 && ball) base = atomicAdd(&scal[5], __popc(ball));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (in) scratch[base + __popc(ball & ((1u << lane) - 1u))] = x;
+    }
+    __syncthreads();
+    kth_by_rank<1>(scratch, m1, k1, tslot);
+    t_lo = t_hi = *tslot;
+    __syncthreads();
+    return;
+  }
   uint32_t* h2 = hist + 256;                    // reuse: counts of sub-bins
   uint32_t* kmin = reinterpret_cast<uint32_t*>(fs + 64);   // per sub-bin min / max keys
   uint32_t* kmax = kmin + 256;
@@ -321,14 +414,32 @@ __device__ void kth_bracket(const float2* se, int n, int k, uint32_t* hist, int*
   __syncthreads();
 }
 
-// Stage the head's lookahead queries (bf16 bits and fp32 norms) in shared memory:
-// one 16-byte load per piece, all issued together.
-__device__ void stage_queries(SelCtx& c) {
+// Start copying the head's lookahead queries (bf16 bits) into shared memory with
+// 16-byte cp.async, so that their latency overlaps the bracket and classification.
+__device__ void issue_queries(SelCtx& c) {
   for (int idx = threadIdx.x; idx < c.N * 16; idx += blockDim.x) {
     const int n = idx >> 4, part = idx & 15;
     const int j = n / c.G, gg = n - j * c.G;
-    const uint4 v = ldg_nc(c.q_la + (((long long)c.b * c.n_la + j) * c.Hq + c.h * c.G + gg) * kD + part * 8);
-    reinterpret_cast<uint4*>(c.qb + n * kD)[part] = v;
+    sel_cp_async16(c.qb + n * kD + part * 8,
+                   c.q_la + (((long long)c.b * c.n_la + j) * c.Hq + c.h * c.G + gg) * kD + part * 8);
+  }
+  c.qstate = 1;
+}
+
+// Make the head's lookahead queries (bf16 bits and fp32 norms) ready in shared
+// memory: finish the copies issue_queries started, or load them now (one 16-byte
+// load per piece, all issued together).  Idempotent; every thread calls it.
+__device__ void stage_queries(SelCtx& c) {
+  if (c.qstate == 2) return;
+  if (c.qstate == 1) {
+    sel_cp_async_wait_all();
+  } else {
+    for (int idx = threadIdx.x; idx < c.N * 16; idx += blockDim.x) {
+      const int n = idx >> 4, part = idx & 15;
+      const int j = n / c.G, gg = n - j * c.G;
+      const uint4 v = ldg_nc(c.q_la + (((long long)c.b * c.n_la + j) * c.Hq + c.h * c.G + gg) * kD + part * 8);
+      reinterpret_cast<uint4*>(c.qb + n * kD)[part] = v;
+    }
   }
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -343,6 +454,7 @@ __device__ void stage_queries(SelCtx& c) {
     if (lane == 0) c.qn[n] = sqrtf(ss);
   }
   __syncthreads();
+  c.qstate = 2;
 }
 
 __device__ __forceinline__ uint4 lds16v(const uint16_t* p) { return *reinterpret_cast<const uint4*>(p); }
@@ -438,27 +550,30 @@ __device__ void warp_exact_block_score(const SelCtx& c, int blk, uint32_t* out, 
       }
     }
   best_lo = warp_max(best_lo);
+  // bit idx of `mine`: this lane's dot idx can be the block's maximum
+  unsigned mine = 0u;
+#pragma unroll
+  for (int idx = 0; idx < 16; ++idx)
+    if (vhi[idx] != neg_inf() && vhi[idx] >= best_lo) mine |= 1u << idx;
   bool have = false;
   uint32_t* tmp = c.tmp + warp * kLimbs;
-#pragma unroll
-  for (int idx = 0; idx < 16; ++idx) {
-    const bool cand = vhi[idx] != neg_inf() && vhi[idx] >= best_lo;
-    unsigned mask = __ballot_sync(0xffffffffu, cand);
-    while (mask) {
-      const int src = __ffs(mask) - 1;
-      mask &= mask - 1;
-      const int sg = src >> 2, st = src & 3;
-      const int nt = idx >> 2, e = idx & 3;
-      const int tau = sg + (e >= 2 ? 8 : 0);
-      const int n = nt * 8 + 2 * st + (e & 1);
-      warp_exact_dot<false>(kst + tau * kD, c.qb + n * kD, tmp, lane);
-      if (lane == 0) {
-        if (!have || exact_cmp(tmp, out) > 0)
-          for (int i = 0; i < kLimbs; ++i) out[i] = tmp[i];
-      }
-      have = true;
-      __syncwarp();
+  // one candidate dot at a time (lowest lane first, then lowest idx), summed exactly
+  for (unsigned lanes = __ballot_sync(0xffffffffu, mine != 0u); lanes;
+       lanes = __ballot_sync(0xffffffffu, mine != 0u)) {
+    const int src = __ffs(lanes) - 1;
+    const int idx = __ffs(__shfl_sync(0xffffffffu, mine, src)) - 1;
+    if (lane == src) mine &= mine - 1u;
+    const int sg = src >> 2, st = src & 3;
+    const int nt = idx >> 2, e = idx & 3;
+    const int tau = sg + (e >= 2 ? 8 : 0);
+    const int n = nt * 8 + 2 * st + (e & 1);
+    warp_exact_dot<false>(kst + tau * kD, c.qb + n * kD, tmp, lane);
+    if (lane == 0) {
+      if (!have || exact_cmp(tmp, out) > 0)
+        for (int i = 0; i < kLimbs; ++i) out[i] = tmp[i];
     }
+    have = true;
+    __syncwarp();
   }
   if (!have && lane == 0) {
     for (int i = 0; i < kLimbs - 1; ++i) out[i] = 0u;
@@ -525,32 +640,58 @@ __device__ void warp_exact_pooled_score(const SelCtx& c, int blk, uint32_t* out,
 }
 
 // Mark (cls = 1) the r best of the uncertain candidates U[0..nU) by exact order;
-// cand_blk maps a candidate index to its block (nullptr = identity).  The running
-// top-r set T (exact values, in rank order) is merged with each batch of
-// kSelWarps freshly scored blocks by counting, for every member of the union, how
-// many members rank before it; the r first go to the other buffer.
+// cand_blk maps a candidate index to its block (nullptr = identity).  Up to Kb
+// candidates: every warp scores candidates warp, warp + kSelWarps, ... into tval,
+// then each candidate's rank is the number of candidates ordered before it (exact
+// value descending, block ascending) and the r first are marked.  More than Kb
+// (rare; bounded memory): the running top-r set T (exact values, in rank order)
+// is merged with each batch of kSelWarps freshly scored blocks by counting, for
+// every member of the union, how many members rank before it; the r first go to
+// the other buffer.
 template <bool kPooled>
 __device__ void refine_top_r(SelCtx& c, const int* U, int nU, int r, const int* cand_blk,
                              uint8_t* cls) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   stage_queries(c);
+  const bool single = nU <= c.kcap;
+  const int chunk = single ? nU : kSelWarps;
+  uint32_t* vals = single ? c.tval : c.bval;  // exact values of this round's candidates
   int tcount = 0;
   uint32_t* tv = c.tval;
   int* ti = c.tidx;
   uint32_t* tv2 = c.tval2;
   int* ti2 = c.tidx2;
-  for (int base = 0; base < nU; base += kSelWarps) {
-    const int nbat = min(kSelWarps, nU - base);
-    if (warp < nbat) {
-      const int ci = U[base + warp];
+  for (int base = 0; base < nU; base += chunk) {
+    const int nbat = min(chunk, nU - base);
+    for (int i = warp; i < nbat; i += kSelWarps) {
+      const int ci = U[base + i];
       const int blk = cand_blk ? cand_blk[ci] : ci;
       if constexpr (kPooled)
-        warp_exact_pooled_score(c, blk, c.bval + warp * kLimbs, warp, lane);
+        warp_exact_pooled_score(c, blk, vals + i * kLimbs, warp, lane);
       else
-        warp_exact_block_score(c, blk, c.bval + warp * kLimbs, warp, lane);
-      if (lane == 0) c.bidx[warp] = ci;
+        warp_exact_block_score(c, blk, vals + i * kLimbs, warp, lane);
+      if (lane == 0 && !single) c.bidx[i] = ci;
     }
     __syncthreads();
+    if (single) {
+      for (int m = threadIdx.x; m < nU; m += blockDim.x) {
+        uint32_t mv[kLimbs];
+#pragma unroll
+        for (int i = 0; i < kLimbs; ++i) mv[i] = vals[m * kLimbs + i];
+        const int mci = U[m];
+        const int mblk = cand_blk ? cand_blk[mci] : mci;
+        int rk = 0;
+        for (int o = 0; o < nU; ++o) {
+          const int oci = U[o];
+          const int oblk = cand_blk ? cand_blk[oci] : oci;
+          const int cmpv = exact_cmp(vals + o * kLimbs, mv);
+          rk += (cmpv > 0 || (cmpv == 0 && oblk < mblk)) ? 1 : 0;
+        }
+        cls[mci] = rk < r ? 1 : 0;
+      }
+      __syncthreads();
+      return;
+    }
     const int tot = tcount + nbat;
     for (int m = threadIdx.x; m < tot; m += blockDim.x) {
       const uint32_t* mv = m < tcount ? tv + m * kLimbs : c.bval + (m - tcount) * kLimbs;
@@ -597,7 +738,7 @@ __device__ void select_best(SelCtx& c, const float2* se, int n, int k, const int
     return;
   }
   float t_lo, t_hi, em;
-  kth_bracket(se, n, k, c.hist, c.scal, c.fscal, t_lo, t_hi, em);
+  kth_bracket(se, n, k, c.hist, c.scal, c.fscal, reinterpret_cast<float*>(U), t_lo, t_hi, em);
   const float hi_t = __fadd_ru(t_hi, em), lo_t = __fsub_rd(t_lo, em);
   if (threadIdx.x == 0) { c.scal[2] = 0; c.scal[3] = 0; }
   __syncthreads();
@@ -624,6 +765,18 @@ __device__ void select_best(SelCtx& c, const float2* se, int n, int k, const int
     for (int i = threadIdx.x; i < nU; i += blockDim.x) cls[U[i]] = r > 0 ? 1 : 0;
     __syncthreads();
     return;
+  }
+  // the refine takes kSelWarps blocks per round: bring the keys of the later
+  // rounds (up to kPrefetchBlocks blocks) into L2 now
+  constexpr int kLines = kPooled ? 2 * kD * 2 / 128 : kBS * kD * 2 / 128;
+  constexpr int kPrefetchBlocks = 64;
+  const int npre = min(nU, kSelWarps + kPrefetchBlocks) - kSelWarps;
+  for (int idx = threadIdx.x; idx < npre * kLines; idx += blockDim.x) {
+    const int ci = U[kSelWarps + idx / kLines];
+    const int blk = cand_blk ? cand_blk[ci] : ci;
+    const char* line = reinterpret_cast<const char*>(c.k + (long long)blk * (kPooled ? 2 * kD : kBS * kD)) +
+                       (idx % kLines) * 128;
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(line));
   }
   refine_top_r<kPooled>(c, U, nU, r, cand_blk, cls);
 }
@@ -690,6 +843,8 @@ __device__ SelCtx make_ctx(char* sm, const SelLayout& L, const Shape& s, const u
   c.hist = reinterpret_cast<uint32_t*>(sm + L.hist);
   c.scal = reinterpret_cast<int*>(sm + L.scal);
   c.fscal = reinterpret_cast<float*>(sm + L.fscal);
+  c.qstate = 0;
+  c.kcap = s.Kb;
   return c;
 }
 
@@ -697,28 +852,37 @@ __device__ SelCtx make_ctx(char* sm, const SelLayout& L, const Shape& s, const u
 // F = the best min(cap, |M|) of the missing blocks M of S (ascending S of ns <= Kb
 // entries, one per thread), written ascending to fetch[head].  se, cls, U, cblk
 // hold at least Kb entries.
-// With host_kv (device address of the mapped host tier) each fetched block's
-// 8 KiB is also prefetched into L2, so the gather that follows reads it there.
-template <bool kPooled>
-__device__ void capped_diff(SelCtx& c, const Shape& s, const float2* scores, const int* S, int ns,
-                            const int* blk2slot, int cap, int head, int* fetch, int* nfetch, float2* se,
-                            uint8_t* cls, int* U, int* cblk, int* red, const uint16_t* host_kv = nullptr) {
+//
+// diff_prepare lists M in S order in cblk[0..nM) with their scores in se[0..nM)
+// and returns nM.  With se_all, se[x] already holds block x's score (the top-K
+// pass loaded them); otherwise the scores are read from `scores`.
+__device__ int diff_prepare(const Shape& s, const float2* scores, const int* S, int ns, const int* blk2slot,
+                            int head, float2* se, int* cblk, int* red, bool se_all) {
   const int* b2s = blk2slot + (long long)head * s.nb_max;
-  // missing blocks of S, in S order (ascending); one entry per thread (ns <= Kb <= 256)
   int x = -1, miss = 0;
+  float2 sx = make_float2(0.f, 0.f);
   if ((int)threadIdx.x < ns) {
     x = S[threadIdx.x];
     miss = (x >= 0 && x < s.nb_max && b2s[x] < 0) ? 1 : 0;
+    if (miss) sx = se_all ? se[x] : scores[(long long)head * s.nb_max + x];
   }
+  // every se[x] is read before the scan's first barrier, every se[pos] written after
   const int pos = block_excl_scan(miss, red, red + 31);
   const int nM = red[31];
   if (miss) {
     cblk[pos] = x;
-    se[pos] = scores[(long long)head * s.nb_max + x];
+    se[pos] = sx;
   }
   __syncthreads();
-  const int C = cap < nM ? cap : nM;
-  select_best<kPooled>(c, se, nM, C, cblk, cls, U);
+  return nM;
+}
+
+// diff_emit writes the marked (cls == 1) entries of cblk[0..nM) to fetch[head] in
+// order, pads with -1 and sets nfetch[head].  With host_kv (device address of
+// the mapped host tier) each fetched block's 8 KiB is also prefetched into L2,
+// so the gather that follows reads it there.
+__device__ void diff_emit(const Shape& s, int nM, const uint8_t* cls, const int* cblk, int head, int* fetch,
+                          int* nfetch, int* red, const uint16_t* host_kv) {
   int* out = fetch + (long long)head * s.Kb;
   const int take = ((int)threadIdx.x < nM && cls[threadIdx.x] == 1) ? 1 : 0;
   const int opos = block_excl_scan(take, red, red + 31);
@@ -736,8 +900,11 @@ __device__ void capped_diff(SelCtx& c, const Shape& s, const float2* scores, con
 }
 
 // ---------------------------------------------------------------- a2 kernel
-// With kDiff the same CTA then runs a3 on the selection it just wrote (one launch
-// for top-K and capped diff).
+// Pass 0 selects S (top-K of all nb blocks; every block when nb <= Kb) and writes
+// it in ascending block order.  With kDiff, pass 1 runs a3 on that S in the same
+// CTA (one launch for top-K and capped diff).  The passes form one loop that is
+// not unrolled, so both run the same copy of the selection code and the second
+// finds it in the instruction cache.
 template <bool kPooled, bool kDiff>
 __global__ void __launch_bounds__(kSelThreads, 2)
 topk_select_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __restrict__ k_hbm,
@@ -756,40 +923,44 @@ topk_select_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* _
   uint8_t* cls = reinterpret_cast<uint8_t*>(sm + L.cls);
   int* U = reinterpret_cast<int*>(sm + L.U);
   int* red = reinterpret_cast<int*>(sm + L.red);
-  if (nb <= s.Kb) {
-    for (int i = threadIdx.x; i < s.Kb; i += blockDim.x) out[i] = i < nb ? i : -1;
-    if (threadIdx.x == 0) nsel[head] = nb;
-    if constexpr (kDiff) {
-      __syncthreads();  // the selection written above is visible to the whole CTA
-      capped_diff<kPooled>(c, s, scores, out, nb, blk2slot, cap, head, fetch, nfetch, se, cls, U,
-                           reinterpret_cast<int*>(sm + L.cblk), red, host_kv);
-    }
-    return;
-  }
+  int* cblk = reinterpret_cast<int*>(sm + L.cblk);
   const float2* src = scores + (long long)head * s.nb_max;
   for (int i = threadIdx.x; i < nb; i += blockDim.x) se[i] = src[i];
+  if (nb > s.Kb) issue_queries(c);
   __syncthreads();
-  select_best<kPooled>(c, se, nb, s.Kb, nullptr, cls, U);
-  // compaction in ascending block order
-  const int per = (nb + kSelThreads - 1) / kSelThreads;
-  const int i0 = threadIdx.x * per, i1 = min(nb, i0 + per);
-  int cnt = 0;
-  for (int i = i0; i < i1; ++i) cnt += cls[i] == 1;
-  int total = 0;
-  int pos = block_excl_scan(cnt, red, red + 31);
-  total = red[31];
-  for (int i = i0; i < i1; ++i)
-    if (cls[i] == 1) {
-      if (pos < s.Kb) out[pos] = i;
-      ++pos;
+  int ns = 0;
+#pragma unroll 1
+  for (int pass = 0; pass < (kDiff ? 2 : 1); ++pass) {
+    int n = nb, k = s.Kb;
+    const int* cb = nullptr;
+    if (pass == 1) {
+      __syncthreads();  // the selection written by pass 0 is visible to the whole CTA
+      n = diff_prepare(s, scores, out, ns, blk2slot, head, se, cblk, red, true);
+      k = cap < n ? cap : n;
+      cb = cblk;
     }
-  for (int i = total + threadIdx.x; i < s.Kb; i += blockDim.x) out[i] = -1;
-  if (threadIdx.x == 0) nsel[head] = total < s.Kb ? total : s.Kb;
-  if constexpr (kDiff) {
-    __syncthreads();  // the selection written above is visible to the whole CTA
-    capped_diff<kPooled>(c, s, scores, out, total < s.Kb ? total : s.Kb, blk2slot, cap, head, fetch, nfetch, se,
-                         cls, U, reinterpret_cast<int*>(sm + L.cblk), red, host_kv);
+    select_best<kPooled>(c, se, n, k, cb, cls, U);
+    if (pass == 0) {
+      // compaction in ascending block order
+      const int per = (nb + kSelThreads - 1) / kSelThreads;
+      const int i0 = threadIdx.x * per, i1 = min(nb, i0 + per);
+      int cnt = 0;
+      for (int i = i0; i < i1; ++i) cnt += cls[i] == 1;
+      int pos = block_excl_scan(cnt, red, red + 31);
+      const int total = red[31];
+      for (int i = i0; i < i1; ++i)
+        if (cls[i] == 1) {
+          if (pos < s.Kb) out[pos] = i;
+          ++pos;
+        }
+      for (int i = total + threadIdx.x; i < s.Kb; i += blockDim.x) out[i] = -1;
+      ns = total < s.Kb ? total : s.Kb;
+      if (threadIdx.x == 0) nsel[head] = ns;
+    } else {
+      diff_emit(s, n, cls, cblk, head, fetch, nfetch, red, host_kv);
+    }
   }
+  if (c.qstate == 1) sel_cp_async_wait_all();  // no copy left in flight at exit
 }
 
 // ---------------------------------------------------------------- a3 kernel
@@ -813,8 +984,11 @@ fetch_diff_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __
   int* red = reinterpret_cast<int*>(sm + L.red);
   int ns = nsel[head];
   ns = ns < 0 ? 0 : (ns > s.Kb ? s.Kb : ns);
-  capped_diff<kPooled>(c, s, scores, sel + (long long)head * s.Kb, ns, blk2slot, cap, head, fetch, nfetch, se, cls,
-                       U, cblk, red);
+  issue_queries(c);
+  const int nM = diff_prepare(s, scores, sel + (long long)head * s.Kb, ns, blk2slot, head, se, cblk, red, false);
+  select_best<kPooled>(c, se, nM, cap < nM ? cap : nM, cblk, cls, U);
+  diff_emit(s, nM, cls, cblk, head, fetch, nfetch, red, nullptr);
+  if (c.qstate == 1) sel_cp_async_wait_all();  // no copy left in flight at exit
 }
 
 // ---------------------------------------------------------------- launchers
