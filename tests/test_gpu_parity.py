@@ -76,9 +76,13 @@ def test_cap_zero_empty_resident_set():
     assert (sc.out.cpu().numpy() == 0).all()
 
 
-def test_duplicate_blocks_force_exact_ties():
-    """48 identical top blocks straddle the rank-32 boundary: ties go to the lower index."""
-    w = syn.Workload("ties", L=1, B=1, Hq=32, Hkv=8, ctx=[2048], Kb=32, C=8, n_hot=0)
+@pytest.mark.parametrize("ctx", [2048, 8192])
+def test_duplicate_blocks_force_exact_ties(ctx):
+    """48 identical top blocks straddle the rank-32 boundary: ties go to the lower index.
+
+    128 blocks take the rank-count bracket; 512 take the histogram pass with the
+    tied blocks inside the bin that holds the threshold."""
+    w = syn.Workload("ties", L=1, B=1, Hq=32, Hkv=8, ctx=[ctx], Kb=32, C=8, n_hot=0)
     K, V = syn.layer_kv(w, 0)
     Kf = syn.bf16_bits_to_f32(K) * np.float32(1.0 / 64)     # power-of-two scaling is exact
     for h in range(w.Hkv):
@@ -92,8 +96,12 @@ def test_duplicate_blocks_force_exact_ties():
     c.step(1)
 
 
-def test_all_zero_keys():
-    w = syn.Workload("zeros", L=1, B=1, Hq=32, Hkv=8, ctx=[1024], Kb=32, C=4, n_hot=0)
+@pytest.mark.parametrize("ctx", [1024, 4800])
+def test_all_zero_keys(ctx):
+    """Every score ties at 0 and every block is uncertain (more than Kb: the batched
+    refine).  300 blocks also put more than 256 entries in one histogram bin (the
+    second histogram pass)."""
+    w = syn.Workload("zeros", L=1, B=1, Hq=32, Hkv=8, ctx=[ctx], Kb=32, C=4, n_hot=0)
     K, V = syn.layer_kv(w, 0)
     K[:] = 0
     c = Case(w, K=K, V=V)
