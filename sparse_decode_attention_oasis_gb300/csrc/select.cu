@@ -7,8 +7,9 @@
 // explanatory figure step 3; Table 2 caption: the per-step fetch cap).
 //
 // Exact selection from certified intervals.  The scores come with a bound e,
-// |s~ - s| <= e.  With t the r-th largest s~, bracketed as t_lo <= t <= t_hi by a
-// two-level histogram, and E = max e over the candidates:
+// |s~ - s| <= e.  With t the r-th largest s~, bracketed as t_lo <= t <= t_hi (by
+// rank counting, or a histogram pass and rank counting inside the bin that holds
+// t), and E = max e over the candidates:
 //   s~_i - e_i > t_hi + E  => i is certainly among the r best,
 //   s~_i + e_i < t_lo - E  => i certainly is not,
 // (every candidate that could rank at or above a "certain" one has s~ > t, and
@@ -20,10 +21,14 @@
 //      block's maximum - normally one;
 //   2. those dots are evaluated exactly: each bf16 is m * 2^(E-134), each
 //      product is an integer times 2^-266, and a 544-bit two's complement
-//      fixed-point number (17 limbs of 32 bits) holds the sum with no rounding;
-//      the limbs are summed with 64-bit warp reductions;
-//   3. U is merged into a running top-r set by exact comparison (a rank count
-//      over the union), kSelWarps blocks at a time.
+//      fixed-point number (17 limbs of 32 bits) holds the sum with no rounding
+//      (a 64-bit integer warp sum when the products span at most 40 binades,
+//      else limb by limb);
+//   3. one rank count over U by exact comparison marks its r best (a U larger
+//      than Kb is merged into a running top-r set kSelWarps blocks at a time).
+// Every routine has one call site per kernel, so that the code a CTA runs once
+// stays small: run once per head, the phases are bound by latency, including
+// instruction fetch.
 // The result equals the definition for every finite input whose tensor-core
 // accumulation stays within the modelled bound (the GPU tests check every block
 // score of every case against its exact value).
