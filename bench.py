@@ -94,7 +94,8 @@ def parse():
     ap.add_argument("--no-hostlink", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-worker", type=int, default=0, help=argparse.SUPPRESS)
-    ap.add_argument("--cpu-heads", type=int, default=3)
+    ap.add_argument("--cpu-heads", type=int, default=12,
+                    help="(request, KV head) pairs the CPU baseline times (about 0.8 s each on config 2)")
     return ap.parse_args()
 
 
@@ -128,8 +129,9 @@ def workload_desc(w) -> str:
 
 
 # --------------------------------------------------------------------------- CPU oracle timing
-def cpu_sample(args, nheads: int, step: int = 0):
-    """Time the oracle's layer-step on `nheads` sampled (request, KV head) pairs of layer 0.
+def cpu_sample(args, nheads: int, step: int = 0, warm: int = 0):
+    """Time the oracle's layer-step on `nheads` sampled (request, KV head) pairs of layer 0,
+    after `warm` untimed ones (first-call costs of the process).
 
     Returns seconds per head (the oracle as it stands, numpy float64/exact).
     """
@@ -140,10 +142,10 @@ def cpu_sample(args, nheads: int, step: int = 0):
 
     w = workload(args)
     rng = np.random.default_rng(1234 + step)
-    picks = [(int(rng.integers(w.B)), int(rng.integers(w.Hkv))) for _ in range(nheads)]
+    picks = [(int(rng.integers(w.B)), int(rng.integers(w.Hkv))) for _ in range(nheads + warm)]
     G = w.G
     total = 0.0
-    for (b, h) in picks:
+    for i, (b, h) in enumerate(picks):
         Kh, Vh = syn.head_kv(w, 0, b, h)
         qh, qlah = syn.head_queries(w, 0, b, h, step)
         sub = syn.Workload("sub", L=1, B=1, Hq=G, Hkv=1, ctx=[w.ctx[b]], Kb=w.Kb, C=w.C, n_la=w.n_la,
@@ -163,28 +165,38 @@ def cpu_sample(args, nheads: int, step: int = 0):
         qla = qlah[None]
         t0 = time.perf_counter()
         ref.layer_step(K, qla, q, [w.ctx[b]], host, kp, vp, b2s, s2b, lu, w.Kb, w.C, step)
-        total += time.perf_counter() - t0
+        if i >= warm:
+            total += time.perf_counter() - t0
     return total / nheads
 
 
-def cpu_baseline(args, heads: int):
-    """Run the oracle sample in a fresh process (all host cores for its BLAS)."""
-    cores = os.cpu_count() or 1
+def _cpu_worker_sec_per_head(args, heads: int, threads: int) -> float:
+    """Seconds per head of the oracle sample, in a fresh process with `threads` BLAS threads."""
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        env[k] = str(cores)
+        env[k] = str(threads)
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-worker", str(heads), "--layers", str(args.layers),
-           "--batch", str(args.batch), "--ctx", str(args.ctx)]
+           "--batch", str(args.batch), "--ctx", str(args.ctx), "--workload", args.workload, "--ratio", str(args.ratio)]
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=1800)
     if r.returncode != 0:
         raise RuntimeError("cpu baseline worker failed:\n" + r.stderr[-2000:])
-    per_head = json.loads(r.stdout.strip().splitlines()[-1])["sec_per_head"]
+    return json.loads(r.stdout.strip().splitlines()[-1])["sec_per_head"]
+
+
+def cpu_baseline(args, heads: int):
+    """Time the oracle sample with all host cores for its BLAS, and with one thread."""
+    cores = os.cpu_count() or 1
     w = workload(args)
-    layer_step_s = per_head * w.B * w.Hkv
-    return {"value": 1.0 / layer_step_s, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{heads} (request, KV head) pairs of layer 0 of the {w.name} workload, one full "
-                      f"layer-step each (exact scoring, top-K, capped diff, LRU slots, fp64 attention); "
-                      f"layer-step time = time per head x {w.B * w.Hkv} heads"}
+    all_cores = _cpu_worker_sec_per_head(args, heads, cores)
+    one = _cpu_worker_sec_per_head(args, max(1, heads // 3), 1)
+    return {"value": 1.0 / (all_cores * w.B * w.Hkv), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "value_1_thread": 1.0 / (one * w.B * w.Hkv),
+            "sample": f"{heads} (request, KV head) pairs of layer 0 of the {w.name} workload ({max(1, heads // 3)} "
+                      f"with one thread), after one untimed pair, one full layer-step each (exact scoring, "
+                      f"top-K, capped diff, LRU slots, fp64 attention), {heads * all_cores:.1f} s of oracle "
+                      f"time; layer-step time = time per head x "
+                      f"{w.B * w.Hkv} heads; cores = the BLAS threads given to the oracle process "
+                      f"(its numpy arithmetic; the rest of the oracle is one Python thread)"}
 
 
 # --------------------------------------------------------------------------- clocks
@@ -891,7 +903,7 @@ def run_gpu(args, rank, world, local_rank):
 def main():
     args = parse()
     if args.cpu_worker:
-        print(json.dumps({"sec_per_head": cpu_sample(args, args.cpu_worker)}), flush=True)
+        print(json.dumps({"sec_per_head": cpu_sample(args, args.cpu_worker, warm=1)}), flush=True)
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -56,13 +56,15 @@ STREAM_APPEND_V = 6
 # counter-based generator (numpy side)
 # --------------------------------------------------------------------------
 def mix32_np(x: np.ndarray) -> np.ndarray:
-    """32-bit integer bijection on uint64 arrays holding values < 2**32."""
-    x = np.asarray(x, dtype=np.uint64) & np.uint64(M32)
-    x = x ^ (x >> np.uint64(16))
-    x = (x * np.uint64(_C1)) & np.uint64(M32)
-    x = x ^ (x >> np.uint64(15))
-    x = (x * np.uint64(_C2)) & np.uint64(M32)
-    x = x ^ (x >> np.uint64(15))
+    """32-bit integer bijection, elementwise; returns uint32 (the input is taken
+    mod 2**32).  uint32 products wrap mod 2**32, as the definition wants."""
+    x = np.asarray(x)
+    x = (x & np.uint64(M32)).astype(np.uint32) if x.dtype != np.uint32 else x.copy()
+    x ^= x >> np.uint32(16)
+    x *= np.uint32(_C1)
+    x ^= x >> np.uint32(15)
+    x *= np.uint32(_C2)
+    x ^= x >> np.uint32(15)
     return x
 
 
@@ -97,15 +99,17 @@ def hash_normals(seed: int, stream: int, layer: int, b: int, h: int,
                  start: int, count: int) -> np.ndarray:
     """float32 N(0,1) draws for elements [start, start+count) of one chunk."""
     k1, k2 = chunk_key(seed, stream, layer, b, h)
-    idx = np.arange(start, start + count, dtype=np.uint64)
-    v = mix32_np(mix32_np(idx ^ np.uint64(k1)) ^ np.uint64(k2))
-    return NORMAL_TABLE[(v >> np.uint64(16)).astype(np.int64)]
+    idx = (np.arange(start, start + count, dtype=np.uint64) & np.uint64(M32)).astype(np.uint32)
+    v = mix32_np(mix32_np(idx ^ np.uint32(k1)) ^ np.uint32(k2))
+    return NORMAL_TABLE[v >> np.uint32(16)]
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float32 to bfloat16 (round to nearest, ties to even); finite input."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    r = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    # uint32 wrap-around only drops bits above 2**32, which the shift and the
+    # 16-bit result drop anyway
+    r = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
     return r.astype(np.uint16)
 
 
@@ -421,17 +425,17 @@ def head_kv_torch(w: Workload, layer: int, b: int, h: int, device):
 # vectorised draws (same bits as the per-head functions above)
 # --------------------------------------------------------------------------
 def _chunk_keys_multi(seed: int, stream: int, layer: int, bs_, hs_):
-    k1 = np.array([chunk_key(seed, stream, layer, int(b), int(h))[0] for b, h in zip(bs_, hs_)], np.uint64)
-    k2 = np.array([mix32_int(int(k) ^ _K2_SALT) for k in k1], np.uint64)
+    k1 = np.array([chunk_key(seed, stream, layer, int(b), int(h))[0] for b, h in zip(bs_, hs_)], np.uint32)
+    k2 = np.array([mix32_int(int(k) ^ _K2_SALT) for k in k1], np.uint32)
     return k1, k2
 
 
 def hash_normals_multi(seed: int, stream: int, layer: int, bs_, hs_, start: int, count: int) -> np.ndarray:
     """[len(bs_)][count] float32 draws; row r equals hash_normals(..., bs_[r], hs_[r], start, count)."""
     k1, k2 = _chunk_keys_multi(seed, stream, layer, bs_, hs_)
-    idx = np.arange(start, start + count, dtype=np.uint64)[None, :]
+    idx = (np.arange(start, start + count, dtype=np.uint64) & np.uint64(M32)).astype(np.uint32)[None, :]
     v = mix32_np(mix32_np(idx ^ k1[:, None]) ^ k2[:, None])
-    return NORMAL_TABLE[(v >> np.uint64(16)).astype(np.int64)]
+    return NORMAL_TABLE[v >> np.uint32(16)]
 
 
 class QueryStream:
