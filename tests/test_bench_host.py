@@ -1,5 +1,6 @@
 """Host-side logic of the benchmark (no GPU): algorithmic bytes, workload
-selection, host-tier sizing and the L2 note."""
+selection, host-tier sizing, the L2 note, the --impl flag and the CPU
+baseline's reporting rule."""
 import importlib.util
 import os
 
@@ -57,3 +58,36 @@ def test_l2_note(bench):
     assert bench.l2_note(syn.qwen3_8b_decode(), "maxdot").startswith("inputs larger than L2 (2.00 GiB of keys")
     assert "pooled keys" in bench.l2_note(syn.qwen3_8b_decode(), "pooled")
     assert "smaller than" in bench.l2_note(syn.tiny(), "maxdot")
+
+
+def test_impl_flag_parsing(bench, monkeypatch):
+    for argv, want in [(["bench.py"], None), (["bench.py", "--impl", "reference"], "reference"),
+                       (["bench.py", "--steps", "2", "--impl=reference"], "reference"),
+                       (["bench.py", "--impl", "gb300"], "gb300")]:
+        monkeypatch.setattr(bench.sys, "argv", argv)
+        assert bench._impl_from_argv() == want
+
+
+@pytest.mark.parametrize("one,allc,faster", [(0.5, 2.0, "one"), (3.0, 1.5, "all")])
+def test_cpu_baseline_reports_the_faster_thread_setting(bench, monkeypatch, one, allc, faster):
+    """`value` is the faster of the one-thread and all-cores timings, `cores` the
+    threads it used; both values are reported and scaled by the pairs per layer."""
+    import argparse
+
+    calls = []
+
+    def fake(args, heads, threads):
+        calls.append((heads, threads))
+        return one if threads == 1 else allc
+
+    monkeypatch.setattr(bench, "_cpu_worker_sec_per_head", fake)
+    monkeypatch.setattr(bench.os, "cpu_count", lambda: 16)
+    ns = argparse.Namespace(workload="qwen3_8b_decode", ratio="0.01", batch=32, layers=36, ctx=32768)
+    r = bench.cpu_baseline(ns, 12)
+    per = 32 * 8
+    assert calls == [(48, 1), (4, 16)]
+    assert r["value_1_thread"] == pytest.approx(1.0 / (one * per))
+    assert r["value_16_threads"] == pytest.approx(1.0 / (allc * per))
+    assert r["cores"] == (1 if faster == "one" else 16)
+    assert r["value"] == max(r["value_1_thread"], r["value_16_threads"])
+    assert r["kind"] == "oracle" and r["unit"] == bench.UNIT
