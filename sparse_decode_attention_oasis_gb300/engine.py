@@ -479,6 +479,9 @@ class DecodeState:
         copy="lag": the cross-step pipeline (f4): attn(l) over the selection the
           previous step made for layer l, then select(l) and gather(l) for the next
           step; one stream.
+        copy="fork": score(l) and top-K + diff(l) on ``main``; attn(l-1) on a side
+          stream once score(l) is done (beside top-K(l)); gather(l) on a second side
+          stream once top-K(l) is done; score(l+1) waits for both.
         copy="gather": select(0); select(1); attn(0); select(2); attn(1); ... with
           the whole gather (oasis_gather_h2d) of layer l right after select(l), on
           ``side`` if given (attn(l) then waits for it).
