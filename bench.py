@@ -113,7 +113,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-worker", type=int, default=0, help=argparse.SUPPRESS)
     ap.add_argument("--cpu-heads", type=int, default=12,
-                    help="(request, KV head) pairs the CPU baseline times (about 0.8 s each on config 2)")
+                    help="(request, KV head) pairs the CPU baseline times (about 0.3 s each on the Qwen3-8B decode shape)")
     return ap.parse_args()
 
 
