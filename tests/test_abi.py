@@ -109,3 +109,40 @@ def test_set_option_validates(lib):
     assert lib.oasis_set_option(1, -1) == 1
     assert lib.oasis_set_option(99, 0) == 1
     assert lib.oasis_set_option(1, 0) == 0
+
+
+def _header_signatures():
+    """{name: (return type, [parameter types])} from the declarations in oasis.h."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    sigs = {}
+    for ret, name, params in re.findall(r"OASIS_API\s+([\w\s\*]+?)\b(oasis_\w+)\s*\(([^;]*?)\)\s*;", text, flags=re.S):
+        ps = [] if params.strip() in ("", "void") else [p.strip() for p in params.split(",")]
+        types = [re.sub(r"\s+", " ", p if p.endswith("*") else re.sub(r"\b\w+$", "", p)).strip() for p in ps]
+        sigs[name] = (re.sub(r"\s+", " ", ret).strip(), types)
+    return sigs
+
+
+def _ctypes_kind(t):
+    if t is ctypes.c_void_p or t is ctypes.c_char_p or (isinstance(t, type) and issubclass(t, ctypes._Pointer)):
+        return "pointer"
+    return {ctypes.c_int32: "int32", ctypes.c_int: "int32", ctypes.c_size_t: "size", ctypes.c_float: "float"}[t]
+
+
+def _c_kind(t):
+    if t.endswith("*") or t == "oasis_stream_t":
+        return "pointer"
+    return {"int32_t": "int32", "oasis_status": "int32", "size_t": "size", "float": "float",
+            "uint32_t": "int32"}[t]
+
+
+def test_binding_signatures_match_the_header():
+    """Every call's ctypes argument list has the header's arity and argument kinds
+    (pointer, 32-bit integer, size, float), and the same kind of return value: a
+    mismatch would pass every CPU test and corrupt arguments on the GPU."""
+    sigs = _header_signatures()
+    assert len(sigs) == len(declared_functions())
+    for name, (ret, params) in sigs.items():
+        argtypes, restype = binding._SIGS[name]
+        assert len(argtypes) == len(params), (name, params)
+        assert [_ctypes_kind(a) for a in argtypes] == [_c_kind(p) for p in params], name
+        assert _ctypes_kind(restype) == _c_kind(ret), (name, ret)
