@@ -29,6 +29,17 @@ K, V ~ N(0,1); per (layer, request, KV head) a unit vector u; every key of a
 hot block gets +3u; the true query of each query head in the GQA group is
 2u + e with e ~ N(0,1) drifting across decode steps as AR(1) with coefficient
 rho; lookahead query j is the true query plus N(0, 0.3**2) noise.
+
+Drifting hot set (``hot_mode="drift"``, the long-output reasoning workload of
+Table 1's long-output rows): per (layer, request, KV head) a plane spanned by
+two orthonormal vectors a, c and a pool of ``n_pool`` planted blocks; pool
+block i (in draw order) has its own direction v_i = cos(phi_i) a + sin(phi_i) c,
+phi_i = 2 pi i / n_pool, and each of its keys gets +3 v_i.  The query
+direction u_s drifts as an AR(1) process on that great circle: a 2-vector
+w_s = rho_u w_{s-1} + sqrt(1 - rho_u**2) xi_s (w_0, xi_s ~ N(0, I_2)),
+u_s = (w_s / |w_s|) . [a; c].  The true query is 2 u_s + e_s as above.  The hot
+set at step s is the ``n_hot`` pool blocks best aligned with u_s; rho_u = 0.997
+makes it turn over by about 5% per step (see :func:`hot_set_turnover`).
 """
 from __future__ import annotations
 
@@ -50,6 +61,8 @@ STREAM_QNOISE = 3
 STREAM_LANOISE = 4
 STREAM_APPEND_K = 5
 STREAM_APPEND_V = 6
+STREAM_PLANE_C = 7      # second vector of the drift plane
+STREAM_UDRIFT = 8       # the 2-D AR(1) draws of the drifting query direction
 
 
 # --------------------------------------------------------------------------
@@ -134,17 +147,24 @@ class Workload:
     d: int = 128
     bs: int = 16
     n_hot: int = 16
-    hot_mode: str = "random"  # "random" | "spans_sink_recent"
+    hot_mode: str = "random"  # "random" | "spans_sink_recent" | "drift"
     steps: int = 1
     rho: float = 0.9
     la_sigma: float = 0.3
     seed: int = 0
     nb_max: Optional[int] = None
     P: Optional[int] = None   # HBM slots per (layer, request, KV head)
+    n_pool: int = 256         # planted blocks per head with their own direction ("drift")
+    rho_u: float = 0.997      # AR(1) coefficient of the drifting query direction ("drift")
 
     def __post_init__(self):
         if len(self.ctx) != self.B:
             raise ValueError("ctx must list one context length per request")
+        if self.hot_mode not in ("random", "spans_sink_recent", "drift"):
+            raise ValueError(f"unknown hot_mode {self.hot_mode!r}")
+        # planted blocks are drawn from the blocks of the starting context, so that
+        # appends (which advance ctx in place) do not change them
+        self.ctx0 = list(self.ctx)
         if self.nb_max is None:
             self.nb_max = max(-(-c // self.bs) for c in self.ctx)
         if self.P is None:
@@ -160,6 +180,10 @@ class Workload:
 
     def nb(self, b: int) -> int:
         return -(-self.ctx[b] // self.bs)
+
+    def nb0(self, b: int) -> int:
+        """Blocks of request b's starting context (the planted blocks lie among them)."""
+        return -(-self.ctx0[b] // self.bs)
 
 
 def fetch_cap_from_ratio(ratio: Optional[float], Kb: int) -> int:
@@ -201,22 +225,35 @@ def long_output_ctx(B: int, start: int = 8192, end: int = 32768, steps: int = 25
     return [start + (r * span) // max(1, B - 1) for r in range(B)]
 
 
-def long_output(seed: int = 0, B: int = 128, L: int = 36, steps: int = 256) -> Workload:
-    """Long-output reasoning decode: Qwen3-8B shape, batch 128, ctx 8K..32K, ratio 0.02."""
+def long_output(seed: int = 0, B: int = 128, L: int = 36, steps: int = 256, rho_u: float = 0.997) -> Workload:
+    """Long-output reasoning decode: Qwen3-8B shape, batch 128, ctx 8K..32K, ratio 0.02,
+    a hot set of 64 blocks drifting through a pool of 256 planted blocks per head
+    (about 5% of the hot set replaced per step at rho_u = 0.997)."""
     ctx = long_output_ctx(B, steps=steps)
     w = Workload("long_output", L=L, B=B, Hq=32, Hkv=8, ctx=ctx, Kb=128,
-                 C=fetch_cap_from_ratio(0.02, 128), n_hot=64, steps=steps, seed=seed,
-                 nb_max=-(-(max(ctx) + steps) // 16))
+                 C=fetch_cap_from_ratio(0.02, 128), n_hot=64, hot_mode="drift", n_pool=256,
+                 rho_u=rho_u, steps=steps, seed=seed, nb_max=-(-(max(ctx) + steps) // 16))
     return w
 
 
 # --------------------------------------------------------------------------
 # per-head draws (host)
 # --------------------------------------------------------------------------
-def hot_blocks(w: Workload, layer: int, b: int, h: int) -> np.ndarray:
-    """Sorted indices of the planted hot blocks of one (layer, request, KV head)."""
-    nb = w.nb(b)
+def pool_blocks(w: Workload, layer: int, b: int, h: int) -> np.ndarray:
+    """The planted pool of a drifting-hot-set workload, in draw order (pool index i
+    has direction angle 2 pi i / n_pool)."""
+    nb = w.nb0(b)
     rng = np.random.default_rng([w.seed, 101, layer, b, h])
+    return rng.choice(nb, size=min(w.n_pool, nb), replace=False).astype(np.int64)
+
+
+def hot_blocks(w: Workload, layer: int, b: int, h: int) -> np.ndarray:
+    """Sorted indices of the planted blocks of one (layer, request, KV head)
+    (for ``hot_mode="drift"``: the whole pool)."""
+    nb = w.nb0(b)
+    rng = np.random.default_rng([w.seed, 101, layer, b, h])
+    if w.hot_mode == "drift":
+        return np.sort(pool_blocks(w, layer, b, h))
     if w.hot_mode == "random":
         n = min(w.n_hot, nb)
         return np.sort(rng.choice(nb, size=n, replace=False)).astype(np.int64)
@@ -244,19 +281,113 @@ def unit_dir(w: Workload, layer: int, b: int, h: int) -> np.ndarray:
     return (z / np.linalg.norm(z)).astype(np.float32)
 
 
+def drift_plane(w: Workload, layer: int, b: int, h: int):
+    """Orthonormal float64 pair (a, c) spanning the plane of the drifting direction."""
+    a = hash_normals(w.seed, STREAM_U, layer, b, h, 0, w.d).astype(np.float64)
+    a = a / np.linalg.norm(a)
+    c = hash_normals(w.seed, STREAM_PLANE_C, layer, b, h, 0, w.d).astype(np.float64)
+    c = c - (c @ a) * a
+    return a, c / np.linalg.norm(c)
+
+
+def pool_dirs(w: Workload, layer: int, b: int, h: int) -> np.ndarray:
+    """float64 [n][d] directions of the planted pool (pool index i at angle 2 pi i / n_pool)."""
+    a, c = drift_plane(w, layer, b, h)
+    n = len(pool_blocks(w, layer, b, h))
+    phi = 2.0 * np.pi * np.arange(n) / w.n_pool
+    return np.cos(phi)[:, None] * a[None, :] + np.sin(phi)[:, None] * c[None, :]
+
+
+def planted_shifts(w: Workload, layer: int, b: int, h: int):
+    """(blocks int64 [n], float32 [n][d] shift added to every key of that block)."""
+    if w.hot_mode == "drift":
+        blocks = pool_blocks(w, layer, b, h)
+        return blocks, (3.0 * pool_dirs(w, layer, b, h)).astype(np.float32)
+    blocks = hot_blocks(w, layer, b, h)
+    shift = (np.float32(3.0) * unit_dir(w, layer, b, h)).astype(np.float32)
+    return blocks, np.repeat(shift[None, :], len(blocks), axis=0)
+
+
+def _drift_w(w: Workload, layer: int, b: int, h: int, step: int) -> np.ndarray:
+    """The 2-vector w_step of the AR(1) process of one head (float64)."""
+    x = hash_normals(w.seed, STREAM_UDRIFT, layer, b, h, 0, 2).astype(np.float64)
+    a = math.sqrt(1.0 - w.rho_u * w.rho_u)
+    for s in range(1, step + 1):
+        xi = hash_normals(w.seed, STREAM_UDRIFT, layer, b, h, 2 * s, 2).astype(np.float64)
+        x = w.rho_u * x + a * xi
+    return x
+
+
+def _dir_from_w(x: np.ndarray, a: np.ndarray, c: np.ndarray) -> np.ndarray:
+    """u = (x / |x|) . [a; c] for one 2-vector or rows of 2-vectors (float64)."""
+    x = np.asarray(x, dtype=np.float64)
+    n = np.sqrt(x[..., 0] * x[..., 0] + x[..., 1] * x[..., 1])
+    return (x[..., 0] / n)[..., None] * a + (x[..., 1] / n)[..., None] * c
+
+
+def query_dir(w: Workload, layer: int, b: int, h: int, step: int) -> np.ndarray:
+    """float64 mean direction of the true queries of one head at a decode step."""
+    if w.hot_mode != "drift":
+        return unit_dir(w, layer, b, h).astype(np.float64)
+    a, c = drift_plane(w, layer, b, h)
+    return _dir_from_w(_drift_w(w, layer, b, h, step), a, c)
+
+
+def hot_set(w: Workload, layer: int, b: int, h: int, step: int) -> List[int]:
+    """The n_hot planted blocks best aligned with the query direction at `step`
+    (sorted; alignment ties to the lower pool index).  For the fixed modes: the
+    planted blocks themselves."""
+    if w.hot_mode != "drift":
+        return hot_blocks(w, layer, b, h).tolist()
+    al = pool_dirs(w, layer, b, h) @ query_dir(w, layer, b, h, step)
+    order = np.argsort(-al, kind="stable")[: w.n_hot]
+    return sorted(pool_blocks(w, layer, b, h)[order].tolist())
+
+
+def hot_set_turnover(w: Workload, layer: int, steps: int, heads=None) -> float:
+    """Mean fraction of the hot set replaced per decode step, over `heads`
+    ((request, KV head) pairs; default all) and steps 1..steps-1."""
+    pairs = heads if heads is not None else [(b, h) for b in range(w.B) for h in range(w.Hkv)]
+    if w.hot_mode != "drift":
+        return 0.0
+    tot, n = 0.0, 0
+    for (b, h) in pairs:
+        pool, dirs = pool_blocks(w, layer, b, h), pool_dirs(w, layer, b, h)
+        a, c = drift_plane(w, layer, b, h)
+        x = hash_normals(w.seed, STREAM_UDRIFT, layer, b, h, 0, 2).astype(np.float64)
+        f = math.sqrt(1.0 - w.rho_u * w.rho_u)
+        prev = None
+        for s in range(steps):
+            if s:
+                x = w.rho_u * x + f * hash_normals(w.seed, STREAM_UDRIFT, layer, b, h, 2 * s, 2).astype(np.float64)
+            order = np.argsort(-(dirs @ _dir_from_w(x, a, c)), kind="stable")[: w.n_hot]
+            cur = set(pool[order].tolist())
+            if prev is not None:
+                tot += len(cur - prev) / max(1, len(cur))
+                n += 1
+            prev = cur
+    return tot / max(1, n)
+
+
 def head_kv_f32(w: Workload, layer: int, b: int, h: int, ntok: Optional[int] = None):
     """float32 keys/values of one head before bf16 rounding, tokens [0, ntok)."""
     if ntok is None:
         ntok = w.ctx[b]
     K = hash_normals(w.seed, STREAM_K, layer, b, h, 0, ntok * w.d).reshape(ntok, w.d)
     V = hash_normals(w.seed, STREAM_V, layer, b, h, 0, ntok * w.d).reshape(ntok, w.d)
-    shift = (np.float32(3.0) * unit_dir(w, layer, b, h)).astype(np.float32)
-    hot = hot_blocks(w, layer, b, h)
-    if len(hot):
-        tok = (hot[:, None] * w.bs + np.arange(w.bs)[None, :]).reshape(-1)
-        tok = tok[tok < ntok]
-        K[tok] = K[tok] + shift[None, :]
+    tok, rows = _planted_rows(w, layer, b, h, ntok)
+    if len(tok):
+        K[tok] = K[tok] + rows
     return K, V
+
+
+def _planted_rows(w: Workload, layer: int, b: int, h: int, ntok: int):
+    """Token indices < ntok of the planted blocks and the float32 shift of each."""
+    blocks, shifts = planted_shifts(w, layer, b, h)
+    tok = (blocks[:, None] * w.bs + np.arange(w.bs)[None, :]).reshape(-1)
+    rows = np.repeat(shifts, w.bs, axis=0)
+    keep = tok < ntok
+    return tok[keep], rows[keep]
 
 
 def head_kv(w: Workload, layer: int, b: int, h: int):
@@ -292,7 +423,7 @@ def _query_noise(w: Workload, layer: int, b: int, hq: int, step: int) -> np.ndar
 def head_queries(w: Workload, layer: int, b: int, h: int, step: int = 0):
     """True queries [G][d] and lookahead queries [n_la][G][d] (bf16 bits) of one KV head."""
     G, d = w.G, w.d
-    u = unit_dir(w, layer, b, h).astype(np.float64)
+    u = query_dir(w, layer, b, h, step)
     q = np.zeros((G, d), np.float32)
     qla = np.zeros((w.n_la, G, d), np.float32)
     for g in range(G):
@@ -408,12 +539,10 @@ def head_kv_torch(w: Workload, layer: int, b: int, h: int, device):
     n = w.ctx[b] * w.d
     Kf = hash_normals_torch(w.seed, STREAM_K, layer, b, h, 0, n, device).view(w.ctx[b], w.d)
     Vf = hash_normals_torch(w.seed, STREAM_V, layer, b, h, 0, n, device).view(w.ctx[b], w.d)
-    hot = hot_blocks(w, layer, b, h)
-    if len(hot):
-        shift = torch.from_numpy((np.float32(3.0) * unit_dir(w, layer, b, h)).astype(np.float32)).to(device)
-        tok = (hot[:, None] * w.bs + np.arange(w.bs)[None, :]).reshape(-1)
-        tok = torch.from_numpy(tok[tok < w.ctx[b]]).to(device)
-        Kf[tok] = Kf[tok] + shift[None, :]
+    tok, rows = _planted_rows(w, layer, b, h, w.ctx[b])
+    if len(tok):
+        tok = torch.from_numpy(tok).to(device)
+        Kf[tok] = Kf[tok] + torch.from_numpy(rows).to(device)
     K = torch.zeros((w.T_max, w.d), dtype=torch.bfloat16, device=device)
     V = torch.zeros_like(K)
     K[: w.ctx[b]] = Kf.to(torch.bfloat16)
@@ -438,6 +567,33 @@ def hash_normals_multi(seed: int, stream: int, layer: int, bs_, hs_, start: int,
     return NORMAL_TABLE[v >> np.uint32(16)]
 
 
+class _DriftDirs:
+    """Per-step query directions of every head of one layer of a drifting-hot-set
+    workload, [B*Hq][d] float64 (rows of one KV head repeated over its group);
+    the same values as :func:`query_dir` step by step."""
+
+    def __init__(self, w: Workload, layer: int):
+        self.w, self.layer, self.step = w, layer, 0
+        planes = [drift_plane(w, layer, b, h) for b in range(w.B) for h in range(w.Hkv)]
+        self.a = np.stack([p[0] for p in planes])
+        self.c = np.stack([p[1] for p in planes])
+        self.bb = np.repeat(np.arange(w.B), w.Hkv)
+        self.hh = np.tile(np.arange(w.Hkv), w.B)
+        self.x = None
+
+    def next(self) -> np.ndarray:
+        w = self.w
+        if self.x is None:
+            self.x = hash_normals_multi(w.seed, STREAM_UDRIFT, self.layer, self.bb, self.hh, 0, 2).astype(np.float64)
+        else:
+            xi = hash_normals_multi(w.seed, STREAM_UDRIFT, self.layer, self.bb, self.hh,
+                                    2 * self.step, 2).astype(np.float64)
+            self.x = w.rho_u * self.x + math.sqrt(1.0 - w.rho_u * w.rho_u) * xi
+        self.step += 1
+        u = _dir_from_w(self.x, self.a, self.c)                      # [B*Hkv][d]
+        return np.repeat(u, w.G, axis=0)
+
+
 class QueryStream:
     """Queries of one layer for decode steps 0, 1, 2, ... (AR(1) noise carried over).
 
@@ -452,13 +608,17 @@ class QueryStream:
         B, Hq, d, G = w.B, w.Hq, w.d, w.G
         self.bb = np.repeat(np.arange(B), Hq)
         self.hq = np.tile(np.arange(Hq), B)
-        u = np.stack([unit_dir(w, layer, b, h) for b in range(B) for h in range(w.Hkv)])
-        self.u = u.reshape(B, w.Hkv, 1, d).repeat(G, axis=2).reshape(B * Hq, d).astype(np.float64)
+        self.drift = _DriftDirs(w, layer) if w.hot_mode == "drift" else None
+        if self.drift is None:
+            u = np.stack([unit_dir(w, layer, b, h) for b in range(B) for h in range(w.Hkv)])
+            self.u = u.reshape(B, w.Hkv, 1, d).repeat(G, axis=2).reshape(B * Hq, d).astype(np.float64)
         self.e = None
 
     def next(self):
         w = self.w
         d = w.d
+        if self.drift is not None:
+            self.u = self.drift.next()
         if self.e is None:
             self.e = hash_normals_multi(w.seed, STREAM_QNOISE, self.layer, self.bb, self.hq, 0, d).astype(np.float64)
         else:
@@ -496,12 +656,10 @@ def kv_request_torch(w: Workload, layer: int, b: int, device):
     Kf = draw(keys)
     Vf = draw(vkeys)
     for h in range(H):
-        hot = hot_blocks(w, layer, b, h)
-        if len(hot):
-            shift = torch.from_numpy((np.float32(3.0) * unit_dir(w, layer, b, h)).astype(np.float32)).to(device)
-            tok = (hot[:, None] * w.bs + np.arange(w.bs)[None, :]).reshape(-1)
-            tok = torch.from_numpy(tok[tok < w.ctx[b]]).to(device)
-            Kf[h, tok] = Kf[h, tok] + shift[None, :]
+        tok, rows = _planted_rows(w, layer, b, h, w.ctx[b])
+        if len(tok):
+            tok = torch.from_numpy(tok).to(device)
+            Kf[h, tok] = Kf[h, tok] + torch.from_numpy(rows).to(device)
     K = torch.zeros((H, w.T_max, w.d), dtype=torch.bfloat16, device=device)
     V = torch.zeros_like(K)
     K[:, : w.ctx[b]] = Kf.to(torch.bfloat16)
@@ -540,9 +698,11 @@ class QueryStreamTorch:
         self.step = 0
         self.bb = np.repeat(np.arange(w.B), w.Hq)
         self.hq = np.tile(np.arange(w.Hq), w.B)
-        u = np.stack([unit_dir(w, layer, b, h) for b in range(w.B) for h in range(w.Hkv)])
-        u = u.reshape(w.B, w.Hkv, 1, w.d).repeat(w.G, axis=2).reshape(w.B * w.Hq, w.d).astype(np.float64)
-        self.u2 = torch.from_numpy(2.0 * u).to(device)
+        self.drift = _DriftDirs(w, layer) if w.hot_mode == "drift" else None
+        if self.drift is None:
+            u = np.stack([unit_dir(w, layer, b, h) for b in range(w.B) for h in range(w.Hkv)])
+            u = u.reshape(w.B, w.Hkv, 1, w.d).repeat(w.G, axis=2).reshape(w.B * w.Hq, w.d).astype(np.float64)
+            self.u2 = torch.from_numpy(2.0 * u).to(device)
         self.e = None
         self.a = math.sqrt(1.0 - w.rho * w.rho)
 
@@ -550,6 +710,8 @@ class QueryStreamTorch:
         import torch
 
         w, d, dev = self.w, self.w.d, self.device
+        if self.drift is not None:  # the drifting direction is a few host flops per head
+            self.u2 = torch.from_numpy(2.0 * self.drift.next()).to(dev)
         if self.e is None:
             self.e = hash_normals_multi_torch(w.seed, STREAM_QNOISE, self.layer, self.bb, self.hq, 0, d,
                                               dev).double()
