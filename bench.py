@@ -917,7 +917,7 @@ def run_gpu(args, rank, world, local_rank):
         "device_error_word": errw,
         "setup_s": round(gen_s, 1), "alloc_s": round(alloc_s, 1),
         "host_tier_warm_s": None if warm_s is None else round(warm_s, 2),
-        "score_kernel": os.environ.get("OASIS_SCORE_KERNEL", "mma"),
+        "score_kernel": "mma.sync",
     }
     if not args.no_cpu_baseline and world == 1:
         try:

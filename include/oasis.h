@@ -118,9 +118,9 @@ OASIS_API const char* oasis_last_error(void);
  * fp32-accumulated bf16 products with a wide margin.  Selection never trusts
  * s~ inside this interval: it re-scores those blocks exactly.
  * Two kernels implement it: by default warp-level mma.sync tiles fed by direct
- * 16-byte loads; with the environment variable OASIS_SCORE_KERNEL=tc (read at
- * every call) a tcgen05/TMA/TMEM kernel.  Their s~ may differ inside the bound;
- * everything selection derives from them is identical.
+ * 16-byte loads; after oasis_set_option(OASIS_OPT_SCORE_KERNEL,
+ * OASIS_SCORE_KERNEL_TC) a tcgen05/TMA/TMEM kernel.  Their s~ may differ inside
+ * the bound; everything selection derives from them is identical.
  */
 OASIS_API oasis_status oasis_score_blocks(const oasis_shape* shape, const void* k_hbm,
                                 const int32_t* ctx_len, const void* q_la,
@@ -277,8 +277,9 @@ OASIS_API oasis_status oasis_copy_fetched(const oasis_shape* shape, const void* 
  *   Each warp stages its first fetched block from the host before it scores and
  *   writes it to the slot after, so the host-link latency overlaps the HBM-bound
  *   scoring.  Results are those of the two calls made one after the other.
- *   err_word is required (it receives both calls' bits).  With
- *   OASIS_SCORE_KERNEL=tc the two are launched one after the other instead.
+ *   err_word is required (it receives both calls' bits).  With the tcgen05
+ *   scorer selected (OASIS_OPT_SCORE_KERNEL) the two are launched one after the
+ *   other instead.
  */
 OASIS_API oasis_status oasis_score_blocks_copy(const oasis_shape* shape, const void* k_hbm,
                                                const int32_t* ctx_len, const void* q_la,
@@ -363,6 +364,10 @@ OASIS_API size_t oasis_attn_workspace_bytes(const oasis_shape* shape);
  *     between calls; two calls whose kernels overlap on the GPU (different
  *     streams without ordering) race on it and produce wrong outputs.  Order
  *     such calls, or use oasis_sparse_decode_attn with separate workspaces.
+ *   - The array's address is cached per device for the life of the process.
+ *     cudaDeviceReset destroys the context that holds it, so the cached address
+ *     is stale afterwards: do not use this call in a process after a
+ *     cudaDeviceReset of that device (use oasis_sparse_decode_attn instead).
  */
 #define OASIS_ATTN_NOALLOC_MAX_WORKSPACE_BYTES (8u << 20)
 OASIS_API oasis_status oasis_sparse_decode_attn_noalloc(const oasis_shape* shape, const void* q,
@@ -483,6 +488,16 @@ OASIS_API oasis_status oasis_touch_host(const void* host_ptr, size_t bytes, uint
  * Unknown options or values return OASIS_ERR_INVALID.
  */
 #define OASIS_OPT_SCORE_CTAS_PER_SM 1
+/*
+ * OASIS_OPT_SCORE_KERNEL: which kernel oasis_score_blocks (and
+ *   oasis_score_blocks_copy) launches: OASIS_SCORE_KERNEL_MMA (mma.sync, the
+ *   default) or OASIS_SCORE_KERNEL_TC (TMA + tcgen05 + TMEM).  Same definition and
+ *   bound; selection results do not depend on it.  Read at every scoring call
+ *   (an atomic load, no environment lookup).
+ */
+#define OASIS_OPT_SCORE_KERNEL 2
+#define OASIS_SCORE_KERNEL_MMA 0
+#define OASIS_SCORE_KERNEL_TC 1
 OASIS_API oasis_status oasis_set_option(int32_t option, int32_t value);
 
 /*

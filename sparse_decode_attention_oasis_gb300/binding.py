@@ -274,10 +274,14 @@ def oasis_touch_host(host_tensor, nbytes: Optional[int] = None, sink=None, strea
 
 
 OPT_SCORE_CTAS_PER_SM = 1
+OPT_SCORE_KERNEL = 2
+SCORE_KERNEL_MMA = 0
+SCORE_KERNEL_TC = 1
 
 
 def oasis_set_option(option: int, value: int):
-    """Process-wide launch option (OPT_SCORE_CTAS_PER_SM: scorer CTAs per SM, 0 = as many as fit)."""
+    """Process-wide launch option (OPT_SCORE_CTAS_PER_SM: scorer CTAs per SM, 0 = as many as
+    fit; OPT_SCORE_KERNEL: SCORE_KERNEL_MMA or SCORE_KERNEL_TC)."""
     _check("oasis_set_option", load().oasis_set_option(int(option), int(value)))
 
 

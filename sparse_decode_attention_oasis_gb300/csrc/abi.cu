@@ -86,13 +86,6 @@ oasis_status check_shape(const oasis_shape* sh, const char* fn, oasis::Shape* ou
 
 }  // namespace
 
-namespace oasis {
-static std::atomic<int> g_score_ctas_per_sm{0};
-int score_ctas_per_sm_option() { return g_score_ctas_per_sm.load(std::memory_order_relaxed); }
-// Record the message oasis_last_error() returns on this thread.
-void set_last_error(const std::string& msg) { g_last_error = msg; }
-}  // namespace oasis
-
 namespace {
 
 #define REQUIRE(cond, msg) \
@@ -100,18 +93,44 @@ namespace {
 
 }  // namespace
 
+namespace oasis {
+static std::atomic<int> g_score_ctas_per_sm{0};
+static std::atomic<int> g_score_kernel{0};  // 0: mma.sync scorer, 1: tcgen05/TMA scorer
+int score_ctas_per_sm_option() { return g_score_ctas_per_sm.load(std::memory_order_relaxed); }
+// Record the message oasis_last_error() returns on this thread.
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+
+// The shape checks of every call, for entry points defined in other files.
+oasis_status validate_shape(const oasis_shape* sh, const char* fn, Shape* out) { return check_shape(sh, fn, out); }
+
+// The argument checks of the attention call other than its workspace (shared by
+// oasis_sparse_decode_attn and its allocation-free variant, so the two accept
+// and reject exactly the same arguments with the same messages).
+oasis_status validate_attn_args(const char* fn, const void* q, const void* k_pool, const void* v_pool,
+                                const int32_t* sel, const int32_t* nsel, const int32_t* blk2slot,
+                                const int32_t* ctx_len, float scale, const float* out) {
+  REQUIRE(q && aligned(q, 16), "q must be a 16-byte aligned device pointer");
+  REQUIRE(k_pool && v_pool && aligned(k_pool, 16) && aligned(v_pool, 16),
+          "k_pool/v_pool must be 16-byte aligned device pointers");
+  REQUIRE(sel && nsel && blk2slot && ctx_len, "table pointers must be non-NULL");
+  REQUIRE(aligned(sel, 4) && aligned(nsel, 4) && aligned(blk2slot, 4) && aligned(ctx_len, 4),
+          "int32 arrays must be 4-byte aligned");
+  REQUIRE(out && aligned(out, 16), "out must be a 16-byte aligned device pointer");
+  REQUIRE(scale == scale && scale > 0.f, "scale must be a positive number");
+  return OASIS_OK;
+}
+}  // namespace oasis
+
 extern "C" {
 
 const char* oasis_version(void) { return "oasis-gb300 0.1 sm_103a"; }
 
 const char* oasis_last_error(void) { return g_last_error.c_str(); }
 
-// Scoring kernel: "mma" (mma.sync, registers only, default) or "tc" (TMA + tcgen05),
-// chosen by OASIS_SCORE_KERNEL; both implement the same definition and bound.
-static bool use_tc_scoring() {
-  const char* v = getenv("OASIS_SCORE_KERNEL");
-  return v && strcmp(v, "tc") == 0;
-}
+// Scoring kernel: mma.sync (registers only, the default) or TMA + tcgen05, chosen
+// by oasis_set_option(OASIS_OPT_SCORE_KERNEL, ...); both implement the same
+// definition and bound.
+static bool use_tc_scoring() { return oasis::g_score_kernel.load(std::memory_order_relaxed) == 1; }
 
 oasis_status oasis_score_blocks(const oasis_shape* shape, const void* k_hbm, const int32_t* ctx_len,
                                 const void* q_la, float* scores, uint32_t* err_word, oasis_stream_t stream) {
@@ -481,6 +500,12 @@ oasis_status oasis_set_option(int32_t option, int32_t value) {
     oasis::g_score_ctas_per_sm.store(value, std::memory_order_relaxed);
     return OASIS_OK;
   }
+  if (option == OASIS_OPT_SCORE_KERNEL) {
+    REQUIRE(value == OASIS_SCORE_KERNEL_MMA || value == OASIS_SCORE_KERNEL_TC,
+            "OASIS_OPT_SCORE_KERNEL takes OASIS_SCORE_KERNEL_MMA or OASIS_SCORE_KERNEL_TC");
+    oasis::g_score_kernel.store(value, std::memory_order_relaxed);
+    return OASIS_OK;
+  }
   return fail(OASIS_ERR_INVALID, fn, "unknown option");
 }
 
@@ -547,16 +572,10 @@ oasis_status oasis_sparse_decode_attn(const oasis_shape* shape, const void* q, c
   oasis::Shape s;
   oasis_status st = check_shape(shape, fn, &s);
   if (st != OASIS_OK) return st;
-  REQUIRE(q && aligned(q, 16), "q must be a 16-byte aligned device pointer");
-  REQUIRE(k_pool && v_pool && aligned(k_pool, 16) && aligned(v_pool, 16),
-          "k_pool/v_pool must be 16-byte aligned device pointers");
-  REQUIRE(sel && nsel && blk2slot && ctx_len, "table pointers must be non-NULL");
-  REQUIRE(aligned(sel, 4) && aligned(nsel, 4) && aligned(blk2slot, 4) && aligned(ctx_len, 4),
-          "int32 arrays must be 4-byte aligned");
-  REQUIRE(out && aligned(out, 16), "out must be a 16-byte aligned device pointer");
+  st = oasis::validate_attn_args(fn, q, k_pool, v_pool, sel, nsel, blk2slot, ctx_len, scale, out);
+  if (st != OASIS_OK) return st;
   REQUIRE(workspace && aligned(workspace, 16), "workspace must be a 16-byte aligned device pointer");
   REQUIRE(ws_bytes >= oasis::attn_workspace_bytes(s), "workspace is smaller than oasis_attn_workspace_bytes()");
-  REQUIRE(scale == scale && scale > 0.f, "scale must be a positive number");
   cudaError_t e = oasis::launch_sparse_decode_attn(s, static_cast<const uint16_t*>(q),
                                                    static_cast<const uint16_t*>(k_pool),
                                                    static_cast<const uint16_t*>(v_pool), sel, nsel, blk2slot,

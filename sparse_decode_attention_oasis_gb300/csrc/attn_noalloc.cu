@@ -18,6 +18,9 @@ cudaError_t launch_sparse_decode_attn(const Shape&, const uint16_t*, const uint1
                                       cudaStream_t);
 size_t attn_workspace_bytes(const Shape&);
 void set_last_error(const std::string&);
+oasis_status validate_shape(const oasis_shape*, const char*, Shape*);
+oasis_status validate_attn_args(const char*, const void*, const void*, const void*, const int32_t*, const int32_t*,
+                                const int32_t*, const int32_t*, float, const float*);
 }  // namespace oasis
 
 namespace {
@@ -49,8 +52,6 @@ cudaError_t scratch_for_current_device(void** out) {
   return cudaSuccess;
 }
 
-bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
 oasis_status fail(oasis_status st, const std::string& msg) {
   oasis::set_last_error("oasis_sparse_decode_attn_noalloc: " + msg);
   return st;
@@ -64,26 +65,19 @@ OASIS_API oasis_status oasis_sparse_decode_attn_noalloc(const oasis_shape* shape
                                                         const void* v_pool, const int32_t* sel, const int32_t* nsel,
                                                         const int32_t* blk2slot, const int32_t* ctx_len, float scale,
                                                         float* out, oasis_stream_t stream) {
-  if (!shape) return fail(OASIS_ERR_INVALID, "shape is NULL");
-  const oasis_shape& sh = *shape;
-  if (sh.B < 1 || sh.Hq < 1 || sh.Hkv < 1 || sh.nb_max < 1 || sh.n_la < 1 || sh.Kb < 1 || sh.P < 1 ||
-      sh.Hq % sh.Hkv)
-    return fail(OASIS_ERR_INVALID, "invalid shape");
-  const int G = sh.Hq / sh.Hkv;
-  if (sh.d != 128 || sh.bs != 16 || (G != 1 && G != 2 && G != 4 && G != 8) || sh.Kb > 256 || sh.P < sh.Kb ||
-      sh.P > 1024 || sh.nb_max > 8192 || (long long)sh.B * sh.Hkv > 65535)
-    return fail(OASIS_ERR_UNSUPPORTED, "shape outside the supported range");
-  const oasis::Shape s{sh.B, sh.Hq, sh.Hkv, sh.d, sh.bs, sh.nb_max, sh.n_la, sh.Kb, sh.P};
+  static const char* fn = "oasis_sparse_decode_attn_noalloc";
+  // the same shape and argument checks (and messages) as oasis_sparse_decode_attn
+  oasis::Shape s;
+  oasis_status st = oasis::validate_shape(shape, fn, &s);
+  if (st != OASIS_OK) return st;
+  st = oasis::validate_attn_args(fn, q, k_pool, v_pool, sel, nsel, blk2slot, ctx_len, scale, out);
+  if (st != OASIS_OK) return st;
   const size_t need = oasis::attn_workspace_bytes(s);
   if (need > kNoAllocWorkspaceBytes)
     return fail(OASIS_ERR_UNSUPPORTED, "this shape needs " + std::to_string(need) +
                                            " bytes of attention scratch, more than the built-in " +
                                            std::to_string(kNoAllocWorkspaceBytes) +
                                            " bytes; use oasis_sparse_decode_attn with a workspace");
-  if (!q || !aligned_to(q, 16) || !k_pool || !v_pool || !aligned_to(k_pool, 16) || !aligned_to(v_pool, 16) ||
-      !sel || !nsel || !blk2slot || !ctx_len || !out || !aligned_to(out, 16) || !aligned_to(sel, 4) ||
-      !aligned_to(nsel, 4) || !aligned_to(blk2slot, 4) || !aligned_to(ctx_len, 4) || !(scale > 0.f))
-    return fail(OASIS_ERR_INVALID, "bad pointer, alignment or scale");
   void* ws = nullptr;
   cudaError_t e = scratch_for_current_device(&ws);
   if (e == cudaSuccess)

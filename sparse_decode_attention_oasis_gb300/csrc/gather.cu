@@ -76,8 +76,12 @@ gather_h2d_kernel(Shape s, const uint16_t* __restrict__ host_kv, const int* __re
   if (nf < 0 || nf > Kb) { ew |= OASIS_EW_BAD_COUNT; nf = nf < 0 ? 0 : Kb; }
   if (threadIdx.x == 0) { scal[0] = 0; scal[1] = 0; }
   __syncthreads();
+  // An out-of-range entry of S is flagged but left in place: S is only searched
+  // (binary search for resident blocks, which lie in [0, nb_max)), and keeping
+  // the value keeps the list ascending, so it can never match or misplace a
+  // valid block.  A bad entry of F is cleared: F drives the copies.
   for (int i = threadIdx.x; i < Kb; i += blockDim.x) {
-    if (i < ns && (S[i] < 0 || S[i] >= s.nb_max)) { ew |= OASIS_EW_BAD_BLOCK; S[i] = -1; }
+    if (i < ns && (S[i] < 0 || S[i] >= s.nb_max)) ew |= OASIS_EW_BAD_BLOCK;
     if (i < nf && (F[i] < 0 || F[i] >= s.nb_max)) { ew |= OASIS_EW_BAD_BLOCK; F[i] = -1; }
   }
   for (int p = threadIdx.x; p < P; p += blockDim.x)

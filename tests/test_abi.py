@@ -109,6 +109,9 @@ def test_set_option_validates(lib):
     assert lib.oasis_set_option(1, -1) == 1
     assert lib.oasis_set_option(99, 0) == 1
     assert lib.oasis_set_option(1, 0) == 0
+    assert lib.oasis_set_option(2, 2) == 1        # OASIS_OPT_SCORE_KERNEL: only MMA (0) or TC (1)
+    assert lib.oasis_set_option(2, 1) == 0
+    assert lib.oasis_set_option(2, 0) == 0
 
 
 def _header_signatures():
@@ -146,3 +149,22 @@ def test_binding_signatures_match_the_header():
         assert len(argtypes) == len(params), (name, params)
         assert [_ctypes_kind(a) for a in argtypes] == [_c_kind(p) for p in params], name
         assert _ctypes_kind(restype) == _c_kind(ret), (name, ret)
+
+
+@pytest.mark.parametrize("kw,ptr,status", [
+    (dict(Hq=64, Hkv=8, n_la=5), 16, 4),   # n_la * G = 40 > 32
+    (dict(Hq=30), 16, 1), (dict(d=64), 16, 4), (dict(nb_max=9000), 16, 4),
+    ({}, 8, 1),                            # a q pointer that is not 16-byte aligned
+])
+def test_noalloc_attention_validates_like_the_workspace_call(lib, kw, ptr, status):
+    """Both attention entry points share their shape and argument checks: the same
+    status and message (after the function name) for every rejected call; nothing
+    is launched, so no GPU is needed."""
+    s = _shape(**kw)
+    a = lib.oasis_sparse_decode_attn(ctypes.byref(s), ptr, 16, 16, 16, 16, 16, 16, 0.1, 16, 1 << 30, 16, None)
+    ea = lib.oasis_last_error().decode()
+    b = lib.oasis_sparse_decode_attn_noalloc(ctypes.byref(s), ptr, 16, 16, 16, 16, 16, 16, 0.1, 16, None)
+    eb = lib.oasis_last_error().decode()
+    assert a == b == status
+    assert ea.startswith("oasis_sparse_decode_attn: ") and eb.startswith("oasis_sparse_decode_attn_noalloc: ")
+    assert ea.split(": ", 1)[1] == eb.split(": ", 1)[1]

@@ -125,6 +125,58 @@ def test_copy_reports_out_of_range_fetch_entry():
     assert torch.equal(st.k_pool, kp0) and torch.equal(st.v_pool, vp0)
 
 
+@pytest.mark.parametrize("call", ["gather", "assign"])
+def test_out_of_range_sel_entry_leaves_resident_selected_blocks_alone(call):
+    """An out-of-range last entry of S (still ascending) is flagged; every resident
+    block of S keeps its slot and its LRU clock, as the oracle gives for S without
+    that entry (the bad entry must not make a selected block a victim)."""
+    from sparse_decode_attention_oasis_gb300 import binding as B
+    from sparse_decode_attention_oasis_gb300.engine import DecodeState
+
+    w = syn.Workload("badsel", L=1, B=1, Hq=32, Hkv=8, ctx=[1024], Kb=16, C=4, n_hot=4)
+    st = DecodeState(w, l_phys=1)
+    K, V = syn.layer_kv(w, 0)
+    b2s, s2b, lu = [np.array(t) for t in syn.initial_tables(w, 0)]
+    rng = np.random.default_rng(5)
+    lu[...] = rng.integers(-1, 3, size=lu.shape).astype(np.int32)
+    st.fill_layer_numpy(0, K, V, b2s, s2b, lu)
+    sel = np.full((w.B, w.Hkv, w.Kb), -1, np.int32)
+    nsel = np.zeros((w.B, w.Hkv), np.int32)
+    fetch = np.full((w.B, w.Hkv, w.Kb), -1, np.int32)
+    nfetch = np.zeros((w.B, w.Hkv), np.int32)
+    want = {}
+    for h in range(w.Hkv):
+        res = sorted(int(x) for x in s2b[0, h] if x >= 0)
+        missing = sorted(set(range(w.nb(0))) - set(res))
+        # the 11 largest resident blocks (the end of S, where the bad entry sits) and 4 missing ones
+        S = sorted(res[-11:] + [int(x) for x in rng.choice(missing, 4, replace=False)])
+        F = sorted(x for x in S if b2s[0, h, x] < 0)
+        bad = S + [w.nb_max + 3] if h % 2 == 0 else S   # half of the heads carry the bad entry
+        sel[0, h, :len(bad)] = bad
+        nsel[0, h] = len(bad)
+        fetch[0, h, :len(F)] = F
+        nfetch[0, h] = len(F)
+        want[h] = (S, F)
+    step = 7
+    for h, (S, F) in want.items():
+        ref.assign_slots(S, F, b2s[0, h], s2b[0, h], lu[0, h], step)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stepd = torch.full((1,), step, dtype=torch.int32, device="cuda")
+    s = st.shape
+    if call == "gather":
+        B.oasis_gather_h2d(s, st.host[0], dev(sel), dev(nsel), dev(fetch), dev(nfetch), st.blk2slot[0],
+                           st.slot2blk[0], st.last_used[0], stepd, st.k_pool[0], st.v_pool[0], err)
+    else:
+        B.oasis_assign_slots(s, dev(sel), dev(nsel), dev(fetch), dev(nfetch), st.blk2slot[0], st.slot2blk[0],
+                             st.last_used[0], stepd, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == B.EW_BAD_BLOCK
+    np.testing.assert_array_equal(st.blk2slot[0].cpu().numpy(), b2s)
+    np.testing.assert_array_equal(st.slot2blk[0].cpu().numpy(), s2b)
+    np.testing.assert_array_equal(st.last_used[0].cpu().numpy(), lu)
+
+
 def test_cross_step_pipeline_matches_oracle():
     """copy="lag": step 0 selects, gathers and attends; later steps attend the
     previous step's selection first (oracle prev_S), then select and gather."""

@@ -10,14 +10,22 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 
+def _use(kernel):
+    from sparse_decode_attention_oasis_gb300 import binding as B
+
+    B.oasis_set_option(B.OPT_SCORE_KERNEL, B.SCORE_KERNEL_TC if kernel == "tc" else B.SCORE_KERNEL_MMA)
+
+
 @pytest.fixture(autouse=True)
-def _tc_kernel(monkeypatch):
+def _tc_kernel():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from sparse_decode_attention_oasis_gb300 import build
 
     build.build()
-    monkeypatch.setenv("OASIS_SCORE_KERNEL", "tc")
+    _use("tc")
+    yield
+    _use("mma")  # the process-wide default for the tests that follow
 
 
 def test_tc_tiny_workload_two_steps():
@@ -34,12 +42,12 @@ def test_tc_shapes(Hq, n_la, ctx):
     c.step(0)
 
 
-def test_tc_matches_the_default_kernel_within_bounds(monkeypatch):
+def test_tc_matches_the_default_kernel_within_bounds():
     w = syn.Workload("cmp", L=1, B=2, Hq=32, Hkv=8, ctx=[4096, 2500], Kb=32, C=4, n_hot=16)
     c = Case(w)
     r, sc = c.step(0)
     tc_scores = sc.scores.cpu().numpy().copy()
-    monkeypatch.setenv("OASIS_SCORE_KERNEL", "mma")
+    _use("mma")
     c2 = Case(w)
     r2, sc2 = c2.step(0)
     mma_scores = sc2.scores.cpu().numpy()

@@ -78,3 +78,15 @@ def test_noalloc_rejects_shapes_beyond_its_array(lib):
     st = lib.load().oasis_sparse_decode_attn_noalloc(ctypes.byref(big), p, p, p, p, p, p, p, 0.1, p, None)
     assert st == 4
     assert "bytes" in lib.oasis_last_error()
+
+
+def test_noalloc_rejects_what_the_workspace_call_rejects(lib):
+    """n_la * G > 32 is outside the supported range for both attention calls."""
+    s = lib.Shape.of(B=2, Hq=64, Hkv=8, nb_max=256, n_la=5, Kb=32, P=32)
+    dummy = torch.empty(64, dtype=torch.float32, device="cuda")
+    p = dummy.data_ptr()
+    raw = lib.load()
+    a = raw.oasis_sparse_decode_attn(ctypes.byref(s), p, p, p, p, p, p, p, 0.1, p, 1 << 20, p, None)
+    b = raw.oasis_sparse_decode_attn_noalloc(ctypes.byref(s), p, p, p, p, p, p, p, 0.1, p, None)
+    assert a == b == 4
+    assert "n_la * G" in lib.oasis_last_error()
