@@ -271,6 +271,44 @@ OASIS_API oasis_status oasis_copy_fetched(const oasis_shape* shape, const void* 
                                           uint32_t* err_word, oasis_stream_t stream);
 
 /*
+ * oasis_copy_fetched_wait: oasis_copy_fetched that first waits, with a bounded
+ *   number of polls, for a host-written ready flag.  A host-side producer that
+ *   fills the host tier (a slower tier, a remote fetch, the compensating fetch
+ *   after a misprediction that the limitations list on the metalmedia.ai page
+ *   mentions) writes the data, then sets *ready_flag >= ready_value; the copy
+ *   reads the blocks only after it sees that.  Each thread block polls the flag
+ *   (relaxed system-scope loads about 256 ns apart) at most max_polls times;
+ *   if the flag is still below ready_value it sets OASIS_EW_TIMEOUT in err_word
+ *   and copies nothing, so no kernel is left waiting whatever the host does.
+ *   The pools' slots of F then keep their old contents (the table half has
+ *   already mapped them): the caller must not attend them before a copy
+ *   succeeds.  The call itself returns OASIS_OK once enqueued; read the outcome
+ *   with oasis_error_word_status.
+ * Arguments: as oasis_copy_fetched, plus
+ *   ready_flag   uint32 in page-locked, device-mapped host memory (cudaHostAlloc
+ *                mapped / cudaHostRegister mapped), 4-byte aligned
+ *   ready_value  the copy proceeds once *ready_flag >= ready_value
+ *   max_polls    1 .. OASIS_MAX_READY_POLLS (about max_polls x 0.25-0.5 us)
+ */
+#define OASIS_MAX_READY_POLLS (1 << 22)
+OASIS_API oasis_status oasis_copy_fetched_wait(const oasis_shape* shape, const void* host_kv,
+                                               const int32_t* fetch, const int32_t* nfetch,
+                                               const int32_t* blk2slot, void* k_pool, void* v_pool,
+                                               const uint32_t* ready_flag, uint32_t ready_value,
+                                               int32_t max_polls, uint32_t* err_word,
+                                               oasis_stream_t stream);
+
+/*
+ * oasis_error_word_status: waits for `stream` (cudaStreamSynchronize), reads the
+ *   device error word and returns OASIS_ERR_TIMEOUT if OASIS_EW_TIMEOUT is set
+ *   (a bounded wait gave up), else OASIS_OK; *bits (may be NULL) receives the
+ *   whole word.  A blocking call: use it outside the decode loop's hot path or
+ *   after a step, not between the launches of one.
+ */
+OASIS_API oasis_status oasis_error_word_status(const uint32_t* err_word, oasis_stream_t stream,
+                                               uint32_t* bits);
+
+/*
  * oasis_score_blocks_copy: oasis_score_blocks of one layer and
  *   oasis_copy_fetched of another (the copy arguments may belong to any layer
  *   of the same shape; they must not alias k_hbm, q_la or scores) in one launch.

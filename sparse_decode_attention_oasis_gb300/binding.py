@@ -59,6 +59,9 @@ _SIGS = {
     "oasis_assign_slots": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP],
                            ctypes.c_int),
     "oasis_copy_fetched": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
+    "oasis_copy_fetched_wait": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_uint32,
+                                 ctypes.c_int32, _VP, _VP], ctypes.c_int),
+    "oasis_error_word_status": ([_VP, _VP, _VP], ctypes.c_int),
     "oasis_score_blocks_copy": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                  _VP, _VP, _VP], ctypes.c_int),
     "oasis_set_agreement": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
@@ -185,6 +188,23 @@ def oasis_copy_fetched(shape: Shape, host_kv, fetch, nfetch, blk2slot, k_pool, v
     _check("oasis_copy_fetched", load().oasis_copy_fetched(
         ctypes.byref(shape), _ptr(host_kv), _ptr(fetch), _ptr(nfetch), _ptr(blk2slot), _ptr(k_pool),
         _ptr(v_pool), _ptr(err_word), _stream(stream)))
+
+
+def oasis_copy_fetched_wait(shape: Shape, host_kv, fetch, nfetch, blk2slot, k_pool, v_pool, ready_flag,
+                            ready_value: int, max_polls: int, err_word, stream=None):
+    """oasis_copy_fetched after a bounded wait for *ready_flag >= ready_value (a uint32 in
+    page-locked mapped host memory); on expiry nothing is copied and err_word gets EW_TIMEOUT."""
+    _check("oasis_copy_fetched_wait", load().oasis_copy_fetched_wait(
+        ctypes.byref(shape), _ptr(host_kv), _ptr(fetch), _ptr(nfetch), _ptr(blk2slot), _ptr(k_pool),
+        _ptr(v_pool), _ptr(ready_flag), int(ready_value), int(max_polls), _ptr(err_word), _stream(stream)))
+
+
+def oasis_error_word_status(err_word, stream=None):
+    """(status, bits): waits for the stream and reads the error word; status is
+    ERR_TIMEOUT (3) when a bounded wait gave up, else OK (0).  Does not raise."""
+    bits = ctypes.c_uint32(0)
+    st = load().oasis_error_word_status(_ptr(err_word), _stream(stream), ctypes.byref(bits))
+    return int(st), int(bits.value)
 
 
 def oasis_score_blocks_copy(shape: Shape, k_hbm, ctx_len, q_la, scores, host_kv, fetch, nfetch,

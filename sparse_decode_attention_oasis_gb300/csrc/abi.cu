@@ -24,6 +24,7 @@ size_t attn_workspace_bytes(const Shape&);
 cudaError_t launch_assign_slots(const Shape&, const int*, const int*, const int*, const int*, int*, int*, int*,
                                 const int*, unsigned*, cudaStream_t);
 cudaError_t launch_copy_fetched(const Shape&, const CopyJob&, cudaStream_t);
+cudaError_t launch_copy_fetched_wait(const Shape&, const CopyJob&, const unsigned*, unsigned, int, cudaStream_t);
 cudaError_t launch_score_blocks_copy(const Shape&, const uint16_t*, const int*, const uint16_t*, float2*,
                                      const CopyJob&, cudaStream_t);
 cudaError_t launch_set_agreement(const Shape&, const int*, const int*, const int*, const int*, const int*, int*,
@@ -288,6 +289,39 @@ oasis_status oasis_copy_fetched(const oasis_shape* shape, const void* host_kv, c
   if (st != OASIS_OK) return st;
   cudaError_t e = oasis::launch_copy_fetched(s, job, (cudaStream_t)stream);
   return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
+}
+
+oasis_status oasis_copy_fetched_wait(const oasis_shape* shape, const void* host_kv, const int32_t* fetch,
+                                     const int32_t* nfetch, const int32_t* blk2slot, void* k_pool, void* v_pool,
+                                     const uint32_t* ready_flag, uint32_t ready_value, int32_t max_polls,
+                                     uint32_t* err_word, oasis_stream_t stream) {
+  static const char* fn = "oasis_copy_fetched_wait";
+  oasis::Shape s;
+  oasis_status st = check_shape(shape, fn, &s);
+  if (st != OASIS_OK) return st;
+  oasis::CopyJob job;
+  st = make_copy_job(fn, host_kv, fetch, nfetch, blk2slot, k_pool, v_pool, err_word, &job);
+  if (st != OASIS_OK) return st;
+  REQUIRE(ready_flag && aligned(ready_flag, 4), "ready_flag must be a 4-byte aligned pointer");
+  REQUIRE(max_polls >= 1 && max_polls <= OASIS_MAX_READY_POLLS, "max_polls must be in [1, OASIS_MAX_READY_POLLS]");
+  void* dev_flag = mapped_host_ptr(ready_flag);
+  REQUIRE(dev_flag, "ready_flag must be in page-locked, device-mapped host memory");
+  cudaError_t e = oasis::launch_copy_fetched_wait(s, job, static_cast<const unsigned*>(dev_flag), ready_value,
+                                                  max_polls, (cudaStream_t)stream);
+  return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
+}
+
+oasis_status oasis_error_word_status(const uint32_t* err_word, oasis_stream_t stream, uint32_t* bits) {
+  static const char* fn = "oasis_error_word_status";
+  REQUIRE(err_word && aligned(err_word, 4), "err_word must be a 4-byte aligned device pointer");
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(fn, e);
+  uint32_t v = 0;
+  e = cudaMemcpy(&v, err_word, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(fn, e);
+  if (bits) *bits = v;
+  if (v & OASIS_EW_TIMEOUT) return fail(OASIS_ERR_TIMEOUT, fn, "a bounded wait on a host flag gave up");
+  return OASIS_OK;
 }
 
 oasis_status oasis_score_blocks_copy(const oasis_shape* shape, const void* k_hbm, const int32_t* ctx_len,

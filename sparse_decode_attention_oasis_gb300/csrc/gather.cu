@@ -258,8 +258,52 @@ cudaError_t launch_assign_slots(const Shape& s, const int* sel, const int* nsel,
 // The data half on its own: warps of 4-warp CTAs, 8 KiB of staging per warp.
 constexpr int kCopyWarps = 4;
 
-__global__ void __launch_bounds__(kCopyWarps * 32) copy_fetched_kernel(Shape s, CopyJob job) {
+// A host-written ready flag that a copy may wait for (the host tier of a layer
+// being filled by a host-side producer).  `flag` is the device address of a
+// word of page-locked mapped host memory; the wait ends when *flag >= `value`
+// or after `max_polls` polls.
+struct ReadyWait {
+  const unsigned* flag;
+  unsigned value;
+  int max_polls;
+};
+
+// Relaxed system-scope load: sees the host's write to mapped memory.
+__device__ __forceinline__ unsigned ld_relaxed_sys(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Thread 0 of the CTA polls the flag (bounded by max_polls, 256 ns apart); the
+// CTA learns the outcome through shared memory.  False: the wait gave up, the
+// error word has OASIS_EW_TIMEOUT, and the CTA must not copy.
+__device__ __forceinline__ bool wait_ready(const ReadyWait& w, unsigned* err) {
+  __shared__ int ok;
+  if (threadIdx.x == 0) {
+    int polls = 0;
+    bool ready = ld_relaxed_sys(w.flag) >= w.value;
+    while (!ready && ++polls < w.max_polls) {
+      __nanosleep(256);
+      ready = ld_relaxed_sys(w.flag) >= w.value;
+    }
+    if (ready) {
+      __threadfence_system();  // the host data written before the flag is read after it
+    } else if (err) {
+      atomicOr(err, OASIS_EW_TIMEOUT);
+    }
+    ok = ready ? 1 : 0;
+  }
+  __syncthreads();
+  return ok != 0;
+}
+
+template <bool kWait>
+__global__ void __launch_bounds__(kCopyWarps * 32) copy_fetched_kernel(Shape s, CopyJob job, ReadyWait rw) {
   extern __shared__ uint4 copy_buf[];
+  if constexpr (kWait) {
+    if (!wait_ready(rw, job.err)) return;
+  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint4* buf = copy_buf + warp * (kCopyUnitBytes / 16);
   const long long gwarp = (long long)blockIdx.x * kCopyWarps + warp;
@@ -268,14 +312,26 @@ __global__ void __launch_bounds__(kCopyWarps * 32) copy_fetched_kernel(Shape s, 
   copy_finish(job, s, gwarp, nwarps, buf, lane);
 }
 
-cudaError_t launch_copy_fetched(const Shape& s, const CopyJob& job, cudaStream_t stream) {
+static int copy_grid(const Shape& s) {
   // one warp per live entry up to four CTAs per SM; a warp streams any further entries
   const long long items = (long long)s.B * s.Hkv * s.Kb;
   long long ctas = (items + kCopyWarps - 1) / kCopyWarps;
   const long long cap = 4LL * sm_count();
   if (ctas > cap) ctas = cap;
   if (ctas < 1) ctas = 1;
-  copy_fetched_kernel<<<(int)ctas, kCopyWarps * 32, kCopyWarps * kCopyUnitBytes, stream>>>(s, job);
+  return (int)ctas;
+}
+
+cudaError_t launch_copy_fetched(const Shape& s, const CopyJob& job, cudaStream_t stream) {
+  copy_fetched_kernel<false><<<copy_grid(s), kCopyWarps * 32, kCopyWarps * kCopyUnitBytes, stream>>>(
+      s, job, ReadyWait{nullptr, 0u, 0});
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_fetched_wait(const Shape& s, const CopyJob& job, const unsigned* flag, unsigned value,
+                                     int max_polls, cudaStream_t stream) {
+  copy_fetched_kernel<true><<<copy_grid(s), kCopyWarps * 32, kCopyWarps * kCopyUnitBytes, stream>>>(
+      s, job, ReadyWait{flag, value, max_polls});
   return cudaGetLastError();
 }
 

@@ -53,8 +53,14 @@ class Case:
             q, qla = syn.layer_queries(w, 0, step)
         if C is not None:
             w.C = C
-        r = ref.layer_step(self.K, qla, q, w.ctx, self.host, self.kp, self.vp, self.b2s, self.s2b,
-                           self.lu, w.Kb, w.C, step, bs=w.bs, scoring=self.scoring, lookahead_out=lookahead)
+        if w.B * w.Hkv >= 8 and w.nb_max >= 1024:  # large case: the oracle head by head in worker processes
+            import oracle_pool
+
+            r = oracle_pool.layer_step(self.K, qla, q, w.ctx, self.host, self.kp, self.vp, self.b2s, self.s2b,
+                                       self.lu, w.Kb, w.C, step, scoring=self.scoring, lookahead_out=lookahead)
+        else:
+            r = ref.layer_step(self.K, qla, q, w.ctx, self.host, self.kp, self.vp, self.b2s, self.s2b,
+                               self.lu, w.Kb, w.C, step, bs=w.bs, scoring=self.scoring, lookahead_out=lookahead)
         sc = self.st.layer_step(0, _dev_bits(qla), _dev_bits(q), step, gather=gather)
         torch.cuda.synchronize()
         self.compare(r, sc)

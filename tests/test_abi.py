@@ -128,7 +128,8 @@ def _header_signatures():
 def _ctypes_kind(t):
     if t is ctypes.c_void_p or t is ctypes.c_char_p or (isinstance(t, type) and issubclass(t, ctypes._Pointer)):
         return "pointer"
-    return {ctypes.c_int32: "int32", ctypes.c_int: "int32", ctypes.c_size_t: "size", ctypes.c_float: "float"}[t]
+    return {ctypes.c_int32: "int32", ctypes.c_int: "int32", ctypes.c_uint32: "int32", ctypes.c_size_t: "size",
+            ctypes.c_float: "float"}[t]
 
 
 def _c_kind(t):

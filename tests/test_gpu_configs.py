@@ -1,16 +1,12 @@
 """Parity on the shapes of the other workloads: long input (128K context, span and
 sink/recent hot blocks), GQA 8 with the fetch-ratio sweep, long output (growing
-context with token appends), and the full-size Qwen3-8B decode shape sampled
-head by head in the pipelined launch configuration the benchmark times."""
-import math
-
-import numpy as np
+context with token appends, the drifting hot set).  Whole full-size decode steps
+are in test_gpu_fullsize.py."""
 import pytest
 
-from oracle import oasis_ref as ref
 from sparse_decode_attention_oasis_gb300 import synthetic as syn
 
-from gpu_helpers import Case, _check_out, _dev_bits
+from gpu_helpers import Case
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -52,43 +48,24 @@ def test_long_output_growing_context_with_appends():
     assert w.ctx == [x + 6 for x in ctx]
 
 
-def test_full_size_qwen3_8b_sampled_heads_pipelined():
-    """36 layers x batch 32 x ctx 32K on the GPU; sampled (layer, request, head) against the oracle."""
-    from sparse_decode_attention_oasis_gb300.engine import DecodeState
-
-    w = syn.qwen3_8b_decode()
-    dev = torch.device("cuda", 0)
-    st = DecodeState(w, device=dev, l_phys=w.L, l_host=4)
-    st.fill_synthetic()
-    qs = [syn.QueryStream(w, l) for l in range(w.L)]
-    out = torch.empty((w.L, w.B, w.Hq, w.d), dtype=torch.float32, device=dev)
-    side = torch.cuda.Stream(dev)
-    rng = np.random.default_rng(11)
-    samples = [(int(rng.integers(0, 4)), int(rng.integers(w.B)), int(rng.integers(w.Hkv))) for _ in range(3)]
-    samples.append((3, w.B - 1, w.Hkv - 1))
-    oracle_state = {}
-    for (l, b, h) in samples:
-        K, V = syn.head_kv(w, l, b, h)
-        sub = syn.Workload("sub", L=1, B=1, Hq=w.G, Hkv=1, ctx=[w.ctx[b]], Kb=w.Kb, C=w.C, nb_max=w.nb_max)
-        host = syn.host_tier_from_kv(sub, K[None, None], V[None, None])
-        b2s, s2b, lu = [t[b:b + 1, h:h + 1].copy() for t in syn.initial_tables(w, l)]
-        kp, vp = syn.pools_from_tables(sub, host, s2b)
-        oracle_state[(l, b, h)] = (K[None, None], host, b2s, s2b, lu, kp, vp)
-    for step in range(2):
-        qla_l, q_l = [], []
-        for l in range(w.L):
-            qb, qlab = qs[l].next()
-            q_l.append(_dev_bits(qb))
-            qla_l.append(_dev_bits(qlab))
-        st.decode_step(step, qla_l, q_l, out_layers=out, side=side)
-        torch.cuda.synchronize()
-        assert int(st.scratch.err.item()) == 0 and int(st.scratch2.err.item()) == 0
-        for (l, b, h), (K, host, b2s, s2b, lu, kp, vp) in oracle_state.items():
-            qh, qlah = syn.head_queries(w, l, b, h, step)
-            r = ref.layer_step(K, qlah[None], qh[None], [w.ctx[b]], host, kp, vp, b2s, s2b, lu,
-                               w.Kb, w.C, step)
-            np.testing.assert_array_equal(st.blk2slot[l, b, h].cpu().numpy(), b2s[0, 0])
-            np.testing.assert_array_equal(st.slot2blk[l, b, h].cpu().numpy(), s2b[0, 0])
-            np.testing.assert_array_equal(st.last_used[l, b, h].cpu().numpy(), lu[0, 0])
-            got = out[l, b, h * w.G:(h + 1) * w.G].cpu().numpy().astype(np.float64)
-            _check_out(got, r["out"][0], f"layer {l} request {b} head {h} step {step}")
+@pytest.mark.parametrize("scoring", ["maxdot", "pooled"])
+def test_long_output_drifting_hot_set_batch2_ctx_8k_to_32k_with_appends(scoring):
+    """The long-output workload itself: contexts 8,192 and 32,512 tokens (nb_max
+    2,048), budget 128 blocks, cap 2, the hot set drifting through 256 planted
+    blocks per head, one token appended per request every step, eight steps,
+    everything compared with the oracle after every step."""
+    w = syn.long_output(B=2, L=1)
+    assert w.ctx == [8192, 32512] and w.hot_mode == "drift" and w.C == 2 and w.Kb == 128
+    c = Case(w, scoring=scoring)
+    fetched = 0
+    for step in range(8):
+        r, sc = c.step(step, append=True)
+        fetched += sum(len(f) for f in r["F"].values())
+    c.compare_caches()
+    if scoring == "pooled":
+        c.compare_pooled()
+    assert w.ctx == [8200, 32520]
+    assert fetched > 0
+    moved = sum(len(set(syn.hot_set(w, 0, b, h, 7)) - set(syn.hot_set(w, 0, b, h, 0)))
+                for b in range(w.B) for h in range(w.Hkv))
+    assert moved > 0

@@ -1,0 +1,134 @@
+"""The scorers' certified bound under inputs built to break it.
+
+Every block score the GPU writes is an approximation s~ with a bound e, and
+selection is exact only if |s~ - score| <= e holds for every block.  The bound
+models fp32 tensor-core accumulation of bf16 products; these tests feed the
+scorers rows that stress that model - dot products whose terms cancel almost
+completely, entries spread over 20 to 40 binades within one row, and 32 query
+rows per KV head (GQA 8 x 4 lookahead queries) - and check, for every block,
+the bound, then the selected and fetched blocks bit for bit against the oracle,
+for the max-dot scorer (both kernels) and the pooled scorer.
+"""
+import numpy as np
+import pytest
+
+from oracle import oasis_ref as ref
+from sparse_decode_attention_oasis_gb300 import synthetic as syn
+
+from gpu_helpers import _dev_bits
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_decode_attention_oasis_gb300 import build
+
+    build.build()
+
+
+def _bf16(x):
+    return syn.f32_to_bf16_bits(np.asarray(x, dtype=np.float32))
+
+
+def adversarial_inputs(seed, B, Hkv, G, n_la, ctx, d=128, spread=30):
+    """Keys [B][Hkv][T][d] and lookahead queries [B][n_la][Hq][d] (bf16 bits).
+
+    Queries: half of the rows have equal entries in each pair (2i, 2i+1), with
+    the pair's magnitude spread over `spread` binades; the other half are random
+    with the same spread.  Keys: the odd entry of each pair is minus the even one
+    plus a small residual (2^-10 of it), so against a paired query row the 64
+    pair sums cancel to a residue far below the sum of |products|; the pairs'
+    magnitudes are spread over `spread` binades within every row as well.
+    """
+    rng = np.random.default_rng(seed)
+    Hq = G * Hkv
+    T = max(ctx)
+    nb_max = -(-T // 16)
+    K = np.zeros((B, Hkv, nb_max * 16, d), np.uint16)
+    for b in range(B):
+        for h in range(Hkv):
+            mag = np.exp2(rng.uniform(-spread / 2, spread / 2, size=(ctx[b], d // 2)))
+            sgn = rng.choice([-1.0, 1.0], size=(ctx[b], d // 2))
+            even = sgn * mag * rng.uniform(1, 2, size=mag.shape)
+            odd = -even * (1 + rng.choice([-1, 1], size=mag.shape) * 2.0 ** -10)
+            rows = np.empty((ctx[b], d))
+            rows[:, 0::2], rows[:, 1::2] = even, odd
+            K[b, h, :ctx[b]] = _bf16(rows)
+    q = np.empty((B, n_la, Hq, d))
+    mag = np.exp2(rng.uniform(-spread / 2, spread / 2, size=(B, n_la, Hq, d // 2)))
+    paired = np.repeat(mag * rng.choice([-1.0, 1.0], size=mag.shape), 2, axis=-1)
+    free = np.exp2(rng.uniform(-spread / 2, spread / 2, size=q.shape)) * rng.choice([-1.0, 1.0], size=q.shape)
+    pick = (np.arange(Hq) % 2 == 0)[None, None, :, None]
+    q = np.where(pick, paired, free)
+    return K, _bf16(q)
+
+
+def _check(shape_w, K, qla, scoring, kernel="mma"):
+    from sparse_decode_attention_oasis_gb300 import binding as B
+    from sparse_decode_attention_oasis_gb300.engine import _bf16_from_bits
+
+    w = shape_w
+    s = B.Shape.from_workload(w)
+    dev = torch.device("cuda", 0)
+    Kd = _bf16_from_bits(K, dev)
+    qd = _dev_bits(qla)
+    ctx = torch.tensor(w.ctx, dtype=torch.int32, device=dev)
+    b2s = np.full((w.B, w.Hkv, w.nb_max), -1, np.int32)
+    rng = np.random.default_rng(1)
+    for b in range(w.B):
+        for h in range(w.Hkv):
+            res = rng.choice(w.nb(b), size=min(w.P, w.nb(b)) // 2, replace=False)
+            b2s[b, h, res] = np.arange(len(res))
+    b2sd = torch.from_numpy(b2s).to(dev)
+    scores = torch.zeros((w.B, w.Hkv, w.nb_max, 2), dtype=torch.float32, device=dev)
+    sel = torch.empty((w.B, w.Hkv, w.Kb), dtype=torch.int32, device=dev)
+    nsel = torch.empty((w.B, w.Hkv), dtype=torch.int32, device=dev)
+    fetch = torch.empty_like(sel)
+    nfetch = torch.empty_like(nsel)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    if scoring == "pooled":
+        Kp = torch.zeros((w.B, w.Hkv, w.nb_max, 2, w.d), dtype=torch.bfloat16, device=dev)
+        B.oasis_pool_keys(s, Kd, ctx, Kp)
+        B.oasis_score_blocks_pooled(s, Kp, ctx, qd, scores, err_word=err)
+        B.oasis_topk_select_diff_pooled(s, scores, Kp, qd, ctx, b2sd, w.C, sel, nsel, fetch, nfetch)
+        pooled = {(b, h): ref.pool_keys(K[b, h], w.ctx[b], w.nb_max) for b in range(w.B) for h in range(w.Hkv)}
+        want = ref.block_scores_pooled(pooled, qla, w.ctx, w.d)
+    else:
+        B.oasis_set_option(B.OPT_SCORE_KERNEL, B.SCORE_KERNEL_TC if kernel == "tc" else B.SCORE_KERNEL_MMA)
+        try:
+            B.oasis_score_blocks(s, Kd, ctx, qd, scores, err)
+            B.oasis_topk_select_diff(s, scores, Kd, qd, ctx, b2sd, w.C, sel, nsel, fetch, nfetch)
+            torch.cuda.synchronize()
+        finally:
+            B.oasis_set_option(B.OPT_SCORE_KERNEL, B.SCORE_KERNEL_MMA)
+        want = ref.block_scores(K, qla, w.ctx)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    sc, sl, ns = scores.cpu().numpy().astype(np.float64), sel.cpu().numpy(), nsel.cpu().numpy()
+    fe, nf = fetch.cpu().numpy(), nfetch.cpu().numpy()
+    worst = 0.0
+    for (b, h), (exact, key) in want.items():
+        nb = w.nb(b)
+        approx, bound = sc[b, h, :nb, 0], sc[b, h, :nb, 1]
+        gap = np.abs(approx - exact)
+        assert (gap <= bound).all(), f"score outside its bound at {(b, h)}: worst {np.max(gap / bound):.3g} x e"
+        worst = max(worst, float(np.max(gap / np.maximum(bound, 1e-300))))
+        S = ref.topk_select(key, w.Kb)
+        F = ref.fetch_diff_capped(S, b2s[b, h], w.C, key)
+        assert ns[b, h] == len(S) and sl[b, h, :len(S)].tolist() == S, (b, h)
+        assert nf[b, h] == len(F) and fe[b, h, :len(F)].tolist() == F, (b, h)
+    return worst
+
+
+@pytest.mark.parametrize("scoring,kernel", [("maxdot", "mma"), ("maxdot", "tc"), ("pooled", "mma")])
+@pytest.mark.parametrize("spread", [20, 40])
+def test_cancellation_and_exponent_spread_with_32_query_rows(scoring, kernel, spread):
+    w = syn.Workload("adv", L=1, B=1, Hq=16, Hkv=2, ctx=[64 * 16 - 5], Kb=16, C=4, n_hot=0, n_la=4, P=16)
+    assert w.n_la * w.G == 32
+    K, qla = adversarial_inputs(7 + spread, w.B, w.Hkv, w.G, w.n_la, w.ctx, spread=spread)
+    worst = _check(w, K, qla, scoring, kernel)
+    assert worst <= 1.0
