@@ -112,6 +112,12 @@ def parse():
     ap.add_argument("--no-hostlink", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-worker", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--ref-pairs", type=int, default=1,
+                    help="(request, KV head) pairs the reference arm times per step")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip the short measurements of the other synthetic configurations")
+    ap.add_argument("--no-host-fit", action="store_true",
+                    help="skip the headline re-measured with as many host-tier layers as fit")
     ap.add_argument("--cpu-heads", type=int, default=12,
                     help="(request, KV head) pairs the CPU baseline times (about 0.3 s each on the Qwen3-8B decode shape)")
     return ap.parse_args()
@@ -139,11 +145,30 @@ def l2_note(w, scoring) -> str:
     return f"inputs {rel} L2 ({nbytes / 2 ** 30:.2f} GiB of {what} per layer)"
 
 
+def planned_layers(args, w):
+    """(HBM layers, host-tier layers) the GPU arm plans for the workload (layer l uses
+    HBM buffer l mod the first and host buffer l mod the second)."""
+    l_phys = args.phys_layers or (min(12, w.L) if w.name == "long_output" else w.L)
+    return l_phys, min(host_layers_for(w, args.host_layers), l_phys)
+
+
+def config_dict(args, w, l_phys, l_host, score_ctas, world=1):
+    """The `config` of the JSON line; the reference arm reports the same one."""
+    return {"workload": workload_desc(w), "l2": l2_note(w, args.scoring),
+            "scoring": args.scoring, "copy": args.copy, "score_ctas_per_sm": score_ctas,
+            "host_tier_layers": l_host, "host_tier_aliased": l_host < w.L,
+            "hbm_layers": l_phys, "hbm_layers_aliased": l_phys < w.L,
+            "host_alloc": args.host_alloc,
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def workload_desc(w) -> str:
     ctx = f"{w.ctx[0]}" if min(w.ctx) == max(w.ctx) else f"{min(w.ctx)}-{max(w.ctx)} (+1 token per step)"
+    hot = (f"{w.n_hot}-block hot set drifting through {w.n_pool} planted blocks/head (AR(1) rho_u {w.rho_u})"
+           if w.hot_mode == "drift" else f"{w.n_hot} planted hot blocks/head")
     return (f"{w.name}: {w.L} layers, batch {w.B}, {w.Hq}/{w.Hkv} heads, d {w.d}, bf16, ctx {ctx}, "
             f"block {w.bs}, budget {w.Kb * w.bs} tokens ({w.Kb} blocks), {w.n_la} lookahead queries, "
-            f"fetch cap {w.C} blocks/head/step, {w.n_hot} planted hot blocks/head")
+            f"fetch cap {w.C} blocks/head/step, {hot}")
 
 
 # --------------------------------------------------------------------------- CPU oracle timing
@@ -518,28 +543,43 @@ def measure_hostlink(st, qla0, dev):
 
 # --------------------------------------------------------------------------- reference arm
 def run_reference(args, rank):
+    """The CPU oracle as the reference arm: each timed step runs one full oracle
+    layer-step on `--ref-pairs` sampled (request, KV head) pairs of layer 0; the
+    layer-steps/s of the whole workload is extrapolated from the time per pair."""
     if rank != 0:
         return
     w = workload(args)
+    pairs = max(1, args.ref_pairs)
     per_step = []
+    t_all = time.perf_counter()
     for s in range(args.warmup + args.steps):
-        t = cpu_sample(args, 1, step=s)
+        t = cpu_sample(args, pairs, step=s)
         if s >= args.warmup:
-            per_step.append(t)
-    sec_per_head = sum(per_step) / len(per_step)
+            per_step.append(t * pairs)
+    wall = time.perf_counter() - t_all
+    sec_per_head = sum(per_step) / (len(per_step) * pairs)
     value = 1.0 / (sec_per_head * w.B * w.Hkv)
     try:
         cores = int(os.environ.get("OPENBLAS_NUM_THREADS", ""))
     except ValueError:
         cores = os.cpu_count() or 1
+    l_phys, l_host = planned_layers(args, w)
+    score_ctas = args.score_ctas if args.score_ctas >= 0 else (2 if args.copy == "pipe" else 0)
+    heads = w.B * w.Hkv
     line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": 0,
             "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1000.0 * w.L / value, "higher_is_better": True, "scaling": "weak",
+            # the time each timed step actually took (the sample), not the extrapolation
+            "ms_per_step": 1000.0 * sum(per_step) / len(per_step),
+            "extrapolated": True, "pairs_per_step": pairs, "pairs_timed": pairs * args.steps,
+            "ms_per_step_extrapolated": 1000.0 * w.L / value,
+            "run_wall_s": round(wall, 2),
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_desc(w)},
+            "config": config_dict(args, w, l_phys, l_host, score_ctas),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": "one (request, KV head) pair of layer 0 per step, scaled to a "
-                                       f"full layer-step ({w.B * w.Hkv} heads); cores = BLAS threads"},
+                             "sample": f"{pairs} (request, KV head) pair(s) of layer 0 per timed step, one full "
+                                       f"oracle layer-step each; layer-steps/s extrapolated from the time per pair "
+                                       f"x {heads} pairs per layer-step; cores = BLAS threads"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -572,6 +612,234 @@ def launches_per_step(st, copy):
     return st.w.L * per_layer + (1 if copy == "carry" else 0)
 
 
+def make_state(args, w, dev, l_phys, l_host, scoring="maxdot"):
+    """A filled, warmed DecodeState; the host tier shrinks if page-locked memory runs out."""
+    import torch
+
+    from sparse_decode_attention_oasis_gb300.engine import DecodeState
+
+    while True:
+        try:
+            st = DecodeState(w, device=dev, l_phys=l_phys, l_host=l_host, scoring=scoring,
+                             host_alloc=args.host_alloc)
+            break
+        except RuntimeError:
+            if l_host <= 2:
+                raise
+            l_host = max(2, l_host // 2)
+            torch.cuda.empty_cache()
+    st.fill_synthetic()
+    st.warm_host_tier()
+    return st
+
+
+def device_queries(w, dev, nsteps):
+    """q [n][L][B][Hq][d] and q_la [n][L][B][n_la][Hq][d] (bf16, device) of decode steps 0..n-1."""
+    import torch
+
+    from sparse_decode_attention_oasis_gb300 import synthetic as syn
+
+    qs = [syn.QueryStreamTorch(w, l, dev) for l in range(w.L)]
+    q_dev = torch.empty((nsteps, w.L, w.B, w.Hq, w.d), dtype=torch.bfloat16, device=dev)
+    qla_dev = torch.empty((nsteps, w.L, w.B, w.n_la, w.Hq, w.d), dtype=torch.bfloat16, device=dev)
+    for s_ in range(nsteps):
+        for l in range(w.L):
+            qb, qlab = qs[l].next()
+            q_dev[s_, l].copy_(qb)
+            qla_dev[s_, l].copy_(qlab)
+    return q_dev, qla_dev
+
+
+def token_appends(w, dev, n=16):
+    """(k_new, v_new) pairs, bf16 [L][B][Hkv][d], for workloads whose context grows."""
+    import torch
+
+    if w.name != "long_output":
+        return None
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    k_app = torch.randn((n, w.L, w.B, w.Hkv, w.d), generator=gen, device=dev).to(torch.bfloat16)
+    v_app = torch.randn((n, w.L, w.B, w.Hkv, w.d), generator=gen, device=dev).to(torch.bfloat16)
+    return [(k_app[i], v_app[i]) for i in range(n)]
+
+
+def exact_topk_turnover(st, q_steps, K=64, layer=0):
+    """Mean fraction of the exact top-K blocks of the true queries (the a1 score of
+    the true query, then top-K) that change from one decode step to the next, over
+    all heads of `layer`; q_steps: that layer's true queries of consecutive steps."""
+    import torch
+
+    from sparse_decode_attention_oasis_gb300 import binding as B
+    from sparse_decode_attention_oasis_gb300.engine import AgreementProbe
+
+    probe = AgreementProbe(st, K=K)
+    prev, tos = None, []
+    counts = torch.empty((st.shape.B, st.shape.Hkv, 3), dtype=torch.int32, device=st.device)
+    for q in q_steps:
+        probe._topk(probe.shape1, layer, q, "exact", torch.cuda.current_stream(st.device))
+        cur = (probe.sel["exact"].clone(), probe.nsel["exact"].clone())
+        if prev is not None:
+            B.oasis_set_agreement(probe.shape, cur[0], cur[1], prev[0], prev[1], None, counts, probe.err)
+            c = counts.sum(dim=(0, 1)).tolist()
+            tos.append(1.0 - c[0] / c[2])
+        prev = cur
+    torch.cuda.synchronize(st.device)
+    return sum(tos) / len(tos) if tos else None
+
+
+def light_measure(args, st, q_dev, qla_dev, start, preroll, steps, appends, world, dev):
+    """Eager pre-roll steps, then `steps` timed steps as one graph (event nodes around
+    the scorer), then two eager steps that count attended and fetched blocks."""
+    import torch
+
+    w = st.w
+    L = w.L
+    main = torch.cuda.current_stream(dev)
+    n_in = q_dev.shape[0]
+
+    def eager(s_, **kw):
+        if appends is not None:
+            st.append_step(*appends[s_ % len(appends)], stream=main)
+        k = s_ % n_in
+        st.decode_step(s_, qla_dev[k], q_dev[k], main=main, side=main, copy=args.copy, **kw)
+
+    for k in range(preroll):
+        eager(start + k)
+    torch.cuda.synchronize()
+    first = start + preroll
+    marks = GraphEvents(L * steps * 2 + 16)
+    ts_first = first % n_in
+    if ts_first + steps > n_in:
+        ts_first = 0
+    # the graph's LRU clock starts at `first`; its inputs are steps ts_first.. of the query buffers
+    ms, clk = _timed_graph_at(st, first, ts_first, q_dev, qla_dev, steps, args.copy, appends, world, dev, marks)
+    score_ms = marks.durations()["score"]
+    marks.close()
+    attended = torch.zeros((), dtype=torch.int64, device=dev)
+    fetched = torch.zeros((), dtype=torch.int64, device=dev)
+    nxt = first + steps
+    for k in range(2):
+        eager(nxt + k, count=attended, fetched=fetched)
+    torch.cuda.synchronize()
+    err = st.error_word()
+    att = float(attended.item()) / (2 * L * w.B * w.Hkv)
+    fetched_step = float(fetched.item()) / 2 * 2 * w.bs * w.d * 2
+    ab = algorithmic_bytes(w, att, st.scoring)
+    peak = measured_peaks()[0]
+    path = ab["total"] * L * steps / (ms / 1000.0) / 1e9
+    sc_avg = sum(score_ms) / len(score_ms)
+    return {"value": aggregate_value(world, L, steps, ms), "unit": UNIT, "steps": steps,
+            "ms_per_step": ms / steps, "path_hbm_gbs": path, "path_hbm_frac": path / peak,
+            "scorer_us": round(1000.0 * sc_avg, 2),
+            "scorer_frac": ab["score"] / (sc_avg / 1000.0) / 1e9 / peak,
+            "attended_blocks_per_head": round(att, 2), "fetched_bytes_per_step": int(fetched_step),
+            "fetched_gbs": fetched_step / (ms / steps / 1000.0) / 1e9,
+            "clocks": clk, "device_error_word": err}, nxt + 2
+
+
+def _timed_graph_at(st, lru_first, in_first, q_dev, qla_dev, steps, copy, appends, world, dev, marks):
+    import torch
+
+    from sparse_decode_attention_oasis_gb300.engine import StepGraph
+
+    ts = range(in_first, in_first + steps)
+    outs = [torch.empty((st.w.L, st.w.B, st.w.Hq, st.w.d), dtype=torch.float32, device=dev) for _ in range(2)]
+    app = None if appends is None else [appends[s_ % len(appends)] for s_ in ts]
+    g = StepGraph(st, lru_first, [qla_dev[s_] for s_ in ts], [q_dev[s_] for s_ in ts],
+                  [outs[k % 2] for k in range(steps)], mark=marks, copy=copy, appends=app)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index or 0)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.2)
+    with torch.cuda.stream(g.stream):
+        e0.record(g.stream)
+        g.replay()
+        e1.record(g.stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    del g
+    return reduce_max(e0.elapsed_time(e1), world, dev), clk
+
+
+def measure_other_configs(args, dev, world):
+    """Short measurements of the other synthetic configurations, each on its own state
+    (layers aliased in HBM and in the host tier to bound set-up time; every aliased
+    buffer is far larger than L2): Llama-3.1-8B 128K, the Qwen3-32B fetch-ratio sweep
+    and long-output decode with its drifting hot set."""
+    import gc
+
+    import torch
+
+    from sparse_decode_attention_oasis_gb300 import synthetic as syn
+
+    out = {}
+    steps, pre = 8, 8
+    plans = [("llama31_8b_long", syn.llama31_8b_long(), 8, 4, None),
+             ("qwen3_32b_ratio_sweep", syn.qwen3_32b(ratio=0.01), 8, 4, [0.01, 0.02, 0.05, 0.10, 0.20, None]),
+             ("long_output", syn.long_output(), 6, 4, None)]
+    for name, w, l_phys, l_host, ratios in plans:
+        t0 = time.time()
+        try:
+            st = make_state(args, w, dev, l_phys, min(l_host, l_phys))
+            n_in = pre + steps + 2
+            q_dev, qla_dev = device_queries(w, dev, n_in)
+            appends = token_appends(w, dev)
+            entry = {"workload": workload_desc(w), "hbm_layers": st.L_phys, "host_tier_layers": st.L_host,
+                     "aliased": True, "setup_s": round(time.time() - t0, 1)}
+            if name == "long_output":
+                heads = [(b, h) for b in range(0, w.B, 8) for h in range(w.Hkv)]
+                entry["hot_set_turnover"] = round(syn.hot_set_turnover(w, 0, 64, heads=heads), 4)
+                entry["exact_top64_turnover"] = round(
+                    exact_topk_turnover(st, [q_dev[k, 0] for k in range(8)], K=64), 4)
+            runs = {}
+            s0 = 0
+            for ratio in (ratios or ["cfg"]):
+                if ratio != "cfg":
+                    w.C = syn.fetch_cap_from_ratio(ratio, w.Kb)
+                key = "cfg" if ratio == "cfg" else ("fetch_all" if ratio is None else f"ratio_{ratio}")
+                r, s0 = light_measure(args, st, q_dev, qla_dev, s0, pre, steps, appends, world, dev)
+                r["fetch_cap"] = w.C
+                runs[key] = r
+            entry.update(runs["cfg"] if list(runs) == ["cfg"] else {"ratios": runs})
+            out[name] = entry
+        except Exception as e:  # one configuration failing does not lose the others
+            out[name] = {"unavailable": f"{type(e).__name__}: {str(e)[-300:]}"}
+        finally:
+            st = q_dev = qla_dev = appends = None
+            gc.collect()
+            torch.cuda.empty_cache()
+            empty = getattr(torch._C, "_host_emptyCache", None)
+            if empty is not None:
+                empty()
+    return out
+
+
+def measure_host_fit(args, st, q_dev, qla_dev, start, world, dev):
+    """The headline workload again with as many host-tier layers as 60% of the
+    available host memory holds (less aliasing of host data, more page-locked memory)."""
+    fit = host_layers_for(st.w, 0)
+    if fit <= st.L_host:
+        return {"host_tier_layers": st.L_host, "skipped": "no more host layers fit than the headline uses"}
+    t0 = time.time()
+    while True:
+        try:
+            st.rebuild_host_tier(fit)
+            break
+        except RuntimeError:
+            if fit <= st.L_host:
+                raise
+            fit = max(st.L_host, fit * 3 // 4)
+    rebuild = time.time() - t0
+    t1 = time.time()
+    st.warm_host_tier()
+    warm = time.time() - t1
+    r, _ = light_measure(args, st, q_dev, qla_dev, start, 8, args.steps, None, world, dev)
+    r.update({"host_tier_layers": st.L_host, "host_tier_aliased": st.L_host < st.w.L,
+              "rebuild_s": round(rebuild, 1), "host_tier_warm_s": round(warm, 2)})
+    return r
+
+
 def run_gpu(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -590,8 +858,7 @@ def run_gpu(args, rank, world, local_rank):
         torch.distributed.barrier()
     w = workload(args)
     L = w.L
-    l_phys = args.phys_layers or (min(12, L) if args.workload == "long_output" else L)
-    l_host = min(host_layers_for(w, args.host_layers), l_phys)
+    l_phys, l_host = planned_layers(args, w)
     t0 = time.time()
     while True:
         try:
@@ -815,8 +1082,11 @@ def run_gpu(args, rank, world, local_rank):
         pab = algorithmic_bytes(w, attended_per_head, "pooled")
         pavg = sum(pscore) / len(pscore)
         pach = pab["score"] / (pavg / 1000.0) / 1e9
+        ppath = pab["total"] * L * args.steps / (pms / 1000.0) / 1e9
         pooled = {"value": aggregate_value(world, L, args.steps, pms), "unit": UNIT,
                   "ms_per_step": pms / args.steps,
+                  "path_hbm_gbs": ppath, "path_hbm_frac": ppath / measured_peaks()[0],
+                  "path_bytes_per_layer_step": pab,
                   "score_kernel": {"kernel": "score_pooled_kernel", "avg_launch_ms": pavg,
                                    "bytes_per_launch": pab["score"], "achieved_gbs": pach,
                                    "frac": pach / measured_peaks()[0]}}
@@ -872,6 +1142,41 @@ def run_gpu(args, rank, world, local_rank):
                    "rows_per_kv_head": {"plain": w.G, "fused": (1 + w.n_la) * w.G}}
 
     hostlink = measure_hostlink(st, qla_dev[first], dev) if not args.no_hostlink else None
+    if hostlink is not None and kernel_ms["gather"]:
+        # the gather of the timed decode step itself: fetched bytes per layer over its launch time
+        per_layer = fetched_bytes_per_step / L
+        g_mean = sum(kernel_ms["gather"]) / len(kernel_ms["gather"])
+        g_p50 = statistics.median(kernel_ms["gather"])
+        hostlink["decode_gather"] = {
+            "bytes_per_launch": int(per_layer), "mean_us": round(1000.0 * g_mean, 2),
+            "p50_us": round(1000.0 * g_p50, 2), "max_us": round(1000.0 * max(kernel_ms["gather"]), 2),
+            "achieved_gbs_mean": per_layer / (g_mean / 1000.0) / 1e9,
+            "achieved_gbs_p50": per_layer / (g_p50 / 1000.0) / 1e9,
+            "frac_mean": per_layer / (g_mean / 1000.0) / 1e9 / hostlink["peak"],
+            "frac_p50": per_layer / (g_p50 / 1000.0) / 1e9 / hostlink["peak"],
+            "source": "gather launches of the per-kernel timing graph (3 replays x layers)"}
+
+    launches = launches_per_step(st, args.copy)
+    # exact top-64 turnover of the true queries from one step to the next (layer 0)
+    top64_turnover = exact_topk_turnover(st, [q_dev[first + k, 0] for k in range(min(8, args.steps))], K=64)
+
+    # the headline workload again with more host-tier layers, then the other configurations
+    host_fit = None
+    if world == 1 and not args.no_host_fit and args.workload == "qwen3_8b_decode":
+        try:
+            host_fit = measure_host_fit(args, st, q_dev, qla_dev, nxt, world, dev)
+        except Exception as e:
+            host_fit = {"unavailable": f"{type(e).__name__}: {str(e)[-300:]}"}
+    errw |= st.error_word()
+    other = None
+    if world == 1 and not args.no_other_configs and args.workload == "qwen3_8b_decode":
+        import gc
+
+        st = graph = g1 = None
+        q_dev = qla_dev = q_host = qla_host = None
+        gc.collect()
+        torch.cuda.empty_cache()
+        other = measure_other_configs(args, dev, world)
 
     if rank != 0:
         return
@@ -885,12 +1190,7 @@ def run_gpu(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_desc(w), "l2": l2_note(w, args.scoring),
-                   "scoring": args.scoring, "copy": args.copy, "score_ctas_per_sm": score_ctas,
-                   "host_tier_layers": l_host, "host_tier_aliased": l_host < L,
-                   "hbm_layers": l_phys, "hbm_layers_aliased": l_phys < L,
-                   "host_alloc": args.host_alloc,
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": config_dict(args, w, l_phys, l_host, score_ctas, world),
         "path_hbm_gbs": path_gbs, "path_hbm_frac": path_gbs / peak,
         "roofline": {"kernel": "score_blocks_pooled" if args.scoring == "pooled" else "score_blocks",
                      "bound": "hbm", "achieved": achieved, "peak": peak,
@@ -898,6 +1198,9 @@ def run_gpu(args, rank, world, local_rank):
                      "traffic": score_traffic_per_launch() if args.scoring == "maxdot" else None,
                      "bytes_per_launch": ab["score"],
                      "avg_launch_ms": score_avg_ms},
+        "kernel_times_source": "a separate one-step CUDA graph of the same launch order with an event-record "
+                               "node around every kernel, replayed 3 times; the nodes perturb the schedule, so "
+                               "these per-kernel figures need not add up to ms_per_step",
         "kernel_avg_us": {k: round(1000.0 * sum(v) / len(v), 2) for k, v in kernel_ms.items() if v},
         "kernel_p50_us": {k: round(1000.0 * statistics.median(v), 2) for k, v in kernel_ms.items() if v},
         "kernel_max_us": {k: round(1000.0 * max(v), 2) for k, v in kernel_ms.items() if v},
@@ -905,9 +1208,12 @@ def run_gpu(args, rank, world, local_rank):
         "fetched_bytes_per_step": int(fetched_bytes_per_step),
         "timed_steps": [pre + args.warmup, pre + args.warmup + args.steps - 1],
         "ms_per_step_eager_python": eager_ms,
-        "gpu_launches": launches_per_step(st, args.copy) * args.steps,
+        "gpu_launches": launches * args.steps,
         "copy_mode": args.copy,
         "hostlink": hostlink,
+        "true_query_top64_turnover": None if top64_turnover is None else round(top64_turnover, 4),
+        "host_tier_fit": host_fit,
+        "other_configs": other,
         "prediction_agreement": agreement,
         "pooled_scoring": pooled,
         "lag_pipeline": lag,

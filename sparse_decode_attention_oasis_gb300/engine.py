@@ -148,25 +148,10 @@ class DecodeState:
         self.blk2slot = torch.full((Lp, s.B, s.Hkv, s.nb_max), -1, dtype=torch.int32, device=dev)
         self.slot2blk = torch.full((Lp, s.B, s.Hkv, s.P), -1, dtype=torch.int32, device=dev)
         self.last_used = torch.full((Lp, s.B, s.Hkv, s.P), -1, dtype=torch.int32, device=dev)
-        host_shape = (self.L_host, s.B, s.Hkv, s.nb_max, 2, 16, 128)
-        self._host_buf = None
         if host_alloc not in ("thp", "cuda", "thp_layers", "cuda_layers"):
             raise ValueError(f"unknown host_alloc {host_alloc!r}")
-        if pin_host and host_alloc == "thp":
-            nbytes = int(np.prod(host_shape)) * 2
-            self._host_buf = HugePinnedBuffer(nbytes)
-            self.host = self._host_buf.tensor.view(torch.bfloat16).view(host_shape)
-        elif pin_host and host_alloc == "cuda":  # page-locked by the CUDA allocator (cudaHostAlloc), base pages
-            self.host = torch.empty(host_shape, dtype=torch.bfloat16, pin_memory=True)
-        elif pin_host:  # one allocation (and registration) per layer: "thp_layers" or "cuda_layers"
-            per = host_shape[1:]
-            if host_alloc == "thp_layers":
-                self._host_bufs = [HugePinnedBuffer(int(np.prod(per)) * 2) for _ in range(self.L_host)]
-                self.host = [b_.tensor.view(torch.bfloat16).view(per) for b_ in self._host_bufs]
-            else:
-                self.host = [torch.empty(per, dtype=torch.bfloat16, pin_memory=True) for _ in range(self.L_host)]
-        else:
-            self.host = torch.zeros(host_shape, dtype=torch.bfloat16)
+        self.pin_host, self.host_alloc = pin_host, host_alloc
+        self._alloc_host()
         self.ctx = torch.tensor(w.ctx, dtype=torch.int32, device=dev)
         self.scratch = LayerScratch(s, dev)
         self.scratch2 = None
@@ -180,7 +165,6 @@ class DecodeState:
         self.b2sl = [self.blk2slot[l] for l in range(Lp)]
         self.s2bl = [self.slot2blk[l] for l in range(Lp)]
         self.lul = [self.last_used[l] for l in range(Lp)]
-        self.hostl = [self.host[l] for l in range(self.L_host)]
         self.fused_select = True  # a2 + a3 in one launch (oasis_topk_select_diff) on the decode path
         # prefetching the fetched blocks' host data into L2 from that launch moved the
         # host-link latency into it (top-K + diff +15 us, gather -15 us): off
@@ -188,6 +172,56 @@ class DecodeState:
         self._lag_sel = None  # per-layer selections of the cross-step pipeline (copy="lag")
         self._lag_nsel = None
         self._lag_ready = False
+
+    def _alloc_host(self):
+        """The host tier, bf16 [L_host][B][Hkv][nb_max][2][16][128], page-locked and mapped."""
+        s = self.shape
+        host_shape = (self.L_host, s.B, s.Hkv, s.nb_max, 2, 16, 128)
+        self._host_buf, self._host_bufs = None, None
+        if self.pin_host and self.host_alloc == "thp":
+            nbytes = int(np.prod(host_shape)) * 2
+            self._host_buf = HugePinnedBuffer(nbytes)
+            self.host = self._host_buf.tensor.view(torch.bfloat16).view(host_shape)
+        elif self.pin_host and self.host_alloc == "cuda":  # page-locked by the CUDA allocator (cudaHostAlloc)
+            self.host = torch.empty(host_shape, dtype=torch.bfloat16, pin_memory=True)
+        elif self.pin_host:  # one allocation (and registration) per layer: "thp_layers" or "cuda_layers"
+            per = host_shape[1:]
+            if self.host_alloc == "thp_layers":
+                self._host_bufs = [HugePinnedBuffer(int(np.prod(per)) * 2) for _ in range(self.L_host)]
+                self.host = [b_.tensor.view(torch.bfloat16).view(per) for b_ in self._host_bufs]
+            else:
+                self.host = [torch.empty(per, dtype=torch.bfloat16, pin_memory=True) for _ in range(self.L_host)]
+        else:
+            self.host = torch.zeros(host_shape, dtype=torch.bfloat16)
+        self.hostl = [self.host[l] for l in range(self.L_host)]
+
+    def _free_host(self):
+        self.hostl = None
+        self.host = None
+        for buf in ([self._host_buf] if self._host_buf is not None else []) + list(self._host_bufs or []):
+            buf.close()
+        self._host_buf, self._host_bufs = None, None
+
+    def rebuild_host_tier(self, l_host: int):
+        """Replace the host tier by one holding l_host layers (layer l then reads host
+        buffer l mod l_host) and refill it from the generator.  Tables and HBM slots
+        are left as they are (for timing: a slot keeps the data of the host buffer
+        it was fetched from)."""
+        torch.cuda.synchronize(self.device)
+        self._free_host()
+        empty = getattr(torch._C, "_host_emptyCache", None)  # return cached page-locked memory
+        if empty is not None:
+            empty()
+        self.L_host = max(1, min(int(l_host), self.L_phys))
+        self._alloc_host()
+        w = self.w
+        for layer in range(self.L_host):
+            for b in range(w.B):
+                Kr, Vr = syn.kv_request_torch(w, layer, b, self.device)
+                kb = Kr.view(w.Hkv, w.nb_max, 16, 128)
+                vb = Vr.view(w.Hkv, w.nb_max, 16, 128)
+                self.hostl[layer][b].copy_(torch.stack([kb, vb], dim=2))
+        torch.cuda.synchronize(self.device)
 
     # ---------------------------------------------------------------- filling
     def fill_layer_numpy(self, layer: int, K_bits: np.ndarray, V_bits: np.ndarray,

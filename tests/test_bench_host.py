@@ -91,3 +91,29 @@ def test_cpu_baseline_reports_the_faster_thread_setting(bench, monkeypatch, one,
     assert r["cores"] == (1 if faster == "one" else 16)
     assert r["value"] == max(r["value_1_thread"], r["value_16_threads"])
     assert r["kind"] == "oracle" and r["unit"] == bench.UNIT
+
+
+def test_reference_arm_line_says_what_it_timed(bench, monkeypatch, capsys):
+    """The reference arm's line: the measured time of each timed step (so steps x
+    ms_per_step fits the run), the extrapolated layer-step time beside it, the
+    pairs it timed, and the same config as the GPU arm's line."""
+    monkeypatch.setattr(bench.sys, "argv", ["bench.py", "--impl", "reference", "--workload", "tiny",
+                                            "--steps", "2", "--warmup", "1"])
+    args = bench.parse()
+    bench.run_reference(args, 0)
+    import json
+
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["extrapolated"] is True
+    assert line["pairs_timed"] == 2 and line["pairs_per_step"] == 1
+    assert line["steps"] * line["ms_per_step"] / 1000.0 <= line["run_wall_s"]
+    w = bench.workload(args)
+    assert line["ms_per_step_extrapolated"] == pytest.approx(1000.0 * w.L / line["value"])
+    l_phys, l_host = bench.planned_layers(args, w)
+    assert line["config"] == bench.config_dict(args, w, l_phys, l_host, 0)
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_workload_description_names_the_drifting_hot_set(bench):
+    assert "drifting through 256 planted blocks" in bench.workload_desc(syn.long_output())
+    assert "64 planted hot blocks" in bench.workload_desc(syn.qwen3_8b_decode())
