@@ -27,7 +27,12 @@
 
 namespace oasis {
 
-constexpr int kGatherThreads = 256;
+// 128 threads (4 warps, under 48 registers each): the decode step runs this kernel
+// on a side stream beside the previous layer's attention, whose 2 CTAs per SM
+// (4 warps x 208 registers each) must still fit next to two of these CTAs, or
+// attention spills into a second wave.  The copy is bound by the host link, not
+// by the threads that issue it.
+constexpr int kGatherThreads = 128;
 constexpr int kGatherUnroll = 4;
 
 __device__ __forceinline__ uint4 ld_host16(const void* p) {
