@@ -518,9 +518,10 @@ OASIS_API oasis_status oasis_touch_host(const void* host_ptr, size_t bytes, uint
 
 /*
  * Process-wide launch options (the pages have no counterpart: scheduling knobs).
- * OASIS_OPT_SCORE_CTAS_PER_SM: the mma.sync block scorers (max-dot and pooled,
- *   with or without a carried copy) size their persistent grid to value CTAs per SM (0 = as many as
- *   fit, the default).  A caller that runs the selection, gather and attention
+ * OASIS_OPT_SCORE_CTAS_PER_SM: the mma.sync max-dot block scorer (with or without
+ *   a carried copy) sizes its persistent grid to value CTAs per SM (0 = as many as
+ *   fit, the default).  The pooled scorer always runs one CTA per SM (its shared-
+ *   memory ring fills the SM) and ignores it.  A caller that runs the selection, gather and attention
  *   kernels of one layer beside the scorer of the next on another stream leaves
  *   them room this way.  Read at every launch; results do not depend on it.
  * Unknown options or values return OASIS_ERR_INVALID.

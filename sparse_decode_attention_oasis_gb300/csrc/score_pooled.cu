@@ -7,26 +7,53 @@
 //   P_n(x) = sum_i max(q_i hi_i, q_i lo_i) = sum_i q+_i hi_i + sum_i q-_i lo_i,
 // q+ = max(q, 0), q- = min(q, 0) (lo <= hi).  So P_n(x) = q'.k' with
 // q' = [q+ | q-] and k' = [hi | lo], a 256-long dot product, and a block is ONE
-// 256-element row: one warp scores 16 blocks as a 16 x N tile
+// 256-element row: one warp scores a tile of 16 blocks as a 16 x N tile
 // D = K' (16 x 256) * Q'^T (256 x N) with mma.m16n8k16 (bf16 in, fp32 accumulate).
 // score(x) = max over lookahead j and group heads g of P / sqrt(d).  The reads are
 // 512 bytes per block instead of 4 KiB.
 //
+// Streaming.  A tile (16 consecutive blocks of one head) is 8 KiB of contiguous
+// memory.  Each warp streams its tiles through a ring of kStages shared-memory
+// stages with cp.async (16 bytes per lane per copy, 512 contiguous bytes per
+// warp instruction), so kStages - 1 tiles are in flight while one is computed;
+// one CTA of 8 warps per SM keeps up to 7 x 16 tiles (128 KiB) moving.  Rows are
+// stored with their 16-byte chunks XOR-ed by (row & 1) << 2, which makes the
+// fragment reads below conflict-free.
+//
+// Work split.  The valid tiles of all heads (ceil(nb_b / 16) per head of request
+// b) form one sequence in (request, KV head, tile) order; CTA c takes an equal
+// contiguous share and its warps interleave over it, so heads with short
+// contexts cost nothing and every SM gets the same number of tiles.  The share
+// spans few heads: the Q' fragments of up to kHeadsCached heads at a time are
+// built in shared memory (fragment order) between two barriers.
+//
 // As in the full scorer, the 256-long axis is permuted identically for K' and Q'
-// so that each thread's 16-byte loads of rows g and g+8 are its A fragments
-// (chunks t, t+4, ..., t+28 of the row).  Each CTA takes a contiguous range of
-// chunks of 128 blocks; Q' fragments are built in shared memory (fragment order,
-// conflict-free) whenever that range moves to another head.  Bound: e = 2^-12 |q'|
-// |k'| / sqrt(d) + |s~| 2^-22 + 2^-60 with |q'| = |q|; the modelled tensor-core
-// accumulation error of 16 steps of 16 exact products is 272 x 2^-23 ~ 2^-14.9,
-// a 7x margin.  Optionally carries the copy half of a gather (fetch_copy.cuh).
+// so that each thread's 16-byte reads of rows g and g+8 are its A fragments
+// (chunks t, t+4, ..., t+28 of the row).  Bound: e = 2^-12 |q'| |k'| / sqrt(d) +
+// |s~| 2^-22 + 2^-60 with |q'| = |q|; the modelled tensor-core accumulation error
+// of 16 steps of 16 exact products is 272 x 2^-23 ~ 2^-14.9, a 7x margin.
+// Optionally carries the copy half of a gather (fetch_copy.cuh).
 #include "fetch_copy.cuh"
 
 namespace oasis {
 
-constexpr int kPsWarps = 4;
-constexpr int kPsChunk = 128;  // blocks per (CTA, head) work item
-constexpr int kPK = 2 * kD;    // pooled elements per block
+constexpr int kPsWarps = 8;
+constexpr int kTileBlocks = 16;
+constexpr int kPK = 2 * kD;                             // pooled elements per block
+constexpr int kTileBytes = kTileBlocks * kPK * 2;       // 8 KiB
+constexpr int kMaxPrefix = 512;                         // requests with an exact tile prefix
+
+// Q' fragment sets held at once: two heads up to 16 query rows, one above (the
+// ring and the fragments must fit in one SM's shared memory)
+template <int NT>
+struct HeadsCached { static constexpr int value = NT <= 2 ? 2 : 1; };
+
+template <int NT>
+struct PooledSmem {
+  uint2 qf[HeadsCached<NT>::value][NT][8][2][32];  // Q' fragments [head][n-tile][chunk i][half][lane]
+  float qn2[2];                                // squared max query norm per cached head
+  int pre[kMaxPrefix + 1];                     // tiles before request b (all its KV heads)
+};
 
 // positive / negative part of each bf16 of a word pair
 __device__ __forceinline__ uint32_t bf2_pos(uint32_t w) {
@@ -38,42 +65,123 @@ __device__ __forceinline__ uint32_t bf2_neg(uint32_t w) {
   return w & m;
 }
 
+__device__ __forceinline__ void ps_cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void ps_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void ps_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ uint4 ps_lds(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+// byte offset of 16-byte chunk c of row r inside a staged tile
+__device__ __forceinline__ uint32_t ps_swz(int r, int c) { return (uint32_t)(r * (kPK * 2) + ((c ^ ((r & 1) << 2)) << 4)); }
+
+// Tile sequence of the launch: tile index -> (head, first block of the tile).
+struct TileMap {
+  const int* pre;   // shared, [B + 1] when exact
+  int B, Hkv, nb_max, tpb_nominal;
+  bool exact;
+  __device__ void locate(int idx, int& head, int& blk0) const {
+    if (!exact) {  // every head gets ceil(nb_max / 16) tiles; empty ones are skipped
+      head = idx / tpb_nominal;
+      blk0 = (idx - head * tpb_nominal) * kTileBlocks;
+      return;
+    }
+    int lo = 0, hi = B - 1;  // the last b with pre[b] <= idx
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= idx) lo = mid; else hi = mid - 1;
+    }
+    const int tb = (pre[lo + 1] - pre[lo]) / Hkv;
+    const int local = idx - pre[lo];
+    const int h = local / tb;
+    head = lo * Hkv + h;
+    blk0 = (local - h * tb) * kTileBlocks;
+  }
+  __device__ int first_tile(int head) const {  // first tile index of `head`
+    if (!exact) return head * tpb_nominal;
+    const int b = head / Hkv, h = head - b * Hkv;
+    return pre[b] + h * ((pre[b + 1] - pre[b]) / Hkv);
+  }
+};
+
 template <int NT, bool kCopy>
-__global__ void __launch_bounds__(kPsWarps * 32, 3)
+__global__ void __launch_bounds__(kPsWarps * 32, 1)
 score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restrict__ ctx_len,
-                    const uint16_t* __restrict__ q_la, float2* __restrict__ scores, int chunks_per_head,
-                    int total_chunks, float inv_sqrt_d, CopyJob job) {
-  __shared__ uint2 qf[NT][8][2][32];  // Q' fragments [n-tile][chunk i][half][lane]
-  __shared__ float qn_w[kPsWarps];
-  extern __shared__ uint4 copy_buf[];  // [kPsWarps][512] when kCopy
+                    const uint16_t* __restrict__ q_la, float2* __restrict__ scores, float inv_sqrt_d, CopyJob job) {
+  constexpr int kStages = kCopy ? 2 : 3;
+  constexpr int kHeadsCached = HeadsCached<NT>::value;
+  extern __shared__ __align__(128) uint8_t ps_dyn[];
+  PooledSmem<NT>& sm = *reinterpret_cast<PooledSmem<NT>*>(ps_dyn);
+  uint8_t* ring_base = ps_dyn + ((sizeof(PooledSmem<NT>) + 127) & ~size_t(127));
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   const long long gwarp = (long long)blockIdx.x * kPsWarps + warp;
   const long long nwarps = (long long)gridDim.x * kPsWarps;
+  uint4* copy_buf = reinterpret_cast<uint4*>(ring_base + (size_t)kPsWarps * kStages * kTileBytes);
   if constexpr (kCopy) copy_begin(job, s, gwarp, nwarps, copy_buf + warp * (kCopyUnitBytes / 16), lane);
+  const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(ring_base)) + warp * kStages * kTileBytes;
   const int G = s.Hq / s.Hkv;
   const int N = s.n_la * G;
 
-  // a contiguous range of chunks per CTA: consecutive chunks mostly share a head,
-  // so the Q' fragments are rebuilt only when the head changes
-  const int c_begin = (int)((long long)blockIdx.x * total_chunks / gridDim.x);
-  const int c_end = (int)((long long)(blockIdx.x + 1) * total_chunks / gridDim.x);
-  int cur_head = -1;
-  float qnorm = 0.f;
-  for (int chunk = c_begin; chunk < c_end; ++chunk) {
-    const int head = chunk / chunks_per_head;
-    const int c = chunk - head * chunks_per_head;
-    const int b = head / s.Hkv, h = head - b * s.Hkv;
-    const int nb = clamp_nb(ctx_len[b], s.nb_max);
-    const int blk0 = c * kPsChunk;
-    if (blk0 >= nb) continue;
-    const int blk1 = min(nb, blk0 + kPsChunk);
-    if (head != cur_head) {
-    cur_head = head;
-    __syncthreads();  // every warp is done with the previous head's fragments
-    float qn2 = 0.f;
-    for (int nt = warp; nt < NT; nt += kPsWarps) {
+  // the tile prefix over requests (every CTA computes the same one)
+  TileMap map{sm.pre, s.B, s.Hkv, s.nb_max, (s.nb_max + kTileBlocks - 1) / kTileBlocks, s.B <= kMaxPrefix};
+  int total;
+  if (map.exact) {
+    int run = 0;  // serial over requests in chunks of blockDim.x
+    for (int b0 = 0; b0 < s.B; b0 += blockDim.x) {
+      const int b = b0 + threadIdx.x;
+      const int tiles = b < s.B ? (clamp_nb(ctx_len[b], s.nb_max) + kTileBlocks - 1) / kTileBlocks * s.Hkv : 0;
+      // block inclusive scan of `tiles`
+      int x = tiles;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      __shared__ int wsum[kPsWarps];
+      if (lane == 31) wsum[warp] = x;
+      __syncthreads();
+      int off = 0;
+      for (int w = 0; w < warp; ++w) off += wsum[w];
+      int tot = 0;
+      for (int w = 0; w < kPsWarps; ++w) tot += wsum[w];
+      if (b < s.B) sm.pre[b] = run + off + x - tiles;
+      run += tot;
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) sm.pre[s.B] = run;
+    __syncthreads();
+    total = sm.pre[s.B];
+  } else {
+    total = s.B * s.Hkv * map.tpb_nominal;
+  }
+  const int T0 = (int)((long long)blockIdx.x * total / gridDim.x);
+  const int T1 = (int)((long long)(blockIdx.x + 1) * total / gridDim.x);
+  if (T0 >= T1) {
+    if constexpr (kCopy) copy_finish(job, s, gwarp, nwarps, copy_buf + warp * (kCopyUnitBytes / 16), lane);
+    return;
+  }
+  int head_first, head_last, unused;
+  map.locate(T0, head_first, unused);
+  map.locate(T1 - 1, head_last, unused);
+
+  for (int hg = head_first; hg <= head_last; hg += kHeadsCached) {
+    const int nh = min(kHeadsCached, head_last - hg + 1);
+    __syncthreads();  // every warp is done with the previous group's fragments
+    if (threadIdx.x < 2) sm.qn2[threadIdx.x] = 0.f;
+    __syncthreads();
+    // Q' fragments of the group's heads: warp w builds (head slot, n-tile) pairs w, w + 8, ...
+    for (int pair = warp; pair < nh * NT; pair += kPsWarps) {
+      const int hs = pair / NT, nt = pair - hs * NT;
+      const int head = hg + hs;
+      const int b = head / s.Hkv, h = head - b * s.Hkv;
       const int n = nt * 8 + g;
       uint4 v[4];
 #pragma unroll
@@ -94,33 +202,61 @@ score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restr
           ss = fmaf(bf_hi(w[m]), bf_hi(w[m]), ss);
         }
         // chunk t + 4i of q' is q+ chunk t + 4i; chunk t + 4(i + 4) is q- chunk t + 4i
-        qf[nt][i][0][lane] = make_uint2(bf2_pos(w[0]), bf2_pos(w[1]));
-        qf[nt][i][1][lane] = make_uint2(bf2_pos(w[2]), bf2_pos(w[3]));
-        qf[nt][i + 4][0][lane] = make_uint2(bf2_neg(w[0]), bf2_neg(w[1]));
-        qf[nt][i + 4][1][lane] = make_uint2(bf2_neg(w[2]), bf2_neg(w[3]));
+        sm.qf[hs][nt][i][0][lane] = make_uint2(bf2_pos(w[0]), bf2_pos(w[1]));
+        sm.qf[hs][nt][i][1][lane] = make_uint2(bf2_pos(w[2]), bf2_pos(w[3]));
+        sm.qf[hs][nt][i + 4][0][lane] = make_uint2(bf2_neg(w[0]), bf2_neg(w[1]));
+        sm.qf[hs][nt][i + 4][1][lane] = make_uint2(bf2_neg(w[2]), bf2_neg(w[3]));
       }
       ss += __shfl_xor_sync(0xffffffffu, ss, 1);
       ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-      qn2 = fmaxf(qn2, ss);
+      ss = warp_max(ss);
+      // non-negative floats order like their bit patterns
+      if (lane == 0) atomicMax(reinterpret_cast<int*>(&sm.qn2[hs]), __float_as_int(ss));
     }
-    qn2 = warp_max(qn2);
-    if (lane == 0) qn_w[warp] = qn2;
     __syncthreads();
-    float qmax = qn_w[0];
-#pragma unroll
-    for (int w = 1; w < kPsWarps; ++w) qmax = fmaxf(qmax, qn_w[w]);
-    qnorm = sqrtf(qmax);
-    }
 
-    const uint16_t* base = kp + (long long)head * s.nb_max * kPK;
-    for (int tile = blk0 + warp * 16; tile < blk1; tile += kPsWarps * 16) {
-      const int r0 = tile + g, r1 = tile + g + 8;
+    // this group's share of the tile sequence; warp w takes tiles w, w + 8, ...
+    const int g0 = max(T0, map.first_tile(hg));
+    const int g1 = hg + nh <= head_last ? min(T1, map.first_tile(hg + nh)) : T1;
+    const int ntiles = g0 < g1 ? (g1 - g0 - warp + kPsWarps - 1) / kPsWarps : 0;
+
+    // issue tile k of this warp into its stage; rows past the head's valid blocks are not read
+    auto issue = [&](int k) {
+      if (k < ntiles) {
+        int head, blk0;
+        map.locate(g0 + warp + k * kPsWarps, head, blk0);
+        const int b = head / s.Hkv;
+        const int nb = clamp_nb(ctx_len[b], s.nb_max);
+        const int rows = min(kTileBlocks, nb - blk0);
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(kp + ((long long)head * s.nb_max + blk0) * kPK);
+        const uint32_t dst = ring + (k % kStages) * kTileBytes;
+#pragma unroll
+        for (int m = 0; m < kTileBlocks; ++m)
+          if (m < rows) ps_cp_async16(dst + ps_swz(m, lane), src + m * (kPK * 2) + lane * 16);
+      }
+      ps_commit();  // one group per tile slot (empty past the end), so wait_group counts tiles
+    };
+#pragma unroll
+    for (int k = 0; k < kStages - 1; ++k) issue(k);
+    for (int k = 0; k < ntiles; ++k) {
+      issue(k + kStages - 1);
+      ps_wait<kStages - 1>();
+      __syncwarp();
+      int head, blk0;
+      map.locate(g0 + warp + k * kPsWarps, head, blk0);
+      const int hs = head - hg;
+      const int b = head / s.Hkv;
+      const int nb = clamp_nb(ctx_len[b], s.nb_max);
+      const int blk1 = min(nb, blk0 + kTileBlocks);
+      const uint32_t stage = ring + (k % kStages) * kTileBytes;
       uint4 ra[8], rb[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        ra[i] = r0 < blk1 ? ldg_stream(base + (long long)r0 * kPK + (t + 4 * i) * 8) : make_uint4(0u, 0u, 0u, 0u);
-        rb[i] = r1 < blk1 ? ldg_stream(base + (long long)r1 * kPK + (t + 4 * i) * 8) : make_uint4(0u, 0u, 0u, 0u);
+        ra[i] = ps_lds(stage + ps_swz(g, t + 4 * i));
+        rb[i] = ps_lds(stage + ps_swz(g + 8, t + 4 * i));
       }
+      __syncwarp();  // the stage is free for the copy issued in the next iteration
+      const int r0 = blk0 + g, r1 = blk0 + g + 8;
       float acc[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
@@ -132,7 +268,7 @@ score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restr
         for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            const uint2 q = qf[nt][i][hh][lane];
+            const uint2 q = sm.qf[hs][nt][i][hh][lane];
             mma_bf16_16816(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3], A[2 * hh], Bw[2 * hh], A[2 * hh + 1],
                            Bw[2 * hh + 1], q.x, q.y);
           }
@@ -164,6 +300,7 @@ score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restr
       s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
       s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
       if (t == 0) {
+        const float qnorm = sqrtf(sm.qn2[hs]);
         float2* out = scores + (long long)head * s.nb_max;
         if (r0 < blk1) {
           const float sc = m0 * inv_sqrt_d;
@@ -179,43 +316,37 @@ score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restr
         }
       }
     }
+    ps_wait<0>();  // the empty trailing groups: nothing is left in flight
   }
   if constexpr (kCopy) copy_finish(job, s, gwarp, nwarps, copy_buf + warp * (kCopyUnitBytes / 16), lane);
 }
 
-template <int NT>
-static int pooled_grid_limit() {
-  static int per_sm_cached[kMaxDevicesCached] = {};
-  const int dev = current_device();
-  int& per_sm = per_sm_cached[dev];
-  if (!per_sm) {
-    int v = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, score_pooled_kernel<NT, false>, kPsWarps * 32, 0);
-    per_sm = v < 1 ? 1 : v;
-  }
-  const int cap = score_ctas_per_sm_option();
-  return sm_count() * (cap > 0 && cap < per_sm ? cap : per_sm);
+template <int NT, bool kCopy>
+static size_t pooled_smem_bytes() {
+  constexpr int kStages = kCopy ? 2 : 3;
+  return ((sizeof(PooledSmem<NT>) + 127) & ~size_t(127)) + (size_t)kPsWarps * kStages * kTileBytes +
+         (kCopy ? (size_t)kPsWarps * kCopyUnitBytes : 0);
+}
+
+template <int NT, bool kCopy>
+static cudaError_t launch_nt2(const Shape& s, const uint16_t* kp, const int* ctx, const uint16_t* q_la,
+                              float2* scores, const CopyJob& job, cudaStream_t stream) {
+  static int attr_cache[kMaxDevicesCached] = {};
+  const size_t smem = pooled_smem_bytes<NT, kCopy>();
+  cudaError_t e = ensure_dyn_smem((const void*)score_pooled_kernel<NT, kCopy>, smem, attr_cache);
+  if (e != cudaSuccess) return e;
+  // one CTA per SM (its shared memory); OASIS_OPT_SCORE_CTAS_PER_SM cannot raise that
+  const int grid = sm_count();
+  score_pooled_kernel<NT, kCopy><<<grid, kPsWarps * 32, smem, stream>>>(s, kp, ctx, q_la, scores,
+                                                                       1.0f / sqrtf((float)s.d), job);
+  return cudaGetLastError();
 }
 
 template <int NT>
 static cudaError_t launch_nt(const Shape& s, const uint16_t* kp, const int* ctx, const uint16_t* q_la,
                              float2* scores, const CopyJob* job, cudaStream_t stream) {
-  const int chunks_per_head = (s.nb_max + kPsChunk - 1) / kPsChunk;
-  const int total = s.B * s.Hkv * chunks_per_head;
-  const float inv = 1.0f / sqrtf((float)s.d);
-  const int lim = pooled_grid_limit<NT>();
-  if (job) {
-    static int attr_cache[kMaxDevicesCached] = {};
-    cudaError_t e = ensure_dyn_smem((const void*)score_pooled_kernel<NT, true>, kPsWarps * kCopyUnitBytes, attr_cache);
-    if (e != cudaSuccess) return e;
-    score_pooled_kernel<NT, true><<<lim, kPsWarps * 32, kPsWarps * kCopyUnitBytes, stream>>>(
-        s, kp, ctx, q_la, scores, chunks_per_head, total, inv, *job);
-  } else {
-    const int grid = max(1, min(total, lim));
-    score_pooled_kernel<NT, false><<<grid, kPsWarps * 32, 0, stream>>>(s, kp, ctx, q_la, scores, chunks_per_head,
-                                                                        total, inv, CopyJob{});
-  }
-  return cudaGetLastError();
+  if (job) return launch_nt2<NT, true>(s, kp, ctx, q_la, scores, *job, stream);
+  return launch_nt2<NT, false>(s, kp, ctx, q_la, scores, CopyJob{}, stream);
 }
 
 cudaError_t launch_score_pooled(const Shape& s, const uint16_t* kp, const int* ctx, const uint16_t* q_la,

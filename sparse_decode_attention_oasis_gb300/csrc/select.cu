@@ -60,7 +60,8 @@ struct SelCtx {
   uint32_t* hist;              // [256]
   int* scal;                   // [8] scalars
   float* fscal;                // [kSelWarps]
-  int qstate;                  // queries: 0 not staged, 1 copies in flight, 2 staged with norms
+  int qstate;                  // queries: 0 not staged, 1 copies in flight, 3 landed (visible after the
+                               // next CTA barrier), 2 staged with norms
   int kcap;                    // entries of tval (Kb)
 };
 
@@ -274,6 +275,34 @@ __device__ void kth_by_rank(const float* v, int m, int k, float* out) {
   __syncthreads();
 }
 
+// Small k (the per-step fetch cap): the k-th largest of se[0..n).x, n <= 256, by
+// one warp: each lane holds up to 8 values; every round takes the warp's largest
+// remaining value and counts its copies, until k values have been counted.
+constexpr int kSmallK = 16;
+__device__ void kth_small_k(const float2* se, int n, int k, float* out) {
+  const int lane = threadIdx.x & 31;
+  float v[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = lane + 32 * j < n ? se[lane + 32 * j].x : neg_inf();
+  int left = k;
+  for (int round = 0; round < k; ++round) {
+    float m = v[0];
+#pragma unroll
+    for (int j = 1; j < 8; ++j) m = fmaxf(m, v[j]);
+    m = warp_max(m);
+    int cnt = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) cnt += __popc(__ballot_sync(0xffffffffu, v[j] == m));
+    if (cnt >= left) {
+      if (lane == 0) *out = m;
+      return;
+    }
+    left -= cnt;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = v[j] == m ? neg_inf() : v[j];
+  }
+}
+
 // Bracket [t_lo, t_hi] around the k-th largest s~ among se[0..n) (1 <= k <= n), and
 // E = max e.  Up to kRankMax entries: t itself, by rank counting.  Longer lists:
 // a pass of 256 bins, bin1 = floor(256 (x - min)/(max - min)), finds the bin that
@@ -284,7 +313,7 @@ __device__ void kth_by_rank(const float* v, int m, int k, float* out) {
 // subtraction and a multiplication by a positive constant, exact sub-bin
 // offsets), so the k-th largest lies in the selected bin and cell.
 __device__ void kth_bracket(const float2* se, int n, int k, uint32_t* hist, int* scal, float* fs, float* scratch,
-                            float& t_lo, float& t_hi, float& emax) {
+                            uint8_t* bins, float& t_lo, float& t_hi, float& emax) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float* tslot = fs + 60;   // fs[0 .. 3 kSelWarps) hold the partial reductions, fs + 64 the cell keys
   float mn = __int_as_float(0x7f800000), mx = neg_inf(), em = 0.f;
@@ -309,20 +338,25 @@ __device__ void kth_bracket(const float2* se, int n, int k, uint32_t* hist, int*
   }
   emax = em;
   if (small) {
-    kth_by_rank<2>(reinterpret_cast<const float*>(se), n, k, tslot);
+    if (k <= kSmallK) {
+      if (warp == 0) kth_small_k(se, n, k, tslot);
+      __syncthreads();
+    } else {
+      kth_by_rank<2>(reinterpret_cast<const float*>(se), n, k, tslot);
+    }
     t_lo = t_hi = *tslot;
     __syncthreads();
     return;
   }
   const float span = mx - mn;
   const float sc1 = span > 1e-30f ? 256.0f / span : 0.f;
-  const int n_pad = (n + 31) & ~31;
-  // pass 1
-  for (int i = threadIdx.x; i < n_pad; i += blockDim.x) {
-    uint32_t bin = 1024u;
-    if (i < n) bin = (uint32_t)min(255, (int)((se[i].x - mn) * sc1));
-    const unsigned peers = __match_any_sync(0xffffffffu, bin);
-    if (i < n && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+  // pass 1: plain shared-memory atomics (a warp's same-bin lanes serialise in
+  // hardware, far cheaper than grouping them first); each entry's bin is kept
+  // in `bins` for the listing pass
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int bin = min(255, (int)((se[i].x - mn) * sc1));
+    bins[i] = (uint8_t)bin;
+    atomicAdd(&hist[bin], 1u);
   }
   __syncthreads();
   if (warp == 0) {
@@ -349,20 +383,9 @@ __device__ void kth_bracket(const float2* se, int n, int k, uint32_t* hist, int*
   const int k1 = k - scal[1];
   const int m1 = (int)hist[b1];
   if (m1 <= kRankMax) {
-    // list bin b1's entries (warp-aggregated slots), then rank them
-    for (int i = threadIdx.x; i < n_pad; i += blockDim.x) {
-      float x = 0.f;
-      bool in = false;
-      if (i < n) {
-        x = se[i].x;
-        in = (int)min(255, (int)((x - mn) * sc1)) == b1;
-      }
-      const unsigned ball = __ballot_sync(0xffffffffu, in);
-      int base = 0;
-      if (lane == 0 && ball) base = atomicAdd(&scal[5], __popc(ball));
-      base = __shfl_sync(0xffffffffu, base, 0);
-      if (in) scratch[base + __popc(ball & ((1u << lane) - 1u))] = x;
-    }
+    // list bin b1's entries (a handful: one shared atomic each), then rank them
+    for (int i = threadIdx.x; i < n; i += blockDim.x)
+      if (bins[i] == (uint8_t)b1) scratch[atomicAdd(&scal[5], 1)] = se[i].x;
     __syncthreads();
     kth_by_rank<1>(scratch, m1, k1, tslot);
     t_lo = t_hi = *tslot;
@@ -374,24 +397,16 @@ __device__ void kth_bracket(const float2* se, int n, int k, uint32_t* hist, int*
   uint32_t* kmax = kmin + 256;
   for (int i = threadIdx.x; i < 256; i += blockDim.x) { h2[i] = 0u; kmin[i] = 0xffffffffu; kmax[i] = 0u; }
   __syncthreads();
-  for (int i = threadIdx.x; i < n_pad; i += blockDim.x) {
-    uint32_t bin = 1024u;
-    uint32_t key = 0u;
-    if (i < n) {
-      const float x = se[i].x;
-      const float y = (x - mn) * sc1;
-      const int bb1 = min(255, (int)y);
-      if (bb1 == b1) {
-        bin = (uint32_t)max(0, min(255, (int)((y - (float)bb1) * 256.0f)));
-        key = float_key(x);
-      }
-    }
-    const unsigned peers = __match_any_sync(0xffffffffu, bin);
-    if (bin < 1024u) {
-      atomicMin(&kmin[bin], key);
-      atomicMax(&kmax[bin], key);
-      if (lane == __ffs(peers) - 1) atomicAdd(&h2[bin], (uint32_t)__popc(peers));
-    }
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    if (bins[i] != (uint8_t)b1) continue;
+    const float x = se[i].x;
+    const float y = (x - mn) * sc1;
+    const int bb1 = min(255, (int)y);  // == b1: the same arithmetic as pass 1
+    const uint32_t bin = (uint32_t)max(0, min(255, (int)((y - (float)bb1) * 256.0f)));
+    const uint32_t key = float_key(x);
+    atomicMin(&kmin[bin], key);
+    atomicMax(&kmax[bin], key);
+    atomicAdd(&h2[bin], 1u);
   }
   __syncthreads();
   if (warp == 0) {
@@ -436,6 +451,25 @@ __device__ void issue_queries(SelCtx& c) {
 // load per piece, all issued together).  Idempotent; every thread calls it.
 __device__ void stage_queries(SelCtx& c) {
   if (c.qstate == 2) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (c.qstate == 3) {
+    // landed and visible (a CTA barrier followed every thread's wait): each warp
+    // forms all N norms itself, so no further barrier is needed (every warp
+    // writes the same values)
+    for (int n = 0; n < c.N; ++n) {
+      const uint32_t w0 = reinterpret_cast<const uint32_t*>(c.qb + n * kD)[lane];
+      const uint32_t w1 = reinterpret_cast<const uint32_t*>(c.qb + n * kD)[lane + 32];
+      float ss = bf_lo(w0) * bf_lo(w0);
+      ss = fmaf(bf_hi(w0), bf_hi(w0), ss);
+      ss = fmaf(bf_lo(w1), bf_lo(w1), ss);
+      ss = fmaf(bf_hi(w1), bf_hi(w1), ss);
+      ss = warp_sum(ss);
+      if (lane == 0) c.qn[n] = sqrtf(ss);
+    }
+    __syncwarp();
+    c.qstate = 2;
+    return;
+  }
   if (c.qstate == 1) {
     sel_cp_async_wait_all();
   } else {
@@ -447,7 +481,6 @@ __device__ void stage_queries(SelCtx& c) {
     }
   }
   __syncthreads();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int n = warp; n < c.N; n += kSelWarps) {
     const uint32_t w0 = reinterpret_cast<const uint32_t*>(c.qb + n * kD)[lane];
     const uint32_t w1 = reinterpret_cast<const uint32_t*>(c.qb + n * kD)[lane + 32];
@@ -743,10 +776,20 @@ __device__ void select_best(SelCtx& c, const float2* se, int n, int k, const int
     return;
   }
   float t_lo, t_hi, em;
-  kth_bracket(se, n, k, c.hist, c.scal, c.fscal, reinterpret_cast<float*>(U), t_lo, t_hi, em);
+  kth_bracket(se, n, k, c.hist, c.scal, c.fscal, reinterpret_cast<float*>(U), cls, t_lo, t_hi, em);
   const float hi_t = __fadd_ru(t_hi, em), lo_t = __fsub_rd(t_lo, em);
   if (threadIdx.x == 0) { c.scal[2] = 0; c.scal[3] = 0; }
+  // the queries copied at kernel start have landed once every thread has waited
+  // for its own copies; the barrier below makes them visible to the whole CTA
+  if (c.qstate == 1) {
+    sel_cp_async_wait_all();
+    c.qstate = 3;
+  }
   __syncthreads();
+  // classify; an uncertain block's keys are prefetched into L2 at once, so the
+  // exact refine that follows finds them there (at most kPrefetchBlocks blocks)
+  constexpr int kLines = kPooled ? 2 * kD * 2 / 128 : kBS * kD * 2 / 128;
+  constexpr int kPrefetchBlocks = 64;
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const float2 v = se[i];
     const float lo = __fsub_rd(v.x, v.y), hi = __fadd_ru(v.x, v.y);
@@ -758,7 +801,14 @@ __device__ void select_best(SelCtx& c, const float2* se, int n, int k, const int
       cl = 0;
     } else {
       cl = 2;
-      U[atomicAdd(&c.scal[2], 1)] = i;
+      const int slot = atomicAdd(&c.scal[2], 1);
+      U[slot] = i;
+      if (slot < kPrefetchBlocks) {
+        const int blk = cand_blk ? cand_blk[i] : i;
+        const char* base = reinterpret_cast<const char*>(c.k + (long long)blk * (kPooled ? 2 * kD : kBS * kD));
+#pragma unroll 4
+        for (int ln = 0; ln < kLines; ++ln) asm volatile("prefetch.global.L2 [%0];" ::"l"(base + ln * 128));
+      }
     }
     cls[i] = cl;
   }
@@ -770,18 +820,6 @@ __device__ void select_best(SelCtx& c, const float2* se, int n, int k, const int
     for (int i = threadIdx.x; i < nU; i += blockDim.x) cls[U[i]] = r > 0 ? 1 : 0;
     __syncthreads();
     return;
-  }
-  // the refine takes kSelWarps blocks per round: bring the keys of the later
-  // rounds (up to kPrefetchBlocks blocks) into L2 now
-  constexpr int kLines = kPooled ? 2 * kD * 2 / 128 : kBS * kD * 2 / 128;
-  constexpr int kPrefetchBlocks = 64;
-  const int npre = min(nU, kSelWarps + kPrefetchBlocks) - kSelWarps;
-  for (int idx = threadIdx.x; idx < npre * kLines; idx += blockDim.x) {
-    const int ci = U[kSelWarps + idx / kLines];
-    const int blk = cand_blk ? cand_blk[ci] : ci;
-    const char* line = reinterpret_cast<const char*>(c.k + (long long)blk * (kPooled ? 2 * kD : kBS * kD)) +
-                       (idx % kLines) * 128;
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(line));
   }
   refine_top_r<kPooled>(c, U, nU, r, cand_blk, cls);
 }
@@ -932,6 +970,11 @@ topk_select_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* _
   const float2* src = scores + (long long)head * s.nb_max;
   for (int i = threadIdx.x; i < nb; i += blockDim.x) se[i] = src[i];
   if (nb > s.Kb) issue_queries(c);
+  if (kDiff) {  // the diff reads this head's blk2slot row after the top-K: bring it into L2 now
+    const char* row = reinterpret_cast<const char*>(blk2slot + (long long)head * s.nb_max);
+    for (int ln = threadIdx.x; ln * 128 < s.nb_max * 4; ln += blockDim.x)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(row + ln * 128));
+  }
   __syncthreads();
   int ns = 0;
 #pragma unroll 1
