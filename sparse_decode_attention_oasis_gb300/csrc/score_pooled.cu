@@ -29,7 +29,9 @@
 //
 // As in the full scorer, the 256-long axis is permuted identically for K' and Q'
 // so that each thread's 16-byte reads of rows g and g+8 are its A fragments
-// (chunks t, t+4, ..., t+28 of the row).  Bound: e = 2^-12 |q'| |k'| / sqrt(d) +
+// (chunks t, t+4, ..., t+28 of the row).  The rows' norms |k'| come from the
+// diagonal of the Gram tile K' K'^T, a second set of MMAs on the same fragments,
+// instead of 64 scalar multiply-adds per row and thread.  Bound: e = 2^-12 |q'| |k'| / sqrt(d) +
 // |s~| 2^-22 + 2^-60 with |q'| = |q|; the modelled tensor-core accumulation error
 // of 16 steps of 16 exact products is 272 x 2^-23 ~ 2^-14.9, a 7x margin.
 // Optionally carries the copy half of a gather (fetch_copy.cuh).
@@ -219,15 +221,25 @@ score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restr
     const int g0 = max(T0, map.first_tile(hg));
     const int g1 = hg + nh <= head_last ? min(T1, map.first_tile(hg + nh)) : T1;
     const int ntiles = g0 < g1 ? (g1 - g0 - warp + kPsWarps - 1) / kPsWarps : 0;
+    // tile index -> (head slot, first block) without a search: the group's heads
+    // own consecutive runs of the sequence starting at ft[0] and ft[1]
+    const int ft0 = map.first_tile(hg);
+    const int ft1 = nh > 1 ? map.first_tile(hg + 1) : 0x7fffffff;
+    const int nbh0 = clamp_nb(ctx_len[hg / s.Hkv], s.nb_max);
+    const int nbh1 = nh > 1 ? clamp_nb(ctx_len[(hg + 1) / s.Hkv], s.nb_max) : 0;
+    auto where = [&](int idx, int& hs, int& blk0, int& nbv) {
+      hs = (kHeadsCached > 1 && idx >= ft1) ? 1 : 0;
+      blk0 = (idx - (hs ? ft1 : ft0)) * kTileBlocks;
+      nbv = hs ? nbh1 : nbh0;
+    };
 
     // issue tile k of this warp into its stage; rows past the head's valid blocks are not read
     auto issue = [&](int k) {
       if (k < ntiles) {
-        int head, blk0;
-        map.locate(g0 + warp + k * kPsWarps, head, blk0);
-        const int b = head / s.Hkv;
-        const int nb = clamp_nb(ctx_len[b], s.nb_max);
-        const int rows = min(kTileBlocks, nb - blk0);
+        int hs, blk0, nbv;
+        where(g0 + warp + k * kPsWarps, hs, blk0, nbv);
+        const int head = hg + hs;
+        const int rows = min(kTileBlocks, nbv - blk0);
         const uint8_t* src = reinterpret_cast<const uint8_t*>(kp + ((long long)head * s.nb_max + blk0) * kPK);
         const uint32_t dst = ring + (k % kStages) * kTileBytes;
 #pragma unroll
@@ -242,12 +254,10 @@ score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restr
       issue(k + kStages - 1);
       ps_wait<kStages - 1>();
       __syncwarp();
-      int head, blk0;
-      map.locate(g0 + warp + k * kPsWarps, head, blk0);
-      const int hs = head - hg;
-      const int b = head / s.Hkv;
-      const int nb = clamp_nb(ctx_len[b], s.nb_max);
-      const int blk1 = min(nb, blk0 + kTileBlocks);
+      int hs, blk0, nbv;
+      where(g0 + warp + k * kPsWarps, hs, blk0, nbv);
+      const int head = hg + hs;
+      const int blk1 = min(nbv, blk0 + kTileBlocks);
       const uint32_t stage = ring + (k % kStages) * kTileBytes;
       uint4 ra[8], rb[8];
 #pragma unroll
@@ -284,21 +294,29 @@ score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restr
       m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
       m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
       m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
-      float s0 = 0.f, s1 = 0.f;
+      // |k'|^2 of the 16 rows: the diagonal of the Gram tile K' K'^T, formed on the
+      // tensor cores from the A fragments themselves (the B fragment of column n is
+      // row n's own A words).  Row r's entry sits in lane 4 (r & 7) + ((r & 7) >> 1).
+      // The products are exact and positive, so the fp32 sum is at most 2^-15.9 of
+      // itself below the exact one; (1 + 2^-14) makes it an upper bound.
+      float gr[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const uint32_t A[4] = {ra[i].x, ra[i].y, ra[i].z, ra[i].w};
         const uint32_t Bw[4] = {rb[i].x, rb[i].y, rb[i].z, rb[i].w};
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          s0 = fmaf(bf_lo(A[w]), bf_lo(A[w]), s0); s0 = fmaf(bf_hi(A[w]), bf_hi(A[w]), s0);
-          s1 = fmaf(bf_lo(Bw[w]), bf_lo(Bw[w]), s1); s1 = fmaf(bf_hi(Bw[w]), bf_hi(Bw[w]), s1);
+        for (int hh = 0; hh < 2; ++hh) {
+          mma_bf16_16816(gr[0][0], gr[0][1], gr[0][2], gr[0][3], A[2 * hh], Bw[2 * hh], A[2 * hh + 1],
+                         Bw[2 * hh + 1], A[2 * hh], A[2 * hh + 1]);
+          mma_bf16_16816(gr[1][0], gr[1][1], gr[1][2], gr[1][3], A[2 * hh], Bw[2 * hh], A[2 * hh + 1],
+                         Bw[2 * hh + 1], Bw[2 * hh], Bw[2 * hh + 1]);
         }
       }
-      s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
-      s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
-      s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
-      s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+      const int holder = 4 * g + (g >> 1);
+      const float d0 = (g & 1) ? gr[0][1] : gr[0][0];   // row g, column g
+      const float d1 = (g & 1) ? gr[1][3] : gr[1][2];   // row g + 8, column g + 8
+      const float s0 = __shfl_sync(0xffffffffu, d0, holder) * 1.00006103515625f;  // x (1 + 2^-14)
+      const float s1 = __shfl_sync(0xffffffffu, d1, holder) * 1.00006103515625f;
       if (t == 0) {
         const float qnorm = sqrtf(sm.qn2[hs]);
         float2* out = scores + (long long)head * s.nb_max;
