@@ -707,13 +707,15 @@ def light_measure(args, st, q_dev, qla_dev, start, preroll, steps, appends, worl
         eager(start + k)
     torch.cuda.synchronize()
     first = start + preroll
-    marks = GraphEvents(L * steps * 2 + 16)
+    marks = GraphEvents(L * steps * 3 + 16)
+    marks.names = {"score", "topk", "end"}
     ts_first = first % n_in
     if ts_first + steps > n_in:
         ts_first = 0
     # the graph's LRU clock starts at `first`; its inputs are steps ts_first.. of the query buffers
     ms, clk = _timed_graph_at(st, first, ts_first, q_dev, qla_dev, steps, args.copy, appends, world, dev, marks)
-    score_ms = marks.durations()["score"]
+    durs = marks.durations()
+    score_ms, topk_ms = durs["score"], durs["topk"]
     marks.close()
     attended = torch.zeros((), dtype=torch.int64, device=dev)
     fetched = torch.zeros((), dtype=torch.int64, device=dev)
@@ -731,6 +733,7 @@ def light_measure(args, st, q_dev, qla_dev, start, preroll, steps, appends, worl
     return {"value": aggregate_value(world, L, steps, ms), "unit": UNIT, "steps": steps,
             "ms_per_step": ms / steps, "path_hbm_gbs": path, "path_hbm_frac": path / peak,
             "scorer_us": round(1000.0 * sc_avg, 2),
+            "topk_diff_us_p50": round(1000.0 * statistics.median(topk_ms), 2) if topk_ms else None,
             "scorer_frac": ab["score"] / (sc_avg / 1000.0) / 1e9 / peak,
             "attended_blocks_per_head": round(att, 2), "fetched_bytes_per_step": int(fetched_step),
             "fetched_gbs": fetched_step / (ms / steps / 1000.0) / 1e9,

@@ -15,8 +15,9 @@
 // Streaming.  A tile (16 consecutive blocks of one head) is 8 KiB of contiguous
 // memory.  Each warp streams its tiles through a ring of kStages shared-memory
 // stages with cp.async (16 bytes per lane per copy, 512 contiguous bytes per
-// warp instruction), so kStages - 1 tiles are in flight while one is computed;
-// one CTA of 8 warps per SM keeps up to 7 x 16 tiles (128 KiB) moving.  Rows are
+// warp instruction); a stage is refilled as soon as its tile is in registers, so
+// kStages tiles are in flight while one is computed: one CTA of 8 warps per SM
+// keeps up to 24 tiles (192 KiB) moving.  Rows are
 // stored with their 16-byte chunks XOR-ed by (row & 1) << 2, which makes the
 // fragment reads below conflict-free.
 //
@@ -249,9 +250,11 @@ score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restr
       ps_commit();  // one group per tile slot (empty past the end), so wait_group counts tiles
     };
 #pragma unroll
-    for (int k = 0; k < kStages - 1; ++k) issue(k);
+    // every stage is filled up front; a stage is refilled as soon as its tile is in
+    // registers, so kStages tiles are in flight while one is computed
+#pragma unroll
+    for (int k = 0; k < kStages; ++k) issue(k);
     for (int k = 0; k < ntiles; ++k) {
-      issue(k + kStages - 1);
       ps_wait<kStages - 1>();
       __syncwarp();
       int hs, blk0, nbv;
@@ -265,7 +268,8 @@ score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restr
         ra[i] = ps_lds(stage + ps_swz(g, t + 4 * i));
         rb[i] = ps_lds(stage + ps_swz(g + 8, t + 4 * i));
       }
-      __syncwarp();  // the stage is free for the copy issued in the next iteration
+      __syncwarp();  // every lane has its fragments: the stage takes the tile kStages ahead
+      issue(k + kStages);
       const int r0 = blk0 + g, r1 = blk0 + g + 8;
       float acc[NT][4];
 #pragma unroll
