@@ -36,8 +36,9 @@
 
 namespace oasis {
 
-constexpr int kSelThreads = 256;
+constexpr int kSelThreads = 256;               // threads per CTA (512 for few heads with long contexts)
 constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelMaxWarps = 16;
 constexpr int kLimbs = 17;
 constexpr int kMaxN = 32;      // lookahead queries x GQA group
 
@@ -224,15 +225,16 @@ __device__ __forceinline__ int block_excl_scan(int v, int* red, int* total) {
   }
   if (lane == 31) red[warp] = x;
   __syncthreads();
+  const int nw = blockDim.x >> 5;
   if (warp == 0) {
-    int w = lane < kSelWarps ? red[lane] : 0;
+    int w = lane < nw ? red[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += y;
     }
-    if (lane < kSelWarps) red[lane] = w;
-    if (lane == kSelWarps - 1) *total = w;
+    if (lane < nw) red[lane] = w;
+    if (lane == nw - 1) *total = w;
   }
   __syncthreads();
   const int base = warp ? red[warp - 1] : 0;
@@ -247,7 +249,7 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   if (lane == 0) red[warp] = v;
   __syncthreads();
   float r = red[0];
-  for (int i = 1; i < kSelWarps; ++i) r = fmaxf(r, red[i]);
+  for (int i = 1; i < (int)(blockDim.x >> 5); ++i) r = fmaxf(r, red[i]);
   __syncthreads();
   return r;
 }
@@ -333,7 +335,7 @@ __device__ void kth_bracket(const float2* se, int n, int k, uint32_t* hist, int*
   if (threadIdx.x == 0) { *tslot = neg_inf(); scal[5] = 0; }
   __syncthreads();
   mn = fs[0]; mx = fs[1]; em = fs[2];
-  for (int w = 1; w < kSelWarps; ++w) {
+  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
     mn = fminf(mn, fs[3 * w]); mx = fmaxf(mx, fs[3 * w + 1]); em = fmaxf(em, fs[3 * w + 2]);
   }
   emax = em;
@@ -481,7 +483,7 @@ __device__ void stage_queries(SelCtx& c) {
     }
   }
   __syncthreads();
-  for (int n = warp; n < c.N; n += kSelWarps) {
+  for (int n = warp; n < c.N; n += (int)(blockDim.x >> 5)) {
     const uint32_t w0 = reinterpret_cast<const uint32_t*>(c.qb + n * kD)[lane];
     const uint32_t w1 = reinterpret_cast<const uint32_t*>(c.qb + n * kD)[lane + 32];
     float ss = bf_lo(w0) * bf_lo(w0);
@@ -692,7 +694,8 @@ __device__ void refine_top_r(SelCtx& c, const int* U, int nU, int r, const int* 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   stage_queries(c);
   const bool single = nU <= c.kcap;
-  const int chunk = single ? nU : kSelWarps;
+  const int nw = blockDim.x >> 5;
+  const int chunk = single ? nU : nw;
   uint32_t* vals = single ? c.tval : c.bval;  // exact values of this round's candidates
   int tcount = 0;
   uint32_t* tv = c.tval;
@@ -701,7 +704,7 @@ __device__ void refine_top_r(SelCtx& c, const int* U, int nU, int r, const int* 
   int* ti2 = c.tidx2;
   for (int base = 0; base < nU; base += chunk) {
     const int nbat = min(chunk, nU - base);
-    for (int i = warp; i < nbat; i += kSelWarps) {
+    for (int i = warp; i < nbat; i += nw) {
       const int ci = U[base + i];
       const int blk = cand_blk ? cand_blk[ci] : ci;
       if constexpr (kPooled)
@@ -786,10 +789,6 @@ __device__ void select_best(SelCtx& c, const float2* se, int n, int k, const int
     c.qstate = 3;
   }
   __syncthreads();
-  // classify; an uncertain block's keys are prefetched into L2 at once, so the
-  // exact refine that follows finds them there (at most kPrefetchBlocks blocks)
-  constexpr int kLines = kPooled ? 2 * kD * 2 / 128 : kBS * kD * 2 / 128;
-  constexpr int kPrefetchBlocks = 64;
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const float2 v = se[i];
     const float lo = __fsub_rd(v.x, v.y), hi = __fadd_ru(v.x, v.y);
@@ -801,14 +800,7 @@ __device__ void select_best(SelCtx& c, const float2* se, int n, int k, const int
       cl = 0;
     } else {
       cl = 2;
-      const int slot = atomicAdd(&c.scal[2], 1);
-      U[slot] = i;
-      if (slot < kPrefetchBlocks) {
-        const int blk = cand_blk ? cand_blk[i] : i;
-        const char* base = reinterpret_cast<const char*>(c.k + (long long)blk * (kPooled ? 2 * kD : kBS * kD));
-#pragma unroll 4
-        for (int ln = 0; ln < kLines; ++ln) asm volatile("prefetch.global.L2 [%0];" ::"l"(base + ln * 128));
-      }
+      U[atomicAdd(&c.scal[2], 1)] = i;
     }
     cls[i] = cl;
   }
@@ -821,6 +813,19 @@ __device__ void select_best(SelCtx& c, const float2* se, int n, int k, const int
     __syncthreads();
     return;
   }
+  // the refine takes one block per warp and round: bring the keys of the later
+  // rounds (up to kPrefetchBlocks blocks) into L2 now
+  constexpr int kLines = kPooled ? 2 * kD * 2 / 128 : kBS * kD * 2 / 128;
+  constexpr int kPrefetchBlocks = 64;
+  const int nw = blockDim.x >> 5;
+  const int npre = min(nU, nw + kPrefetchBlocks) - nw;
+  for (int idx = threadIdx.x; idx < npre * kLines; idx += blockDim.x) {
+    const int ci = U[nw + idx / kLines];
+    const int blk = cand_blk ? cand_blk[ci] : ci;
+    const char* line = reinterpret_cast<const char*>(c.k + (long long)blk * (kPooled ? 2 * kD : kBS * kD)) +
+                       (idx % kLines) * 128;
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(line));
+  }
   refine_top_r<kPooled>(c, U, nU, r, cand_blk, cls);
 }
 
@@ -832,24 +837,26 @@ struct SelLayout {
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
-__host__ __device__ inline SelLayout sel_layout(int ncap, bool with_cblk, int kb) {
+// ncap: entries of the candidate list; kb: the budget (the diff's lists are at most
+// kb long); nw: warps per CTA.
+__host__ __device__ inline SelLayout sel_layout(int ncap, bool with_cblk, int kb, int nw = kSelWarps) {
   SelLayout L;
   size_t o = 0;
   L.se = o; o = align16(o + sizeof(float2) * ncap);
   L.cls = o; o = align16(o + ncap);
   L.U = o; o = align16(o + sizeof(int) * ncap);
-  L.cblk = o; o = align16(o + (with_cblk ? sizeof(int) * ncap : 0));
-  L.kst = o; o = align16(o + sizeof(uint16_t) * kSelWarps * kBS * kD);
+  L.cblk = o; o = align16(o + (with_cblk ? sizeof(int) * kb : 0));
+  L.kst = o; o = align16(o + sizeof(uint16_t) * nw * kBS * kD);
   L.qb = o; o = align16(o + sizeof(uint16_t) * kMaxN * kD);
   L.qn = o; o = align16(o + sizeof(float) * kMaxN);
-  L.tmp = o; o = align16(o + sizeof(uint32_t) * kSelWarps * kLimbs);
-  L.bval = o; o = align16(o + sizeof(uint32_t) * kSelWarps * kLimbs);
-  L.bidx = o; o = align16(o + sizeof(int) * kSelWarps);
+  L.tmp = o; o = align16(o + sizeof(uint32_t) * nw * kLimbs);
+  L.bval = o; o = align16(o + sizeof(uint32_t) * nw * kLimbs);
+  L.bidx = o; o = align16(o + sizeof(int) * nw);
   L.tval = o; o = align16(o + sizeof(uint32_t) * kb * kLimbs);
   L.tidx = o; o = align16(o + sizeof(int) * kb);
   L.tval2 = o; o = align16(o + sizeof(uint32_t) * kb * kLimbs);
   L.tidx2 = o; o = align16(o + sizeof(int) * kb);
-  L.rank = o; o = align16(o + sizeof(int) * (kb + kSelWarps));
+  L.rank = o; o = align16(o + sizeof(int) * (kb + nw));
   L.hist = o; o = align16(o + sizeof(uint32_t) * 512);
   L.scal = o; o = align16(o + sizeof(int) * 8);
   L.fscal = o; o = align16(o + sizeof(float) * (64 + 512));
@@ -948,14 +955,14 @@ __device__ void diff_emit(const Shape& s, int nM, const uint8_t* cls, const int*
 // CTA (one launch for top-K and capped diff).  The passes form one loop that is
 // not unrolled, so both run the same copy of the selection code and the second
 // finds it in the instruction cache.
-template <bool kPooled, bool kDiff>
-__global__ void __launch_bounds__(kSelThreads, 2)
+template <bool kPooled, bool kDiff, int NTH = kSelThreads>
+__global__ void __launch_bounds__(NTH, 512 / NTH)
 topk_select_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __restrict__ k_hbm,
                    const uint16_t* __restrict__ q_la, const int* __restrict__ ctx_len,
                    int* __restrict__ sel, int* __restrict__ nsel, const int* __restrict__ blk2slot, int cap,
                    int* __restrict__ fetch, int* __restrict__ nfetch, const uint16_t* __restrict__ host_kv) {
   extern __shared__ __align__(16) char sm[];
-  const SelLayout L = sel_layout(s.nb_max, kDiff, s.Kb);
+  const SelLayout L = sel_layout(s.nb_max, kDiff, s.Kb, NTH / 32);
   const int head = blockIdx.x;
   const int b = head / s.Hkv;
   const int ctx = ctx_len[b];
@@ -968,7 +975,12 @@ topk_select_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* _
   int* red = reinterpret_cast<int*>(sm + L.red);
   int* cblk = reinterpret_cast<int*>(sm + L.cblk);
   const float2* src = scores + (long long)head * s.nb_max;
-  for (int i = threadIdx.x; i < nb; i += blockDim.x) se[i] = src[i];
+  {  // 16-byte loads (two entries) where the row allows, then the odd tail entry
+    const int n2 = (((reinterpret_cast<uintptr_t>(src) & 15) == 0) ? nb : 0) >> 1;
+    for (int i = threadIdx.x; i < n2; i += blockDim.x)
+      reinterpret_cast<float4*>(se)[i] = reinterpret_cast<const float4*>(src)[i];
+    for (int i = 2 * n2 + threadIdx.x; i < nb; i += blockDim.x) se[i] = src[i];
+  }
   if (nb > s.Kb) issue_queries(c);
   if (kDiff) {  // the diff reads this head's blk2slot row after the top-K: bring it into L2 now
     const char* row = reinterpret_cast<const char*>(blk2slot + (long long)head * s.nb_max);
@@ -990,7 +1002,7 @@ topk_select_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* _
     select_best<kPooled>(c, se, n, k, cb, cls, U);
     if (pass == 0) {
       // compaction in ascending block order
-      const int per = (nb + kSelThreads - 1) / kSelThreads;
+      const int per = (nb + NTH - 1) / NTH;
       const int i0 = threadIdx.x * per, i1 = min(nb, i0 + per);
       int cnt = 0;
       for (int i = i0; i < i1; ++i) cnt += cls[i] == 1;
@@ -1043,19 +1055,35 @@ fetch_diff_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __
 size_t topk_smem_bytes(const Shape& s) { return sel_layout(s.nb_max, false, s.Kb).total; }
 size_t diff_smem_bytes(const Shape& s) { return sel_layout(s.Kb, true, s.Kb).total; }
 
+template <bool kPooled, bool kDiff, int NTH>
+static cudaError_t launch_topk_nth(const Shape& s, const float2* scores, const uint16_t* k, const uint16_t* q_la,
+                                   const int* ctx, int* sel, int* nsel, cudaStream_t stream, const int* blk2slot,
+                                   int cap, int* fetch, int* nfetch, const uint16_t* host_kv) {
+  static int attr_cache[kMaxDevicesCached] = {};
+  const size_t smem = sel_layout(s.nb_max, kDiff, s.Kb, NTH / 32).total;
+  cudaError_t e = ensure_dyn_smem((const void*)topk_select_kernel<kPooled, kDiff, NTH>, smem, attr_cache);
+  if (e != cudaSuccess) return e;
+  topk_select_kernel<kPooled, kDiff, NTH><<<s.B * s.Hkv, NTH, smem, stream>>>(s, scores, k, q_la, ctx, sel, nsel,
+                                                                              blk2slot, cap, fetch, nfetch, host_kv);
+  return cudaGetLastError();
+}
+
+// Long candidate lists over few heads (at most one CTA per SM anyway) get 16 warps
+// per head for the passes over all blocks; everything else 8 warps, two CTAs per SM.
 template <bool kPooled, bool kDiff = false>
 static cudaError_t launch_topk(const Shape& s, const float2* scores, const uint16_t* k, const uint16_t* q_la,
                                const int* ctx, int* sel, int* nsel, cudaStream_t stream,
                                const int* blk2slot = nullptr, int cap = 0, int* fetch = nullptr,
                                int* nfetch = nullptr, const uint16_t* host_kv = nullptr) {
-  static int attr_cache[kMaxDevicesCached] = {};
-  const size_t smem = sel_layout(s.nb_max, kDiff, s.Kb).total;
-  cudaError_t e = ensure_dyn_smem((const void*)topk_select_kernel<kPooled, kDiff>, smem, attr_cache);
-  if (e != cudaSuccess) return e;
-  topk_select_kernel<kPooled, kDiff><<<s.B * s.Hkv, kSelThreads, smem, stream>>>(s, scores, k, q_la, ctx, sel, nsel,
-                                                                                  blk2slot, cap, fetch, nfetch,
-                                                                                  host_kv);
-  return cudaGetLastError();
+  if constexpr (kDiff) {
+    const bool wide = s.nb_max > 4096 && s.B * s.Hkv <= sm_count() &&
+                      sel_layout(s.nb_max, kDiff, s.Kb, 16).total <= 227 * 1024;
+    if (wide)
+      return launch_topk_nth<kPooled, kDiff, 512>(s, scores, k, q_la, ctx, sel, nsel, stream, blk2slot, cap, fetch,
+                                                  nfetch, host_kv);
+  }
+  return launch_topk_nth<kPooled, kDiff, kSelThreads>(s, scores, k, q_la, ctx, sel, nsel, stream, blk2slot, cap,
+                                                      fetch, nfetch, host_kv);
 }
 
 cudaError_t launch_topk_select_diff(const Shape& s, const float2* scores, const uint16_t* k, const uint16_t* q_la,

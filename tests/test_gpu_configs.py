@@ -21,10 +21,12 @@ def _lib():
     build.build()
 
 
-def test_llama_long_input_shape_128k_context():
+@pytest.mark.parametrize("scoring", ["maxdot", "pooled"])
+def test_llama_long_input_shape_128k_context(scoring):
+    """8,192 blocks per head over few heads: the selection runs 16 warps per head."""
     w = syn.llama31_8b_long(B=1, L=1)
     assert w.nb_max == 8192 and w.C == 6
-    c = Case(w)
+    c = Case(w, scoring=scoring)
     c.step(0)
     c.step(1)
 
