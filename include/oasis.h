@@ -535,6 +535,13 @@ OASIS_API oasis_status oasis_touch_host(const void* host_ptr, size_t bytes, uint
  *   (an atomic load, no environment lookup).
  */
 #define OASIS_OPT_SCORE_KERNEL 2
+/*
+ * OASIS_OPT_COPY_CTAS: the thread blocks (4 warps each) of oasis_copy_fetched and
+ *   oasis_copy_fetched_wait; 0 (the default) = one warp per fetch entry up to four
+ *   blocks per SM.  A small value confines the zero-copy host reads to a few SMs
+ *   (each warp then streams several entries); results do not depend on it.
+ */
+#define OASIS_OPT_COPY_CTAS 3
 #define OASIS_SCORE_KERNEL_MMA 0
 #define OASIS_SCORE_KERNEL_TC 1
 OASIS_API oasis_status oasis_set_option(int32_t option, int32_t value);

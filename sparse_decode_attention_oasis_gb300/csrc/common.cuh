@@ -91,6 +91,7 @@ __device__ __forceinline__ float key_float(uint32_t k) {
 
 // Process-wide launch option set by oasis_set_option (0 = the kernel's own choice).
 int score_ctas_per_sm_option();
+int copy_ctas_option();
 
 // Host-side caches so that a launch costs no more than the launch itself.
 constexpr int kMaxDevicesCached = 64;

@@ -318,6 +318,8 @@ __global__ void __launch_bounds__(kCopyWarps * 32) copy_fetched_kernel(Shape s, 
 }
 
 static int copy_grid(const Shape& s) {
+  const int fixed = copy_ctas_option();  // a caller may confine the copy to a few SMs
+  if (fixed > 0) return fixed;
   // one warp per live entry up to four CTAs per SM; a warp streams any further entries
   const long long items = (long long)s.B * s.Hkv * s.Kb;
   long long ctas = (items + kCopyWarps - 1) / kCopyWarps;
