@@ -16,8 +16,9 @@
 // memory.  Each warp streams its tiles through a ring of kStages shared-memory
 // stages with cp.async (16 bytes per lane per copy, 512 contiguous bytes per
 // warp instruction); a stage is refilled as soon as its tile is in registers, so
-// kStages tiles are in flight while one is computed: one CTA of 8 warps per SM
-// keeps up to 24 tiles (192 KiB) moving.  Rows are
+// kStages tiles are in flight while one is computed: one CTA of 12 warps per SM
+// (three per scheduler, to hide the tile's instruction latency) keeps up to 24
+// tiles (192 KiB) moving.  Rows are
 // stored with their 16-byte chunks XOR-ed by (row & 1) << 2, which makes the
 // fragment reads below conflict-free.
 //
@@ -40,7 +41,7 @@
 
 namespace oasis {
 
-constexpr int kPsWarps = 8;
+constexpr int kPsWarps = 12;
 constexpr int kTileBlocks = 16;
 constexpr int kPK = 2 * kD;                             // pooled elements per block
 constexpr int kTileBytes = kTileBlocks * kPK * 2;       // 8 KiB
@@ -117,7 +118,7 @@ template <int NT, bool kCopy>
 __global__ void __launch_bounds__(kPsWarps * 32, 1)
 score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restrict__ ctx_len,
                     const uint16_t* __restrict__ q_la, float2* __restrict__ scores, float inv_sqrt_d, CopyJob job) {
-  constexpr int kStages = kCopy ? 2 : 3;
+  constexpr int kStages = kCopy ? 1 : 2;
   constexpr int kHeadsCached = HeadsCached<NT>::value;
   extern __shared__ __align__(128) uint8_t ps_dyn[];
   PooledSmem<NT>& sm = *reinterpret_cast<PooledSmem<NT>*>(ps_dyn);
@@ -345,7 +346,7 @@ score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restr
 
 template <int NT, bool kCopy>
 static size_t pooled_smem_bytes() {
-  constexpr int kStages = kCopy ? 2 : 3;
+  constexpr int kStages = kCopy ? 1 : 2;
   return ((sizeof(PooledSmem<NT>) + 127) & ~size_t(127)) + (size_t)kPsWarps * kStages * kTileBytes +
          (kCopy ? (size_t)kPsWarps * kCopyUnitBytes : 0);
 }

@@ -455,24 +455,8 @@ __device__ void stage_queries(SelCtx& c) {
   if (c.qstate == 2) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (c.qstate == 3) {
-    // landed and visible (a CTA barrier followed every thread's wait): each warp
-    // forms all N norms itself, so no further barrier is needed (every warp
-    // writes the same values)
-    for (int n = 0; n < c.N; ++n) {
-      const uint32_t w0 = reinterpret_cast<const uint32_t*>(c.qb + n * kD)[lane];
-      const uint32_t w1 = reinterpret_cast<const uint32_t*>(c.qb + n * kD)[lane + 32];
-      float ss = bf_lo(w0) * bf_lo(w0);
-      ss = fmaf(bf_hi(w0), bf_hi(w0), ss);
-      ss = fmaf(bf_lo(w1), bf_lo(w1), ss);
-      ss = fmaf(bf_hi(w1), bf_hi(w1), ss);
-      ss = warp_sum(ss);
-      if (lane == 0) c.qn[n] = sqrtf(ss);
-    }
-    __syncwarp();
-    c.qstate = 2;
-    return;
-  }
-  if (c.qstate == 1) {
+    // landed and visible already (a CTA barrier followed every thread's wait)
+  } else if (c.qstate == 1) {
     sel_cp_async_wait_all();
   } else {
     for (int idx = threadIdx.x; idx < c.N * 16; idx += blockDim.x) {
@@ -482,7 +466,7 @@ __device__ void stage_queries(SelCtx& c) {
       reinterpret_cast<uint4*>(c.qb + n * kD)[part] = v;
     }
   }
-  __syncthreads();
+  if (c.qstate != 3) __syncthreads();  // state 3: already visible
   for (int n = warp; n < c.N; n += (int)(blockDim.x >> 5)) {
     const uint32_t w0 = reinterpret_cast<const uint32_t*>(c.qb + n * kD)[lane];
     const uint32_t w1 = reinterpret_cast<const uint32_t*>(c.qb + n * kD)[lane + 32];
