@@ -13,19 +13,15 @@
 // 512 bytes per block instead of 4 KiB.
 //
 // Streaming.  A tile (16 consecutive blocks of one head) is 8 KiB of contiguous
-// memory.  Each warp streams its tiles through a ring of kStages shared-memory
-// stages with cp.async (16 bytes per lane per copy, 512 contiguous bytes per
-// warp instruction); a stage is refilled as soon as its tile is in registers, so
-// kStages tiles are in flight while one is computed: one CTA of 12 warps per SM
-// (three per scheduler, to hide the tile's instruction latency) keeps up to 24
-// tiles (192 KiB) moving.  Rows are
-// stored with their 16-byte chunks XOR-ed by (row & 1) << 2, which makes the
-// fragment reads below conflict-free.
+// memory; each thread loads its A fragments of a tile straight into registers
+// with sixteen 16-byte loads (every warp instruction covers full 32-byte
+// sectors), 4 CTAs of 4 warps per SM.  (A cp.async shared-memory ring per warp
+// reached only 4.3 TB/s with no MMA at all: the register loads stream faster.)
 //
 // Work split.  The valid tiles of all heads (ceil(nb_b / 16) per head of request
 // b) form one sequence in (request, KV head, tile) order; CTA c takes an equal
 // contiguous share and its warps interleave over it, so heads with short
-// contexts cost nothing and every SM gets the same number of tiles.  The share
+// contexts cost nothing and every CTA gets the same number of tiles.  The share
 // spans few heads: the Q' fragments of up to kHeadsCached heads at a time are
 // built in shared memory (fragment order) between two barriers.
 //
@@ -41,14 +37,13 @@
 
 namespace oasis {
 
-constexpr int kPsWarps = 12;
+constexpr int kPsWarps = 4;
 constexpr int kTileBlocks = 16;
 constexpr int kPK = 2 * kD;                             // pooled elements per block
-constexpr int kTileBytes = kTileBlocks * kPK * 2;       // 8 KiB
 constexpr int kMaxPrefix = 512;                         // requests with an exact tile prefix
 
-// Q' fragment sets held at once: two heads up to 16 query rows, one above (the
-// ring and the fragments must fit in one SM's shared memory)
+// Q' fragment sets held at once: two heads up to 16 query rows, one above (three
+// CTAs share an SM's shared memory)
 template <int NT>
 struct HeadsCached { static constexpr int value = NT <= 2 ? 2 : 1; };
 
@@ -68,22 +63,6 @@ __device__ __forceinline__ uint32_t bf2_neg(uint32_t w) {
   const uint32_t m = ((w & 0x8000u) ? 0xffffu : 0u) | ((w & 0x80000000u) ? 0xffff0000u : 0u);
   return w & m;
 }
-
-__device__ __forceinline__ void ps_cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void ps_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void ps_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-__device__ __forceinline__ uint4 ps_lds(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-
-// byte offset of 16-byte chunk c of row r inside a staged tile
-__device__ __forceinline__ uint32_t ps_swz(int r, int c) { return (uint32_t)(r * (kPK * 2) + ((c ^ ((r & 1) << 2)) << 4)); }
 
 // Tile sequence of the launch: tile index -> (head, first block of the tile).
 struct TileMap {
@@ -115,22 +94,20 @@ struct TileMap {
 };
 
 template <int NT, bool kCopy>
-__global__ void __launch_bounds__(kPsWarps * 32, 1)
+__global__ void __launch_bounds__(kPsWarps * 32, 4)
 score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restrict__ ctx_len,
                     const uint16_t* __restrict__ q_la, float2* __restrict__ scores, float inv_sqrt_d, CopyJob job) {
-  constexpr int kStages = kCopy ? 1 : 2;
   constexpr int kHeadsCached = HeadsCached<NT>::value;
   extern __shared__ __align__(128) uint8_t ps_dyn[];
   PooledSmem<NT>& sm = *reinterpret_cast<PooledSmem<NT>*>(ps_dyn);
-  uint8_t* ring_base = ps_dyn + ((sizeof(PooledSmem<NT>) + 127) & ~size_t(127));
+  uint8_t* copy_base = ps_dyn + ((sizeof(PooledSmem<NT>) + 127) & ~size_t(127));
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   const long long gwarp = (long long)blockIdx.x * kPsWarps + warp;
   const long long nwarps = (long long)gridDim.x * kPsWarps;
-  uint4* copy_buf = reinterpret_cast<uint4*>(ring_base + (size_t)kPsWarps * kStages * kTileBytes);
+  uint4* copy_buf = reinterpret_cast<uint4*>(copy_base);
   if constexpr (kCopy) copy_begin(job, s, gwarp, nwarps, copy_buf + warp * (kCopyUnitBytes / 16), lane);
-  const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(ring_base)) + warp * kStages * kTileBytes;
   const int G = s.Hq / s.Hkv;
   const int N = s.n_la * G;
 
@@ -235,43 +212,19 @@ score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restr
       nbv = hs ? nbh1 : nbh0;
     };
 
-    // issue tile k of this warp into its stage; rows past the head's valid blocks are not read
-    auto issue = [&](int k) {
-      if (k < ntiles) {
-        int hs, blk0, nbv;
-        where(g0 + warp + k * kPsWarps, hs, blk0, nbv);
-        const int head = hg + hs;
-        const int rows = min(kTileBlocks, nbv - blk0);
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(kp + ((long long)head * s.nb_max + blk0) * kPK);
-        const uint32_t dst = ring + (k % kStages) * kTileBytes;
-#pragma unroll
-        for (int m = 0; m < kTileBlocks; ++m)
-          if (m < rows) ps_cp_async16(dst + ps_swz(m, lane), src + m * (kPK * 2) + lane * 16);
-      }
-      ps_commit();  // one group per tile slot (empty past the end), so wait_group counts tiles
-    };
-#pragma unroll
-    // every stage is filled up front; a stage is refilled as soon as its tile is in
-    // registers, so kStages tiles are in flight while one is computed
-#pragma unroll
-    for (int k = 0; k < kStages; ++k) issue(k);
     for (int k = 0; k < ntiles; ++k) {
-      ps_wait<kStages - 1>();
-      __syncwarp();
       int hs, blk0, nbv;
       where(g0 + warp + k * kPsWarps, hs, blk0, nbv);
       const int head = hg + hs;
       const int blk1 = min(nbv, blk0 + kTileBlocks);
-      const uint32_t stage = ring + (k % kStages) * kTileBytes;
+      const uint16_t* base = kp + (long long)head * s.nb_max * kPK;
+      const int r0 = blk0 + g, r1 = blk0 + g + 8;
       uint4 ra[8], rb[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        ra[i] = ps_lds(stage + ps_swz(g, t + 4 * i));
-        rb[i] = ps_lds(stage + ps_swz(g + 8, t + 4 * i));
+        ra[i] = r0 < blk1 ? ldg_stream(base + (long long)r0 * kPK + (t + 4 * i) * 8) : make_uint4(0u, 0u, 0u, 0u);
+        rb[i] = r1 < blk1 ? ldg_stream(base + (long long)r1 * kPK + (t + 4 * i) * 8) : make_uint4(0u, 0u, 0u, 0u);
       }
-      __syncwarp();  // every lane has its fragments: the stage takes the tile kStages ahead
-      issue(k + kStages);
-      const int r0 = blk0 + g, r1 = blk0 + g + 8;
       float acc[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
@@ -339,16 +292,13 @@ score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restr
         }
       }
     }
-    ps_wait<0>();  // the empty trailing groups: nothing is left in flight
   }
   if constexpr (kCopy) copy_finish(job, s, gwarp, nwarps, copy_buf + warp * (kCopyUnitBytes / 16), lane);
 }
 
 template <int NT, bool kCopy>
 static size_t pooled_smem_bytes() {
-  constexpr int kStages = kCopy ? 1 : 2;
-  return ((sizeof(PooledSmem<NT>) + 127) & ~size_t(127)) + (size_t)kPsWarps * kStages * kTileBytes +
-         (kCopy ? (size_t)kPsWarps * kCopyUnitBytes : 0);
+  return ((sizeof(PooledSmem<NT>) + 127) & ~size_t(127)) + (kCopy ? (size_t)kPsWarps * kCopyUnitBytes : 0);
 }
 
 template <int NT, bool kCopy>
@@ -358,8 +308,15 @@ static cudaError_t launch_nt2(const Shape& s, const uint16_t* kp, const int* ctx
   const size_t smem = pooled_smem_bytes<NT, kCopy>();
   cudaError_t e = ensure_dyn_smem((const void*)score_pooled_kernel<NT, kCopy>, smem, attr_cache);
   if (e != cudaSuccess) return e;
-  // one CTA per SM (its shared memory); OASIS_OPT_SCORE_CTAS_PER_SM cannot raise that
-  const int grid = sm_count();
+  static int per_sm_cached[kMaxDevicesCached] = {};
+  int& per_sm = per_sm_cached[current_device()];
+  if (!per_sm) {
+    int v = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, score_pooled_kernel<NT, kCopy>, kPsWarps * 32, smem);
+    per_sm = v < 1 ? 1 : v;
+  }
+  const int cap = score_ctas_per_sm_option();
+  const int grid = sm_count() * (cap > 0 && cap < per_sm ? cap : per_sm);
   score_pooled_kernel<NT, kCopy><<<grid, kPsWarps * 32, smem, stream>>>(s, kp, ctx, q_la, scores,
                                                                        1.0f / sqrtf((float)s.d), job);
   return cudaGetLastError();
