@@ -14,13 +14,15 @@
 // (row mod 8) to spread the fragment reads over the banks.  Per block the warp
 // computes S = Q K^T with the G query heads as the rows of one m16n8k16 tile
 // (rows >= G are zero; the d axis is permuted identically for Q and K), runs the
-// online softmax in fp32 (exp2 with scale*log2(e) folded in), and accumulates
-// O += P V with P split into a bf16 high part and a bf16 residual (two MMAs, ~16
-// significant bits); V rows are re-paired into B fragments with byte permutes,
-// the output column of n-tile j / column n being d = 16 n + j.  The 4 warps merge
-// in shared memory; with one split the CTA writes the output, otherwise a second
-// kernel merges the splits of each query head.  The split count is chosen so
-// the grid covers the GPU about four times.
+// online softmax in fp32 (exp2 with scale*log2(e) folded in), and accumulates the
+// output transposed, O^T += V^T P^T, so that the 16 rows of each MMA are 16 of
+// the 128 output dimensions and the G queries its columns: the S accumulators
+// of a thread are exactly its B fragment of P^T, and ldmatrix.trans reads V's
+// A fragments straight from the staged rows.  Per block that is 8 d-slices x 2
+// MMAs (P split into a bf16 high part and a bf16 residual, ~16 significant bits)
+// and 32 fp32 accumulators per thread.  The 4 warps merge in shared memory; with
+// one split the CTA writes the output, otherwise a second kernel merges the
+// splits of each query head.
 #include "common.cuh"
 
 namespace oasis {
@@ -36,6 +38,15 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// Four 8x8 b16 matrices, transposed: lane 8i + r gives the address of row r of
+// matrix i; register i receives matrix i transposed (the A-fragment layout).
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                              uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
 __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -46,7 +57,7 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
 __device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 256 + ((c ^ (r & 7)) << 4)); }
 
 template <int G>
-__global__ void __launch_bounds__(kAttnWarps * 32, 2)
+__global__ void __launch_bounds__(kAttnWarps * 32, 3)
 attn_partial_kernel(Shape s, const uint16_t* __restrict__ q, const uint16_t* __restrict__ k_pool,
                     const uint16_t* __restrict__ v_pool, const int* __restrict__ sel,
                     const int* __restrict__ nsel, const int* __restrict__ blk2slot,
@@ -80,9 +91,15 @@ attn_partial_kernel(Shape s, const uint16_t* __restrict__ q, const uint16_t* __r
     for (int i = 0; i < 4; ++i) qa[i][0] = qa[i][1] = qa[i][2] = qa[i][3] = 0u;
   }
 
-  float o[16][4];
+  // O^T accumulators: slice m holds d = 16m + g (regs 0, 1) and 16m + g + 8
+  // (regs 2, 3) for queries 2t and 2t + 1
+  float o[8][4];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  for (int m = 0; m < 8; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.f;
+  // ldmatrix row of this lane: matrix i = lane / 8 covers tokens 8 (i / 2) .. + 7 and
+  // the lower (i even) or upper 8 dimensions of a 16-wide slice
+  const int lm_row = (lane & 7) + ((lane >> 4) << 3);
+  const int lm_hi = (lane >> 3) & 1;
   float m_run = neg_inf(), l_run = 0.f;
   const long long slot_base = (long long)head * s.P;
 
@@ -171,30 +188,22 @@ attn_partial_kernel(Shape s, const uint16_t* __restrict__ q, const uint16_t* __r
       rs += __shfl_xor_sync(0xffffffffu, rs, 2);
       l_run = l_run * alpha + rs;
       m_run = m_new;
+      // alpha of this thread's output columns (queries 2t, 2t + 1), held by rows 2t, 2t + 1
+      const float a0 = __shfl_sync(0xffffffffu, alpha, (2 * t) * 4);
+      const float a1 = __shfl_sync(0xffffffffu, alpha, (2 * t + 1) * 4);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) { o[j][0] *= alpha; o[j][1] *= alpha; }
+      for (int m = 0; m < 8; ++m) { o[m][0] *= a0; o[m][1] *= a1; o[m][2] *= a0; o[m][3] *= a1; }
+      // B fragments of P^T (tokens x queries): tokens 2t, 2t+1 of n-tile 0 and 1 for query g
       const uint32_t ph0 = pack_bf16x2(pv[0][0], pv[0][1]);
       const uint32_t ph1 = pack_bf16x2(pv[1][0], pv[1][1]);
       const uint32_t pl0 = pack_bf16x2(pv[0][0] - bf_lo(ph0), pv[0][1] - bf_hi(ph0));
       const uint32_t pl1 = pack_bf16x2(pv[1][0] - bf_lo(ph1), pv[1][1] - bf_hi(ph1));
-      uint4 vr[4][2];
-      const int vrow[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) vr[r][hf] = lds_v4(dv + swz(vrow[r], 2 * g + hf));
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const uint32_t sel_half = (j & 1) ? 0x7632u : 0x5410u;
-        const int wi = j >> 1;
-        const uint32_t w0[4] = {vr[0][wi >> 2].x, vr[0][wi >> 2].y, vr[0][wi >> 2].z, vr[0][wi >> 2].w};
-        const uint32_t w1[4] = {vr[1][wi >> 2].x, vr[1][wi >> 2].y, vr[1][wi >> 2].z, vr[1][wi >> 2].w};
-        const uint32_t w2[4] = {vr[2][wi >> 2].x, vr[2][wi >> 2].y, vr[2][wi >> 2].z, vr[2][wi >> 2].w};
-        const uint32_t w3[4] = {vr[3][wi >> 2].x, vr[3][wi >> 2].y, vr[3][wi >> 2].z, vr[3][wi >> 2].w};
-        const uint32_t b0 = __byte_perm(w0[wi & 3], w1[wi & 3], sel_half);
-        const uint32_t b1 = __byte_perm(w2[wi & 3], w3[wi & 3], sel_half);
-        mma_bf16_16816(o[j][0], o[j][1], o[j][2], o[j][3], ph0, 0u, ph1, 0u, b0, b1);
-        mma_bf16_16816(o[j][0], o[j][1], o[j][2], o[j][3], pl0, 0u, pl1, 0u, b0, b1);
+      for (int m = 0; m < 8; ++m) {
+        uint32_t v0, v1, v2, v3;  // A fragments of V^T for dimensions 16m .. 16m + 15
+        ldsm_x4_trans(dv + swz(lm_row, 2 * m + lm_hi), v0, v1, v2, v3);
+        mma_bf16_16816(o[m][0], o[m][1], o[m][2], o[m][3], v0, v1, v2, v3, ph0, ph1);
+        mma_bf16_16816(o[m][0], o[m][1], o[m][2], o[m][3], v0, v1, v2, v3, pl0, pl1);
       }
       __syncwarp();  // the stage is refilled by the next issue
       if (nxt < 0) break;
@@ -206,14 +215,18 @@ attn_partial_kernel(Shape s, const uint16_t* __restrict__ q, const uint16_t* __r
   // merge the warps of this split (the staging ring is reused for the partial outputs)
   __syncthreads();
   float* sm_o = reinterpret_cast<float*>(asmem);  // [kAttnWarps][G][kD]
-  if (g < G) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      sm_o[(warp * G + g) * kD + 32 * t + j] = o[j][0];
-      sm_o[(warp * G + g) * kD + 32 * t + 16 + j] = o[j][1];
+  for (int e = 0; e < 2; ++e) {
+    const int qq = 2 * t + e;
+    if (qq < G) {
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        sm_o[(warp * G + qq) * kD + 16 * m + g] = o[m][e];
+        sm_o[(warp * G + qq) * kD + 16 * m + g + 8] = o[m][2 + e];
+      }
     }
-    if (t == 0) { sm_m[warp][g] = m_run; sm_l[warp][g] = l_run; }
   }
+  if (g < G && t == 0) { sm_m[warp][g] = m_run; sm_l[warp][g] = l_run; }
   __syncthreads();
   const long long pbase = ((long long)head * nsplit + split) * G;
   for (int idx = threadIdx.x; idx < G * kD; idx += blockDim.x) {
@@ -272,7 +285,7 @@ attn_combine_kernel(Shape s, const float* __restrict__ part_o, const float* __re
 }
 
 // Splits per head: as many as keep the whole grid resident at once (2 CTAs per
-// SM: 208 registers x 128 threads), each split holding at least 4 entries of S.
+// SM counted, though three fit), each split holding at least 4 entries of S.
 // A second wave would double the latency chain; a warp with more blocks keeps
 // its 2-stage ring busy instead.
 int attn_nsplit(const Shape& s) {
