@@ -83,11 +83,13 @@ def parse():
                          "available host memory holds); 8 layers (32 GiB) gave ~15%% more layer-steps/s than 29 on the same box")
     ap.add_argument("--preroll", type=int, default=40,
                     help="untimed decode steps run first, so the timed steps see a warmed-up resident set")
-    ap.add_argument("--copy", default="overlap", choices=["overlap", "fork", "pipe", "gather", "carry", "lag"],
+    ap.add_argument("--copy", default="overlap", choices=["overlap", "hide", "fork", "pipe", "gather", "carry", "lag"],
                     help="gather: one gather launch per layer after its selection, one stream; "
                          "overlap: gather of layer l on a side stream beside the attention of layer l-1; "
                          "carry: the host copy of layer l rides in layer l+1's scoring launch; "
                          "lag: cross-step pipeline, attention over the previous step's selection; "
+                         "hide: the gather of layer l (table half, then a copy confined to a few SMs) beside the "
+                         "scorer of layer l+1, which takes its chunks from an atomic counter; "
                          "pipe: scorers back to back, each layer's selection, gather and attention on a side stream")
     ap.add_argument("--score-ctas", type=int, default=-1,
                     help="scorer CTAs per SM (0 = as many as fit; -1 = 2 with --copy pipe, else 0)")
@@ -608,7 +610,8 @@ def launches_per_step(st, copy):
     nsplit = st.scratch.ws_bytes // (s.B * s.Hkv * G * (s.d + 2) * 4)
     attn = 1 if nsplit <= 1 else 2  # split-K partials, then the combine kernel
     select = 1 if st.fused_select else 2  # top-K and diff in one launch, or two
-    per_layer = 1 + select + 1 + attn  # score (maybe carrying a copy), selection, gather or assign, attention
+    gather = 2 if copy == "hide" else 1  # the one-launch gather, or assign + copy
+    per_layer = 1 + select + gather + attn  # score (maybe carrying a copy), selection, gather or assign, attention
     return st.w.L * per_layer + (1 if copy == "carry" else 0)
 
 

@@ -127,6 +127,28 @@ OASIS_API oasis_status oasis_score_blocks(const oasis_shape* shape, const void* 
                                 float* scores, uint32_t* err_word, oasis_stream_t stream);
 
 /*
+ * a1, with work handed out at run time: the same scores as oasis_score_blocks
+ * (the mma.sync kernel, same bound), but each thread block takes its next chunk
+ * of 64 blocks from an atomic counter instead of a fixed stride, so blocks that
+ * start late - because kernels of other streams still hold their SMs - take
+ * fewer chunks rather than finishing last.  The grid leaves `reserve_ctas`
+ * thread-block slots of the GPU unused, room for such kernels.
+ * Arguments: as oasis_score_blocks, plus
+ *   work          device uint32 [2], 8-byte aligned: must be zero before the
+ *                 call; the last thread block to finish sets it back to zero, so
+ *                 it is ready for the next call.  Calls that may overlap on the
+ *                 GPU need different work words; a call that does not complete
+ *                 (an error) can leave it non-zero.
+ *   reserve_ctas  0 .. 4096 thread-block slots (of 128 threads, about 16K
+ *                 registers each) left free
+ * There is no error word: nothing here can fail once launched.
+ */
+OASIS_API oasis_status oasis_score_blocks_dynamic(const oasis_shape* shape, const void* k_hbm,
+                                                  const int32_t* ctx_len, const void* q_la,
+                                                  float* scores, uint32_t* work,
+                                                  int32_t reserve_ctas, oasis_stream_t stream);
+
+/*
  * a2. Top-K under the token budget.
  * Defines: keep, per KV head, the Kb highest-scoring blocks (OasisKV pages:
  * abstract, 2,048-token KV budget; Figure 7 caption, top-K blocks).

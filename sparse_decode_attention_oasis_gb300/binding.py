@@ -51,6 +51,8 @@ _SIGS = {
     "oasis_version": ([], ctypes.c_char_p),
     "oasis_last_error": ([], ctypes.c_char_p),
     "oasis_score_blocks": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
+    "oasis_score_blocks_dynamic": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, ctypes.c_int32, _VP],
+                                   ctypes.c_int),
     "oasis_topk_select": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
     "oasis_fetch_diff_capped": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                  ctypes.c_int32, _VP, _VP, _VP], ctypes.c_int),
@@ -149,6 +151,15 @@ def oasis_attn_workspace_bytes(shape: Shape) -> int:
 def oasis_score_blocks(shape: Shape, k_hbm, ctx_len, q_la, scores, err_word=None, stream=None):
     _check("oasis_score_blocks", load().oasis_score_blocks(
         ctypes.byref(shape), _ptr(k_hbm), _ptr(ctx_len), _ptr(q_la), _ptr(scores), _ptr(err_word),
+        _stream(stream)))
+
+
+def oasis_score_blocks_dynamic(shape: Shape, k_hbm, ctx_len, q_la, scores, work, reserve_ctas: int = 0,
+                               stream=None):
+    """oasis_score_blocks with chunks from an atomic counter (work: device int32/uint32 [2],
+    zero before the call and left zero after it); reserve_ctas thread-block slots stay free."""
+    _check("oasis_score_blocks_dynamic", load().oasis_score_blocks_dynamic(
+        ctypes.byref(shape), _ptr(k_hbm), _ptr(ctx_len), _ptr(q_la), _ptr(scores), _ptr(work), int(reserve_ctas),
         _stream(stream)))
 
 

@@ -9,6 +9,8 @@
 
 namespace oasis {
 cudaError_t launch_score_blocks(const Shape&, const uint16_t*, const int*, const uint16_t*, float2*, cudaStream_t);
+cudaError_t launch_score_blocks_dyn(const Shape&, const uint16_t*, const int*, const uint16_t*, float2*, unsigned*, int,
+                                    cudaStream_t);
 cudaError_t launch_score_blocks_tc(const Shape&, const uint16_t*, const int*, const uint16_t*, float2*, unsigned*,
                                    cudaStream_t);
 cudaError_t launch_topk_select(const Shape&, const float2*, const uint16_t*, const uint16_t*, const int*, int*,
@@ -154,6 +156,25 @@ oasis_status oasis_score_blocks(const oasis_shape* shape, const void* k_hbm, con
                       : oasis::launch_score_blocks(s, static_cast<const uint16_t*>(k_hbm), ctx_len,
                                                    static_cast<const uint16_t*>(q_la),
                                                    reinterpret_cast<float2*>(scores), (cudaStream_t)stream);
+  return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
+}
+
+oasis_status oasis_score_blocks_dynamic(const oasis_shape* shape, const void* k_hbm, const int32_t* ctx_len,
+                                        const void* q_la, float* scores, uint32_t* work, int32_t reserve_ctas,
+                                        oasis_stream_t stream) {
+  static const char* fn = "oasis_score_blocks_dynamic";
+  oasis::Shape s;
+  oasis_status st = check_shape(shape, fn, &s);
+  if (st != OASIS_OK) return st;
+  REQUIRE(k_hbm && aligned(k_hbm, 16), "k_hbm must be a 16-byte aligned device pointer");
+  REQUIRE(q_la && aligned(q_la, 16), "q_la must be a 16-byte aligned device pointer");
+  REQUIRE(ctx_len && aligned(ctx_len, 4), "ctx_len must be a 4-byte aligned device pointer");
+  REQUIRE(scores && aligned(scores, 8), "scores must be an 8-byte aligned device pointer");
+  REQUIRE(work && aligned(work, 8), "work must be an 8-byte aligned device pointer to two uint32");
+  REQUIRE(reserve_ctas >= 0 && reserve_ctas <= 4096, "reserve_ctas must be in [0, 4096]");
+  cudaError_t e = oasis::launch_score_blocks_dyn(s, static_cast<const uint16_t*>(k_hbm), ctx_len,
+                                                 static_cast<const uint16_t*>(q_la), reinterpret_cast<float2*>(scores),
+                                                 work, reserve_ctas, (cudaStream_t)stream);
   return e == cudaSuccess ? OASIS_OK : cuda_fail(fn, e);
 }
 

@@ -38,11 +38,16 @@ struct QFrag {
   uint32_t w[NT][4][4];  // [n-tile][d chunk i][word]
 };
 
-template <int NT, bool kCopy>
+// kDyn: chunks are handed out by an atomic counter (work[0]) instead of a fixed
+// stride, so thread blocks that start late (their SM still busy with another
+// kernel) simply take fewer chunks; the last block to finish (work[1] counts
+// them) leaves both words at zero for the next launch.
+template <int NT, bool kCopy, bool kDyn = false>
 __global__ void __launch_bounds__(kScoreWarps * 32, (NT <= 2 ? 4 : 3))
 score_blocks_kernel(Shape s, const uint16_t* __restrict__ k_hbm, const int* __restrict__ ctx_len,
                     const uint16_t* __restrict__ q_la, float2* __restrict__ scores,
-                    int chunks_per_head, int total_chunks, float inv_sqrt_d, CopyJob job) {
+                    int chunks_per_head, int total_chunks, float inv_sqrt_d, CopyJob job,
+                    unsigned* __restrict__ work = nullptr, int chunk_blocks = kScoreChunk) {
   extern __shared__ uint4 copy_buf[];  // [kScoreWarps][512] when kCopy
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -54,15 +59,22 @@ score_blocks_kernel(Shape s, const uint16_t* __restrict__ k_hbm, const int* __re
   const int N = s.n_la * G;
   const long long T_max = (long long)s.nb_max * kBS;
 
-  for (int chunk = blockIdx.x; chunk < total_chunks; chunk += gridDim.x) {
+  __shared__ int dyn_next;
+  int chunk = blockIdx.x;
+  if constexpr (kDyn) {
+    if (threadIdx.x == 0) dyn_next = (int)atomicAdd(work, 1u);
+    __syncthreads();
+    chunk = dyn_next;
+  }
+  for (; chunk < total_chunks;) {
     const int head = chunk / chunks_per_head;  // b * Hkv + h
     const int c = chunk - head * chunks_per_head;
     const int b = head / s.Hkv, h = head - b * s.Hkv;
     const int ctx = ctx_len[b];
     const int nb = clamp_nb(ctx, s.nb_max);
-    const int blk0 = c * kScoreChunk;
-    if (blk0 >= nb) continue;
-    const int blk1 = min(nb, blk0 + kScoreChunk);
+    const int blk0 = c * chunk_blocks;
+    const int blk1 = min(nb, blk0 + chunk_blocks);
+    if (blk0 < nb) {
 
     // Q fragments: query n = nt*8 + g is lookahead j = n / G, head hG + n % G.
     QFrag<NT> qf;
@@ -181,6 +193,24 @@ score_blocks_kernel(Shape s, const uint16_t* __restrict__ k_hbm, const int* __re
         scores[(long long)head * s.nb_max + blk] = make_float2(sc, e);
       }
     }
+    }  // blk0 < nb
+    if constexpr (kDyn) {
+      __syncthreads();  // every thread has read dyn_next
+      if (threadIdx.x == 0) dyn_next = (int)atomicAdd(work, 1u);
+      __syncthreads();
+      chunk = dyn_next;
+    } else {
+      chunk += gridDim.x;
+    }
+  }
+  if constexpr (kDyn) {
+    if (threadIdx.x == 0) {
+      __threadfence();  // this block's last fetch is ordered before its count
+      if (atomicAdd(work + 1, 1u) == gridDim.x - 1) {  // every block has fetched past the end
+        work[0] = 0u;
+        work[1] = 0u;
+      }
+    }
   }
   if constexpr (kCopy) copy_finish(job, s, gwarp, nwarps, copy_buf + warp * (kCopyUnitBytes / 16), lane);
 }
@@ -207,6 +237,31 @@ static cudaError_t launch_score(const Shape& s, const uint16_t* k, const int* ct
     case 2: score_blocks_kernel<2, kCopy><<<grid, block, smem, stream>>>(s, k, ctx, q_la, scores, chunks_per_head, total, inv, job); break;
     case 3: score_blocks_kernel<3, kCopy><<<grid, block, smem, stream>>>(s, k, ctx, q_la, scores, chunks_per_head, total, inv, job); break;
     case 4: score_blocks_kernel<4, kCopy><<<grid, block, smem, stream>>>(s, k, ctx, q_la, scores, chunks_per_head, total, inv, job); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+// The dynamic variant: chunks of 64 blocks from an atomic counter; the grid leaves
+// `reserve` thread-block slots of the GPU free for kernels on other streams.
+cudaError_t launch_score_blocks_dyn(const Shape& s, const uint16_t* k, const int* ctx, const uint16_t* q_la,
+                                    float2* scores, unsigned* work, int reserve, cudaStream_t stream) {
+  const int N = s.n_la * (s.Hq / s.Hkv);
+  const int NT = (N + 7) / 8;
+  constexpr int kDynChunk = 64;
+  const int chunks_per_head = (s.nb_max + kDynChunk - 1) / kDynChunk;
+  const int total = s.B * s.Hkv * chunks_per_head;
+  const float inv = 1.0f / sqrtf((float)s.d);
+  int grid = score_grid_limit(NT) - reserve;
+  if (grid > total) grid = total;
+  if (grid < 1) grid = 1;
+  const dim3 block(kScoreWarps * 32);
+  const CopyJob job{};
+  switch (NT) {
+    case 1: score_blocks_kernel<1, false, true><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, chunks_per_head, total, inv, job, work, kDynChunk); break;
+    case 2: score_blocks_kernel<2, false, true><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, chunks_per_head, total, inv, job, work, kDynChunk); break;
+    case 3: score_blocks_kernel<3, false, true><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, chunks_per_head, total, inv, job, work, kDynChunk); break;
+    case 4: score_blocks_kernel<4, false, true><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, chunks_per_head, total, inv, job, work, kDynChunk); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

@@ -107,6 +107,7 @@ class LayerScratch:
         self.ws = torch.empty(max(16, self.ws_bytes), dtype=torch.uint8, device=dev)
         self.out = torch.empty((s.B, s.Hq, 128), dtype=torch.float32, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.work = torch.zeros(2, dtype=torch.int32, device=dev)  # chunk counter of the dynamic scorer
 
 
 class _SelView:
@@ -169,6 +170,8 @@ class DecodeState:
         # prefetching the fetched blocks' host data into L2 from that launch moved the
         # host-link latency into it (top-K + diff +15 us, gather -15 us): off
         self.prefetch_host = False
+        self.hide_reserve = 16      # copy="hide": scorer thread-block slots left free
+        self.hide_copy_ctas = 16    # copy="hide": thread blocks of the confined copy
         self._lag_sel = None  # per-layer selections of the cross-step pipeline (copy="lag")
         self._lag_nsel = None
         self._lag_ready = False
@@ -396,13 +399,16 @@ class DecodeState:
         self._score_lp(lp, q_la, sc, st, mark, carry)
         self._topk_diff_lp(lp, q_la, sc, st, mark, host_layer)
 
-    def _score_lp(self, lp, q_la, sc, st, mark=None, carry=None):
+    def _score_lp(self, lp, q_la, sc, st, mark=None, carry=None, reserve=None):
         s = self.shape
         pooled = self.scoring == "pooled"
         K = self.Kpl[lp] if pooled else self.Kl[lp]
         if mark:
             mark("score", st)
-        if carry is None:
+        if reserve is not None and not pooled and carry is None:
+            # chunks from an atomic counter, leaving `reserve` thread-block slots free
+            B.oasis_score_blocks_dynamic(s, K, self.ctx, q_la, sc.scores, sc.work, reserve, st)
+        elif carry is None:
             if pooled:
                 B.oasis_score_blocks_pooled(s, K, self.ctx, q_la, sc.scores, err_word=sc.err, stream=st)
             else:
@@ -450,11 +456,19 @@ class DecodeState:
         B.oasis_assign_slots(s, sc.sel, sc.nsel, sc.fetch, sc.nfetch, self.b2sl[lp], self.s2bl[lp],
                              self.lul[lp], step, sc.err, st)
 
-    def _copy(self, layer, sc, st):
+    def _copy(self, layer, sc, st, ctas=0):
+        """The data half of layer `layer`'s gather; ctas > 0 confines its zero-copy host
+        reads to that many thread blocks (a few SMs)."""
         s = self.shape
         lp, lh = layer % self.L_phys, layer % self.L_host
-        B.oasis_copy_fetched(s, self.hostl[lh], sc.fetch, sc.nfetch, self.b2sl[lp], self.kpl[lp],
-                             self.vpl[lp], sc.err, st)
+        if ctas:
+            B.oasis_set_option(B.OPT_COPY_CTAS, ctas)
+        try:
+            B.oasis_copy_fetched(s, self.hostl[lh], sc.fetch, sc.nfetch, self.b2sl[lp], self.kpl[lp],
+                                 self.vpl[lp], sc.err, st)
+        finally:
+            if ctas:
+                B.oasis_set_option(B.OPT_COPY_CTAS, 0)
 
     def _attend(self, layer, q, sc, st, out=None):
         s = self.shape
@@ -510,6 +524,13 @@ class DecodeState:
         copy="pipe": the scorers of all layers back to back on ``main``; layer l's
           top-K + diff, gather and attention on a side stream once its scores
           exist, running beside the following scorers (a ring of 4 scratch sets).
+        copy="hide": the gather of layer l runs beside the scorer of layer l+1:
+            main: score(l) topk(l) [wait copy(l-1)] attn(l-1) score(l+1) ...
+            side: assign(l) and copy(l) once topk(l) and attn(l-1) are done.
+          The scorer takes its chunks from an atomic counter and leaves
+          ``hide_reserve`` thread-block slots free; the copy's zero-copy host reads
+          are confined to ``hide_copy_ctas`` thread blocks (a few SMs), so no
+          kernel with a deadline shares an SM with a stalled host read.
         copy="lag": the cross-step pipeline (f4): attn(l) over the selection the
           previous step made for layer l, then select(l) and gather(l) for the next
           step; one stream.
@@ -551,6 +572,32 @@ class DecodeState:
             if count is not None or fetched is not None:
                 self._tally(l, scr[l % 2], count, fetched)
 
+        if copy == "hide":
+            side = side if (side is not None and side is not main) else self._side_stream()
+            ev_sel = [torch.cuda.Event() for _ in range(2)]
+            ev_cp = [torch.cuda.Event() for _ in range(2)]
+            for l in range(L):
+                sc = scr[l % 2]
+                lp = l % self.L_phys
+                self._score_lp(lp, q_la_layers[l], sc, main, mark, reserve=self.hide_reserve)
+                self._topk_diff_lp(lp, q_la_layers[l], sc, main, mark, host_layer=l)
+                if l > 0:
+                    main.wait_event(ev_cp[(l - 1) % 2])
+                    attend(l - 1)
+                ev_sel[l % 2].record(main)
+                side.wait_event(ev_sel[l % 2])
+                if mark:
+                    mark("assign", side)
+                self._assign(l, step, sc, side)
+                if mark:
+                    mark("copy", side)
+                self._copy(l, sc, side, ctas=self.hide_copy_ctas)
+                if mark:
+                    mark("gather_end", side)
+                ev_cp[l % 2].record(side)
+            main.wait_event(ev_cp[(L - 1) % 2])
+            attend(L - 1)
+            return
         if copy == "pipe":
             # scorers back to back on `main`; each layer's selection, gather and
             # attention on a side stream as soon as its scores exist, beside the

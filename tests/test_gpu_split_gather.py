@@ -83,9 +83,35 @@ def _multi_layer(copy, L=3, steps=3, host_alloc="cuda"):
             _check_out(out[l].cpu().numpy().astype(np.float64), r["out"], f"layer {l} step {step}")
 
 
-@pytest.mark.parametrize("copy", ["carry", "gather", "overlap", "fork", "pipe"])
+@pytest.mark.parametrize("copy", ["carry", "gather", "overlap", "fork", "pipe", "hide"])
 def test_multi_layer_decode_step_all_orders(copy):
-    _multi_layer(copy, L=6 if copy == "pipe" else 3)
+    _multi_layer(copy, L=6 if copy in ("pipe", "hide") else 3)
+
+
+def test_dynamic_scorer_equals_the_static_one_and_leaves_its_counter_at_zero():
+    """oasis_score_blocks_dynamic writes the same (approximation, bound) pairs as
+    oasis_score_blocks, call after call, and leaves its work counter at zero."""
+    from sparse_decode_attention_oasis_gb300 import binding as B
+    from sparse_decode_attention_oasis_gb300.engine import DecodeState
+
+    w = syn.Workload("dyn", L=1, B=3, Hq=32, Hkv=8, ctx=[4096, 1000, 17], Kb=32, C=4, n_hot=16)
+    st = DecodeState(w, l_phys=1)
+    K, V = syn.layer_kv(w, 0)
+    st.fill_layer_numpy(0, K, V, *[np.array(t) for t in syn.initial_tables(w, 0)])
+    _, qla = syn.layer_queries(w, 0, 0)
+    q = _dev_bits(qla)
+    s = st.shape
+    ref_scores = torch.zeros((w.B, w.Hkv, w.nb_max, 2), dtype=torch.float32, device="cuda")
+    B.oasis_score_blocks(s, st.K[0], st.ctx, q, ref_scores)
+    work = torch.zeros(2, dtype=torch.int32, device="cuda")
+    for reserve in (0, 16, 0):
+        got = torch.zeros_like(ref_scores)
+        B.oasis_score_blocks_dynamic(s, st.K[0], st.ctx, q, got, work, reserve)
+        torch.cuda.synchronize()
+        for b in range(w.B):
+            nb = w.nb(b)
+            assert torch.equal(got[b, :, :nb], ref_scores[b, :, :nb])
+        assert work.tolist() == [0, 0]
 
 
 @pytest.mark.parametrize("host_alloc", ["thp", "thp_layers", "cuda_layers"])
