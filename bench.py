@@ -83,13 +83,11 @@ def parse():
                          "available host memory holds); 8 layers (32 GiB) gave ~15%% more layer-steps/s than 29 on the same box")
     ap.add_argument("--preroll", type=int, default=40,
                     help="untimed decode steps run first, so the timed steps see a warmed-up resident set")
-    ap.add_argument("--copy", default="overlap", choices=["overlap", "hide", "fork", "pipe", "gather", "carry", "lag"],
+    ap.add_argument("--copy", default="overlap", choices=["overlap", "fork", "pipe", "gather", "carry", "lag"],
                     help="gather: one gather launch per layer after its selection, one stream; "
                          "overlap: gather of layer l on a side stream beside the attention of layer l-1; "
                          "carry: the host copy of layer l rides in layer l+1's scoring launch; "
                          "lag: cross-step pipeline, attention over the previous step's selection; "
-                         "hide: the gather of layer l (table half, then a copy confined to a few SMs) beside the "
-                         "scorer of layer l+1, which takes its chunks from an atomic counter; "
                          "pipe: scorers back to back, each layer's selection, gather and attention on a side stream")
     ap.add_argument("--score-ctas", type=int, default=-1,
                     help="scorer CTAs per SM (0 = as many as fit; -1 = 2 with --copy pipe, else 0)")
@@ -103,6 +101,8 @@ def parse():
                     help="layers of distinct keys and pools in HBM (layer l uses l mod N; 0 = all, or 12 for "
                          "long_output, whose 36 layers of keys do not fit)")
     ap.add_argument("--no-pooled", action="store_true", help="skip the pooled-scoring variant")
+    ap.add_argument("--dynamic-scorer", action="store_true",
+                    help="max-dot scoring with chunks from an atomic counter (oasis_score_blocks_dynamic)")
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the cross-step pipeline and fused look-ahead attention measurements")
     ap.add_argument("--host-alloc", default="cuda", choices=["cuda", "thp", "thp_layers", "cuda_layers"],
@@ -161,6 +161,7 @@ def config_dict(args, w, l_phys, l_host, score_ctas, world=1):
             "host_tier_layers": l_host, "host_tier_aliased": l_host < w.L,
             "hbm_layers": l_phys, "hbm_layers_aliased": l_phys < w.L,
             "host_alloc": args.host_alloc,
+            "dynamic_scorer": bool(getattr(args, "dynamic_scorer", False)),
             "parallelism": "replicas" if world > 1 else "single GPU"}
 
 
@@ -610,8 +611,7 @@ def launches_per_step(st, copy):
     nsplit = st.scratch.ws_bytes // (s.B * s.Hkv * G * (s.d + 2) * 4)
     attn = 1 if nsplit <= 1 else 2  # split-K partials, then the combine kernel
     select = 1 if st.fused_select else 2  # top-K and diff in one launch, or two
-    gather = 2 if copy == "hide" else 1  # the one-launch gather, or assign + copy
-    per_layer = 1 + select + gather + attn  # score (maybe carrying a copy), selection, gather or assign, attention
+    per_layer = 1 + select + 1 + attn  # score (maybe carrying a copy), selection, gather or assign, attention
     return st.w.L * per_layer + (1 if copy == "carry" else 0)
 
 
@@ -631,6 +631,7 @@ def make_state(args, w, dev, l_phys, l_host, scoring="maxdot"):
                 raise
             l_host = max(2, l_host // 2)
             torch.cuda.empty_cache()
+    st.dynamic_scorer = args.dynamic_scorer
     st.fill_synthetic()
     st.warm_host_tier()
     return st
@@ -877,6 +878,7 @@ def run_gpu(args, rank, world, local_rank):
             l_host = max(2, l_host // 2)
             torch.cuda.empty_cache()
     alloc_s = time.time() - t0
+    st.dynamic_scorer = args.dynamic_scorer
     st.fill_synthetic()
     torch.cuda.synchronize()
     gen_s = time.time() - t0

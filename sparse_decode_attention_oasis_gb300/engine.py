@@ -170,8 +170,9 @@ class DecodeState:
         # prefetching the fetched blocks' host data into L2 from that launch moved the
         # host-link latency into it (top-K + diff +15 us, gather -15 us): off
         self.prefetch_host = False
-        self.hide_reserve = 16      # copy="hide": scorer thread-block slots left free
-        self.hide_copy_ctas = 16    # copy="hide": thread blocks of the confined copy
+        # max-dot scoring through oasis_score_blocks_dynamic (chunks from an atomic
+        # counter) instead of the fixed-stride persistent grid
+        self.dynamic_scorer = False
         self._lag_sel = None  # per-layer selections of the cross-step pipeline (copy="lag")
         self._lag_nsel = None
         self._lag_ready = False
@@ -399,15 +400,14 @@ class DecodeState:
         self._score_lp(lp, q_la, sc, st, mark, carry)
         self._topk_diff_lp(lp, q_la, sc, st, mark, host_layer)
 
-    def _score_lp(self, lp, q_la, sc, st, mark=None, carry=None, reserve=None):
+    def _score_lp(self, lp, q_la, sc, st, mark=None, carry=None):
         s = self.shape
         pooled = self.scoring == "pooled"
         K = self.Kpl[lp] if pooled else self.Kl[lp]
         if mark:
             mark("score", st)
-        if reserve is not None and not pooled and carry is None:
-            # chunks from an atomic counter, leaving `reserve` thread-block slots free
-            B.oasis_score_blocks_dynamic(s, K, self.ctx, q_la, sc.scores, sc.work, reserve, st)
+        if self.dynamic_scorer and not pooled and carry is None:
+            B.oasis_score_blocks_dynamic(s, K, self.ctx, q_la, sc.scores, sc.work, 0, st)
         elif carry is None:
             if pooled:
                 B.oasis_score_blocks_pooled(s, K, self.ctx, q_la, sc.scores, err_word=sc.err, stream=st)
@@ -524,13 +524,6 @@ class DecodeState:
         copy="pipe": the scorers of all layers back to back on ``main``; layer l's
           top-K + diff, gather and attention on a side stream once its scores
           exist, running beside the following scorers (a ring of 4 scratch sets).
-        copy="hide": the gather of layer l runs beside the scorer of layer l+1:
-            main: score(l) topk(l) [wait copy(l-1)] attn(l-1) score(l+1) ...
-            side: assign(l) and copy(l) once topk(l) and attn(l-1) are done.
-          The scorer takes its chunks from an atomic counter and leaves
-          ``hide_reserve`` thread-block slots free; the copy's zero-copy host reads
-          are confined to ``hide_copy_ctas`` thread blocks (a few SMs), so no
-          kernel with a deadline shares an SM with a stalled host read.
         copy="lag": the cross-step pipeline (f4): attn(l) over the selection the
           previous step made for layer l, then select(l) and gather(l) for the next
           step; one stream.
@@ -572,32 +565,6 @@ class DecodeState:
             if count is not None or fetched is not None:
                 self._tally(l, scr[l % 2], count, fetched)
 
-        if copy == "hide":
-            side = side if (side is not None and side is not main) else self._side_stream()
-            ev_sel = [torch.cuda.Event() for _ in range(2)]
-            ev_cp = [torch.cuda.Event() for _ in range(2)]
-            for l in range(L):
-                sc = scr[l % 2]
-                lp = l % self.L_phys
-                self._score_lp(lp, q_la_layers[l], sc, main, mark, reserve=self.hide_reserve)
-                self._topk_diff_lp(lp, q_la_layers[l], sc, main, mark, host_layer=l)
-                if l > 0:
-                    main.wait_event(ev_cp[(l - 1) % 2])
-                    attend(l - 1)
-                ev_sel[l % 2].record(main)
-                side.wait_event(ev_sel[l % 2])
-                if mark:
-                    mark("assign", side)
-                self._assign(l, step, sc, side)
-                if mark:
-                    mark("copy", side)
-                self._copy(l, sc, side, ctas=self.hide_copy_ctas)
-                if mark:
-                    mark("gather_end", side)
-                ev_cp[l % 2].record(side)
-            main.wait_event(ev_cp[(L - 1) % 2])
-            attend(L - 1)
-            return
         if copy == "pipe":
             # scorers back to back on `main`; each layer's selection, gather and
             # attention on a side stream as soon as its scores exist, beside the

@@ -83,9 +83,9 @@ def _multi_layer(copy, L=3, steps=3, host_alloc="cuda"):
             _check_out(out[l].cpu().numpy().astype(np.float64), r["out"], f"layer {l} step {step}")
 
 
-@pytest.mark.parametrize("copy", ["carry", "gather", "overlap", "fork", "pipe", "hide"])
+@pytest.mark.parametrize("copy", ["carry", "gather", "overlap", "fork", "pipe"])
 def test_multi_layer_decode_step_all_orders(copy):
-    _multi_layer(copy, L=6 if copy in ("pipe", "hide") else 3)
+    _multi_layer(copy, L=6 if copy == "pipe" else 3)
 
 
 def test_dynamic_scorer_equals_the_static_one_and_leaves_its_counter_at_zero():
