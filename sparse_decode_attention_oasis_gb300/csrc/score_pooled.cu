@@ -15,7 +15,8 @@
 // Streaming.  A tile (16 consecutive blocks of one head) is 8 KiB of contiguous
 // memory; each thread loads its A fragments of a tile straight into registers
 // with sixteen 16-byte loads (every warp instruction covers full 32-byte
-// sectors), 4 CTAs of 4 warps per SM.  (A cp.async shared-memory ring per warp
+// sectors), 4 CTAs of 4 warps per SM, and reloads each chunk's registers with
+// the same chunk of its next tile as soon as the chunk's MMAs are issued.  (A cp.async shared-memory ring per warp
 // reached only 4.3 TB/s with no MMA at all: the register loads stream faster.)
 //
 // Work split.  The valid tiles of all heads (ceil(nb_b / 16) per head of request
@@ -212,46 +213,36 @@ score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restr
       nbv = hs ? nbh1 : nbh0;
     };
 
-    for (int k = 0; k < ntiles; ++k) {
-      int hs, blk0, nbv;
-      where(g0 + warp + k * kPsWarps, hs, blk0, nbv);
-      const int head = hg + hs;
-      const int blk1 = min(nbv, blk0 + kTileBlocks);
-      const uint16_t* base = kp + (long long)head * s.nb_max * kPK;
-      const int r0 = blk0 + g, r1 = blk0 + g + 8;
-      uint4 ra[8], rb[8];
+    // Rolling prefetch: once chunk i of the current tile has fed its MMAs, its
+    // registers receive chunk i of this warp's next tile, so a tile's worth of
+    // loads stays in flight through the MMAs and the epilogue.
+    uint4 ra[8], rb[8];
+    int hs_c = 0, blk0_c = 0, nbv_c = 0;
+    if (ntiles > 0) {
+      where(g0 + warp, hs_c, blk0_c, nbv_c);
+      const int blk1 = min(nbv_c, blk0_c + kTileBlocks);
+      const uint16_t* base = kp + (long long)(hg + hs_c) * s.nb_max * kPK;
+      const int r0 = blk0_c + g, r1 = blk0_c + g + 8;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         ra[i] = r0 < blk1 ? ldg_stream(base + (long long)r0 * kPK + (t + 4 * i) * 8) : make_uint4(0u, 0u, 0u, 0u);
         rb[i] = r1 < blk1 ? ldg_stream(base + (long long)r1 * kPK + (t + 4 * i) * 8) : make_uint4(0u, 0u, 0u, 0u);
       }
+    }
+    for (int k = 0; k < ntiles; ++k) {
+      const int hs = hs_c, blk0 = blk0_c;
+      const int head = hg + hs;
+      const int blk1 = min(nbv_c, blk0 + kTileBlocks);
+      const int r0 = blk0 + g, r1 = blk0 + g + 8;
+      int hs_n = 0, blk0_n = 0, nbv_n = 0;
+      if (k + 1 < ntiles) where(g0 + warp + (k + 1) * kPsWarps, hs_n, blk0_n, nbv_n);
+      const int blk1_n = min(nbv_n, blk0_n + kTileBlocks);  // 0 when there is no next tile
+      const uint16_t* base_n = kp + (long long)(hg + hs_n) * s.nb_max * kPK;
+      const int r0n = blk0_n + g, r1n = blk0_n + g + 8;
+      const bool ok0 = r0n < blk1_n, ok1 = r1n < blk1_n;
       float acc[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t A[4] = {ra[i].x, ra[i].y, ra[i].z, ra[i].w};
-        const uint32_t Bw[4] = {rb[i].x, rb[i].y, rb[i].z, rb[i].w};
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const uint2 q = sm.qf[hs][nt][i][hh][lane];
-            mma_bf16_16816(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3], A[2 * hh], Bw[2 * hh], A[2 * hh + 1],
-                           Bw[2 * hh + 1], q.x, q.y);
-          }
-      }
-      float m0 = neg_inf(), m1 = neg_inf();
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int n0 = nt * 8 + 2 * t;
-        if (n0 < N) { m0 = fmaxf(m0, acc[nt][0]); m1 = fmaxf(m1, acc[nt][2]); }
-        if (n0 + 1 < N) { m0 = fmaxf(m0, acc[nt][1]); m1 = fmaxf(m1, acc[nt][3]); }
-      }
-      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
-      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
-      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
-      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
       // |k'|^2 of the 16 rows: the diagonal of the Gram tile K' K'^T, formed on the
       // tensor cores from the A fragments themselves (the B fragment of column n is
       // row n's own A words).  Row r's entry sits in lane 4 (r & 7) + ((r & 7) >> 1).
@@ -264,12 +255,34 @@ score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restr
         const uint32_t Bw[4] = {rb[i].x, rb[i].y, rb[i].z, rb[i].w};
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const uint2 q = sm.qf[hs][nt][i][hh][lane];
+            mma_bf16_16816(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3], A[2 * hh], Bw[2 * hh], A[2 * hh + 1],
+                           Bw[2 * hh + 1], q.x, q.y);
+          }
           mma_bf16_16816(gr[0][0], gr[0][1], gr[0][2], gr[0][3], A[2 * hh], Bw[2 * hh], A[2 * hh + 1],
                          Bw[2 * hh + 1], A[2 * hh], A[2 * hh + 1]);
           mma_bf16_16816(gr[1][0], gr[1][1], gr[1][2], gr[1][3], A[2 * hh], Bw[2 * hh], A[2 * hh + 1],
                          Bw[2 * hh + 1], Bw[2 * hh], Bw[2 * hh + 1]);
         }
+        ra[i] = ok0 ? ldg_stream(base_n + (long long)r0n * kPK + (t + 4 * i) * 8) : make_uint4(0u, 0u, 0u, 0u);
+        rb[i] = ok1 ? ldg_stream(base_n + (long long)r1n * kPK + (t + 4 * i) * 8) : make_uint4(0u, 0u, 0u, 0u);
       }
+      hs_c = hs_n;
+      blk0_c = blk0_n;
+      nbv_c = nbv_n;
+      float m0 = neg_inf(), m1 = neg_inf();
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int n0 = nt * 8 + 2 * t;
+        if (n0 < N) { m0 = fmaxf(m0, acc[nt][0]); m1 = fmaxf(m1, acc[nt][2]); }
+        if (n0 + 1 < N) { m0 = fmaxf(m0, acc[nt][1]); m1 = fmaxf(m1, acc[nt][3]); }
+      }
+      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
+      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
       const int holder = 4 * g + (g >> 1);
       const float d0 = (g & 1) ? gr[0][1] : gr[0][0];   // row g, column g
       const float d1 = (g & 1) ? gr[1][3] : gr[1][2];   // row g + 8, column g + 8

@@ -1,10 +1,11 @@
-"""The allocation-free attention call, checked against the workspace call.
+"""The allocation-free attention call, checked against the oracle and the workspace call.
 
 Callers that cannot allocate device memory when they call - a serving loop whose
 device-memory budget is fixed at start-up, or host code that must not call
 cudaMalloc on its decode path - use oasis_sparse_decode_attn_noalloc, which keeps
 its scratch in a device array built into the library.  Its output must match
-oasis_sparse_decode_attn's, call after call (the array is shared and reused).
+the oracle's attention over the same selection, and oasis_sparse_decode_attn's,
+call after call (the array is shared and reused).
 """
 import ctypes
 
@@ -68,6 +69,27 @@ def test_noalloc_matches_the_workspace_call_on_two_calls_in_a_row(lib):
             torch.cuda.synchronize()
             assert torch.isfinite(out).all()
             assert _close(out, ref)
+
+
+@pytest.mark.parametrize("w", [
+    syn.Workload("ragged", L=1, B=3, Hq=32, Hkv=8, ctx=[4096, 1000, 17], Kb=32, C=4, n_hot=16),
+    syn.Workload("gqa8", L=1, B=2, Hq=64, Hkv=8, n_la=4, ctx=[3000, 2048], Kb=24, C=3, n_hot=12),
+], ids=["ragged", "gqa8"])
+def test_noalloc_matches_the_oracle(lib, w):
+    """The oracle's decode step (selection, gather, attention over the attended
+    blocks) against the allocation-free call run on the device's selection, which
+    the harness has checked index for index against the oracle's."""
+    from gpu_helpers import Case, _check_out, _dev_bits
+
+    case = Case(w)
+    q, qla = syn.layer_queries(w, 0, 0)
+    r, sc = case.step(0, q=q, qla=qla)
+    st = case.st
+    out = torch.full_like(sc.out, float("nan"))
+    lib.oasis_sparse_decode_attn_noalloc(st.shape, _dev_bits(q), st.k_pool[0], st.v_pool[0], sc.sel, sc.nsel,
+                                         st.blk2slot[0], st.ctx, st.scale, out)
+    torch.cuda.synchronize()
+    _check_out(out.cpu().numpy().astype(np.float64), r["out"], f"allocation-free attention ({w.name})")
 
 
 def test_noalloc_rejects_shapes_beyond_its_array(lib):
