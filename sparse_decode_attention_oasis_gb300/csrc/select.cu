@@ -619,36 +619,52 @@ __device__ void warp_exact_pooled_score(const SelCtx& c, int blk, uint32_t* out,
   __syncwarp();
   const uint16_t* hi = kst;
   const uint16_t* lo = kst + kD;
-  float my_lo = neg_inf(), my_hi = neg_inf();
-  for (int n = 0; n < c.N; ++n) {
-    const uint16_t* q = c.qb + n * kD;
-    float v = 0.f, a = 0.f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = lane + 32 * j;
-      const uint32_t qb = q[e];
-      const uint32_t kb = (qb & 0x8000u) ? lo[e] : hi[e];
-      const float p = __uint_as_float(qb << 16) * __uint_as_float(kb << 16);
-      v += p;
-      a += fabsf(p);
-    }
-    v = warp_sum(v);
-    a = warp_sum(a);
-    if (lane == n) {
-      const float eps = __fmaf_ru(1.52587890625e-05f /* 2^-16 */, a, 7.52316384526264e-37f /* 2^-120 */);
-      my_lo = __fsub_rd(v, eps);
-      my_hi = __fadd_ru(v, eps);
-      if (!(fabsf(v) <= 3.0e38f) || !(a <= 3.0e38f)) { my_lo = neg_inf(); my_hi = __int_as_float(0x7f800000); }
+  // Screening: fp32 pooled dots with error bounds, P lanes per query (the largest
+  // power of two with N * P <= 32), each over 128 / P elements taken as bf16 pairs,
+  // then log2(P) shuffles.  Lane rotation of the word index keeps the shared-memory
+  // reads of one instruction in distinct banks.  Any summation order of the 128
+  // exact products errs by at most 127 * 2^-24 < 2^-16 of their absolute sum.
+  int P = 1;
+  while (c.N * P * 2 <= 32) P *= 2;
+  const int n = lane / P, part = lane - n * P;
+  const int wpl = 64 / P;  // bf16 pairs per lane
+  float v0 = 0.f, v1 = 0.f, a0 = 0.f, a1 = 0.f;
+  if (n < c.N) {
+    const uint32_t* qw = reinterpret_cast<const uint32_t*>(c.qb + n * kD) + part * wpl;
+    const uint32_t* hw = reinterpret_cast<const uint32_t*>(hi) + part * wpl;
+    const uint32_t* lw = reinterpret_cast<const uint32_t*>(lo) + part * wpl;
+    for (int w = 0; w < wpl; ++w) {
+      const int ww = (w + lane) & (wpl - 1);
+      const uint32_t qv = qw[ww], hv = hw[ww], lv = lw[ww];
+      // a negative query element meets the block's minimum, a non-negative one its maximum
+      const float p0 = bf_lo(qv) * ((qv & 0x8000u) ? bf_lo(lv) : bf_lo(hv));
+      const float p1 = bf_hi(qv) * ((qv & 0x80000000u) ? bf_hi(lv) : bf_hi(hv));
+      v0 += p0;
+      a0 += fabsf(p0);
+      v1 += p1;
+      a1 += fabsf(p1);
     }
   }
+  float v = v0 + v1, a = a0 + a1;
+  for (int o = 1; o < P; o <<= 1) {
+    v += __shfl_xor_sync(0xffffffffu, v, o);
+    a += __shfl_xor_sync(0xffffffffu, a, o);
+  }
+  float my_lo = neg_inf(), my_hi = neg_inf();
+  if (part == 0 && n < c.N) {
+    const float eps = __fmaf_ru(1.52587890625e-05f /* 2^-16 */, a, 7.52316384526264e-37f /* 2^-120 */);
+    my_lo = __fsub_rd(v, eps);
+    my_hi = __fadd_ru(v, eps);
+    if (!(fabsf(v) <= 3.0e38f) || !(a <= 3.0e38f)) { my_lo = neg_inf(); my_hi = __int_as_float(0x7f800000); }
+  }
   const float best_lo = warp_max(my_lo);
-  unsigned mask = __ballot_sync(0xffffffffu, lane < c.N && my_hi >= best_lo);
+  unsigned mask = __ballot_sync(0xffffffffu, part == 0 && n < c.N && my_hi >= best_lo);
   uint32_t* tmp = c.tmp + warp * kLimbs;
   bool have = false;
   while (mask) {
-    const int n = __ffs(mask) - 1;
+    const int qn = (__ffs(mask) - 1) / P;
     mask &= mask - 1;
-    warp_exact_dot<true>(hi, c.qb + n * kD, tmp, lane, lo);
+    warp_exact_dot<true>(hi, c.qb + qn * kD, tmp, lane, lo);
     if (lane == 0) {
       if (!have || exact_cmp(tmp, out) > 0)
         for (int i = 0; i < kLimbs; ++i) out[i] = tmp[i];
