@@ -101,6 +101,8 @@ def parse():
                     help="layers of distinct keys and pools in HBM (layer l uses l mod N; 0 = all, or 12 for "
                          "long_output, whose 36 layers of keys do not fit)")
     ap.add_argument("--no-pooled", action="store_true", help="skip the pooled-scoring variant")
+    ap.add_argument("--score-kernel", default="mma", choices=["mma", "tc"],
+                    help="max-dot scorer: mma.sync from registers (default) or TMA + tcgen05 with TMEM accumulators")
     ap.add_argument("--dynamic-scorer", action="store_true",
                     help="max-dot scoring with chunks from an atomic counter (oasis_score_blocks_dynamic)")
     ap.add_argument("--no-variants", action="store_true",
@@ -162,6 +164,7 @@ def config_dict(args, w, l_phys, l_host, score_ctas, world=1):
             "hbm_layers": l_phys, "hbm_layers_aliased": l_phys < w.L,
             "host_alloc": args.host_alloc,
             "dynamic_scorer": bool(getattr(args, "dynamic_scorer", False)),
+            "score_kernel": getattr(args, "score_kernel", "mma"),
             "parallelism": "replicas" if world > 1 else "single GPU"}
 
 
@@ -928,6 +931,7 @@ def run_gpu(args, rank, world, local_rank):
     from sparse_decode_attention_oasis_gb300 import binding as _B
 
     _B.oasis_set_option(_B.OPT_SCORE_CTAS_PER_SM, score_ctas)
+    _B.oasis_set_option(_B.OPT_SCORE_KERNEL, _B.SCORE_KERNEL_TC if args.score_kernel == "tc" else _B.SCORE_KERNEL_MMA)
     main = torch.cuda.current_stream(dev)
     side = main  # the overlap mode makes its own side stream; the others run on one stream
     out_dev = torch.empty((L, w.B, w.Hq, w.d), dtype=torch.float32, device=dev)
@@ -1231,7 +1235,7 @@ def run_gpu(args, rank, world, local_rank):
         "device_error_word": errw,
         "setup_s": round(gen_s, 1), "alloc_s": round(alloc_s, 1),
         "host_tier_warm_s": None if warm_s is None else round(warm_s, 2),
-        "score_kernel": "mma.sync",
+        "score_kernel": "tcgen05 (TMA ring, TMEM accumulators)" if args.score_kernel == "tc" else "mma.sync",
     }
     if not args.no_cpu_baseline and world == 1:
         try:

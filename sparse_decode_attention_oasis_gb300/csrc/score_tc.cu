@@ -10,10 +10,13 @@
 //               (M=128 tokens, N=16|32 queries, K=16, bf16 -> fp32) per tile into
 //               one of two TMEM accumulators and commits to the stage's "empty"
 //               and the accumulator's "tfull" mbarriers;
-//   warps 2..5  epilogue: tcgen05.ld of its 32 TMEM lanes (one token per
-//               thread), masked max over the valid queries, the token's key norm
-//               from the swizzled shared-memory tile, a 16-lane reduction per
-//               block, and the (score, bound) store.
+//   warps 2..9  epilogue, two groups of four: group g takes the tiles that
+//               went to accumulator g, so two tiles' epilogues overlap; a warp
+//               reads its 32 TMEM lanes (one token per thread) with tcgen05.ld,
+//               takes the masked max over the valid queries and the token's key
+//               norm from the swizzled shared-memory tile (four independent
+//               partial sums), reduces over 16 lanes per block and stores
+//               (score, bound).
 // Every mbarrier wait is bounded: on expiry the CTA raises OASIS_EW_TIMEOUT in the
 // error word, stops, waits (bounded) for its own TMA copies and MMAs, frees TMEM
 // and returns.
@@ -26,8 +29,10 @@ namespace oasis {
 namespace tc {
 
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 64;
+constexpr int kEpiGroups = 2;
+constexpr int kThreads = 64 + kEpiGroups * 128;
+// one 32-column TMEM accumulator per epilogue group (an allocation is a power of two >= 32)
+constexpr uint32_t kTmemCols = kEpiGroups <= 2 ? 64u : (kEpiGroups <= 4 ? 128u : 256u);
 constexpr uint32_t kKBox = 128 * 128;                    // 128 rows x 128 B
 constexpr uint32_t kQBox = 32 * 128;                     // up to 32 rows x 128 B
 constexpr uint32_t kStageBytes = 2 * kKBox + 2 * kQBox;  // 40 KiB, multiple of 1024
@@ -36,8 +41,8 @@ constexpr unsigned long long kWaitNs = 2000000000ull;  // a wait gives up after 
 struct Bars {
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t tfull[kEpiGroups];
+  uint64_t tempty[kEpiGroups];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -163,7 +168,7 @@ __device__ __forceinline__ uint4 lds16(uint32_t addr) {
 
 // sum of squares of one 128-element bf16 row held as two swizzled 128-byte rows
 __device__ __forceinline__ float row_sumsq(uint32_t box0, uint32_t box1, int row) {
-  float ss = 0.f;
+  float ss[4] = {0.f, 0.f, 0.f, 0.f};  // independent chains: one per word of a 16-byte chunk
 #pragma unroll
   for (int bx = 0; bx < 2; ++bx) {
     const uint32_t base = (bx ? box1 : box0) + row * 128;
@@ -173,12 +178,12 @@ __device__ __forceinline__ float row_sumsq(uint32_t box0, uint32_t box1, int row
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        ss = fmaf(bf_lo(w[m]), bf_lo(w[m]), ss);
-        ss = fmaf(bf_hi(w[m]), bf_hi(w[m]), ss);
+        ss[m] = fmaf(bf_lo(w[m]), bf_lo(w[m]), ss[m]);
+        ss[m] = fmaf(bf_hi(w[m]), bf_hi(w[m]), ss[m]);
       }
     }
   }
-  return ss;
+  return (ss[0] + ss[1]) + (ss[2] + ss[3]);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -202,7 +207,7 @@ score_blocks_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
       mbar_init(&bars->full[i], 1);
       mbar_init(&bars->empty[i], 5);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kEpiGroups; ++i) {
       mbar_init(&bars->tfull[i], 1);
       mbar_init(&bars->tempty[i], 4);
     }
@@ -254,7 +259,7 @@ score_blocks_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         const int b = head / s.Hkv;
         const int nb = clamp_nb(ctx_len[b], s.nb_max);
         if (t * 8 >= nb) continue;
-        const int st = i % kStages, r = i / kStages, a = i & 1, u = i >> 1;
+        const int st = i % kStages, r = i / kStages, a = i % kEpiGroups, u = i / kEpiGroups;
         if (!mbar_wait(&bars->tempty[a], (u & 1) ^ 1, abort_flag)) { timed_out = true; break; }
         if (!mbar_wait(&bars->full[st], r & 1, abort_flag)) { timed_out = true; break; }
         tc_fence_after();
@@ -277,7 +282,8 @@ score_blocks_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;
+    const int quarter = warp & 3;  // the TMEM lanes this warp may read
+    const int group = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     int i = 0;
     int cached_head = -1;
@@ -288,7 +294,11 @@ score_blocks_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
       const int ctx = ctx_len[b];
       const int nb = clamp_nb(ctx, s.nb_max);
       if (t * 8 >= nb) continue;
-      const int st = i % kStages, r = i / kStages, a = i & 1, u = i >> 1;
+      const int st = i % kStages, r = i / kStages, a = i % kEpiGroups, u = i / kEpiGroups;
+      if (a != group) {  // the other group's tile
+        ++i;
+        continue;
+      }
       bool ok = mbar_wait(&bars->tfull[a], u & 1, abort_flag);
       ok = ok && mbar_wait(&bars->full[st], r & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) { timed_out = true; break; }
@@ -346,7 +356,7 @@ score_blocks_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
   }
   if (warp == 1 && lane == 0 && done_tiles > 0) {
     const int j = done_tiles - 1;
-    mbar_drain(&bars->tfull[j & 1], (j >> 1) & 1);
+    mbar_drain(&bars->tfull[j % kEpiGroups], (j / kEpiGroups) & 1);
   }
   tc_fence_before();
   __syncthreads();
