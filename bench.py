@@ -850,6 +850,76 @@ def measure_host_fit(args, st, q_dev, qla_dev, start, world, dev):
     return r
 
 
+def measure_spans(st, first_step, qla_steps, q_steps, out_dev, copy, appends, steps=3):
+    """Kernel spans of `steps` decode steps captured as one CUDA graph with the span
+    trace on (no event nodes between kernels), replayed once."""
+    import torch
+
+    from sparse_decode_attention_oasis_gb300.engine import KernelTrace, StepGraph
+
+    L = st.w.L
+    tr = KernelTrace(capacity=max(64, 2 * L * steps), device=st.device)
+    tr.start()
+    try:
+        g = StepGraph(st, first_step, qla_steps, q_steps, [out_dev] * steps, copy=copy, appends=appends)
+    finally:
+        tr.stop()
+    with torch.cuda.stream(g.stream):
+        g.replay()
+    torch.cuda.synchronize()
+    sp = tr.spans()
+    del g, tr
+    torch.cuda.synchronize()
+    return sp
+
+
+def summarize_spans(sp, L, steps, copy, gather_bytes=None, link_gbs=None):
+    """Per-kind span statistics (us) and, for the overlap order, the gaps of the
+    critical path between consecutive kernels of a layer."""
+    import numpy as np
+
+    def stats(x):
+        x = np.asarray(x, dtype=np.float64)
+        if x.size == 0:
+            return None
+        return {"p50": round(float(np.median(x)), 2), "mean": round(float(x.mean()), 2),
+                "max": round(float(x.max()), 2), "n": int(x.size)}
+
+    out = {"source": f"per-launch spans (earliest block start to latest block end, %globaltimer) of {steps} "
+                     f"decode steps captured as one CUDA graph with the span trace on and no event nodes, "
+                     f"replayed once", "steps": steps, "kernel_us": {}}
+    for name, (a, b) in sp.items():
+        if len(a):
+            out["kernel_us"][name] = stats((b - a) / 1000.0)
+    score_name = "score" if len(sp["score"][0]) else "score_pooled"
+    S0, S1 = (x / 1000.0 for x in sp[score_name])
+    if len(S0) > 1:
+        out["layer_period_us"] = stats(np.diff(S0))
+    n = L * steps
+    if copy == "overlap" and all(len(sp[k][0]) == n for k in (score_name, "select", "gather", "attn")):
+        T0, T1 = (x / 1000.0 for x in sp["select"])
+        G0, G1 = (x / 1000.0 for x in sp["gather"])
+        A0, A1 = (x / 1000.0 for x in sp["attn"])
+        prev = [i for i in range(n) if i % L]  # attention of layer l-1 runs beside the gather of layer l
+        nxt = range(n - 1)
+        out["gaps_us"] = {
+            "score_end_to_select_start": stats(T0 - S1),
+            "select_end_to_gather_start": stats(G0 - T1),
+            "select_end_to_attn_prev_start": stats([A0[i - 1] - T1[i] for i in prev]),
+            "gather_end_to_next_score_start": stats([S0[i + 1] - G1[i] for i in nxt]),
+            "next_score_start_after_gather_and_attn_prev": stats(
+                [S0[i + 1] - max(G1[i], A1[i - 1]) for i in nxt if i % L]),
+        }
+    if gather_bytes and len(sp["gather"][0]):
+        g_us = (sp["gather"][1] - sp["gather"][0]) / 1000.0
+        gbs = gather_bytes / (g_us * 1e3)
+        out["decode_gather_gbs"] = stats(gbs)
+        if link_gbs:
+            out["decode_gather_link_frac_p50"] = round(float(np.median(gbs)) / link_gbs, 4)
+            out["decode_gather_link_frac_of_mean_time"] = round(gather_bytes / (float(g_us.mean()) * 1e3) / link_gbs, 4)
+    return out
+
+
 def run_gpu(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -1008,6 +1078,12 @@ def run_gpu(args, rank, world, local_rank):
     del g_iso
     torch.cuda.synchronize()
     iso.close()
+    # the same launch order without event nodes: kernel spans from the span trace
+    span_steps = 3
+    span_ts = [first + k % args.steps for k in range(span_steps)]
+    spans_raw = measure_spans(st, nxt, [qla_dev[s_] for s_ in span_ts], [q_dev[s_] for s_ in span_ts], out_dev,
+                              args.copy, app_list([nxt + k for k in range(span_steps)]), steps=span_steps)
+    nxt += span_steps
     # attended blocks (selected and resident) per head, counted on eager steps
     attended = torch.zeros((), dtype=torch.int64, device=dev)
     fetched = torch.zeros((), dtype=torch.int64, device=dev)
@@ -1167,6 +1243,16 @@ def run_gpu(args, rank, world, local_rank):
             "frac_mean": per_layer / (g_mean / 1000.0) / 1e9 / hostlink["peak"],
             "frac_p50": per_layer / (g_p50 / 1000.0) / 1e9 / hostlink["peak"],
             "source": "gather launches of the per-kernel timing graph (3 replays x layers)"}
+    kernel_spans = summarize_spans(spans_raw, L, span_steps, args.copy, gather_bytes=fetched_bytes_per_step / L,
+                                   link_gbs=hostlink["peak"] if hostlink else None)
+    if hostlink is not None and "decode_gather" in hostlink and "gather" in kernel_spans["kernel_us"]:
+        gs = kernel_spans["kernel_us"]["gather"]
+        per_layer = fetched_bytes_per_step / L
+        hostlink["decode_gather"].update({
+            "span_p50_us": gs["p50"], "span_mean_us": gs["mean"],
+            "span_frac_p50": per_layer / (gs["p50"] * 1e3) / hostlink["peak"],
+            "span_frac_mean": per_layer / (gs["mean"] * 1e3) / hostlink["peak"],
+            "span_source": "gather spans of the traced graph (no event nodes)"})
 
     launches = launches_per_step(st, args.copy)
     # exact top-64 turnover of the true queries from one step to the next (layer 0)
@@ -1216,6 +1302,7 @@ def run_gpu(args, rank, world, local_rank):
         "kernel_avg_us": {k: round(1000.0 * sum(v) / len(v), 2) for k, v in kernel_ms.items() if v},
         "kernel_p50_us": {k: round(1000.0 * statistics.median(v), 2) for k, v in kernel_ms.items() if v},
         "kernel_max_us": {k: round(1000.0 * max(v), 2) for k, v in kernel_ms.items() if v},
+        "kernel_spans": kernel_spans,
         "attended_blocks_per_head": round(attended_per_head, 2),
         "fetched_bytes_per_step": int(fetched_bytes_per_step),
         "timed_steps": [pre + args.warmup, pre + args.warmup + args.steps - 1],

@@ -542,10 +542,10 @@ OASIS_API oasis_status oasis_touch_host(const void* host_ptr, size_t bytes, uint
  * Process-wide launch options (the pages have no counterpart: scheduling knobs).
  * OASIS_OPT_SCORE_CTAS_PER_SM: the mma.sync max-dot block scorer (with or without
  *   a carried copy) sizes its persistent grid to value CTAs per SM (0 = as many as
- *   fit, the default).  The pooled scorer always runs one CTA per SM (its shared-
- *   memory ring fills the SM) and ignores it.  A caller that runs the selection, gather and attention
- *   kernels of one layer beside the scorer of the next on another stream leaves
- *   them room this way.  Read at every launch; results do not depend on it.
+ *   fit, the default); so does the pooled scorer (4 CTAs of 4 warps per SM when
+ *   0).  A caller that runs the selection, gather and attention kernels of one
+ *   layer beside the scorer of the next on another stream leaves them room this
+ *   way.  Read at every launch; results do not depend on it.
  * Unknown options or values return OASIS_ERR_INVALID.
  */
 #define OASIS_OPT_SCORE_CTAS_PER_SM 1
@@ -595,6 +595,49 @@ OASIS_API oasis_status oasis_set_agreement(const oasis_shape* shape, const int32
                                            const int32_t* nexact, const int32_t* blk2slot,
                                            int32_t* counts, uint32_t* err_word,
                                            oasis_stream_t stream);
+
+/*
+ * Kernel span trace (diagnostics; the pages have no counterpart).  With a trace
+ * buffer set, thread 0 of every thread block of the kernels below reads the GPU's
+ * nanosecond global timer when the block starts and when it ends, and each launch
+ * gets one record: the earliest start and the latest end over its blocks.  A
+ * CUDA graph replays without event nodes between its kernels, so the records
+ * show where a replayed decode step spends its time without perturbing it.
+ *
+ * Kinds (record arrays):
+ *   OASIS_TRACE_SCORE        max-dot scorers (mma.sync, dynamic, copy-carrying, tcgen05)
+ *   OASIS_TRACE_SCORE_POOLED pooled-key scorer
+ *   OASIS_TRACE_SELECT       top-K (+ diff) and diff-only selection kernels
+ *   OASIS_TRACE_GATHER       gather_h2d (slot assignment, with or without the copy)
+ *   OASIS_TRACE_COPY         copy of fetched blocks (oasis_copy_fetched[_wait])
+ *   OASIS_TRACE_ATTN         attention partial kernel (its combine launch is not traced)
+ *   OASIS_TRACE_APPEND       token append
+ * Buffer (caller-owned device memory of oasis_trace_bytes(capacity) bytes, zeroed
+ * by the caller before it is set):
+ *   uint32 ctl[2 * OASIS_TRACE_KINDS]   per kind: records begun, blocks finished
+ *   (padding to 128 bytes)
+ *   uint64 rec[OASIS_TRACE_KINDS][capacity][2]
+ *     rec[k][i][0] = ~(earliest start in ns), rec[k][i][1] = latest end in ns of
+ *     the i-th launch of kind k (modulo capacity); unused records are zero.
+ * oasis_trace_set(buf, capacity) makes later launches record into buf; NULL turns
+ * tracing off.  The pointer is read when a kernel is launched, so a CUDA graph
+ * captured while it is set keeps recording into that buffer on every replay.
+ * Records are not cleared when the index wraps: give the buffer the capacity of
+ * the launches made between two zeroings.  Launches of one kind that overlap in
+ * time share one record.  The buffer must
+ * stay allocated while any launch or graph that records into it may run.
+ * Errors: capacity < 1 or a buffer not 16-byte aligned -> OASIS_ERR_INVALID.
+ */
+#define OASIS_TRACE_KINDS 7
+#define OASIS_TRACE_SCORE 0
+#define OASIS_TRACE_SCORE_POOLED 1
+#define OASIS_TRACE_SELECT 2
+#define OASIS_TRACE_GATHER 3
+#define OASIS_TRACE_COPY 4
+#define OASIS_TRACE_ATTN 5
+#define OASIS_TRACE_APPEND 6
+OASIS_API size_t oasis_trace_bytes(int32_t capacity);
+OASIS_API oasis_status oasis_trace_set(void* dev_buf, int32_t capacity);
 
 #ifdef __cplusplus
 }

@@ -83,6 +83,8 @@ _SIGS = {
                                        _VP, _VP, _VP, _VP], ctypes.c_int),
     "oasis_touch_host": ([_VP, ctypes.c_size_t, _VP, _VP], ctypes.c_int),
     "oasis_set_option": ([ctypes.c_int32, ctypes.c_int32], ctypes.c_int),
+    "oasis_trace_bytes": ([ctypes.c_int32], ctypes.c_size_t),
+    "oasis_trace_set": ([_VP, ctypes.c_int32], ctypes.c_int),
     "oasis_sparse_decode_attn": ([ctypes.POINTER(Shape), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                   ctypes.c_float, _VP, ctypes.c_size_t, _VP, _VP], ctypes.c_int),
     "oasis_attn_workspace_bytes": ([ctypes.POINTER(Shape)], ctypes.c_size_t),
@@ -315,6 +317,20 @@ def oasis_set_option(option: int, value: int):
     """Process-wide launch option (OPT_SCORE_CTAS_PER_SM: scorer CTAs per SM, 0 = as many as
     fit; OPT_SCORE_KERNEL: SCORE_KERNEL_MMA or SCORE_KERNEL_TC)."""
     _check("oasis_set_option", load().oasis_set_option(int(option), int(value)))
+
+
+TRACE_KINDS = 7
+TRACE_SCORE, TRACE_SCORE_POOLED, TRACE_SELECT, TRACE_GATHER, TRACE_COPY, TRACE_ATTN, TRACE_APPEND = range(7)
+TRACE_HEADER_BYTES = 128
+
+
+def oasis_trace_bytes(capacity: int) -> int:
+    return int(load().oasis_trace_bytes(int(capacity)))
+
+
+def oasis_trace_set(dev_buf, capacity: int = 0):
+    """Make later launches record their spans into dev_buf (None: tracing off)."""
+    _check("oasis_trace_set", load().oasis_trace_set(_ptr(dev_buf), int(capacity)))
 
 
 def oasis_sparse_decode_attn(shape: Shape, q, k_pool, v_pool, sel, nsel, blk2slot, ctx_len,

@@ -1,5 +1,6 @@
 // C ABI entry points: argument validation, then the kernel launches.
 #include <atomic>
+#include <mutex>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -97,6 +98,12 @@ namespace {
 }  // namespace
 
 namespace oasis {
+static std::mutex g_trace_mu;
+static TraceBuf g_trace{nullptr, nullptr, 0};
+TraceBuf trace_buf() {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  return g_trace;
+}
 static std::atomic<int> g_score_ctas_per_sm{0};
 static std::atomic<int> g_score_kernel{0};  // 0: mma.sync scorer, 1: tcgen05/TMA scorer
 static std::atomic<int> g_copy_ctas{0};     // 0: the copy kernel's own grid
@@ -136,6 +143,30 @@ const char* oasis_last_error(void) { return g_last_error.c_str(); }
 // by oasis_set_option(OASIS_OPT_SCORE_KERNEL, ...); both implement the same
 // definition and bound.
 static bool use_tc_scoring() { return oasis::g_score_kernel.load(std::memory_order_relaxed) == 1; }
+
+// ------------------------------------------------------------------ span trace
+static constexpr size_t kTraceHeaderBytes = 128;  // ctl words, padded
+
+size_t oasis_trace_bytes(int32_t capacity) {
+  if (capacity < 1) return 0;
+  return kTraceHeaderBytes + (size_t)OASIS_TRACE_KINDS * (size_t)capacity * 2 * sizeof(unsigned long long);
+}
+
+oasis_status oasis_trace_set(void* dev_buf, int32_t capacity) {
+  static const char* fn = "oasis_trace_set";
+  if (dev_buf == nullptr) {
+    std::lock_guard<std::mutex> lk(oasis::g_trace_mu);
+    oasis::g_trace = oasis::TraceBuf{nullptr, nullptr, 0};
+    return OASIS_OK;
+  }
+  REQUIRE(capacity >= 1, "capacity must be >= 1");
+  REQUIRE(aligned(dev_buf, 16), "the trace buffer must be 16-byte aligned");
+  std::lock_guard<std::mutex> lk(oasis::g_trace_mu);
+  oasis::g_trace = oasis::TraceBuf{static_cast<unsigned*>(dev_buf),
+                                   reinterpret_cast<unsigned long long*>(static_cast<char*>(dev_buf) + kTraceHeaderBytes),
+                                   (int)capacity};
+  return OASIS_OK;
+}
 
 oasis_status oasis_score_blocks(const oasis_shape* shape, const void* k_hbm, const int32_t* ctx_len,
                                 const void* q_la, float* scores, uint32_t* err_word, oasis_stream_t stream) {

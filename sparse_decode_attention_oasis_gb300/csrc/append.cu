@@ -20,7 +20,8 @@ __global__ void __launch_bounds__(kAppendThreads)
 append_kv_kernel(Shape s, const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
                  int* __restrict__ ctx_len, uint16_t* __restrict__ k_hbm, uint16_t* __restrict__ host_kv,
                  const int* __restrict__ blk2slot, uint16_t* __restrict__ k_pool, uint16_t* __restrict__ v_pool,
-                 int advance, unsigned* __restrict__ err) {
+                 int advance, unsigned* __restrict__ err, TraceBuf tb) {
+  TraceScope trace_(tb, OASIS_TRACE_APPEND);
   const int b = blockIdx.x;
   const int t = ctx_len[b];
   const long long T_max = (long long)s.nb_max * kBS;
@@ -58,7 +59,7 @@ cudaError_t launch_append_kv(const Shape& s, const uint16_t* k_new, const uint16
                              uint16_t* k_hbm, uint16_t* host_kv, const int* blk2slot, uint16_t* k_pool,
                              uint16_t* v_pool, int advance, unsigned* err, cudaStream_t stream) {
   append_kv_kernel<<<s.B, kAppendThreads, 0, stream>>>(s, k_new, v_new, ctx, k_hbm, host_kv, blk2slot, k_pool,
-                                                       v_pool, advance, err);
+                                                       v_pool, advance, err, trace_buf());
   return cudaGetLastError();
 }
 

@@ -62,7 +62,9 @@ attn_partial_kernel(Shape s, const uint16_t* __restrict__ q, const uint16_t* __r
                     const uint16_t* __restrict__ v_pool, const int* __restrict__ sel,
                     const int* __restrict__ nsel, const int* __restrict__ blk2slot,
                     const int* __restrict__ ctx_len, float scale_log2, float* __restrict__ part_o,
-                    float* __restrict__ part_ml, float* __restrict__ out, int nsplit, int per_split) {
+                    float* __restrict__ part_ml, float* __restrict__ out, int nsplit, int per_split,
+                    TraceBuf tb) {
+  TraceScope trace_(tb, OASIS_TRACE_ATTN);
   extern __shared__ __align__(128) uint8_t asmem[];
   __shared__ float sm_m[kAttnWarps][G];
   __shared__ float sm_l[kAttnWarps][G];
@@ -317,12 +319,13 @@ cudaError_t launch_sparse_decode_attn(const Shape& s, const uint16_t* q, const u
   dim3 block(kAttnWarps * 32);
   static int attr_cache[4][kMaxDevicesCached] = {};
   cudaError_t e = cudaSuccess;
+  const TraceBuf tb = trace_buf();
 #define OASIS_ATTN_LAUNCH(GG, IDX)                                                                              \
   e = ensure_dyn_smem((const void*)attn_partial_kernel<GG>, kAttnSmem, attr_cache[IDX]);                      \
   if (e != cudaSuccess) return e;                                                                              \
   attn_partial_kernel<GG><<<grid, block, kAttnSmem, stream>>>(s, q, k_pool, v_pool, sel, nsel, blk2slot, ctx,  \
                                                               scale_log2, part_o, part_ml, out, nsplit,       \
-                                                              per_split);
+                                                              per_split, tb);
   switch (G) {
     case 1: OASIS_ATTN_LAUNCH(1, 0) break;
     case 2: OASIS_ATTN_LAUNCH(2, 1) break;

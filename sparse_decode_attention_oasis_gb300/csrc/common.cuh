@@ -93,6 +93,56 @@ __device__ __forceinline__ float key_float(uint32_t k) {
 int score_ctas_per_sm_option();
 int copy_ctas_option();
 
+// Kernel span trace (oasis_trace_set): passed by value to every traced kernel;
+// ctl == nullptr when tracing is off.
+struct TraceBuf {
+  unsigned* ctl;            // [2 * OASIS_TRACE_KINDS]: records begun, blocks finished, per kind
+  unsigned long long* rec;  // [OASIS_TRACE_KINDS][cap][2]: ~earliest start, latest end (ns)
+  int cap;
+};
+TraceBuf trace_buf();  // the buffer set now (host)
+
+__device__ __forceinline__ unsigned long long trace_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// One object per thread block, first statement of a traced kernel: thread 0 reads
+// the timer and the kind's record index when the block starts and folds its start
+// and end into that record when the block ends (any return); the last block of
+// the launch to finish moves the kind on to the next record.  Launches of one
+// kind that are stream-ordered read distinct indices: every block of the earlier
+// launch has finished, index advanced, before any block of the later one starts.
+struct TraceScope {
+  unsigned* ctl;
+  unsigned long long* rec;
+  int cap, kind;
+  unsigned long long t0 = 0;
+  unsigned seq = 0;
+  __device__ __forceinline__ TraceScope(const TraceBuf& b, int k) : ctl(b.ctl), rec(b.rec), cap(b.cap), kind(k) {
+    if (ctl != nullptr && threadIdx.x == 0 && threadIdx.y == 0 && threadIdx.z == 0) {
+      t0 = trace_now();
+      seq = *reinterpret_cast<volatile unsigned*>(ctl + 2 * kind);
+    }
+  }
+  __device__ __forceinline__ ~TraceScope() {
+    if (ctl != nullptr && threadIdx.x == 0 && threadIdx.y == 0 && threadIdx.z == 0) {
+      const unsigned long long t1 = trace_now();
+      unsigned long long* r = rec + ((long long)kind * cap + (long long)(seq % (unsigned)cap)) * 2;
+      atomicMax(r, ~t0);
+      atomicMax(r + 1, t1);
+      __threadfence();
+      const unsigned blocks = gridDim.x * gridDim.y * gridDim.z;
+      if (atomicAdd(ctl + 2 * kind + 1, 1u) == blocks - 1) {
+        ctl[2 * kind + 1] = 0u;
+        __threadfence();
+        atomicAdd(ctl + 2 * kind, 1u);
+      }
+    }
+  }
+};
+
 // Host-side caches so that a launch costs no more than the launch itself.
 constexpr int kMaxDevicesCached = 64;
 

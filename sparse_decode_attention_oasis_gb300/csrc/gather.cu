@@ -50,7 +50,8 @@ gather_h2d_kernel(Shape s, const uint16_t* __restrict__ host_kv, const int* __re
                   const int* __restrict__ nfetch, int* __restrict__ blk2slot,
                   int* __restrict__ slot2blk, int* __restrict__ last_used, const int* __restrict__ step_ptr,
                   uint16_t* __restrict__ k_pool, uint16_t* __restrict__ v_pool,
-                  unsigned* __restrict__ err) {
+                  unsigned* __restrict__ err, TraceBuf trace) {
+  TraceScope trace_(trace, OASIS_TRACE_GATHER);
   extern __shared__ __align__(16) int gsm[];
   const int Kb = s.Kb, P = s.P;
   int* S = gsm;              // [Kb]
@@ -241,7 +242,7 @@ static cudaError_t launch_gather(const Shape& s, const uint16_t* host_kv, const 
     if (e != cudaSuccess) return e;
   }
   gather_h2d_kernel<kCopy><<<s.B * s.Hkv, kGatherThreads, smem, stream>>>(
-      s, host_kv, sel, nsel, fetch, nfetch, blk2slot, slot2blk, last_used, step, k_pool, v_pool, err);
+      s, host_kv, sel, nsel, fetch, nfetch, blk2slot, slot2blk, last_used, step, k_pool, v_pool, err, trace_buf());
   return cudaGetLastError();
 }
 
@@ -304,7 +305,9 @@ __device__ __forceinline__ bool wait_ready(const ReadyWait& w, unsigned* err) {
 }
 
 template <bool kWait>
-__global__ void __launch_bounds__(kCopyWarps * 32) copy_fetched_kernel(Shape s, CopyJob job, ReadyWait rw) {
+__global__ void __launch_bounds__(kCopyWarps * 32) copy_fetched_kernel(Shape s, CopyJob job, ReadyWait rw,
+                                                                       TraceBuf tb) {
+  TraceScope trace_(tb, OASIS_TRACE_COPY);
   extern __shared__ uint4 copy_buf[];
   if constexpr (kWait) {
     if (!wait_ready(rw, job.err)) return;
@@ -331,14 +334,14 @@ static int copy_grid(const Shape& s) {
 
 cudaError_t launch_copy_fetched(const Shape& s, const CopyJob& job, cudaStream_t stream) {
   copy_fetched_kernel<false><<<copy_grid(s), kCopyWarps * 32, kCopyWarps * kCopyUnitBytes, stream>>>(
-      s, job, ReadyWait{nullptr, 0u, 0});
+      s, job, ReadyWait{nullptr, 0u, 0}, trace_buf());
   return cudaGetLastError();
 }
 
 cudaError_t launch_copy_fetched_wait(const Shape& s, const CopyJob& job, const unsigned* flag, unsigned value,
                                      int max_polls, cudaStream_t stream) {
   copy_fetched_kernel<true><<<copy_grid(s), kCopyWarps * 32, kCopyWarps * kCopyUnitBytes, stream>>>(
-      s, job, ReadyWait{flag, value, max_polls});
+      s, job, ReadyWait{flag, value, max_polls}, trace_buf());
   return cudaGetLastError();
 }
 

@@ -216,7 +216,8 @@ template <int NT, bool kCopy, bool kDyn = false>
 __global__ void __launch_bounds__(kScoreWarps * 32, (NT <= 2 ? 4 : 3))
 score_blocks_kernel(Shape s, const uint16_t* __restrict__ k_hbm, const int* __restrict__ ctx_len,
                     const uint16_t* __restrict__ q_la, float2* __restrict__ scores, float inv_sqrt_d,
-                    CopyJob job, unsigned* __restrict__ work = nullptr, int chunk_blocks = 0) {
+                    CopyJob job, TraceBuf tb, unsigned* __restrict__ work = nullptr, int chunk_blocks = 0) {
+  TraceScope trace_(tb, OASIS_TRACE_SCORE);
   extern __shared__ uint4 copy_buf[];  // [kScoreWarps][512] when kCopy
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -321,11 +322,12 @@ static cudaError_t launch_score(const Shape& s, const uint16_t* k, const int* ct
   if (grid < 1) grid = 1;
   const dim3 block(kScoreWarps * 32);
   const size_t smem = kCopy ? kScoreCopySmem : 0;
+  const TraceBuf tb = trace_buf();
   switch (NT) {
-    case 1: score_blocks_kernel<1, kCopy><<<grid, block, smem, stream>>>(s, k, ctx, q_la, scores, inv, job); break;
-    case 2: score_blocks_kernel<2, kCopy><<<grid, block, smem, stream>>>(s, k, ctx, q_la, scores, inv, job); break;
-    case 3: score_blocks_kernel<3, kCopy><<<grid, block, smem, stream>>>(s, k, ctx, q_la, scores, inv, job); break;
-    case 4: score_blocks_kernel<4, kCopy><<<grid, block, smem, stream>>>(s, k, ctx, q_la, scores, inv, job); break;
+    case 1: score_blocks_kernel<1, kCopy><<<grid, block, smem, stream>>>(s, k, ctx, q_la, scores, inv, job, tb); break;
+    case 2: score_blocks_kernel<2, kCopy><<<grid, block, smem, stream>>>(s, k, ctx, q_la, scores, inv, job, tb); break;
+    case 3: score_blocks_kernel<3, kCopy><<<grid, block, smem, stream>>>(s, k, ctx, q_la, scores, inv, job, tb); break;
+    case 4: score_blocks_kernel<4, kCopy><<<grid, block, smem, stream>>>(s, k, ctx, q_la, scores, inv, job, tb); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -345,11 +347,12 @@ cudaError_t launch_score_blocks_dyn(const Shape& s, const uint16_t* k, const int
   if (grid < 1) grid = 1;
   const dim3 block(kScoreWarps * 32);
   const CopyJob job{};
+  const TraceBuf tb = trace_buf();
   switch (NT) {
-    case 1: score_blocks_kernel<1, false, true><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, inv, job, work, kDynChunk); break;
-    case 2: score_blocks_kernel<2, false, true><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, inv, job, work, kDynChunk); break;
-    case 3: score_blocks_kernel<3, false, true><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, inv, job, work, kDynChunk); break;
-    case 4: score_blocks_kernel<4, false, true><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, inv, job, work, kDynChunk); break;
+    case 1: score_blocks_kernel<1, false, true><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, inv, job, tb, work, kDynChunk); break;
+    case 2: score_blocks_kernel<2, false, true><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, inv, job, tb, work, kDynChunk); break;
+    case 3: score_blocks_kernel<3, false, true><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, inv, job, tb, work, kDynChunk); break;
+    case 4: score_blocks_kernel<4, false, true><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, inv, job, tb, work, kDynChunk); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

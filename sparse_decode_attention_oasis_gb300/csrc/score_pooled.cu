@@ -97,7 +97,9 @@ struct TileMap {
 template <int NT, bool kCopy>
 __global__ void __launch_bounds__(kPsWarps * 32, 4)
 score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restrict__ ctx_len,
-                    const uint16_t* __restrict__ q_la, float2* __restrict__ scores, float inv_sqrt_d, CopyJob job) {
+                    const uint16_t* __restrict__ q_la, float2* __restrict__ scores, float inv_sqrt_d, CopyJob job,
+                    TraceBuf tb) {
+  TraceScope trace_(tb, OASIS_TRACE_SCORE_POOLED);
   constexpr int kHeadsCached = HeadsCached<NT>::value;
   extern __shared__ __align__(128) uint8_t ps_dyn[];
   PooledSmem<NT>& sm = *reinterpret_cast<PooledSmem<NT>*>(ps_dyn);
@@ -331,7 +333,7 @@ static cudaError_t launch_nt2(const Shape& s, const uint16_t* kp, const int* ctx
   const int cap = score_ctas_per_sm_option();
   const int grid = sm_count() * (cap > 0 && cap < per_sm ? cap : per_sm);
   score_pooled_kernel<NT, kCopy><<<grid, kPsWarps * 32, smem, stream>>>(s, kp, ctx, q_la, scores,
-                                                                       1.0f / sqrtf((float)s.d), job);
+                                                                       1.0f / sqrtf((float)s.d), job, trace_buf());
   return cudaGetLastError();
 }
 

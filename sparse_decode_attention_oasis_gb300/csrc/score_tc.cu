@@ -190,7 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 score_blocks_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
                        Shape s, const int* __restrict__ ctx_len, float2* __restrict__ scores,
                        unsigned* __restrict__ err, int tiles_per_head, int total_tiles, int npad,
-                       float inv_sqrt_d) {
+                       float inv_sqrt_d, TraceBuf tb) {
+  TraceScope trace_(tb, OASIS_TRACE_SCORE);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + (size_t)kStages * kStageBytes);
@@ -419,7 +420,8 @@ cudaError_t launch_score_blocks_tc(const Shape& s, const uint16_t* k, const int*
   cudaError_t e = ensure_dyn_smem((const void*)score_blocks_tc_kernel, kSmemBytes, attr_cache);
   if (e != cudaSuccess) return e;
   score_blocks_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mk, mq, s, ctx, scores, err, tiles_per_head,
-                                                                 total, npad, 1.0f / sqrtf((float)s.d));
+                                                                 total, npad, 1.0f / sqrtf((float)s.d),
+                                                                 trace_buf());
   return cudaGetLastError();
 }
 

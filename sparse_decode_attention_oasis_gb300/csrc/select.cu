@@ -960,7 +960,9 @@ __global__ void __launch_bounds__(NTH, 512 / NTH)
 topk_select_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __restrict__ k_hbm,
                    const uint16_t* __restrict__ q_la, const int* __restrict__ ctx_len,
                    int* __restrict__ sel, int* __restrict__ nsel, const int* __restrict__ blk2slot, int cap,
-                   int* __restrict__ fetch, int* __restrict__ nfetch, const uint16_t* __restrict__ host_kv) {
+                   int* __restrict__ fetch, int* __restrict__ nfetch, const uint16_t* __restrict__ host_kv,
+                   TraceBuf tb) {
+  TraceScope trace_(tb, OASIS_TRACE_SELECT);
   extern __shared__ __align__(16) char sm[];
   const SelLayout L = sel_layout(s.nb_max, kDiff, s.Kb, NTH / 32);
   const int head = blockIdx.x;
@@ -1030,7 +1032,8 @@ fetch_diff_kernel(Shape s, const float2* __restrict__ scores, const uint16_t* __
                   const uint16_t* __restrict__ q_la, const int* __restrict__ ctx_len,
                   const int* __restrict__ sel, const int* __restrict__ nsel,
                   const int* __restrict__ blk2slot, int cap, int* __restrict__ fetch,
-                  int* __restrict__ nfetch) {
+                  int* __restrict__ nfetch, TraceBuf tb) {
+  TraceScope trace_(tb, OASIS_TRACE_SELECT);
   extern __shared__ __align__(16) char sm[];
   const SelLayout L = sel_layout(s.Kb, true, s.Kb);
   const int head = blockIdx.x;
@@ -1064,7 +1067,8 @@ static cudaError_t launch_topk_nth(const Shape& s, const float2* scores, const u
   cudaError_t e = ensure_dyn_smem((const void*)topk_select_kernel<kPooled, kDiff, NTH>, smem, attr_cache);
   if (e != cudaSuccess) return e;
   topk_select_kernel<kPooled, kDiff, NTH><<<s.B * s.Hkv, NTH, smem, stream>>>(s, scores, k, q_la, ctx, sel, nsel,
-                                                                              blk2slot, cap, fetch, nfetch, host_kv);
+                                                                              blk2slot, cap, fetch, nfetch, host_kv,
+                                                                              trace_buf());
   return cudaGetLastError();
 }
 
@@ -1104,7 +1108,7 @@ static cudaError_t launch_diff(const Shape& s, const float2* scores, const uint1
   cudaError_t e = ensure_dyn_smem((const void*)fetch_diff_kernel<kPooled>, smem, attr_cache);
   if (e != cudaSuccess) return e;
   fetch_diff_kernel<kPooled><<<s.B * s.Hkv, kSelThreads, smem, stream>>>(s, scores, k, q_la, ctx, sel, nsel,
-                                                                        blk2slot, cap, fetch, nfetch);
+                                                                        blk2slot, cap, fetch, nfetch, trace_buf());
   return cudaGetLastError();
 }
 

@@ -850,6 +850,48 @@ class AgreementProbe:
         return out
 
 
+class KernelTrace:
+    """Kernel span records (oasis_trace_set) in a device buffer owned here.
+
+    ``start()`` makes later launches record (a CUDA graph captured meanwhile keeps
+    recording on every replay), ``stop()`` ends that for new launches,
+    ``spans()`` returns, per kind, the (start, end) nanosecond arrays of the
+    recorded launches in launch order.  Diagnostics only: results do not depend on
+    it.
+    """
+
+    KINDS = {"score": B.TRACE_SCORE, "score_pooled": B.TRACE_SCORE_POOLED, "select": B.TRACE_SELECT,
+             "gather": B.TRACE_GATHER, "copy": B.TRACE_COPY, "attn": B.TRACE_ATTN, "append": B.TRACE_APPEND}
+
+    def __init__(self, capacity: int = 1024, device="cuda"):
+        self.capacity = int(capacity)
+        nbytes = B.oasis_trace_bytes(self.capacity)
+        self.buf = torch.zeros((nbytes + 7) // 8, dtype=torch.int64, device=device)
+
+    def start(self):
+        B.oasis_trace_set(self.buf, self.capacity)
+
+    @staticmethod
+    def stop():
+        B.oasis_trace_set(None)
+
+    def reset(self):
+        self.buf.zero_()
+
+    def spans(self):
+        raw = self.buf.cpu().numpy().view(np.uint8)
+        ctl = raw[:B.TRACE_HEADER_BYTES].view(np.uint32)[:2 * B.TRACE_KINDS]
+        rec = raw[B.TRACE_HEADER_BYTES:B.TRACE_HEADER_BYTES + B.TRACE_KINDS * self.capacity * 16]
+        rec = rec.view(np.uint64).reshape(B.TRACE_KINDS, self.capacity, 2)
+        out = {}
+        for name, k in self.KINDS.items():
+            n = int(ctl[2 * k])
+            if n > self.capacity:
+                raise RuntimeError(f"{n} launches of kind {name} overflowed a trace of {self.capacity} records")
+            out[name] = ((~rec[k, :n, 0]).astype(np.int64), rec[k, :n, 1].astype(np.int64))
+        return out
+
+
 class StepGraph:
     """Decode steps captured as one CUDA graph and replayed.
 
