@@ -117,3 +117,31 @@ def test_reference_arm_line_says_what_it_timed(bench, monkeypatch, capsys):
 def test_workload_description_names_the_drifting_hot_set(bench):
     assert "drifting through 256 planted blocks" in bench.workload_desc(syn.long_output())
     assert "64 planted hot blocks" in bench.workload_desc(syn.qwen3_8b_decode())
+
+
+def test_span_summary_of_a_hand_made_overlap_timeline(bench):
+    """Two layers, one step, in ns: score 0-300us, select 302-322, gather 324-350
+    (side), attention of layer 0 runs 324-340 beside layer 1's gather; the gaps of
+    the critical path follow from these numbers alone."""
+    import numpy as np
+
+    us = lambda *v: np.array([int(x * 1000) for x in v], dtype=np.int64)  # noqa: E731
+    sp = {
+        "score": (us(0, 352), us(300, 652)),
+        "select": (us(302, 654), us(322, 674)),
+        "gather": (us(324, 676), us(350, 700)),
+        "attn": (us(676, 702), us(690, 716)),
+        "score_pooled": (us(), us()), "copy": (us(), us()), "append": (us(), us()),
+    }
+    out = bench.summarize_spans(sp, L=2, steps=1, copy="overlap", gather_bytes=4_194_304, link_gbs=200.0)
+    k = out["kernel_us"]
+    assert k["score"]["p50"] == 300.0 and k["select"]["p50"] == 20.0 and k["gather"]["mean"] == 25.0
+    assert out["layer_period_us"]["p50"] == 352.0
+    g = out["gaps_us"]
+    assert g["score_end_to_select_start"]["p50"] == 2.0
+    assert g["select_end_to_gather_start"]["p50"] == 2.0
+    assert g["gather_end_to_next_score_start"]["p50"] == 2.0
+    assert g["select_end_to_attn_prev_start"]["p50"] == 2.0  # attention of layer 0 after layer 1's select
+    assert g["next_score_start_after_gather_and_attn_prev"] is None  # no layer after layer 1 here
+    # 4 MiB in 26 and 24 us: 161.3 and 174.8 GB/s
+    assert abs(out["decode_gather_gbs"]["p50"] - (4_194_304 / 26000 + 4_194_304 / 24000) / 2) < 0.1
