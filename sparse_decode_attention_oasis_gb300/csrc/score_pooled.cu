@@ -161,6 +161,39 @@ score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restr
     __syncthreads();  // every warp is done with the previous group's fragments
     if (threadIdx.x < 2) sm.qn2[threadIdx.x] = 0.f;
     __syncthreads();
+    // this group's share of the tile sequence; warp w takes tiles w, w + 8, ...
+    const int g0 = max(T0, map.first_tile(hg));
+    const int g1 = hg + nh <= head_last ? min(T1, map.first_tile(hg + nh)) : T1;
+    const int ntiles = g0 < g1 ? (g1 - g0 - warp + kPsWarps - 1) / kPsWarps : 0;
+    // tile index -> (head slot, first block) without a search: the group's heads
+    // own consecutive runs of the sequence starting at ft[0] and ft[1]
+    const int ft0 = map.first_tile(hg);
+    const int ft1 = nh > 1 ? map.first_tile(hg + 1) : 0x7fffffff;
+    const int nbh0 = clamp_nb(ctx_len[hg / s.Hkv], s.nb_max);
+    const int nbh1 = nh > 1 ? clamp_nb(ctx_len[(hg + 1) / s.Hkv], s.nb_max) : 0;
+    auto where = [&](int idx, int& hs, int& blk0, int& nbv) {
+      hs = (kHeadsCached > 1 && idx >= ft1) ? 1 : 0;
+      blk0 = (idx - (hs ? ft1 : ft0)) * kTileBlocks;
+      nbv = hs ? nbh1 : nbh0;
+    };
+
+    // Rolling prefetch: the first tile's loads go out before the Q' fragments are
+    // built (they do not depend on them); then, once chunk i of the current tile
+    // has fed its MMAs, its registers receive chunk i of this warp's next tile, so
+    // a tile's worth of loads stays in flight through the MMAs and the epilogue.
+    uint4 ra[8], rb[8];
+    int hs_c = 0, blk0_c = 0, nbv_c = 0;
+    if (ntiles > 0) {
+      where(g0 + warp, hs_c, blk0_c, nbv_c);
+      const int blk1 = min(nbv_c, blk0_c + kTileBlocks);
+      const uint16_t* base = kp + (long long)(hg + hs_c) * s.nb_max * kPK;
+      const int r0 = blk0_c + g, r1 = blk0_c + g + 8;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        ra[i] = r0 < blk1 ? ldg_stream(base + (long long)r0 * kPK + (t + 4 * i) * 8) : make_uint4(0u, 0u, 0u, 0u);
+        rb[i] = r1 < blk1 ? ldg_stream(base + (long long)r1 * kPK + (t + 4 * i) * 8) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
     // Q' fragments of the group's heads: warp w builds (head slot, n-tile) pairs w, w + 8, ...
     for (int pair = warp; pair < nh * NT; pair += kPsWarps) {
       const int hs = pair / NT, nt = pair - hs * NT;
@@ -199,38 +232,6 @@ score_pooled_kernel(Shape s, const uint16_t* __restrict__ kp, const int* __restr
     }
     __syncthreads();
 
-    // this group's share of the tile sequence; warp w takes tiles w, w + 8, ...
-    const int g0 = max(T0, map.first_tile(hg));
-    const int g1 = hg + nh <= head_last ? min(T1, map.first_tile(hg + nh)) : T1;
-    const int ntiles = g0 < g1 ? (g1 - g0 - warp + kPsWarps - 1) / kPsWarps : 0;
-    // tile index -> (head slot, first block) without a search: the group's heads
-    // own consecutive runs of the sequence starting at ft[0] and ft[1]
-    const int ft0 = map.first_tile(hg);
-    const int ft1 = nh > 1 ? map.first_tile(hg + 1) : 0x7fffffff;
-    const int nbh0 = clamp_nb(ctx_len[hg / s.Hkv], s.nb_max);
-    const int nbh1 = nh > 1 ? clamp_nb(ctx_len[(hg + 1) / s.Hkv], s.nb_max) : 0;
-    auto where = [&](int idx, int& hs, int& blk0, int& nbv) {
-      hs = (kHeadsCached > 1 && idx >= ft1) ? 1 : 0;
-      blk0 = (idx - (hs ? ft1 : ft0)) * kTileBlocks;
-      nbv = hs ? nbh1 : nbh0;
-    };
-
-    // Rolling prefetch: once chunk i of the current tile has fed its MMAs, its
-    // registers receive chunk i of this warp's next tile, so a tile's worth of
-    // loads stays in flight through the MMAs and the epilogue.
-    uint4 ra[8], rb[8];
-    int hs_c = 0, blk0_c = 0, nbv_c = 0;
-    if (ntiles > 0) {
-      where(g0 + warp, hs_c, blk0_c, nbv_c);
-      const int blk1 = min(nbv_c, blk0_c + kTileBlocks);
-      const uint16_t* base = kp + (long long)(hg + hs_c) * s.nb_max * kPK;
-      const int r0 = blk0_c + g, r1 = blk0_c + g + 8;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        ra[i] = r0 < blk1 ? ldg_stream(base + (long long)r0 * kPK + (t + 4 * i) * 8) : make_uint4(0u, 0u, 0u, 0u);
-        rb[i] = r1 < blk1 ? ldg_stream(base + (long long)r1 * kPK + (t + 4 * i) * 8) : make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
     for (int k = 0; k < ntiles; ++k) {
       const int hs = hs_c, blk0 = blk0_c;
       const int head = hg + hs;
