@@ -129,9 +129,10 @@ OASIS_API oasis_status oasis_score_blocks(const oasis_shape* shape, const void* 
 /*
  * a1, with work handed out at run time: the same scores as oasis_score_blocks
  * (the mma.sync kernel, same bound), but each thread block takes its next chunk
- * of 64 blocks from an atomic counter instead of a fixed stride, so blocks that
- * start late - because kernels of other streams still hold their SMs - take
- * fewer chunks rather than finishing last.  The grid leaves `reserve_ctas`
+ * of 64 blocks from an atomic counter instead of a fixed equal share of the valid
+ * blocks (what oasis_score_blocks gives it), so thread blocks that start late -
+ * because kernels of other streams still hold their SMs - take fewer chunks
+ * rather than finishing last.  The grid leaves `reserve_ctas`
  * thread-block slots of the GPU unused, room for such kernels.
  * Arguments: as oasis_score_blocks, plus
  *   work          device uint32 [2], 8-byte aligned: must be zero before the
