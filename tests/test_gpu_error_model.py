@@ -131,4 +131,10 @@ def test_cancellation_and_exponent_spread_with_32_query_rows(scoring, kernel, sp
     assert w.n_la * w.G == 32
     K, qla = adversarial_inputs(7 + spread, w.B, w.Hkv, w.G, w.n_la, w.ctx, spread=spread)
     worst = _check(w, K, qla, scoring, kernel)
-    assert worst <= 1.0
+    # The bound e carries a margin over the modelled accumulation error: 2^-12
+    # against 136 x 2^-23 = 2^-15.9 for the 8 k-steps of the max-dot scorers, 272 x
+    # 2^-23 = 2^-14.9 for the 16 k-steps of the pooled one.  The observed error must
+    # stay inside the model itself, not only inside e (measured on GB300: at most
+    # 5.5e-4 e for max-dot, 1.3e-3 e for pooled).
+    model = {"maxdot": 2.0 ** -15.9, "pooled": 2.0 ** -14.9}[scoring] / 2.0 ** -12
+    assert worst <= model, f"{scoring}/{kernel}: error {worst:.3g} e beyond the model's {model:.3g} e"
