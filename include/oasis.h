@@ -128,9 +128,10 @@ OASIS_API oasis_status oasis_score_blocks(const oasis_shape* shape, const void* 
 
 /*
  * a1, with work handed out at run time: the same scores as oasis_score_blocks
- * (the mma.sync kernel, same bound), but each thread block takes its next chunk
- * of 64 blocks from an atomic counter instead of a fixed equal share of the valid
- * blocks (what oasis_score_blocks gives it), so thread blocks that start late -
+ * (the mma.sync kernel, same bound), but only part of the valid blocks
+ * (OASIS_OPT_SCORE_STATIC_SHARE, 75% by default) is split into fixed equal shares
+ * as oasis_score_blocks splits all of them; thread blocks then take chunks of 64
+ * blocks of the rest from an atomic counter, so thread blocks that start late -
  * because kernels of other streams still hold their SMs - take fewer chunks
  * rather than finishing last.  The grid leaves `reserve_ctas`
  * thread-block slots of the GPU unused, room for such kernels.
@@ -565,6 +566,13 @@ OASIS_API oasis_status oasis_touch_host(const void* host_ptr, size_t bytes, uint
  *   (each warp then streams several entries); results do not depend on it.
  */
 #define OASIS_OPT_COPY_CTAS 3
+/*
+ * OASIS_OPT_SCORE_STATIC_SHARE: the part of oasis_score_blocks_dynamic's work, in
+ *   per mille of the valid blocks, split into fixed equal shares before the rest
+ *   is handed out in chunks (0 = all in chunks, 1000 = none; default 750).
+ *   Read at every launch; results do not depend on it.
+ */
+#define OASIS_OPT_SCORE_STATIC_SHARE 4
 #define OASIS_SCORE_KERNEL_MMA 0
 #define OASIS_SCORE_KERNEL_TC 1
 OASIS_API oasis_status oasis_set_option(int32_t option, int32_t value);

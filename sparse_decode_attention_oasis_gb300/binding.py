@@ -309,6 +309,7 @@ def oasis_touch_host(host_tensor, nbytes: Optional[int] = None, sink=None, strea
 OPT_SCORE_CTAS_PER_SM = 1
 OPT_SCORE_KERNEL = 2
 OPT_COPY_CTAS = 3
+OPT_SCORE_STATIC_SHARE = 4
 SCORE_KERNEL_MMA = 0
 SCORE_KERNEL_TC = 1
 

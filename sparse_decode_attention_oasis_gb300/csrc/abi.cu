@@ -109,6 +109,8 @@ static std::atomic<int> g_score_kernel{0};  // 0: mma.sync scorer, 1: tcgen05/TM
 static std::atomic<int> g_copy_ctas{0};     // 0: the copy kernel's own grid
 int score_ctas_per_sm_option() { return g_score_ctas_per_sm.load(std::memory_order_relaxed); }
 int copy_ctas_option() { return g_copy_ctas.load(std::memory_order_relaxed); }
+static std::atomic<int> g_score_static_share{750};  // per mille, oasis_score_blocks_dynamic
+int score_static_share_option() { return g_score_static_share.load(std::memory_order_relaxed); }
 // Record the message oasis_last_error() returns on this thread.
 void set_last_error(const std::string& msg) { g_last_error = msg; }
 
@@ -591,6 +593,11 @@ oasis_status oasis_set_option(int32_t option, int32_t value) {
   if (option == OASIS_OPT_COPY_CTAS) {
     REQUIRE(value >= 0 && value <= 65535, "OASIS_OPT_COPY_CTAS takes 0 (the kernel's choice) to 65535");
     oasis::g_copy_ctas.store(value, std::memory_order_relaxed);
+    return OASIS_OK;
+  }
+  if (option == OASIS_OPT_SCORE_STATIC_SHARE) {
+    REQUIRE(value >= 0 && value <= 1000, "OASIS_OPT_SCORE_STATIC_SHARE takes 0 to 1000 (per mille)");
+    oasis::g_score_static_share.store(value, std::memory_order_relaxed);
     return OASIS_OK;
   }
   if (option == OASIS_OPT_SCORE_KERNEL) {

@@ -92,6 +92,7 @@ __device__ __forceinline__ float key_float(uint32_t k) {
 // Process-wide launch option set by oasis_set_option (0 = the kernel's own choice).
 int score_ctas_per_sm_option();
 int copy_ctas_option();
+int score_static_share_option();  // per mille of the valid blocks in fixed shares (dynamic scorer)
 
 // Kernel span trace (oasis_trace_set): passed by value to every traced kernel;
 // ctl == nullptr when tracing is off.

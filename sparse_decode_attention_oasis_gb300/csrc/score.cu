@@ -207,16 +207,20 @@ struct BlockSeq {
   }
 };
 
-// kDyn: chunks of `chunk_blocks` blocks of one head are handed out by an atomic
-// counter (work[0]) instead of the static split, so thread blocks that start late
-// (their SM still busy with another kernel) simply take fewer chunks; the last
-// block to finish (work[1] counts them) leaves both words at zero for the next
-// launch.
+// kDyn: a share of the sequence of valid blocks is split into equal contiguous
+// ranges as in the static kernel (static_permille / 1000 of it); the rest is
+// handed out in chunks of `chunk_blocks` positions by an atomic counter
+// (work[0]), so thread blocks that start late (their SM still busy with a kernel
+// of another stream) take fewer chunks instead of finishing last.  Each block
+// claims its next chunk before it scores the current one, so the atomic's latency
+// overlaps the scoring.  The last block to finish (work[1] counts them) leaves
+// both words at zero for the next launch.
 template <int NT, bool kCopy, bool kDyn = false>
 __global__ void __launch_bounds__(kScoreWarps * 32, (NT <= 2 ? 4 : 3))
 score_blocks_kernel(Shape s, const uint16_t* __restrict__ k_hbm, const int* __restrict__ ctx_len,
                     const uint16_t* __restrict__ q_la, float2* __restrict__ scores, float inv_sqrt_d,
-                    CopyJob job, TraceBuf tb, unsigned* __restrict__ work = nullptr, int chunk_blocks = 0) {
+                    CopyJob job, TraceBuf tb, unsigned* __restrict__ work = nullptr, int chunk_blocks = 0,
+                    int static_permille = 1000) {
   TraceScope trace_(tb, OASIS_TRACE_SCORE);
   extern __shared__ uint4 copy_buf[];  // [kScoreWarps][512] when kCopy
   const int lane = threadIdx.x & 31;
@@ -225,78 +229,76 @@ score_blocks_kernel(Shape s, const uint16_t* __restrict__ k_hbm, const int* __re
   const long long nwarps = (long long)gridDim.x * kScoreWarps;
   if constexpr (kCopy) copy_begin(job, s, gwarp, nwarps, copy_buf + warp * (kCopyUnitBytes / 16), lane);
 
+  __shared__ int pre[kMaxPrefix + 1];
+  __shared__ int wsum[kScoreWarps];
+  __shared__ int dyn_next;
   if constexpr (kDyn) {
-    __shared__ int dyn_next;
-    const int chunks_per_head = (s.nb_max + chunk_blocks - 1) / chunk_blocks;
-    const int total_chunks = s.B * s.Hkv * chunks_per_head;
+    // the first chunk is claimed now; its latency overlaps the prefix and the static share
     if (threadIdx.x == 0) dyn_next = (int)atomicAdd(work, 1u);
+  }
+  BlockSeq seq{pre, s.Hkv, s.nb_max, s.B, s.B <= kMaxPrefix};
+  int total;
+  if (seq.exact) {
+    int run = 0;
+    for (int b0 = 0; b0 < s.B; b0 += kScoreWarps * 32) {
+      const int b = b0 + threadIdx.x;
+      const int n = b < s.B ? clamp_nb(ctx_len[b], s.nb_max) * s.Hkv : 0;
+      int x = n;  // inclusive scan over the CTA
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) wsum[warp] = x;
+      __syncthreads();
+      int off = 0, tot = 0;
+#pragma unroll
+      for (int w = 0; w < kScoreWarps; ++w) {
+        off += w < warp ? wsum[w] : 0;
+        tot += wsum[w];
+      }
+      if (b < s.B) pre[b] = run + off + x - n;
+      run += tot;
+      __syncthreads();  // wsum is rewritten by the next round
+    }
+    if (threadIdx.x == 0) pre[s.B] = run;
     __syncthreads();
-    int chunk = dyn_next;
-    while (chunk < total_chunks) {
-      const int head = chunk / chunks_per_head;  // b * Hkv + h
-      const int c = chunk - head * chunks_per_head;
-      const int b = head / s.Hkv, h = head - b * s.Hkv;
-      const int ctx = ctx_len[b];
-      const int nb = clamp_nb(ctx, s.nb_max);
-      const int blk0 = c * chunk_blocks;
-      const int blk1 = min(nb, blk0 + chunk_blocks);
-      if (blk0 < blk1) score_segment<NT>(s, k_hbm, q_la, scores, b, h, ctx, blk0, blk1, inv_sqrt_d, warp, lane);
-      __syncthreads();  // every thread has read dyn_next
-      if (threadIdx.x == 0) dyn_next = (int)atomicAdd(work, 1u);
-      __syncthreads();
-      chunk = dyn_next;
-    }
-    if (threadIdx.x == 0) {
-      __threadfence();  // this block's last fetch is ordered before its count
-      if (atomicAdd(work + 1, 1u) == gridDim.x - 1) {  // every block has fetched past the end
-        work[0] = 0u;
-        work[1] = 0u;
-      }
-    }
+    total = pre[s.B];
   } else {
-    __shared__ int pre[kMaxPrefix + 1];
-    __shared__ int wsum[kScoreWarps];
-    BlockSeq seq{pre, s.Hkv, s.nb_max, s.B, s.B <= kMaxPrefix};
-    int total;
-    if (seq.exact) {
-      int run = 0;
-      for (int b0 = 0; b0 < s.B; b0 += kScoreWarps * 32) {
-        const int b = b0 + threadIdx.x;
-        const int n = b < s.B ? clamp_nb(ctx_len[b], s.nb_max) * s.Hkv : 0;
-        int x = n;  // inclusive scan over the CTA
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, x, o);
-          if (lane >= o) x += y;
-        }
-        if (lane == 31) wsum[warp] = x;
-        __syncthreads();
-        int off = 0, tot = 0;
-#pragma unroll
-        for (int w = 0; w < kScoreWarps; ++w) {
-          off += w < warp ? wsum[w] : 0;
-          tot += wsum[w];
-        }
-        if (b < s.B) pre[b] = run + off + x - n;
-        run += tot;
-        __syncthreads();  // wsum is rewritten by the next round
-      }
-      if (threadIdx.x == 0) pre[s.B] = run;
-      __syncthreads();
-      total = pre[s.B];
-    } else {
-      total = s.B * s.Hkv * s.nb_max;
-    }
-    const int T0 = (int)((long long)blockIdx.x * total / gridDim.x);
-    const int T1 = (int)((long long)(blockIdx.x + 1) * total / gridDim.x);
-    for (int pos = T0; pos < T1;) {
+    total = s.B * s.Hkv * s.nb_max;
+  }
+  // score positions [p0, p1) of the sequence: one segment per (request, head) run
+  auto run_range = [&](int p0, int p1) {
+    for (int pos = p0; pos < p1;) {
       int b, h, blk0, run_end;
       seq.locate(pos, b, h, blk0, run_end);
-      const int end = min(T1, run_end);
+      const int end = min(p1, run_end);
       const int ctx = ctx_len[b];
       const int blk1 = min(blk0 + (end - pos), clamp_nb(ctx, s.nb_max));
       if (blk0 < blk1) score_segment<NT>(s, k_hbm, q_la, scores, b, h, ctx, blk0, blk1, inv_sqrt_d, warp, lane);
       pos = end;
+    }
+  };
+  const int stat = kDyn ? (int)((long long)total * static_permille / 1000) : total;
+  run_range((int)((long long)blockIdx.x * stat / gridDim.x), (int)((long long)(blockIdx.x + 1) * stat / gridDim.x));
+  if constexpr (kDyn) {
+    __syncthreads();  // dyn_next is visible
+    int chunk = dyn_next;
+    for (;;) {
+      const long long c0 = stat + (long long)chunk * chunk_blocks;
+      if (c0 >= total) break;
+      __syncthreads();  // every thread has read dyn_next
+      if (threadIdx.x == 0) dyn_next = (int)atomicAdd(work, 1u);  // the next chunk, claimed ahead
+      run_range((int)c0, (int)min((long long)total, c0 + chunk_blocks));
+      __syncthreads();
+      chunk = dyn_next;
+    }
+    if (threadIdx.x == 0) {
+      __threadfence();  // this block's last claim is ordered before its count
+      if (atomicAdd(work + 1, 1u) == gridDim.x - 1) {  // every block has claimed past the end
+        work[0] = 0u;
+        work[1] = 0u;
+      }
     }
   }
   if constexpr (kCopy) copy_finish(job, s, gwarp, nwarps, copy_buf + warp * (kCopyUnitBytes / 16), lane);
@@ -341,6 +343,7 @@ cudaError_t launch_score_blocks_dyn(const Shape& s, const uint16_t* k, const int
   const int NT = (N + 7) / 8;
   constexpr int kDynChunk = 64;
   const long long total = (long long)s.B * s.Hkv * ((s.nb_max + kDynChunk - 1) / kDynChunk);
+  const int share = score_static_share_option();
   const float inv = 1.0f / sqrtf((float)s.d);
   int grid = score_grid_limit(NT) - reserve;
   if (grid > total) grid = (int)total;
@@ -349,10 +352,10 @@ cudaError_t launch_score_blocks_dyn(const Shape& s, const uint16_t* k, const int
   const CopyJob job{};
   const TraceBuf tb = trace_buf();
   switch (NT) {
-    case 1: score_blocks_kernel<1, false, true><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, inv, job, tb, work, kDynChunk); break;
-    case 2: score_blocks_kernel<2, false, true><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, inv, job, tb, work, kDynChunk); break;
-    case 3: score_blocks_kernel<3, false, true><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, inv, job, tb, work, kDynChunk); break;
-    case 4: score_blocks_kernel<4, false, true><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, inv, job, tb, work, kDynChunk); break;
+    case 1: score_blocks_kernel<1, false, true><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, inv, job, tb, work, kDynChunk, share); break;
+    case 2: score_blocks_kernel<2, false, true><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, inv, job, tb, work, kDynChunk, share); break;
+    case 3: score_blocks_kernel<3, false, true><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, inv, job, tb, work, kDynChunk, share); break;
+    case 4: score_blocks_kernel<4, false, true><<<grid, block, 0, stream>>>(s, k, ctx, q_la, scores, inv, job, tb, work, kDynChunk, share); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

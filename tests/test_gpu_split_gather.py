@@ -48,11 +48,12 @@ def test_cap_zero_copy_is_a_no_op():
     c.step(0, gather="carry")
 
 
-def _multi_layer(copy, L=3, steps=3, host_alloc="cuda"):
+def _multi_layer(copy, L=3, steps=3, host_alloc="cuda", dynamic=False):
     from sparse_decode_attention_oasis_gb300.engine import DecodeState
 
     w = syn.Workload("layers", L=L, B=2, Hq=32, Hkv=8, ctx=[3000, 1777], Kb=32, C=3, n_hot=16)
     st = DecodeState(w, l_phys=L, l_host=L, host_alloc=host_alloc)
+    st.dynamic_scorer = dynamic
     layers = []
     for l in range(L):
         K, V = syn.layer_kv(w, l)
@@ -88,6 +89,10 @@ def test_multi_layer_decode_step_all_orders(copy):
     _multi_layer(copy, L=6 if copy == "pipe" else 3)
 
 
+def test_multi_layer_decode_step_with_the_dynamic_scorer():
+    _multi_layer("overlap", L=4, dynamic=True)
+
+
 def test_dynamic_scorer_equals_the_static_one_and_leaves_its_counter_at_zero():
     """oasis_score_blocks_dynamic writes the same (approximation, bound) pairs as
     oasis_score_blocks, call after call, and leaves its work counter at zero."""
@@ -104,14 +109,19 @@ def test_dynamic_scorer_equals_the_static_one_and_leaves_its_counter_at_zero():
     ref_scores = torch.zeros((w.B, w.Hkv, w.nb_max, 2), dtype=torch.float32, device="cuda")
     B.oasis_score_blocks(s, st.K[0], st.ctx, q, ref_scores)
     work = torch.zeros(2, dtype=torch.int32, device="cuda")
-    for reserve in (0, 16, 0):
-        got = torch.zeros_like(ref_scores)
-        B.oasis_score_blocks_dynamic(s, st.K[0], st.ctx, q, got, work, reserve)
-        torch.cuda.synchronize()
-        for b in range(w.B):
-            nb = w.nb(b)
-            assert torch.equal(got[b, :, :nb], ref_scores[b, :, :nb])
-        assert work.tolist() == [0, 0]
+    try:
+        for share in (750, 0, 500, 1000):  # per mille of the blocks in fixed shares
+            B.oasis_set_option(B.OPT_SCORE_STATIC_SHARE, share)
+            for reserve in (0, 16, 0):
+                got = torch.zeros_like(ref_scores)
+                B.oasis_score_blocks_dynamic(s, st.K[0], st.ctx, q, got, work, reserve)
+                torch.cuda.synchronize()
+                for b in range(w.B):
+                    nb = w.nb(b)
+                    assert torch.equal(got[b, :, :nb], ref_scores[b, :, :nb]), (share, reserve)
+                assert work.tolist() == [0, 0]
+    finally:
+        B.oasis_set_option(B.OPT_SCORE_STATIC_SHARE, 750)
 
 
 @pytest.mark.parametrize("host_alloc", ["thp", "thp_layers", "cuda_layers"])
