@@ -456,19 +456,12 @@ class DecodeState:
         B.oasis_assign_slots(s, sc.sel, sc.nsel, sc.fetch, sc.nfetch, self.b2sl[lp], self.s2bl[lp],
                              self.lul[lp], step, sc.err, st)
 
-    def _copy(self, layer, sc, st, ctas=0):
-        """The data half of layer `layer`'s gather; ctas > 0 confines its zero-copy host
-        reads to that many thread blocks (a few SMs)."""
+    def _copy(self, layer, sc, st):
+        """The data half of layer `layer`'s gather (its slots already assigned)."""
         s = self.shape
         lp, lh = layer % self.L_phys, layer % self.L_host
-        if ctas:
-            B.oasis_set_option(B.OPT_COPY_CTAS, ctas)
-        try:
-            B.oasis_copy_fetched(s, self.hostl[lh], sc.fetch, sc.nfetch, self.b2sl[lp], self.kpl[lp],
-                                 self.vpl[lp], sc.err, st)
-        finally:
-            if ctas:
-                B.oasis_set_option(B.OPT_COPY_CTAS, 0)
+        B.oasis_copy_fetched(s, self.hostl[lh], sc.fetch, sc.nfetch, self.b2sl[lp], self.kpl[lp],
+                             self.vpl[lp], sc.err, st)
 
     def _attend(self, layer, q, sc, st, out=None):
         s = self.shape
