@@ -189,3 +189,18 @@ def test_exact_negative_dots_compare_correctly():
             if blk == 11:
                 rows[(blk, tok, 1)] = -(2.0 ** -20)
     _two_block_case(rows, {0: 1.0, 1: 1.0}, 4)
+
+
+@pytest.mark.parametrize("C,scoring", [(256, "maxdot"), (7, "maxdot"), (7, "pooled")])
+def test_largest_budget_slots_and_query_rows(C, scoring):
+    """The largest shapes the ABI accepts in the per-head dimensions: a 256-block
+    (4,096-token) budget, 1,024 slots per head and 32 query rows per KV head (GQA 8 x
+    4 lookahead queries), over ragged contexts with more blocks than slots;
+    fetch-all (C = Kb) and a small cap, three steps each."""
+    w = syn.Workload("maxdims", L=1, B=2, Hq=16, Hkv=2, ctx=[32768 - 3, 20000], Kb=256, C=C, n_hot=64,
+                     n_la=4, P=1024)
+    # more blocks than slots, so the resident sets are partial and blocks are fetched
+    assert w.Kb == 256 and w.P == 1024 and w.n_la * w.G == 32 and min(w.nb(b) for b in range(w.B)) > w.P
+    c = Case(w, scoring=scoring)
+    for step in range(3):
+        c.step(step)
