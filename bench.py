@@ -66,7 +66,11 @@ sys.path.insert(0, ROOT)
 
 METRIC = "sparse decode layer-steps/sec and achieved HBM GB/s (% of GB300 peak)"
 UNIT = "layer-steps/s"
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "score_blocks_traffic.json")
+# ncu DRAM traffic of one scoring launch, per scorer kernel, with the hash of the
+# kernel source it was taken on
+PROFILE_TRAFFIC = {"mma": os.path.join(ROOT, "profiles", "score_blocks_traffic.json"),
+                   "tc": os.path.join(ROOT, "profiles", "score_blocks_tc_traffic.json")}
+KERNEL_SOURCE = {"mma": "score.cu", "tc": "score_tc.cu"}
 
 
 def parse():
@@ -101,8 +105,8 @@ def parse():
                     help="layers of distinct keys and pools in HBM (layer l uses l mod N; 0 = all, or 12 for "
                          "long_output, whose 36 layers of keys do not fit)")
     ap.add_argument("--no-pooled", action="store_true", help="skip the pooled-scoring variant")
-    ap.add_argument("--score-kernel", default="mma", choices=["mma", "tc"],
-                    help="max-dot scorer: mma.sync from registers (default) or TMA + tcgen05 with TMEM accumulators")
+    ap.add_argument("--score-kernel", default="tc", choices=["tc", "mma"],
+                    help="max-dot scorer: TMA + tcgen05 with TMEM accumulators (default) or mma.sync from registers")
     ap.add_argument("--dynamic-scorer", action="store_true",
                     help="max-dot scoring with chunks from an atomic counter (oasis_score_blocks_dynamic)")
     ap.add_argument("--no-variants", action="store_true",
@@ -164,7 +168,7 @@ def config_dict(args, w, l_phys, l_host, score_ctas, world=1):
             "hbm_layers": l_phys, "hbm_layers_aliased": l_phys < w.L,
             "host_alloc": args.host_alloc,
             "dynamic_scorer": bool(getattr(args, "dynamic_scorer", False)),
-            "score_kernel": getattr(args, "score_kernel", "mma"),
+            "score_kernel": getattr(args, "score_kernel", "tc"),
             "parallelism": "replicas" if world > 1 else "single GPU"}
 
 
@@ -419,9 +423,9 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def kernel_source_hash() -> str:
-    """Hash of the scoring kernel's code with comments and blank lines removed."""
-    src = os.path.join(ROOT, "sparse_decode_attention_oasis_gb300", "csrc", "score.cu")
+def kernel_source_hash(kernel: str = "tc") -> str:
+    """Hash of a scoring kernel's code with comments and blank lines removed."""
+    src = os.path.join(ROOT, "sparse_decode_attention_oasis_gb300", "csrc", KERNEL_SOURCE[kernel])
     code = []
     for line in open(src, encoding="utf-8"):
         line = line.split("//", 1)[0].strip()
@@ -430,12 +434,13 @@ def kernel_source_hash() -> str:
     return hashlib.sha256("\n".join(code).encode()).hexdigest()[:16]
 
 
-def score_traffic_per_launch():
+def score_traffic_per_launch(kernel: str = "tc"):
     """ncu dram bytes of one score launch (full workload), if captured for this kernel source."""
-    if not os.path.exists(PROFILE_TRAFFIC):
+    path = PROFILE_TRAFFIC[kernel]
+    if not os.path.exists(path):
         return None
-    d = json.load(open(PROFILE_TRAFFIC))
-    if d.get("score_cu_sha256_16") != kernel_source_hash():
+    d = json.load(open(path))
+    if d.get("source_sha256_16") != kernel_source_hash(kernel):
         return None
     return d.get("bytes_per_launch_full")
 
@@ -1290,10 +1295,11 @@ def run_gpu(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_dict(args, w, l_phys, l_host, score_ctas, world),
         "path_hbm_gbs": path_gbs, "path_hbm_frac": path_gbs / peak,
-        "roofline": {"kernel": "score_blocks_pooled" if args.scoring == "pooled" else "score_blocks",
+        "roofline": {"kernel": "score_blocks_pooled" if args.scoring == "pooled" else
+                     ("score_blocks_tc" if args.score_kernel == "tc" else "score_blocks"),
                      "bound": "hbm", "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": score_traffic_per_launch() if args.scoring == "maxdot" else None,
+                     "traffic": score_traffic_per_launch(args.score_kernel) if args.scoring == "maxdot" else None,
                      "bytes_per_launch": ab["score"],
                      "avg_launch_ms": score_avg_ms},
         "kernel_times_source": "a separate one-step CUDA graph of the same launch order with an event-record "

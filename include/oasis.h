@@ -117,10 +117,12 @@ OASIS_API const char* oasis_last_error(void);
  * rounding of the 1/sqrt(d) product); it is an upper bound on the error of
  * fp32-accumulated bf16 products with a wide margin.  Selection never trusts
  * s~ inside this interval: it re-scores those blocks exactly.
- * Two kernels implement it: by default warp-level mma.sync tiles fed by direct
- * 16-byte loads; after oasis_set_option(OASIS_OPT_SCORE_KERNEL,
- * OASIS_SCORE_KERNEL_TC) a tcgen05/TMA/TMEM kernel.  Their s~ may differ inside
- * the bound; everything selection derives from them is identical.
+ * Two kernels implement it: by default a tcgen05/TMA/TMEM kernel (two CTAs per
+ * SM, each a TMA producer, a single-thread MMA issuer and two groups of epilogue
+ * warps); after oasis_set_option(OASIS_OPT_SCORE_KERNEL, OASIS_SCORE_KERNEL_MMA)
+ * warp-level mma.sync tiles fed by direct 16-byte loads (also used for shapes
+ * whose layer has more than 2^31 - 1 key rows).  Their s~ may differ inside the
+ * bound; everything selection derives from them is identical.
  */
 OASIS_API oasis_status oasis_score_blocks(const oasis_shape* shape, const void* k_hbm,
                                 const int32_t* ctx_len, const void* q_la,
@@ -553,8 +555,8 @@ OASIS_API oasis_status oasis_touch_host(const void* host_ptr, size_t bytes, uint
 #define OASIS_OPT_SCORE_CTAS_PER_SM 1
 /*
  * OASIS_OPT_SCORE_KERNEL: which kernel oasis_score_blocks (and
- *   oasis_score_blocks_copy) launches: OASIS_SCORE_KERNEL_MMA (mma.sync, the
- *   default) or OASIS_SCORE_KERNEL_TC (TMA + tcgen05 + TMEM).  Same definition and
+ *   oasis_score_blocks_copy) launches: OASIS_SCORE_KERNEL_TC (TMA + tcgen05 +
+ *   TMEM, the default) or OASIS_SCORE_KERNEL_MMA (mma.sync).  Same definition and
  *   bound; selection results do not depend on it.  Read at every scoring call
  *   (an atomic load, no environment lookup).
  */

@@ -12,6 +12,7 @@ namespace oasis {
 cudaError_t launch_score_blocks(const Shape&, const uint16_t*, const int*, const uint16_t*, float2*, cudaStream_t);
 cudaError_t launch_score_blocks_dyn(const Shape&, const uint16_t*, const int*, const uint16_t*, float2*, unsigned*, int,
                                     cudaStream_t);
+bool score_tc_fits(const Shape& s);
 cudaError_t launch_score_blocks_tc(const Shape&, const uint16_t*, const int*, const uint16_t*, float2*, unsigned*,
                                    cudaStream_t);
 cudaError_t launch_topk_select(const Shape&, const float2*, const uint16_t*, const uint16_t*, const int*, int*,
@@ -105,7 +106,7 @@ TraceBuf trace_buf() {
   return g_trace;
 }
 static std::atomic<int> g_score_ctas_per_sm{0};
-static std::atomic<int> g_score_kernel{0};  // 0: mma.sync scorer, 1: tcgen05/TMA scorer
+static std::atomic<int> g_score_kernel{OASIS_SCORE_KERNEL_TC};  // tcgen05/TMA scorer unless set to mma.sync
 static std::atomic<int> g_copy_ctas{0};     // 0: the copy kernel's own grid
 int score_ctas_per_sm_option() { return g_score_ctas_per_sm.load(std::memory_order_relaxed); }
 int copy_ctas_option() { return g_copy_ctas.load(std::memory_order_relaxed); }
@@ -141,10 +142,13 @@ const char* oasis_version(void) { return "oasis-gb300 0.1 sm_103a"; }
 
 const char* oasis_last_error(void) { return g_last_error.c_str(); }
 
-// Scoring kernel: mma.sync (registers only, the default) or TMA + tcgen05, chosen
+// Scoring kernel: TMA + tcgen05 (the default) or mma.sync from registers, chosen
 // by oasis_set_option(OASIS_OPT_SCORE_KERNEL, ...); both implement the same
-// definition and bound.
-static bool use_tc_scoring() { return oasis::g_score_kernel.load(std::memory_order_relaxed) == 1; }
+// definition and bound.  Shapes with more than 2^31 - 1 key rows in one layer
+// (beyond the tensor map's 32-bit coordinates) take the mma.sync kernel.
+static bool use_tc_scoring(const oasis::Shape& s) {
+  return oasis::g_score_kernel.load(std::memory_order_relaxed) == OASIS_SCORE_KERNEL_TC && oasis::score_tc_fits(s);
+}
 
 // ------------------------------------------------------------------ span trace
 static constexpr size_t kTraceHeaderBytes = 128;  // ctl words, padded
@@ -181,7 +185,7 @@ oasis_status oasis_score_blocks(const oasis_shape* shape, const void* k_hbm, con
   REQUIRE(ctx_len && aligned(ctx_len, 4), "ctx_len must be a 4-byte aligned device pointer");
   REQUIRE(scores && aligned(scores, 8), "scores must be an 8-byte aligned device pointer");
   REQUIRE(!err_word || aligned(err_word, 4), "err_word must be NULL or a 4-byte aligned device pointer");
-  cudaError_t e = use_tc_scoring()
+  cudaError_t e = use_tc_scoring(s)
                       ? oasis::launch_score_blocks_tc(s, static_cast<const uint16_t*>(k_hbm), ctx_len,
                                                       static_cast<const uint16_t*>(q_la),
                                                       reinterpret_cast<float2*>(scores), err_word,
@@ -399,7 +403,7 @@ oasis_status oasis_score_blocks_copy(const oasis_shape* shape, const void* k_hbm
   const auto* q = static_cast<const uint16_t*>(q_la);
   auto* sc = reinterpret_cast<float2*>(scores);
   cudaError_t e;
-  if (use_tc_scoring()) {
+  if (use_tc_scoring(s)) {
     e = oasis::launch_score_blocks_tc(s, k, ctx_len, q, sc, err_word, (cudaStream_t)stream);
     if (e == cudaSuccess) e = oasis::launch_copy_fetched(s, job, (cudaStream_t)stream);
   } else {

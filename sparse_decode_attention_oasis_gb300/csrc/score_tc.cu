@@ -2,10 +2,13 @@
 //
 // Same definition and certified bound as score.cu (OasisKV, metalmedia.ai page,
 // Figure 7 caption: the draft queries are matched against the keys to choose the
-// next step's top-K blocks).  Persistent, warp-specialised, one CTA per SM:
+// next step's top-K blocks).  Persistent, warp-specialised, two CTAs per SM (one
+// CTA per SM, with a 4-stage ring, streamed only 84% of the measured copy peak:
+// a single producer-MMA-epilogue pipeline per SM does not keep enough loads in
+// flight; two pipelines of 2 stages reach it):
 //   warp 0      TMA producer: per 128-token tile, two 64-column boxes of keys
 //               (SWIZZLE_128B) and the head's N lookahead-query rows, into a
-//               4-stage ring; completion counted on a "full" mbarrier;
+//               2-stage ring; completion counted on a "full" mbarrier;
 //   warp 1      owns 64 TMEM columns; one lane issues 8 x tcgen05.mma
 //               (M=128 tokens, N=16|32 queries, K=16, bf16 -> fp32) per tile into
 //               one of two TMEM accumulators and commits to the stage's "empty"
@@ -28,7 +31,7 @@
 namespace oasis {
 namespace tc {
 
-constexpr int kStages = 4;
+constexpr int kStages = 2;  // per CTA; two CTAs per SM
 constexpr int kEpiGroups = 2;
 constexpr int kThreads = 64 + kEpiGroups * 128;
 // one 32-column TMEM accumulator per epilogue group (an allocation is a power of two >= 32)
@@ -186,7 +189,77 @@ __device__ __forceinline__ float row_sumsq(uint32_t box0, uint32_t box1, int row
   return (ss[0] + ss[1]) + (ss[2] + ss[3]);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// The valid 128-token tiles of all heads, in (request, KV head, tile) order, form
+// one sequence (an exclusive prefix over requests in shared memory, B <= 512;
+// above that every head gets tiles_per_head positions and the ones past its
+// context are skipped); CTA c takes the c-th of gridDim.x equal contiguous ranges.
+constexpr int kTcMaxPrefix = 512;
+
+struct TileSeq {
+  const int* pre;  // shared, [B + 1] when exact
+  int B, Hkv, tiles_per_head;
+  bool exact;
+  __device__ void locate(int idx, int& head, int& t) const {
+    if (!exact) {
+      head = idx / tiles_per_head;
+      t = idx - head * tiles_per_head;
+      return;
+    }
+    int lo = 0, hi = B - 1;  // the last b with pre[b] <= idx (that request has tiles)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= idx) lo = mid; else hi = mid - 1;
+    }
+    const int tb = (pre[lo + 1] - pre[lo]) / Hkv;
+    if (tb <= 0) {  // idx past the sequence (an empty range): nothing is read there
+      head = lo * Hkv;
+      t = 0;
+      return;
+    }
+    const int local = idx - pre[lo];
+    const int h = local / tb;
+    head = lo * Hkv + h;
+    t = local - h * tb;
+  }
+};
+
+// Walks a CTA's range of the sequence one tile at a time: located once, then each
+// step adds one (the single producer and MMA threads see no search or division
+// per tile; the context length is read again only when the request changes).
+struct TileIter {
+  const TileSeq& seq;
+  const int* ctx_len;
+  int nb_max;
+  int b, h, t, tb, ctx, nb;
+  __device__ TileIter(const TileSeq& q, const int* cl, int nbm, int idx) : seq(q), ctx_len(cl), nb_max(nbm) {
+    int head;
+    seq.locate(idx, head, t);
+    b = head / seq.Hkv;
+    h = head - b * seq.Hkv;
+    load();
+  }
+  __device__ void load() {
+    ctx = ctx_len[b];
+    nb = clamp_nb(ctx, nb_max);
+    tb = seq.exact ? (seq.pre[b + 1] - seq.pre[b]) / seq.Hkv : seq.tiles_per_head;
+  }
+  __device__ void next() {
+    if (++t < tb) return;
+    t = 0;
+    if (++h < seq.Hkv) return;
+    h = 0;
+    ++b;
+    if (b < seq.B) load();
+    while (seq.exact && b < seq.B && tb == 0) {  // requests without tiles own no positions
+      ++b;
+      if (b < seq.B) load();
+    }
+  }
+  __device__ int head() const { return b * seq.Hkv + h; }
+  __device__ bool valid() const { return t * 8 < nb; }
+};
+
+__global__ void __launch_bounds__(kThreads, 2)
 score_blocks_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
                        Shape s, const int* __restrict__ ctx_len, float2* __restrict__ scores,
                        unsigned* __restrict__ err, int tiles_per_head, int total_tiles, int npad,
@@ -199,9 +272,38 @@ score_blocks_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = s.Hq / s.Hkv;
   const int N = s.n_la * G;
-  const int per = (total_tiles + gridDim.x - 1) / gridDim.x;
-  const int t_start = blockIdx.x * per;
-  const int t_end = min(total_tiles, t_start + per);
+  __shared__ int tpre[kTcMaxPrefix + 1];
+  __shared__ int wsum[kThreads / 32];
+  const TileSeq seq{tpre, s.B, s.Hkv, tiles_per_head, s.B <= kTcMaxPrefix};
+  int seq_total = total_tiles;
+  if (seq.exact) {
+    int run = 0;
+    for (int b0 = 0; b0 < s.B; b0 += kThreads) {
+      const int b = b0 + threadIdx.x;
+      const int n = b < s.B ? (clamp_nb(ctx_len[b], s.nb_max) + 7) / 8 * s.Hkv : 0;
+      int x = n;  // inclusive scan over the CTA
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) wsum[warp] = x;
+      __syncthreads();
+      int off = 0, tot = 0;
+      for (int w = 0; w < kThreads / 32; ++w) {
+        off += w < warp ? wsum[w] : 0;
+        tot += wsum[w];
+      }
+      if (b < s.B) tpre[b] = run + off + x - n;
+      run += tot;
+      __syncthreads();  // wsum is rewritten by the next round
+    }
+    if (threadIdx.x == 0) tpre[s.B] = run;
+    __syncthreads();
+    seq_total = tpre[s.B];
+  }
+  const int t_start = (int)((long long)blockIdx.x * seq_total / gridDim.x);
+  const int t_end = (int)((long long)(blockIdx.x + 1) * seq_total / gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -232,11 +334,10 @@ score_blocks_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     if (lane == 0) {
       const uint32_t tx = 2 * kKBox + 2 * (uint32_t)N * 128;
       int i = 0;
-      for (int idx = t_start; idx < t_end; ++idx) {
-        const int head = idx / tiles_per_head, t = idx - head * tiles_per_head;
-        const int b = head / s.Hkv, h = head - b * s.Hkv;
-        const int nb = clamp_nb(ctx_len[b], s.nb_max);
-        if (t * 8 >= nb) continue;
+      TileIter it(seq, ctx_len, s.nb_max, t_start);
+      for (int idx = t_start; idx < t_end; ++idx, it.next()) {
+        if (!it.valid()) continue;
+        const int head = it.head(), b = it.b, h = it.h, t = it.t;
         const int st = i % kStages, r = i / kStages;
         if (!mbar_wait(&bars->empty[st], (r & 1) ^ 1, abort_flag)) { timed_out = true; break; }
         uint8_t* buf = smem + (size_t)st * kStageBytes;
@@ -255,11 +356,9 @@ score_blocks_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     if (lane == 0) {
       const uint32_t idesc = instr_desc(npad);
       int i = 0;
-      for (int idx = t_start; idx < t_end; ++idx) {
-        const int head = idx / tiles_per_head, t = idx - head * tiles_per_head;
-        const int b = head / s.Hkv;
-        const int nb = clamp_nb(ctx_len[b], s.nb_max);
-        if (t * 8 >= nb) continue;
+      TileIter it(seq, ctx_len, s.nb_max, t_start);
+      for (int idx = t_start; idx < t_end; ++idx, it.next()) {
+        if (!it.valid()) continue;
         const int st = i % kStages, r = i / kStages, a = i % kEpiGroups, u = i / kEpiGroups;
         if (!mbar_wait(&bars->tempty[a], (u & 1) ^ 1, abort_flag)) { timed_out = true; break; }
         if (!mbar_wait(&bars->full[st], r & 1, abort_flag)) { timed_out = true; break; }
@@ -289,12 +388,10 @@ score_blocks_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
     int i = 0;
     int cached_head = -1;
     float qnorm = 0.f;
-    for (int idx = t_start; idx < t_end; ++idx) {
-      const int head = idx / tiles_per_head, t = idx - head * tiles_per_head;
-      const int b = head / s.Hkv;
-      const int ctx = ctx_len[b];
-      const int nb = clamp_nb(ctx, s.nb_max);
-      if (t * 8 >= nb) continue;
+    TileIter it(seq, ctx_len, s.nb_max, t_start);
+    for (int idx = t_start; idx < t_end; ++idx, it.next()) {
+      if (!it.valid()) continue;
+      const int head = it.head(), t = it.t, ctx = it.ctx, nb = it.nb;
       const int st = i % kStages, r = i / kStages, a = i % kEpiGroups, u = i / kEpiGroups;
       if (a != group) {  // the other group's tile
         ++i;
@@ -383,6 +480,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace tc
 
+// The key tensor map addresses rows with 32-bit coordinates.
+bool score_tc_fits(const Shape& s) { return (long long)s.B * s.Hkv * s.nb_max * kBS <= 0x7fffffffLL; }
+
 cudaError_t launch_score_blocks_tc(const Shape& s, const uint16_t* k, const int* ctx, const uint16_t* q_la,
                                    float2* scores, unsigned* err, cudaStream_t stream) {
   using namespace tc;
@@ -415,7 +515,7 @@ cudaError_t launch_score_blocks_tc(const Shape& s, const uint16_t* k, const int*
   const int tiles_per_head = (s.nb_max + 7) / 8;
   const int total = s.B * s.Hkv * tiles_per_head;
   const int sms = sm_count();
-  const int grid = total < sms ? total : sms;
+  const int grid = total < 2 * sms ? total : 2 * sms;  // two CTAs per SM
   static int attr_cache[kMaxDevicesCached] = {};
   cudaError_t e = ensure_dyn_smem((const void*)score_blocks_tc_kernel, kSmemBytes, attr_cache);
   if (e != cudaSuccess) return e;

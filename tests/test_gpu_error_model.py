@@ -104,7 +104,7 @@ def _check(shape_w, K, qla, scoring, kernel="mma"):
             B.oasis_topk_select_diff(s, scores, Kd, qd, ctx, b2sd, w.C, sel, nsel, fetch, nfetch)
             torch.cuda.synchronize()
         finally:
-            B.oasis_set_option(B.OPT_SCORE_KERNEL, B.SCORE_KERNEL_MMA)
+            B.oasis_set_option(B.OPT_SCORE_KERNEL, B.SCORE_KERNEL_TC)  # the library's default
         want = ref.block_scores(K, qla, w.ctx)
     torch.cuda.synchronize()
     assert int(err.item()) == 0

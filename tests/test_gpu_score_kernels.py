@@ -1,4 +1,6 @@
-"""The TMA + tcgen05 scoring kernel, checked like the default one (bound, selection, full step)."""
+"""The two scoring kernels: the mma.sync one (the alternative to the default TMA +
+tcgen05 kernel) checked like the default (bound, selection, full step), and the
+two against each other."""
 import numpy as np
 import pytest
 
@@ -17,18 +19,18 @@ def _use(kernel):
 
 
 @pytest.fixture(autouse=True)
-def _tc_kernel():
+def _mma_kernel():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from sparse_decode_attention_oasis_gb300 import build
 
     build.build()
-    _use("tc")
+    _use("mma")
     yield
-    _use("mma")  # the process-wide default for the tests that follow
+    _use("tc")  # the process-wide default for the tests that follow
 
 
-def test_tc_tiny_workload_two_steps():
+def test_mma_tiny_workload_two_steps():
     c = Case(syn.tiny())
     c.step(0)
     c.step(1)
@@ -36,13 +38,14 @@ def test_tc_tiny_workload_two_steps():
 
 @pytest.mark.parametrize("Hq,n_la,ctx", [(32, 4, [4096, 1000, 17]), (64, 4, [2048, 1531]),
                                         (16, 3, [1024, 700]), (8, 4, [3000, 129])])
-def test_tc_shapes(Hq, n_la, ctx):
-    w = syn.Workload("tc", L=1, B=len(ctx), Hq=Hq, Hkv=8, ctx=ctx, Kb=32, C=5, n_hot=16, n_la=n_la)
+def test_mma_shapes(Hq, n_la, ctx):
+    w = syn.Workload("mma", L=1, B=len(ctx), Hq=Hq, Hkv=8, ctx=ctx, Kb=32, C=5, n_hot=16, n_la=n_la)
     c = Case(w)
     c.step(0)
 
 
-def test_tc_matches_the_default_kernel_within_bounds():
+def test_tc_matches_the_mma_kernel_within_bounds():
+    _use("tc")
     w = syn.Workload("cmp", L=1, B=2, Hq=32, Hkv=8, ctx=[4096, 2500], Kb=32, C=4, n_hot=16)
     c = Case(w)
     r, sc = c.step(0)

@@ -95,7 +95,8 @@ def test_multi_layer_decode_step_with_the_dynamic_scorer():
 
 def test_dynamic_scorer_equals_the_static_one_and_leaves_its_counter_at_zero():
     """oasis_score_blocks_dynamic writes the same (approximation, bound) pairs as
-    oasis_score_blocks, call after call, and leaves its work counter at zero."""
+    oasis_score_blocks with the mma.sync kernel, call after call, and leaves its
+    work counter at zero."""
     from sparse_decode_attention_oasis_gb300 import binding as B
     from sparse_decode_attention_oasis_gb300.engine import DecodeState
 
@@ -107,7 +108,11 @@ def test_dynamic_scorer_equals_the_static_one_and_leaves_its_counter_at_zero():
     q = _dev_bits(qla)
     s = st.shape
     ref_scores = torch.zeros((w.B, w.Hkv, w.nb_max, 2), dtype=torch.float32, device="cuda")
-    B.oasis_score_blocks(s, st.K[0], st.ctx, q, ref_scores)
+    B.oasis_set_option(B.OPT_SCORE_KERNEL, B.SCORE_KERNEL_MMA)  # the dynamic scorer is the mma.sync kernel
+    try:
+        B.oasis_score_blocks(s, st.K[0], st.ctx, q, ref_scores)
+    finally:
+        B.oasis_set_option(B.OPT_SCORE_KERNEL, B.SCORE_KERNEL_TC)
     work = torch.zeros(2, dtype=torch.int32, device="cuda")
     try:
         for share in (750, 0, 500, 1000):  # per mille of the blocks in fixed shares
