@@ -106,7 +106,7 @@ __device__ __forceinline__ void copy_store(const CopyJob& j, const Shape& s, int
   }
 }
 
-// Warp-level driver.  copy_begin stages the warp's first live item (if any);
+// Warp-level copy loop.  copy_begin stages the warp's first live item (if any);
 // copy_finish (after the host kernel's own work) stores it and then streams the
 // warp's remaining items one at a time.  Both scan from the same start, so no
 // state has to be kept between them.
