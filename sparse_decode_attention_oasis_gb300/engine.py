@@ -172,6 +172,9 @@ class DecodeState:
         self.prefetch_host = False
         # max-dot scoring through oasis_score_blocks_dynamic (chunks from an atomic
         # counter) instead of the fixed-stride persistent grid
+        # max-dot scoring through oasis_score_blocks_dynamic (the mma.sync kernel with a
+        # share of fixed ranges and chunks from an atomic counter) instead of the
+        # default scorer; a pooled or copy-carrying launch ignores it
         self.dynamic_scorer = False
         self._lag_sel = None  # per-layer selections of the cross-step pipeline (copy="lag")
         self._lag_nsel = None
