@@ -51,3 +51,25 @@ def test_single_rank_is_identity():
 
     assert bench.reduce_max(3.5, 1) == 3.5
     assert bench.aggregate_value(1, 36, 10, 1000.0) == pytest.approx(360.0)
+
+
+def test_torchrun_reference_arm_prints_one_line_from_rank_0():
+    """The launch the N > 1 contract uses (torch.distributed.run, two ranks on
+    127.0.0.1): rank 0 alone times the reference arm and prints one JSON line; the
+    other rank exits 0 without work."""
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py", "--impl", "reference",
+           "--gpus", "2", "--steps", "1", "--warmup", "3", "--ref-pairs", "1", "--workload", "tiny"]
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1")
+    r = subprocess.run(cmd, cwd=root, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 1 and d["warmup"] == 3
+    assert d["e2e"]["value"] == d["value"] and d["cpu_baseline"]["kind"] == "oracle"
